@@ -1,0 +1,155 @@
+/*
+ * norm_oracle.c - TEST INFRASTRUCTURE: the plain, slow CPU float64 oracle.
+ *
+ * Only the test suite, __graft_entry__.smoke() and the CPU-baseline /
+ * reference arm of bench.py may load or run this code.  The CUDA library
+ * shares no code, header, table or helper with it, and neither includes
+ * the other.
+ *
+ * Every function takes the fp32 input bytes the GPU sees, promotes them to
+ * double, evaluates the operation's textbook definition in double with an
+ * explicit two-pass variance, and writes the result in double (y64) and/or
+ * rounded once to float (y32).  Either output pointer may be NULL.
+ * `threads` only splits independent units (rows, batch entries, samples)
+ * across OpenMP threads; the arithmetic inside a unit is sequential and in
+ * the order written here.
+ *
+ * Sources (the three web pages the method is taken from):
+ *  - LayerNorm: POPCORNBENCH transcript "Kimi-K2.6 l1_p40", opening problem
+ *    analysis: per batch element, mean and population variance (unbiased =
+ *    False) over the last three dims; y = (x - mean) / sqrt(var + eps) *
+ *    weight + bias with elementwise weight/bias of the normalized shape.
+ *  - GroupNorm + LeakyReLU + x+x: transcript "Kimi-K2.6 l2_p62", first
+ *    design turn: groups of C/G contiguous channels, var = sum((x-mean)^2)/M,
+ *    y = (x - mean)/sqrt(var + eps) * gamma_c + beta_c, LeakyReLU(t) =
+ *    max(0, t) + negative_slope * min(0, t), then x + x.
+ *  - RMSNorm: transcript "Kimi-K2.6 l1_p36", reference model quoted in the
+ *    analysis turn: rms = sqrt(mean(x^2, dim=1) + eps), y = x / rms, over
+ *    dim 1 of an NCHW tensor whose trailing dims flatten to S = H*W.
+ *
+ * Pins (tests/test_oracle_pins.py): exact rational brute force on tiny
+ * inputs, closed forms (constant rows, affine invariance, two-valued rows,
+ * one-hot and constant RMS positions, GroupNorm with one channel per group
+ * as worked on the GroupNorm page), invariants of the outputs, float64
+ * torch.nn.functional on CPU as a third voice, and planted-mistake
+ * (mutation) runs that every pin set must catch.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG -1
+
+static void oracle_store(double v, int64_t i, double *y64, float *y32)
+{
+    if (y64)
+        y64[i] = v;
+    if (y32)
+        y32[i] = (float)v;
+}
+
+/* LayerNorm over contiguous rows x[rows][L]; gamma/beta [L] or NULL
+ * (identity affine: weight 1, bias 0). */
+int oracle_layer_norm(const float *x, const float *gamma, const float *beta,
+                      int64_t rows, int64_t L, double eps,
+                      double *y64, float *y32, int threads)
+{
+    if (!x || rows < 0 || L <= 0 || !(eps >= 0.0) || (!y64 && !y32))
+        return ORACLE_BAD_ARG;
+    if (threads < 1)
+        threads = 1;
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * L;
+        /* pass 1: mean */
+        double sum = 0.0;
+        for (int64_t i = 0; i < L; ++i)
+            sum += (double)xr[i];
+        const double mean = sum / (double)L;
+        /* pass 2: population variance about the mean */
+        double sq = 0.0;
+        for (int64_t i = 0; i < L; ++i) {
+            const double d = (double)xr[i] - mean;
+            sq += d * d;
+        }
+        const double var = sq / (double)L;
+        const double denom = sqrt(var + eps);
+        for (int64_t i = 0; i < L; ++i) {
+            const double w = gamma ? (double)gamma[i] : 1.0;
+            const double b = beta ? (double)beta[i] : 0.0;
+            const double v = ((double)xr[i] - mean) / denom * w + b;
+            oracle_store(v, r * L + i, y64, y32);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* RMSNorm over dim 1 of x[B][C][S] (S = product of the trailing dims), no
+ * affine: for each (b, s), ms = (1/C) sum_c x[b][c][s]^2,
+ * rms = sqrt(ms + eps), y[b][c][s] = x[b][c][s] / rms. */
+int oracle_rms_channel(const float *x, int64_t B, int64_t C, int64_t S, double eps,
+                       double *y64, float *y32, int threads)
+{
+    if (!x || B < 0 || C <= 0 || S < 0 || !(eps >= 0.0) || (!y64 && !y32))
+        return ORACLE_BAD_ARG;
+    if (threads < 1)
+        threads = 1;
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 1)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t s = 0; s < S; ++s) {
+            const float *xp = x + b * C * S + s;
+            double sq = 0.0;
+            for (int64_t c = 0; c < C; ++c) {
+                const double v = (double)xp[c * S];
+                sq += v * v;
+            }
+            const double rms = sqrt(sq / (double)C + eps);
+            for (int64_t c = 0; c < C; ++c)
+                oracle_store((double)xp[c * S] / rms, b * C * S + c * S + s, y64, y32);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* GroupNorm over x[N][C] with G groups of M = C/G contiguous channels
+ * (group g holds channels g*M .. g*M+M-1), per-channel gamma/beta [C] or
+ * NULL (weight 1, bias 0), population variance, then
+ * LeakyReLU(t) = max(0, t) + slope * min(0, t), then out = l + l. */
+int oracle_group_lrelu_x2(const float *x, const float *gamma, const float *beta,
+                          int64_t N, int64_t C, int64_t G, double eps, double slope,
+                          double *y64, float *y32, int threads)
+{
+    if (!x || N < 0 || C <= 0 || G <= 0 || C % G != 0 || !(eps >= 0.0) || (!y64 && !y32))
+        return ORACLE_BAD_ARG;
+    if (threads < 1)
+        threads = 1;
+    const int64_t M = C / G;
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 16)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < G; ++g) {
+            const int64_t c0 = g * M;
+            const float *xg = x + n * C + c0;
+            double sum = 0.0;
+            for (int64_t j = 0; j < M; ++j)
+                sum += (double)xg[j];
+            const double mean = sum / (double)M;
+            double sq = 0.0;
+            for (int64_t j = 0; j < M; ++j) {
+                const double d = (double)xg[j] - mean;
+                sq += d * d;
+            }
+            const double var = sq / (double)M;
+            const double denom = sqrt(var + eps);
+            for (int64_t j = 0; j < M; ++j) {
+                const int64_t c = c0 + j;
+                const double w = gamma ? (double)gamma[c] : 1.0;
+                const double b = beta ? (double)beta[c] : 0.0;
+                const double t = ((double)xg[j] - mean) / denom * w + b;
+                const double l = fmax(0.0, t) + slope * fmin(0.0, t);
+                oracle_store(l + l, n * C + c, y64, y32);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
