@@ -1,0 +1,554 @@
+#!/usr/bin/env python3
+"""Benchmark of the fp32 normalization kernels on GB300: one JSON line.
+
+Default workload (the one the headline metric is quoted on): LayerNorm of an
+fp32 (16, 64, 256, 256) tensor over its last three dims (16 rows of 4,194,304),
+x ~ N(0,1), gamma ~ N(1,0.1), beta ~ N(0,0.1), eps 1e-5.  A step is one call of
+norm_layer_fwd over that batch.  Between timed steps L2 is flushed by writing a
+buffer twice the size of L2, so every step reads x and gamma/beta from HBM.
+
+value  = algorithmic bytes per step (x read once + y written once + gamma and
+         beta read once) / mean device time of a step, in GB/s, summed over
+         ranks (each rank runs the full workload on its own GPU: weak scaling,
+         no collective on the data path).
+e2e    = the same metric with host buffers: pinned host -> device copy of
+         x/gamma/beta, the call, device -> host copy of y, all inside the timed
+         region.
+roofline.achieved / peak: the dominant kernel's algorithmic GB/s against the
+         measured HBM copy bandwidth of this GPU pool.
+cpu_baseline: the float64 CPU oracle (test infrastructure) on the host cores.
+per_config: the other workloads (RMSNorm (2,64,32,32) and (112,64,512,512),
+         GroupNorm+LeakyReLU+x2 (1024,8192)/512 groups, LayerNorm cancellation
+         stress) timed the same way, N=1 only.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       [--config ln|ln_stress|gn|rms|rms_small] [--no-extras]
+Under torchrun each rank drives one GPU (RANK/LOCAL_RANK/WORLD_SIZE from env).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 roofline per norm kernel (elements/s)"
+FALLBACK_HBM_GBS = 6800.0
+DATA = ("synthetic: seeded counter-based SplitMix64 + Box-Muller normals (seed 0; tensor ids x=0, "
+        "gamma=1, beta=2), identical bytes for the GPU path and the CPU oracle")
+
+CONFIGS = {
+    "rms_small": dict(op="rms", B=2, C=64, S=32 * 32, x=(0.0, 1.0),
+                      workload="RMSNorm over dim 1 of fp32 NCHW (2,64,32,32), x~N(0,1), eps 1e-5"),
+    "ln": dict(op="ln", rows=16, L=64 * 256 * 256, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
+               workload="LayerNorm fp32 (16,64,256,256) over the last 3 dims (4,194,304 per row), "
+                        "x~N(0,1), gamma~N(1,0.1), beta~N(0,0.1) of (64,256,256), eps 1e-5"),
+    "gn": dict(op="gn", N=1024, C=8192, G=512, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
+               workload="GroupNorm+LeakyReLU(0.01)+x2 fp32 (1024,8192), 512 groups of 16 contiguous "
+                        "channels, y~N(0,1), gamma~N(1,0.1), beta~N(0,0.1), eps 1e-5"),
+    "rms": dict(op="rms", B=112, C=64, S=512 * 512, x=(0.0, 1.0),
+                workload="RMSNorm over dim 1 of fp32 NCHW (112,64,512,512), x~N(0,1), eps 1e-5"),
+    "ln_stress": dict(op="ln", rows=16, L=64 * 256 * 256, x=(1000.0, 1e-2), gamma="ones", beta="zeros",
+                      workload="LayerNorm cancellation stress fp32 (16,64,256,256), x~N(1000,0.01^2), "
+                               "gamma=1, beta=0 (passed as tensors), eps 1e-5"),
+}
+EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress"]
+
+
+# ---------------------------------------------------------------------------- sizes
+
+def elements(cfg) -> int:
+    if cfg["op"] == "ln":
+        return cfg["rows"] * cfg["L"]
+    if cfg["op"] == "gn":
+        return cfg["N"] * cfg["C"]
+    return cfg["B"] * cfg["C"] * cfg["S"]
+
+
+def param_elems(cfg) -> int:
+    if cfg["op"] == "ln":
+        return 2 * cfg["L"]
+    if cfg["op"] == "gn":
+        return 2 * cfg["C"]
+    return 0
+
+
+def algorithmic_bytes(cfg) -> int:
+    """x read once + y written once + gamma/beta read once (fp32)."""
+    return 8 * elements(cfg) + 4 * param_elems(cfg)
+
+
+def shape_config(name, cfg):
+    out = {"workload": cfg["workload"], "name": name, "elements": elements(cfg),
+           "algorithmic_bytes_per_step": algorithmic_bytes(cfg),
+           "l2": "flushed between timed steps (write of 2x L2 bytes, outside the timed events)"}
+    for k in ("rows", "L", "N", "C", "G", "B", "S"):
+        if k in cfg:
+            out[{"L": "row_len"}.get(k, k)] = cfg[k]
+    return out
+
+
+# ---------------------------------------------------------------------------- inputs
+
+def host_inputs(cfg, seed=0):
+    import numpy as np
+    import normgen
+    n = elements(cfg)
+    x = normgen.normal(n, cfg["x"][0], cfg["x"][1], seed=seed, tensor_id=normgen.TENSOR_X)
+    g = b = None
+    if cfg["op"] in ("ln", "gn"):
+        pn = cfg["L"] if cfg["op"] == "ln" else cfg["C"]
+        if cfg.get("gamma") == "ones":
+            g = np.ones(pn, dtype=np.float32)
+        else:
+            g = normgen.normal(pn, cfg["gamma"][0], cfg["gamma"][1], seed=seed, tensor_id=normgen.TENSOR_GAMMA)
+        if cfg.get("beta") == "zeros":
+            b = np.zeros(pn, dtype=np.float32)
+        else:
+            b = normgen.normal(pn, cfg["beta"][0], cfg["beta"][1], seed=seed, tensor_id=normgen.TENSOR_BETA)
+    return x, g, b
+
+
+def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
+    """The C-ABI call of one step (device pointers) and the number of our kernel launches it makes."""
+    op = cfg["op"]
+    if op == "ln":
+        rows, L = cfg["rows"], cfg["L"]
+        persistent = (L % 4 == 0 and L <= ng.norm_layer_max_resident_row_len()
+                      and L >= (1 << 20))
+        return (lambda: ng.norm_layer_fwd(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if persistent else 2)
+    if op == "gn":
+        return (lambda: ng.norm_group_lrelu_x2_fwd(x, g, b, y, cfg["N"], cfg["C"], cfg["G"], 1e-5, 0.01, stream)), 1
+    return (lambda: ng.norm_rms_channel_fwd(x, y, cfg["B"], cfg["C"], cfg["S"], 1e-5, stream)), 1
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (100 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.25)  # let the sampler start before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self):
+        return time.perf_counter()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        window = [l for (t, l) in self.lines if t0 - 0.1 <= t <= t1 + 0.1] or [l for (_, l) in self.lines]
+        for line in window:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def gpu_id_for(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ---------------------------------------------------------------------------- peaks / ncu traffic
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: copy of 1 Gi bf16, read+write bytes)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "memory_bound_normalization_norm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None, "no ncu DRAM counters committed"
+    entry = rec.get(config_name)
+    if not entry:
+        return None, "no ncu DRAM counters for this workload"
+    if entry.get("kernel_source_hash") != kernel_source_hash():
+        return None, "kernels changed since the ncu DRAM counters were taken"
+    return entry.get("dram_bytes_per_launch"), entry.get("note", "")
+
+
+# ---------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (timing only: no data-path collective)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(bytes_per_rank: int, world: int, max_seconds_per_step: float) -> float:
+    """Whole-job GB/s: the bytes all ranks moved in one step over the slowest rank's step time."""
+    return bytes_per_rank * world / max_seconds_per_step / 1e9
+
+
+# ---------------------------------------------------------------------------- GPU timing
+
+def time_steps(call, steps, warmup, flush, stream, sampler=None, world=1):
+    """W untimed steps, then K steps each bracketed by CUDA events on `stream`, with an L2
+    flush between steps outside the events.  Returns (mean seconds per step, t0, t1)."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    dist_barrier(world)
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    return total_ms / 1e3 / steps, t0, t1
+
+
+def check_status(ng):
+    st = ng.norm_last_error()
+    if st != 0:
+        raise RuntimeError(f"device status {ng.norm_status_string(st)}")
+
+
+def run_config(ng, name, cfg, steps, warmup, stream, flush, sampler=None, world=1, want_e2e=False):
+    import torch
+    x, g, b = host_inputs(cfg)
+    dev = torch.device("cuda")
+    xd = torch.from_numpy(x).to(dev)
+    gd = None if g is None else torch.from_numpy(g).to(dev)
+    bd = None if b is None else torch.from_numpy(b).to(dev)
+    yd = torch.empty_like(xd)
+    ws = None
+    ws_bytes = 0
+    if cfg["op"] == "ln":
+        ws_bytes = ng.norm_layer_workspace_bytes(cfg["rows"], cfg["L"])
+        ws = torch.zeros((ws_bytes + 3) // 4 + 64, dtype=torch.float32, device=dev)
+    call, launches = make_call(ng, cfg, xd, gd, bd, yd, ws, ws_bytes, stream.cuda_stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    sec, t0, t1 = time_steps(call, steps, warmup, flush, stream, world=world)
+    clocks = sampler.stop(t0, t1) if sampler else None
+    check_status(ng)
+    res = {"name": name, "seconds_per_step": sec, "launches_per_step": launches, "clocks": clocks,
+           "t_region_s": t1 - t0}
+    if want_e2e:
+        res["e2e"] = run_e2e(ng, cfg, x, g, b, xd, gd, bd, yd, ws, ws_bytes, stream, min(steps, 20), world)
+    del xd, gd, bd, yd, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_e2e(ng, cfg, x, g, b, xd, gd, bd, yd, ws, ws_bytes, stream, steps, world):
+    """Host buffers in, host buffer out: pinned H2D of the inputs, the call, D2H of y."""
+    import torch
+    xh = torch.from_numpy(x).pin_memory()
+    gh = None if g is None else torch.from_numpy(g).pin_memory()
+    bh = None if b is None else torch.from_numpy(b).pin_memory()
+    yh = torch.empty(xh.shape, dtype=torch.float32).pin_memory()
+    call, _ = make_call(ng, cfg, xd, gd, bd, yd, ws, ws_bytes, stream.cuda_stream)
+    h2d = xh.numel() * 4 + (0 if gh is None else gh.numel() * 4) + (0 if bh is None else bh.numel() * 4)
+    d2h = yh.numel() * 4
+
+    def step():
+        with torch.cuda.stream(stream):
+            xd.copy_(xh, non_blocking=True)
+            if gh is not None:
+                gd.copy_(gh, non_blocking=True)
+                bd.copy_(bh, non_blocking=True)
+            call()
+            yh.copy_(yd, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    sec = s.elapsed_time(e) / 1e3 / steps
+    return {"seconds_per_step": sec, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ---------------------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(cfg, min_seconds, max_reps=1000, rows_per_step=None, x=None, g=None, b=None):
+    """Time the float64 oracle (as it stands) on the host cores; returns (GB/s, seconds, reps, threads, sample)."""
+    import oracle
+    threads = oracle.default_threads()
+    o = oracle.get()
+    if x is None:
+        x, g, b = host_inputs(cfg)
+    op = cfg["op"]
+    if op == "ln":
+        rows = cfg["rows"] if rows_per_step is None else max(1, min(cfg["rows"], rows_per_step))
+        xs = x[: rows * cfg["L"]]
+        fn = lambda: o.layer_norm(xs, g, b, rows, cfg["L"], 1e-5, threads=threads)  # noqa: E731
+        nbytes = 8 * rows * cfg["L"] + 8 * cfg["L"]
+        sample = f"{rows} of {cfg['rows']} rows of the workload per repetition"
+        used = min(threads, rows)
+    elif op == "gn":
+        fn = lambda: o.group_lrelu_x2(x, g, b, cfg["N"], cfg["C"], cfg["G"], 1e-5, 0.01, threads=threads)  # noqa
+        nbytes = algorithmic_bytes(cfg)
+        sample = "the full workload per repetition"
+        used = min(threads, cfg["N"])
+    else:
+        fn = lambda: o.rms_channel(x, cfg["B"], cfg["C"], cfg["S"], 1e-5, threads=threads)  # noqa: E731
+        nbytes = algorithmic_bytes(cfg)
+        sample = "the full workload per repetition"
+        used = min(threads, cfg["B"])
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return nbytes * reps / el / 1e9, el, reps, used, sample
+
+
+# ---------------------------------------------------------------------------- main
+
+def reference_arm(args, world, rank):
+    """The reference arm: the float64 CPU oracle on this host's cores, same metric and workload."""
+    if rank != 0:
+        return 0
+    cfg = CONFIGS[args.config]
+    import oracle
+    x, g, b = host_inputs(cfg)
+    # size each step so that the whole run stays within a few minutes
+    budget_s = 150.0
+    gbs, el, reps, used, sample = time_oracle(cfg, 0.0, max_reps=1, x=x, g=g, b=b)
+    per_step = el
+    rows_per_step = None
+    if cfg["op"] == "ln" and per_step * (args.steps + args.warmup) > budget_s:
+        per_row = per_step / cfg["rows"] * max(1, min(oracle.default_threads(), cfg["rows"]))
+        rows_per_step = max(1, int(budget_s / (args.steps + args.warmup) / max(per_row, 1e-9)))
+    for _ in range(args.warmup):
+        time_oracle(cfg, 0.0, max_reps=1, rows_per_step=rows_per_step, x=x, g=g, b=b)
+    times = []
+    nbytes_tot = 0.0
+    for _ in range(args.steps):
+        gbs, el, reps, used, sample = time_oracle(cfg, 0.0, max_reps=1, rows_per_step=rows_per_step, x=x, g=g,
+                                                  b=b)
+        times.append(el)
+        nbytes_tot += gbs * el * 1e9
+    total = sum(times)
+    value = nbytes_tot / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": shape_config(args.config, cfg),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": sample + " (float64 two-pass C oracle, OpenMP over independent units)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default="ln")
+    ap.add_argument("--no-extras", action="store_true", help="skip the per_config measurements")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU time budget of cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    import memory_bound_normalization_norm_gb300 as ng
+
+    cfg = CONFIGS[args.config]
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        with torch.cuda.stream(stream):
+            flush_buf.fill_(1.0)
+
+    sampler = ClockSampler(gpu_id_for(local))
+    main_res = run_config(ng, args.config, cfg, args.steps, args.warmup, stream, flush, sampler, world,
+                          want_e2e=True)
+    sec = dist_max(main_res["seconds_per_step"], world, device="cuda")
+    nbytes = algorithmic_bytes(cfg)
+    value = weak_scaling_value(nbytes, world, sec)
+    e2e_sec = dist_max(main_res["e2e"]["seconds_per_step"], world, device="cuda")
+    peak, peak_note = hbm_peak()
+    achieved = nbytes / main_res["seconds_per_step"] / 1e9
+    traffic, traffic_note = ncu_traffic(args.config)
+
+    extras = []
+    if world == 1 and not args.no_extras:
+        for name in EXTRA_ORDER:
+            if name == args.config:
+                continue
+            c = CONFIGS[name]
+            k = min(args.steps, 200 if name != "rms" else 50)
+            r = run_config(ng, name, c, k, 5, stream, flush)
+            a = algorithmic_bytes(c) / r["seconds_per_step"] / 1e9
+            extras.append({"config": name, "workload": c["workload"], "steps": k,
+                           "us_per_step": round(r["seconds_per_step"] * 1e6, 3),
+                           "algorithmic_bytes": algorithmic_bytes(c), "achieved_gbs": round(a, 2),
+                           "frac_of_measured_peak": round(a / peak, 4),
+                           "elements_per_s": round(elements(c) / r["seconds_per_step"], 1),
+                           "launches_per_step": r["launches_per_step"]})
+
+    cpu = None
+    if rank == 0 and args.cpu_seconds > 0:
+        gbs, el, reps, used, sample = time_oracle(cfg, args.cpu_seconds, max_reps=200)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+               "sample": f"{sample}, {reps} repetitions in {el:.1f} s (float64 two-pass C oracle)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": DATA,
+            "config": shape_config(args.config, cfg),
+            "elements_per_s": round(elements(cfg) * world / sec, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_source": peak_note, "traffic_note": traffic_note,
+                         "kernel": "ln_persistent_kernel" if cfg["op"] == "ln" else cfg["op"]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(weak_scaling_value(nbytes, world, e2e_sec), 3), "unit": "GB/s",
+                    "h2d_bytes_per_step": main_res["e2e"]["h2d_bytes_per_step"],
+                    "d2h_bytes_per_step": main_res["e2e"]["d2h_bytes_per_step"]},
+            "gpu_launches": main_res["launches_per_step"] * args.steps,
+            "clocks": main_res["clocks"],
+            "per_config": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

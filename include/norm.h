@@ -1,0 +1,181 @@
+/*
+ * norm.h - C ABI of libnormgb300.so: fp32 reduce-then-apply normalization on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, each one stream-ordered launch sequence of the library's
+ * own CUDA kernels:
+ *
+ *   norm_layer_fwd           LayerNorm over very long contiguous rows
+ *   norm_rms_channel_fwd     RMSNorm over dim 1 of an NCHW tensor
+ *   norm_group_lrelu_x2_fwd  per-row GroupNorm, then LeakyReLU, then x + x
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named x, y, gamma, beta, workspace are DEVICE pointers on the
+ *     current CUDA device.  The caller owns all of them; the library never
+ *     frees caller memory and allocates nothing on these calls unless a
+ *     function says so (norm_layer_fwd with workspace == NULL).
+ *   - Tensors are fp32, dense and contiguous in the row-major layout stated
+ *     per function.  Strided (non-contiguous) views cannot be detected from a
+ *     raw pointer; passing one gives wrong results, not an error.
+ *   - Every call is asynchronous on `stream` (0 = the legacy default stream).
+ *     Argument errors are returned synchronously, before anything is
+ *     launched.  A launch failure returns NORM_ERR_CUDA.  Faults detected on
+ *     the device (a grid barrier that gave up waiting) are recorded in a
+ *     per-device error word that norm_last_error() reads.
+ *   - y == x (exact aliasing, in place) is allowed.  Any other overlap of y
+ *     with an input is rejected with NORM_ERR_INVALID_ARG.
+ *   - eps must be finite and >= 0.  Sizes must be >= 0; a size of 0 in any
+ *     extent makes the call a no-op that returns NORM_OK.
+ *   - Pointers must be 4-byte aligned (NORM_ERR_MISALIGNED otherwise).  The
+ *     fastest kernels also want 16-byte aligned pointers and extents that are
+ *     multiples of 4; other valid inputs run a slower exact path.
+ *   - All index arithmetic is 64-bit; tensors of more than 2^31 elements are
+ *     supported.
+ *
+ * Thread safety: calls may be issued from several host threads.  The
+ * process-wide options of norm_set_option() are read at launch time.
+ */
+#ifndef NORM_GB300_NORM_H
+#define NORM_GB300_NORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NORM_OK = 0,
+    NORM_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad eps, overlap, C % groups != 0 */
+    NORM_ERR_MISALIGNED = 2,  /* a float pointer that is not 4-byte aligned */
+    NORM_ERR_WORKSPACE = 3,   /* workspace too small or misaligned */
+    NORM_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    NORM_ERR_TIMEOUT = 5,     /* a device-side wait gave up (see norm_last_error) */
+    NORM_ERR_UNSUPPORTED = 6  /* no usable device, or a request this build cannot serve */
+} norm_status_t;
+
+/* ------------------------------------------------------------------ LayerNorm
+ * Defined by the LayerNorm page (POPCORNBENCH transcript "Kimi-K2.6 l1_p40",
+ * opening problem analysis): for every row r of x[rows][row_len],
+ *     mean_r = (1/row_len) * sum_i x[r][i]
+ *     var_r  = (1/row_len) * sum_i (x[r][i] - mean_r)^2      (population)
+ *     y[r][i] = (x[r][i] - mean_r) / sqrt(var_r + eps) * gamma[i] + beta[i]
+ * An input of shape (B, d1, ..., dk) normalized over its last k dims is
+ * rows = B, row_len = d1*...*dk.
+ *
+ * x, y     [rows][row_len] fp32, contiguous.
+ * gamma    [row_len] elementwise weight, or NULL for weight 1.
+ * beta     [row_len] elementwise bias, or NULL for bias 0.
+ * workspace  device scratch of at least norm_layer_workspace_bytes(rows,
+ *          row_len) bytes, 256-byte aligned, zero-filled before its first use
+ *          (cudaMemset or norm_layer_workspace_reset).  The kernels leave it
+ *          ready for the next call, except after NORM_ERR_TIMEOUT, when it
+ *          must be reset again.  A workspace must not be shared by calls that
+ *          can run at the same time (different streams).
+ *          workspace == NULL: the library uses its own per-device workspace,
+ *          allocated with cudaMalloc on the first such call on a device and
+ *          kept until exit; such calls must then be serialized by the caller
+ *          (one stream at a time).
+ *
+ * Rows whose length is a multiple of 4 with 16-byte aligned x/y/gamma/beta
+ * and at most norm_layer_max_resident_row_len() elements are read from HBM
+ * once: a persistent cooperative kernel keeps every CTA's slice of a row on
+ * chip across a bounded grid barrier.  Other shapes take a two-kernel path
+ * that reads x twice.  Both produce the same statistics definition.
+ */
+size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len);
+
+norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *beta, float *y,
+                             int64_t rows, int64_t row_len, float eps,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Zero `bytes` of a LayerNorm workspace on `stream` (stream-ordered). */
+norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStream_t stream);
+
+/* Longest row (in elements) that the single-read persistent LayerNorm kernel
+ * can hold on chip on the current device; 0 if the device cannot run it. */
+int64_t norm_layer_max_resident_row_len(void);
+
+/* ------------------------------------------------------------------ RMSNorm
+ * Defined by the RMSNorm page (POPCORNBENCH transcript "Kimi-K2.6 l1_p36",
+ * the reference model quoted in the analysis turn): for x[B][C][S] (an NCHW
+ * tensor with S = H*W, or any trailing dims flattened into S),
+ *     ms[b][s]   = (1/C) * sum_c x[b][c][s]^2
+ *     y[b][c][s] = x[b][c][s] / sqrt(ms[b][s] + eps)
+ * No affine parameters.  The channel stride is S elements.
+ *
+ * x, y  [B][C][S] fp32, contiguous.  Any C >= 1 and S >= 1; C <= 128 keeps a
+ *       position's channels in registers (one HBM read), larger C re-reads x.
+ */
+norm_status_t norm_rms_channel_fwd(const float *x, float *y, int64_t B, int64_t C, int64_t S,
+                                   float eps, cudaStream_t stream);
+
+/* -------------------------------------------- GroupNorm + LeakyReLU + x + x
+ * Defined by the GroupNorm page (POPCORNBENCH transcript "Kimi-K2.6 l2_p62",
+ * first design turn): x[N][C] is split per row into num_groups groups of
+ * M = C / num_groups CONTIGUOUS channels (group g = channels g*M .. g*M+M-1);
+ *     mean, var = population mean and variance of the group's M values
+ *     t  = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c]
+ *     l  = max(0, t) + negative_slope * min(0, t)
+ *     y  = l + l
+ *
+ * x, y          [N][C] fp32, contiguous.
+ * gamma, beta   [C] per-channel weight and bias, or NULL (1 and 0).
+ * num_groups    must divide C.
+ * M a power of two in 4..128 with C % 4 == 0 and 16-byte aligned pointers
+ * takes the vectorized kernel (4 channels per thread); any other M takes a
+ * warp-per-group kernel.
+ */
+norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const float *beta,
+                                      float *y, int64_t N, int64_t C, int64_t num_groups,
+                                      float eps, float negative_slope, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ status
+ * Synchronize `stream`, then read and clear the current device's error word.
+ * Returns NORM_OK if no device-side wait gave up since the last call, else
+ * the recorded status (NORM_ERR_TIMEOUT).  After a timeout the library-owned
+ * LayerNorm workspace of this device is reset here; caller-owned workspaces
+ * must be reset by the caller.  Returns NORM_ERR_CUDA if the synchronize
+ * itself fails.
+ */
+norm_status_t norm_last_error(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *norm_status_string(norm_status_t status);
+
+/* ------------------------------------------------------------------ options
+ * Process-wide knobs, read when a call launches.  Not meant to be changed
+ * while other threads are launching.
+ *   NORM_OPT_LN_PATH             0 = choose automatically, 1 = force the
+ *                                persistent single-read kernel (error
+ *                                NORM_ERR_UNSUPPORTED if the shape does not
+ *                                fit), 2 = force the two-kernel path.
+ *   NORM_OPT_BARRIER_TIMEOUT_NS  how long a CTA waits at the LayerNorm grid
+ *                                barrier (or for its own bulk copies) before
+ *                                it records NORM_ERR_TIMEOUT and returns
+ *                                without writing y.  Default 200 ms.
+ *   NORM_OPT_BARRIER_EXTRA_ARRIVALS  test hook: the grid barrier waits for
+ *                                this many arrivals more than there are CTAs,
+ *                                so it can only end by timing out.  Default 0.
+ *   NORM_OPT_LN_CTAS             CTAs of the persistent kernel (0 = one per
+ *                                SM, the default).
+ * Returns NORM_ERR_INVALID_ARG for an unknown option or a negative value.
+ */
+typedef enum {
+    NORM_OPT_LN_PATH = 1,
+    NORM_OPT_BARRIER_TIMEOUT_NS = 2,
+    NORM_OPT_BARRIER_EXTRA_ARRIVALS = 3,
+    NORM_OPT_LN_CTAS = 4
+} norm_option_t;
+
+norm_status_t norm_set_option(norm_option_t option, int64_t value);
+int64_t norm_get_option(norm_option_t option);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NORM_GB300_NORM_H */

@@ -1,0 +1,169 @@
+// gn_kernels.cu - GroupNorm over contiguous channel groups of each row, fused
+// with LeakyReLU and x + x (GroupNorm page, POPCORNBENCH transcript
+// "Kimi-K2.6 l2_p62": groups of M = C/G contiguous channels, population
+// variance, per-channel affine, LeakyReLU(t) = max(0,t) + slope*min(0,t),
+// then x + x).
+//
+// Vector path: one thread owns 4 consecutive channels (one float4), so a group
+// of M channels is TPG = M/4 adjacent lanes and a warp covers 32 float4 =
+// 512 contiguous bytes.  Mean and then the exact M2 about the mean are reduced
+// over the TPG lanes with xor shuffles (the group's values never leave
+// registers), the epilogue is applied in registers and the float4 is stored
+// once.  Every byte of x is read once and every byte of y written once;
+// gamma/beta (2*C floats) stay cache resident.
+#include "norm_internal.cuh"
+
+namespace normk {
+
+namespace {
+
+constexpr int GN_THREADS = 256;
+
+template <int TPG>
+__device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int o = TPG / 2; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// grid: x = column blocks of GN_THREADS*U float4, y = rows (folded by gridDim.y)
+template <int TPG, int U>
+__global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const float4 *x, const float4 *__restrict__ gamma,
+                                                             const float4 *__restrict__ beta, float4 *y,
+                                                             int64_t N, int C4, float invM, float eps,
+                                                             float slope)
+{
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    const int col0 = blockIdx.x * (GN_THREADS * U) + threadIdx.x;
+    for (int64_t n = blockIdx.y; n < N; n += gridDim.y) {
+        const float4 *xr = x + n * C4;
+        float4 *yr = y + n * C4;
+        // all loads of the row block first (x and this thread's gamma/beta), so
+        // they are in flight together
+        float4 v[U], g[U], b[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = col0 + u * GN_THREADS;
+            const bool in = c < C4;
+            v[u] = in ? ld_stream_f4(xr + c, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+            g[u] = (in && gamma) ? ld_ro_f4(gamma + c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
+            b[u] = (in && beta) ? ld_ro_f4(beta + c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = col0 + u * GN_THREADS;
+            // C4 is a multiple of TPG, so whole groups are in or out of range
+            // together and every lane takes part in the shuffles.
+            const float mean = group_sum<TPG>((v[u].x + v[u].y) + (v[u].z + v[u].w)) * invM;
+            const float dx = v[u].x - mean, dy = v[u].y - mean, dz = v[u].z - mean, dw = v[u].w - mean;
+            const float m2 = group_sum<TPG>((dx * dx + dy * dy) + (dz * dz + dw * dw));
+            const float rstd = rsqrtf(fmaf(m2, invM, eps));
+            if (c < C4) {
+                float4 t;
+                t.x = fmaf(dx * rstd, g[u].x, b[u].x);
+                t.y = fmaf(dy * rstd, g[u].y, b[u].y);
+                t.z = fmaf(dz * rstd, g[u].z, b[u].z);
+                t.w = fmaf(dw * rstd, g[u].w, b[u].w);
+                t.x = t.x > 0.f ? t.x : slope * t.x;
+                t.y = t.y > 0.f ? t.y : slope * t.y;
+                t.z = t.z > 0.f ? t.z : slope * t.z;
+                t.w = t.w > 0.f ? t.w : slope * t.w;
+                t.x += t.x;
+                t.y += t.y;
+                t.z += t.z;
+                t.w += t.w;
+                st_stream_f4(yr + c, t, pol_stream);
+            }
+        }
+    }
+}
+
+template <int TPG, int U>
+cudaError_t launch_vec(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
+                       int64_t M, float eps, float slope, cudaStream_t stream)
+{
+    const int C4 = static_cast<int>(C / 4);
+    const int per_block = GN_THREADS * U;
+    dim3 grid((C4 + per_block - 1) / per_block, static_cast<unsigned>(N < 65535 ? N : 65535));
+    gn_vec4_kernel<TPG, U><<<grid, GN_THREADS, 0, stream>>>(
+        reinterpret_cast<const float4 *>(x), reinterpret_cast<const float4 *>(gamma),
+        reinterpret_cast<const float4 *>(beta), reinterpret_cast<float4 *>(y), N, C4, 1.0f / static_cast<float>(M),
+        eps, slope);
+    return cudaGetLastError();
+}
+
+// Any M: one warp per (row, group); lanes stride over the group's channels.
+// Mean, then M2 about the mean (a second read that hits L1/L2), then apply.
+__global__ void __launch_bounds__(256) gn_warp_kernel(const float *x, const float *__restrict__ gamma,
+                                                      const float *__restrict__ beta, float *y, int64_t N,
+                                                      int64_t C, int64_t G, int64_t M, float eps, float slope)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const float invM = 1.0f / static_cast<float>(M);
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < N * G;
+         w += warps) {
+        const int64_t n = w / G, g = w - n * G;
+        const int64_t base = n * C + g * M;
+        float s = 0.f;
+        for (int64_t j = lane; j < M; j += 32)
+            s += ld_plain_f1(x + base + j);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float mean = s * invM;
+        float q = 0.f;
+        for (int64_t j = lane; j < M; j += 32) {
+            const float d = ld_plain_f1(x + base + j) - mean;
+            q = fmaf(d, d, q);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            q += __shfl_xor_sync(0xffffffffu, q, o);
+        const float rstd = rsqrtf(fmaf(q, invM, eps));
+        for (int64_t j = lane; j < M; j += 32) {
+            const int64_t c = g * M + j;
+            const float gw = gamma ? gamma[c] : 1.f;
+            const float bw = beta ? beta[c] : 0.f;
+            float t = fmaf((ld_plain_f1(x + base + j) - mean) * rstd, gw, bw);
+            t = t > 0.f ? t : slope * t;
+            y[base + j] = t + t;
+        }
+    }
+}
+
+} // namespace
+
+cudaError_t gn_vec4_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
+                           int64_t M, float eps, float slope, cudaStream_t stream)
+{
+    switch (M) {
+    case 4: return launch_vec<1, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 8: return launch_vec<2, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 16: return launch_vec<4, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 32: return launch_vec<8, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 64: return launch_vec<16, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 128: return launch_vec<32, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t gn_warp_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
+                           int64_t G, float eps, float slope, int sm_count, cudaStream_t stream)
+{
+    const int64_t warps_needed = N * G;
+    int64_t blocks = (warps_needed + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 16;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    gn_warp_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, gamma, beta, y, N, C, G, C / G, eps,
+                                                                       slope);
+    return cudaGetLastError();
+}
+
+} // namespace normk

@@ -1,0 +1,472 @@
+// norm_api.cu - the extern "C" entry points declared in include/norm.h:
+// argument validation (always before any CUDA call), per-device state,
+// LayerNorm path planning, the device error word, and options.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "norm_internal.cuh"
+
+// Per-device error word: kernels record the first device-side failure here
+// (NORM_ERR_TIMEOUT); norm_last_error() reads and clears it.
+__device__ unsigned g_norm_error_word;
+
+namespace {
+
+using normk::LnParams;
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kWsHeader = sizeof(normk::LnSync);
+// Shortest row for which the automatic choice takes the persistent kernel: a
+// row must stream for longer than a grid barrier takes for the barrier to hide
+// behind the prefetch of the next rows.
+constexpr int64_t kPersistentMinRowLen = int64_t(1) << 20;
+
+struct DeviceState {
+    bool init = false;
+    bool ok = false;
+    int sm_count = 0;
+    int smem_optin = 0;
+    int coop = 0;
+    int ln_max_dyn_smem = 0; // dynamic smem the persistent kernel may use
+    int ln_ctas_per_sm = 0;  // at the full dynamic smem budget
+    unsigned *err = nullptr;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+std::atomic<int64_t> g_opt_ln_path{0};
+std::atomic<int64_t> g_opt_timeout_ns{200000000};
+std::atomic<int64_t> g_opt_extra_arrivals{0};
+std::atomic<int64_t> g_opt_ln_ctas{0};
+
+// Resolve (and on first use initialize) the state of the current device.
+norm_status_t device_state(DeviceState **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return NORM_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &s = g_dev[dev];
+    if (!s.init) {
+        s.init = true;
+        s.ok = false;
+        if (cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&s.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&s.coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return NORM_ERR_CUDA;
+        }
+        void *err = nullptr;
+        if (cudaGetSymbolAddress(&err, g_norm_error_word) != cudaSuccess) {
+            cudaGetLastError();
+            return NORM_ERR_CUDA;
+        }
+        s.err = static_cast<unsigned *>(err);
+        // The persistent kernel's static shared memory is small (barriers,
+        // reduction scratch); leave room for it under the opt-in limit.
+        s.ln_max_dyn_smem = s.smem_optin - 1024;
+        if (normk::ln_persistent_setup(s.ln_max_dyn_smem) != cudaSuccess ||
+            normk::ln_persistent_occupancy(s.ln_max_dyn_smem, &s.ln_ctas_per_sm) != cudaSuccess) {
+            cudaGetLastError();
+            s.ln_ctas_per_sm = 0;
+        }
+        s.ok = true;
+    }
+    if (!s.ok)
+        return NORM_ERR_CUDA;
+    *out = &s;
+    return NORM_OK;
+}
+
+bool aligned(const void *p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// [a, a+na) and [b, b+nb) in bytes intersect.
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0)
+        return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool valid_eps(float eps)
+{
+    return std::isfinite(eps) && eps >= 0.f;
+}
+
+// Product of non-negative extents without overflow of the byte count.
+bool safe_mul(int64_t a, int64_t b, int64_t *out)
+{
+    if (a < 0 || b < 0)
+        return false;
+    if (a != 0 && b > (int64_t(1) << 60) / a)
+        return false;
+    *out = a * b;
+    return true;
+}
+
+// ------------------------------------------------------------------ LN plan
+
+struct LnPlan {
+    int path = 0; // 1 persistent, 2 split
+    int grid = 0;
+    int dyn_smem = 0;
+    int max_n4 = 0;
+    int parts = 0;
+    int64_t chunk = 0;
+    bool vec4 = false;
+    size_t ws_bytes = 0;
+};
+
+void plan_split(int64_t rows, int64_t L, bool vec4, const DeviceState &d, LnPlan *pl)
+{
+    const int64_t target = int64_t(4) * d.sm_count;
+    int64_t P = (target + rows - 1) / rows;
+    const int64_t maxP = (L + 4095) / 4096;
+    if (P > maxP)
+        P = maxP;
+    if (P < 1)
+        P = 1;
+    int64_t chunk = (L + P - 1) / P;
+    if (vec4)
+        chunk = (chunk + 3) & ~int64_t(3);
+    P = (L + chunk - 1) / chunk;
+    pl->path = 2;
+    pl->vec4 = vec4;
+    pl->parts = static_cast<int>(P);
+    pl->chunk = chunk;
+    pl->ws_bytes = kWsHeader + static_cast<size_t>(rows) * static_cast<size_t>(P) * 16u;
+}
+
+// Fills the persistent plan if the shape fits on chip; returns false if not.
+bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
+{
+    (void)rows;
+    if (!d.coop || d.ln_ctas_per_sm < 1 || (L & 3) != 0)
+        return false;
+    const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
+    int grid = d.sm_count * d.ln_ctas_per_sm;
+    const int64_t want = g_opt_ln_ctas.load();
+    if (want > 0 && want < grid)
+        grid = static_cast<int>(want);
+    const int64_t L4 = L / 4;
+    const int64_t max_n4 = (L4 + grid - 1) / grid;
+    if (max_n4 > int64_t(cfg.threads) * cfg.v4_per_thread)
+        return false;
+    const int64_t smem = 2 * max_n4 * 16;
+    if (smem > d.ln_max_dyn_smem)
+        return false;
+    pl->path = 1;
+    pl->vec4 = true;
+    pl->grid = grid;
+    pl->max_n4 = static_cast<int>(max_n4 < 1 ? 1 : max_n4);
+    pl->dyn_smem = static_cast<int>(2 * int64_t(pl->max_n4) * 16);
+    pl->ws_bytes = kWsHeader + 2u * static_cast<size_t>(grid) * 16u;
+    return true;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *norm_status_string(norm_status_t s)
+{
+    switch (s) {
+    case NORM_OK: return "NORM_OK";
+    case NORM_ERR_INVALID_ARG: return "NORM_ERR_INVALID_ARG";
+    case NORM_ERR_MISALIGNED: return "NORM_ERR_MISALIGNED";
+    case NORM_ERR_WORKSPACE: return "NORM_ERR_WORKSPACE";
+    case NORM_ERR_CUDA: return "NORM_ERR_CUDA";
+    case NORM_ERR_TIMEOUT: return "NORM_ERR_TIMEOUT";
+    case NORM_ERR_UNSUPPORTED: return "NORM_ERR_UNSUPPORTED";
+    }
+    return "NORM_ERR_UNKNOWN";
+}
+
+norm_status_t norm_set_option(norm_option_t option, int64_t value)
+{
+    if (value < 0)
+        return NORM_ERR_INVALID_ARG;
+    switch (option) {
+    case NORM_OPT_LN_PATH:
+        if (value > 2)
+            return NORM_ERR_INVALID_ARG;
+        g_opt_ln_path = value;
+        return NORM_OK;
+    case NORM_OPT_BARRIER_TIMEOUT_NS:
+        if (value == 0)
+            return NORM_ERR_INVALID_ARG;
+        g_opt_timeout_ns = value;
+        return NORM_OK;
+    case NORM_OPT_BARRIER_EXTRA_ARRIVALS:
+        if (value > 1024)
+            return NORM_ERR_INVALID_ARG;
+        g_opt_extra_arrivals = value;
+        return NORM_OK;
+    case NORM_OPT_LN_CTAS:
+        g_opt_ln_ctas = value;
+        return NORM_OK;
+    }
+    return NORM_ERR_INVALID_ARG;
+}
+
+int64_t norm_get_option(norm_option_t option)
+{
+    switch (option) {
+    case NORM_OPT_LN_PATH: return g_opt_ln_path.load();
+    case NORM_OPT_BARRIER_TIMEOUT_NS: return g_opt_timeout_ns.load();
+    case NORM_OPT_BARRIER_EXTRA_ARRIVALS: return g_opt_extra_arrivals.load();
+    case NORM_OPT_LN_CTAS: return g_opt_ln_ctas.load();
+    }
+    return -1;
+}
+
+size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len)
+{
+    if (rows <= 0 || row_len <= 0)
+        return kWsHeader;
+    DeviceState *d = nullptr;
+    if (device_state(&d) != NORM_OK)
+        return 0;
+    LnPlan ps, pp;
+    plan_split(rows, row_len, (row_len & 3) == 0, *d, &ps);
+    size_t bytes = ps.ws_bytes;
+    if (plan_persistent(rows, row_len, *d, &pp) && pp.ws_bytes > bytes)
+        bytes = pp.ws_bytes;
+    return bytes;
+}
+
+int64_t norm_layer_max_resident_row_len(void)
+{
+    DeviceState *d = nullptr;
+    if (device_state(&d) != NORM_OK || !d->coop || d->ln_ctas_per_sm < 1)
+        return 0;
+    const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
+    int64_t per_cta = int64_t(cfg.threads) * cfg.v4_per_thread;
+    const int64_t by_smem = d->ln_max_dyn_smem / 32;
+    if (by_smem < per_cta)
+        per_cta = by_smem;
+    return per_cta * 4 * d->sm_count * d->ln_ctas_per_sm;
+}
+
+norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStream_t stream)
+{
+    if (!workspace || bytes < kWsHeader)
+        return NORM_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(workspace, 0, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    return NORM_OK;
+}
+
+norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *beta, float *y, int64_t rows,
+                             int64_t row_len, float eps, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream)
+{
+    int64_t n = 0;
+    if (rows < 0 || row_len < 0 || !valid_eps(eps) || !safe_mul(rows, row_len, &n))
+        return NORM_ERR_INVALID_ARG;
+    if (n == 0)
+        return NORM_OK;
+    if (!x || !y)
+        return NORM_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(y, 4) || !aligned(gamma, 4) || !aligned(beta, 4))
+        return NORM_ERR_MISALIGNED;
+    const size_t nb = static_cast<size_t>(n) * 4u, pb = static_cast<size_t>(row_len) * 4u;
+    if ((x != y && overlaps(x, nb, y, nb)) || overlaps(gamma, pb, y, nb) || overlaps(beta, pb, y, nb))
+        return NORM_ERR_INVALID_ARG;
+    if (workspace && (!aligned(workspace, 256) || overlaps(workspace, workspace_bytes, y, nb) ||
+                      overlaps(workspace, workspace_bytes, x, nb)))
+        return NORM_ERR_WORKSPACE;
+
+    DeviceState *d = nullptr;
+    norm_status_t st = device_state(&d);
+    if (st != NORM_OK)
+        return st;
+
+    const bool vec4 = (row_len & 3) == 0 && aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
+                      aligned(beta, 16);
+    const int64_t path_opt = g_opt_ln_path.load();
+    LnPlan pl;
+    bool persistent = false;
+    if (path_opt != 2 && vec4) {
+        LnPlan pp;
+        if (plan_persistent(rows, row_len, *d, &pp) && (path_opt == 1 || row_len >= kPersistentMinRowLen)) {
+            pl = pp;
+            persistent = true;
+        }
+    }
+    if (path_opt == 1 && !persistent)
+        return NORM_ERR_UNSUPPORTED;
+    if (!persistent)
+        plan_split(rows, row_len, vec4, *d, &pl);
+
+    void *ws = workspace;
+    if (!ws) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (d->ws_bytes < pl.ws_bytes) {
+            // Grow the library-owned workspace (callers serialize these calls).
+            if (cudaDeviceSynchronize() != cudaSuccess) {
+                cudaGetLastError();
+                return NORM_ERR_CUDA;
+            }
+            if (d->ws)
+                cudaFree(d->ws);
+            d->ws = nullptr;
+            d->ws_bytes = 0;
+            void *p = nullptr;
+            if (cudaMalloc(&p, pl.ws_bytes) != cudaSuccess || cudaMemset(p, 0, pl.ws_bytes) != cudaSuccess ||
+                cudaDeviceSynchronize() != cudaSuccess) {
+                cudaGetLastError();
+                if (p)
+                    cudaFree(p);
+                return NORM_ERR_CUDA;
+            }
+            d->ws = p;
+            d->ws_bytes = pl.ws_bytes;
+        }
+        ws = d->ws;
+    } else if (workspace_bytes < pl.ws_bytes) {
+        return NORM_ERR_WORKSPACE;
+    }
+
+    LnParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = x;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.y = y;
+    p.rows = rows;
+    p.row_len = row_len;
+    p.eps = eps;
+    p.sync = static_cast<normk::LnSync *>(ws);
+    p.part = reinterpret_cast<float4 *>(static_cast<char *>(ws) + kWsHeader);
+    p.err = d->err;
+    p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
+    p.chunk = pl.chunk;
+    p.parts = pl.parts;
+    cudaError_t e;
+    if (persistent) {
+        p.max_n4 = pl.max_n4;
+        p.expected = static_cast<unsigned>(pl.grid) + static_cast<unsigned>(g_opt_extra_arrivals.load());
+        e = normk::ln_persistent_launch(p, pl.grid, pl.dyn_smem, stream);
+    } else {
+        e = normk::ln_split_launch(p, pl.vec4, stream);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    return NORM_OK;
+}
+
+norm_status_t norm_rms_channel_fwd(const float *x, float *y, int64_t B, int64_t C, int64_t S, float eps,
+                                   cudaStream_t stream)
+{
+    int64_t bc = 0, n = 0;
+    if (B < 0 || C < 0 || S < 0 || !valid_eps(eps) || !safe_mul(B, C, &bc) || !safe_mul(bc, S, &n))
+        return NORM_ERR_INVALID_ARG;
+    if (n == 0)
+        return NORM_OK;
+    if (!x || !y)
+        return NORM_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(y, 4))
+        return NORM_ERR_MISALIGNED;
+    const size_t nb = static_cast<size_t>(n) * 4u;
+    if (x != y && overlaps(x, nb, y, nb))
+        return NORM_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    norm_status_t st = device_state(&d);
+    if (st != NORM_OK)
+        return st;
+    if (normk::rms_channel_launch(x, y, B, C, S, eps, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    return NORM_OK;
+}
+
+norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const float *beta, float *y, int64_t N,
+                                      int64_t C, int64_t num_groups, float eps, float negative_slope,
+                                      cudaStream_t stream)
+{
+    int64_t n = 0;
+    if (N < 0 || C < 0 || num_groups <= 0 || !valid_eps(eps) || !std::isfinite(negative_slope) ||
+        !safe_mul(N, C, &n))
+        return NORM_ERR_INVALID_ARG;
+    if (C % num_groups != 0)
+        return NORM_ERR_INVALID_ARG;
+    if (n == 0)
+        return NORM_OK;
+    if (!x || !y)
+        return NORM_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(y, 4) || !aligned(gamma, 4) || !aligned(beta, 4))
+        return NORM_ERR_MISALIGNED;
+    const size_t nb = static_cast<size_t>(n) * 4u, pb = static_cast<size_t>(C) * 4u;
+    if ((x != y && overlaps(x, nb, y, nb)) || overlaps(gamma, pb, y, nb) || overlaps(beta, pb, y, nb))
+        return NORM_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    norm_status_t st = device_state(&d);
+    if (st != NORM_OK)
+        return st;
+    const int64_t M = C / num_groups;
+    const bool pow2 = M >= 4 && M <= 128 && (M & (M - 1)) == 0;
+    const bool vec = pow2 && (C & 3) == 0 && C / 4 < (int64_t(1) << 30) && aligned(x, 16) && aligned(y, 16) &&
+                     aligned(gamma, 16) && aligned(beta, 16);
+    cudaError_t e = vec ? normk::gn_vec4_launch(x, gamma, beta, y, N, C, M, eps, negative_slope, stream)
+                        : normk::gn_warp_launch(x, gamma, beta, y, N, C, num_groups, eps, negative_slope,
+                                                d->sm_count, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    return NORM_OK;
+}
+
+norm_status_t norm_last_error(cudaStream_t stream)
+{
+    DeviceState *d = nullptr;
+    norm_status_t st = device_state(&d);
+    if (st != NORM_OK)
+        return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    unsigned word = 0;
+    if (cudaMemcpy(&word, d->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    if (word == 0)
+        return NORM_OK;
+    if (cudaMemset(d->err, 0, sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    if (word == NORM_ERR_TIMEOUT) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (d->ws && cudaMemset(d->ws, 0, d->ws_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return NORM_ERR_CUDA;
+        }
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    return static_cast<norm_status_t>(word);
+}
+
+} // extern "C"

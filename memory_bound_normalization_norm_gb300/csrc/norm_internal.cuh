@@ -1,0 +1,305 @@
+// norm_internal.cuh - device helpers and launcher declarations shared by the
+// kernels of libnormgb300 (sm_103a).  Inline PTX only; no library kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "norm.h"
+
+namespace normk {
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// L2 eviction policies (createpolicy, sm_80+).  evict_first for data that is
+// touched once (x, y), evict_last for data re-read by every row (gamma, beta).
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Coherent 128-bit / 32-bit global loads that do not allocate in L1, with an
+// L2 eviction policy.  (Coherent rather than .nc so that y == x is safe.)
+// Pure loads are not `volatile`: the compiler may schedule them freely, which
+// is what lets independent loads of an unrolled loop be in flight together.
+__device__ __forceinline__ float4 ld_stream_f4(const float4 *p, uint64_t pol)
+{
+    float4 v;
+    asm("ld.global.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ float ld_stream_f1(const float *p, uint64_t pol)
+{
+    float v;
+    asm("ld.global.L1::no_allocate.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+    return v;
+}
+
+// Read-only (non-coherent path) 128-bit load with an L2 policy: for gamma/beta,
+// which the kernels never write.
+__device__ __forceinline__ float4 ld_ro_f4(const float4 *p, uint64_t pol)
+{
+    float4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream_f4(float4 *p, float4 v, uint64_t pol)
+{
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;"
+                 :
+                 : "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream_f1(float *p, float v, uint64_t pol)
+{
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.f32 [%0], %1, %2;"
+                 :
+                 : "l"(p), "f"(v), "l"(pol)
+                 : "memory");
+}
+
+// Plain coherent scalar load (never the read-only path).
+__device__ __forceinline__ float ld_plain_f1(const float *p)
+{
+    float v;
+    asm("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// 128-bit load served from L2 (never a possibly stale L1 line): for data
+// written by other CTAs of the same kernel after a grid-scope acquire.
+__device__ __forceinline__ float4 ld_l2_f4(const float4 *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+// ---- mbarrier + bulk copy (TMA engine, non-tensor form)
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after timeout_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t timeout_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns)
+            return false;
+    }
+    return true;
+}
+
+// Bulk copy global -> this CTA's shared memory; completion is signalled on
+// `bar` as transaction bytes.  dst, src and bytes must be 16-byte multiples.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+// ---- gpu-scope synchronization primitives
+
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(unsigned *p, unsigned v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_release_gpu(unsigned *p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Record the first device-side failure in the per-device error word.
+__device__ __forceinline__ void record_error(unsigned *err, unsigned code)
+{
+    if (err)
+        atomicCAS(err, 0u, code);
+}
+
+// ---------------------------------------------------------------- statistics
+
+// A partial of (count, mean, M2 = sum of squared deviations from mean).
+struct Moments {
+    float n, mean, m2;
+};
+
+// Chan et al. pairwise update: fold b into a.
+__device__ __forceinline__ void chan_merge(Moments &a, const Moments &b)
+{
+    const float n = a.n + b.n;
+    if (b.n == 0.f)
+        return;
+    const float delta = b.mean - a.mean;
+    const float f = b.n / n;
+    a.mean = fmaf(delta, f, a.mean);
+    a.m2 = a.m2 + b.m2 + delta * delta * a.n * f;
+    a.n = n;
+}
+
+__device__ __forceinline__ Moments shfl_xor_moments(const Moments &a, int lane_mask)
+{
+    Moments b;
+    b.n = __shfl_xor_sync(0xffffffffu, a.n, lane_mask);
+    b.mean = __shfl_xor_sync(0xffffffffu, a.mean, lane_mask);
+    b.m2 = __shfl_xor_sync(0xffffffffu, a.m2, lane_mask);
+    return b;
+}
+
+// Butterfly merge over the 32 lanes of a warp; every lane ends with the
+// result.  The order of merges is fixed, so the result is deterministic.
+__device__ __forceinline__ Moments warp_merge(Moments a)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Moments b = shfl_xor_moments(a, o);
+        // Merge in lane order so both partners compute the same value.
+        const int lane = threadIdx.x & 31;
+        if (lane & o) {
+            Moments lo = b;
+            chan_merge(lo, a);
+            a = lo;
+        } else {
+            chan_merge(a, b);
+        }
+    }
+    return a;
+}
+
+// ---------------------------------------------------------------- launchers
+
+// Workspace header of the LayerNorm kernels (256 bytes, zeroed by the caller
+// before first use; the kernels leave it zeroed, except after a timeout).
+struct LnSync {
+    unsigned count[2]; // arrivals at the grid barrier of slot 0 / 1
+    unsigned gen[2];   // generation of slot 0 / 1 (bumped when all arrived)
+    unsigned pad[60];
+};
+static_assert(sizeof(LnSync) == 256, "LnSync must be 256 bytes");
+
+struct LnParams {
+    const float *x;
+    const float *gamma; // may be null
+    const float *beta;  // may be null
+    float *y;
+    int64_t rows;
+    int64_t row_len; // elements
+    float eps;
+    LnSync *sync;
+    float4 *part; // partials: persistent [2][grid], split [rows][P]
+    unsigned *err;
+    uint64_t timeout_ns;
+    unsigned expected; // arrivals the grid barrier waits for
+    int max_n4;        // persistent: float4 capacity of each smem buffer
+    int64_t chunk;     // split: elements per CTA (multiple of 4 on the vector path)
+    int parts;         // split: CTAs per row (P)
+};
+
+// Persistent single-read LayerNorm (one CTA per SM, cooperative launch).
+struct LnPersistentConfig {
+    int threads;     // CTA size
+    int v4_per_thread;
+};
+LnPersistentConfig ln_persistent_config();
+// Max dynamic shared memory the kernel may use; called once per device.
+cudaError_t ln_persistent_setup(int max_dynamic_smem);
+// Number of co-resident CTAs per SM for `dyn_smem` bytes.
+cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm);
+cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream);
+
+// Two-kernel LayerNorm (partials, then merge + apply); any shape.
+cudaError_t ln_split_launch(const LnParams &p, bool vec4, cudaStream_t stream);
+
+// GroupNorm + LeakyReLU + x2.
+cudaError_t gn_vec4_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
+                           int64_t M, float eps, float slope, cudaStream_t stream);
+cudaError_t gn_warp_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
+                           int64_t G, float eps, float slope, int sm_count, cudaStream_t stream);
+
+// RMSNorm over dim 1 of [B][C][S].
+cudaError_t rms_channel_launch(const float *x, float *y, int64_t B, int64_t C, int64_t S, float eps,
+                               cudaStream_t stream);
+
+} // namespace normk

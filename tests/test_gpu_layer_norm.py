@@ -1,0 +1,167 @@
+"""LayerNorm on the GPU against the float64 oracle, element by element.
+
+Both kernels are covered: the persistent single-read kernel (forced, and chosen
+automatically for long rows) and the two-kernel split path (forced, and taken for
+ragged or misaligned rows).  Shapes span several CTAs per row with ragged slices,
+rows shorter than one float4 per CTA, the largest row the persistent kernel
+holds on chip, and the two full-size workloads: (16, 64, 256, 256) with N(0,1)
+inputs and the cancellation stress x ~ N(1000, 0.01^2).
+"""
+import numpy as np
+import pytest
+import torch
+
+import normgen
+import oracle
+from gpu_util import TOL, Guarded, assert_parity, device
+
+pytestmark = pytest.mark.gpu
+
+AUTO, PERSISTENT, SPLIT = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def ng():
+    import memory_bound_normalization_norm_gb300 as m
+    yield m
+    m.norm_set_option(m.NORM_OPT_LN_PATH, AUTO)
+
+
+def run_ln(ng, x, g, b, rows, L, eps=1e-5, path=AUTO, offset=0, inplace=False, workspace=None):
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, path)
+    xb = Guarded(rows * L, x, offset=offset)
+    gd = None if g is None else Guarded(L, g, offset=offset).t
+    bd = None if b is None else Guarded(L, b, offset=offset).t
+    yb = xb if inplace else Guarded(rows * L, offset=offset)
+    if workspace is None:
+        ng.norm_layer_fwd(xb.t, gd, bd, yb.t, rows, L, eps)
+    else:
+        ws, nbytes = workspace
+        ng.norm_layer_fwd(xb.t, gd, bd, yb.t, rows, L, eps, ws, nbytes)
+    assert ng.norm_last_error() == 0
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, AUTO)
+    assert yb.guards_intact(), "LayerNorm wrote outside its output"
+    return yb.numpy()
+
+
+def inputs(rows, L, seed, mean=0.0, std=1.0, affine=True):
+    x = normgen.normal(rows * L, mean, std, seed=seed, tensor_id=0)
+    if not affine:
+        return x, None, None
+    g = normgen.normal(L, 1.0, 0.1, seed=seed, tensor_id=1)
+    b = normgen.normal(L, 0.0, 0.1, seed=seed, tensor_id=2)
+    return x, g, b
+
+
+SHAPES = [
+    (1, 4), (2, 64), (3, 600), (5, 4 * 152 * 13 + 4), (2, 65536 + 4), (4, 1 << 18), (1, 3 * (1 << 20)),
+]
+
+
+@pytest.mark.parametrize("path", [PERSISTENT, SPLIT])
+@pytest.mark.parametrize("rows,L", SHAPES)
+def test_layer_norm_paths(ng, path, rows, L):
+    x, g, b = inputs(rows, L, seed=rows * 7 + L)
+    want = oracle.layer_norm(x, g, b, rows, L)
+    assert_parity(run_ln(ng, x, g, b, rows, L, path=path), want, f"LN path={path} {rows}x{L}")
+
+
+@pytest.mark.parametrize("rows,L", [(1, 1), (2, 3), (3, 1001), (4, 4097), (2, 100003)])
+def test_layer_norm_ragged_rows(ng, rows, L):
+    x, g, b = inputs(rows, L, seed=L)
+    assert_parity(run_ln(ng, x, g, b, rows, L), oracle.layer_norm(x, g, b, rows, L), f"LN ragged {rows}x{L}")
+
+
+@pytest.mark.parametrize("path", [AUTO, SPLIT])
+def test_layer_norm_misaligned_pointers(ng, path):
+    rows, L = 3, 8192
+    x, g, b = inputs(rows, L, seed=11)
+    got = run_ln(ng, x, g, b, rows, L, path=path, offset=1)
+    assert_parity(got, oracle.layer_norm(x, g, b, rows, L), "LN misaligned")
+
+
+@pytest.mark.parametrize("path", [PERSISTENT, SPLIT])
+def test_layer_norm_identity_affine_and_in_place(ng, path):
+    rows, L = 3, 152 * 4 * 20
+    x, _, _ = inputs(rows, L, seed=5, affine=False)
+    want = oracle.layer_norm(x, None, None, rows, L)
+    assert_parity(run_ln(ng, x, None, None, rows, L, path=path), want, "LN no affine")
+    assert_parity(run_ln(ng, x, None, None, rows, L, path=path, inplace=True), want, "LN in place")
+
+
+@pytest.mark.parametrize("path", [PERSISTENT, SPLIT])
+def test_layer_norm_constant_rows_give_beta(ng, path):
+    rows, L = 2, 152 * 4 * 3
+    x = np.full(rows * L, 3.5, dtype=np.float32)
+    _, g, b = inputs(rows, L, seed=9)
+    got = run_ln(ng, x, g, b, rows, L, path=path).reshape(rows, L)
+    assert np.array_equal(got, np.stack([b, b])), "constant row must give exactly beta"
+
+
+def test_layer_norm_largest_resident_row(ng):
+    L = ng.norm_layer_max_resident_row_len()
+    assert L >= 64 * 256 * 256, "the (64, 256, 256) row must fit on chip"
+    x, g, b = inputs(2, L, seed=3)
+    got = run_ln(ng, x, g, b, 2, L, path=PERSISTENT)
+    assert_parity(got, oracle.layer_norm(x, g, b, 2, L), "LN largest resident row")
+    with pytest.raises(ng.NormError):
+        ng.norm_set_option(ng.NORM_OPT_LN_PATH, PERSISTENT)
+        try:
+            xd = torch.zeros(L + 4, device="cuda")
+            ng.norm_layer_fwd(xd, None, None, xd, 1, L + 4, 1e-5)
+        finally:
+            ng.norm_set_option(ng.NORM_OPT_LN_PATH, AUTO)
+
+
+def test_layer_norm_caller_workspace_reused(ng):
+    rows, L = 4, 152 * 4 * 50
+    nbytes = ng.norm_layer_workspace_bytes(rows, L)
+    ws = torch.zeros((nbytes + 255) // 4 + 64, dtype=torch.float32, device="cuda")
+    for seed in (1, 2, 3):
+        for path in (PERSISTENT, SPLIT):
+            x, g, b = inputs(rows, L, seed=seed)
+            got = run_ln(ng, x, g, b, rows, L, path=path, workspace=(ws, nbytes))
+            assert_parity(got, oracle.layer_norm(x, g, b, rows, L), f"LN caller workspace seed={seed}")
+    small = torch.zeros(64, dtype=torch.float32, device="cuda")
+    with pytest.raises(ng.NormError) as e:
+        ng.norm_layer_fwd(small, None, None, small, 1, 64, 1e-5, ws, 16)
+    assert e.value.status == ng.NORM_ERR_WORKSPACE
+
+
+def test_layer_norm_deterministic(ng):
+    rows, L = 3, 1 << 20
+    x, g, b = inputs(rows, L, seed=21)
+    a = run_ln(ng, x, g, b, rows, L, path=PERSISTENT)
+    c = run_ln(ng, x, g, b, rows, L, path=PERSISTENT)
+    assert a.tobytes() == c.tobytes()
+
+
+def test_layer_norm_empty_is_noop(ng):
+    yb = Guarded(16)
+    ng.norm_layer_fwd(None, None, None, yb.t, 0, 16, 1e-5)
+    ng.norm_layer_fwd(yb.t, None, None, yb.t, 4, 0, 1e-5)
+    torch.cuda.synchronize()
+    assert (yb.buf.view(torch.int32) == 0x7FC0DEAD).all()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("path", [AUTO, SPLIT])
+def test_layer_norm_full_size_normal(ng, path):
+    """(16, 64, 256, 256) over the last 3 dims, x ~ N(0,1), gamma ~ N(1,0.1), beta ~ N(0,0.1)."""
+    rows, L = 16, 64 * 256 * 256
+    x, g, b = inputs(rows, L, seed=0)
+    want = oracle.layer_norm(x, g, b, rows, L)
+    assert_parity(run_ln(ng, x, g, b, rows, L, path=path), want, f"LN full size path={path}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("path", [AUTO, SPLIT])
+def test_layer_norm_full_size_cancellation_stress(ng, path):
+    """(16, 64, 256, 256), x ~ N(1000, 0.01^2), gamma = 1, beta = 0 passed as tensors."""
+    rows, L = 16, 64 * 256 * 256
+    x = normgen.normal(rows * L, 1000.0, 1e-2, seed=0, tensor_id=0)
+    g = np.ones(L, dtype=np.float32)
+    b = np.zeros(L, dtype=np.float32)
+    want = oracle.layer_norm(x, g, b, rows, L)
+    err = assert_parity(run_ln(ng, x, g, b, rows, L, path=path), want, f"LN stress path={path}")
+    assert err < TOL / 4, f"cancellation stress margin too thin: {err:.2e}"

@@ -1,0 +1,100 @@
+"""Channel RMSNorm on the GPU against the float64 oracle, element by element.
+
+Covers every register-resident channel bucket (exact and ragged C up to 128),
+the two-read kernel (C > 128), odd spatial sizes, in place, misaligned pointers,
+the small (2, 64, 32, 32) workload in full, and the (112, 64, 512, 512) workload
+(7.5 GB in) on sampled outputs: whole batch entries at both ends and the middle
+plus random positions, each recomputed by the oracle from regenerated inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import normgen
+import oracle
+from gpu_util import Guarded, assert_parity, device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ng():
+    import memory_bound_normalization_norm_gb300 as m
+    return m
+
+
+def run_rms(ng, x, B, C, S, eps=1e-5, offset=0, inplace=False):
+    xb = Guarded(B * C * S, x, offset=offset)
+    yb = xb if inplace else Guarded(B * C * S, offset=offset)
+    ng.norm_rms_channel_fwd(xb.t, yb.t, B, C, S, eps)
+    out = yb.numpy()
+    assert yb.guards_intact(), "RMSNorm wrote outside its output"
+    return out
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 4, 5, 8, 13, 16, 31, 32, 33, 63, 64, 65, 100, 128, 129, 200])
+@pytest.mark.parametrize("B,S", [(1, 1), (3, 257), (2, 4096)])
+def test_channels(ng, C, B, S):
+    x = normgen.normal(B * C * S, seed=C * 1000 + S, tensor_id=0)
+    assert_parity(run_rms(ng, x, B, C, S), oracle.rms_channel(x, B, C, S), f"RMS B={B} C={C} S={S}")
+
+
+def test_in_place_and_misaligned(ng):
+    B, C, S = 3, 64, 1023
+    x = normgen.normal(B * C * S, seed=5)
+    want = oracle.rms_channel(x, B, C, S)
+    assert_parity(run_rms(ng, x, B, C, S, inplace=True), want, "RMS in place")
+    assert_parity(run_rms(ng, x, B, C, S, offset=1), want, "RMS misaligned")
+
+
+def test_zero_input_is_zero(ng):
+    B, C, S = 2, 64, 300
+    x = np.zeros(B * C * S, dtype=np.float32)
+    assert np.array_equal(run_rms(ng, x, B, C, S), x)
+
+
+def test_large_values_do_not_overflow(ng):
+    B, C, S = 1, 64, 512
+    x = normgen.normal(B * C * S, 0.0, 1e18, seed=6)
+    assert_parity(run_rms(ng, x, B, C, S), oracle.rms_channel(x, B, C, S), "RMS large values")
+
+
+def test_small_workload_full(ng):
+    """(2, 64, 32, 32), x ~ N(0,1) seed 0, eps 1e-5."""
+    B, C, S = 2, 64, 32 * 32
+    x = normgen.normal(B * C * S, seed=0, tensor_id=0)
+    assert_parity(run_rms(ng, x, B, C, S), oracle.rms_channel(x, B, C, S), "RMS (2,64,32,32)")
+
+
+def test_many_batches_fold_grid(ng):
+    B, C, S = 70000, 4, 3
+    x = normgen.normal(B * C * S, seed=7)
+    assert_parity(run_rms(ng, x, B, C, S), oracle.rms_channel(x, B, C, S), "RMS 70000 batches")
+
+
+@pytest.mark.slow
+def test_full_size_sampled(ng):
+    """(112, 64, 512, 512), x ~ N(0,1) seed 0: 1.88e9 elements, int64 indexing throughout."""
+    B, C, S = 112, 64, 512 * 512
+    n = B * C * S
+    x = normgen.normal(n, seed=0, tensor_id=0)
+    xd = torch.from_numpy(x).to("cuda")
+    yd = torch.empty_like(xd)
+    ng.norm_rms_channel_fwd(xd, yd, B, C, S, 1e-5)
+    torch.cuda.synchronize()
+    del xd
+    # whole batch entries: first, middle, last
+    for b in (0, 57, B - 1):
+        sl = slice(b * C * S, (b + 1) * C * S)
+        want = oracle.rms_channel(x[sl], 1, C, S)
+        assert_parity(yd[sl].cpu().numpy(), want, f"RMS full size batch {b}")
+    # random positions anywhere, inputs regenerated from the stream one channel at a time
+    rng = np.random.default_rng(0)
+    bs = rng.integers(0, B, 512)
+    ss = rng.integers(0, S, 512)
+    idx = (bs[:, None] * C * S + np.arange(C)[None, :] * S + ss[:, None]).astype(np.int64)
+    cols = np.stack([np.concatenate([normgen.normal(1, seed=0, tensor_id=0, start=int(i)) for i in row])
+                     for row in idx])
+    want = np.stack([oracle.rms_channel(cols[k], 1, C, 1) for k in range(len(bs))])
+    got = yd[torch.from_numpy(idx.ravel()).to("cuda")].cpu().numpy().reshape(want.shape)
+    assert_parity(got, want, "RMS full size sampled positions")
