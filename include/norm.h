@@ -92,6 +92,32 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
                              int64_t rows, int64_t row_len, float eps,
                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* LayerNorm that allocates nothing.  The pages have no counterpart: this is a
+ * service for callers that cannot allocate device memory at the time of the
+ * call (inside an allocator's own callbacks, under a fixed memory pool, or
+ * in a plugin that is handed only its inputs and outputs), so they can pass
+ * neither a workspace nor workspace == NULL (which allocates once).
+ *
+ * Same operation, arguments and results as norm_layer_fwd without the
+ * workspace: the scratch lives in a static device array of
+ * NORM_NOALLOC_SCRATCH_BYTES (1 MiB) inside the library, held by every device
+ * that loads the library until the process exits.
+ *   - Returns NORM_ERR_WORKSPACE, without launching, when the shape needs
+ *     more scratch than that (norm_layer_workspace_bytes(rows, row_len) >
+ *     NORM_NOALLOC_SCRATCH_BYTES, e.g. more than ~65,000 rows of short
+ *     length).
+ *   - The first call on a device looks up the array's device address on the
+ *     current device; make that first call before any stream capture.
+ *   - Every call clears the array's 256-byte barrier header with a
+ *     stream-ordered memset, then runs the LayerNorm kernels on `stream`.
+ *   - All calls on a device share the one array: calls that can overlap on
+ *     the GPU (different streams, or different host threads without
+ *     ordering) race and give wrong results.  Serialize them.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine. */
+#define NORM_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+norm_status_t norm_layer_fwd_noalloc(const float *x, const float *gamma, const float *beta, float *y,
+                                     int64_t rows, int64_t row_len, float eps, cudaStream_t stream);
+
 /* Zero `bytes` of a LayerNorm workspace on `stream` (stream-ordered). */
 norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStream_t stream);
 

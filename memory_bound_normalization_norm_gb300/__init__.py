@@ -8,6 +8,7 @@ fallback: importing this package fails loudly if the compiled library is missing
 Entry points (same names and argument order as the C functions):
 
 * ``norm_layer_fwd(x, gamma, beta, y, rows, row_len, eps, workspace=None, workspace_bytes=0, stream=None)``
+* ``norm_layer_fwd_noalloc(x, gamma, beta, y, rows, row_len, eps, stream=None)``
 * ``norm_rms_channel_fwd(x, y, B, C, S, eps, stream=None)``
 * ``norm_group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream=None)``
 * ``norm_last_error(stream=None)``, ``norm_layer_workspace_bytes(rows, row_len)``,
@@ -44,6 +45,7 @@ NORM_OPT_LN_CTAS = 4
 EXPORTED = (
     "norm_layer_workspace_bytes",
     "norm_layer_fwd",
+    "norm_layer_fwd_noalloc",
     "norm_layer_workspace_reset",
     "norm_layer_max_resident_row_len",
     "norm_rms_channel_fwd",
@@ -76,6 +78,8 @@ _lib.norm_layer_workspace_bytes.restype = _sz
 _lib.norm_layer_workspace_bytes.argtypes = [_i64, _i64]
 _lib.norm_layer_fwd.restype = _int
 _lib.norm_layer_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _f32, _vp, _sz, _vp]
+_lib.norm_layer_fwd_noalloc.restype = _int
+_lib.norm_layer_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _f32, _vp]
 _lib.norm_layer_workspace_reset.restype = _int
 _lib.norm_layer_workspace_reset.argtypes = [_vp, _sz, _vp]
 _lib.norm_layer_max_resident_row_len.restype = _i64
@@ -144,6 +148,13 @@ def norm_layer_max_resident_row_len() -> int:
 def norm_layer_fwd(x, gamma, beta, y, rows, row_len, eps, workspace=None, workspace_bytes=0, stream=None):
     _check(_lib.norm_layer_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), rows, row_len, eps,
                                _ptr(workspace), workspace_bytes, _stream(stream)), "norm_layer_fwd")
+
+
+def norm_layer_fwd_noalloc(x, gamma, beta, y, rows, row_len, eps, stream=None):
+    """LayerNorm whose scratch is a fixed 1 MiB array inside the library, for callers
+    that cannot allocate device memory; see include/norm.h for its limits."""
+    _check(_lib.norm_layer_fwd_noalloc(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), rows, row_len, eps,
+                                       _stream(stream)), "norm_layer_fwd_noalloc")
 
 
 def norm_layer_workspace_reset(workspace, workspace_bytes, stream=None):
