@@ -71,20 +71,23 @@ typedef enum {
  * beta     [row_len] elementwise bias, or NULL for bias 0.
  * workspace  device scratch of at least norm_layer_workspace_bytes(rows,
  *          row_len) bytes, 256-byte aligned, zero-filled before its first use
- *          (cudaMemset or norm_layer_workspace_reset).  The kernels leave it
- *          ready for the next call, except after NORM_ERR_TIMEOUT, when it
- *          must be reset again.  A workspace must not be shared by calls that
+ *          (cudaMemset or norm_layer_workspace_reset).  The kernels keep it
+ *          consistent from call to call, except after NORM_ERR_TIMEOUT, when
+ *          it must be zero-filled again.  A workspace must not be shared by calls that
  *          can run at the same time (different streams).
  *          workspace == NULL: the library uses its own per-device workspace,
  *          allocated with cudaMalloc on the first such call on a device and
  *          kept until exit; such calls must then be serialized by the caller
  *          (one stream at a time).
  *
- * Rows whose length is a multiple of 4 with 16-byte aligned x/y/gamma/beta
- * and at most norm_layer_max_resident_row_len() elements are read from HBM
- * once: a persistent cooperative kernel keeps every CTA's slice of a row on
- * chip across a bounded grid barrier.  Other shapes take a two-kernel path
- * that reads x twice.  Both produce the same statistics definition.
+ * Rows of 2^20 or more elements (up to norm_layer_max_resident_row_len()),
+ * with a length that is a multiple of 4 and 16-byte aligned x/y/gamma/beta,
+ * are read from HBM once: a persistent cooperative kernel (one CTA per SM)
+ * gives every CTA the same column slice of each row, holds the slice on chip
+ * (shared memory, then registers) from the moment it arrives until y is
+ * written, and merges the row's statistics across the GPU with one bounded
+ * grid barrier per row.  Other shapes take a two-kernel path that reads x
+ * twice.  Both produce the same statistics definition.
  */
 size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len);
 
@@ -108,7 +111,8 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
  *     length).
  *   - The first call on a device looks up the array's device address on the
  *     current device; make that first call before any stream capture.
- *   - Every call clears the array's 256-byte barrier header with a
+ *   - Every call zeroes the part of the array that the shape uses
+ *     (norm_layer_workspace_bytes(rows, row_len) bytes) with a
  *     stream-ordered memset, then runs the LayerNorm kernels on `stream`.
  *   - All calls on a device share the one array: calls that can overlap on
  *     the GPU (different streams, or different host threads without
@@ -122,7 +126,10 @@ norm_status_t norm_layer_fwd_noalloc(const float *x, const float *gamma, const f
 norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStream_t stream);
 
 /* Longest row (in elements) that the single-read persistent LayerNorm kernel
- * can hold on chip on the current device; 0 if the device cannot run it. */
+ * serves on the current device: each CTA's slice of a row must fit its two
+ * shared-memory row buffers and its threads' registers (7,200 float4 per CTA,
+ * 4,377,600 elements on a 152-SM GB300).  0 if the device cannot run the
+ * kernel. */
 int64_t norm_layer_max_resident_row_len(void);
 
 /* ------------------------------------------------------------------ RMSNorm
@@ -183,9 +190,10 @@ const char *norm_status_string(norm_status_t status);
  *                                barrier (or for its own bulk copies) before
  *                                it records NORM_ERR_TIMEOUT and returns
  *                                without writing y.  Default 200 ms.
- *   NORM_OPT_BARRIER_EXTRA_ARRIVALS  test hook: the grid barrier waits for
- *                                this many arrivals more than there are CTAs,
- *                                so it can only end by timing out.  Default 0.
+ *   NORM_OPT_BARRIER_EXTRA_ARRIVALS  test hook: when > 0, the grid barrier
+ *                                waits for partial statistics that no CTA
+ *                                publishes, so it can only end by timing
+ *                                out.  Default 0.
  *   NORM_OPT_LN_CTAS             CTAs of the persistent kernel (0 = one per
  *                                SM, the default).
  * Returns NORM_ERR_INVALID_ARG for an unknown option or a negative value.

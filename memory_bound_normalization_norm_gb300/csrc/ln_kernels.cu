@@ -4,34 +4,50 @@
 // gamma + beta with elementwise gamma/beta).
 //
 // Statistics.  All partial statistics are (count, mean, M2) triples of
-// d = x - K, where the pivot K is an element of the row (the first element
-// of the CTA's slice in the persistent kernel, x[r][0] in the split path).
+// d = x - K, where the pivot K is an element of the row (the median of its
+// first, middle and last elements in the persistent kernel, x[r][0] in the
+// split path).
 // Shifting by an element of the row keeps the partial sums small when
 // |mean| >> std (for x ~ N(1000, 0.01^2) an fp32 sum of raw x would lose the
 // variance entirely); d is exact whenever x and K are within a factor of 2.
-// Per thread the triple is computed two-pass from registers, then folded with
-// Chan's pairwise update (Chan, Golub, LeVeque 1979) across the warp, the CTA
-// and finally across all CTAs of the row in a fixed order, each CTA's mean
-// first re-expressed against one reference pivot K_ref ((K_c - K_ref) is
-// exact for clustered data).  The row mean is then K_ref + delta, carried as
-// an unevaluated fp32 pair (hi, lo), and the output is
+// Per thread the triple comes from shifted sums (sum d, sum d^2), which a
+// pivot inside the bulk of the row keeps well conditioned; triples are
+// folded with Chan's pairwise update (Chan, Golub, LeVeque 1979) across the
+// warp and the CTA, and across CTAs with the two-pass formula over partials,
+// in a fixed order.  The row mean is then K + delta, carried as an
+// unevaluated fp32 pair (hi, lo), and the output is
 // ((x - hi) - lo) * rstd * gamma + beta.
 //
 // Persistent path (one CTA per SM, cooperative launch so all CTAs are
-// co-resident).  CTA c owns the same float4 column slice of every row.  For
-// row r it:
-//   1. waits for its slice, bulk-copied (TMA engine) into shared-memory
-//      buffer r%2, and moves it into registers (V float4 per thread);
-//   2. immediately reuses the buffer for the bulk copy of row r+2, so two
-//      future rows stream from HBM while row r is reduced and written;
-//   3. reduces its triple and publishes it to the workspace, then waits at a
-//      per-row grid barrier (acquire/release counters, bounded by
-//      %globaltimer: on timeout it records NORM_ERR_TIMEOUT, drains its own
-//      bulk copies and returns without writing y);
-//   4. merges all CTAs' triples (identically in every CTA) and writes y from
-//      the registers with evict-first stores; gamma/beta are read through L2
-//      with an evict-last policy so they come from HBM once per launch.
-// x is read from HBM once and y written once.
+// co-resident).  CTA c owns the same float4 column slice of every row.  Row
+// slices arrive by bulk copy (TMA engine, 32 KB pieces) into two
+// shared-memory buffers, two rows ahead; the slice of the row being written
+// lives in registers.  x is read from HBM once and stays on chip until y is
+// written.  Warp 0 coordinates (bulk copies, grid barrier, merge); warps
+// 1..15 own the data.  Iteration r:
+//   1. warps 1..15 reduce the two-pass triples of row r+1 from its buffer
+//      and start loading their first gamma/beta batch of row r, while warp 0
+//      waits for and merges the triples of row r, published one iteration
+//      earlier, so the grid-wide wait is normally over when warp 0 looks;
+//   2. warp 0 publishes row r+1's triple; warps 1..15 write y of row r from
+//      registers, streaming gamma/beta through L2 (evict-last, so they come
+//      from HBM once per launch) two batches deep, then move row r+1 from its
+//      buffer into registers;
+//   3. warp 0 refills the buffer with the bulk copy of row r+3.
+//
+// Grid barrier without atomics.  Each CTA publishes its (mean, M2) as two
+// 64-bit words, each carrying a 32-bit tag in its high half, written with
+// st.relaxed.gpu (single-copy atomic).  Warp 0 polls the G records of the row
+// with plain L2 loads (ld.global.cg, which overlap) until every tag matches,
+// so the barrier and its data arrive in the same round trip.  Records sit in 4 rotating slots.  Tags count rows: row r
+// of a launch is tagged row_base + r + 1, where row_base (workspace header)
+// is the number of rows the persistent kernel has already processed on this
+// workspace.  A slot therefore only ever holds tags smaller than the one
+// awaited, and a zeroed workspace holds tag 0, which is never awaited.
+// row_base is read at kernel start and advanced by CTA 0 after its last
+// merge, which proves every CTA has read it.  Every wait is bounded by
+// %globaltimer: on timeout a CTA records NORM_ERR_TIMEOUT, drains its own bulk
+// copies and returns without writing y.
 //
 // Split path (any shape): kernel 1 writes one triple per (row, chunk) CTA;
 // kernel 2 merges the row's triples and applies, re-reading x.
@@ -41,10 +57,17 @@ namespace normk {
 
 namespace {
 
-constexpr int LN_T = 512; // threads per CTA, persistent kernel
-constexpr int LN_V = 14;  // float4 per thread held in registers
-constexpr int LN_AB = 5;  // gamma/beta float4 loaded ahead per batch
+// Warp 0 coordinates; warps 1..15 own the row slice (15 float4 each).
+constexpr int LN_DATA_WARPS = 15;
+constexpr int LN_T = 32 * LN_DATA_WARPS;  // data threads
+constexpr int LN_THREADS = LN_T + 32;     // CTA size
+constexpr int LN_V = 15;                  // float4 of the slice per data thread
+constexpr int LN_GB = 3;                  // gamma/beta float4 per load batch
+constexpr int LN_NB = LN_V / LN_GB;       // batches per row
+constexpr int LN_SLOTS = 4;               // partial-record slots: reused 4 rows later
+constexpr int LN_MAX_GRID = 160;          // CTAs whose records one warp loads at once
 constexpr uint32_t LN_BULK_CHUNK = 32768;
+static_assert(LN_V % LN_GB == 0, "whole gamma/beta batches");
 
 struct RowMean {
     float hi, lo, rstd;
@@ -90,6 +113,18 @@ __device__ __forceinline__ float4 ln_apply4(float4 v, const RowMean &rm, float4 
     return o;
 }
 
+// Two-pass triple of the 4 values of q shifted by K.
+__device__ __forceinline__ Moments quad_moments(float4 q, float K)
+{
+    const float a = q.x - K, b = q.y - K, c = q.z - K, d = q.w - K;
+    Moments m;
+    m.n = 4.f;
+    m.mean = ((a + b) + (c + d)) * 0.25f;
+    const float da = a - m.mean, db = b - m.mean, dc = c - m.mean, dd = d - m.mean;
+    m.m2 = (da * da + db * db) + (dc * dc + dd * dd);
+    return m;
+}
+
 // CTA-wide fold of per-thread triples; the result is valid in thread 0.
 template <int T>
 __device__ __forceinline__ Moments cta_merge(Moments m, Moments *scratch)
@@ -108,198 +143,345 @@ __device__ __forceinline__ Moments cta_merge(Moments m, Moments *scratch)
     return r;
 }
 
-__global__ void __launch_bounds__(LN_T, 1) ln_persistent_kernel(LnParams p)
+// ---------------------------------------------------------------- persistent path
+
+__device__ __forceinline__ unsigned long long tagged(unsigned tag, float v)
+{
+    return (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
+}
+
+__device__ __forceinline__ unsigned record_tag(unsigned long long w)
+{
+    return static_cast<unsigned>(w >> 32);
+}
+
+__device__ __forceinline__ float record_value(unsigned long long w)
+{
+    return __uint_as_float(static_cast<unsigned>(w & 0xffffffffull));
+}
+
+// Tag of row r's records (never 0, the tag of a zeroed workspace, for the
+// first 2^32 - 1 rows processed on a workspace).
+__device__ __forceinline__ unsigned row_tag(unsigned row_base, int64_t r)
+{
+    return row_base + static_cast<unsigned>(r) + 1u;
+}
+
+struct GridMerge {
+    Moments tot;
+    bool ok;
+};
+
+// Warp 0: poll the G <= LN_MAX_GRID records (mean, M2 of x - K, all about
+// the row's one pivot K) of a row until every tag equals `tag` (bounded),
+// then merge them with the two-pass formula over partials:
+//   delta = sum_c n_c m_c / N,   M2 = sum_c M2_c + sum_c n_c (m_c - delta)^2,
+// with each count n_c known from the partition (q or q + 1 float4).  The
+// sums are warp reductions in a fixed order, so every CTA computes the same
+// bits; the result is valid in lane 0.
+__device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *rec, int G, unsigned q4,
+                                                    unsigned rem, unsigned tag, uint64_t timeout_ns)
+{
+    constexpr int J = LN_MAX_GRID / 32;
+    const int lane = threadIdx.x & 31;
+    GridMerge g;
+    g.ok = true;
+    uint64_t t0 = 0;
+    for (int attempt = 0;; ++attempt) {
+        // the words live only inside one attempt, so they stay in registers
+        unsigned long long w[J][2];
+        unsigned bad = 0;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            // lanes past the last CTA re-read record G-1 (branch-free loads)
+            const int i = min(lane + 32 * j, G - 1);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                w[j][e] = ld_cg_u64(rec + 2 * i + e);
+                bad |= record_tag(w[j][e]) ^ tag;
+            }
+        }
+        if (__all_sync(0xffffffffu, bad == 0)) {
+            const float N = 4.f * (static_cast<float>(q4) * static_cast<float>(G) + static_cast<float>(rem));
+            float sm = 0.f; // sum of n_c * m_c
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int i = lane + 32 * j;
+                if (i < G) {
+                    const float n = 4.f * static_cast<float>(q4 + (static_cast<unsigned>(i) < rem ? 1u : 0u));
+                    sm = fmaf(n, record_value(w[j][0]), sm);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                sm += __shfl_xor_sync(0xffffffffu, sm, o);
+            const float delta = __shfl_sync(0xffffffffu, sm, 0) / N;
+            float sq = 0.f; // sum of M2_c + n_c (m_c - delta)^2
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int i = lane + 32 * j;
+                if (i < G) {
+                    const float n = 4.f * static_cast<float>(q4 + (static_cast<unsigned>(i) < rem ? 1u : 0u));
+                    const float dm = record_value(w[j][0]) - delta;
+                    sq += fmaf(n * dm, dm, record_value(w[j][1]));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            g.tot.n = N;
+            g.tot.mean = delta;
+            g.tot.m2 = __shfl_sync(0xffffffffu, sq, 0);
+            return g;
+        }
+        if (attempt == 0)
+            t0 = globaltimer_ns();
+        else if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > timeout_ns)) {
+            g.ok = false;
+            return g;
+        }
+        __nanosleep(20);
+    }
+}
+
+// Pivot of row q: the median of its first, middle and last elements.  A
+// pivot inside the bulk of the row keeps the shifted sums small, and one
+// outlier cannot become the pivot.
+__device__ __forceinline__ float row_pivot(const float *x, int64_t q, int64_t row_len)
+{
+    const float *xr = x + q * row_len;
+    const float a = ld_plain_f1(xr), b = ld_plain_f1(xr + (row_len >> 1)), c = ld_plain_f1(xr + (row_len - 1));
+    return fmaxf(fminf(a, b), fminf(fmaxf(a, b), c));
+}
+
+__global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p)
 {
     extern __shared__ __align__(128) float4 ln_smem[];
-    __shared__ __align__(8) uint64_t bars[2];
-    __shared__ Moments red[LN_T / 32];
+    __shared__ __align__(8) uint64_t bar_x[2];
+    __shared__ Moments red[LN_DATA_WARPS];
+    __shared__ float pivot[2]; // the pivot K of a row, by row parity
     __shared__ RowMean row_mean;
+    __shared__ unsigned row_base_s;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, cta = blockIdx.x;
+    const int64_t R = p.rows;
     const int64_t L4 = p.row_len >> 2;
-    const int64_t f0 = (static_cast<int64_t>(cta) * L4) / G;
-    const int64_t f1 = (static_cast<int64_t>(cta + 1) * L4) / G;
-    const int n4 = static_cast<int>(f1 - f0);
+    // CTA c owns n4 = q4 (+1 for the first rem CTAs) float4 of every row,
+    // starting at f0; the merge recomputes every CTA's count the same way.
+    const unsigned q4 = static_cast<unsigned>(L4 / G), rem = static_cast<unsigned>(L4 % G);
+    const int64_t f0 = static_cast<int64_t>(cta) * q4 + min(static_cast<unsigned>(cta), rem);
+    const int n4 = static_cast<int>(q4 + (static_cast<unsigned>(cta) < rem ? 1u : 0u));
     const float4 *x4 = reinterpret_cast<const float4 *>(p.x);
     float4 *y4 = reinterpret_cast<float4 *>(p.y);
     const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma);
     const float4 *b4 = reinterpret_cast<const float4 *>(p.beta);
+    unsigned long long *records = reinterpret_cast<unsigned long long *>(p.part);
+    const int buf_f4 = (p.max_n4 + 7) & ~7;
 
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
 
-    // Thread 0 tracks the bulk copies it issued (rows < issued) and those
-    // already consumed (rows < consumed) so that an early exit can drain them.
-    // Abort decisions are block-wide votes (__syncthreads_or), so every thread
-    // leaves the row loop at the same barrier.
-    int64_t issued = 0, consumed = 0;
-    bool aborted = false;
-
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        mbar_init(&bar_x[0], 1);
+        mbar_init(&bar_x[1], 1);
         fence_mbar_init();
         fence_proxy_async_smem();
+        row_base_s = ld_relaxed_gpu_u32(&p.sync->row_base);
+        if (R > 0)
+            pivot[0] = row_pivot(p.x, 0, p.row_len);
     }
     __syncthreads();
+    const unsigned row_base = row_base_s;
+    bool aborted = false;
 
-    auto issue_row = [&](int64_t r) {
-        uint64_t *bar = &bars[r & 1];
-        const uint32_t bytes = static_cast<uint32_t>(n4) * 16u;
-        mbar_arrive_expect_tx(bar, bytes);
-        const float4 *src = x4 + r * L4 + f0;
-        float4 *dst = ln_smem + ((r & 1) ? p.max_n4 : 0);
-        for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK) {
-            const uint32_t nb = (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK;
-            bulk_g2s(dst + off / 16, src + off / 16, nb, bar, pol_stream);
+    // Warp 0 and warps 1..15 run separate loops with the same two block-wide
+    // barriers per iteration, so each role keeps only its own state in
+    // registers.  Abort decisions are block-wide votes (__syncthreads_or).
+    if (warp == 0) {
+        // ------------------------------------------------ coordinator
+        // Lane 0 tracks the bulk copies it issued (rows < issued) and those
+        // whose completion it observed (rows < waited), so that an early exit
+        // can drain them.
+        int64_t issued = 0, waited = 0;
+        auto issue_x = [&](int64_t q) {
+            uint64_t *bar = &bar_x[q & 1];
+            const uint32_t bytes = static_cast<uint32_t>(n4) * 16u;
+            mbar_arrive_expect_tx(bar, bytes);
+            const float4 *src = x4 + q * L4 + f0;
+            float4 *dst = ln_smem + (q & 1) * buf_f4;
+            for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
+                bulk_g2s(dst + off / 16, src + off / 16,
+                         (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, bar, pol_stream);
+        };
+        if (lane == 0) {
+            issue_x(0);
+            issued = 1;
+            if (R > 1) {
+                issue_x(1);
+                issued = 2;
+            }
         }
-    };
-
-    if (tid == 0) {
-        issue_row(0);
-        issued = 1;
-        if (p.rows > 1) {
-            issue_row(1);
-            issued = 2;
-        }
-    }
-
-    for (int64_t r = 0; r < p.rows; ++r) {
-        const int b = static_cast<int>(r & 1);
-        const uint32_t parity = static_cast<uint32_t>((r >> 1) & 1);
-        const bool last_row = (r + 1 == p.rows);
-
-        // 1. slice of row r -> registers
-        const bool landed = mbar_wait_bounded(&bars[b], parity, p.timeout_ns);
-        const float4 *cur = ln_smem + (b ? p.max_n4 : 0);
-        // this CTA's pivot: the first element of its slice (any element of
-        // the row serves; a CTA without elements contributes nothing)
-        const float K = (n4 > 0) ? cur[0].x : 0.f;
-        float4 v[LN_V];
-#pragma unroll
-        for (int k = 0; k < LN_V; ++k) {
-            const int i = tid + k * LN_T;
-            v[k] = (i < n4) ? cur[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        // everyone has read the buffer; leave together if any wait gave up
-        if (__syncthreads_or(landed ? 0 : 1)) {
-            aborted = true;
-            break;
-        }
-        if (tid == 0) {
-            consumed = r + 1;
-            // 2. refill the buffer with row r+2 while row r is processed
-            if (r + 2 < p.rows) {
+        for (int64_t r = -1; r < R; ++r) {
+            const int64_t nx = r + 1;
+            bool fail = false;
+            if (r >= 0) {
+                const GridMerge gm = poll_and_merge(records + static_cast<int64_t>(r % LN_SLOTS) * G * 2, G, q4,
+                                                    rem, row_tag(row_base, r) + p.tag_skew, p.timeout_ns);
+                if (!gm.ok) {
+                    fail = true;
+                    if (lane == 0)
+                        record_error(p.err, NORM_ERR_TIMEOUT);
+                } else if (lane == 0) {
+                    row_mean = finish_row(pivot[r & 1], gm.tot, p.eps);
+                    // every CTA has read row_base once CTA 0 has merged the last row
+                    if (r + 1 == R && cta == 0)
+                        st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(R));
+                }
+            }
+            if (nx < R && lane == 0) {
+                if (mbar_wait_bounded(&bar_x[nx & 1], static_cast<uint32_t>((nx >> 1) & 1), p.timeout_ns))
+                    waited = nx + 1;
+                else
+                    fail = true;
+            }
+            if (__syncthreads_or(fail ? 1 : 0)) { // 1: triples of row nx reduced, row r merged
+                aborted = true;
+                break;
+            }
+            if (nx < R) {
+                Moments c = {0.f, 0.f, 0.f};
+                if (lane < LN_DATA_WARPS)
+                    c = red[lane];
+                c = warp_merge(c);
+                if (lane == 0) {
+                    const unsigned tag = row_tag(row_base, nx);
+                    unsigned long long *out = records + (static_cast<int64_t>(nx % LN_SLOTS) * G + cta) * 2;
+                    st_relaxed_gpu_u64(out + 0, tagged(tag, c.mean));
+                    st_relaxed_gpu_u64(out + 1, tagged(tag, c.m2));
+                }
+            }
+            // the pivot of row nx + 1 for the data warps' next iteration (its
+            // slot was last read for row nx - 1, which is merged already)
+            if (lane == 0 && nx + 1 < R)
+                pivot[(nx + 1) & 1] = row_pivot(p.x, nx + 1, p.row_len);
+            __syncthreads(); // 2: y of row r written, row nx moved out of its buffer
+            if (lane == 0 && nx + 2 < R) {
                 fence_proxy_async_smem();
-                issue_row(r + 2);
-                issued = r + 3;
+                issue_x(nx + 2);
+                issued = nx + 3;
             }
         }
-
-        // 3. per-thread two-pass triple of d = x - K over valid elements
-        Moments m = {0.f, 0.f, 0.f};
-        {
-            float s = 0.f;
-            int cnt = 0;
-#pragma unroll
-            for (int k = 0; k < LN_V; ++k) {
-                if (tid + k * LN_T < n4) {
-                    s += ((v[k].x - K) + (v[k].y - K)) + ((v[k].z - K) + (v[k].w - K));
-                    cnt += 4;
-                }
-            }
-            if (cnt > 0) {
-                m.n = static_cast<float>(cnt);
-                m.mean = s / m.n;
-                float q = 0.f;
-#pragma unroll
-                for (int k = 0; k < LN_V; ++k) {
-                    if (tid + k * LN_T < n4) {
-                        const float a = (v[k].x - K) - m.mean, bq = (v[k].y - K) - m.mean;
-                        const float c = (v[k].z - K) - m.mean, d = (v[k].w - K) - m.mean;
-                        q = fmaf(a, a, q);
-                        q = fmaf(bq, bq, q);
-                        q = fmaf(c, c, q);
-                        q = fmaf(d, d, q);
-                    }
-                }
-                m.m2 = q;
-            }
-        }
-        const Moments cm = cta_merge<LN_T>(m, red);
-
-        // publish + grid barrier (thread 0), then merge of all partials (warp 0)
-        bool ok = true;
-        if (tid < 32) {
-            float4 *slot = p.part + static_cast<int64_t>(b) * G;
-            if (tid == 0) {
-                const unsigned gen0 = ld_acquire_gpu(&p.sync->gen[b]);
-                slot[cta] = make_float4(cm.n, cm.mean, cm.m2, K);
-                const unsigned old = atom_add_acq_rel_gpu(&p.sync->count[b], 1u);
-                if (old + 1 == p.expected) {
-                    st_relaxed_gpu(&p.sync->count[b], 0u);
-                    red_add_release_gpu(&p.sync->gen[b], 1u);
-                } else {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (ld_acquire_gpu(&p.sync->gen[b]) == gen0) {
-                        if (globaltimer_ns() - t0 > p.timeout_ns) {
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(32);
-                    }
-                }
-                if (!ok)
+        // Drain: never leave a bulk copy in flight into shared memory.
+        if (lane == 0) {
+            for (int64_t q = waited; q < issued; ++q) {
+                if (!mbar_wait_bounded(&bar_x[q & 1], static_cast<uint32_t>((q >> 1) & 1), p.timeout_ns))
                     record_error(p.err, NORM_ERR_TIMEOUT);
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            __syncwarp();
-            if (ok) {
-                // reference pivot: the last CTA's (its slice is never empty)
-                const float K_ref = ld_l2_f4(slot + (G - 1)).w;
-                const Moments tot = merge_partials_warp(slot, G, K_ref);
-                if (tid == 0)
-                    row_mean = finish_row(K_ref, tot, p.eps);
-            }
-        }
-        if (__syncthreads_or(ok ? 0 : 1)) {
-            aborted = true;
-            break;
-        }
-
-        // 4. apply from registers; gamma/beta are loaded LN_AB float4 at a
-        //    time ahead of the stores that need them
-        const RowMean rm = row_mean;
-        const uint64_t pol_gb = last_row ? pol_stream : pol_keep;
-        float4 *yr = y4 + r * L4 + f0;
-#pragma unroll
-        for (int k0 = 0; k0 < LN_V; k0 += LN_AB) {
-            float4 g[LN_AB], bb[LN_AB];
-#pragma unroll
-            for (int j = 0; j < LN_AB; ++j) {
-                const int i = tid + (k0 + j) * LN_T;
-                const bool in = (k0 + j < LN_V) && i < n4;
-                g[j] = (in && g4) ? ld_ro_f4(g4 + f0 + i, pol_gb) : make_float4(1.f, 1.f, 1.f, 1.f);
-                bb[j] = (in && b4) ? ld_ro_f4(b4 + f0 + i, pol_gb) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int j = 0; j < LN_AB; ++j) {
-                const int i = tid + (k0 + j) * LN_T;
-                if ((k0 + j < LN_V) && i < n4)
-                    st_stream_f4(yr + i, ln_apply4(v[k0 + j], rm, g[j], bb[j]), pol_stream);
-            }
-        }
-    }
-
-    // Drain: never leave a bulk copy in flight into shared memory.
-    if (tid == 0) {
-        for (int64_t q = consumed; q < issued; ++q) {
-            if (!mbar_wait_bounded(&bars[q & 1], static_cast<uint32_t>((q >> 1) & 1), p.timeout_ns))
+            if (aborted)
                 record_error(p.err, NORM_ERR_TIMEOUT);
         }
-        if (aborted)
-            record_error(p.err, NORM_ERR_TIMEOUT);
+    } else {
+        // ------------------------------------------------ data warps 1..15
+        const int dt = tid - 32;
+        float4 v[LN_V]; // this thread's part of the slice of row r
+        for (int64_t r = -1; r < R; ++r) {
+            const int64_t nx = r + 1;
+            const uint64_t pol_gb = (r + 1 == R) ? pol_stream : pol_keep;
+            auto load_gb = [&](int bt, float4 *g, float4 *bb) {
+#pragma unroll
+                for (int j = 0; j < LN_GB; ++j) {
+                    const int i = dt + (bt * LN_GB + j) * LN_T;
+                    const bool in = i < n4;
+                    g[j] = (in && g4) ? ld_ro_f4(g4 + f0 + i, pol_gb) : make_float4(1.f, 1.f, 1.f, 1.f);
+                    bb[j] = (in && b4) ? ld_ro_f4(b4 + f0 + i, pol_gb) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            };
+            // gamma/beta batches of row r, two in flight (double buffer)
+            float4 gA[LN_GB], bA[LN_GB], gB[LN_GB], bB[LN_GB];
+            if (r >= 0)
+                load_gb(0, gA, bA);
+
+            // 1. triple of row nx from its shared-memory buffer, about the
+            //    row's pivot K
+            bool fail = false;
+            const float K = (nx < R) ? pivot[nx & 1] : 0.f; // set by warp 0 a row ahead
+            if (nx < R) {
+                const float4 *buf = ln_smem + (nx & 1) * buf_f4;
+                if (!mbar_wait_bounded(&bar_x[nx & 1], static_cast<uint32_t>((nx >> 1) & 1), p.timeout_ns)) {
+                    fail = true;
+                } else {
+                    // one pass over shared memory: shifted sums of d = x - K
+                    float s1 = 0.f, s2 = 0.f;
+                    int cnt = 0;
+#pragma unroll
+                    for (int k = 0; k < LN_V; ++k) {
+                        const int i = dt + k * LN_T;
+                        if (i < n4) {
+                            const float4 q = buf[i];
+                            const float a = q.x - K, bq = q.y - K, c = q.z - K, d = q.w - K;
+                            s1 += (a + bq) + (c + d);
+                            s2 = fmaf(a, a, fmaf(bq, bq, fmaf(c, c, fmaf(d, d, s2))));
+                            cnt += 4;
+                        }
+                    }
+                    Moments m = {0.f, 0.f, 0.f};
+                    if (cnt > 0) {
+                        m.n = static_cast<float>(cnt);
+                        m.mean = s1 / m.n;
+                        m.m2 = fmaxf(fmaf(-s1, m.mean, s2), 0.f);
+                    }
+                    m = warp_merge(m);
+                    if (lane == 0)
+                        red[warp - 1] = m;
+                }
+            }
+            if (r >= 0)
+                load_gb(1, gB, bB);
+            if (__syncthreads_or(fail ? 1 : 0)) { // 1
+                aborted = true;
+                break;
+            }
+
+            // 2. y of row r from registers; gamma/beta two batches deep
+            if (r >= 0) {
+                const RowMean rm = row_mean;
+                float4 *yr = y4 + r * L4 + f0;
+                auto write_batch = [&](int bt, const float4 *g, const float4 *bb) {
+#pragma unroll
+                    for (int j = 0; j < LN_GB; ++j) {
+                        const int k = bt * LN_GB + j;
+                        const int i = dt + k * LN_T;
+                        if (i < n4)
+                            st_stream_f4(yr + i, ln_apply4(v[k], rm, g[j], bb[j]), pol_stream);
+                    }
+                };
+                // batches alternate between the A and B registers (the branch on
+                // bt's parity is resolved at compile time)
+#pragma unroll
+                for (int bt = 0; bt < LN_NB; ++bt) {
+                    if ((bt & 1) == 0) {
+                        write_batch(bt, gA, bA);
+                        if (bt + 2 < LN_NB)
+                            load_gb(bt + 2, gA, bA);
+                    } else {
+                        write_batch(bt, gB, bB);
+                        if (bt + 2 < LN_NB)
+                            load_gb(bt + 2, gB, bB);
+                    }
+                }
+            }
+            // row nx moves into registers
+            if (nx < R) {
+                const float4 *buf = ln_smem + (nx & 1) * buf_f4;
+#pragma unroll
+                for (int k = 0; k < LN_V; ++k) {
+                    const int i = dt + k * LN_T;
+                    v[k] = (i < n4) ? buf[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            __syncthreads(); // 2
+        }
     }
 }
 
@@ -399,7 +581,7 @@ __global__ void __launch_bounds__(LS_T) ln_split_apply_kernel(LnParams p)
 
 LnPersistentConfig ln_persistent_config()
 {
-    return LnPersistentConfig{LN_T, LN_V};
+    return LnPersistentConfig{LN_THREADS, LN_T, LN_V, LN_SLOTS * 16, LN_MAX_GRID};
 }
 
 cudaError_t ln_persistent_setup(int max_dynamic_smem)
@@ -410,7 +592,7 @@ cudaError_t ln_persistent_setup(int max_dynamic_smem)
 
 cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, ln_persistent_kernel, LN_T, dyn_smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, ln_persistent_kernel, LN_THREADS, dyn_smem);
 }
 
 cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream)
@@ -418,7 +600,7 @@ cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cuda
     LnParams args = p;
     void *kargs[] = {&args};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ln_persistent_kernel), dim3(grid),
-                                       dim3(LN_T), kargs, static_cast<size_t>(dyn_smem), stream);
+                                       dim3(LN_THREADS), kargs, static_cast<size_t>(dyn_smem), stream);
 }
 
 cudaError_t ln_split_launch(const LnParams &p, bool vec4, cudaStream_t stream)

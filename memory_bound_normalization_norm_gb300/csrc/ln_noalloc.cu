@@ -63,10 +63,10 @@ extern "C" norm_status_t norm_layer_fwd_noalloc(const float *x, const float *gam
     norm_status_t st = scratch_address(&scratch);
     if (st != NORM_OK)
         return st;
-    // The array keeps whatever the previous call left in it; the barrier
-    // header must start at zero.  (The partial statistics are always written
-    // before they are read.)
-    if (cudaMemsetAsync(scratch, 0, sizeof(normk::LnSync), stream) != cudaSuccess) {
+    // The array keeps whatever the previous call left in it (including the
+    // state of a call that gave up waiting): start from zeros, as from a
+    // fresh workspace, over every byte this shape uses.
+    if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
     }

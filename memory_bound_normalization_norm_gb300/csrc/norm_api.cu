@@ -120,8 +120,8 @@ bool safe_mul(int64_t a, int64_t b, int64_t *out)
 struct LnPlan {
     int path = 0; // 1 persistent, 2 split
     int grid = 0;
-    int dyn_smem = 0;
     int max_n4 = 0;
+    int dyn_smem = 0;
     int parts = 0;
     int64_t chunk = 0;
     bool vec4 = false;
@@ -148,30 +148,61 @@ void plan_split(int64_t rows, int64_t L, bool vec4, const DeviceState &d, LnPlan
     pl->ws_bytes = kWsHeader + static_cast<size_t>(rows) * static_cast<size_t>(P) * 16u;
 }
 
-// Fills the persistent plan if the shape fits on chip; returns false if not.
-bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
+// CTAs of the persistent kernel on this device.
+int persistent_grid(const DeviceState &d)
 {
-    (void)rows;
-    if (!d.coop || d.ln_ctas_per_sm < 1 || (L & 3) != 0)
-        return false;
     const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
     int grid = d.sm_count * d.ln_ctas_per_sm;
     const int64_t want = g_opt_ln_ctas.load();
     if (want > 0 && want < grid)
         grid = static_cast<int>(want);
+    if (grid > cfg.max_grid)
+        grid = cfg.max_grid;
+    return grid;
+}
+
+// Largest per-CTA slice (float4) the persistent kernel holds: the data
+// threads' share, and two row buffers in dynamic shared memory.
+int64_t persistent_max_slice(const DeviceState &d)
+{
+    const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
+    int64_t m = int64_t(cfg.data_threads) * cfg.v4_per_thread;
+    const int64_t by_smem = (d.ln_max_dyn_smem / 32) / 8 * 8; // two buffers, 128-byte rounded
+    return m < by_smem ? m : by_smem;
+}
+
+// Longest row the persistent kernel serves with one HBM read of x: every
+// CTA's slice fits its shared-memory buffers, and the kernel partitions rows
+// with 32-bit arithmetic (row_len/4 * (grid + 1) < 2^32).
+int64_t persistent_max_row_len(const DeviceState &d)
+{
+    if (!d.coop || d.ln_ctas_per_sm < 1)
+        return 0;
+    const int grid = persistent_grid(d);
+    const int64_t by_slice = persistent_max_slice(d) * grid * 4;
+    const int64_t by_index = ((int64_t(1) << 32) - 1) / (grid + 1) * 4;
+    const int64_t m = by_slice < by_index ? by_slice : by_index;
+    return m & ~int64_t(3);
+}
+
+// Fills the persistent plan if the shape qualifies; returns false if not.
+bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
+{
+    (void)rows;
+    if ((L & 3) != 0 || L > persistent_max_row_len(d))
+        return false;
+    const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
+    const int grid = persistent_grid(d);
     const int64_t L4 = L / 4;
-    const int64_t max_n4 = (L4 + grid - 1) / grid;
-    if (max_n4 > int64_t(cfg.threads) * cfg.v4_per_thread)
-        return false;
-    const int64_t smem = 2 * max_n4 * 16;
-    if (smem > d.ln_max_dyn_smem)
-        return false;
+    int64_t max_n4 = (L4 + grid - 1) / grid;
+    if (max_n4 < 1)
+        max_n4 = 1;
     pl->path = 1;
     pl->vec4 = true;
     pl->grid = grid;
-    pl->max_n4 = static_cast<int>(max_n4 < 1 ? 1 : max_n4);
-    pl->dyn_smem = static_cast<int>(2 * int64_t(pl->max_n4) * 16);
-    pl->ws_bytes = kWsHeader + 2u * static_cast<size_t>(grid) * 16u;
+    pl->max_n4 = static_cast<int>(max_n4);
+    pl->dyn_smem = static_cast<int>(2 * ((max_n4 + 7) / 8 * 8) * 16);
+    pl->ws_bytes = kWsHeader + static_cast<size_t>(cfg.record_bytes_per_cta) * static_cast<size_t>(grid);
     return true;
 }
 
@@ -249,14 +280,9 @@ size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len)
 int64_t norm_layer_max_resident_row_len(void)
 {
     DeviceState *d = nullptr;
-    if (device_state(&d) != NORM_OK || !d->coop || d->ln_ctas_per_sm < 1)
+    if (device_state(&d) != NORM_OK)
         return 0;
-    const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
-    int64_t per_cta = int64_t(cfg.threads) * cfg.v4_per_thread;
-    const int64_t by_smem = d->ln_max_dyn_smem / 32;
-    if (by_smem < per_cta)
-        per_cta = by_smem;
-    return per_cta * 4 * d->sm_count * d->ln_ctas_per_sm;
+    return persistent_max_row_len(*d);
 }
 
 norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStream_t stream)
@@ -358,8 +384,8 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
     p.parts = pl.parts;
     cudaError_t e;
     if (persistent) {
+        p.tag_skew = static_cast<unsigned>(g_opt_extra_arrivals.load());
         p.max_n4 = pl.max_n4;
-        p.expected = static_cast<unsigned>(pl.grid) + static_cast<unsigned>(g_opt_extra_arrivals.load());
         e = normk::ln_persistent_launch(p, pl.grid, pl.dyn_smem, stream);
     } else {
         e = normk::ln_split_launch(p, pl.vec4, stream);

@@ -32,6 +32,13 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ uint64_t policy_evict_last()
 {
     uint64_t p;
@@ -106,6 +113,18 @@ __device__ __forceinline__ float4 ld_l2_f4(const float4 *p)
     return v;
 }
 
+// 128-bit shared-memory load that the compiler may neither drop nor merge
+// with another load of the same address.
+__device__ __forceinline__ float4 ld_shared_f4(const float4 *p)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(smem_u32(p))
+                 : "memory");
+    return v;
+}
+
 // ---- mbarrier + bulk copy (TMA engine, non-tensor form)
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
@@ -129,12 +148,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -166,6 +204,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Prefetch global memory into L2 (bulk, no destination); src and bytes must
+// be 16-byte multiples.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- gpu-scope synchronization primitives
 
 __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v)
@@ -183,6 +228,41 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
 }
 
 __device__ __forceinline__ void st_relaxed_gpu(unsigned *p, unsigned v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// 64-bit load from L2 (bypassing L1) that the compiler may not merge or drop,
+// and that the hardware may overlap with other loads (unlike ld.relaxed.gpu,
+// whose loads were measured to complete one after another).  A naturally
+// aligned 8-byte word written by one 64-bit store is read whole.
+__device__ __forceinline__ unsigned long long ld_cg_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.global.cg.b64 %0, [%1];" : "=l"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_gpu_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u32(unsigned *p, unsigned v)
 {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -250,12 +330,12 @@ __device__ __forceinline__ Moments warp_merge(Moments a)
 
 // ---------------------------------------------------------------- launchers
 
-// Workspace header of the LayerNorm kernels (256 bytes, zeroed by the caller
-// before first use; the kernels leave it zeroed, except after a timeout).
+// Workspace header of the LayerNorm kernels (256 bytes).  The caller zeroes
+// the whole workspace before first use and after a timeout; between those,
+// the persistent kernel keeps it consistent from call to call.
 struct LnSync {
-    unsigned count[2]; // arrivals at the grid barrier of slot 0 / 1
-    unsigned gen[2];   // generation of slot 0 / 1 (bumped when all arrived)
-    unsigned pad[60];
+    unsigned row_base; // rows the persistent kernel has processed on this workspace (mod 2^32)
+    unsigned pad[63];
 };
 static_assert(sizeof(LnSync) == 256, "LnSync must be 256 bytes");
 
@@ -268,19 +348,22 @@ struct LnParams {
     int64_t row_len; // elements
     float eps;
     LnSync *sync;
-    float4 *part; // partials: persistent [2][grid], split [rows][P]
+    float4 *part; // persistent: tagged records [slots][grid][3] (u64); split: partials [rows][P]
     unsigned *err;
     uint64_t timeout_ns;
-    unsigned expected; // arrivals the grid barrier waits for
-    int max_n4;        // persistent: float4 capacity of each smem buffer
+    unsigned tag_skew; // test hook: 0, or an offset that makes the grid barrier unreachable
+    int max_n4;        // float4 capacity of each shared-memory row buffer
     int64_t chunk;     // split: elements per CTA (multiple of 4 on the vector path)
     int parts;         // split: CTAs per row (P)
 };
 
 // Persistent single-read LayerNorm (one CTA per SM, cooperative launch).
 struct LnPersistentConfig {
-    int threads;     // CTA size
-    int v4_per_thread;
+    int threads;              // CTA size
+    int data_threads;         // threads that own the row slice
+    int v4_per_thread;        // float4 of the slice per data thread
+    int record_bytes_per_cta; // workspace bytes of barrier records per CTA
+    int max_grid;             // most CTAs the kernel supports
 };
 LnPersistentConfig ln_persistent_config();
 // Max dynamic shared memory the kernel may use; called once per device.
