@@ -188,8 +188,9 @@ const char *norm_status_string(norm_status_t status);
  *                                fit), 2 = force the two-kernel path.
  *   NORM_OPT_BARRIER_TIMEOUT_NS  how long a CTA waits at the LayerNorm grid
  *                                barrier (or for its own bulk copies) before
- *                                it records NORM_ERR_TIMEOUT and returns
- *                                without writing y.  Default 200 ms.
+ *                                it records NORM_ERR_TIMEOUT and stops; rows
+ *                                whose statistics were not merged are not
+ *                                written.  Default 200 ms.
  *   NORM_OPT_BARRIER_EXTRA_ARRIVALS  test hook: when > 0, the grid barrier
  *                                waits for partial statistics that no CTA
  *                                publishes, so it can only end by timing

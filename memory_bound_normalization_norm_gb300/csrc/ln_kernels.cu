@@ -22,32 +22,36 @@
 // co-resident).  CTA c owns the same float4 column slice of every row.  Row
 // slices arrive by bulk copy (TMA engine, 32 KB pieces) into two
 // shared-memory buffers, two rows ahead; the slice of the row being written
-// lives in registers.  x is read from HBM once and stays on chip until y is
-// written.  Warp 0 coordinates (bulk copies, grid barrier, merge); warps
-// 1..15 own the data.  Iteration r:
-//   1. warps 1..15 reduce the two-pass triples of row r+1 from its buffer
-//      and start loading their first gamma/beta batch of row r, while warp 0
-//      waits for and merges the triples of row r, published one iteration
-//      earlier, so the grid-wide wait is normally over when warp 0 looks;
-//   2. warp 0 publishes row r+1's triple; warps 1..15 write y of row r from
-//      registers, streaming gamma/beta through L2 (evict-last, so they come
-//      from HBM once per launch) two batches deep, then move row r+1 from its
-//      buffer into registers;
-//   3. warp 0 refills the buffer with the bulk copy of row r+3.
+// lives in registers, and gamma/beta of the slice live in tensor memory
+// (TMEM), loaded once per launch.  x is read from HBM once and stays on chip
+// until y is written; gamma and beta are read from HBM once.  Warp 0
+// coordinates the grid barrier; warps 1..15 own the data (warp 1 also issues
+// the bulk copies).  Iteration r:
+//   1. warps 1..15 reduce the triples of row r+1 from its buffer; barrier 1
+//      (block-wide) also checks that warp 0 has merged row r;
+//   2. warp 0 publishes the CTA's triple of row r+1, then, without waiting
+//      for the data warps again, polls and merges row r+1 until the next
+//      barrier 1, so the grid-wide exchange has a whole iteration to finish;
+//   3. warps 1..15 write y of row r from registers and TMEM, move row r+1
+//      from its buffer into registers, and warp 1 refills the buffer with
+//      the bulk copy of row r+3.
+// The pivot's three candidate elements travel with each row's bulk copy.
 //
 // Grid barrier without atomics.  Each CTA publishes its (mean, M2) as two
-// 64-bit words, each carrying a 32-bit tag in its high half, written with
-// st.relaxed.gpu (single-copy atomic).  Warp 0 polls the G records of the row
-// with plain L2 loads (ld.global.cg, which overlap) until every tag matches,
-// so the barrier and its data arrive in the same round trip.  Records sit in 4 rotating slots.  Tags count rows: row r
-// of a launch is tagged row_base + r + 1, where row_base (workspace header)
-// is the number of rows the persistent kernel has already processed on this
-// workspace.  A slot therefore only ever holds tags smaller than the one
-// awaited, and a zeroed workspace holds tag 0, which is never awaited.
-// row_base is read at kernel start and advanced by CTA 0 after its last
-// merge, which proves every CTA has read it.  Every wait is bounded by
-// %globaltimer: on timeout a CTA records NORM_ERR_TIMEOUT, drains its own bulk
-// copies and returns without writing y.
+// 64-bit words, each carrying a 32-bit tag in its high half.  Both the
+// record and the polls go through the bulk-copy unit (a 16-byte bulk store;
+// one bulk load of all G records per attempt): plain loads and stores would
+// queue behind the SM's own y stores, which drain at HBM speed.  The barrier
+// and its data arrive in the same round trip.  Records sit in 4 rotating
+// slots.  Tags count rows: row r of a launch is tagged row_base + r + 1,
+// where row_base (workspace header) is the number of rows the persistent
+// kernel has already processed on this workspace.  A slot therefore only
+// ever holds tags smaller than the one awaited, and a zeroed workspace holds
+// tag 0, which is never awaited.  row_base is read at kernel start and
+// advanced by CTA 0 after its last merge, which proves every CTA has read
+// it.  Every wait is bounded by %globaltimer: on timeout a CTA records
+// NORM_ERR_TIMEOUT, drains its own bulk copies, frees its TMEM and returns
+// without writing the remaining rows of y.
 //
 // Split path (any shape): kernel 1 writes one triple per (row, chunk) CTA;
 // kernel 2 merges the row's triples and applies, re-reading x.
@@ -62,12 +66,19 @@ constexpr int LN_DATA_WARPS = 15;
 constexpr int LN_T = 32 * LN_DATA_WARPS;  // data threads
 constexpr int LN_THREADS = LN_T + 32;     // CTA size
 constexpr int LN_V = 15;                  // float4 of the slice per data thread
-constexpr int LN_GB = 3;                  // gamma/beta float4 per load batch
+constexpr int LN_GB = 3;                  // gamma/beta float4 per TMEM load batch
 constexpr int LN_NB = LN_V / LN_GB;       // batches per row
+constexpr uint32_t LN_TMEM_COLS = 512;    // TMEM columns the CTA allocates (all)
+constexpr int LN_TM_COLS = 8 * LN_V;      // TMEM columns of one data thread: gamma, beta
+constexpr uint32_t LN_TM_BETA = 4 * LN_V; // column offset of beta within them
 constexpr int LN_SLOTS = 4;               // partial-record slots: reused 4 rows later
 constexpr int LN_MAX_GRID = 160;          // CTAs whose records one warp loads at once
 constexpr uint32_t LN_BULK_CHUNK = 32768;
 static_assert(LN_V % LN_GB == 0, "whole gamma/beta batches");
+// warps 1..15 sit in TMEM quarters by warp % 4 and take column ranges by
+// warp / 4, so at most four of them share a quarter
+static_assert(4 * LN_TM_COLS <= static_cast<int>(LN_TMEM_COLS), "gamma/beta of a quarter fit TMEM");
+static_assert(LN_DATA_WARPS + 1 <= 16, "warp / 4 < 4");
 
 struct RowMean {
     float hi, lo, rstd;
@@ -111,18 +122,6 @@ __device__ __forceinline__ float4 ln_apply4(float4 v, const RowMean &rm, float4 
     o.z = fmaf(((v.z - rm.hi) - rm.lo) * rm.rstd, g.z, b.z);
     o.w = fmaf(((v.w - rm.hi) - rm.lo) * rm.rstd, g.w, b.w);
     return o;
-}
-
-// Two-pass triple of the 4 values of q shifted by K.
-__device__ __forceinline__ Moments quad_moments(float4 q, float K)
-{
-    const float a = q.x - K, b = q.y - K, c = q.z - K, d = q.w - K;
-    Moments m;
-    m.n = 4.f;
-    m.mean = ((a + b) + (c + d)) * 0.25f;
-    const float da = a - m.mean, db = b - m.mean, dc = c - m.mean, dd = d - m.mean;
-    m.m2 = (da * da + db * db) + (dc * dc + dd * dd);
-    return m;
 }
 
 // CTA-wide fold of per-thread triples; the result is valid in thread 0.
@@ -172,15 +171,65 @@ struct GridMerge {
     bool ok;
 };
 
-// Warp 0: poll the G <= LN_MAX_GRID records (mean, M2 of x - K, all about
-// the row's one pivot K) of a row until every tag equals `tag` (bounded),
-// then merge them with the two-pass formula over partials:
+// Merge a row's G <= LN_MAX_GRID records (mean, M2 of x - K, all about the
+// row's one pivot K), held by warp 0 as w[j][0..1] for CTA lane + 32 j, with
+// the two-pass formula over partials:
 //   delta = sum_c n_c m_c / N,   M2 = sum_c M2_c + sum_c n_c (m_c - delta)^2,
-// with each count n_c known from the partition (q or q + 1 float4).  The
+// with each count n_c known from the partition (q4 or q4 + 1 float4).  The
 // sums are warp reductions in a fixed order, so every CTA computes the same
-// bits; the result is valid in lane 0.
-__device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *rec, int G, unsigned q4,
-                                                    unsigned rem, unsigned tag, uint64_t timeout_ns)
+// bits; all lanes return the result.
+__device__ __forceinline__ Moments merge_records(const unsigned long long (&w)[LN_MAX_GRID / 32][2], int G,
+                                                 unsigned q4, unsigned rem)
+{
+    constexpr int J = LN_MAX_GRID / 32;
+    const int lane = threadIdx.x & 31;
+    const float N = 4.f * (static_cast<float>(q4) * static_cast<float>(G) + static_cast<float>(rem));
+    float sm = 0.f; // sum of n_c * m_c
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int i = lane + 32 * j;
+        if (i < G) {
+            const float n = 4.f * static_cast<float>(q4 + (static_cast<unsigned>(i) < rem ? 1u : 0u));
+            sm = fmaf(n, record_value(w[j][0]), sm);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    const float delta = __shfl_sync(0xffffffffu, sm, 0) / N;
+    float sq = 0.f; // sum of M2_c + n_c (m_c - delta)^2
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int i = lane + 32 * j;
+        if (i < G) {
+            const float n = 4.f * static_cast<float>(q4 + (static_cast<unsigned>(i) < rem ? 1u : 0u));
+            const float dm = record_value(w[j][0]) - delta;
+            sq += fmaf(n * dm, dm, record_value(w[j][1]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    Moments t;
+    t.n = N;
+    t.mean = delta;
+    t.m2 = __shfl_sync(0xffffffffu, sq, 0);
+    return t;
+}
+
+// Warp 0: read the G records of a row until every tag equals `tag`
+// (bounded by timeout_ns), then merge them.
+//
+// BULK = false: plain L2 loads (ld.global.cg), which overlap.  BULK = true:
+// one bulk copy (TMA unit) of all records into rec_s per attempt, completed
+// on `bar`; `phase` is the parity of bar's next completion and `inflight`
+// tells the caller that a copy into rec_s may still be running after a
+// timeout, which it must drain before exit.
+template <bool BULK>
+__device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *rec, unsigned long long *rec_s,
+                                                    uint64_t *bar, uint32_t &phase, bool &inflight, int G,
+                                                    unsigned q4, unsigned rem, unsigned tag, uint64_t timeout_ns,
+                                                    uint64_t pol)
 {
     constexpr int J = LN_MAX_GRID / 32;
     const int lane = threadIdx.x & 31;
@@ -188,6 +237,27 @@ __device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *re
     g.ok = true;
     uint64_t t0 = 0;
     for (int attempt = 0;; ++attempt) {
+        if (BULK) {
+            int landed = 0;
+            if (lane == 0) {
+                // the warp's reads of the previous attempt precede the copy
+                fence_proxy_async_smem();
+                const uint32_t bytes = static_cast<uint32_t>(G) * 16u;
+                mbar_arrive_expect_tx(bar, bytes);
+                bulk_g2s(rec_s, rec, bytes, bar, pol);
+                inflight = true;
+                landed = mbar_wait_bounded(bar, phase, timeout_ns) ? 1 : 0;
+                if (landed) {
+                    inflight = false;
+                    phase ^= 1u;
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, landed, 0)) {
+                g.ok = false;
+                return g;
+            }
+            __syncwarp();
+        }
         // the words live only inside one attempt, so they stay in registers
         unsigned long long w[J][2];
         unsigned bad = 0;
@@ -197,41 +267,12 @@ __device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *re
             const int i = min(lane + 32 * j, G - 1);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                w[j][e] = ld_cg_u64(rec + 2 * i + e);
+                w[j][e] = BULK ? rec_s[2 * i + e] : ld_cg_u64(rec + 2 * i + e);
                 bad |= record_tag(w[j][e]) ^ tag;
             }
         }
         if (__all_sync(0xffffffffu, bad == 0)) {
-            const float N = 4.f * (static_cast<float>(q4) * static_cast<float>(G) + static_cast<float>(rem));
-            float sm = 0.f; // sum of n_c * m_c
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int i = lane + 32 * j;
-                if (i < G) {
-                    const float n = 4.f * static_cast<float>(q4 + (static_cast<unsigned>(i) < rem ? 1u : 0u));
-                    sm = fmaf(n, record_value(w[j][0]), sm);
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                sm += __shfl_xor_sync(0xffffffffu, sm, o);
-            const float delta = __shfl_sync(0xffffffffu, sm, 0) / N;
-            float sq = 0.f; // sum of M2_c + n_c (m_c - delta)^2
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int i = lane + 32 * j;
-                if (i < G) {
-                    const float n = 4.f * static_cast<float>(q4 + (static_cast<unsigned>(i) < rem ? 1u : 0u));
-                    const float dm = record_value(w[j][0]) - delta;
-                    sq += fmaf(n * dm, dm, record_value(w[j][1]));
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            g.tot.n = N;
-            g.tot.mean = delta;
-            g.tot.m2 = __shfl_sync(0xffffffffu, sq, 0);
+            g.tot = merge_records(w, G, q4, rem);
             return g;
         }
         if (attempt == 0)
@@ -240,28 +281,52 @@ __device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *re
             g.ok = false;
             return g;
         }
-        __nanosleep(20);
+        if (BULK)
+            __syncwarp();
+        else
+            __nanosleep(20);
     }
 }
 
-// Pivot of row q: the median of its first, middle and last elements.  A
+// Pivot of a row: the median of its first, middle and last elements.  A
 // pivot inside the bulk of the row keeps the shifted sums small, and one
-// outlier cannot become the pivot.
-__device__ __forceinline__ float row_pivot(const float *x, int64_t q, int64_t row_len)
+// outlier cannot become the pivot.  The three elements arrive by bulk copy
+// with the row, each in the 16-byte piece that contains it (row_len is a
+// multiple of 4, so element i sits at float i % 4 of piece i / 4).
+__device__ __forceinline__ float row_pivot(const float4 *piece, int64_t row_len)
 {
-    const float *xr = x + q * row_len;
-    const float a = ld_plain_f1(xr), b = ld_plain_f1(xr + (row_len >> 1)), c = ld_plain_f1(xr + (row_len - 1));
+    const int64_t mid = row_len >> 1;
+    const float a = piece[0].x;
+    const float4 pm = piece[1], pl = piece[2];
+    const int jm = static_cast<int>(mid & 3);
+    const float b = jm == 0 ? pm.x : jm == 1 ? pm.y : jm == 2 ? pm.z : pm.w;
+    const float c = pl.w; // row_len - 1 is float 3 of its piece
     return fmaxf(fminf(a, b), fminf(fmaxf(a, b), c));
 }
+
+#ifndef LN_BULK_BARRIER
+#define LN_BULK_BARRIER 1
+#endif
+// How the grid barrier's records travel: plain loads and stores (0) or bulk
+// copies (1).
+constexpr bool LN_BULK_RECORDS = LN_BULK_BARRIER != 0;
+
+// Named barriers of the persistent kernel (0 is __syncthreads).
+constexpr int LN_BAR_PUBLISHED = 1; // warp 0 has issued the row's record
+constexpr int LN_BAR_ROW_DONE = 2;  // y of row r written, row r+1 in registers
 
 __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p)
 {
     extern __shared__ __align__(128) float4 ln_smem[];
     __shared__ __align__(8) uint64_t bar_x[2];
     __shared__ Moments red[LN_DATA_WARPS];
-    __shared__ float pivot[2]; // the pivot K of a row, by row parity
-    __shared__ RowMean row_mean;
+    __shared__ float4 piv_in[2][3]; // pieces holding a row's pivot candidates, by row parity
+    __shared__ RowMean row_mean[2]; // merged statistics of a row, by row parity
     __shared__ unsigned row_base_s;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ __align__(8) uint64_t bar_rec;                             // record fetches (bulk)
+    __shared__ __align__(16) unsigned long long rec_in[LN_BULK_RECORDS ? 2 * LN_MAX_GRID : 2];
+    __shared__ __align__(16) unsigned long long rec_out[2];               // this CTA's record (bulk)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -280,72 +345,40 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     const int buf_f4 = (p.max_n4 + 7) & ~7;
 
     const uint64_t pol_stream = policy_evict_first();
-    const uint64_t pol_keep = policy_evict_last();
 
+    // The CTA holds all 512 TMEM columns (it is alone on its SM: its 512
+    // threads at 128 registers take the whole register file).
+    if (warp == 0)
+        tmem_alloc(&tmem_base_s, LN_TMEM_COLS);
     if (tid == 0) {
         mbar_init(&bar_x[0], 1);
         mbar_init(&bar_x[1], 1);
+        mbar_init(&bar_rec, 1);
         fence_mbar_init();
         fence_proxy_async_smem();
         row_base_s = ld_relaxed_gpu_u32(&p.sync->row_base);
-        if (R > 0)
-            pivot[0] = row_pivot(p.x, 0, p.row_len);
     }
+    tmem_fence_before_sync();
     __syncthreads();
+    tmem_fence_after_sync();
     const unsigned row_base = row_base_s;
+    const uint32_t tmem_base = tmem_base_s;
     bool aborted = false;
 
-    // Warp 0 and warps 1..15 run separate loops with the same two block-wide
-    // barriers per iteration, so each role keeps only its own state in
-    // registers.  Abort decisions are block-wide votes (__syncthreads_or).
+    // Warp 0 and warps 1..15 run separate loops.  Per iteration r both pass
+    // the block-wide barrier 1 (__syncthreads_or: abort vote; the triples of
+    // row r+1 are reduced and row r is merged) and the named barriers
+    // LN_BAR_PUBLISHED and LN_BAR_ROW_DONE, at which warp 0 only arrives: it
+    // goes on merging row r+1 until the next barrier 1.
     if (warp == 0) {
         // ------------------------------------------------ coordinator
-        // Lane 0 tracks the bulk copies it issued (rows < issued) and those
-        // whose completion it observed (rows < waited), so that an early exit
-        // can drain them.
-        int64_t issued = 0, waited = 0;
-        auto issue_x = [&](int64_t q) {
-            uint64_t *bar = &bar_x[q & 1];
-            const uint32_t bytes = static_cast<uint32_t>(n4) * 16u;
-            mbar_arrive_expect_tx(bar, bytes);
-            const float4 *src = x4 + q * L4 + f0;
-            float4 *dst = ln_smem + (q & 1) * buf_f4;
-            for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
-                bulk_g2s(dst + off / 16, src + off / 16,
-                         (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, bar, pol_stream);
-        };
-        if (lane == 0) {
-            issue_x(0);
-            issued = 1;
-            if (R > 1) {
-                issue_x(1);
-                issued = 2;
-            }
-        }
+        uint32_t rec_phase = 0;    // parity of bar_rec's next completion
+        bool rec_inflight = false; // a record fetch may still be writing rec_in
+        const uint64_t pol_rec = policy_evict_last();
+        bool fail = false;         // the merge of the previous row gave up
         for (int64_t r = -1; r < R; ++r) {
             const int64_t nx = r + 1;
-            bool fail = false;
-            if (r >= 0) {
-                const GridMerge gm = poll_and_merge(records + static_cast<int64_t>(r % LN_SLOTS) * G * 2, G, q4,
-                                                    rem, row_tag(row_base, r) + p.tag_skew, p.timeout_ns);
-                if (!gm.ok) {
-                    fail = true;
-                    if (lane == 0)
-                        record_error(p.err, NORM_ERR_TIMEOUT);
-                } else if (lane == 0) {
-                    row_mean = finish_row(pivot[r & 1], gm.tot, p.eps);
-                    // every CTA has read row_base once CTA 0 has merged the last row
-                    if (r + 1 == R && cta == 0)
-                        st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(R));
-                }
-            }
-            if (nx < R && lane == 0) {
-                if (mbar_wait_bounded(&bar_x[nx & 1], static_cast<uint32_t>((nx >> 1) & 1), p.timeout_ns))
-                    waited = nx + 1;
-                else
-                    fail = true;
-            }
-            if (__syncthreads_or(fail ? 1 : 0)) { // 1: triples of row nx reduced, row r merged
+            if (__syncthreads_or(fail ? 1 : 0)) { // 1
                 aborted = true;
                 break;
             }
@@ -354,63 +387,110 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 if (lane < LN_DATA_WARPS)
                     c = red[lane];
                 c = warp_merge(c);
+                // read now: the bulk copy of row nx + 2, issued after
+                // LN_BAR_ROW_DONE, overwrites these pieces.  (The data warps
+                // saw row nx land before barrier 1; this wait returns at once
+                // and orders the read after the copy for this warp as well.)
+                fail = !mbar_wait_bounded(&bar_x[nx & 1], static_cast<uint32_t>((nx >> 1) & 1), p.timeout_ns);
+                const float K = row_pivot(piv_in[nx & 1], p.row_len);
+                const unsigned tag = row_tag(row_base, nx);
+                unsigned long long *slot = records + static_cast<int64_t>(nx % LN_SLOTS) * G * 2;
                 if (lane == 0) {
-                    const unsigned tag = row_tag(row_base, nx);
-                    unsigned long long *out = records + (static_cast<int64_t>(nx % LN_SLOTS) * G + cta) * 2;
-                    st_relaxed_gpu_u64(out + 0, tagged(tag, c.mean));
-                    st_relaxed_gpu_u64(out + 1, tagged(tag, c.m2));
+                    if (LN_BULK_RECORDS) {
+                        bulk_wait_read_all(); // the previous record has left rec_out
+                        rec_out[0] = tagged(tag, c.mean);
+                        rec_out[1] = tagged(tag, c.m2);
+                        fence_proxy_async_smem();
+                        bulk_s2g(slot + 2 * cta, rec_out, 16);
+                        bulk_commit();
+                    } else {
+                        st_relaxed_gpu_u64(slot + 2 * cta + 0, tagged(tag, c.mean));
+                        st_relaxed_gpu_u64(slot + 2 * cta + 1, tagged(tag, c.m2));
+                    }
                 }
-            }
-            // the pivot of row nx + 1 for the data warps' next iteration (its
-            // slot was last read for row nx - 1, which is merged already)
-            if (lane == 0 && nx + 1 < R)
-                pivot[(nx + 1) & 1] = row_pivot(p.x, nx + 1, p.row_len);
-            __syncthreads(); // 2: y of row r written, row nx moved out of its buffer
-            if (lane == 0 && nx + 2 < R) {
-                fence_proxy_async_smem();
-                issue_x(nx + 2);
-                issued = nx + 3;
+                __syncwarp();
+                bar_arrive_named(LN_BAR_PUBLISHED, LN_THREADS);
+                bar_arrive_named(LN_BAR_ROW_DONE, LN_THREADS);
+                // merge row nx while the data warps write row r and reduce
+                // row nx + 1; due at the next barrier 1
+                const GridMerge gm = poll_and_merge<LN_BULK_RECORDS>(slot, rec_in, &bar_rec, rec_phase, rec_inflight,
+                                                                     G, q4, rem, tag + p.tag_skew, p.timeout_ns,
+                                                                     pol_rec);
+                if (!gm.ok || fail) {
+                    fail = true;
+                    if (lane == 0)
+                        record_error(p.err, NORM_ERR_TIMEOUT);
+                } else if (lane == 0) {
+                    row_mean[nx & 1] = finish_row(K, gm.tot, p.eps);
+                    // every CTA has read row_base once CTA 0 has merged the last row
+                    if (nx + 1 == R && cta == 0)
+                        st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(R));
+                }
+            } else {
+                bar_arrive_named(LN_BAR_PUBLISHED, LN_THREADS);
+                bar_arrive_named(LN_BAR_ROW_DONE, LN_THREADS);
             }
         }
-        // Drain: never leave a bulk copy in flight into shared memory.
         if (lane == 0) {
-            for (int64_t q = waited; q < issued; ++q) {
-                if (!mbar_wait_bounded(&bar_x[q & 1], static_cast<uint32_t>((q >> 1) & 1), p.timeout_ns))
-                    record_error(p.err, NORM_ERR_TIMEOUT);
-            }
+            // never leave a bulk copy in flight into or out of shared memory
+            if (rec_inflight && !mbar_wait_bounded(&bar_rec, rec_phase, p.timeout_ns))
+                record_error(p.err, NORM_ERR_TIMEOUT);
+            if (LN_BULK_RECORDS)
+                bulk_wait_all();
             if (aborted)
                 record_error(p.err, NORM_ERR_TIMEOUT);
         }
     } else {
         // ------------------------------------------------ data warps 1..15
         const int dt = tid - 32;
+        // Thread 32 (warp 1, lane 0) issues the bulk copies of x.  It tracks
+        // those it issued (rows < issued) and those whose completion it
+        // observed (rows < waited), so that an early exit can drain them.
+        const bool issuer = dt == 0;
+        int64_t issued = 0, waited = 0;
+        // Row q's slice, plus the three 16-byte pieces of the row that hold
+        // its pivot candidates, all on bar_x[q & 1].
+        auto issue_x = [&](int64_t q) {
+            uint64_t *bar = &bar_x[q & 1];
+            const uint32_t bytes = static_cast<uint32_t>(n4) * 16u;
+            mbar_arrive_expect_tx(bar, bytes + 48u);
+            const float4 *row = x4 + q * L4;
+            bulk_g2s(&piv_in[q & 1][0], row, 16u, bar, pol_stream);
+            bulk_g2s(&piv_in[q & 1][1], row + ((p.row_len >> 1) >> 2), 16u, bar, pol_stream);
+            bulk_g2s(&piv_in[q & 1][2], row + (L4 - 1), 16u, bar, pol_stream);
+            const float4 *src = row + f0;
+            float4 *dst = ln_smem + (q & 1) * buf_f4;
+            for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
+                bulk_g2s(dst + off / 16, src + off / 16,
+                         (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, bar, pol_stream);
+            issued = q + 1;
+        };
+        if (issuer) {
+            issue_x(0);
+            if (R > 1)
+                issue_x(1);
+        }
+        // This thread's TMEM cells: lane 32*(warp % 4) + lane of its warp's
+        // quarter, LN_TM_COLS columns from (warp / 4) * LN_TM_COLS: gamma of
+        // its k-th float4 at column 4k, beta at LN_TM_BETA + 4k.  The four
+        // (or three) data warps of a quarter take disjoint column ranges.
+        const uint32_t tm = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
+                            static_cast<uint32_t>((warp >> 2) * LN_TM_COLS);
         float4 v[LN_V]; // this thread's part of the slice of row r
         for (int64_t r = -1; r < R; ++r) {
             const int64_t nx = r + 1;
-            const uint64_t pol_gb = (r + 1 == R) ? pol_stream : pol_keep;
-            auto load_gb = [&](int bt, float4 *g, float4 *bb) {
-#pragma unroll
-                for (int j = 0; j < LN_GB; ++j) {
-                    const int i = dt + (bt * LN_GB + j) * LN_T;
-                    const bool in = i < n4;
-                    g[j] = (in && g4) ? ld_ro_f4(g4 + f0 + i, pol_gb) : make_float4(1.f, 1.f, 1.f, 1.f);
-                    bb[j] = (in && b4) ? ld_ro_f4(b4 + f0 + i, pol_gb) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            };
-            // gamma/beta batches of row r, two in flight (double buffer)
-            float4 gA[LN_GB], bA[LN_GB], gB[LN_GB], bB[LN_GB];
-            if (r >= 0)
-                load_gb(0, gA, bA);
 
             // 1. triple of row nx from its shared-memory buffer, about the
             //    row's pivot K
             bool fail = false;
-            const float K = (nx < R) ? pivot[nx & 1] : 0.f; // set by warp 0 a row ahead
             if (nx < R) {
                 const float4 *buf = ln_smem + (nx & 1) * buf_f4;
                 if (!mbar_wait_bounded(&bar_x[nx & 1], static_cast<uint32_t>((nx >> 1) & 1), p.timeout_ns)) {
                     fail = true;
                 } else {
+                    if (issuer)
+                        waited = nx + 1;
+                    const float K = row_pivot(piv_in[nx & 1], p.row_len);
                     // one pass over shared memory: shifted sums of d = x - K
                     float s1 = 0.f, s2 = 0.f;
                     int cnt = 0;
@@ -436,17 +516,58 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                         red[warp - 1] = m;
                 }
             }
-            if (r >= 0)
-                load_gb(1, gB, bB);
             if (__syncthreads_or(fail ? 1 : 0)) { // 1
                 aborted = true;
                 break;
             }
+            // the CTA's record of row nx goes out before this CTA's y stores
+            bar_sync_named(LN_BAR_PUBLISHED, LN_THREADS);
 
-            // 2. y of row r from registers; gamma/beta two batches deep
-            if (r >= 0) {
-                const RowMean rm = row_mean;
+            if (r < 0) {
+                // 2'. before the first row: gamma and beta of the slice go to
+                //     TMEM once, staged through v (free until row 0 arrives)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float4 *src = h == 0 ? g4 : b4;
+                    const float4 dflt = h == 0 ? make_float4(1.f, 1.f, 1.f, 1.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < LN_V; ++k) {
+                        const int i = dt + k * LN_T;
+                        v[k] = (src && i < n4) ? ld_stream_f4(src + f0 + i, pol_stream) : dflt;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < LN_V; ++k)
+                        tmem_st4(tm + static_cast<uint32_t>(h * LN_TM_BETA + 4 * k), v[k]);
+                    tmem_wait_st();
+                }
+            } else {
+                // 2. y of row r from registers, gamma/beta from TMEM, one
+                //    batch of LN_GB float4 loaded while the previous one is
+                //    written
+                const RowMean rm = row_mean[r & 1];
                 float4 *yr = y4 + r * L4 + f0;
+                float4 gA[LN_GB], bA[LN_GB], gB[LN_GB], bB[LN_GB];
+                // tcgen05 loads and waits are warp-collective: reconverge
+                // after the divergent stores first
+                auto load_gb = [&](int bt, float4 *g, float4 *bb) {
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < LN_GB; ++j) {
+                        const uint32_t c = static_cast<uint32_t>(4 * (bt * LN_GB + j));
+                        g[j] = tmem_ld4(tm + c);
+                        bb[j] = tmem_ld4(tm + LN_TM_BETA + c);
+                    }
+                };
+                auto pin_gb = [&](float4 *g, float4 *bb) {
+                    __syncwarp();
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < LN_GB; ++j) {
+                        tmem_pin(g[j]);
+                        tmem_pin(bb[j]);
+                    }
+                };
                 auto write_batch = [&](int bt, const float4 *g, const float4 *bb) {
 #pragma unroll
                     for (int j = 0; j < LN_GB; ++j) {
@@ -456,18 +577,24 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                             st_stream_f4(yr + i, ln_apply4(v[k], rm, g[j], bb[j]), pol_stream);
                     }
                 };
+                load_gb(0, gA, bA);
+                pin_gb(gA, bA);
                 // batches alternate between the A and B registers (the branch on
                 // bt's parity is resolved at compile time)
 #pragma unroll
                 for (int bt = 0; bt < LN_NB; ++bt) {
                     if ((bt & 1) == 0) {
+                        if (bt + 1 < LN_NB)
+                            load_gb(bt + 1, gB, bB);
                         write_batch(bt, gA, bA);
-                        if (bt + 2 < LN_NB)
-                            load_gb(bt + 2, gA, bA);
+                        if (bt + 1 < LN_NB)
+                            pin_gb(gB, bB);
                     } else {
+                        if (bt + 1 < LN_NB)
+                            load_gb(bt + 1, gA, bA);
                         write_batch(bt, gB, bB);
-                        if (bt + 2 < LN_NB)
-                            load_gb(bt + 2, gB, bB);
+                        if (bt + 1 < LN_NB)
+                            pin_gb(gA, bA);
                     }
                 }
             }
@@ -480,8 +607,28 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                     v[k] = (i < n4) ? buf[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-            __syncthreads(); // 2
+            __syncwarp();
+            bar_sync_named(LN_BAR_ROW_DONE, LN_THREADS);
+            // buffer nx & 1 and its pivot pieces are free: refill them
+            if (issuer && nx + 2 < R) {
+                fence_proxy_async_smem();
+                issue_x(nx + 2);
+            }
         }
+        // Drain: never leave a bulk copy in flight into shared memory.
+        if (issuer) {
+            for (int64_t q = waited; q < issued; ++q) {
+                if (!mbar_wait_bounded(&bar_x[q & 1], static_cast<uint32_t>((q >> 1) & 1), p.timeout_ns))
+                    record_error(p.err, NORM_ERR_TIMEOUT);
+            }
+        }
+    }
+    // Every TMEM access of every thread is complete before warp 0 frees it.
+    tmem_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tmem_fence_after_sync();
+        tmem_dealloc(tmem_base, LN_TMEM_COLS);
     }
 }
 
@@ -582,6 +729,15 @@ __global__ void __launch_bounds__(LS_T) ln_split_apply_kernel(LnParams p)
 LnPersistentConfig ln_persistent_config()
 {
     return LnPersistentConfig{LN_THREADS, LN_T, LN_V, LN_SLOTS * 16, LN_MAX_GRID};
+}
+
+cudaError_t ln_persistent_static_smem(int *bytes)
+{
+    cudaFuncAttributes a;
+    const cudaError_t e = cudaFuncGetAttributes(&a, ln_persistent_kernel);
+    if (e == cudaSuccess)
+        *bytes = static_cast<int>(a.sharedSizeBytes);
+    return e;
 }
 
 cudaError_t ln_persistent_setup(int max_dynamic_smem)

@@ -69,10 +69,14 @@ norm_status_t device_state(DeviceState **out)
             return NORM_ERR_CUDA;
         }
         s.err = static_cast<unsigned *>(err);
-        // The persistent kernel's static shared memory is small (barriers,
-        // reduction scratch); leave room for it under the opt-in limit.
-        s.ln_max_dyn_smem = s.smem_optin - 1024;
-        if (normk::ln_persistent_setup(s.ln_max_dyn_smem) != cudaSuccess ||
+        // Dynamic shared memory of the persistent kernel: what the opt-in
+        // limit leaves beside its static shared memory (barriers, reduction
+        // scratch, the fetched records).
+        int static_smem = 0;
+        s.ln_max_dyn_smem = 0;
+        if (normk::ln_persistent_static_smem(&static_smem) == cudaSuccess)
+            s.ln_max_dyn_smem = s.smem_optin - static_smem;
+        if (s.ln_max_dyn_smem <= 0 || normk::ln_persistent_setup(s.ln_max_dyn_smem) != cudaSuccess ||
             normk::ln_persistent_occupancy(s.ln_max_dyn_smem, &s.ln_ctas_per_sm) != cudaSuccess) {
             cudaGetLastError();
             s.ln_ctas_per_sm = 0;

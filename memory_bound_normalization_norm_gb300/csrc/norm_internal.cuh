@@ -204,11 +204,32 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// Prefetch global memory into L2 (bulk, no destination); src and bytes must
-// be 16-byte multiples.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+// Bulk copy this CTA's shared memory -> global, tracked by the issuing
+// thread's bulk async-groups (bulk_commit / bulk_wait_*).  dst, src and
+// bytes must be 16-byte multiples.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes)
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk group of this thread has finished reading
+// its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---- gpu-scope synchronization primitives
@@ -277,6 +298,90 @@ __device__ __forceinline__ void record_error(unsigned *err, unsigned code)
 {
     if (err)
         atomicCAS(err, 0u, code);
+}
+
+// Named CTA barriers (ids 1..15; id 0 is __syncthreads).  `count` threads,
+// a multiple of 32, take part; bar_arrive signals without waiting.
+__device__ __forceinline__ void bar_sync_named(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive_named(int id, int count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---------------------------------------------------------------- tensor memory
+// Tensor memory (TMEM) is a 128-lane x 512-column array of 32-bit cells per
+// SM.  An address is (lane << 16) | column.  A warp reaches only the 32
+// lanes of its quarter: lanes 32*(w % 4) .. 32*(w % 4) + 31 for warp w of
+// the CTA.  With the .32x32b shape, thread t of the warp moves the cells of
+// lane (address lane) + t, N consecutive columns.  The .sync.aligned forms
+// are executed by all 32 threads of the warp with the same address.
+
+// Allocate `ncols` columns (a power of two, 32..512) for this CTA; one full
+// warp executes it.  The TMEM address is written to *dst (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Free the columns again; executed by the warp that allocated them.
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Order tensor-memory operations around a thread barrier.
+__device__ __forceinline__ void tmem_fence_before_sync()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Store 4 columns of this thread's lane.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, float4 v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+                 "r"(__float_as_uint(v.w))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Load 4 columns of this thread's lane.  The registers are valid only after
+// tmem_wait_ld_pin() on them.
+__device__ __forceinline__ float4 tmem_ld4(uint32_t taddr)
+{
+    uint32_t a, b, c, d;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(taddr)
+                 : "memory");
+    return make_float4(__uint_as_float(a), __uint_as_float(b), __uint_as_float(c), __uint_as_float(d));
+}
+
+__device__ __forceinline__ void tmem_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// After tmem_wait_ld(): make every later use of v depend on the wait, so the
+// compiler cannot move a use of the loaded registers above it.
+__device__ __forceinline__ void tmem_pin(float4 &v)
+{
+    asm volatile("" : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w));
 }
 
 // ---------------------------------------------------------------- statistics
@@ -348,7 +453,7 @@ struct LnParams {
     int64_t row_len; // elements
     float eps;
     LnSync *sync;
-    float4 *part; // persistent: tagged records [slots][grid][3] (u64); split: partials [rows][P]
+    float4 *part; // persistent: tagged records [slots][grid][2] (u64); split: partials [rows][P]
     unsigned *err;
     uint64_t timeout_ns;
     unsigned tag_skew; // test hook: 0, or an offset that makes the grid barrier unreachable
@@ -367,6 +472,7 @@ struct LnPersistentConfig {
 };
 LnPersistentConfig ln_persistent_config();
 // Max dynamic shared memory the kernel may use; called once per device.
+cudaError_t ln_persistent_static_smem(int *bytes);
 cudaError_t ln_persistent_setup(int max_dynamic_smem);
 // Number of co-resident CTAs per SM for `dyn_smem` bytes.
 cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm);
