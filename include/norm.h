@@ -127,8 +127,8 @@ norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStre
 
 /* Longest row (in elements) that the single-read persistent LayerNorm kernel
  * serves on the current device: each CTA's slice of a row must fit its two
- * shared-memory row buffers and its threads' registers (7,200 float4 per CTA,
- * 4,377,600 elements on a 152-SM GB300).  0 if the device cannot run the
+ * shared-memory row buffers and its threads' registers (6,912 float4 per CTA,
+ * 4,202,496 elements on a 152-SM GB300).  0 if the device cannot run the
  * kernel. */
 int64_t norm_layer_max_resident_row_len(void);
 

@@ -21,37 +21,33 @@
 // Persistent path (one CTA per SM, cooperative launch so all CTAs are
 // co-resident).  CTA c owns the same float4 column slice of every row.  Row
 // slices arrive by bulk copy (TMA engine, 32 KB pieces) into two
-// shared-memory buffers, two rows ahead; the slice of the row being written
-// lives in registers, and gamma/beta of the slice live in tensor memory
-// (TMEM), loaded once per launch.  x is read from HBM once and stays on chip
-// until y is written; gamma and beta are read from HBM once.  Warp 0
-// coordinates the grid barrier; warps 1..15 own the data (warp 1 also issues
-// the bulk copies).  Iteration r:
-//   1. warps 1..15 reduce the triples of row r+1 from its buffer; barrier 1
-//      (block-wide) also checks that warp 0 has merged row r;
-//   2. warp 0 publishes the CTA's triple of row r+1, then, without waiting
-//      for the data warps again, polls and merges row r+1 until the next
-//      barrier 1, so the grid-wide exchange has a whole iteration to finish;
-//   3. warps 1..15 write y of row r from registers and TMEM, move row r+1
-//      from its buffer into registers, and warp 1 refills the buffer with
-//      the bulk copy of row r+3.
-// The pivot's three candidate elements travel with each row's bulk copy.
+// shared-memory buffers; the slice of the row being written lives in
+// registers, and gamma/beta of the slice live in tensor memory (TMEM),
+// loaded once per launch.  x is read from HBM once and stays on chip until y
+// is written; gamma and beta are read from HBM once.  Three warp roles run
+// concurrently: warps 1..3 reduce a row's statistics as soon as it lands and
+// publish the CTA's triple, warp 0 merges the triples of all CTAs, warps
+// 4..15 write y.  A row's triples go out about two rows before its y is
+// written, which hides the grid-wide exchange (several microseconds under
+// full HBM load) behind other rows' work.  The pivot's three candidate
+// elements travel with each row's bulk copy.
 //
 // Grid barrier without atomics.  Each CTA publishes its (mean, M2) as two
-// 64-bit words, each carrying a 32-bit tag in its high half.  Both the
-// record and the polls go through the bulk-copy unit (a 16-byte bulk store;
-// one bulk load of all G records per attempt): plain loads and stores would
-// queue behind the SM's own y stores, which drain at HBM speed.  The barrier
-// and its data arrive in the same round trip.  Records sit in 4 rotating
-// slots.  Tags count rows: row r of a launch is tagged row_base + r + 1,
-// where row_base (workspace header) is the number of rows the persistent
-// kernel has already processed on this workspace.  A slot therefore only
-// ever holds tags smaller than the one awaited, and a zeroed workspace holds
-// tag 0, which is never awaited.  row_base is read at kernel start and
-// advanced by CTA 0 after its last merge, which proves every CTA has read
-// it.  Every wait is bounded by %globaltimer: on timeout a CTA records
-// NORM_ERR_TIMEOUT, drains its own bulk copies, frees its TMEM and returns
-// without writing the remaining rows of y.
+// 64-bit words, each carrying a 32-bit tag in its high half, written with
+// st.relaxed.gpu (single-copy atomic).  Warp 0 polls the G records of the
+// row with plain L2 loads (ld.global.cg, which overlap) until every tag
+// matches, so the barrier and its data arrive in the same round trip.  It
+// polls after the CTA's y stores have been issued: its loads would
+// otherwise queue behind them.  Records sit in 4 rotating slots.  Tags count
+// rows: row r of a launch is tagged row_base + r + 1, where row_base
+// (workspace header) is the number of rows the persistent kernel has already
+// processed on this workspace.  A slot therefore only ever holds tags
+// smaller than the one awaited, and a zeroed workspace holds tag 0, which is
+// never awaited.  row_base is read at kernel start and advanced by CTA 0
+// after its last merge, which proves every CTA has read it.  Every wait is
+// bounded by %globaltimer: on timeout a CTA records NORM_ERR_TIMEOUT, drains
+// its own bulk copies, frees its TMEM and returns without writing the
+// remaining rows of y.
 //
 // Split path (any shape): kernel 1 writes one triple per (row, chunk) CTA;
 // kernel 2 merges the row's triples and applies, re-reading x.
@@ -61,24 +57,31 @@ namespace normk {
 
 namespace {
 
-// Warp 0 coordinates; warps 1..15 own the row slice (15 float4 each).
-constexpr int LN_DATA_WARPS = 15;
-constexpr int LN_T = 32 * LN_DATA_WARPS;  // data threads
-constexpr int LN_THREADS = LN_T + 32;     // CTA size
-constexpr int LN_V = 15;                  // float4 of the slice per data thread
+// Warp roles of the persistent kernel: warp 0 coordinates the grid
+// barrier, warps 1..3 reduce row statistics from shared memory, warps 4..15
+// write y (18 float4 of the slice each, held in registers).
+constexpr int LN_THREADS = 512;           // CTA size
+constexpr int LN_STATS_WARPS = 3;         // warps 1..3
+constexpr int LN_S = 32 * LN_STATS_WARPS; // statistics threads
+constexpr int LN_APPLY_WARP0 = 4;         // first apply warp
+constexpr int LN_A = LN_THREADS - 32 * LN_APPLY_WARP0; // apply threads (warps 4..15)
+constexpr int LN_V = 18;                  // float4 of the slice per apply thread
 constexpr int LN_GB = 3;                  // gamma/beta float4 per TMEM load batch
 constexpr int LN_NB = LN_V / LN_GB;       // batches per row
 constexpr uint32_t LN_TMEM_COLS = 512;    // TMEM columns the CTA allocates (all)
-constexpr int LN_TM_COLS = 8 * LN_V;      // TMEM columns of one data thread: gamma, beta
+constexpr int LN_TM_COLS = 8 * LN_V;      // TMEM columns of one apply thread: gamma, beta
 constexpr uint32_t LN_TM_BETA = 4 * LN_V; // column offset of beta within them
 constexpr int LN_SLOTS = 4;               // partial-record slots: reused 4 rows later
 constexpr int LN_MAX_GRID = 160;          // CTAs whose records one warp loads at once
 constexpr uint32_t LN_BULK_CHUNK = 32768;
+constexpr int LN_BAR_APPLIED = 1;         // named barrier of warp 0 and the apply warps
+constexpr int LN_BAR_STATS = 2;           // named barrier of the statistics warps
 static_assert(LN_V % LN_GB == 0, "whole gamma/beta batches");
-// warps 1..15 sit in TMEM quarters by warp % 4 and take column ranges by
-// warp / 4, so at most four of them share a quarter
-static_assert(4 * LN_TM_COLS <= static_cast<int>(LN_TMEM_COLS), "gamma/beta of a quarter fit TMEM");
-static_assert(LN_DATA_WARPS + 1 <= 16, "warp / 4 < 4");
+static_assert(LN_APPLY_WARP0 % 4 == 0 && LN_A % 128 == 0, "apply warps fill whole TMEM quarters");
+// apply warp w sits in TMEM quarter w % 4 and takes column range
+// w / 4 - 1 of it, so three of them share a quarter
+static_assert((LN_THREADS / 128 - 1) * LN_TM_COLS <= static_cast<int>(LN_TMEM_COLS),
+              "gamma/beta of a quarter fit TMEM");
 
 struct RowMean {
     float hi, lo, rstd;
@@ -217,19 +220,11 @@ __device__ __forceinline__ Moments merge_records(const unsigned long long (&w)[L
     return t;
 }
 
-// Warp 0: read the G records of a row until every tag equals `tag`
-// (bounded by timeout_ns), then merge them.
-//
-// BULK = false: plain L2 loads (ld.global.cg), which overlap.  BULK = true:
-// one bulk copy (TMA unit) of all records into rec_s per attempt, completed
-// on `bar`; `phase` is the parity of bar's next completion and `inflight`
-// tells the caller that a copy into rec_s may still be running after a
-// timeout, which it must drain before exit.
-template <bool BULK>
-__device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *rec, unsigned long long *rec_s,
-                                                    uint64_t *bar, uint32_t &phase, bool &inflight, int G,
-                                                    unsigned q4, unsigned rem, unsigned tag, uint64_t timeout_ns,
-                                                    uint64_t pol)
+// Warp 0: read the G records of a row with plain L2 loads (ld.global.cg,
+// which overlap) until every tag equals `tag` (bounded by timeout_ns), then
+// merge them.
+__device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *rec, int G, unsigned q4, unsigned rem,
+                                                    unsigned tag, uint64_t timeout_ns)
 {
     constexpr int J = LN_MAX_GRID / 32;
     const int lane = threadIdx.x & 31;
@@ -237,27 +232,6 @@ __device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *re
     g.ok = true;
     uint64_t t0 = 0;
     for (int attempt = 0;; ++attempt) {
-        if (BULK) {
-            int landed = 0;
-            if (lane == 0) {
-                // the warp's reads of the previous attempt precede the copy
-                fence_proxy_async_smem();
-                const uint32_t bytes = static_cast<uint32_t>(G) * 16u;
-                mbar_arrive_expect_tx(bar, bytes);
-                bulk_g2s(rec_s, rec, bytes, bar, pol);
-                inflight = true;
-                landed = mbar_wait_bounded(bar, phase, timeout_ns) ? 1 : 0;
-                if (landed) {
-                    inflight = false;
-                    phase ^= 1u;
-                }
-            }
-            if (!__shfl_sync(0xffffffffu, landed, 0)) {
-                g.ok = false;
-                return g;
-            }
-            __syncwarp();
-        }
         // the words live only inside one attempt, so they stay in registers
         unsigned long long w[J][2];
         unsigned bad = 0;
@@ -267,7 +241,7 @@ __device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *re
             const int i = min(lane + 32 * j, G - 1);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                w[j][e] = BULK ? rec_s[2 * i + e] : ld_cg_u64(rec + 2 * i + e);
+                w[j][e] = ld_cg_u64(rec + 2 * i + e);
                 bad |= record_tag(w[j][e]) ^ tag;
             }
         }
@@ -281,10 +255,7 @@ __device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *re
             g.ok = false;
             return g;
         }
-        if (BULK)
-            __syncwarp();
-        else
-            __nanosleep(20);
+        __nanosleep(32);
     }
 }
 
@@ -304,29 +275,16 @@ __device__ __forceinline__ float row_pivot(const float4 *piece, int64_t row_len)
     return fmaxf(fminf(a, b), fminf(fmaxf(a, b), c));
 }
 
-#ifndef LN_BULK_BARRIER
-#define LN_BULK_BARRIER 1
-#endif
-// How the grid barrier's records travel: plain loads and stores (0) or bulk
-// copies (1).
-constexpr bool LN_BULK_RECORDS = LN_BULK_BARRIER != 0;
-
-// Named barriers of the persistent kernel (0 is __syncthreads).
-constexpr int LN_BAR_PUBLISHED = 1; // warp 0 has issued the row's record
-constexpr int LN_BAR_ROW_DONE = 2;  // y of row r written, row r+1 in registers
-
 __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p)
 {
     extern __shared__ __align__(128) float4 ln_smem[];
     __shared__ __align__(8) uint64_t bar_x[2];
-    __shared__ Moments red[LN_DATA_WARPS];
-    __shared__ float4 piv_in[2][3]; // pieces holding a row's pivot candidates, by row parity
-    __shared__ RowMean row_mean[2]; // merged statistics of a row, by row parity
+    __shared__ Moments red[LN_STATS_WARPS];             // per-warp triples of a row
+    __shared__ float4 piv_in[2][3];                     // a row's pivot candidates, by row parity
+    __shared__ float piv_k[2];                          // a row's pivot, by row parity
+    __shared__ RowMean row_mean[2];                     // merged statistics, by row parity
     __shared__ unsigned row_base_s;
     __shared__ uint32_t tmem_base_s;
-    __shared__ __align__(8) uint64_t bar_rec;                             // record fetches (bulk)
-    __shared__ __align__(16) unsigned long long rec_in[LN_BULK_RECORDS ? 2 * LN_MAX_GRID : 2];
-    __shared__ __align__(16) unsigned long long rec_out[2];               // this CTA's record (bulk)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -353,7 +311,6 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     if (tid == 0) {
         mbar_init(&bar_x[0], 1);
         mbar_init(&bar_x[1], 1);
-        mbar_init(&bar_rec, 1);
         fence_mbar_init();
         fence_proxy_async_smem();
         row_base_s = ld_relaxed_gpu_u32(&p.sync->row_base);
@@ -365,174 +322,167 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     const uint32_t tmem_base = tmem_base_s;
     bool aborted = false;
 
-    // Warp 0 and warps 1..15 run separate loops.  Per iteration r both pass
-    // the block-wide barrier 1 (__syncthreads_or: abort vote; the triples of
-    // row r+1 are reduced and row r is merged) and the named barriers
-    // LN_BAR_PUBLISHED and LN_BAR_ROW_DONE, at which warp 0 only arrives: it
-    // goes on merging row r+1 until the next barrier 1.
+    // Row q's slice, plus the three 16-byte pieces of the row that hold its
+    // pivot candidates, all on bar_x[q & 1] (row q lives in buffer q & 1).
+    auto issue_x = [&](int64_t q) {
+        uint64_t *bar = &bar_x[q & 1];
+        const uint32_t bytes = static_cast<uint32_t>(n4) * 16u;
+        mbar_arrive_expect_tx(bar, bytes + 48u);
+        const float4 *row = x4 + q * L4;
+        bulk_g2s(&piv_in[q & 1][0], row, 16u, bar, pol_stream);
+        bulk_g2s(&piv_in[q & 1][1], row + ((p.row_len >> 1) >> 2), 16u, bar, pol_stream);
+        bulk_g2s(&piv_in[q & 1][2], row + (L4 - 1), 16u, bar, pol_stream);
+        const float4 *src = row + f0;
+        float4 *dst = ln_smem + (q & 1) * buf_f4;
+        for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
+            bulk_g2s(dst + off / 16, src + off / 16, (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK,
+                     bar, pol_stream);
+    };
+    auto x_parity = [](int64_t q) { return static_cast<uint32_t>((q >> 1) & 1); };
+
+    // Iteration r (-2 <= r < R) starts with a block-wide barrier that is
+    // also the abort vote (__syncthreads_or).  By then warp 0 has merged row
+    // r.  During it:
+    //   warps 1..3    reduce row r+2 from its buffer (it lands meanwhile) and
+    //                 publish the CTA's triple of it at once;
+    //   warps 4..15   write y of row r, move row r+1 from its buffer into
+    //                 registers, and meet warp 0 at barrier LN_BAR_APPLIED;
+    //                 then warp 4 refills that buffer with row r+3;
+    //   warp 0        after LN_BAR_APPLIED, merges row r+1, whose triples
+    //                 every CTA published during the previous iteration.
+    // A row's triples are published about two iterations before its y is
+    // written, so the grid-wide exchange has that long to complete, and the
+    // reduction of a row overlaps the writing of an earlier one.
     if (warp == 0) {
         // ------------------------------------------------ coordinator
-        uint32_t rec_phase = 0;    // parity of bar_rec's next completion
-        bool rec_inflight = false; // a record fetch may still be writing rec_in
-        const uint64_t pol_rec = policy_evict_last();
-        bool fail = false;         // the merge of the previous row gave up
-        for (int64_t r = -1; r < R; ++r) {
-            const int64_t nx = r + 1;
-            if (__syncthreads_or(fail ? 1 : 0)) { // 1
+        bool fail = false; // the merge of the previous row gave up
+        for (int64_t r = -2; r < R; ++r) {
+            if (__syncthreads_or(fail ? 1 : 0)) {
                 aborted = true;
                 break;
             }
-            if (nx < R) {
+            const int64_t q = r + 1; // the row merged now
+            // Poll once the apply warps have issued their y stores: loads
+            // issued while those stores queue would wait behind them.
+            bar_sync_named(LN_BAR_APPLIED, LN_A + 32);
+            if (q < 0 || q >= R)
+                continue;
+            const GridMerge gm = poll_and_merge(records + static_cast<int64_t>(q % LN_SLOTS) * G * 2, G, q4, rem,
+                                                row_tag(row_base, q) + p.tag_skew, p.timeout_ns);
+            if (!gm.ok) {
+                fail = true;
+                if (lane == 0)
+                    record_error(p.err, NORM_ERR_TIMEOUT);
+            } else if (lane == 0) {
+                row_mean[q & 1] = finish_row(piv_k[q & 1], gm.tot, p.eps);
+                // every CTA has read row_base once CTA 0 has merged the last row
+                if (q + 1 == R && cta == 0)
+                    st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(R));
+            }
+        }
+    } else if (warp < LN_APPLY_WARP0) {
+        // ------------------------------------------------ statistics warps 1..3
+        const int st = tid - 32;
+        bool fail = false; // row q's copy did not land in time
+        for (int64_t r = -2; r < R; ++r) {
+            if (__syncthreads_or(fail ? 1 : 0)) {
+                aborted = true;
+                break;
+            }
+            const int64_t q = r + 2; // the row reduced and published now
+            if (q >= R)
+                continue;
+            fail = !mbar_wait_bounded(&bar_x[q & 1], x_parity(q), p.timeout_ns);
+            Moments m = {0.f, 0.f, 0.f};
+            const float K = fail ? 0.f : row_pivot(piv_in[q & 1], p.row_len);
+            if (!fail) {
+                // shifted sums of d = x - K over this thread's float4, four
+                // independent accumulator pairs
+                const float4 *buf = ln_smem + (q & 1) * buf_f4;
+                float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+                int i = st;
+                for (; i + 3 * LN_S < n4; i += 4 * LN_S) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 v = buf[i + u * LN_S];
+                        const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
+                        s1[u] += (a + b) + (c + d);
+                        s2[u] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[u]))));
+                    }
+                }
+                for (; i < n4; i += LN_S) {
+                    const float4 v = buf[i];
+                    const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
+                    s1[0] += (a + b) + (c + d);
+                    s2[0] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[0]))));
+                }
+                const int nv = n4 > st ? (n4 - st + LN_S - 1) / LN_S : 0; // float4 of this thread
+                if (nv > 0) {
+                    const float S1 = (s1[0] + s1[1]) + (s1[2] + s1[3]);
+                    const float S2 = (s2[0] + s2[1]) + (s2[2] + s2[3]);
+                    m.n = 4.f * static_cast<float>(nv);
+                    m.mean = S1 / m.n;
+                    m.m2 = fmaxf(fmaf(-S1, m.mean, S2), 0.f);
+                }
+            }
+            m = warp_merge(m);
+            if (lane == 0)
+                red[warp - 1] = m;
+            bar_sync_named(LN_BAR_STATS, LN_S);
+            if (warp == 1) {
+                // the CTA's triple of row q goes out now, one bulk store
                 Moments c = {0.f, 0.f, 0.f};
-                if (lane < LN_DATA_WARPS)
+                if (lane < LN_STATS_WARPS)
                     c = red[lane];
                 c = warp_merge(c);
-                // read now: the bulk copy of row nx + 2, issued after
-                // LN_BAR_ROW_DONE, overwrites these pieces.  (The data warps
-                // saw row nx land before barrier 1; this wait returns at once
-                // and orders the read after the copy for this warp as well.)
-                fail = !mbar_wait_bounded(&bar_x[nx & 1], static_cast<uint32_t>((nx >> 1) & 1), p.timeout_ns);
-                const float K = row_pivot(piv_in[nx & 1], p.row_len);
-                const unsigned tag = row_tag(row_base, nx);
-                unsigned long long *slot = records + static_cast<int64_t>(nx % LN_SLOTS) * G * 2;
-                if (lane == 0) {
-                    if (LN_BULK_RECORDS) {
-                        bulk_wait_read_all(); // the previous record has left rec_out
-                        rec_out[0] = tagged(tag, c.mean);
-                        rec_out[1] = tagged(tag, c.m2);
-                        fence_proxy_async_smem();
-                        bulk_s2g(slot + 2 * cta, rec_out, 16);
-                        bulk_commit();
-                    } else {
-                        st_relaxed_gpu_u64(slot + 2 * cta + 0, tagged(tag, c.mean));
-                        st_relaxed_gpu_u64(slot + 2 * cta + 1, tagged(tag, c.m2));
-                    }
+                if (lane == 0 && !fail) {
+                    piv_k[q & 1] = K;
+                    const unsigned tag = row_tag(row_base, q);
+                    unsigned long long *out = records + (static_cast<int64_t>(q % LN_SLOTS) * G + cta) * 2;
+                    st_relaxed_gpu_u64(out + 0, tagged(tag, c.mean));
+                    st_relaxed_gpu_u64(out + 1, tagged(tag, c.m2));
                 }
-                __syncwarp();
-                bar_arrive_named(LN_BAR_PUBLISHED, LN_THREADS);
-                bar_arrive_named(LN_BAR_ROW_DONE, LN_THREADS);
-                // merge row nx while the data warps write row r and reduce
-                // row nx + 1; due at the next barrier 1
-                const GridMerge gm = poll_and_merge<LN_BULK_RECORDS>(slot, rec_in, &bar_rec, rec_phase, rec_inflight,
-                                                                     G, q4, rem, tag + p.tag_skew, p.timeout_ns,
-                                                                     pol_rec);
-                if (!gm.ok || fail) {
-                    fail = true;
-                    if (lane == 0)
-                        record_error(p.err, NORM_ERR_TIMEOUT);
-                } else if (lane == 0) {
-                    row_mean[nx & 1] = finish_row(K, gm.tot, p.eps);
-                    // every CTA has read row_base once CTA 0 has merged the last row
-                    if (nx + 1 == R && cta == 0)
-                        st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(R));
-                }
-            } else {
-                bar_arrive_named(LN_BAR_PUBLISHED, LN_THREADS);
-                bar_arrive_named(LN_BAR_ROW_DONE, LN_THREADS);
             }
-        }
-        if (lane == 0) {
-            // never leave a bulk copy in flight into or out of shared memory
-            if (rec_inflight && !mbar_wait_bounded(&bar_rec, rec_phase, p.timeout_ns))
-                record_error(p.err, NORM_ERR_TIMEOUT);
-            if (LN_BULK_RECORDS)
-                bulk_wait_all();
-            if (aborted)
-                record_error(p.err, NORM_ERR_TIMEOUT);
+            // red is reused next iteration
+            bar_sync_named(LN_BAR_STATS, LN_S);
         }
     } else {
-        // ------------------------------------------------ data warps 1..15
-        const int dt = tid - 32;
-        // Thread 32 (warp 1, lane 0) issues the bulk copies of x.  It tracks
+        // ------------------------------------------------ apply warps 4..15
+        const int at = tid - 32 * LN_APPLY_WARP0;
+        // Thread 32 * LN_APPLY_WARP0 issues the bulk copies of x.  It tracks
         // those it issued (rows < issued) and those whose completion it
         // observed (rows < waited), so that an early exit can drain them.
-        const bool issuer = dt == 0;
+        const bool issuer = at == 0;
         int64_t issued = 0, waited = 0;
-        // Row q's slice, plus the three 16-byte pieces of the row that hold
-        // its pivot candidates, all on bar_x[q & 1].
-        auto issue_x = [&](int64_t q) {
-            uint64_t *bar = &bar_x[q & 1];
-            const uint32_t bytes = static_cast<uint32_t>(n4) * 16u;
-            mbar_arrive_expect_tx(bar, bytes + 48u);
-            const float4 *row = x4 + q * L4;
-            bulk_g2s(&piv_in[q & 1][0], row, 16u, bar, pol_stream);
-            bulk_g2s(&piv_in[q & 1][1], row + ((p.row_len >> 1) >> 2), 16u, bar, pol_stream);
-            bulk_g2s(&piv_in[q & 1][2], row + (L4 - 1), 16u, bar, pol_stream);
-            const float4 *src = row + f0;
-            float4 *dst = ln_smem + (q & 1) * buf_f4;
-            for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
-                bulk_g2s(dst + off / 16, src + off / 16,
-                         (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, bar, pol_stream);
-            issued = q + 1;
-        };
         if (issuer) {
             issue_x(0);
-            if (R > 1)
+            issued = 1;
+            if (R > 1) {
                 issue_x(1);
+                issued = 2;
+            }
         }
         // This thread's TMEM cells: lane 32*(warp % 4) + lane of its warp's
-        // quarter, LN_TM_COLS columns from (warp / 4) * LN_TM_COLS: gamma of
-        // its k-th float4 at column 4k, beta at LN_TM_BETA + 4k.  The four
-        // (or three) data warps of a quarter take disjoint column ranges.
+        // quarter, LN_TM_COLS columns from (warp / 4 - 1) * LN_TM_COLS:
+        // gamma of its k-th float4 at column 4k, beta at LN_TM_BETA + 4k.
         const uint32_t tm = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
-                            static_cast<uint32_t>((warp >> 2) * LN_TM_COLS);
+                            static_cast<uint32_t>((warp / 4 - 1) * LN_TM_COLS);
         float4 v[LN_V]; // this thread's part of the slice of row r
-        for (int64_t r = -1; r < R; ++r) {
-            const int64_t nx = r + 1;
-
-            // 1. triple of row nx from its shared-memory buffer, about the
-            //    row's pivot K
-            bool fail = false;
-            if (nx < R) {
-                const float4 *buf = ln_smem + (nx & 1) * buf_f4;
-                if (!mbar_wait_bounded(&bar_x[nx & 1], static_cast<uint32_t>((nx >> 1) & 1), p.timeout_ns)) {
-                    fail = true;
-                } else {
-                    if (issuer)
-                        waited = nx + 1;
-                    const float K = row_pivot(piv_in[nx & 1], p.row_len);
-                    // one pass over shared memory: shifted sums of d = x - K
-                    float s1 = 0.f, s2 = 0.f;
-                    int cnt = 0;
-#pragma unroll
-                    for (int k = 0; k < LN_V; ++k) {
-                        const int i = dt + k * LN_T;
-                        if (i < n4) {
-                            const float4 q = buf[i];
-                            const float a = q.x - K, bq = q.y - K, c = q.z - K, d = q.w - K;
-                            s1 += (a + bq) + (c + d);
-                            s2 = fmaf(a, a, fmaf(bq, bq, fmaf(c, c, fmaf(d, d, s2))));
-                            cnt += 4;
-                        }
-                    }
-                    Moments m = {0.f, 0.f, 0.f};
-                    if (cnt > 0) {
-                        m.n = static_cast<float>(cnt);
-                        m.mean = s1 / m.n;
-                        m.m2 = fmaxf(fmaf(-s1, m.mean, s2), 0.f);
-                    }
-                    m = warp_merge(m);
-                    if (lane == 0)
-                        red[warp - 1] = m;
-                }
-            }
-            if (__syncthreads_or(fail ? 1 : 0)) { // 1
+        for (int64_t r = -2; r < R; ++r) {
+            if (__syncthreads_or(0)) {
                 aborted = true;
                 break;
             }
-            // the CTA's record of row nx goes out before this CTA's y stores
-            bar_sync_named(LN_BAR_PUBLISHED, LN_THREADS);
-
-            if (r < 0) {
-                // 2'. before the first row: gamma and beta of the slice go to
-                //     TMEM once, staged through v (free until row 0 arrives)
+            if (r == -2) {
+                // before the first row: gamma and beta of the slice go to
+                // TMEM once, staged through v (free until row 0 is moved in)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float4 *src = h == 0 ? g4 : b4;
                     const float4 dflt = h == 0 ? make_float4(1.f, 1.f, 1.f, 1.f) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int k = 0; k < LN_V; ++k) {
-                        const int i = dt + k * LN_T;
+                        const int i = at + k * LN_A;
                         v[k] = (src && i < n4) ? ld_stream_f4(src + f0 + i, pol_stream) : dflt;
                     }
                     __syncwarp();
@@ -541,16 +491,17 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                         tmem_st4(tm + static_cast<uint32_t>(h * LN_TM_BETA + 4 * k), v[k]);
                     tmem_wait_st();
                 }
-            } else {
-                // 2. y of row r from registers, gamma/beta from TMEM, one
-                //    batch of LN_GB float4 loaded while the previous one is
-                //    written
+            }
+            if (r >= 0) {
+                // y of row r from registers, gamma/beta from TMEM in batches
+                // of LN_GB float4
                 const RowMean rm = row_mean[r & 1];
                 float4 *yr = y4 + r * L4 + f0;
-                float4 gA[LN_GB], bA[LN_GB], gB[LN_GB], bB[LN_GB];
-                // tcgen05 loads and waits are warp-collective: reconverge
-                // after the divergent stores first
-                auto load_gb = [&](int bt, float4 *g, float4 *bb) {
+#pragma unroll
+                for (int bt = 0; bt < LN_NB; ++bt) {
+                    float4 g[LN_GB], bb[LN_GB];
+                    // tcgen05 loads and waits are warp-collective: reconverge
+                    // after the divergent stores first
                     __syncwarp();
 #pragma unroll
                     for (int j = 0; j < LN_GB; ++j) {
@@ -558,67 +509,49 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                         g[j] = tmem_ld4(tm + c);
                         bb[j] = tmem_ld4(tm + LN_TM_BETA + c);
                     }
-                };
-                auto pin_gb = [&](float4 *g, float4 *bb) {
-                    __syncwarp();
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < LN_GB; ++j) {
                         tmem_pin(g[j]);
                         tmem_pin(bb[j]);
                     }
-                };
-                auto write_batch = [&](int bt, const float4 *g, const float4 *bb) {
 #pragma unroll
                     for (int j = 0; j < LN_GB; ++j) {
                         const int k = bt * LN_GB + j;
-                        const int i = dt + k * LN_T;
+                        const int i = at + k * LN_A;
                         if (i < n4)
                             st_stream_f4(yr + i, ln_apply4(v[k], rm, g[j], bb[j]), pol_stream);
                     }
-                };
-                load_gb(0, gA, bA);
-                pin_gb(gA, bA);
-                // batches alternate between the A and B registers (the branch on
-                // bt's parity is resolved at compile time)
-#pragma unroll
-                for (int bt = 0; bt < LN_NB; ++bt) {
-                    if ((bt & 1) == 0) {
-                        if (bt + 1 < LN_NB)
-                            load_gb(bt + 1, gB, bB);
-                        write_batch(bt, gA, bA);
-                        if (bt + 1 < LN_NB)
-                            pin_gb(gB, bB);
-                    } else {
-                        if (bt + 1 < LN_NB)
-                            load_gb(bt + 1, gA, bA);
-                        write_batch(bt, gB, bB);
-                        if (bt + 1 < LN_NB)
-                            pin_gb(gA, bA);
-                    }
                 }
             }
-            // row nx moves into registers
-            if (nx < R) {
-                const float4 *buf = ln_smem + (nx & 1) * buf_f4;
+            const int64_t q = r + 1; // the row moved into registers now
+            if (q >= 0 && q < R) {
+                // row q landed before the statistics warps reduced it (an
+                // iteration ago); the issuer's wait returns at once and
+                // lets it account for the copy
+                if (issuer && mbar_wait_bounded(&bar_x[q & 1], x_parity(q), p.timeout_ns))
+                    waited = q + 1;
+                const float4 *buf = ln_smem + (q & 1) * buf_f4;
 #pragma unroll
                 for (int k = 0; k < LN_V; ++k) {
-                    const int i = dt + k * LN_T;
+                    const int i = at + k * LN_A;
                     v[k] = (i < n4) ? buf[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
             __syncwarp();
-            bar_sync_named(LN_BAR_ROW_DONE, LN_THREADS);
-            // buffer nx & 1 and its pivot pieces are free: refill them
-            if (issuer && nx + 2 < R) {
+            bar_sync_named(LN_BAR_APPLIED, LN_A + 32);
+            // buffer q & 1 and its pivot pieces are free (the statistics
+            // warps reduced row q an iteration ago): refill them with row q + 2
+            if (issuer && q + 2 >= 2 && q + 2 < R) {
                 fence_proxy_async_smem();
-                issue_x(nx + 2);
+                issue_x(q + 2);
+                issued = q + 3;
             }
         }
         // Drain: never leave a bulk copy in flight into shared memory.
         if (issuer) {
-            for (int64_t q = waited; q < issued; ++q) {
-                if (!mbar_wait_bounded(&bar_x[q & 1], static_cast<uint32_t>((q >> 1) & 1), p.timeout_ns))
+            for (int64_t qq = waited; qq < issued; ++qq) {
+                if (!mbar_wait_bounded(&bar_x[qq & 1], x_parity(qq), p.timeout_ns))
                     record_error(p.err, NORM_ERR_TIMEOUT);
             }
         }
@@ -728,7 +661,7 @@ __global__ void __launch_bounds__(LS_T) ln_split_apply_kernel(LnParams p)
 
 LnPersistentConfig ln_persistent_config()
 {
-    return LnPersistentConfig{LN_THREADS, LN_T, LN_V, LN_SLOTS * 16, LN_MAX_GRID};
+    return LnPersistentConfig{LN_THREADS, LN_A, LN_V, LN_SLOTS * 16, LN_MAX_GRID};
 }
 
 cudaError_t ln_persistent_static_smem(int *bytes)

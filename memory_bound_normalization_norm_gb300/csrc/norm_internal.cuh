@@ -32,13 +32,6 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_normal()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 __device__ __forceinline__ uint64_t policy_evict_last()
 {
     uint64_t p;
@@ -113,18 +106,6 @@ __device__ __forceinline__ float4 ld_l2_f4(const float4 *p)
     return v;
 }
 
-// 128-bit shared-memory load that the compiler may neither drop nor merge
-// with another load of the same address.
-__device__ __forceinline__ float4 ld_shared_f4(const float4 *p)
-{
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(smem_u32(p))
-                 : "memory");
-    return v;
-}
-
 // ---- mbarrier + bulk copy (TMA engine, non-tensor form)
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
@@ -148,31 +129,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Non-blocking test of phase `parity` of `bar`.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -204,65 +166,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// Bulk copy this CTA's shared memory -> global, tracked by the issuing
-// thread's bulk async-groups (bulk_commit / bulk_wait_*).  dst, src and
-// bytes must be 16-byte multiples.
-__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until every committed bulk group of this thread has finished reading
-// its shared-memory source.
-__device__ __forceinline__ void bulk_wait_read_all()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Wait until every committed bulk group of this thread has completed.
-__device__ __forceinline__ void bulk_wait_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // ---- gpu-scope synchronization primitives
-
-__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v)
-{
-    unsigned old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_relaxed_gpu(unsigned *p, unsigned v)
-{
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long *p, unsigned long long v)
 {
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long *p)
-{
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
 }
 
 // 64-bit load from L2 (bypassing L1) that the compiler may not merge or drop,
@@ -288,11 +196,6 @@ __device__ __forceinline__ void st_relaxed_gpu_u32(unsigned *p, unsigned v)
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void red_add_release_gpu(unsigned *p, unsigned v)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Record the first device-side failure in the per-device error word.
 __device__ __forceinline__ void record_error(unsigned *err, unsigned code)
 {
@@ -300,16 +203,11 @@ __device__ __forceinline__ void record_error(unsigned *err, unsigned code)
         atomicCAS(err, 0u, code);
 }
 
-// Named CTA barriers (ids 1..15; id 0 is __syncthreads).  `count` threads,
-// a multiple of 32, take part; bar_arrive signals without waiting.
+// Named CTA barrier (ids 1..15; id 0 is __syncthreads) over `count`
+// threads, a multiple of 32.
 __device__ __forceinline__ void bar_sync_named(int id, int count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void bar_arrive_named(int id, int count)
-{
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- tensor memory
