@@ -66,7 +66,7 @@ constexpr int LN_S = 32 * LN_STATS_WARPS; // statistics threads
 constexpr int LN_APPLY_WARP0 = 4;         // first apply warp
 constexpr int LN_A = LN_THREADS - 32 * LN_APPLY_WARP0; // apply threads (warps 4..15)
 constexpr int LN_V = 18;                  // float4 of the slice per apply thread
-constexpr int LN_GB = 3;                  // gamma/beta float4 per TMEM load batch
+constexpr int LN_GB = 2;                  // gamma/beta float4 per TMEM load batch
 constexpr int LN_NB = LN_V / LN_GB;       // batches per row
 constexpr uint32_t LN_TMEM_COLS = 512;    // TMEM columns the CTA allocates (all)
 constexpr int LN_TM_COLS = 8 * LN_V;      // TMEM columns of one apply thread: gamma, beta
@@ -76,6 +76,7 @@ constexpr int LN_MAX_GRID = 160;          // CTAs whose records one warp loads a
 constexpr uint32_t LN_BULK_CHUNK = 32768;
 constexpr int LN_BAR_APPLIED = 1;         // named barrier of warp 0 and the apply warps
 constexpr int LN_BAR_STATS = 2;           // named barrier of the statistics warps
+constexpr int LN_BAR_FILL = 3;            // named barrier of the apply warps (TMEM fill)
 static_assert(LN_V % LN_GB == 0, "whole gamma/beta batches");
 static_assert(LN_APPLY_WARP0 % 4 == 0 && LN_A % 128 == 0, "apply warps fill whole TMEM quarters");
 // apply warp w sits in TMEM quarter w % 4 and takes column range
@@ -279,7 +280,9 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 {
     extern __shared__ __align__(128) float4 ln_smem[];
     __shared__ __align__(8) uint64_t bar_x[2];
-    __shared__ Moments red[LN_STATS_WARPS];             // per-warp triples of a row
+    __shared__ __align__(8) uint64_t bar_gb; // gamma, then beta, into buffer 1
+    __shared__ Moments red[2][LN_STATS_WARPS];          // per-warp triples, by row parity
+    __shared__ __align__(16) unsigned long long rec_out[2][2]; // this CTA's record, by row parity
     __shared__ float4 piv_in[2][3];                     // a row's pivot candidates, by row parity
     __shared__ float piv_k[2];                          // a row's pivot, by row parity
     __shared__ RowMean row_mean[2];                     // merged statistics, by row parity
@@ -311,6 +314,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     if (tid == 0) {
         mbar_init(&bar_x[0], 1);
         mbar_init(&bar_x[1], 1);
+        mbar_init(&bar_gb, 1);
         fence_mbar_init();
         fence_proxy_async_smem();
         row_base_s = ld_relaxed_gpu_u32(&p.sync->row_base);
@@ -365,19 +369,19 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             // Poll once the apply warps have issued their y stores: loads
             // issued while those stores queue would wait behind them.
             bar_sync_named(LN_BAR_APPLIED, LN_A + 32);
-            if (q < 0 || q >= R)
-                continue;
-            const GridMerge gm = poll_and_merge(records + static_cast<int64_t>(q % LN_SLOTS) * G * 2, G, q4, rem,
-                                                row_tag(row_base, q) + p.tag_skew, p.timeout_ns);
-            if (!gm.ok) {
-                fail = true;
-                if (lane == 0)
-                    record_error(p.err, NORM_ERR_TIMEOUT);
-            } else if (lane == 0) {
-                row_mean[q & 1] = finish_row(piv_k[q & 1], gm.tot, p.eps);
-                // every CTA has read row_base once CTA 0 has merged the last row
-                if (q + 1 == R && cta == 0)
-                    st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(R));
+            if (q >= 0 && q < R) {
+                const GridMerge gm = poll_and_merge(records + static_cast<int64_t>(q % LN_SLOTS) * G * 2, G, q4,
+                                                    rem, row_tag(row_base, q) + p.tag_skew, p.timeout_ns);
+                if (!gm.ok) {
+                    fail = true;
+                    if (lane == 0)
+                        record_error(p.err, NORM_ERR_TIMEOUT);
+                } else if (lane == 0) {
+                    row_mean[q & 1] = finish_row(piv_k[q & 1], gm.tot, p.eps);
+                    // every CTA has read row_base once CTA 0 has merged the last row
+                    if (q + 1 == R && cta == 0)
+                        st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(R));
+                }
             }
         }
     } else if (warp < LN_APPLY_WARP0) {
@@ -427,25 +431,32 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             }
             m = warp_merge(m);
             if (lane == 0)
-                red[warp - 1] = m;
+                red[q & 1][warp - 1] = m;
             bar_sync_named(LN_BAR_STATS, LN_S);
             if (warp == 1) {
-                // the CTA's triple of row q goes out now, one bulk store
+                // The CTA's triple of row q goes out now as a 16-byte bulk
+                // store: a plain store would stall this warp until the
+                // CTA's y stores ahead of it drain.
                 Moments c = {0.f, 0.f, 0.f};
                 if (lane < LN_STATS_WARPS)
-                    c = red[lane];
+                    c = red[q & 1][lane];
                 c = warp_merge(c);
                 if (lane == 0 && !fail) {
                     piv_k[q & 1] = K;
                     const unsigned tag = row_tag(row_base, q);
-                    unsigned long long *out = records + (static_cast<int64_t>(q % LN_SLOTS) * G + cta) * 2;
-                    st_relaxed_gpu_u64(out + 0, tagged(tag, c.mean));
-                    st_relaxed_gpu_u64(out + 1, tagged(tag, c.m2));
+                    // the store of row q - 2 has read its source
+                    bulk_wait_read_all();
+                    rec_out[q & 1][0] = tagged(tag, c.mean);
+                    rec_out[q & 1][1] = tagged(tag, c.m2);
+                    fence_proxy_async_smem();
+                    bulk_s2g(records + (static_cast<int64_t>(q % LN_SLOTS) * G + cta) * 2, rec_out[q & 1], 16);
+                    bulk_commit();
                 }
             }
-            // red is reused next iteration
-            bar_sync_named(LN_BAR_STATS, LN_S);
         }
+        // the last record has left shared memory
+        if (st == 0)
+            bulk_wait_all();
     } else {
         // ------------------------------------------------ apply warps 4..15
         const int at = tid - 32 * LN_APPLY_WARP0;
@@ -454,13 +465,21 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
         // observed (rows < waited), so that an early exit can drain them.
         const bool issuer = at == 0;
         int64_t issued = 0, waited = 0;
+        // The slice of gamma (h = 0) or beta (h = 1) into buffer 1, for the
+        // TMEM fill before row 1 takes that buffer.
+        auto issue_gb = [&](int h) {
+            const float4 *src = h == 0 ? g4 : b4;
+            const uint32_t bytes = src ? static_cast<uint32_t>(n4) * 16u : 0u;
+            mbar_arrive_expect_tx(&bar_gb, bytes);
+            float4 *dst = ln_smem + buf_f4;
+            for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
+                bulk_g2s(dst + off / 16, src + f0 + off / 16,
+                         (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, &bar_gb, pol_stream);
+        };
         if (issuer) {
             issue_x(0);
             issued = 1;
-            if (R > 1) {
-                issue_x(1);
-                issued = 2;
-            }
+            issue_gb(0);
         }
         // This thread's TMEM cells: lane 32*(warp % 4) + lane of its warp's
         // quarter, LN_TM_COLS columns from (warp / 4 - 1) * LN_TM_COLS:
@@ -474,22 +493,47 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 break;
             }
             if (r == -2) {
-                // before the first row: gamma and beta of the slice go to
-                // TMEM once, staged through v (free until row 0 is moved in)
+                // Before the first row: gamma, then beta, of the slice
+                // arrive by bulk copy in buffer 1 and go to TMEM once; then
+                // buffer 1 receives row 1.  (Bulk copies keep this traffic
+                // off the load path that the statistics warps' shared-memory
+                // reads share.)  If a copy does not land in time, row 1 is
+                // never issued, so the statistics warps give up on it and
+                // the CTA aborts at a later vote.
+                const float4 *buf = ln_smem + buf_f4;
+                bool ok = true;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
+                    const bool landed = mbar_wait_bounded(&bar_gb, static_cast<uint32_t>(h), p.timeout_ns);
+                    if (issuer && !landed && ok) {
+                        // drain it before anything else uses buffer 1
+                        if (!mbar_wait_bounded(&bar_gb, static_cast<uint32_t>(h), p.timeout_ns))
+                            record_error(p.err, NORM_ERR_TIMEOUT);
+                    }
+                    ok = ok && landed;
                     const float4 *src = h == 0 ? g4 : b4;
                     const float4 dflt = h == 0 ? make_float4(1.f, 1.f, 1.f, 1.f) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int k = 0; k < LN_V; ++k) {
                         const int i = at + k * LN_A;
-                        v[k] = (src && i < n4) ? ld_stream_f4(src + f0 + i, pol_stream) : dflt;
+                        v[k] = (src && ok && i < n4) ? buf[i] : dflt;
                     }
                     __syncwarp();
 #pragma unroll
                     for (int k = 0; k < LN_V; ++k)
                         tmem_st4(tm + static_cast<uint32_t>(h * LN_TM_BETA + 4 * k), v[k]);
                     tmem_wait_st();
+                    // every apply thread has read buffer 1: refill it
+                    bar_sync_named(LN_BAR_FILL, LN_A);
+                    if (issuer && ok) {
+                        fence_proxy_async_smem();
+                        if (h == 0) {
+                            issue_gb(1);
+                        } else if (R > 1) {
+                            issue_x(1);
+                            issued = 2;
+                        }
+                    }
                 }
             }
             if (r >= 0) {
