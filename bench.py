@@ -4,8 +4,10 @@
 Default workload (the one the headline metric is quoted on): LayerNorm of an
 fp32 (16, 64, 256, 256) tensor over its last three dims (16 rows of 4,194,304),
 x ~ N(0,1), gamma ~ N(1,0.1), beta ~ N(0,0.1), eps 1e-5.  A step is one call of
-norm_layer_fwd over that batch.  Between timed steps L2 is flushed by writing a
-buffer twice the size of L2, so every step reads x and gamma/beta from HBM.
+norm_layer_fwd over that batch.  K steps run back to back between one pair of
+CUDA events; no step finds its inputs in L2 (a step's x and y are larger than
+twice the L2, or the steps rotate through enough buffer sets to cover three
+L2s).  cold_launch adds the median single launch after an L2 flush.
 
 value  = algorithmic bytes per step (x read once + y written once + gamma and
          beta read once) / mean device time of a step, in GB/s, summed over
@@ -87,10 +89,21 @@ def algorithmic_bytes(cfg) -> int:
     return 8 * elements(cfg) + 4 * param_elems(cfg)
 
 
-def shape_config(name, cfg):
+def l2_note(cfg, l2_bytes=None) -> str:
+    if l2_bytes is None:
+        return "inputs larger than L2 (back-to-back steps rotate through enough buffer sets)"
+    n = buffer_sets(cfg, l2_bytes)
+    mb = 8 * elements(cfg) * n / 2**20
+    if n == 1:
+        return (f"inputs larger than L2: one step moves {mb:.0f} MiB of x and y, more than twice the "
+                f"{l2_bytes / 2**20:.0f} MiB L2; K back-to-back steps between one pair of CUDA events")
+    return (f"inputs larger than L2: back-to-back steps rotate through {n} x/y buffer sets ({mb:.0f} MiB, "
+            f"at least 3x the {l2_bytes / 2**20:.0f} MiB L2); K steps between one pair of CUDA events")
+
+
+def shape_config(name, cfg, l2_bytes=None):
     out = {"workload": cfg["workload"], "name": name, "elements": elements(cfg),
-           "algorithmic_bytes_per_step": algorithmic_bytes(cfg),
-           "l2": "flushed between timed steps (write of 2x L2 bytes, outside the timed events)"}
+           "algorithmic_bytes_per_step": algorithmic_bytes(cfg), "l2": l2_note(cfg, l2_bytes)}
     for k in ("rows", "L", "N", "C", "G", "B", "S"):
         if k in cfg:
             out[{"L": "row_len"}.get(k, k)] = cfg[k]
@@ -284,19 +297,42 @@ def weak_scaling_value(bytes_per_rank: int, world: int, max_seconds_per_step: fl
 
 # ---------------------------------------------------------------------------- GPU timing
 
-def time_steps(call, steps, warmup, flush, stream, sampler=None, world=1):
-    """W untimed steps, then K steps each bracketed by CUDA events on `stream`, with an L2
-    flush between steps outside the events.  Returns (mean seconds per step, t0, t1)."""
+def time_steps(calls, steps, warmup, stream, world=1):
+    """W untimed steps, then K back-to-back steps between one pair of CUDA events on
+    `stream`; step i uses buffer set i % len(calls).  Returns (mean seconds per step, t0, t1)."""
     import torch
-    for _ in range(warmup):
-        flush()
-        call()
+    nset = len(calls)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            calls[i % nset]()
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
     dist_barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            calls[i % nset]()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    dist_barrier(world)
+    return start.elapsed_time(end) / 1e3 / steps, t0, t1
+
+
+def time_cold(call, steps, flush, stream):
+    """Single launches from a cold L2: a flush (write of 2x L2 bytes) before each launch, CUDA
+    events around each launch only.  Returns the median seconds per launch."""
+    import torch
+    for _ in range(3):
+        flush()
+        with torch.cuda.stream(stream):
+            call()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(steps):
             flush()
@@ -304,10 +340,16 @@ def time_steps(call, steps, warmup, flush, stream, sampler=None, world=1):
             call()
             ends[i].record(stream)
     torch.cuda.synchronize()
-    t1 = time.perf_counter()
-    dist_barrier(world)
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    return total_ms / 1e3 / steps, t0, t1
+    return statistics.median(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+
+
+def buffer_sets(cfg, l2_bytes: int) -> int:
+    """Input/output sets to rotate through so that no step finds its data in L2: one set
+    when a step's x + y exceed twice the L2, else enough sets to cover three L2s."""
+    set_bytes = 8 * elements(cfg)
+    if set_bytes > 2 * l2_bytes:
+        return 1
+    return -(-3 * l2_bytes // set_bytes)
 
 
 def check_status(ng):
@@ -316,31 +358,40 @@ def check_status(ng):
         raise RuntimeError(f"device status {ng.norm_status_string(st)}")
 
 
-def run_config(ng, name, cfg, steps, warmup, stream, flush, sampler=None, world=1, want_e2e=False):
+def run_config(ng, name, cfg, steps, warmup, stream, flush, l2_bytes, sampler=None, world=1, want_e2e=False,
+               cold_steps=100):
     import torch
     x, g, b = host_inputs(cfg)
     dev = torch.device("cuda")
     xd = torch.from_numpy(x).to(dev)
     gd = None if g is None else torch.from_numpy(g).to(dev)
     bd = None if b is None else torch.from_numpy(b).to(dev)
-    yd = torch.empty_like(xd)
+    nset = buffer_sets(cfg, l2_bytes)
+    xs = [xd] + [xd.clone() for _ in range(nset - 1)]
+    ys = [torch.empty_like(xd) for _ in range(nset)]
     ws = None
     ws_bytes = 0
     if cfg["op"] == "ln":
         ws_bytes = ng.norm_layer_workspace_bytes(cfg["rows"], cfg["L"])
         ws = torch.zeros((ws_bytes + 3) // 4 + 64, dtype=torch.float32, device=dev)
-    call, launches = make_call(ng, cfg, xd, gd, bd, yd, ws, ws_bytes, stream.cuda_stream)
+    calls = []
+    launches = 1
+    for xk, yk in zip(xs, ys):
+        call, launches = make_call(ng, cfg, xk, gd, bd, yk, ws, ws_bytes, stream.cuda_stream)
+        calls.append(call)
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
-    sec, t0, t1 = time_steps(call, steps, warmup, flush, stream, world=world)
+    sec, t0, t1 = time_steps(calls, steps, warmup, stream, world=world)
     clocks = sampler.stop(t0, t1) if sampler else None
     check_status(ng)
+    cold = time_cold(calls[0], cold_steps, flush, stream) if cold_steps else None
+    check_status(ng)
     res = {"name": name, "seconds_per_step": sec, "launches_per_step": launches, "clocks": clocks,
-           "t_region_s": t1 - t0}
+           "t_region_s": t1 - t0, "buffer_sets": nset, "cold_seconds_per_launch": cold}
     if want_e2e:
-        res["e2e"] = run_e2e(ng, cfg, x, g, b, xd, gd, bd, yd, ws, ws_bytes, stream, min(steps, 20), world)
-    del xd, gd, bd, yd, ws
+        res["e2e"] = run_e2e(ng, cfg, x, g, b, xd, gd, bd, ys[0], ws, ws_bytes, stream, min(steps, 20), world)
+    del xs, ys, xd, gd, bd, ws
     torch.cuda.empty_cache()
     return res
 
@@ -492,7 +543,7 @@ def main(argv=None):
             flush_buf.fill_(1.0)
 
     sampler = ClockSampler(gpu_id_for(local))
-    main_res = run_config(ng, args.config, cfg, args.steps, args.warmup, stream, flush, sampler, world,
+    main_res = run_config(ng, args.config, cfg, args.steps, args.warmup, stream, flush, l2, sampler, world,
                           want_e2e=True)
     sec = dist_max(main_res["seconds_per_step"], world, device="cuda")
     nbytes = algorithmic_bytes(cfg)
@@ -508,15 +559,18 @@ def main(argv=None):
             if name == args.config:
                 continue
             c = CONFIGS[name]
-            k = min(args.steps, 200 if name != "rms" else 50)
-            r = run_config(ng, name, c, k, 5, stream, flush)
+            k = min(args.steps, 1000 if name != "rms" else 50)
+            r = run_config(ng, name, c, k, 5, stream, flush, l2, cold_steps=100 if name != "rms" else 10)
             a = algorithmic_bytes(c) / r["seconds_per_step"] / 1e9
+            cold = r["cold_seconds_per_launch"]
             extras.append({"config": name, "workload": c["workload"], "steps": k,
                            "us_per_step": round(r["seconds_per_step"] * 1e6, 3),
                            "algorithmic_bytes": algorithmic_bytes(c), "achieved_gbs": round(a, 2),
                            "frac_of_measured_peak": round(a / peak, 4),
                            "elements_per_s": round(elements(c) / r["seconds_per_step"], 1),
-                           "launches_per_step": r["launches_per_step"]})
+                           "launches_per_step": r["launches_per_step"], "l2": l2_note(c, l2),
+                           "cold_launch_us": round(cold * 1e6, 3),
+                           "cold_frac_of_measured_peak": round(algorithmic_bytes(c) / cold / 1e9 / peak, 4)})
 
     cpu = None
     if rank == 0 and args.cpu_seconds > 0:
@@ -529,8 +583,13 @@ def main(argv=None):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": DATA,
-            "config": shape_config(args.config, cfg),
+            "config": shape_config(args.config, cfg, l2),
             "elements_per_s": round(elements(cfg) * world / sec, 1),
+            "cold_launch": {"us": round(main_res["cold_seconds_per_launch"] * 1e6, 3),
+                            "frac_of_measured_peak": round(nbytes / main_res["cold_seconds_per_launch"] / 1e9
+                                                           / peak, 4),
+                            "note": "median single launch after an L2 flush (2x L2 written), CUDA events "
+                                    "around each launch"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": peak_note, "traffic_note": traffic_note,

@@ -85,3 +85,17 @@ def test_two_gloo_ranks_reduce_max_time(tmp_path):
     for rank, mx, val in results:
         assert float(mx) == pytest.approx(0.002)
         assert float(val) == pytest.approx(2 * 1e9 / 0.002 / 1e9)
+
+
+def test_buffer_sets_keep_every_step_out_of_l2():
+    l2 = 126 * 2**20
+    # one LayerNorm step moves 512 MiB of x and y: larger than twice the L2 by itself
+    assert bench.buffer_sets(bench.CONFIGS["ln"], l2) == 1
+    assert bench.buffer_sets(bench.CONFIGS["rms"], l2) == 1
+    # GroupNorm (64 MiB) and the small RMSNorm (1 MiB) rotate through >= 3 L2s of sets
+    for name in ("gn", "rms_small"):
+        cfg = bench.CONFIGS[name]
+        n = bench.buffer_sets(cfg, l2)
+        assert n > 1 and n * 8 * bench.elements(cfg) >= 3 * l2
+        assert (n - 1) * 8 * bench.elements(cfg) < 3 * l2
+    assert "rotate through" in bench.l2_note(bench.CONFIGS["gn"], l2)

@@ -1,8 +1,8 @@
 """GroupNorm + LeakyReLU + x2 on the GPU against the float64 oracle, element by element.
 
-Covers the vector kernel (M = 4..128, powers of two) and the warp-per-group kernel
-(M = 1, 2, 3, 48, 256, misaligned pointers), NULL affine, in-place, slopes, and the
-full-size (1024, 8192), 512-group workload.
+Covers the vector kernel (M = 4..128, powers of two) at ragged and wide shapes, the
+warp-per-group kernel (M = 1, 2, 3, 48, 256, misaligned pointers), NULL affine,
+in-place, slopes, and the full-size (1024, 8192), 512-group workload.
 """
 import numpy as np
 import pytest
@@ -91,3 +91,22 @@ def test_many_rows_fold_grid(ng):
     N, C, G = 70000, 16, 1
     x, g, b = inputs(N, C, seed=13)
     assert_parity(run_gn(ng, x, g, b, N, C, G), oracle.group_lrelu_x2(x, g, b, N, C, G), "GN 70000 rows")
+
+
+@pytest.mark.parametrize("N,C,G", [
+    (1000, 4104, 513),  # M = 8: a ragged last column block in every row
+    (5000, 64, 4),      # rows of 16 float4: most of each column block is out of range
+    (3, 12, 3),         # three float4 per row
+])
+def test_ragged_shapes(ng, N, C, G):
+    x, g, b = inputs(N, C, seed=N + C)
+    want = oracle.group_lrelu_x2(x, g, b, N, C, G)
+    assert_parity(run_gn(ng, x, g, b, N, C, G), want, f"GN N={N} C={C} G={G}")
+    assert_parity(run_gn(ng, x, g, b, N, C, G, inplace=True), want, f"GN in place N={N} C={C} G={G}")
+
+
+def test_wide_rows(ng):
+    # 16384 channels: eight column blocks per row
+    N, C, G = 9, 16384, 512
+    x, g, b = inputs(N, C, seed=21)
+    assert_parity(run_gn(ng, x, g, b, N, C, G), oracle.group_lrelu_x2(x, g, b, N, C, G), "GN C=16384")
