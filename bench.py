@@ -7,7 +7,10 @@ x ~ N(0,1), gamma ~ N(1,0.1), beta ~ N(0,0.1), eps 1e-5.  A step is one call of
 norm_layer_fwd over that batch.  K steps run back to back between one pair of
 CUDA events; no step finds its inputs in L2 (a step's x and y are larger than
 twice the L2, or the steps rotate through enough buffer sets to cover three
-L2s).  cold_launch adds the median single launch after an L2 flush.
+L2s).  cold_launch adds the median single launch after an L2 flush, and
+same_size_copy a device copy of the same x/y bytes timed the same way (the
+practical bandwidth ceiling at that transfer size).  For the smaller
+workloads per_config also reports the steps replayed from a CUDA graph.
 
 value  = algorithmic bytes per step (x read once + y written once + gamma and
          beta read once) / mean device time of a step, in GB/s, summed over
@@ -24,7 +27,8 @@ per_config: the other workloads (RMSNorm (2,64,32,32) and (112,64,512,512),
          stress) timed the same way, N=1 only.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       [--config ln|ln_stress|gn|rms|rms_small] [--no-extras]
+       [--config ln|ln_stress|gn|rms|rms_small] [--no-extras] [--cold-steps N]
+       [--rms-batch B] [--cpu-seconds S]
 Under torchrun each rank drives one GPU (RANK/LOCAL_RANK/WORLD_SIZE from env).
 """
 from __future__ import annotations
@@ -343,6 +347,39 @@ def time_cold(call, steps, flush, stream):
     return statistics.median(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
 
 
+def time_graph(calls, stream, launches_per_graph=64, replays=20):
+    """The same back-to-back steps captured once in a CUDA graph and replayed: the per-step
+    time without the host launch path.  Returns seconds per step."""
+    import torch
+    # every buffer set at least once per replay, so no step finds its inputs in L2
+    launches_per_graph = max(launches_per_graph, len(calls))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(launches_per_graph):
+            calls[i % len(calls)]()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3 / (replays * launches_per_graph)
+
+
+def time_same_size_copy(xs, ys, steps, stream):
+    """A device copy of x into y (the same bytes as one step: x read, y written), back to
+    back over the same buffer sets: the practical bandwidth ceiling at this transfer size."""
+    import torch
+    calls = [(lambda a=a, b=b: b.copy_(a)) for a, b in zip(xs, ys)]
+    sec, _, _ = time_steps(calls, steps, 5, stream)
+    return sec
+
+
 def buffer_sets(cfg, l2_bytes: int) -> int:
     """Input/output sets to rotate through so that no step finds its data in L2: one set
     when a step's x + y exceed twice the L2, else enough sets to cover three L2s."""
@@ -359,7 +396,7 @@ def check_status(ng):
 
 
 def run_config(ng, name, cfg, steps, warmup, stream, flush, l2_bytes, sampler=None, world=1, want_e2e=False,
-               cold_steps=100):
+               cold_steps=100, want_graph=False, want_copy=False):
     import torch
     x, g, b = host_inputs(cfg)
     dev = torch.device("cuda")
@@ -387,8 +424,14 @@ def run_config(ng, name, cfg, steps, warmup, stream, flush, l2_bytes, sampler=No
     check_status(ng)
     cold = time_cold(calls[0], cold_steps, flush, stream) if cold_steps else None
     check_status(ng)
+    graph = None
+    if want_graph and nset > 1:
+        graph = time_graph(calls, stream)
+        check_status(ng)
+    copy = time_same_size_copy(xs, ys, min(steps, 200), stream) if want_copy else None
     res = {"name": name, "seconds_per_step": sec, "launches_per_step": launches, "clocks": clocks,
-           "t_region_s": t1 - t0, "buffer_sets": nset, "cold_seconds_per_launch": cold}
+           "t_region_s": t1 - t0, "buffer_sets": nset, "cold_seconds_per_launch": cold,
+           "graph_seconds_per_step": graph, "copy_seconds_per_step": copy}
     if want_e2e:
         res["e2e"] = run_e2e(ng, cfg, x, g, b, xd, gd, bd, ys[0], ws, ws_bytes, stream, min(steps, 20), world)
     del xs, ys, xd, gd, bd, ws
@@ -520,6 +563,10 @@ def main(argv=None):
     ap.add_argument("--config", choices=sorted(CONFIGS), default="ln")
     ap.add_argument("--no-extras", action="store_true", help="skip the per_config measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU time budget of cpu_baseline")
+    ap.add_argument("--cold-steps", type=int, default=100,
+                    help="single launches after an L2 flush for cold_launch (0: skip)")
+    ap.add_argument("--rms-batch", type=int, default=None,
+                    help="batch B of the rms workload (default 112; smaller for profiling captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -534,6 +581,9 @@ def main(argv=None):
     import memory_bound_normalization_norm_gb300 as ng
 
     cfg = CONFIGS[args.config]
+    if args.rms_batch is not None and cfg["op"] == "rms":
+        cfg = dict(cfg, B=args.rms_batch,
+                   workload=cfg["workload"].replace(f"({cfg['B']},", f"({args.rms_batch},"))
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device="cuda")
@@ -544,7 +594,7 @@ def main(argv=None):
 
     sampler = ClockSampler(gpu_id_for(local))
     main_res = run_config(ng, args.config, cfg, args.steps, args.warmup, stream, flush, l2, sampler, world,
-                          want_e2e=True)
+                          want_e2e=True, cold_steps=args.cold_steps, want_copy=world == 1 and not args.no_extras)
     sec = dist_max(main_res["seconds_per_step"], world, device="cuda")
     nbytes = algorithmic_bytes(cfg)
     value = weak_scaling_value(nbytes, world, sec)
@@ -560,9 +610,19 @@ def main(argv=None):
                 continue
             c = CONFIGS[name]
             k = min(args.steps, 1000 if name != "rms" else 50)
-            r = run_config(ng, name, c, k, 5, stream, flush, l2, cold_steps=100 if name != "rms" else 10)
+            r = run_config(ng, name, c, k, 5, stream, flush, l2, cold_steps=100 if name != "rms" else 10,
+                           want_graph=True, want_copy=name != "rms")
             a = algorithmic_bytes(c) / r["seconds_per_step"] / 1e9
             cold = r["cold_seconds_per_launch"]
+            more = {}
+            if r["graph_seconds_per_step"]:
+                gs = r["graph_seconds_per_step"]
+                more["graph_us_per_step"] = round(gs * 1e6, 3)
+                more["graph_frac_of_measured_peak"] = round(algorithmic_bytes(c) / gs / 1e9 / peak, 4)
+            if r["copy_seconds_per_step"]:
+                cs = r["copy_seconds_per_step"]
+                more["same_size_copy_us"] = round(cs * 1e6, 3)
+                more["same_size_copy_frac_of_measured_peak"] = round(8 * elements(c) / cs / 1e9 / peak, 4)
             extras.append({"config": name, "workload": c["workload"], "steps": k,
                            "us_per_step": round(r["seconds_per_step"] * 1e6, 3),
                            "algorithmic_bytes": algorithmic_bytes(c), "achieved_gbs": round(a, 2),
@@ -570,7 +630,8 @@ def main(argv=None):
                            "elements_per_s": round(elements(c) / r["seconds_per_step"], 1),
                            "launches_per_step": r["launches_per_step"], "l2": l2_note(c, l2),
                            "cold_launch_us": round(cold * 1e6, 3),
-                           "cold_frac_of_measured_peak": round(algorithmic_bytes(c) / cold / 1e9 / peak, 4)})
+                           "cold_frac_of_measured_peak": round(algorithmic_bytes(c) / cold / 1e9 / peak, 4),
+                           **more})
 
     cpu = None
     if rank == 0 and args.cpu_seconds > 0:
@@ -585,11 +646,14 @@ def main(argv=None):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": DATA,
             "config": shape_config(args.config, cfg, l2),
             "elements_per_s": round(elements(cfg) * world / sec, 1),
-            "cold_launch": {"us": round(main_res["cold_seconds_per_launch"] * 1e6, 3),
-                            "frac_of_measured_peak": round(nbytes / main_res["cold_seconds_per_launch"] / 1e9
-                                                           / peak, 4),
-                            "note": "median single launch after an L2 flush (2x L2 written), CUDA events "
-                                    "around each launch"},
+            "same_size_copy": None if not main_res["copy_seconds_per_step"] else {
+                "us": round(main_res["copy_seconds_per_step"] * 1e6, 3),
+                "frac_of_measured_peak": round(8 * elements(cfg) / main_res["copy_seconds_per_step"] / 1e9 / peak, 4),
+                "note": "device copy of x into y (same bytes as a step minus gamma/beta), timed the same way"},
+            "cold_launch": None if not main_res["cold_seconds_per_launch"] else {
+                "us": round(main_res["cold_seconds_per_launch"] * 1e6, 3),
+                "frac_of_measured_peak": round(nbytes / main_res["cold_seconds_per_launch"] / 1e9 / peak, 4),
+                "note": "median single launch after an L2 flush (2x L2 written), CUDA events around each launch"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": peak_note, "traffic_note": traffic_note,
