@@ -80,14 +80,20 @@ typedef enum {
  *          kept until exit; such calls must then be serialized by the caller
  *          (one stream at a time).
  *
- * Rows of 2^20 or more elements (up to norm_layer_max_resident_row_len()),
- * with a length that is a multiple of 4 and 16-byte aligned x/y/gamma/beta,
- * are read from HBM once: a persistent cooperative kernel (one CTA per SM)
- * gives every CTA the same column slice of each row, holds the slice on chip
- * (shared memory, then registers) from the moment it arrives until y is
- * written, and merges the row's statistics across the GPU with one bounded
- * grid barrier per row.  Other shapes take a two-kernel path that reads x
- * twice.  Both produce the same statistics definition.
+ * Paths, all with a row length that is a multiple of 4 and 16-byte aligned
+ * x/y/gamma/beta unless stated:
+ *   - rows of at most 16,384 elements: one launch, one CTA per row at a
+ *     time with the row in registers; x is read from HBM once and the
+ *     workspace is not used;
+ *   - rows of 2^20 or more elements (up to norm_layer_max_resident_row_len()):
+ *     a persistent cooperative kernel (one CTA per SM) gives every CTA the
+ *     same column slice of each row, holds the slice on chip (shared memory,
+ *     then registers) from the moment it arrives until y is written, and
+ *     merges the row's statistics across the GPU with one bounded grid
+ *     barrier per row; x is read from HBM once;
+ *   - any other shape (including ragged lengths and misaligned pointers): a
+ *     two-kernel path that reads x twice.
+ * All produce the same statistics definition.
  */
 size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len);
 
@@ -183,14 +189,18 @@ const char *norm_status_string(norm_status_t status);
  * Process-wide knobs, read when a call launches.  Not meant to be changed
  * while other threads are launching.
  *   NORM_OPT_LN_PATH             0 = choose automatically, 1 = force the
- *                                persistent single-read kernel (error
- *                                NORM_ERR_UNSUPPORTED if the shape does not
- *                                fit), 2 = force the two-kernel path.
+ *                                persistent single-read kernel, 2 = force the
+ *                                two-kernel path, 3 = force the row kernel
+ *                                (1 and 3: error NORM_ERR_UNSUPPORTED if the
+ *                                shape does not fit).
  *   NORM_OPT_BARRIER_TIMEOUT_NS  how long a CTA waits at the LayerNorm grid
  *                                barrier (or for its own bulk copies) before
- *                                it records NORM_ERR_TIMEOUT and stops; rows
- *                                whose statistics were not merged are not
- *                                written.  Default 200 ms.
+ *                                it records NORM_ERR_TIMEOUT and stops.  CTAs
+ *                                stop independently: after a timeout every
+ *                                element of y either keeps its previous value
+ *                                or holds its correct result.  Default 200 ms;
+ *                                waits that drain a CTA's own copies before it
+ *                                exits use at least 100 ms.
  *   NORM_OPT_BARRIER_EXTRA_ARRIVALS  test hook: when > 0, the grid barrier
  *                                waits for partial statistics that no CTA
  *                                publishes, so it can only end by timing

@@ -46,8 +46,8 @@
 // never awaited.  row_base is read at kernel start and advanced by CTA 0
 // after its last merge, which proves every CTA has read it.  Every wait is
 // bounded by %globaltimer: on timeout a CTA records NORM_ERR_TIMEOUT, drains
-// its own bulk copies, frees its TMEM and returns without writing the
-// remaining rows of y.
+// its own bulk copies, frees its TMEM and returns without writing its slice
+// of the remaining rows (other CTAs may have written theirs).
 //
 // Split path (any shape): kernel 1 writes one triple per (row, chunk) CTA;
 // kernel 2 merges the row's triples and applies, re-reading x.
@@ -306,6 +306,11 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     const int buf_f4 = (p.max_n4 + 7) & ~7;
 
     const uint64_t pol_stream = policy_evict_first();
+    // Waits for this CTA's own bulk copies after a failure (drains) use at
+    // least 100 ms, whatever the configured limit: a copy always completes
+    // in microseconds, and the CTA must not exit while one still writes its
+    // shared memory.
+    const uint64_t drain_ns = p.timeout_ns > 100000000ull ? p.timeout_ns : 100000000ull;
 
     // The CTA holds all 512 TMEM columns (it is alone on its SM: its 512
     // threads at 128 registers take the whole register file).
@@ -507,7 +512,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                     const bool landed = mbar_wait_bounded(&bar_gb, static_cast<uint32_t>(h), p.timeout_ns);
                     if (issuer && !landed && ok) {
                         // drain it before anything else uses buffer 1
-                        if (!mbar_wait_bounded(&bar_gb, static_cast<uint32_t>(h), p.timeout_ns))
+                        if (!mbar_wait_bounded(&bar_gb, static_cast<uint32_t>(h), drain_ns))
                             record_error(p.err, NORM_ERR_TIMEOUT);
                     }
                     ok = ok && landed;
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 // row q landed before the statistics warps reduced it (an
                 // iteration ago); the issuer's wait returns at once and
                 // lets it account for the copy
-                if (issuer && mbar_wait_bounded(&bar_x[q & 1], x_parity(q), p.timeout_ns))
+                if (issuer && mbar_wait_bounded(&bar_x[q & 1], x_parity(q), drain_ns))
                     waited = q + 1;
                 const float4 *buf = ln_smem + (q & 1) * buf_f4;
 #pragma unroll
@@ -595,17 +600,130 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
         // Drain: never leave a bulk copy in flight into shared memory.
         if (issuer) {
             for (int64_t qq = waited; qq < issued; ++qq) {
-                if (!mbar_wait_bounded(&bar_x[qq & 1], x_parity(qq), p.timeout_ns))
+                if (!mbar_wait_bounded(&bar_x[qq & 1], x_parity(qq), drain_ns))
                     record_error(p.err, NORM_ERR_TIMEOUT);
             }
         }
     }
+    // Whichever role's wait gave up, the vote ended every role's loop: one
+    // record of the failure for the CTA.
+    if (aborted && tid == 0)
+        record_error(p.err, NORM_ERR_TIMEOUT);
     // Every TMEM access of every thread is complete before warp 0 frees it.
     tmem_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
         tmem_fence_after_sync();
         tmem_dealloc(tmem_base, LN_TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- row path
+//
+// Rows of at most LR_T * 16 float4 (16,384 elements), length a multiple of
+// 4, 16-byte aligned: one CTA per row at a time (grid-stride over rows),
+// the row in registers, so x is read from HBM once and there is no
+// workspace and a single launch.  Mean and M2 are the exact two-pass
+// definition over the registers, about the pivot K = x[r][0]:
+//   delta = sum(x - K) / L, mean = K + delta (an fp32 pair), M2 = sum((x -
+//   mean)^2).
+// Several CTAs per SM keep several rows in flight.
+
+constexpr int LR_T = 256;
+
+// Sum of v over the CTA, in a fixed order; every thread gets the result.
+// `scratch` (LR_T / 32 floats) must not be in use by the previous call.
+__device__ __forceinline__ float block_sum(float v, float *scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0)
+        scratch[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < LR_T / 32; ++w)
+        t += scratch[w];
+    return t;
+}
+
+template <int V>
+__global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
+{
+    __shared__ float red[2][LR_T / 32];
+    const int tid = threadIdx.x;
+    const int64_t L4 = p.row_len >> 2;
+    const float Lf = static_cast<float>(p.row_len);
+    const float4 *x4 = reinterpret_cast<const float4 *>(p.x);
+    float4 *y4 = reinterpret_cast<float4 *>(p.y);
+    const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma);
+    const float4 *b4 = reinterpret_cast<const float4 *>(p.beta);
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    // small rows hold gamma/beta in registers across rows; large rows load
+    // them (L2-resident) when applying
+    constexpr bool KEEP_GB = V <= 4;
+    float4 gk[KEEP_GB ? V : 1], bk[KEEP_GB ? V : 1];
+    if (KEEP_GB) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t i = tid + k * LR_T;
+            gk[k] = (g4 && i < L4) ? ld_ro_f4(g4 + i, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
+            bk[k] = (b4 && i < L4) ? ld_ro_f4(b4 + i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+        const float4 *xr = x4 + r * L4;
+        float4 v[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t i = tid + k * LR_T;
+            v[k] = i < L4 ? ld_stream_f4(xr + i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // every thread reads the pivot before any thread of the CTA stores
+        // (the block sums below are barriers), so y == x is safe
+        const float K = ld_plain_f1(p.x + r * p.row_len);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            if (tid + k * LR_T < L4)
+                s += ((v[k].x - K) + (v[k].y - K)) + ((v[k].z - K) + (v[k].w - K));
+        }
+        s = block_sum(s, red[0]);
+        Moments tot;
+        tot.n = Lf;
+        tot.mean = s / Lf;
+        tot.m2 = 0.f;
+        RowMean rm = finish_row(K, tot, p.eps);
+        float q = 0.f;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            if (tid + k * LR_T < L4) {
+                const float a = (v[k].x - rm.hi) - rm.lo, b = (v[k].y - rm.hi) - rm.lo;
+                const float c = (v[k].z - rm.hi) - rm.lo, d = (v[k].w - rm.hi) - rm.lo;
+                q += (a * a + b * b) + (c * c + d * d);
+            }
+        }
+        q = block_sum(q, red[1]);
+        rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        float4 *yr = y4 + r * L4;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t i = tid + k * LR_T;
+            if (i < L4) {
+                float4 g, b;
+                if (KEEP_GB) {
+                    g = gk[k];
+                    b = bk[k];
+                } else {
+                    g = g4 ? ld_ro_f4(g4 + i, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
+                    b = b4 ? ld_ro_f4(b4 + i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                st_stream_f4(yr + i, ln_apply4(v[k], rm, g, b), pol_stream);
+            }
+        }
     }
 }
 
@@ -734,6 +852,34 @@ cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cuda
     void *kargs[] = {&args};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ln_persistent_kernel), dim3(grid),
                                        dim3(LN_THREADS), kargs, static_cast<size_t>(dyn_smem), stream);
+}
+
+int64_t ln_rows_max_row_len()
+{
+    return int64_t(LR_T) * 16 * 4;
+}
+
+cudaError_t ln_rows_launch(const LnParams &p, int sm_count, cudaStream_t stream)
+{
+    const int64_t L4 = p.row_len / 4;
+    int64_t grid = p.rows;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 16;
+    if (grid > cap)
+        grid = cap;
+    const dim3 g(static_cast<unsigned>(grid));
+    if (L4 <= LR_T)
+        ln_rows_kernel<1><<<g, LR_T, 0, stream>>>(p);
+    else if (L4 <= 2 * LR_T)
+        ln_rows_kernel<2><<<g, LR_T, 0, stream>>>(p);
+    else if (L4 <= 4 * LR_T)
+        ln_rows_kernel<4><<<g, LR_T, 0, stream>>>(p);
+    else if (L4 <= 8 * LR_T)
+        ln_rows_kernel<8><<<g, LR_T, 0, stream>>>(p);
+    else if (L4 <= 16 * LR_T)
+        ln_rows_kernel<16><<<g, LR_T, 0, stream>>>(p);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
 }
 
 cudaError_t ln_split_launch(const LnParams &p, bool vec4, cudaStream_t stream)

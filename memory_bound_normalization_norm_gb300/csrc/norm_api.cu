@@ -234,7 +234,7 @@ norm_status_t norm_set_option(norm_option_t option, int64_t value)
         return NORM_ERR_INVALID_ARG;
     switch (option) {
     case NORM_OPT_LN_PATH:
-        if (value > 2)
+        if (value > 3)
             return NORM_ERR_INVALID_ARG;
         g_opt_ln_path = value;
         return NORM_OK;
@@ -330,7 +330,15 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
     const int64_t path_opt = g_opt_ln_path.load();
     LnPlan pl;
     bool persistent = false;
-    if (path_opt != 2 && vec4) {
+    const bool row_kernel_fits = vec4 && row_len <= normk::ln_rows_max_row_len();
+    const bool row_kernel = row_kernel_fits && (path_opt == 3 || (path_opt == 0 && row_len < kPersistentMinRowLen));
+    if (path_opt == 3 && !row_kernel)
+        return NORM_ERR_UNSUPPORTED;
+    if (row_kernel) {
+        pl.path = 3;
+        pl.ws_bytes = 0;
+    }
+    if (!row_kernel && path_opt != 2 && vec4) {
         LnPlan pp;
         if (plan_persistent(rows, row_len, *d, &pp) && (path_opt == 1 || row_len >= kPersistentMinRowLen)) {
             pl = pp;
@@ -339,7 +347,7 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
     }
     if (path_opt == 1 && !persistent)
         return NORM_ERR_UNSUPPORTED;
-    if (!persistent)
+    if (!persistent && !row_kernel)
         plan_split(rows, row_len, vec4, *d, &pl);
 
     void *ws = workspace;
@@ -387,7 +395,9 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
     p.chunk = pl.chunk;
     p.parts = pl.parts;
     cudaError_t e;
-    if (persistent) {
+    if (row_kernel) {
+        e = normk::ln_rows_launch(p, d->sm_count, stream);
+    } else if (persistent) {
         p.tag_skew = static_cast<unsigned>(g_opt_extra_arrivals.load());
         p.max_n4 = pl.max_n4;
         e = normk::ln_persistent_launch(p, pl.grid, pl.dyn_smem, stream);

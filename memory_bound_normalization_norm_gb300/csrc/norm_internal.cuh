@@ -407,6 +407,11 @@ cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cuda
 // Two-kernel LayerNorm (partials, then merge + apply); any shape.
 cudaError_t ln_split_launch(const LnParams &p, bool vec4, cudaStream_t stream);
 
+// One-launch LayerNorm for rows of at most ln_rows_max_row_len() elements
+// (a multiple of 4, 16-byte aligned pointers); no workspace.
+int64_t ln_rows_max_row_len();
+cudaError_t ln_rows_launch(const LnParams &p, int sm_count, cudaStream_t stream);
+
 // GroupNorm + LeakyReLU + x2.
 cudaError_t gn_vec4_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
                            int64_t M, float eps, float slope, cudaStream_t stream);

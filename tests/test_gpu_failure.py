@@ -1,10 +1,13 @@
-"""Failure detection of the LayerNorm grid barrier, without faulting the GPU.
+"""Failure detection of the persistent LayerNorm kernel, without faulting the GPU.
 
-The persistent kernel's grid barrier is told to wait for one arrival more than
-there are CTAs, so it can only end by running out its (2 ms) limit.  Every CTA
-must then record NORM_ERR_TIMEOUT, drain its own bulk copies and return without
-writing y; norm_last_error() reports the status and resets the library-owned
-workspace, after which a normal call works again.
+1. The grid barrier is told to wait for records no CTA publishes, so it can only
+   end by running out its (2 ms) limit.  Every CTA must record NORM_ERR_TIMEOUT,
+   drain its own bulk copies and return without writing y; norm_last_error()
+   reports the status and resets the library-owned workspace, after which a
+   normal call works again.
+2. A 1 ns limit makes the other waits give up too (a row's bulk copy, the
+   gamma/beta copies): the CTA still records the error and drains its copies;
+   every element of y is then either untouched or correct.
 """
 import pytest
 import torch
@@ -46,3 +49,41 @@ def test_barrier_timeout_is_reported_and_recoverable(ng):
     assert ng.norm_last_error() == 0
     assert_parity(yb.numpy(), oracle.layer_norm(x, None, None, rows, L), "LN after recovery")
     assert yb.guards_intact()
+
+
+def test_tiny_wait_limit_aborts_cleanly(ng):
+    """A 1 ns limit makes any wait that is not over at its first look give up: the
+    statistics warps' wait for a row's bulk copy, the apply warps' wait for gamma/beta,
+    or warp 0's poll.  Whichever gives up, the CTA must record NORM_ERR_TIMEOUT and
+    drain its copies (drains wait at least 100 ms whatever the limit).  CTAs stop
+    independently, so y may be partly written: every element is untouched or correct.
+    Then a normal call works."""
+    rows, L = 3, 152 * 4 * 64
+    x, g, b = (normgen.normal(rows * L, seed=5), normgen.normal(L, 1.0, 0.1, seed=5, tensor_id=1),
+               normgen.normal(L, 0.0, 0.1, seed=5, tensor_id=2))
+    want = oracle.layer_norm(x, g, b, rows, L).reshape(rows, L)
+    xb, gb, bb = Guarded(rows * L, x), Guarded(L, g), Guarded(L, b)
+    assert ng.norm_last_error() == 0
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, 1)
+    timeouts = 0
+    for _ in range(3):
+        yb = Guarded(rows * L)
+        ng.norm_set_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS, 1)
+        ng.norm_layer_fwd(xb.t, gb.t, bb.t, yb.t, rows, L, 1e-5)
+        st = ng.norm_last_error()
+        ng.norm_set_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS, 200_000_000)
+        assert st in (ng.NORM_OK, ng.NORM_ERR_TIMEOUT)
+        timeouts += st == ng.NORM_ERR_TIMEOUT
+        got = yb.numpy().reshape(rows, L)
+        written = (yb.t.view(torch.int32).reshape(rows, L) != 0x7FC0DEAD).cpu().numpy()
+        if st == ng.NORM_OK:
+            assert written.all()
+        # CTAs vote to stop independently, so a row may be written by some CTAs
+        # and not others: every element is untouched or correct
+        assert_parity(got[written], want[written], f"written elements after a 1 ns limit (status {st})")
+        assert yb.guards_intact()
+    assert timeouts > 0, "a 1 ns limit must make some wait give up"
+    yb = Guarded(rows * L)
+    ng.norm_layer_fwd(xb.t, gb.t, bb.t, yb.t, rows, L, 1e-5)
+    assert ng.norm_last_error() == 0
+    assert_parity(yb.numpy(), want.reshape(-1), "LN after the aborted calls")

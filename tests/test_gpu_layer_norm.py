@@ -1,8 +1,9 @@
 """LayerNorm on the GPU against the float64 oracle, element by element.
 
-Both kernels are covered: the persistent single-read kernel (forced, and chosen
-automatically for long rows) and the two-kernel split path (forced, and taken for
-ragged or misaligned rows).  Shapes span several CTAs per row with ragged slices,
+All three paths are covered: the persistent single-read kernel (forced, and chosen
+automatically for long rows), the one-launch row kernel (forced, and chosen
+automatically for rows of at most 16,384 elements) and the two-kernel split path
+(forced, and taken for ragged or misaligned rows).  Shapes span several CTAs per row with ragged slices,
 rows shorter than one float4 per CTA, the largest row the persistent kernel
 holds on chip, and the two full-size workloads: (16, 64, 256, 256) with N(0,1)
 inputs and the cancellation stress x ~ N(1000, 0.01^2).
@@ -17,7 +18,7 @@ from gpu_util import TOL, Guarded, assert_parity, device
 
 pytestmark = pytest.mark.gpu
 
-AUTO, PERSISTENT, SPLIT = 0, 1, 2
+AUTO, PERSISTENT, SPLIT, ROWS = 0, 1, 2, 3
 
 
 @pytest.fixture(scope="module")
@@ -122,9 +123,10 @@ def test_layer_norm_caller_workspace_reused(ng):
             x, g, b = inputs(rows, L, seed=seed)
             got = run_ln(ng, x, g, b, rows, L, path=path, workspace=(ws, nbytes))
             assert_parity(got, oracle.layer_norm(x, g, b, rows, L), f"LN caller workspace seed={seed}")
-    small = torch.zeros(64, dtype=torch.float32, device="cuda")
+    # a shape the two-kernel path serves needs more than 16 bytes of workspace
+    small = torch.zeros(1 << 18, dtype=torch.float32, device="cuda")
     with pytest.raises(ng.NormError) as e:
-        ng.norm_layer_fwd(small, None, None, small, 1, 64, 1e-5, ws, 16)
+        ng.norm_layer_fwd(small, None, None, small, 1, 1 << 18, 1e-5, ws, 16)
     assert e.value.status == ng.NORM_ERR_WORKSPACE
 
 
@@ -165,3 +167,45 @@ def test_layer_norm_full_size_cancellation_stress(ng, path):
     want = oracle.layer_norm(x, g, b, rows, L)
     err = assert_parity(run_ln(ng, x, g, b, rows, L, path=path), want, f"LN stress path={path}")
     assert err < TOL / 4, f"cancellation stress margin too thin: {err:.2e}"
+
+
+ROW_SHAPES = [(1, 4), (3, 12), (7, 1000), (256, 1024), (64, 4096), (33, 8192), (9, 16384), (2, 16380),
+              (3000, 64)]
+
+
+@pytest.mark.parametrize("rows,L", ROW_SHAPES)
+def test_layer_norm_row_kernel(ng, rows, L):
+    x, g, b = inputs(rows, L, seed=rows + 3 * L)
+    want = oracle.layer_norm(x, g, b, rows, L)
+    forced = run_ln(ng, x, g, b, rows, L, path=ROWS)
+    assert_parity(forced, want, f"LN row kernel {rows}x{L}")
+    # chosen automatically for these shapes: the same bits
+    assert np.array_equal(run_ln(ng, x, g, b, rows, L), forced)
+
+
+def test_layer_norm_row_kernel_stress_in_place_and_no_affine(ng):
+    rows, L = 8, 16384
+    x, _, _ = inputs(rows, L, seed=77, mean=1000.0, std=1e-2, affine=False)
+    ones, zeros = np.ones(L, np.float32), np.zeros(L, np.float32)
+    want = oracle.layer_norm(x, ones, zeros, rows, L)
+    assert_parity(run_ln(ng, x, ones, zeros, rows, L, path=ROWS), want, "LN row kernel stress")
+    assert_parity(run_ln(ng, x, None, None, rows, L, path=ROWS), want, "LN row kernel no affine")
+    assert_parity(run_ln(ng, x, None, None, rows, L, path=ROWS, inplace=True), want, "LN row kernel in place")
+
+
+@pytest.mark.parametrize("L,offset", [(16388, 0), (1002, 0), (1024, 1)])
+def test_layer_norm_row_kernel_refuses_what_it_cannot_take(ng, L, offset):
+    # longer than 16,384, not a multiple of 4, or misaligned: forced, it refuses;
+    # automatically, another path serves the shape
+    rows = 2
+    x, g, b = inputs(rows, L, seed=L)
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, ROWS)
+    try:
+        xb, yb = Guarded(rows * L, x, offset=offset), Guarded(rows * L, offset=offset)
+        with pytest.raises(ng.NormError) as e:
+            ng.norm_layer_fwd(xb.t, None, None, yb.t, rows, L, 1e-5)
+        assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_LN_PATH, AUTO)
+    assert_parity(run_ln(ng, x, g, b, rows, L, offset=offset), oracle.layer_norm(x, g, b, rows, L),
+                  f"LN auto {rows}x{L}")
