@@ -24,10 +24,11 @@ roofline.achieved / peak: the dominant kernel's algorithmic GB/s against the
 cpu_baseline: the float64 CPU oracle (test infrastructure) on the host cores.
 per_config: the other workloads (RMSNorm (2,64,32,32) and (112,64,512,512),
          GroupNorm+LeakyReLU+x2 (1024,8192)/512 groups, LayerNorm cancellation
-         stress) timed the same way, N=1 only.
+         stress, and LayerNorm over (16384, 4096) rows) timed the same way, N=1
+         only.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       [--config ln|ln_stress|gn|rms|rms_small] [--no-extras] [--cold-steps N]
+       [--config ln|ln_stress|ln_rows|gn|rms|rms_small] [--no-extras] [--cold-steps N]
        [--rms-batch B] [--cpu-seconds S]
 Under torchrun each rank drives one GPU (RANK/LOCAL_RANK/WORLD_SIZE from env).
 """
@@ -66,8 +67,12 @@ CONFIGS = {
     "ln_stress": dict(op="ln", rows=16, L=64 * 256 * 256, x=(1000.0, 1e-2), gamma="ones", beta="zeros",
                       workload="LayerNorm cancellation stress fp32 (16,64,256,256), x~N(1000,0.01^2), "
                                "gamma=1, beta=0 (passed as tensors), eps 1e-5"),
+    # beyond the five workloads above: LayerNorm over many short rows (the row kernel)
+    "ln_rows": dict(op="ln", rows=16384, L=4096, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
+                    workload="LayerNorm fp32 (16384, 4096) over the last dim, x~N(0,1), gamma~N(1,0.1), "
+                             "beta~N(0,0.1), eps 1e-5 (many short rows)"),
 }
-EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress"]
+EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_rows"]
 
 
 # ---------------------------------------------------------------------------- sizes
@@ -135,14 +140,21 @@ def host_inputs(cfg, seed=0):
     return x, g, b
 
 
+def main_kernel_name(cfg) -> str:
+    if cfg["op"] == "ln":
+        return "ln_rows_kernel" if cfg["L"] <= 16384 else "ln_persistent_kernel"
+    if cfg["op"] == "gn":
+        return "gn_vec4_kernel"
+    return "rms_reg_kernel"
+
+
 def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
     """The C-ABI call of one step (device pointers) and the number of our kernel launches it makes."""
     op = cfg["op"]
     if op == "ln":
         rows, L = cfg["rows"], cfg["L"]
-        persistent = (L % 4 == 0 and L <= ng.norm_layer_max_resident_row_len()
-                      and L >= (1 << 20))
-        return (lambda: ng.norm_layer_fwd(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if persistent else 2)
+        one_launch = L % 4 == 0 and (L <= 16384 or (1 << 20) <= L <= ng.norm_layer_max_resident_row_len())
+        return (lambda: ng.norm_layer_fwd(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if one_launch else 2)
     if op == "gn":
         return (lambda: ng.norm_group_lrelu_x2_fwd(x, g, b, y, cfg["N"], cfg["C"], cfg["G"], 1e-5, 0.01, stream)), 1
     return (lambda: ng.norm_rms_channel_fwd(x, y, cfg["B"], cfg["C"], cfg["S"], 1e-5, stream)), 1
@@ -657,7 +669,7 @@ def main(argv=None):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": peak_note, "traffic_note": traffic_note,
-                         "kernel": "ln_persistent_kernel" if cfg["op"] == "ln" else cfg["op"]},
+                         "kernel": main_kernel_name(cfg)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(weak_scaling_value(nbytes, world, e2e_sec), 3), "unit": "GB/s",
                     "h2d_bytes_per_step": main_res["e2e"]["h2d_bytes_per_step"],
