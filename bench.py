@@ -18,7 +18,8 @@ value  = algorithmic bytes per step (x read once + y written once + gamma and
          no collective on the data path).
 e2e    = the same metric with host buffers: pinned host -> device copy of
          x/gamma/beta, the call, device -> host copy of y, all inside the timed
-         region.
+         region (steps alternate between two streams so copies in the two
+         directions overlap).
 roofline.achieved / peak: the dominant kernel's algorithmic GB/s against the
          measured HBM copy bandwidth of this GPU pool.
 cpu_baseline: the float64 CPU oracle (test infrastructure) on the host cores.
@@ -452,39 +453,53 @@ def run_config(ng, name, cfg, steps, warmup, stream, flush, l2_bytes, sampler=No
 
 
 def run_e2e(ng, cfg, x, g, b, xd, gd, bd, yd, ws, ws_bytes, stream, steps, world):
-    """Host buffers in, host buffer out: pinned H2D of the inputs, the call, D2H of y."""
+    """Host buffers in, host buffer out, through the C ABI: every step copies its inputs
+    from pinned host memory (H2D), makes the call and copies y back (D2H).  Steps alternate
+    between two streams with a device buffer set each, so one step's H2D overlaps the
+    previous step's call and D2H (the copy engines run both directions at once)."""
     import torch
     xh = torch.from_numpy(x).pin_memory()
     gh = None if g is None else torch.from_numpy(g).pin_memory()
     bh = None if b is None else torch.from_numpy(b).pin_memory()
-    yh = torch.empty(xh.shape, dtype=torch.float32).pin_memory()
-    call, _ = make_call(ng, cfg, xd, gd, bd, yd, ws, ws_bytes, stream.cuda_stream)
+    yh = [torch.empty(xh.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    streams = [stream, torch.cuda.Stream()]
+    sets = [(xd, gd, bd, yd, ws)]
+    ws2 = None if ws is None else torch.zeros_like(ws)
+    sets.append((torch.empty_like(xd), None if gd is None else torch.empty_like(gd),
+                 None if bd is None else torch.empty_like(bd), torch.empty_like(yd), ws2))
+    calls = [make_call(ng, cfg, xs, gs, bs, ys, wss, ws_bytes, st.cuda_stream)[0]
+             for (xs, gs, bs, ys, wss), st in zip(sets, streams)]
     h2d = xh.numel() * 4 + (0 if gh is None else gh.numel() * 4) + (0 if bh is None else bh.numel() * 4)
-    d2h = yh.numel() * 4
+    d2h = yh[0].numel() * 4
 
-    def step():
-        with torch.cuda.stream(stream):
-            xd.copy_(xh, non_blocking=True)
+    def step(k):
+        i = k % 2
+        xs, gs, bs, ys, _ = sets[i]
+        with torch.cuda.stream(streams[i]):
+            xs.copy_(xh, non_blocking=True)
             if gh is not None:
-                gd.copy_(gh, non_blocking=True)
-                bd.copy_(bh, non_blocking=True)
-            call()
-            yh.copy_(yd, non_blocking=True)
+                gs.copy_(gh, non_blocking=True)
+                bs.copy_(bh, non_blocking=True)
+            calls[i]()
+            yh[i].copy_(ys, non_blocking=True)
 
-    for _ in range(3):
-        step()
+    for k in range(4):
+        step(k)
     torch.cuda.synchronize()
     dist_barrier(world)
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(steps):
-        step()
-    e.record(stream)
+    s.record(streams[0])
+    streams[1].wait_event(s)
+    for k in range(steps):
+        step(k)
+    streams[0].wait_stream(streams[1])
+    e.record(streams[0])
     torch.cuda.synchronize()
     dist_barrier(world)
     sec = s.elapsed_time(e) / 1e3 / steps
-    return {"seconds_per_step": sec, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+    return {"seconds_per_step": sec, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "note": "steps alternate between two streams and two device buffer sets"}
 
 
 # ---------------------------------------------------------------------------- CPU oracle timing
@@ -673,7 +688,8 @@ def main(argv=None):
             "cpu_baseline": cpu,
             "e2e": {"value": round(weak_scaling_value(nbytes, world, e2e_sec), 3), "unit": "GB/s",
                     "h2d_bytes_per_step": main_res["e2e"]["h2d_bytes_per_step"],
-                    "d2h_bytes_per_step": main_res["e2e"]["d2h_bytes_per_step"]},
+                    "d2h_bytes_per_step": main_res["e2e"]["d2h_bytes_per_step"],
+                    "ms_per_step": round(e2e_sec * 1e3, 4), "note": main_res["e2e"]["note"]},
             "gpu_launches": main_res["launches_per_step"] * args.steps,
             "clocks": main_res["clocks"],
             "per_config": extras,
