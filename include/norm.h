@@ -101,6 +101,19 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
                              int64_t rows, int64_t row_len, float eps,
                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* LayerNorm on bfloat16 tensors: x, gamma, beta and y hold bfloat16 values
+ * (the upper 16 bits of the fp32 encoding, passed as uint16_t); statistics and
+ * arithmetic are fp32, and y is rounded to nearest even once.  This is the
+ * bf16 form of the same operation; the pages work in fp32.  Same arguments,
+ * workspace and errors as norm_layer_fwd, with 2-byte elements: pointers must
+ * be 2-byte aligned, and the one-read paths want 8-byte aligned pointers and a
+ * length that is a multiple of 4.  Rows of at most 16,384 elements take the
+ * row kernel; longer rows the two-kernel path (the persistent kernel is fp32
+ * only, so NORM_OPT_LN_PATH = 1 returns NORM_ERR_UNSUPPORTED here). */
+norm_status_t norm_layer_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta, uint16_t *y,
+                                  int64_t rows, int64_t row_len, float eps,
+                                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* LayerNorm that allocates nothing.  The pages have no counterpart: this is a
  * service for callers that cannot allocate device memory at the time of the
  * call (inside an allocator's own callbacks, under a fixed memory pool, or
@@ -152,6 +165,12 @@ int64_t norm_layer_max_resident_row_len(void);
 norm_status_t norm_rms_channel_fwd(const float *x, float *y, int64_t B, int64_t C, int64_t S,
                                    float eps, cudaStream_t stream);
 
+/* RMSNorm on bfloat16 x and y (uint16_t bit patterns), fp32 arithmetic, y
+ * rounded to nearest even once; pointers 2-byte aligned.  Otherwise as
+ * norm_rms_channel_fwd. */
+norm_status_t norm_rms_channel_fwd_bf16(const uint16_t *x, uint16_t *y, int64_t B, int64_t C, int64_t S,
+                                        float eps, cudaStream_t stream);
+
 /* -------------------------------------------- GroupNorm + LeakyReLU + x + x
  * Defined by the GroupNorm page (POPCORNBENCH transcript "Kimi-K2.6 l2_p62",
  * first design turn): x[N][C] is split per row into num_groups groups of
@@ -171,6 +190,14 @@ norm_status_t norm_rms_channel_fwd(const float *x, float *y, int64_t B, int64_t 
 norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const float *beta,
                                       float *y, int64_t N, int64_t C, int64_t num_groups,
                                       float eps, float negative_slope, cudaStream_t stream);
+
+/* GroupNorm + LeakyReLU + x2 on bfloat16 x, gamma, beta and y (uint16_t bit
+ * patterns), fp32 arithmetic, y rounded to nearest even once; pointers 2-byte
+ * aligned (8-byte aligned with C % 4 == 0 for the vectorized kernel).
+ * Otherwise as norm_group_lrelu_x2_fwd. */
+norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta,
+                                           uint16_t *y, int64_t N, int64_t C, int64_t num_groups,
+                                           float eps, float negative_slope, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ status
  * Synchronize `stream`, then read and clear the current device's error word.

@@ -1,4 +1,5 @@
-"""Python binding of libnormgb300.so: fp32 reduce-then-apply normalization on GB300.
+"""Python binding of libnormgb300.so: reduce-then-apply normalization on GB300 (fp32,
+and bf16 storage with fp32 arithmetic).
 
 This module only marshals arguments into the C ABI of ``include/norm.h``; every
 step of every operation runs in the library's own CUDA kernels.  There is no CPU
@@ -11,12 +12,15 @@ Entry points (same names and argument order as the C functions):
 * ``norm_layer_fwd_noalloc(x, gamma, beta, y, rows, row_len, eps, stream=None)``
 * ``norm_rms_channel_fwd(x, y, B, C, S, eps, stream=None)``
 * ``norm_group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream=None)``
+* ``norm_layer_fwd_bf16``, ``norm_rms_channel_fwd_bf16``, ``norm_group_lrelu_x2_fwd_bf16``: the
+  same arguments with bfloat16 tensors
 * ``norm_last_error(stream=None)``, ``norm_layer_workspace_bytes(rows, row_len)``,
   ``norm_layer_workspace_reset(ws, nbytes, stream=None)``, ``norm_set_option``,
   ``norm_get_option``, ``norm_layer_max_resident_row_len()``
 
-Tensor arguments may be ``torch.Tensor`` (CUDA, float32, contiguous: their device
-pointer is passed) or plain integers holding device addresses; ``None`` is NULL.
+Tensor arguments may be ``torch.Tensor`` (CUDA, contiguous, float32 for the fp32
+entry points and bfloat16 for the ``_bf16`` ones: their device pointer is passed) or
+plain integers holding device addresses; ``None`` is NULL.
 ``stream=None`` means torch's current CUDA stream.  Non-zero status codes raise
 :class:`NormError`.  PyTorch is used only for device memory and streams.
 """
@@ -50,6 +54,9 @@ EXPORTED = (
     "norm_layer_max_resident_row_len",
     "norm_rms_channel_fwd",
     "norm_group_lrelu_x2_fwd",
+    "norm_layer_fwd_bf16",
+    "norm_rms_channel_fwd_bf16",
+    "norm_group_lrelu_x2_fwd_bf16",
     "norm_last_error",
     "norm_status_string",
     "norm_set_option",
@@ -88,6 +95,12 @@ _lib.norm_rms_channel_fwd.restype = _int
 _lib.norm_rms_channel_fwd.argtypes = [_vp, _vp, _i64, _i64, _i64, _f32, _vp]
 _lib.norm_group_lrelu_x2_fwd.restype = _int
 _lib.norm_group_lrelu_x2_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _vp]
+_lib.norm_layer_fwd_bf16.restype = _int
+_lib.norm_layer_fwd_bf16.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _f32, _vp, _sz, _vp]
+_lib.norm_rms_channel_fwd_bf16.restype = _int
+_lib.norm_rms_channel_fwd_bf16.argtypes = [_vp, _vp, _i64, _i64, _i64, _f32, _vp]
+_lib.norm_group_lrelu_x2_fwd_bf16.restype = _int
+_lib.norm_group_lrelu_x2_fwd_bf16.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _vp]
 _lib.norm_last_error.restype = _int
 _lib.norm_last_error.argtypes = [_vp]
 _lib.norm_status_string.restype = ctypes.c_char_p
@@ -102,7 +115,7 @@ def _status_string(status: int) -> str:
     return _lib.norm_status_string(int(status)).decode()
 
 
-def _ptr(a):
+def _ptr(a, bf16: bool = False):
     """Device address of a tensor argument (None -> NULL)."""
     if a is None:
         return None
@@ -111,8 +124,9 @@ def _ptr(a):
     dt = getattr(a, "dtype", None)
     if dt is not None and hasattr(a, "data_ptr"):
         import torch
-        if a.dtype != torch.float32 and a.dtype != torch.uint8:
-            raise TypeError(f"expected a float32 tensor, got {a.dtype}")
+        want = torch.bfloat16 if bf16 else torch.float32
+        if a.dtype != want and a.dtype != torch.uint8:
+            raise TypeError(f"expected a {want} tensor, got {a.dtype}")
         if not a.is_cuda:
             raise TypeError("expected a CUDA tensor (the library takes device pointers)")
         if not a.is_contiguous():
@@ -171,6 +185,23 @@ def norm_group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_s
                                         negative_slope, _stream(stream)), "norm_group_lrelu_x2_fwd")
 
 
+def norm_layer_fwd_bf16(x, gamma, beta, y, rows, row_len, eps, workspace=None, workspace_bytes=0, stream=None):
+    _check(_lib.norm_layer_fwd_bf16(_ptr(x, True), _ptr(gamma, True), _ptr(beta, True), _ptr(y, True), rows,
+                                    row_len, eps, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "norm_layer_fwd_bf16")
+
+
+def norm_rms_channel_fwd_bf16(x, y, B, C, S, eps, stream=None):
+    _check(_lib.norm_rms_channel_fwd_bf16(_ptr(x, True), _ptr(y, True), B, C, S, eps, _stream(stream)),
+           "norm_rms_channel_fwd_bf16")
+
+
+def norm_group_lrelu_x2_fwd_bf16(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream=None):
+    _check(_lib.norm_group_lrelu_x2_fwd_bf16(_ptr(x, True), _ptr(gamma, True), _ptr(beta, True), _ptr(y, True), N,
+                                             C, num_groups, eps, negative_slope, _stream(stream)),
+           "norm_group_lrelu_x2_fwd_bf16")
+
+
 def norm_last_error(stream=None) -> int:
     """Synchronize the stream; return (and clear) the device error word as a status code."""
     return int(_lib.norm_last_error(_stream(stream)))
@@ -199,8 +230,9 @@ def raw():
 
 def layer_norm(x, gamma=None, beta=None, eps: float = 1e-5, normalized_ndim: int | None = None, out=None,
                stream=None):
-    """LayerNorm of a CUDA float32 tensor over its last ``normalized_ndim`` dims
-    (default: the dims of ``gamma``, else all but the first)."""
+    """LayerNorm of a CUDA float32 or bfloat16 tensor over its last ``normalized_ndim``
+    dims (default: the dims of ``gamma``, else all but the first); gamma/beta of the
+    same dtype."""
     import torch
     if normalized_ndim is None:
         normalized_ndim = gamma.dim() if gamma is not None else x.dim() - 1
@@ -209,25 +241,28 @@ def layer_norm(x, gamma=None, beta=None, eps: float = 1e-5, normalized_ndim: int
         row_len *= int(d)
     rows = x.numel() // row_len if row_len else 0
     y = torch.empty_like(x) if out is None else out
-    norm_layer_fwd(x, gamma, beta, y, rows, row_len, eps, stream=stream)
+    fn = norm_layer_fwd_bf16 if x.dtype == torch.bfloat16 else norm_layer_fwd
+    fn(x, gamma, beta, y, rows, row_len, eps, stream=stream)
     return y
 
 
 def rms_norm_channel(x, eps: float = 1e-5, out=None, stream=None):
-    """RMSNorm over dim 1 of a CUDA float32 tensor of shape (B, C, *spatial)."""
+    """RMSNorm over dim 1 of a CUDA float32 or bfloat16 tensor of shape (B, C, *spatial)."""
     import torch
     B, C = int(x.shape[0]), int(x.shape[1])
     S = x.numel() // (B * C) if B * C else 0
     y = torch.empty_like(x) if out is None else out
-    norm_rms_channel_fwd(x, y, B, C, S, eps, stream=stream)
+    fn = norm_rms_channel_fwd_bf16 if x.dtype == torch.bfloat16 else norm_rms_channel_fwd
+    fn(x, y, B, C, S, eps, stream=stream)
     return y
 
 
 def group_norm_lrelu_x2(x, num_groups: int, gamma=None, beta=None, eps: float = 1e-5,
                         negative_slope: float = 0.01, out=None, stream=None):
-    """2 * LeakyReLU(GroupNorm(x)) for a CUDA float32 tensor of shape (N, C)."""
+    """2 * LeakyReLU(GroupNorm(x)) for a CUDA float32 or bfloat16 tensor of shape (N, C)."""
     import torch
     N, C = int(x.shape[0]), int(x.shape[1])
     y = torch.empty_like(x) if out is None else out
-    norm_group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream=stream)
+    fn = norm_group_lrelu_x2_fwd_bf16 if x.dtype == torch.bfloat16 else norm_group_lrelu_x2_fwd
+    fn(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream=stream)
     return y

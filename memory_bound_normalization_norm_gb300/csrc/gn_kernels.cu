@@ -29,9 +29,10 @@ __device__ __forceinline__ float group_sum(float v)
 }
 
 // grid: x = column blocks of GN_THREADS*U float4, y = rows (folded by gridDim.y)
-template <int TPG, int U>
-__global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const float4 *x, const float4 *__restrict__ gamma,
-                                                             const float4 *__restrict__ beta, float4 *y,
+// x, y: [N][C] of T; "vector" = 4 consecutive channels; C4 = C / 4.
+template <typename T, int TPG, int U>
+__global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T *__restrict__ gamma,
+                                                             const T *__restrict__ beta, T *y,
                                                              int64_t N, int C4, float invM, float eps,
                                                              float slope)
 {
@@ -39,8 +40,8 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const float4 *x, co
     const uint64_t pol_keep = policy_evict_last();
     const int col0 = blockIdx.x * (GN_THREADS * U) + threadIdx.x;
     for (int64_t n = blockIdx.y; n < N; n += gridDim.y) {
-        const float4 *xr = x + n * C4;
-        float4 *yr = y + n * C4;
+        const T *xr = x + n * C4 * 4;
+        T *yr = y + n * C4 * 4;
         // all loads of the row block first (x and this thread's gamma/beta), so
         // they are in flight together
         float4 v[U], g[U], b[U];
@@ -48,9 +49,9 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const float4 *x, co
         for (int u = 0; u < U; ++u) {
             const int c = col0 + u * GN_THREADS;
             const bool in = c < C4;
-            v[u] = in ? ld_stream_f4(xr + c, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
-            g[u] = (in && gamma) ? ld_ro_f4(gamma + c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
-            b[u] = (in && beta) ? ld_ro_f4(beta + c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = in ? Io<T>::ld4_stream(xr + 4 * c, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+            g[u] = (in && gamma) ? Io<T>::ld4_ro(gamma + 4 * c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
+            b[u] = (in && beta) ? Io<T>::ld4_ro(beta + 4 * c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -75,30 +76,30 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const float4 *x, co
                 t.y += t.y;
                 t.z += t.z;
                 t.w += t.w;
-                st_stream_f4(yr + c, t, pol_stream);
+                Io<T>::st4_stream(yr + 4 * c, t, pol_stream);
             }
         }
     }
 }
 
-template <int TPG, int U>
-cudaError_t launch_vec(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
+template <typename T, int TPG, int U>
+cudaError_t launch_vec(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
                        int64_t M, float eps, float slope, cudaStream_t stream)
 {
     const int C4 = static_cast<int>(C / 4);
     const int per_block = GN_THREADS * U;
     dim3 grid((C4 + per_block - 1) / per_block, static_cast<unsigned>(N < 65535 ? N : 65535));
-    gn_vec4_kernel<TPG, U><<<grid, GN_THREADS, 0, stream>>>(
-        reinterpret_cast<const float4 *>(x), reinterpret_cast<const float4 *>(gamma),
-        reinterpret_cast<const float4 *>(beta), reinterpret_cast<float4 *>(y), N, C4, 1.0f / static_cast<float>(M),
-        eps, slope);
+    gn_vec4_kernel<T, TPG, U><<<grid, GN_THREADS, 0, stream>>>(
+        static_cast<const T *>(x), static_cast<const T *>(gamma), static_cast<const T *>(beta), static_cast<T *>(y),
+        N, C4, 1.0f / static_cast<float>(M), eps, slope);
     return cudaGetLastError();
 }
 
 // Any M: one warp per (row, group); lanes stride over the group's channels.
 // Mean, then M2 about the mean (a second read that hits L1/L2), then apply.
-__global__ void __launch_bounds__(256) gn_warp_kernel(const float *x, const float *__restrict__ gamma,
-                                                      const float *__restrict__ beta, float *y, int64_t N,
+template <typename T>
+__global__ void __launch_bounds__(256) gn_warp_kernel(const T *x, const T *__restrict__ gamma,
+                                                      const T *__restrict__ beta, T *y, int64_t N,
                                                       int64_t C, int64_t G, int64_t M, float eps, float slope)
 {
     const int lane = threadIdx.x & 31;
@@ -110,14 +111,14 @@ __global__ void __launch_bounds__(256) gn_warp_kernel(const float *x, const floa
         const int64_t base = n * C + g * M;
         float s = 0.f;
         for (int64_t j = lane; j < M; j += 32)
-            s += ld_plain_f1(x + base + j);
+            s += Io<T>::ld1(x + base + j);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             s += __shfl_xor_sync(0xffffffffu, s, o);
         const float mean = s * invM;
         float q = 0.f;
         for (int64_t j = lane; j < M; j += 32) {
-            const float d = ld_plain_f1(x + base + j) - mean;
+            const float d = Io<T>::ld1(x + base + j) - mean;
             q = fmaf(d, d, q);
         }
 #pragma unroll
@@ -126,33 +127,41 @@ __global__ void __launch_bounds__(256) gn_warp_kernel(const float *x, const floa
         const float rstd = rsqrtf(fmaf(q, invM, eps));
         for (int64_t j = lane; j < M; j += 32) {
             const int64_t c = g * M + j;
-            const float gw = gamma ? gamma[c] : 1.f;
-            const float bw = beta ? beta[c] : 0.f;
-            float t = fmaf((ld_plain_f1(x + base + j) - mean) * rstd, gw, bw);
+            const float gw = gamma ? Io<T>::ld1(gamma + c) : 1.f;
+            const float bw = beta ? Io<T>::ld1(beta + c) : 0.f;
+            float t = fmaf((Io<T>::ld1(x + base + j) - mean) * rstd, gw, bw);
             t = t > 0.f ? t : slope * t;
-            y[base + j] = t + t;
+            Io<T>::st1(y + base + j, t + t);
         }
     }
 }
 
 } // namespace
 
-cudaError_t gn_vec4_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
-                           int64_t M, float eps, float slope, cudaStream_t stream)
+template <typename T>
+cudaError_t gn_vec4_launch_t(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
+                             int64_t M, float eps, float slope, cudaStream_t stream)
 {
     switch (M) {
-    case 4: return launch_vec<1, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 8: return launch_vec<2, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 16: return launch_vec<4, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 32: return launch_vec<8, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 64: return launch_vec<16, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 128: return launch_vec<32, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 4: return launch_vec<T, 1, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 8: return launch_vec<T, 2, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 16: return launch_vec<T, 4, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 32: return launch_vec<T, 8, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 64: return launch_vec<T, 16, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 128: return launch_vec<T, 32, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t gn_warp_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
-                           int64_t G, float eps, float slope, int sm_count, cudaStream_t stream)
+cudaError_t gn_vec4_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
+                           int64_t M, float eps, float slope, bool bf16, cudaStream_t stream)
+{
+    return bf16 ? gn_vec4_launch_t<__nv_bfloat16>(x, gamma, beta, y, N, C, M, eps, slope, stream)
+                : gn_vec4_launch_t<float>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+}
+
+cudaError_t gn_warp_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
+                           int64_t G, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream)
 {
     const int64_t warps_needed = N * G;
     int64_t blocks = (warps_needed + 7) / 8;
@@ -161,8 +170,14 @@ cudaError_t gn_warp_launch(const float *x, const float *gamma, const float *beta
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    gn_warp_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, gamma, beta, y, N, C, G, C / G, eps,
-                                                                       slope);
+    if (bf16)
+        gn_warp_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(gamma),
+            static_cast<const __nv_bfloat16 *>(beta), static_cast<__nv_bfloat16 *>(y), N, C, G, C / G, eps, slope);
+    else
+        gn_warp_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const float *>(x), static_cast<const float *>(gamma), static_cast<const float *>(beta),
+            static_cast<float *>(y), N, C, G, C / G, eps, slope);
     return cudaGetLastError();
 }
 

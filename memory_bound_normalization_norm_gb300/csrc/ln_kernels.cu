@@ -649,17 +649,17 @@ __device__ __forceinline__ float block_sum(float v, float *scratch)
     return t;
 }
 
-template <int V>
+template <typename T, int V>
 __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
 {
     __shared__ float red[2][LR_T / 32];
     const int tid = threadIdx.x;
-    const int64_t L4 = p.row_len >> 2;
+    const int64_t L4 = p.row_len >> 2; // 4-element vectors per row
     const float Lf = static_cast<float>(p.row_len);
-    const float4 *x4 = reinterpret_cast<const float4 *>(p.x);
-    float4 *y4 = reinterpret_cast<float4 *>(p.y);
-    const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma);
-    const float4 *b4 = reinterpret_cast<const float4 *>(p.beta);
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.y);
+    const T *gm = static_cast<const T *>(p.gamma);
+    const T *bt = static_cast<const T *>(p.beta);
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     // small rows hold gamma/beta in registers across rows; large rows load
@@ -670,21 +670,21 @@ __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t i = tid + k * LR_T;
-            gk[k] = (g4 && i < L4) ? ld_ro_f4(g4 + i, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
-            bk[k] = (b4 && i < L4) ? ld_ro_f4(b4 + i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gk[k] = (gm && i < L4) ? Io<T>::ld4_ro(gm + 4 * i, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
+            bk[k] = (bt && i < L4) ? Io<T>::ld4_ro(bt + 4 * i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
-        const float4 *xr = x4 + r * L4;
+        const T *xr = x + r * p.row_len;
         float4 v[V];
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t i = tid + k * LR_T;
-            v[k] = i < L4 ? ld_stream_f4(xr + i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[k] = i < L4 ? Io<T>::ld4_stream(xr + 4 * i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         // every thread reads the pivot before any thread of the CTA stores
         // (the block sums below are barriers), so y == x is safe
-        const float K = ld_plain_f1(p.x + r * p.row_len);
+        const float K = Io<T>::ld1(xr);
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
         }
         q = block_sum(q, red[1]);
         rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
-        float4 *yr = y4 + r * L4;
+        T *yr = y + r * p.row_len;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t i = tid + k * LR_T;
@@ -718,10 +718,10 @@ __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
                     g = gk[k];
                     b = bk[k];
                 } else {
-                    g = g4 ? ld_ro_f4(g4 + i, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
-                    b = b4 ? ld_ro_f4(b4 + i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    g = gm ? Io<T>::ld4_ro(gm + 4 * i, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
+                    b = bt ? Io<T>::ld4_ro(bt + 4 * i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                st_stream_f4(yr + i, ln_apply4(v[k], rm, g, b), pol_stream);
+                Io<T>::st4_stream(yr + 4 * i, ln_apply4(v[k], rm, g, b), pol_stream);
             }
         }
     }
@@ -731,25 +731,26 @@ __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
 
 constexpr int LS_T = 256;
 
-// One triple per (chunk p, row r) CTA.  Vector form folds each float4 as a
-// two-pass group of 4 into the thread's triple; scalar form is Welford.
-template <bool VEC>
+// One triple per (chunk p, row r) CTA.  Vector form folds each 4-element
+// vector as a two-pass group of 4 into the thread's triple; scalar form is
+// Welford.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(LS_T) ln_split_stats_kernel(LnParams p)
 {
     __shared__ Moments red[LS_T / 32];
     const int P = p.parts;
+    const T *x = static_cast<const T *>(p.x);
     for (int64_t r = blockIdx.y; r < p.rows; r += gridDim.y) {
         const int pc = blockIdx.x;
-        const float *xr = p.x + r * p.row_len;
-        const float K = ld_plain_f1(xr);
+        const T *xr = x + r * p.row_len;
+        const float K = Io<T>::ld1(xr);
         const int64_t lo = static_cast<int64_t>(pc) * p.chunk;
         const int64_t hi = (lo + p.chunk < p.row_len) ? lo + p.chunk : p.row_len;
         Moments m = {0.f, 0.f, 0.f};
         if (VEC) {
             const uint64_t pol = policy_evict_first();
-            const float4 *x4 = reinterpret_cast<const float4 *>(xr);
             for (int64_t i = lo / 4 + threadIdx.x; i < hi / 4; i += LS_T) {
-                const float4 q = ld_stream_f4(x4 + i, pol);
+                const float4 q = Io<T>::ld4_stream(xr + 4 * i, pol);
                 const float a = q.x - K, b = q.y - K, c = q.z - K, d = q.w - K;
                 Moments g;
                 g.n = 4.f;
@@ -760,7 +761,7 @@ __global__ void __launch_bounds__(LS_T) ln_split_stats_kernel(LnParams p)
             }
         } else {
             for (int64_t i = lo + threadIdx.x; i < hi; i += LS_T) {
-                const float d = ld_plain_f1(xr + i) - K;
+                const float d = Io<T>::ld1(xr + i) - K;
                 m.n += 1.f;
                 const float delta = d - m.mean;
                 m.mean += delta / m.n;
@@ -776,15 +777,19 @@ __global__ void __launch_bounds__(LS_T) ln_split_stats_kernel(LnParams p)
     }
 }
 
-template <bool VEC>
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(LS_T) ln_split_apply_kernel(LnParams p)
 {
     __shared__ RowMean row_mean;
     const int P = p.parts;
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.y);
+    const T *gm = static_cast<const T *>(p.gamma);
+    const T *bt = static_cast<const T *>(p.beta);
     for (int64_t r = blockIdx.y; r < p.rows; r += gridDim.y) {
         const int pc = blockIdx.x;
-        const float *xr = p.x + r * p.row_len;
-        float *yr = p.y + r * p.row_len;
+        const T *xr = x + r * p.row_len;
+        T *yr = y + r * p.row_len;
         if (threadIdx.x < 32) {
             const float K = ld_l2_f4(p.part + r * P).w;
             const Moments tot = merge_partials_warp(p.part + r * P, P, K);
@@ -798,21 +803,17 @@ __global__ void __launch_bounds__(LS_T) ln_split_apply_kernel(LnParams p)
         if (VEC) {
             const uint64_t pol = policy_evict_first();
             const uint64_t pol_gb = policy_evict_last();
-            const float4 *x4 = reinterpret_cast<const float4 *>(xr);
-            float4 *y4 = reinterpret_cast<float4 *>(yr);
-            const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma);
-            const float4 *b4 = reinterpret_cast<const float4 *>(p.beta);
             for (int64_t i = lo / 4 + threadIdx.x; i < hi / 4; i += LS_T) {
-                const float4 q = ld_stream_f4(x4 + i, pol);
-                const float4 g = g4 ? ld_ro_f4(g4 + i, pol_gb) : make_float4(1.f, 1.f, 1.f, 1.f);
-                const float4 bb = b4 ? ld_ro_f4(b4 + i, pol_gb) : make_float4(0.f, 0.f, 0.f, 0.f);
-                st_stream_f4(y4 + i, ln_apply4(q, rm, g, bb), pol);
+                const float4 q = Io<T>::ld4_stream(xr + 4 * i, pol);
+                const float4 g = gm ? Io<T>::ld4_ro(gm + 4 * i, pol_gb) : make_float4(1.f, 1.f, 1.f, 1.f);
+                const float4 bb = bt ? Io<T>::ld4_ro(bt + 4 * i, pol_gb) : make_float4(0.f, 0.f, 0.f, 0.f);
+                Io<T>::st4_stream(yr + 4 * i, ln_apply4(q, rm, g, bb), pol);
             }
         } else {
             for (int64_t i = lo + threadIdx.x; i < hi; i += LS_T) {
-                const float g = p.gamma ? p.gamma[i] : 1.f;
-                const float bb = p.beta ? p.beta[i] : 0.f;
-                yr[i] = fmaf(((ld_plain_f1(xr + i) - rm.hi) - rm.lo) * rm.rstd, g, bb);
+                const float g = gm ? Io<T>::ld1(gm + i) : 1.f;
+                const float bb = bt ? Io<T>::ld1(bt + i) : 0.f;
+                Io<T>::st1(yr + i, fmaf(((Io<T>::ld1(xr + i) - rm.hi) - rm.lo) * rm.rstd, g, bb));
             }
         }
         __syncthreads();
@@ -859,7 +860,8 @@ int64_t ln_rows_max_row_len()
     return int64_t(LR_T) * 16 * 4;
 }
 
-cudaError_t ln_rows_launch(const LnParams &p, int sm_count, cudaStream_t stream)
+template <typename T>
+cudaError_t ln_rows_launch_t(const LnParams &p, int sm_count, cudaStream_t stream)
 {
     const int64_t L4 = p.row_len / 4;
     int64_t grid = p.rows;
@@ -868,31 +870,42 @@ cudaError_t ln_rows_launch(const LnParams &p, int sm_count, cudaStream_t stream)
         grid = cap;
     const dim3 g(static_cast<unsigned>(grid));
     if (L4 <= LR_T)
-        ln_rows_kernel<1><<<g, LR_T, 0, stream>>>(p);
+        ln_rows_kernel<T, 1><<<g, LR_T, 0, stream>>>(p);
     else if (L4 <= 2 * LR_T)
-        ln_rows_kernel<2><<<g, LR_T, 0, stream>>>(p);
+        ln_rows_kernel<T, 2><<<g, LR_T, 0, stream>>>(p);
     else if (L4 <= 4 * LR_T)
-        ln_rows_kernel<4><<<g, LR_T, 0, stream>>>(p);
+        ln_rows_kernel<T, 4><<<g, LR_T, 0, stream>>>(p);
     else if (L4 <= 8 * LR_T)
-        ln_rows_kernel<8><<<g, LR_T, 0, stream>>>(p);
+        ln_rows_kernel<T, 8><<<g, LR_T, 0, stream>>>(p);
     else if (L4 <= 16 * LR_T)
-        ln_rows_kernel<16><<<g, LR_T, 0, stream>>>(p);
+        ln_rows_kernel<T, 16><<<g, LR_T, 0, stream>>>(p);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 
-cudaError_t ln_split_launch(const LnParams &p, bool vec4, cudaStream_t stream)
+cudaError_t ln_rows_launch(const LnParams &p, bool bf16, int sm_count, cudaStream_t stream)
+{
+    return bf16 ? ln_rows_launch_t<__nv_bfloat16>(p, sm_count, stream) : ln_rows_launch_t<float>(p, sm_count, stream);
+}
+
+template <typename T>
+cudaError_t ln_split_launch_t(const LnParams &p, bool vec4, cudaStream_t stream)
 {
     dim3 grid(static_cast<unsigned>(p.parts), static_cast<unsigned>(p.rows < 65535 ? p.rows : 65535));
     if (vec4) {
-        ln_split_stats_kernel<true><<<grid, LS_T, 0, stream>>>(p);
-        ln_split_apply_kernel<true><<<grid, LS_T, 0, stream>>>(p);
+        ln_split_stats_kernel<T, true><<<grid, LS_T, 0, stream>>>(p);
+        ln_split_apply_kernel<T, true><<<grid, LS_T, 0, stream>>>(p);
     } else {
-        ln_split_stats_kernel<false><<<grid, LS_T, 0, stream>>>(p);
-        ln_split_apply_kernel<false><<<grid, LS_T, 0, stream>>>(p);
+        ln_split_stats_kernel<T, false><<<grid, LS_T, 0, stream>>>(p);
+        ln_split_apply_kernel<T, false><<<grid, LS_T, 0, stream>>>(p);
     }
     return cudaGetLastError();
+}
+
+cudaError_t ln_split_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_t stream)
+{
+    return bf16 ? ln_split_launch_t<__nv_bfloat16>(p, vec4, stream) : ln_split_launch_t<float>(p, vec4, stream);
 }
 
 } // namespace normk

@@ -300,10 +300,15 @@ norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStre
     return NORM_OK;
 }
 
-norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *beta, float *y, int64_t rows,
-                             int64_t row_len, float eps, void *workspace, size_t workspace_bytes,
-                             cudaStream_t stream)
+} // extern "C"
+
+namespace {
+
+// LayerNorm on tensors of esz-byte elements: 4 = fp32, 2 = bf16.
+norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void *y, int64_t rows, int64_t row_len,
+                        float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream, int esz)
 {
+    const bool bf16 = esz == 2;
     int64_t n = 0;
     if (rows < 0 || row_len < 0 || !valid_eps(eps) || !safe_mul(rows, row_len, &n))
         return NORM_ERR_INVALID_ARG;
@@ -311,9 +316,9 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
         return NORM_OK;
     if (!x || !y)
         return NORM_ERR_INVALID_ARG;
-    if (!aligned(x, 4) || !aligned(y, 4) || !aligned(gamma, 4) || !aligned(beta, 4))
+    if (!aligned(x, esz) || !aligned(y, esz) || !aligned(gamma, esz) || !aligned(beta, esz))
         return NORM_ERR_MISALIGNED;
-    const size_t nb = static_cast<size_t>(n) * 4u, pb = static_cast<size_t>(row_len) * 4u;
+    const size_t nb = static_cast<size_t>(n) * esz, pb = static_cast<size_t>(row_len) * esz;
     if ((x != y && overlaps(x, nb, y, nb)) || overlaps(gamma, pb, y, nb) || overlaps(beta, pb, y, nb))
         return NORM_ERR_INVALID_ARG;
     if (workspace && (!aligned(workspace, 256) || overlaps(workspace, workspace_bytes, y, nb) ||
@@ -325,8 +330,9 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
     if (st != NORM_OK)
         return st;
 
-    const bool vec4 = (row_len & 3) == 0 && aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
-                      aligned(beta, 16);
+    const uintptr_t va = 4u * esz; // alignment of a 4-element vector
+    const bool vec4 = (row_len & 3) == 0 && aligned(x, va) && aligned(y, va) && aligned(gamma, va) &&
+                      aligned(beta, va);
     const int64_t path_opt = g_opt_ln_path.load();
     LnPlan pl;
     bool persistent = false;
@@ -338,7 +344,10 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
         pl.path = 3;
         pl.ws_bytes = 0;
     }
-    if (!row_kernel && path_opt != 2 && vec4) {
+    // the persistent kernel is fp32 only
+    if (path_opt == 1 && bf16)
+        return NORM_ERR_UNSUPPORTED;
+    if (!row_kernel && path_opt != 2 && vec4 && !bf16) {
         LnPlan pp;
         if (plan_persistent(rows, row_len, *d, &pp) && (path_opt == 1 || row_len >= kPersistentMinRowLen)) {
             pl = pp;
@@ -396,13 +405,13 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
     p.parts = pl.parts;
     cudaError_t e;
     if (row_kernel) {
-        e = normk::ln_rows_launch(p, d->sm_count, stream);
+        e = normk::ln_rows_launch(p, bf16, d->sm_count, stream);
     } else if (persistent) {
         p.tag_skew = static_cast<unsigned>(g_opt_extra_arrivals.load());
         p.max_n4 = pl.max_n4;
         e = normk::ln_persistent_launch(p, pl.grid, pl.dyn_smem, stream);
     } else {
-        e = normk::ln_split_launch(p, pl.vec4, stream);
+        e = normk::ln_split_launch(p, bf16, pl.vec4, stream);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -411,8 +420,9 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
     return NORM_OK;
 }
 
-norm_status_t norm_rms_channel_fwd(const float *x, float *y, int64_t B, int64_t C, int64_t S, float eps,
-                                   cudaStream_t stream)
+// RMSNorm on tensors of esz-byte elements.
+norm_status_t rms_channel_fwd(const void *x, void *y, int64_t B, int64_t C, int64_t S, float eps,
+                              cudaStream_t stream, int esz)
 {
     int64_t bc = 0, n = 0;
     if (B < 0 || C < 0 || S < 0 || !valid_eps(eps) || !safe_mul(B, C, &bc) || !safe_mul(bc, S, &n))
@@ -421,25 +431,25 @@ norm_status_t norm_rms_channel_fwd(const float *x, float *y, int64_t B, int64_t 
         return NORM_OK;
     if (!x || !y)
         return NORM_ERR_INVALID_ARG;
-    if (!aligned(x, 4) || !aligned(y, 4))
+    if (!aligned(x, esz) || !aligned(y, esz))
         return NORM_ERR_MISALIGNED;
-    const size_t nb = static_cast<size_t>(n) * 4u;
+    const size_t nb = static_cast<size_t>(n) * esz;
     if (x != y && overlaps(x, nb, y, nb))
         return NORM_ERR_INVALID_ARG;
     DeviceState *d = nullptr;
     norm_status_t st = device_state(&d);
     if (st != NORM_OK)
         return st;
-    if (normk::rms_channel_launch(x, y, B, C, S, eps, stream) != cudaSuccess) {
+    if (normk::rms_channel_launch(x, y, B, C, S, eps, esz == 2, stream) != cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
     }
     return NORM_OK;
 }
 
-norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const float *beta, float *y, int64_t N,
-                                      int64_t C, int64_t num_groups, float eps, float negative_slope,
-                                      cudaStream_t stream)
+// GroupNorm + LeakyReLU + x2 on tensors of esz-byte elements.
+norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
+                                 int64_t num_groups, float eps, float negative_slope, cudaStream_t stream, int esz)
 {
     int64_t n = 0;
     if (N < 0 || C < 0 || num_groups <= 0 || !valid_eps(eps) || !std::isfinite(negative_slope) ||
@@ -451,9 +461,9 @@ norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const 
         return NORM_OK;
     if (!x || !y)
         return NORM_ERR_INVALID_ARG;
-    if (!aligned(x, 4) || !aligned(y, 4) || !aligned(gamma, 4) || !aligned(beta, 4))
+    if (!aligned(x, esz) || !aligned(y, esz) || !aligned(gamma, esz) || !aligned(beta, esz))
         return NORM_ERR_MISALIGNED;
-    const size_t nb = static_cast<size_t>(n) * 4u, pb = static_cast<size_t>(C) * 4u;
+    const size_t nb = static_cast<size_t>(n) * esz, pb = static_cast<size_t>(C) * esz;
     if ((x != y && overlaps(x, nb, y, nb)) || overlaps(gamma, pb, y, nb) || overlaps(beta, pb, y, nb))
         return NORM_ERR_INVALID_ARG;
     DeviceState *d = nullptr;
@@ -462,16 +472,62 @@ norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const 
         return st;
     const int64_t M = C / num_groups;
     const bool pow2 = M >= 4 && M <= 128 && (M & (M - 1)) == 0;
-    const bool vec = pow2 && (C & 3) == 0 && C / 4 < (int64_t(1) << 30) && aligned(x, 16) && aligned(y, 16) &&
-                     aligned(gamma, 16) && aligned(beta, 16);
-    cudaError_t e = vec ? normk::gn_vec4_launch(x, gamma, beta, y, N, C, M, eps, negative_slope, stream)
-                        : normk::gn_warp_launch(x, gamma, beta, y, N, C, num_groups, eps, negative_slope,
+    const uintptr_t va = 4u * esz;
+    const bool vec = pow2 && (C & 3) == 0 && C / 4 < (int64_t(1) << 30) && aligned(x, va) && aligned(y, va) &&
+                     aligned(gamma, va) && aligned(beta, va);
+    const bool bf16 = esz == 2;
+    cudaError_t e = vec ? normk::gn_vec4_launch(x, gamma, beta, y, N, C, M, eps, negative_slope, bf16, stream)
+                        : normk::gn_warp_launch(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, bf16,
                                                 d->sm_count, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
     }
     return NORM_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *beta, float *y, int64_t rows,
+                             int64_t row_len, float eps, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream)
+{
+    return layer_fwd(x, gamma, beta, y, rows, row_len, eps, workspace, workspace_bytes, stream, 4);
+}
+
+norm_status_t norm_layer_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta, uint16_t *y,
+                                  int64_t rows, int64_t row_len, float eps, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream)
+{
+    return layer_fwd(x, gamma, beta, y, rows, row_len, eps, workspace, workspace_bytes, stream, 2);
+}
+
+norm_status_t norm_rms_channel_fwd(const float *x, float *y, int64_t B, int64_t C, int64_t S, float eps,
+                                   cudaStream_t stream)
+{
+    return rms_channel_fwd(x, y, B, C, S, eps, stream, 4);
+}
+
+norm_status_t norm_rms_channel_fwd_bf16(const uint16_t *x, uint16_t *y, int64_t B, int64_t C, int64_t S, float eps,
+                                        cudaStream_t stream)
+{
+    return rms_channel_fwd(x, y, B, C, S, eps, stream, 2);
+}
+
+norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const float *beta, float *y, int64_t N,
+                                      int64_t C, int64_t num_groups, float eps, float negative_slope,
+                                      cudaStream_t stream)
+{
+    return group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream, 4);
+}
+
+norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta,
+                                           uint16_t *y, int64_t N, int64_t C, int64_t num_groups, float eps,
+                                           float negative_slope, cudaStream_t stream)
+{
+    return group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream, 2);
 }
 
 norm_status_t norm_last_error(cudaStream_t stream)

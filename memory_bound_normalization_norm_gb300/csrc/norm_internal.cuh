@@ -2,6 +2,7 @@
 // kernels of libnormgb300 (sm_103a).  Inline PTX only; no library kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -238,6 +239,93 @@ __device__ __forceinline__ void bar_sync_named(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ---------------------------------------------------------------- element types
+// Io<T> moves elements of type T (float, or __nv_bfloat16 with fp32
+// arithmetic) between memory and fp32 registers.  The 4-element forms need
+// p aligned to 4 elements (16 bytes for fp32, 8 for bf16).  bf16 -> fp32 is
+// exact; fp32 -> bf16 rounds to nearest even (CUDA's __float2bfloat16_rn).
+template <typename T>
+struct Io;
+
+template <>
+struct Io<float> {
+    static __device__ __forceinline__ float4 ld4_stream(const float *p, uint64_t pol)
+    {
+        return ld_stream_f4(reinterpret_cast<const float4 *>(p), pol);
+    }
+    static __device__ __forceinline__ float4 ld4_ro(const float *p, uint64_t pol)
+    {
+        return ld_ro_f4(reinterpret_cast<const float4 *>(p), pol);
+    }
+    static __device__ __forceinline__ void st4_stream(float *p, float4 v, uint64_t pol)
+    {
+        st_stream_f4(reinterpret_cast<float4 *>(p), v, pol);
+    }
+    static __device__ __forceinline__ float ld1(const float *p) { return ld_plain_f1(p); }
+    static __device__ __forceinline__ float ld1_stream(const float *p, uint64_t pol) { return ld_stream_f1(p, pol); }
+    static __device__ __forceinline__ void st1(float *p, float v) { *p = v; }
+    static __device__ __forceinline__ void st1_stream(float *p, float v, uint64_t pol) { st_stream_f1(p, v, pol); }
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+template <>
+struct Io<__nv_bfloat16> {
+    static __device__ __forceinline__ float4 unpack(uint32_t a, uint32_t b)
+    {
+        return make_float4(bf16_bits_to_f32(a & 0xffffu), bf16_bits_to_f32(a >> 16), bf16_bits_to_f32(b & 0xffffu),
+                           bf16_bits_to_f32(b >> 16));
+    }
+    static __device__ __forceinline__ float4 ld4_stream(const __nv_bfloat16 *p, uint64_t pol)
+    {
+        uint32_t a, b;
+        asm("ld.global.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+            : "=r"(a), "=r"(b)
+            : "l"(p), "l"(pol));
+        return unpack(a, b);
+    }
+    static __device__ __forceinline__ float4 ld4_ro(const __nv_bfloat16 *p, uint64_t pol)
+    {
+        uint32_t a, b;
+        asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+            : "=r"(a), "=r"(b)
+            : "l"(p), "l"(pol));
+        return unpack(a, b);
+    }
+    static __device__ __forceinline__ void st4_stream(__nv_bfloat16 *p, float4 v, uint64_t pol)
+    {
+        asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p),
+                     "r"(pack_bf16x2(v.x, v.y)), "r"(pack_bf16x2(v.z, v.w)), "l"(pol)
+                     : "memory");
+    }
+    static __device__ __forceinline__ float ld1(const __nv_bfloat16 *p)
+    {
+        unsigned short h;
+        asm("ld.global.u16 %0, [%1];" : "=h"(h) : "l"(p));
+        return bf16_bits_to_f32(h);
+    }
+    static __device__ __forceinline__ float ld1_stream(const __nv_bfloat16 *p, uint64_t pol)
+    {
+        unsigned short h;
+        asm("ld.global.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(h) : "l"(p), "l"(pol));
+        return bf16_bits_to_f32(h);
+    }
+    static __device__ __forceinline__ void st1(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+    static __device__ __forceinline__ void st1_stream(__nv_bfloat16 *p, float v, uint64_t pol)
+    {
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        const unsigned short h = *reinterpret_cast<const unsigned short *>(&b);
+        asm volatile("st.global.L1::no_allocate.L2::cache_hint.u16 [%0], %1, %2;" ::"l"(p), "h"(h), "l"(pol)
+                     : "memory");
+    }
+};
+
 // ---------------------------------------------------------------- tensor memory
 // Tensor memory (TMEM) is a 128-lane x 512-column array of 32-bit cells per
 // SM.  An address is (lane << 16) | column.  A warp reaches only the 32
@@ -370,11 +458,13 @@ struct LnSync {
 };
 static_assert(sizeof(LnSync) == 256, "LnSync must be 256 bytes");
 
+// Tensors are fp32 (float) or bf16 (__nv_bfloat16) in memory; the kernel
+// templated on the element type casts these.
 struct LnParams {
-    const float *x;
-    const float *gamma; // may be null
-    const float *beta;  // may be null
-    float *y;
+    const void *x;
+    const void *gamma; // may be null
+    const void *beta;  // may be null
+    void *y;
     int64_t rows;
     int64_t row_len; // elements
     float eps;
@@ -404,22 +494,24 @@ cudaError_t ln_persistent_setup(int max_dynamic_smem);
 cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm);
 cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream);
 
-// Two-kernel LayerNorm (partials, then merge + apply); any shape.
-cudaError_t ln_split_launch(const LnParams &p, bool vec4, cudaStream_t stream);
+// Two-kernel LayerNorm (partials, then merge + apply); any shape.  bf16:
+// the tensors are bf16, else fp32.  vec4: rows are a multiple of 4 elements
+// and the pointers 4-element aligned.
+cudaError_t ln_split_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_t stream);
 
 // One-launch LayerNorm for rows of at most ln_rows_max_row_len() elements
-// (a multiple of 4, 16-byte aligned pointers); no workspace.
+// (a multiple of 4, 4-element aligned pointers); no workspace.
 int64_t ln_rows_max_row_len();
-cudaError_t ln_rows_launch(const LnParams &p, int sm_count, cudaStream_t stream);
+cudaError_t ln_rows_launch(const LnParams &p, bool bf16, int sm_count, cudaStream_t stream);
 
-// GroupNorm + LeakyReLU + x2.
-cudaError_t gn_vec4_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
-                           int64_t M, float eps, float slope, cudaStream_t stream);
-cudaError_t gn_warp_launch(const float *x, const float *gamma, const float *beta, float *y, int64_t N, int64_t C,
-                           int64_t G, float eps, float slope, int sm_count, cudaStream_t stream);
+// GroupNorm + LeakyReLU + x2 (bf16: the tensors are bf16, else fp32).
+cudaError_t gn_vec4_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
+                           int64_t M, float eps, float slope, bool bf16, cudaStream_t stream);
+cudaError_t gn_warp_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
+                           int64_t G, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream);
 
-// RMSNorm over dim 1 of [B][C][S].
-cudaError_t rms_channel_launch(const float *x, float *y, int64_t B, int64_t C, int64_t S, float eps,
+// RMSNorm over dim 1 of [B][C][S] (bf16: the tensors are bf16, else fp32).
+cudaError_t rms_channel_launch(const void *x, void *y, int64_t B, int64_t C, int64_t S, float eps, bool bf16,
                                cudaStream_t stream);
 
 } // namespace normk

@@ -22,8 +22,8 @@ constexpr int RMS_THREADS = 128;
 // at once would cost 2*CMAX registers.
 // Register cap: exact C <= 64 fits in 128 registers (4 CTAs of 128 threads
 // per SM); C = 128 and the predicated (C < CMAX) forms get up to 255.
-template <int CMAX, bool EXACT>
-__global__ void __launch_bounds__(RMS_THREADS, (EXACT && CMAX <= 64) ? 4 : 2) rms_reg_kernel(const float *x, float *y, int64_t B, int C,
+template <typename T, int CMAX, bool EXACT>
+__global__ void __launch_bounds__(RMS_THREADS, (EXACT && CMAX <= 64) ? 4 : 2) rms_reg_kernel(const T *x, T *y, int64_t B, int C,
                                                                  int64_t S, float invC, float eps)
 {
     const uint64_t pol = policy_evict_first();
@@ -31,11 +31,11 @@ __global__ void __launch_bounds__(RMS_THREADS, (EXACT && CMAX <= 64) ? 4 : 2) rm
     if (s >= S)
         return;
     for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
-        const float *xp = x + b * C * S + s;
+        const T *xp = x + b * C * S + s;
         float v[CMAX];
 #pragma unroll
         for (int c = 0; c < CMAX; ++c) {
-            v[c] = (EXACT || c < C) ? ld_stream_f1(xp, pol) : 0.f;
+            v[c] = (EXACT || c < C) ? Io<T>::ld1_stream(xp, pol) : 0.f;
             xp += S;
         }
         // four independent partial sums, combined in a fixed order
@@ -51,76 +51,86 @@ __global__ void __launch_bounds__(RMS_THREADS, (EXACT && CMAX <= 64) ? 4 : 2) rm
                 a3 = fmaf(v[c + 3], v[c + 3], a3);
         }
         const float inv = rsqrtf(fmaf((a0 + a1) + (a2 + a3), invC, eps));
-        float *yp = y + b * C * S + s;
+        T *yp = y + b * C * S + s;
 #pragma unroll
         for (int c = 0; c < CMAX; ++c) {
             if (EXACT || c < C)
-                st_stream_f1(yp, v[c] * inv, pol);
+                Io<T>::st1_stream(yp, v[c] * inv, pol);
             yp += S;
         }
     }
 }
 
 // Any C: sum of squares in one pass, then a second pass re-reads x to scale.
-__global__ void __launch_bounds__(RMS_THREADS) rms_generic_kernel(const float *x, float *y, int64_t B, int64_t C,
+template <typename T>
+__global__ void __launch_bounds__(RMS_THREADS) rms_generic_kernel(const T *x, T *y, int64_t B, int64_t C,
                                                                   int64_t S, float invC, float eps)
 {
     const int64_t s = static_cast<int64_t>(blockIdx.x) * RMS_THREADS + threadIdx.x;
     if (s >= S)
         return;
     for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
-        const float *xp = x + b * C * S + s;
-        float *yp = y + b * C * S + s;
+        const T *xp = x + b * C * S + s;
+        T *yp = y + b * C * S + s;
         float a = 0.f;
         for (int64_t c = 0; c < C; ++c) {
-            const float v = ld_plain_f1(xp + c * S);
+            const float v = Io<T>::ld1(xp + c * S);
             a = fmaf(v, v, a);
         }
         const float inv = rsqrtf(fmaf(a, invC, eps));
         for (int64_t c = 0; c < C; ++c)
-            yp[c * S] = ld_plain_f1(xp + c * S) * inv;
+            Io<T>::st1(yp + c * S, Io<T>::ld1(xp + c * S) * inv);
     }
 }
 
-template <int CMAX>
-cudaError_t launch_reg(const float *x, float *y, int64_t B, int64_t C, int64_t S, float eps, cudaStream_t stream)
+template <typename T, int CMAX>
+cudaError_t launch_reg(const T *x, T *y, int64_t B, int64_t C, int64_t S, float eps, cudaStream_t stream)
 {
     const int64_t bx = (S + RMS_THREADS - 1) / RMS_THREADS;
     if (bx > 0x7fffffff)
         return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(B < 65535 ? B : 65535));
     if (C == CMAX)
-        rms_reg_kernel<CMAX, true><<<grid, RMS_THREADS, 0, stream>>>(x, y, B, static_cast<int>(C), S,
+        rms_reg_kernel<T, CMAX, true><<<grid, RMS_THREADS, 0, stream>>>(x, y, B, static_cast<int>(C), S,
                                                                      1.0f / static_cast<float>(C), eps);
     else
-        rms_reg_kernel<CMAX, false><<<grid, RMS_THREADS, 0, stream>>>(x, y, B, static_cast<int>(C), S,
+        rms_reg_kernel<T, CMAX, false><<<grid, RMS_THREADS, 0, stream>>>(x, y, B, static_cast<int>(C), S,
                                                                       1.0f / static_cast<float>(C), eps);
     return cudaGetLastError();
 }
 
 } // namespace
 
-cudaError_t rms_channel_launch(const float *x, float *y, int64_t B, int64_t C, int64_t S, float eps,
-                               cudaStream_t stream)
+template <typename T>
+cudaError_t rms_channel_launch_t(const T *x, T *y, int64_t B, int64_t C, int64_t S, float eps, cudaStream_t stream)
 {
     if (C <= 4)
-        return launch_reg<4>(x, y, B, C, S, eps, stream);
+        return launch_reg<T, 4>(x, y, B, C, S, eps, stream);
     if (C <= 8)
-        return launch_reg<8>(x, y, B, C, S, eps, stream);
+        return launch_reg<T, 8>(x, y, B, C, S, eps, stream);
     if (C <= 16)
-        return launch_reg<16>(x, y, B, C, S, eps, stream);
+        return launch_reg<T, 16>(x, y, B, C, S, eps, stream);
     if (C <= 32)
-        return launch_reg<32>(x, y, B, C, S, eps, stream);
+        return launch_reg<T, 32>(x, y, B, C, S, eps, stream);
     if (C <= 64)
-        return launch_reg<64>(x, y, B, C, S, eps, stream);
+        return launch_reg<T, 64>(x, y, B, C, S, eps, stream);
     if (C <= 128)
-        return launch_reg<128>(x, y, B, C, S, eps, stream);
+        return launch_reg<T, 128>(x, y, B, C, S, eps, stream);
     const int64_t bx = (S + RMS_THREADS - 1) / RMS_THREADS;
     if (bx > 0x7fffffff)
         return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(B < 65535 ? B : 65535));
-    rms_generic_kernel<<<grid, RMS_THREADS, 0, stream>>>(x, y, B, C, S, 1.0f / static_cast<float>(C), eps);
+    rms_generic_kernel<T><<<grid, RMS_THREADS, 0, stream>>>(x, y, B, C, S, 1.0f / static_cast<float>(C), eps);
     return cudaGetLastError();
+}
+
+cudaError_t rms_channel_launch(const void *x, void *y, int64_t B, int64_t C, int64_t S, float eps, bool bf16,
+                               cudaStream_t stream)
+{
+    if (bf16)
+        return rms_channel_launch_t(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y), B, C, S,
+                                    eps, stream);
+    return rms_channel_launch_t(static_cast<const float *>(x), static_cast<float *>(y), B, C, S, eps, stream);
 }
 
 } // namespace normk

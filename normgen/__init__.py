@@ -109,3 +109,20 @@ def word(seed: int, tensor_id: int, k: int) -> int:
 def splitmix64_output(s0: int, k: int) -> int:
     """The k-th output of a plain SplitMix64 generator seeded with ``s0``."""
     return int(_load().normgen_splitmix64_output(s0, k))
+
+
+def bf16_bits(a) -> np.ndarray:
+    """bfloat16 encodings (uint16) of finite float32 values, rounded to nearest even:
+    the upper 16 bits of the float32 encoding after adding 0x7FFF plus the lowest kept bit."""
+    u = np.ascontiguousarray(a, dtype=np.float32).reshape(-1).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def bf16_to_f32(h) -> np.ndarray:
+    """float32 values of bfloat16 encodings (exact)."""
+    return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def round_bf16(a) -> np.ndarray:
+    """float32 values rounded to the nearest bfloat16 (ties to even), as float32."""
+    return bf16_to_f32(bf16_bits(a))

@@ -1,0 +1,164 @@
+"""The bfloat16 entry points on the GPU against the float64 oracle, element by element.
+
+Inputs are the seeded float32 streams rounded to bfloat16, so the oracle sees exactly
+the values the GPU reads.  The GPU computes in fp32 and rounds y to bfloat16 once;
+the oracle's float64 result is not rounded.  The bound per element is therefore the
+bfloat16 rounding of the result, 2^-8 |y_ref| (half an ulp of 8 significant bits),
+plus the fp32 tolerance of the fp32 entry points, 1e-4 (1 + |y_ref|).
+
+Covered: LayerNorm through the row kernel and the two-kernel path (vector and scalar
+forms, long rows, misaligned pointers, in place, NULL affine, the full (16, 64, 256,
+256) shape), RMSNorm (several channel counts, in place, the (2, 64, 32, 32)
+workload), GroupNorm + LeakyReLU + x2 (vector and warp kernels, the (1024, 8192)
+workload), and guard zones around every output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import normgen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 64
+SENTINEL = 0x7FC1  # a bfloat16 NaN no kernel writes
+
+
+@pytest.fixture(scope="module")
+def ng():
+    import memory_bound_normalization_norm_gb300 as m
+    yield m
+    m.norm_set_option(m.NORM_OPT_LN_PATH, 0)
+
+
+class BGuarded:
+    """A bfloat16 device buffer of n elements between two guard zones of SENTINEL."""
+
+    def __init__(self, n: int, init=None, offset: int = 0):
+        self.n, self.lo = int(n), GUARD + offset
+        bits = np.full(self.n + 2 * GUARD + offset, SENTINEL, dtype=np.uint16)
+        if init is not None:
+            bits[self.lo:self.lo + self.n] = normgen.bf16_bits(init)
+        self.buf = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+        self.t = self.buf[self.lo:self.lo + self.n]
+
+    def values(self) -> np.ndarray:
+        return normgen.bf16_to_f32(self.t.view(torch.int16).cpu().numpy().view(np.uint16))
+
+    def guards_intact(self) -> bool:
+        bits = self.buf.view(torch.int16).cpu().numpy().view(np.uint16)
+        return bool((bits[:self.lo] == SENTINEL).all() and (bits[self.lo + self.n:] == SENTINEL).all())
+
+
+def assert_bf16_parity(got, want, what):
+    got = np.asarray(got, dtype=np.float64).reshape(-1)
+    want = np.asarray(want, dtype=np.float64).reshape(-1)
+    bound = 2.0**-8 * np.abs(want) + 1e-4 * (1.0 + np.abs(want))
+    err = np.abs(got - want)
+    bad = ~(err <= bound)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements out of bound, worst at {int(np.argmax(err - bound))}: "
+                           f"got {got[np.argmax(err - bound)]}, want {want[np.argmax(err - bound)]}")
+
+
+def bf16_inputs(n, mean=0.0, std=1.0, seed=0, tensor_id=0):
+    return normgen.round_bf16(normgen.normal(n, mean, std, seed=seed, tensor_id=tensor_id))
+
+
+# ------------------------------------------------------------------ LayerNorm
+
+def run_ln(ng, x, g, b, rows, L, path=0, offset=0, inplace=False):
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, path)
+    try:
+        xb = BGuarded(rows * L, x, offset)
+        gb = None if g is None else BGuarded(L, g, offset).t
+        bb = None if b is None else BGuarded(L, b, offset).t
+        yb = xb if inplace else BGuarded(rows * L, offset=offset)
+        ng.norm_layer_fwd_bf16(xb.t, gb, bb, yb.t, rows, L, 1e-5)
+        assert ng.norm_last_error() == 0
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_LN_PATH, 0)
+    assert yb.guards_intact(), "LayerNorm bf16 wrote outside its output"
+    return yb.values()
+
+
+@pytest.mark.parametrize("rows,L,path", [
+    (3, 12, 3), (64, 4096, 3), (9, 16384, 3), (5, 1000, 3),   # row kernel
+    (2, 16388, 2), (3, 4096, 2), (2, 1 << 20, 0),             # two-kernel path, vector form
+    (3, 1001, 0),                                             # two-kernel path, scalar form
+])
+def test_layer_norm_bf16(ng, rows, L, path):
+    x = bf16_inputs(rows * L, seed=rows + L)
+    g = bf16_inputs(L, 1.0, 0.1, seed=rows + L, tensor_id=1)
+    b = bf16_inputs(L, 0.0, 0.1, seed=rows + L, tensor_id=2)
+    want = oracle.layer_norm(x, g, b, rows, L, f64=True)
+    assert_bf16_parity(run_ln(ng, x, g, b, rows, L, path=path), want, f"LN bf16 {rows}x{L} path={path}")
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_layer_norm_bf16_in_place_no_affine_misaligned(ng, offset):
+    rows, L = 7, 2048
+    x = bf16_inputs(rows * L, 2.0, 3.0, seed=11)
+    want = oracle.layer_norm(x, None, None, rows, L, f64=True)
+    assert_bf16_parity(run_ln(ng, x, None, None, rows, L, offset=offset), want, f"LN bf16 offset={offset}")
+    assert_bf16_parity(run_ln(ng, x, None, None, rows, L, offset=offset, inplace=True), want,
+                       f"LN bf16 in place offset={offset}")
+
+
+def test_layer_norm_bf16_refuses_the_persistent_kernel(ng):
+    rows, L = 1, 1 << 20
+    x = BGuarded(rows * L, bf16_inputs(rows * L))
+    y = BGuarded(rows * L)
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, 1)
+    try:
+        with pytest.raises(ng.NormError) as e:
+            ng.norm_layer_fwd_bf16(x.t, None, None, y.t, rows, L, 1e-5)
+        assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_LN_PATH, 0)
+
+
+def test_layer_norm_bf16_full_size(ng):
+    rows, L = 16, 64 * 256 * 256
+    x = bf16_inputs(rows * L, seed=0)
+    g = bf16_inputs(L, 1.0, 0.1, seed=0, tensor_id=1)
+    b = bf16_inputs(L, 0.0, 0.1, seed=0, tensor_id=2)
+    want = oracle.layer_norm(x, g, b, rows, L, f64=True)
+    assert_bf16_parity(run_ln(ng, x, g, b, rows, L), want, "LN bf16 (16, 64, 256, 256)")
+
+
+# ------------------------------------------------------------------ RMSNorm
+
+@pytest.mark.parametrize("B,C,S", [(2, 64, 1024), (3, 1, 37), (2, 3, 129), (2, 128, 300), (2, 200, 65), (1, 48, 513)])
+def test_rms_bf16(ng, B, C, S):
+    x = bf16_inputs(B * C * S, seed=B * C + S)
+    want = oracle.rms_channel(x, B, C, S, f64=True)
+    xb, yb = BGuarded(B * C * S, x), BGuarded(B * C * S)
+    ng.norm_rms_channel_fwd_bf16(xb.t, yb.t, B, C, S, 1e-5)
+    assert ng.norm_last_error() == 0
+    assert_bf16_parity(yb.values(), want, f"RMS bf16 ({B},{C},{S})")
+    assert yb.guards_intact()
+    ng.norm_rms_channel_fwd_bf16(xb.t, xb.t, B, C, S, 1e-5)
+    assert_bf16_parity(xb.values(), want, f"RMS bf16 in place ({B},{C},{S})")
+
+
+# ------------------------------------------------------------------ GroupNorm + LeakyReLU + x2
+
+@pytest.mark.parametrize("N,C,G", [(7, 16 * 32, 32), (5, 4 * 8, 8), (3, 128 * 4, 4), (6, 3 * 16, 16),
+                                   (4, 48 * 5, 5), (9, 64, 64), (1024, 8192, 512)])
+def test_group_norm_bf16(ng, N, C, G):
+    x = bf16_inputs(N * C, seed=N + C)
+    g = bf16_inputs(C, 1.0, 0.1, seed=N + C, tensor_id=1)
+    b = bf16_inputs(C, 0.0, 0.1, seed=N + C, tensor_id=2)
+    want = oracle.group_lrelu_x2(x, g, b, N, C, G, f64=True)
+    xb, gb, bb, yb = BGuarded(N * C, x), BGuarded(C, g), BGuarded(C, b), BGuarded(N * C)
+    ng.norm_group_lrelu_x2_fwd_bf16(xb.t, gb.t, bb.t, yb.t, N, C, G, 1e-5, 0.01)
+    assert ng.norm_last_error() == 0
+    assert_bf16_parity(yb.values(), want, f"GN bf16 ({N},{C})/{G}")
+    assert yb.guards_intact()
+
+
+def test_bf16_entry_points_check_dtype(ng):
+    x = torch.zeros(64, device="cuda")
+    with pytest.raises(TypeError):
+        ng.norm_rms_channel_fwd_bf16(x, x, 1, 4, 16, 1e-5)

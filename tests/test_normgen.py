@@ -60,3 +60,25 @@ def test_into_existing_buffer():
     out = normgen.normal(4097, seed=9, out=buf)
     assert out is buf
     assert buf.tobytes() == normgen.normal(4097, seed=9).tobytes()
+
+
+def test_bf16_rounding_known_values():
+    import normgen
+    vals = np.array([1.0, -2.0, 1.0 + 2**-8, 1.0 + 3 * 2**-8, 1.0 + 2**-8 + 2**-20, 0.0, -0.0, 3.0e38, 1e-40],
+                    dtype=np.float32)
+    want = [0x3F80, 0xC000, 0x3F80, 0x3F82, 0x3F81, 0x0000, 0x8000, 0x7F62, 0x0001]
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties go to the even 0x3F80;
+    # 1 + 3*2^-8 ties to 0x3F82; just above the tie rounds up; 1e-40 is subnormal
+    assert list(normgen.bf16_bits(vals)) == want
+    assert np.array_equal(normgen.bf16_to_f32(normgen.bf16_bits(vals[:2])), vals[:2])
+
+
+def test_bf16_rounding_matches_torch():
+    import normgen
+    torch = pytest.importorskip("torch")
+    x = normgen.normal(100_000, 0.0, 100.0, seed=3)
+    t = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(normgen.bf16_bits(x), t)
+    r = normgen.round_bf16(x)
+    assert np.array_equal(normgen.bf16_bits(r), t)  # representable values map to themselves
+    assert np.all(np.abs(r - x) <= 2.0**-8 * np.abs(x))
