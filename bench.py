@@ -68,12 +68,20 @@ CONFIGS = {
     "ln_stress": dict(op="ln", rows=16, L=64 * 256 * 256, x=(1000.0, 1e-2), gamma="ones", beta="zeros",
                       workload="LayerNorm cancellation stress fp32 (16,64,256,256), x~N(1000,0.01^2), "
                                "gamma=1, beta=0 (passed as tensors), eps 1e-5"),
-    # beyond the five workloads above: LayerNorm over many short rows (the row kernel)
+    # beyond the five workloads above: LayerNorm over many short rows (the row kernel),
+    # and bfloat16 storage (fp32 arithmetic) of three workloads
+    "ln_rows_bf16": dict(op="ln", rows=16384, L=4096, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1), bf16=True,
+                         workload="LayerNorm bf16 (16384, 4096) over the last dim, fp32 arithmetic, x~N(0,1), "
+                                  "gamma~N(1,0.1), beta~N(0,0.1) rounded to bf16, eps 1e-5"),
+    "gn_bf16": dict(op="gn", N=1024, C=8192, G=512, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1), bf16=True,
+                    workload="GroupNorm+LeakyReLU(0.01)+x2 bf16 (1024,8192), 512 groups of 16, fp32 arithmetic"),
+    "rms_bf16": dict(op="rms", B=112, C=64, S=512 * 512, x=(0.0, 1.0), bf16=True,
+                     workload="RMSNorm over dim 1 of bf16 NCHW (112,64,512,512), fp32 arithmetic, eps 1e-5"),
     "ln_rows": dict(op="ln", rows=16384, L=4096, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
                     workload="LayerNorm fp32 (16384, 4096) over the last dim, x~N(0,1), gamma~N(1,0.1), "
                              "beta~N(0,0.1), eps 1e-5 (many short rows)"),
 }
-EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_rows"]
+EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_rows", "ln_rows_bf16", "gn_bf16", "rms_bf16"]
 
 
 # ---------------------------------------------------------------------------- sizes
@@ -94,16 +102,20 @@ def param_elems(cfg) -> int:
     return 0
 
 
+def elem_bytes(cfg) -> int:
+    return 2 if cfg.get("bf16") else 4
+
+
 def algorithmic_bytes(cfg) -> int:
-    """x read once + y written once + gamma/beta read once (fp32)."""
-    return 8 * elements(cfg) + 4 * param_elems(cfg)
+    """x read once + y written once + gamma/beta read once."""
+    return elem_bytes(cfg) * (2 * elements(cfg) + param_elems(cfg))
 
 
 def l2_note(cfg, l2_bytes=None) -> str:
     if l2_bytes is None:
         return "inputs larger than L2 (back-to-back steps rotate through enough buffer sets)"
     n = buffer_sets(cfg, l2_bytes)
-    mb = 8 * elements(cfg) * n / 2**20
+    mb = 2 * elem_bytes(cfg) * elements(cfg) * n / 2**20
     if n == 1:
         return (f"inputs larger than L2: one step moves {mb:.0f} MiB of x and y, more than twice the "
                 f"{l2_bytes / 2**20:.0f} MiB L2; K back-to-back steps between one pair of CUDA events")
@@ -138,7 +150,20 @@ def host_inputs(cfg, seed=0):
             b = np.zeros(pn, dtype=np.float32)
         else:
             b = normgen.normal(pn, cfg["beta"][0], cfg["beta"][1], seed=seed, tensor_id=normgen.TENSOR_BETA)
+    if cfg.get("bf16"):  # the values the GPU stores, so the oracle sees the same
+        x, g, b = (None if a is None else normgen.round_bf16(a) for a in (x, g, b))
     return x, g, b
+
+
+def device_tensor(a, cfg, dev):
+    """A host float32 array on the device in the workload's storage type (bf16: rounded to
+    nearest even by the input generator's helper)."""
+    import numpy as np
+    import torch
+    import normgen
+    if cfg.get("bf16"):
+        return torch.from_numpy(normgen.bf16_bits(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
 
 
 def main_kernel_name(cfg) -> str:
@@ -152,13 +177,18 @@ def main_kernel_name(cfg) -> str:
 def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
     """The C-ABI call of one step (device pointers) and the number of our kernel launches it makes."""
     op = cfg["op"]
+    bf16 = bool(cfg.get("bf16"))
     if op == "ln":
         rows, L = cfg["rows"], cfg["L"]
-        one_launch = L % 4 == 0 and (L <= 16384 or (1 << 20) <= L <= ng.norm_layer_max_resident_row_len())
-        return (lambda: ng.norm_layer_fwd(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if one_launch else 2)
+        one_launch = L % 4 == 0 and (L <= 16384 or
+                                     (not bf16 and (1 << 20) <= L <= ng.norm_layer_max_resident_row_len()))
+        fn = ng.norm_layer_fwd_bf16 if bf16 else ng.norm_layer_fwd
+        return (lambda: fn(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if one_launch else 2)
     if op == "gn":
-        return (lambda: ng.norm_group_lrelu_x2_fwd(x, g, b, y, cfg["N"], cfg["C"], cfg["G"], 1e-5, 0.01, stream)), 1
-    return (lambda: ng.norm_rms_channel_fwd(x, y, cfg["B"], cfg["C"], cfg["S"], 1e-5, stream)), 1
+        fn = ng.norm_group_lrelu_x2_fwd_bf16 if bf16 else ng.norm_group_lrelu_x2_fwd
+        return (lambda: fn(x, g, b, y, cfg["N"], cfg["C"], cfg["G"], 1e-5, 0.01, stream)), 1
+    fn = ng.norm_rms_channel_fwd_bf16 if bf16 else ng.norm_rms_channel_fwd
+    return (lambda: fn(x, y, cfg["B"], cfg["C"], cfg["S"], 1e-5, stream)), 1
 
 
 # ---------------------------------------------------------------------------- clocks
@@ -396,7 +426,7 @@ def time_same_size_copy(xs, ys, steps, stream):
 def buffer_sets(cfg, l2_bytes: int) -> int:
     """Input/output sets to rotate through so that no step finds its data in L2: one set
     when a step's x + y exceed twice the L2, else enough sets to cover three L2s."""
-    set_bytes = 8 * elements(cfg)
+    set_bytes = 2 * elem_bytes(cfg) * elements(cfg)
     if set_bytes > 2 * l2_bytes:
         return 1
     return -(-3 * l2_bytes // set_bytes)
@@ -413,9 +443,7 @@ def run_config(ng, name, cfg, steps, warmup, stream, flush, l2_bytes, sampler=No
     import torch
     x, g, b = host_inputs(cfg)
     dev = torch.device("cuda")
-    xd = torch.from_numpy(x).to(dev)
-    gd = None if g is None else torch.from_numpy(g).to(dev)
-    bd = None if b is None else torch.from_numpy(b).to(dev)
+    xd, gd, bd = (None if a is None else device_tensor(a, cfg, dev) for a in (x, g, b))
     nset = buffer_sets(cfg, l2_bytes)
     xs = [xd] + [xd.clone() for _ in range(nset - 1)]
     ys = [torch.empty_like(xd) for _ in range(nset)]
@@ -458,10 +486,9 @@ def run_e2e(ng, cfg, x, g, b, xd, gd, bd, yd, ws, ws_bytes, stream, steps, world
     between two streams with a device buffer set each, so one step's H2D overlaps the
     previous step's call and D2H (the copy engines run both directions at once)."""
     import torch
-    xh = torch.from_numpy(x).pin_memory()
-    gh = None if g is None else torch.from_numpy(g).pin_memory()
-    bh = None if b is None else torch.from_numpy(b).pin_memory()
-    yh = [torch.empty(xh.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    cpu = torch.device("cpu")
+    xh, gh, bh = (None if a is None else device_tensor(a, cfg, cpu).pin_memory() for a in (x, g, b))
+    yh = [torch.empty(xh.shape, dtype=xh.dtype).pin_memory() for _ in range(2)]
     streams = [stream, torch.cuda.Stream()]
     sets = [(xd, gd, bd, yd, ws)]
     ws2 = None if ws is None else torch.zeros_like(ws)
@@ -469,8 +496,8 @@ def run_e2e(ng, cfg, x, g, b, xd, gd, bd, yd, ws, ws_bytes, stream, steps, world
                  None if bd is None else torch.empty_like(bd), torch.empty_like(yd), ws2))
     calls = [make_call(ng, cfg, xs, gs, bs, ys, wss, ws_bytes, st.cuda_stream)[0]
              for (xs, gs, bs, ys, wss), st in zip(sets, streams)]
-    h2d = xh.numel() * 4 + (0 if gh is None else gh.numel() * 4) + (0 if bh is None else bh.numel() * 4)
-    d2h = yh[0].numel() * 4
+    h2d = sum(0 if t is None else t.numel() * t.element_size() for t in (xh, gh, bh))
+    d2h = yh[0].numel() * yh[0].element_size()
 
     def step(k):
         i = k % 2
@@ -636,9 +663,10 @@ def main(argv=None):
             if name == args.config:
                 continue
             c = CONFIGS[name]
-            k = min(args.steps, 1000 if name != "rms" else 50)
-            r = run_config(ng, name, c, k, 5, stream, flush, l2, cold_steps=100 if name != "rms" else 10,
-                           want_graph=True, want_copy=name != "rms")
+            big = c["op"] == "rms" and c["B"] > 8
+            k = min(args.steps, 50 if big else 1000)
+            r = run_config(ng, name, c, k, 5, stream, flush, l2, cold_steps=10 if big else 100,
+                           want_graph=True, want_copy=not big)
             a = algorithmic_bytes(c) / r["seconds_per_step"] / 1e9
             cold = r["cold_seconds_per_launch"]
             more = {}
@@ -649,7 +677,7 @@ def main(argv=None):
             if r["copy_seconds_per_step"]:
                 cs = r["copy_seconds_per_step"]
                 more["same_size_copy_us"] = round(cs * 1e6, 3)
-                more["same_size_copy_frac_of_measured_peak"] = round(8 * elements(c) / cs / 1e9 / peak, 4)
+                more["same_size_copy_frac_of_measured_peak"] = round(2 * elem_bytes(c) * elements(c) / cs / 1e9 / peak, 4)
             extras.append({"config": name, "workload": c["workload"], "steps": k,
                            "us_per_step": round(r["seconds_per_step"] * 1e6, 3),
                            "algorithmic_bytes": algorithmic_bytes(c), "achieved_gbs": round(a, 2),
@@ -675,7 +703,8 @@ def main(argv=None):
             "elements_per_s": round(elements(cfg) * world / sec, 1),
             "same_size_copy": None if not main_res["copy_seconds_per_step"] else {
                 "us": round(main_res["copy_seconds_per_step"] * 1e6, 3),
-                "frac_of_measured_peak": round(8 * elements(cfg) / main_res["copy_seconds_per_step"] / 1e9 / peak, 4),
+                "frac_of_measured_peak": round(2 * elem_bytes(cfg) * elements(cfg) / main_res["copy_seconds_per_step"] / 1e9
+                                               / peak, 4),
                 "note": "device copy of x into y (same bytes as a step minus gamma/beta), timed the same way"},
             "cold_launch": None if not main_res["cold_seconds_per_launch"] else {
                 "us": round(main_res["cold_seconds_per_launch"] * 1e6, 3),
