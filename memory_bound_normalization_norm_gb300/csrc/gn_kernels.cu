@@ -4,13 +4,14 @@
 // variance, per-channel affine, LeakyReLU(t) = max(0,t) + slope*min(0,t),
 // then x + x).
 //
-// Vector path: one thread owns 4 consecutive channels (one float4), so a group
-// of M channels is TPG = M/4 adjacent lanes and a warp covers 32 float4 =
-// 512 contiguous bytes.  Mean and then the exact M2 about the mean are reduced
-// over the TPG lanes with xor shuffles (the group's values never leave
-// registers), the epilogue is applied in registers and the float4 is stored
-// once.  Every byte of x is read once and every byte of y written once;
-// gamma/beta (2*C floats) stay cache resident.
+// Vector path: one thread owns 4 consecutive channels (a 4-element vector:
+// 16 bytes of fp32 or 8 of bf16), so a group of M channels is TPG = M/4
+// adjacent lanes and a warp covers 128 contiguous elements.  Mean and then
+// the exact M2 about the mean are reduced over the TPG lanes with xor
+// shuffles (the group's values never leave registers), the epilogue is
+// applied in fp32 registers and the vector is stored once.  A CTA keeps its
+// columns' gamma/beta in registers and walks rows with two rows of x loads in
+// flight.  Every byte of x is read once and every byte of y written once.
 #include "norm_internal.cuh"
 
 namespace normk {
@@ -28,8 +29,12 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
-// grid: x = column blocks of GN_THREADS*U float4, y = rows (folded by gridDim.y)
+// grid: x = column blocks of GN_THREADS*U vectors, y = row walkers.
 // x, y: [N][C] of T; "vector" = 4 consecutive channels; C4 = C / 4.
+// A CTA owns a fixed block of GN_THREADS * U vectors of columns and walks
+// rows n = blockIdx.y, + gridDim.y, ...: gamma/beta of its columns are
+// loaded once, and the next two rows' x are loaded while the current row is
+// reduced and written, so every thread keeps two rows of loads in flight.
 template <typename T, int TPG, int U>
 __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T *__restrict__ gamma,
                                                              const T *__restrict__ beta, T *y,
@@ -39,27 +44,44 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     const int col0 = blockIdx.x * (GN_THREADS * U) + threadIdx.x;
-    for (int64_t n = blockIdx.y; n < N; n += gridDim.y) {
+    float4 g[U], b[U], cur[U], nxt[U], nx2[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int c = col0 + u * GN_THREADS;
+        const bool in = c < C4;
+        g[u] = (in && gamma) ? Io<T>::ld4_ro(gamma + 4 * c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
+        b[u] = (in && beta) ? Io<T>::ld4_ro(beta + 4 * c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    auto load_row = [&](int64_t n, float4 *dst) {
         const T *xr = x + n * C4 * 4;
-        T *yr = y + n * C4 * 4;
-        // all loads of the row block first (x and this thread's gamma/beta), so
-        // they are in flight together
-        float4 v[U], g[U], b[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int c = col0 + u * GN_THREADS;
-            const bool in = c < C4;
-            v[u] = in ? Io<T>::ld4_stream(xr + 4 * c, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
-            g[u] = (in && gamma) ? Io<T>::ld4_ro(gamma + 4 * c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
-            b[u] = (in && beta) ? Io<T>::ld4_ro(beta + 4 * c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+            dst[u] = c < C4 ? Io<T>::ld4_stream(xr + 4 * c, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    if (blockIdx.y < N)
+        load_row(blockIdx.y, nxt);
+    if (blockIdx.y + gridDim.y < N)
+        load_row(blockIdx.y + gridDim.y, nx2);
+    for (int64_t n = blockIdx.y; n < N; n += gridDim.y) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            cur[u] = nxt[u];
+            nxt[u] = nx2[u];
+        }
+        // with y == x the rows ahead are other rows: loading them now
+        // cannot race with this row's stores
+        if (n + 2 * gridDim.y < N)
+            load_row(n + 2 * gridDim.y, nx2);
+        T *yr = y + n * C4 * 4;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int c = col0 + u * GN_THREADS;
             // C4 is a multiple of TPG, so whole groups are in or out of range
             // together and every lane takes part in the shuffles.
-            const float mean = group_sum<TPG>((v[u].x + v[u].y) + (v[u].z + v[u].w)) * invM;
-            const float dx = v[u].x - mean, dy = v[u].y - mean, dz = v[u].z - mean, dw = v[u].w - mean;
+            const float mean = group_sum<TPG>((cur[u].x + cur[u].y) + (cur[u].z + cur[u].w)) * invM;
+            const float dx = cur[u].x - mean, dy = cur[u].y - mean, dz = cur[u].z - mean, dw = cur[u].w - mean;
             const float m2 = group_sum<TPG>((dx * dx + dy * dy) + (dz * dz + dw * dw));
             const float rstd = rsqrtf(fmaf(m2, invM, eps));
             if (c < C4) {
@@ -82,13 +104,25 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
     }
 }
 
+
 template <typename T, int TPG, int U>
 cudaError_t launch_vec(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
-                       int64_t M, float eps, float slope, cudaStream_t stream)
+                       int64_t M, float eps, float slope, int sm_count, cudaStream_t stream)
 {
     const int C4 = static_cast<int>(C / 4);
     const int per_block = GN_THREADS * U;
-    dim3 grid((C4 + per_block - 1) / per_block, static_cast<unsigned>(N < 65535 ? N : 65535));
+    const int gx = (C4 + per_block - 1) / per_block;
+    // CTAS_PER_SM CTAs per SM (measured: 8 for fp32, 4 for bf16); each walks
+    // N / gy rows
+    constexpr int CTAS_PER_SM = sizeof(T) == 2 ? 4 : 8;
+    int64_t gy = (static_cast<int64_t>(sm_count) * CTAS_PER_SM + gx - 1) / gx;
+    if (gy > N)
+        gy = N;
+    if (gy > 65535)
+        gy = 65535;
+    if (gy < 1)
+        gy = 1;
+    dim3 grid(gx, static_cast<unsigned>(gy));
     gn_vec4_kernel<T, TPG, U><<<grid, GN_THREADS, 0, stream>>>(
         static_cast<const T *>(x), static_cast<const T *>(gamma), static_cast<const T *>(beta), static_cast<T *>(y),
         N, C4, 1.0f / static_cast<float>(M), eps, slope);
@@ -138,26 +172,28 @@ __global__ void __launch_bounds__(256) gn_warp_kernel(const T *x, const T *__res
 
 } // namespace
 
+// Two vectors a thread per row.
 template <typename T>
 cudaError_t gn_vec4_launch_t(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
-                             int64_t M, float eps, float slope, cudaStream_t stream)
+                             int64_t M, float eps, float slope, int sm_count, cudaStream_t stream)
 {
+    constexpr int U = 2;
     switch (M) {
-    case 4: return launch_vec<T, 1, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 8: return launch_vec<T, 2, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 16: return launch_vec<T, 4, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 32: return launch_vec<T, 8, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 64: return launch_vec<T, 16, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
-    case 128: return launch_vec<T, 32, 2>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    case 4: return launch_vec<T, 1, U>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+    case 8: return launch_vec<T, 2, U>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+    case 16: return launch_vec<T, 4, U>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+    case 32: return launch_vec<T, 8, U>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+    case 64: return launch_vec<T, 16, U>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+    case 128: return launch_vec<T, 32, U>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t gn_vec4_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
-                           int64_t M, float eps, float slope, bool bf16, cudaStream_t stream)
+                           int64_t M, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream)
 {
-    return bf16 ? gn_vec4_launch_t<__nv_bfloat16>(x, gamma, beta, y, N, C, M, eps, slope, stream)
-                : gn_vec4_launch_t<float>(x, gamma, beta, y, N, C, M, eps, slope, stream);
+    return bf16 ? gn_vec4_launch_t<__nv_bfloat16>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream)
+                : gn_vec4_launch_t<float>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
 }
 
 cudaError_t gn_warp_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,

@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 
 // ---------------------------------------------------------------- row path
 //
-// Rows of at most LR_T * 16 float4 (16,384 elements), length a multiple of
+// Rows of at most LR_T * 16 4-element vectors (16,384 elements), length a multiple of
 // 4, 16-byte aligned: one CTA per row at a time (grid-stride over rows),
 // the row in registers, so x is read from HBM once and there is no
 // workspace and a single launch.  Mean and M2 are the exact two-pass
@@ -631,8 +631,9 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 
 constexpr int LR_T = 256;
 
-// Sum of v over the CTA, in a fixed order; every thread gets the result.
-// `scratch` (LR_T / 32 floats) must not be in use by the previous call.
+// Sum of v over a CTA of NT threads, in a fixed order; every thread gets the
+// result.  `scratch` (NT / 32 floats) must not be in use by the previous call.
+template <int NT>
 __device__ __forceinline__ float block_sum(float v, float *scratch)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -644,15 +645,16 @@ __device__ __forceinline__ float block_sum(float v, float *scratch)
     __syncthreads();
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < LR_T / 32; ++w)
+    for (int w = 0; w < NT / 32; ++w)
         t += scratch[w];
     return t;
 }
 
-template <typename T, int V>
-__global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
+// NT threads a CTA, V 4-element vectors a thread.
+template <typename T, int NT, int V>
+__global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
 {
-    __shared__ float red[2][LR_T / 32];
+    __shared__ float red[2][NT / 32];
     const int tid = threadIdx.x;
     const int64_t L4 = p.row_len >> 2; // 4-element vectors per row
     const float Lf = static_cast<float>(p.row_len);
@@ -669,7 +671,7 @@ __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
     if (KEEP_GB) {
 #pragma unroll
         for (int k = 0; k < V; ++k) {
-            const int64_t i = tid + k * LR_T;
+            const int64_t i = tid + k * NT;
             gk[k] = (gm && i < L4) ? Io<T>::ld4_ro(gm + 4 * i, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
             bk[k] = (bt && i < L4) ? Io<T>::ld4_ro(bt + 4 * i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -679,7 +681,7 @@ __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
         float4 v[V];
 #pragma unroll
         for (int k = 0; k < V; ++k) {
-            const int64_t i = tid + k * LR_T;
+            const int64_t i = tid + k * NT;
             v[k] = i < L4 ? Io<T>::ld4_stream(xr + 4 * i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         // every thread reads the pivot before any thread of the CTA stores
@@ -688,10 +690,10 @@ __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
-            if (tid + k * LR_T < L4)
+            if (tid + k * NT < L4)
                 s += ((v[k].x - K) + (v[k].y - K)) + ((v[k].z - K) + (v[k].w - K));
         }
-        s = block_sum(s, red[0]);
+        s = block_sum<NT>(s, red[0]);
         Moments tot;
         tot.n = Lf;
         tot.mean = s / Lf;
@@ -700,18 +702,18 @@ __global__ void __launch_bounds__(LR_T) ln_rows_kernel(LnParams p)
         float q = 0.f;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
-            if (tid + k * LR_T < L4) {
+            if (tid + k * NT < L4) {
                 const float a = (v[k].x - rm.hi) - rm.lo, b = (v[k].y - rm.hi) - rm.lo;
                 const float c = (v[k].z - rm.hi) - rm.lo, d = (v[k].w - rm.hi) - rm.lo;
                 q += (a * a + b * b) + (c * c + d * d);
             }
         }
-        q = block_sum(q, red[1]);
+        q = block_sum<NT>(q, red[1]);
         rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
         T *yr = y + r * p.row_len;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
-            const int64_t i = tid + k * LR_T;
+            const int64_t i = tid + k * NT;
             if (i < L4) {
                 float4 g, b;
                 if (KEEP_GB) {
@@ -860,33 +862,40 @@ int64_t ln_rows_max_row_len()
     return int64_t(LR_T) * 16 * 4;
 }
 
-template <typename T>
+template <typename T, int NT>
 cudaError_t ln_rows_launch_t(const LnParams &p, int sm_count, cudaStream_t stream)
 {
     const int64_t L4 = p.row_len / 4;
     int64_t grid = p.rows;
-    const int64_t cap = static_cast<int64_t>(sm_count) * 16;
+    const int64_t cap = static_cast<int64_t>(sm_count) * (2048 / NT);
     if (grid > cap)
         grid = cap;
     const dim3 g(static_cast<unsigned>(grid));
-    if (L4 <= LR_T)
-        ln_rows_kernel<T, 1><<<g, LR_T, 0, stream>>>(p);
-    else if (L4 <= 2 * LR_T)
-        ln_rows_kernel<T, 2><<<g, LR_T, 0, stream>>>(p);
-    else if (L4 <= 4 * LR_T)
-        ln_rows_kernel<T, 4><<<g, LR_T, 0, stream>>>(p);
-    else if (L4 <= 8 * LR_T)
-        ln_rows_kernel<T, 8><<<g, LR_T, 0, stream>>>(p);
-    else if (L4 <= 16 * LR_T)
-        ln_rows_kernel<T, 16><<<g, LR_T, 0, stream>>>(p);
+    if (L4 <= NT)
+        ln_rows_kernel<T, NT, 1><<<g, NT, 0, stream>>>(p);
+    else if (L4 <= 2 * NT)
+        ln_rows_kernel<T, NT, 2><<<g, NT, 0, stream>>>(p);
+    else if (L4 <= 4 * NT)
+        ln_rows_kernel<T, NT, 4><<<g, NT, 0, stream>>>(p);
+    else if (L4 <= 8 * NT)
+        ln_rows_kernel<T, NT, 8><<<g, NT, 0, stream>>>(p);
+    else if (L4 <= 16 * NT)
+        ln_rows_kernel<T, NT, 16><<<g, NT, 0, stream>>>(p);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 
+// bf16 rows up to 8,192 elements use 128-thread CTAs: a row then holds as
+// many registers per thread as an fp32 row in 256 threads, and twice as
+// many rows (of half the bytes) are in flight per SM.
 cudaError_t ln_rows_launch(const LnParams &p, bool bf16, int sm_count, cudaStream_t stream)
 {
-    return bf16 ? ln_rows_launch_t<__nv_bfloat16>(p, sm_count, stream) : ln_rows_launch_t<float>(p, sm_count, stream);
+    if (!bf16)
+        return ln_rows_launch_t<float, LR_T>(p, sm_count, stream);
+    if (p.row_len <= int64_t(LR_T / 2) * 16 * 4)
+        return ln_rows_launch_t<__nv_bfloat16, LR_T / 2>(p, sm_count, stream);
+    return ln_rows_launch_t<__nv_bfloat16, LR_T>(p, sm_count, stream);
 }
 
 template <typename T>

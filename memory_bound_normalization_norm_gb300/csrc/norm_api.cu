@@ -476,7 +476,7 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     const bool vec = pow2 && (C & 3) == 0 && C / 4 < (int64_t(1) << 30) && aligned(x, va) && aligned(y, va) &&
                      aligned(gamma, va) && aligned(beta, va);
     const bool bf16 = esz == 2;
-    cudaError_t e = vec ? normk::gn_vec4_launch(x, gamma, beta, y, N, C, M, eps, negative_slope, bf16, stream)
+    cudaError_t e = vec ? normk::gn_vec4_launch(x, gamma, beta, y, N, C, M, eps, negative_slope, bf16, d->sm_count, stream)
                         : normk::gn_warp_launch(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, bf16,
                                                 d->sm_count, stream);
     if (e != cudaSuccess) {

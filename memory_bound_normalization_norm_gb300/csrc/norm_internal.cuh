@@ -506,7 +506,7 @@ cudaError_t ln_rows_launch(const LnParams &p, bool bf16, int sm_count, cudaStrea
 
 // GroupNorm + LeakyReLU + x2 (bf16: the tensors are bf16, else fp32).
 cudaError_t gn_vec4_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
-                           int64_t M, float eps, float slope, bool bf16, cudaStream_t stream);
+                           int64_t M, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream);
 cudaError_t gn_warp_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
                            int64_t G, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream);
 
