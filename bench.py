@@ -278,17 +278,21 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
 
 
-def kernel_source_hash() -> str:
+# the kernel source files each workload's counters depend on
+KERNEL_SOURCES = {"ln": ("ln_kernels.cu", "norm_internal.cuh"), "gn": ("gn_kernels.cu", "norm_internal.cuh"),
+                  "rms": ("rms_kernels.cu", "norm_internal.cuh")}
+
+
+def kernel_source_hash(op: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "memory_bound_normalization_norm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[op]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(config_name: str):
+def ncu_traffic(config_name: str, op: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernels."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
@@ -299,7 +303,7 @@ def ncu_traffic(config_name: str):
     entry = rec.get(config_name)
     if not entry:
         return None, "no ncu DRAM counters for this workload"
-    if entry.get("kernel_source_hash") != kernel_source_hash():
+    if entry.get("kernel_source_hash") != kernel_source_hash(op):
         return None, "kernels changed since the ncu DRAM counters were taken"
     return entry.get("dram_bytes_per_launch"), entry.get("note", "")
 
@@ -655,7 +659,7 @@ def main(argv=None):
     e2e_sec = dist_max(main_res["e2e"]["seconds_per_step"], world, device="cuda")
     peak, peak_note = hbm_peak()
     achieved = nbytes / main_res["seconds_per_step"] / 1e9
-    traffic, traffic_note = ncu_traffic(args.config)
+    traffic, traffic_note = ncu_traffic(args.config, cfg["op"])
 
     extras = []
     if world == 1 and not args.no_extras:
