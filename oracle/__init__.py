@@ -87,6 +87,8 @@ class Oracle:
         lib.oracle_rms_channel.argtypes = [vp, i64, i64, i64, dbl, vp, vp, ci]
         lib.oracle_group_lrelu_x2.restype = ci
         lib.oracle_group_lrelu_x2.argtypes = [vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp, ci]
+        lib.oracle_group_lrelu_x2_nchw.restype = ci
+        lib.oracle_group_lrelu_x2_nchw.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, vp, vp, ci]
         self._lib = lib
 
     @staticmethod
@@ -135,6 +137,22 @@ class Oracle:
         return y64 if f64 else y32
 
 
+    def group_lrelu_x2_nchw(self, x, gamma, beta, N, C, S, G, eps=1e-5, slope=0.01, *, f64=False,
+                            threads=None):
+        """2 * LeakyReLU(GroupNorm(x)) over x[N][C][S]: G groups of C/G contiguous channels,
+        each over all S spatial positions."""
+        x = _f32(x, "x")
+        if x.size != N * C * S:
+            raise ValueError("x has the wrong size")
+        g, b = _opt_f32(gamma), _opt_f32(beta)
+        y64, y32 = self._outputs(x.shape, f64)
+        rc = self._lib.oracle_group_lrelu_x2_nchw(_ptr(x), _ptr(g), _ptr(b), N, C, S, G, eps, slope,
+                                                  _ptr(y64), _ptr(y32), threads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_group_lrelu_x2_nchw rejected its arguments ({rc})")
+        return y64 if f64 else y32
+
+
 def get() -> Oracle:
     """The oracle built from ``norm_oracle.c`` as committed."""
     global _default
@@ -165,3 +183,7 @@ def rms_channel(*a, **k):
 
 def group_lrelu_x2(*a, **k):
     return get().group_lrelu_x2(*a, **k)
+
+
+def group_lrelu_x2_nchw(*a, **k):
+    return get().group_lrelu_x2_nchw(*a, **k)

@@ -23,6 +23,9 @@
  *    design turn: groups of C/G contiguous channels, var = sum((x-mean)^2)/M,
  *    y = (x - mean)/sqrt(var + eps) * gamma_c + beta_c, LeakyReLU(t) =
  *    max(0, t) + negative_slope * min(0, t), then x + x.
+ *    The same operation over x[N][C][S] (an NCHW tensor with S = H*W): a
+ *    group holds its M channels at every spatial position, M*S values,
+ *    which are contiguous in memory; gamma/beta stay per channel.
  *  - RMSNorm: transcript "Kimi-K2.6 l1_p36", reference model quoted in the
  *    analysis turn: rms = sqrt(mean(x^2, dim=1) + eps), y = x / rms, over
  *    dim 1 of an NCHW tensor whose trailing dims flatten to S = H*W.
@@ -148,6 +151,52 @@ int oracle_group_lrelu_x2(const float *x, const float *gamma, const float *beta,
                 const double t = ((double)xg[j] - mean) / denom * w + b;
                 const double l = fmax(0.0, t) + slope * fmin(0.0, t);
                 oracle_store(l + l, n * C + c, y64, y32);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* GroupNorm + LeakyReLU + x+x over x[N][C][S]: group g of sample n holds
+ * channels g*M .. g*M+M-1 (M = C/G) at all S positions, i.e. the M*S values
+ * x[n][c][s]; mean and population variance over them; then per element
+ * t = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c] (gamma/beta [C] or
+ * NULL), LeakyReLU, out = l + l.  S = 1 is oracle_group_lrelu_x2. */
+int oracle_group_lrelu_x2_nchw(const float *x, const float *gamma, const float *beta,
+                               int64_t N, int64_t C, int64_t S, int64_t G, double eps, double slope,
+                               double *y64, float *y32, int threads)
+{
+    if (!x || N < 0 || C <= 0 || S <= 0 || G <= 0 || C % G != 0 || !(eps >= 0.0) || (!y64 && !y32))
+        return ORACLE_BAD_ARG;
+    if (threads < 1)
+        threads = 1;
+    const int64_t M = C / G;
+    const double cnt = (double)(M * S);
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 1)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < G; ++g) {
+            const int64_t c0 = g * M;
+            double sum = 0.0;
+            for (int64_t c = c0; c < c0 + M; ++c)
+                for (int64_t s = 0; s < S; ++s)
+                    sum += (double)x[(n * C + c) * S + s];
+            const double mean = sum / cnt;
+            double sq = 0.0;
+            for (int64_t c = c0; c < c0 + M; ++c)
+                for (int64_t s = 0; s < S; ++s) {
+                    const double d = (double)x[(n * C + c) * S + s] - mean;
+                    sq += d * d;
+                }
+            const double denom = sqrt(sq / cnt + eps);
+            for (int64_t c = c0; c < c0 + M; ++c) {
+                const double gw = gamma ? (double)gamma[c] : 1.0;
+                const double bw = beta ? (double)beta[c] : 0.0;
+                for (int64_t s = 0; s < S; ++s) {
+                    const int64_t i = (n * C + c) * S + s;
+                    const double v = ((double)x[i] - mean) / denom * gw + bw;
+                    const double l = fmax(0.0, v) + slope * fmin(0.0, v);
+                    oracle_store(l + l, i, y64, y32);
+                }
             }
         }
     }

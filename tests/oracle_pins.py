@@ -107,6 +107,29 @@ def exact_group_lrelu_x2(x, gamma, beta, N, C, G, eps, slope):
     return out
 
 
+def exact_group_lrelu_x2_nchw(x, gamma, beta, N, C, S, G, eps, slope):
+    x = np.asarray(x, dtype=np.float32).reshape(N, C, S)
+    M = C // G
+    out = np.empty((N, C, S), dtype=np.float64)
+    fe, fs = Fraction(eps), Fraction(slope)
+    for n in range(N):
+        for g in range(G):
+            xs = [[Fraction(float(v)) for v in x[n, c]] for c in range(g * M, (g + 1) * M)]
+            flat = [v for row in xs for v in row]
+            mean = sum(flat) / (M * S)
+            var = sum((v - mean) ** 2 for v in flat) / (M * S)
+            den = _dsqrt(var + fe)
+            for j in range(M):
+                c = g * M + j
+                w = Fraction(float(gamma[c])) if gamma is not None else Fraction(1)
+                b = Fraction(float(beta[c])) if beta is not None else Fraction(0)
+                for s_ in range(S):
+                    t = _dec(xs[j][s_] - mean) / den * _dec(w) + _dec(b)
+                    l = t if t > 0 else _dec(fs) * t
+                    out[n, c, s_] = float(l + l)
+    return out
+
+
 # ----------------------------------------------------------------------------- LayerNorm
 
 def layer_norm_pins(o) -> None:
@@ -307,8 +330,65 @@ def group_lrelu_x2_pins(o) -> None:
     assert np.max(np.abs(np.mean(y * y, axis=2) - var / (var + EPS))) < 1e-12, "GN group variance"
 
 
+# ----------------------------------------------------------------------------- GroupNorm over NCHW
+
+def group_lrelu_x2_nchw_pins(o) -> None:
+    rng = np.random.default_rng(20240917)
+
+    # 1. exact brute force: a group is its M channels at every spatial position
+    for (N, C, S, G) in ((2, 4, 3, 2), (1, 6, 2, 3), (2, 8, 1, 4), (1, 4, 5, 1), (2, 6, 4, 6)):
+        x = _dyadic(rng, N * C * S)
+        g = _dyadic(rng, C, k=32, den=8)
+        b = _dyadic(rng, C, k=32, den=8)
+        for slope in (0.01, 0.25):
+            want = exact_group_lrelu_x2_nchw(x, g, b, N, C, S, G, EPS, slope).reshape(-1)
+            got = o.group_lrelu_x2_nchw(x, g, b, N, C, S, G, EPS, slope, f64=True)
+            _close(got, want, 1e-11, f"GN NCHW brute force {(N, C, S, G)} slope={slope}")
+
+    # 2. S = 1 is the (N, C) operation, bit for bit
+    N, C, G = 3, 48, 6
+    x = normgen.normal(N * C, seed=8)
+    g = normgen.normal(C, 1.0, 0.1, seed=8, tensor_id=1)
+    b = normgen.normal(C, 0.0, 0.1, seed=8, tensor_id=2)
+    assert np.array_equal(o.group_lrelu_x2_nchw(x, g, b, N, C, 1, G, EPS, 0.01, f64=True),
+                          o.group_lrelu_x2(x, g, b, N, C, G, EPS, 0.01, f64=True)), "GN NCHW with S = 1"
+
+    # 3. third voice: torch float64 group_norm on (N, C, H, W) -> leaky_relu -> x + x
+    import torch
+    N, C, H, W, G = 2, 12, 3, 5, 4
+    x = normgen.normal(N * C * H * W, 0.5, 2.0, seed=9)
+    g = normgen.normal(C, 1.0, 0.1, seed=9, tensor_id=1)
+    b = normgen.normal(C, 0.0, 0.1, seed=9, tensor_id=2)
+    t = torch.nn.functional.group_norm(torch.from_numpy(x.astype(np.float64)).reshape(N, C, H, W), G,
+                                       torch.from_numpy(g.astype(np.float64)),
+                                       torch.from_numpy(b.astype(np.float64)), EPS)
+    for slope in (0.01, 1.0):
+        l = torch.nn.functional.leaky_relu(t, slope)
+        _close(o.group_lrelu_x2_nchw(x, g, b, N, C, H * W, G, EPS, slope, f64=True), (l + l).numpy().reshape(-1),
+               1e-12, f"GN NCHW vs torch slope={slope}")
+
+    # 4. invariant: gamma=1, beta=0, slope=1: y/2 over each group's M*S values has
+    #    mean 0 and population variance var/(var+eps)
+    N, C, S, G = 2, 16, 7, 4
+    x = normgen.normal(N * C * S, -1.0, 3.0, seed=10)
+    y = o.group_lrelu_x2_nchw(x, None, None, N, C, S, G, EPS, 1.0, f64=True).reshape(N, G, -1) / 2.0
+    xd = x.astype(np.float64).reshape(N, G, -1)
+    var = np.mean((xd - xd.mean(axis=2, keepdims=True)) ** 2, axis=2)
+    assert np.max(np.abs(y.mean(axis=2))) < 1e-13, "GN NCHW group mean"
+    assert np.max(np.abs(np.mean(y * y, axis=2) - var / (var + EPS))) < 1e-12, "GN NCHW group variance"
+
+    # 5. constant group -> 2 * LReLU(beta) at every position of every channel
+    x = np.full(2 * 8 * 5, 3.25, dtype=np.float32)
+    g = _dyadic(rng, 8, k=32, den=8)
+    b = _dyadic(rng, 8, k=32, den=8)
+    bd = b.astype(np.float64)
+    want = np.tile(np.repeat(2.0 * np.where(bd > 0, bd, 0.01 * bd), 5), 2)
+    _close(o.group_lrelu_x2_nchw(x, g, b, 2, 8, 5, 2, EPS, 0.01, f64=True), want, 0.0, "GN NCHW constant group")
+
+
 ALL_PINS = {
     "layer_norm": layer_norm_pins,
     "rms_channel": rms_channel_pins,
     "group_lrelu_x2": group_lrelu_x2_pins,
+    "group_lrelu_x2_nchw": group_lrelu_x2_nchw_pins,
 }

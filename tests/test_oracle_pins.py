@@ -60,6 +60,20 @@ MUTANTS = [
      "const double t = ((double)xg[j] - mean) / denom * w;"),
     ("group_lrelu_x2", "relu before affine", "const double t = ((double)xg[j] - mean) / denom * w + b;\n                const double l = fmax(0.0, t) + slope * fmin(0.0, t);",
      "const double u = ((double)xg[j] - mean) / denom;\n                const double t = (fmax(0.0, u) + slope * fmin(0.0, u)) * w + b;\n                const double l = t;"),
+    ("group_lrelu_x2_nchw", "count M, not M*S", "const double cnt = (double)(M * S);", "const double cnt = (double)M;"),
+    ("group_lrelu_x2_nchw", "positions read as channels", "sum += (double)x[(n * C + c) * S + s];",
+     "sum += (double)x[(n * S + s) * C + c];"),
+    ("group_lrelu_x2_nchw", "eps outside sqrt", "const double denom = sqrt(sq / cnt + eps);",
+     "const double denom = sqrt(sq / cnt) + eps;"),
+    ("group_lrelu_x2_nchw", "gamma per group", "const double gw = gamma ? (double)gamma[c] : 1.0;",
+     "const double gw = gamma ? (double)gamma[c0] : 1.0;"),
+    ("group_lrelu_x2_nchw", "beta per position", "const double v = ((double)x[i] - mean) / denom * gw + bw;",
+     "const double v = ((double)x[i] - mean) / denom * gw + (beta ? (double)beta[(c0 + s) % C] : 0.0);"),
+    ("group_lrelu_x2_nchw", "slope on positive side", "fmax(0.0, v) + slope * fmin(0.0, v)",
+     "slope * fmax(0.0, v) + fmin(0.0, v)"),
+    ("group_lrelu_x2_nchw", "x+x dropped", "oracle_store(l + l, i, y64, y32);", "oracle_store(l, i, y64, y32);"),
+    ("group_lrelu_x2_nchw", "variance about zero", "const double d = (double)x[(n * C + c) * S + s] - mean;",
+     "const double d = (double)x[(n * C + c) * S + s];"),
 ]
 
 
