@@ -80,8 +80,21 @@ CONFIGS = {
     "ln_rows": dict(op="ln", rows=16384, L=4096, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
                     workload="LayerNorm fp32 (16384, 4096) over the last dim, x~N(0,1), gamma~N(1,0.1), "
                              "beta~N(0,0.1), eps 1e-5 (many short rows)"),
+    # GroupNorm with a spatial extent: a group is its channels at every position
+    "gn_nchw": dict(op="gn_nchw", N=8, C=512, S=64 * 64, G=32, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
+                    workload="GroupNorm+LeakyReLU(0.01)+x2 fp32 NCHW (8,512,64,64), 32 groups of 16 channels x "
+                             "4096 positions (65,536 values), x~N(0,1), gamma~N(1,0.1), beta~N(0,0.1), eps 1e-5"),
+    "gn_nchw_bf16": dict(op="gn_nchw", N=8, C=512, S=64 * 64, G=32, x=(0.0, 1.0), gamma=(1.0, 0.1),
+                         beta=(0.0, 0.1), bf16=True,
+                         workload="GroupNorm+LeakyReLU(0.01)+x2 bf16 NCHW (8,512,64,64), 32 groups, fp32 "
+                                  "arithmetic"),
+    "gn_nchw_long": dict(op="gn_nchw", N=1, C=128, S=512 * 512, G=32, x=(0.0, 1.0), gamma=(1.0, 0.1),
+                         beta=(0.0, 0.1),
+                         workload="GroupNorm+LeakyReLU(0.01)+x2 fp32 NCHW (1,128,512,512), 32 groups of 4 "
+                                  "channels x 262144 positions (1,048,576 values: the two-kernel path)"),
 }
-EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_rows", "ln_rows_bf16", "gn_bf16", "rms_bf16"]
+EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_rows", "ln_rows_bf16", "gn_bf16", "rms_bf16",
+               "gn_nchw", "gn_nchw_bf16", "gn_nchw_long"]
 
 
 # ---------------------------------------------------------------------------- sizes
@@ -91,13 +104,15 @@ def elements(cfg) -> int:
         return cfg["rows"] * cfg["L"]
     if cfg["op"] == "gn":
         return cfg["N"] * cfg["C"]
+    if cfg["op"] == "gn_nchw":
+        return cfg["N"] * cfg["C"] * cfg["S"]
     return cfg["B"] * cfg["C"] * cfg["S"]
 
 
 def param_elems(cfg) -> int:
     if cfg["op"] == "ln":
         return 2 * cfg["L"]
-    if cfg["op"] == "gn":
+    if cfg["op"] in ("gn", "gn_nchw"):
         return 2 * cfg["C"]
     return 0
 
@@ -140,7 +155,7 @@ def host_inputs(cfg, seed=0):
     n = elements(cfg)
     x = normgen.normal(n, cfg["x"][0], cfg["x"][1], seed=seed, tensor_id=normgen.TENSOR_X)
     g = b = None
-    if cfg["op"] in ("ln", "gn"):
+    if cfg["op"] in ("ln", "gn", "gn_nchw"):
         pn = cfg["L"] if cfg["op"] == "ln" else cfg["C"]
         if cfg.get("gamma") == "ones":
             g = np.ones(pn, dtype=np.float32)
@@ -171,7 +186,15 @@ def main_kernel_name(cfg) -> str:
         return "ln_rows_kernel" if cfg["L"] <= 16384 else "ln_persistent_kernel"
     if cfg["op"] == "gn":
         return "gn_vec4_kernel"
+    if cfg["op"] == "gn_nchw":
+        return "gns_reg_kernel" if gn_nchw_one_launch(cfg) else "gns_split_apply_kernel"
     return "rms_reg_kernel"
+
+
+def gn_nchw_one_launch(cfg) -> bool:
+    """Groups of at most 131,072 values (a multiple of 4) take the one-launch register kernel."""
+    L = cfg["C"] // cfg["G"] * cfg["S"]
+    return L % 4 == 0 and L <= 131072
 
 
 def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
@@ -187,6 +210,10 @@ def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
     if op == "gn":
         fn = ng.norm_group_lrelu_x2_fwd_bf16 if bf16 else ng.norm_group_lrelu_x2_fwd
         return (lambda: fn(x, g, b, y, cfg["N"], cfg["C"], cfg["G"], 1e-5, 0.01, stream)), 1
+    if op == "gn_nchw":
+        fn = ng.norm_group_lrelu_x2_nchw_fwd_bf16 if bf16 else ng.norm_group_lrelu_x2_nchw_fwd
+        return ((lambda: fn(x, g, b, y, cfg["N"], cfg["C"], cfg["S"], cfg["G"], 1e-5, 0.01, ws, ws_bytes, stream)),
+                1 if gn_nchw_one_launch(cfg) else 2)
     fn = ng.norm_rms_channel_fwd_bf16 if bf16 else ng.norm_rms_channel_fwd
     return (lambda: fn(x, y, cfg["B"], cfg["C"], cfg["S"], 1e-5, stream)), 1
 
@@ -280,6 +307,7 @@ def hbm_peak():
 
 # the kernel source files each workload's counters depend on
 KERNEL_SOURCES = {"ln": ("ln_kernels.cu", "norm_internal.cuh"), "gn": ("gn_kernels.cu", "norm_internal.cuh"),
+                  "gn_nchw": ("gns_kernels.cu", "ln_kernels.cu", "norm_internal.cuh"),
                   "rms": ("rms_kernels.cu", "norm_internal.cuh")}
 
 
@@ -456,6 +484,9 @@ def run_config(ng, name, cfg, steps, warmup, stream, flush, l2_bytes, sampler=No
     if cfg["op"] == "ln":
         ws_bytes = ng.norm_layer_workspace_bytes(cfg["rows"], cfg["L"])
         ws = torch.zeros((ws_bytes + 3) // 4 + 64, dtype=torch.float32, device=dev)
+    elif cfg["op"] == "gn_nchw":
+        ws_bytes = ng.norm_group_lrelu_x2_nchw_workspace_bytes(cfg["N"], cfg["C"], cfg["S"], cfg["G"])
+        ws = torch.zeros((ws_bytes + 3) // 4 + 64, dtype=torch.float32, device=dev)
     calls = []
     launches = 1
     for xk, yk in zip(xs, ys):
@@ -552,6 +583,12 @@ def time_oracle(cfg, min_seconds, max_reps=1000, rows_per_step=None, x=None, g=N
         used = min(threads, rows)
     elif op == "gn":
         fn = lambda: o.group_lrelu_x2(x, g, b, cfg["N"], cfg["C"], cfg["G"], 1e-5, 0.01, threads=threads)  # noqa
+        nbytes = algorithmic_bytes(cfg)
+        sample = "the full workload per repetition"
+        used = min(threads, cfg["N"])
+    elif op == "gn_nchw":
+        fn = lambda: o.group_lrelu_x2_nchw(x, g, b, cfg["N"], cfg["C"], cfg["S"], cfg["G"], 1e-5, 0.01,  # noqa
+                                           threads=threads)
         nbytes = algorithmic_bytes(cfg)
         sample = "the full workload per repetition"
         used = min(threads, cfg["N"])

@@ -2,12 +2,14 @@
  * norm.h - C ABI of libnormgb300.so: fp32 reduce-then-apply normalization on
  * NVIDIA GB300 (sm_103a).
  *
- * Three operations, each one stream-ordered launch sequence of the library's
+ * Four operations, each one stream-ordered launch sequence of the library's
  * own CUDA kernels:
  *
- *   norm_layer_fwd           LayerNorm over very long contiguous rows
- *   norm_rms_channel_fwd     RMSNorm over dim 1 of an NCHW tensor
- *   norm_group_lrelu_x2_fwd  per-row GroupNorm, then LeakyReLU, then x + x
+ *   norm_layer_fwd                LayerNorm over very long contiguous rows
+ *   norm_rms_channel_fwd          RMSNorm over dim 1 of an NCHW tensor
+ *   norm_group_lrelu_x2_fwd       per-row GroupNorm, then LeakyReLU, then x + x
+ *   norm_group_lrelu_x2_nchw_fwd  the same over an NCHW tensor (groups span
+ *                                 channels and positions)
  *
  * Conventions shared by every entry point:
  *   - Pointers named x, y, gamma, beta, workspace are DEVICE pointers on the
@@ -184,8 +186,11 @@ norm_status_t norm_rms_channel_fwd_bf16(const uint16_t *x, uint16_t *y, int64_t 
  * gamma, beta   [C] per-channel weight and bias, or NULL (1 and 0).
  * num_groups    must divide C.
  * M a power of two in 4..128 with C % 4 == 0 and 16-byte aligned pointers
- * takes the vectorized kernel (4 channels per thread); any other M takes a
- * warp-per-group kernel.
+ * takes the vectorized kernel (4 channels per thread).  Any other M that is a
+ * multiple of 4 (up to 131,072, 16-byte aligned pointers) takes the register
+ * kernel of norm_group_lrelu_x2_nchw_fwd (one CTA, or a cluster of up to 16
+ * CTAs, per group); the rest a warp-per-group kernel that re-reads the group
+ * from cache.  Nothing is allocated.
  */
 norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const float *beta,
                                       float *y, int64_t N, int64_t C, int64_t num_groups,
@@ -198,6 +203,44 @@ norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const 
 norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta,
                                            uint16_t *y, int64_t N, int64_t C, int64_t num_groups,
                                            float eps, float negative_slope, cudaStream_t stream);
+
+/* GroupNorm + LeakyReLU + x2 over an NCHW tensor: the GroupNorm page's
+ * operation (as above) where each channel has S = H*W positions.
+ * x, y          [N][C][S] fp32, contiguous (NCHW with H*W flattened).
+ * Group g of sample n holds channels g*M .. g*M+M-1 (M = C / num_groups) at
+ * all S positions: the M*S values x[n][g*M .. g*M+M-1][0 .. S-1], which are
+ * contiguous.  Their population mean and variance normalize every one of
+ * them; gamma/beta [C] are per channel (or NULL: 1 and 0); then LeakyReLU
+ * and x + x.  S = 1 is norm_group_lrelu_x2_fwd.
+ * workspace     used only by the two-kernel path below: at least
+ *               norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, num_groups)
+ *               bytes, 16-byte aligned, no initial contents needed.  NULL:
+ *               the library allocates its own on first need and keeps it
+ *               (such calls must be serialized by the caller).  It must not
+ *               be a LayerNorm workspace that is still in use.
+ * Paths (L = M*S):
+ *   - L a multiple of 4 with 16-byte aligned pointers and L <= 131,072: one
+ *     launch; each group is held in registers by one CTA or by a thread-
+ *     block cluster of up to 16 CTAs that reduce the statistics through
+ *     distributed shared memory; x is read from HBM once;
+ *   - longer groups and unaligned vectors: a statistics kernel writes
+ *     per-chunk partials to the workspace and an apply kernel re-reads x;
+ *   - non-vector groups of at most 4,096 elements: one warp per group.
+ */
+size_t norm_group_lrelu_x2_nchw_workspace_bytes(int64_t N, int64_t C, int64_t S, int64_t num_groups);
+
+norm_status_t norm_group_lrelu_x2_nchw_fwd(const float *x, const float *gamma, const float *beta, float *y,
+                                           int64_t N, int64_t C, int64_t S, int64_t num_groups, float eps,
+                                           float negative_slope, void *workspace, size_t workspace_bytes,
+                                           cudaStream_t stream);
+
+/* The bfloat16 form (uint16_t bit patterns, fp32 arithmetic, y rounded to
+ * nearest even once; pointers 2-byte aligned, 8-byte aligned for the vector
+ * paths).  Otherwise as norm_group_lrelu_x2_nchw_fwd. */
+norm_status_t norm_group_lrelu_x2_nchw_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta,
+                                                uint16_t *y, int64_t N, int64_t C, int64_t S, int64_t num_groups,
+                                                float eps, float negative_slope, void *workspace,
+                                                size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ status
  * Synchronize `stream`, then read and clear the current device's error word.
@@ -234,13 +277,24 @@ const char *norm_status_string(norm_status_t status);
  *                                out.  Default 0.
  *   NORM_OPT_LN_CTAS             CTAs of the persistent kernel (0 = one per
  *                                SM, the default).
+ *   NORM_OPT_GN_PATH             GroupNorm: 0 = choose automatically, 1 =
+ *                                force the register kernel, 2 = force the
+ *                                two-kernel path (NCHW entry points only),
+ *                                3 = force the warp-per-group kernel (error
+ *                                NORM_ERR_UNSUPPORTED where the forced path
+ *                                cannot serve the call).
+ *   NORM_OPT_GN_CLUSTER          CTAs per group of the register kernel: 0 =
+ *                                the fewest that hold a group, or 1, 2, 4, 8
+ *                                or 16.
  * Returns NORM_ERR_INVALID_ARG for an unknown option or a negative value.
  */
 typedef enum {
     NORM_OPT_LN_PATH = 1,
     NORM_OPT_BARRIER_TIMEOUT_NS = 2,
     NORM_OPT_BARRIER_EXTRA_ARRIVALS = 3,
-    NORM_OPT_LN_CTAS = 4
+    NORM_OPT_LN_CTAS = 4,
+    NORM_OPT_GN_PATH = 5,
+    NORM_OPT_GN_CLUSTER = 6
 } norm_option_t;
 
 norm_status_t norm_set_option(norm_option_t option, int64_t value);

@@ -12,9 +12,12 @@ Entry points (same names and argument order as the C functions):
 * ``norm_layer_fwd_noalloc(x, gamma, beta, y, rows, row_len, eps, stream=None)``
 * ``norm_rms_channel_fwd(x, y, B, C, S, eps, stream=None)``
 * ``norm_group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream=None)``
-* ``norm_layer_fwd_bf16``, ``norm_rms_channel_fwd_bf16``, ``norm_group_lrelu_x2_fwd_bf16``: the
-  same arguments with bfloat16 tensors
+* ``norm_group_lrelu_x2_nchw_fwd(x, gamma, beta, y, N, C, S, num_groups, eps, negative_slope,
+  workspace=None, workspace_bytes=0, stream=None)``
+* ``norm_layer_fwd_bf16``, ``norm_rms_channel_fwd_bf16``, ``norm_group_lrelu_x2_fwd_bf16``,
+  ``norm_group_lrelu_x2_nchw_fwd_bf16``: the same arguments with bfloat16 tensors
 * ``norm_last_error(stream=None)``, ``norm_layer_workspace_bytes(rows, row_len)``,
+  ``norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, num_groups)``,
   ``norm_layer_workspace_reset(ws, nbytes, stream=None)``, ``norm_set_option``,
   ``norm_get_option``, ``norm_layer_max_resident_row_len()``
 
@@ -44,6 +47,8 @@ NORM_OPT_LN_PATH = 1
 NORM_OPT_BARRIER_TIMEOUT_NS = 2
 NORM_OPT_BARRIER_EXTRA_ARRIVALS = 3
 NORM_OPT_LN_CTAS = 4
+NORM_OPT_GN_PATH = 5
+NORM_OPT_GN_CLUSTER = 6
 
 # The C functions this binding exposes (every declaration of include/norm.h).
 EXPORTED = (
@@ -57,6 +62,9 @@ EXPORTED = (
     "norm_layer_fwd_bf16",
     "norm_rms_channel_fwd_bf16",
     "norm_group_lrelu_x2_fwd_bf16",
+    "norm_group_lrelu_x2_nchw_workspace_bytes",
+    "norm_group_lrelu_x2_nchw_fwd",
+    "norm_group_lrelu_x2_nchw_fwd_bf16",
     "norm_last_error",
     "norm_status_string",
     "norm_set_option",
@@ -101,6 +109,11 @@ _lib.norm_rms_channel_fwd_bf16.restype = _int
 _lib.norm_rms_channel_fwd_bf16.argtypes = [_vp, _vp, _i64, _i64, _i64, _f32, _vp]
 _lib.norm_group_lrelu_x2_fwd_bf16.restype = _int
 _lib.norm_group_lrelu_x2_fwd_bf16.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _vp]
+_lib.norm_group_lrelu_x2_nchw_workspace_bytes.restype = _sz
+_lib.norm_group_lrelu_x2_nchw_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64]
+for _name in ("norm_group_lrelu_x2_nchw_fwd", "norm_group_lrelu_x2_nchw_fwd_bf16"):
+    getattr(_lib, _name).restype = _int
+    getattr(_lib, _name).argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _vp, _sz, _vp]
 _lib.norm_last_error.restype = _int
 _lib.norm_last_error.argtypes = [_vp]
 _lib.norm_status_string.restype = ctypes.c_char_p
@@ -202,6 +215,25 @@ def norm_group_lrelu_x2_fwd_bf16(x, gamma, beta, y, N, C, num_groups, eps, negat
            "norm_group_lrelu_x2_fwd_bf16")
 
 
+def norm_group_lrelu_x2_nchw_workspace_bytes(N: int, C: int, S: int, num_groups: int) -> int:
+    return int(_lib.norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, num_groups))
+
+
+def norm_group_lrelu_x2_nchw_fwd(x, gamma, beta, y, N, C, S, num_groups, eps, negative_slope, workspace=None,
+                                 workspace_bytes=0, stream=None):
+    _check(_lib.norm_group_lrelu_x2_nchw_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), N, C, S, num_groups, eps,
+                                             negative_slope, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "norm_group_lrelu_x2_nchw_fwd")
+
+
+def norm_group_lrelu_x2_nchw_fwd_bf16(x, gamma, beta, y, N, C, S, num_groups, eps, negative_slope, workspace=None,
+                                      workspace_bytes=0, stream=None):
+    _check(_lib.norm_group_lrelu_x2_nchw_fwd_bf16(_ptr(x, True), _ptr(gamma, True), _ptr(beta, True),
+                                                  _ptr(y, True), N, C, S, num_groups, eps, negative_slope,
+                                                  _ptr(workspace), workspace_bytes, _stream(stream)),
+           "norm_group_lrelu_x2_nchw_fwd_bf16")
+
+
 def norm_last_error(stream=None) -> int:
     """Synchronize the stream; return (and clear) the device error word as a status code."""
     return int(_lib.norm_last_error(_stream(stream)))
@@ -259,10 +291,17 @@ def rms_norm_channel(x, eps: float = 1e-5, out=None, stream=None):
 
 def group_norm_lrelu_x2(x, num_groups: int, gamma=None, beta=None, eps: float = 1e-5,
                         negative_slope: float = 0.01, out=None, stream=None):
-    """2 * LeakyReLU(GroupNorm(x)) for a CUDA float32 or bfloat16 tensor of shape (N, C)."""
+    """2 * LeakyReLU(GroupNorm(x)) for a CUDA float32 or bfloat16 tensor of shape (N, C) or
+    (N, C, *spatial); a group spans its channels at every spatial position."""
     import torch
     N, C = int(x.shape[0]), int(x.shape[1])
     y = torch.empty_like(x) if out is None else out
-    fn = norm_group_lrelu_x2_fwd_bf16 if x.dtype == torch.bfloat16 else norm_group_lrelu_x2_fwd
-    fn(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream=stream)
+    bf16 = x.dtype == torch.bfloat16
+    if x.dim() == 2:
+        fn = norm_group_lrelu_x2_fwd_bf16 if bf16 else norm_group_lrelu_x2_fwd
+        fn(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream=stream)
+    else:
+        S = x.numel() // (N * C) if N * C else 0
+        fn = norm_group_lrelu_x2_nchw_fwd_bf16 if bf16 else norm_group_lrelu_x2_nchw_fwd
+        fn(x, gamma, beta, y, N, C, S, num_groups, eps, negative_slope, stream=stream)
     return y

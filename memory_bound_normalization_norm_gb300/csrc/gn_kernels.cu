@@ -129,47 +129,6 @@ cudaError_t launch_vec(const void *x, const void *gamma, const void *beta, void 
     return cudaGetLastError();
 }
 
-// Any M: one warp per (row, group); lanes stride over the group's channels.
-// Mean, then M2 about the mean (a second read that hits L1/L2), then apply.
-template <typename T>
-__global__ void __launch_bounds__(256) gn_warp_kernel(const T *x, const T *__restrict__ gamma,
-                                                      const T *__restrict__ beta, T *y, int64_t N,
-                                                      int64_t C, int64_t G, int64_t M, float eps, float slope)
-{
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const float invM = 1.0f / static_cast<float>(M);
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < N * G;
-         w += warps) {
-        const int64_t n = w / G, g = w - n * G;
-        const int64_t base = n * C + g * M;
-        float s = 0.f;
-        for (int64_t j = lane; j < M; j += 32)
-            s += Io<T>::ld1(x + base + j);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            s += __shfl_xor_sync(0xffffffffu, s, o);
-        const float mean = s * invM;
-        float q = 0.f;
-        for (int64_t j = lane; j < M; j += 32) {
-            const float d = Io<T>::ld1(x + base + j) - mean;
-            q = fmaf(d, d, q);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            q += __shfl_xor_sync(0xffffffffu, q, o);
-        const float rstd = rsqrtf(fmaf(q, invM, eps));
-        for (int64_t j = lane; j < M; j += 32) {
-            const int64_t c = g * M + j;
-            const float gw = gamma ? Io<T>::ld1(gamma + c) : 1.f;
-            const float bw = beta ? Io<T>::ld1(beta + c) : 0.f;
-            float t = fmaf((Io<T>::ld1(x + base + j) - mean) * rstd, gw, bw);
-            t = t > 0.f ? t : slope * t;
-            Io<T>::st1(y + base + j, t + t);
-        }
-    }
-}
-
 } // namespace
 
 // Two vectors a thread per row.
@@ -194,27 +153,6 @@ cudaError_t gn_vec4_launch(const void *x, const void *gamma, const void *beta, v
 {
     return bf16 ? gn_vec4_launch_t<__nv_bfloat16>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream)
                 : gn_vec4_launch_t<float>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
-}
-
-cudaError_t gn_warp_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
-                           int64_t G, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream)
-{
-    const int64_t warps_needed = N * G;
-    int64_t blocks = (warps_needed + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(sm_count) * 16;
-    if (blocks > cap)
-        blocks = cap;
-    if (blocks < 1)
-        blocks = 1;
-    if (bf16)
-        gn_warp_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(gamma),
-            static_cast<const __nv_bfloat16 *>(beta), static_cast<__nv_bfloat16 *>(y), N, C, G, C / G, eps, slope);
-    else
-        gn_warp_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const float *>(x), static_cast<const float *>(gamma), static_cast<const float *>(beta),
-            static_cast<float *>(y), N, C, G, C / G, eps, slope);
-    return cudaGetLastError();
 }
 
 } // namespace normk

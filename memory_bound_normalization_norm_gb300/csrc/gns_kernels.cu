@@ -1,0 +1,575 @@
+// gns_kernels.cu - GroupNorm + LeakyReLU + x2 over contiguous segments.
+//
+// The operation is the GroupNorm page's (POPCORNBENCH transcript "Kimi-K2.6
+// l2_p62": population mean and variance of each group, per-channel affine,
+// LeakyReLU(t) = max(0,t) + slope*min(0,t), then x + x), taken to tensors
+// with a spatial extent.  For x[N][C][S] (an NCHW tensor with S = H*W) the
+// group g of sample n holds channels g*M .. g*M+M-1 (M = C/G) at every
+// position: M*S values that are contiguous in memory.  So the tensor is R =
+// N*G segments of L = M*S elements, and element e of segment r belongs to
+// channel (r % G)*M + e/S.  The (N, C) form of the page is S = 1, L = M.
+//
+// Three kernels:
+//  - register path: a segment is split over a thread-block cluster of CL
+//    CTAs (CL = 1 for segments that fit one CTA).  Each CTA holds its slice
+//    in registers, so x is read from HBM once and y written once.  The mean
+//    (about the pivot x[r][0]) and then the exact M2 about the mean are
+//    reduced over the CTA and then over the cluster through distributed
+//    shared memory: every CTA publishes its partial in its own shared memory,
+//    the cluster barrier (a hardware barrier, not a spin on memory) orders
+//    it, and every warp reads the CL partials with ld.shared::cluster and
+//    sums them in lane order, so all CTAs get the same value.
+//  - split path (segments longer than a 16-CTA cluster holds, or unaligned
+//    vectors): the LayerNorm split path's statistics kernel writes one
+//    (n, mean, M2, pivot) partial per (segment, chunk), and the apply kernel
+//    here merges a segment's partials and applies, re-reading x.
+//  - warp path: one warp per segment with scalar loads for short segments
+//    that are not 4-element vectors (x re-read from L1).
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "norm_internal.cuh"
+
+namespace normk {
+
+namespace {
+
+// ------------------------------------------------------------------ cluster helpers
+
+__device__ __forceinline__ unsigned cluster_rank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ unsigned cluster_id_x()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ unsigned cluster_count_x()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives; shared-memory writes
+// before the arrive are visible to the cluster after the wait.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load the float at `local` (this CTA's shared memory) from the same offset
+// in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_peer_f32(const float *local, unsigned rank)
+{
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(local));
+    unsigned ra;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+// Cluster-wide sum of v (identical in all threads of a CTA): thread 0
+// publishes it in `slot`, then each warp adds the cluster's CL values in
+// lane order.  `slot` must not be rewritten until every CTA has passed the
+// next cluster barrier.
+__device__ __forceinline__ float cluster_sum(float v, float *slot, unsigned CL)
+{
+    if (threadIdx.x == 0)
+        *slot = v;
+    cluster_sync_all();
+    const unsigned lane = threadIdx.x & 31;
+    float t = lane < CL ? ld_peer_f32(slot, lane) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+
+// ------------------------------------------------------------------ epilogue
+
+__device__ __forceinline__ float lrelu_x2(float t, float slope)
+{
+    t = t > 0.f ? t : slope * t;
+    return t + t;
+}
+
+__device__ __forceinline__ int64_t seg_div(int64_t e, int64_t S, bool narrow)
+{
+    return narrow ? static_cast<int64_t>(static_cast<uint32_t>(e) / static_cast<uint32_t>(S)) : e / S;
+}
+
+// How the four elements e .. e+3 (e a multiple of 4) map to channels.
+enum AffineMode {
+    AFF_ROW = 0,  // S == 1: four consecutive channels (one vector load)
+    AFF_CHAN = 1, // S % 4 == 0: one channel
+    AFF_ANY = 2,  // anything else: per element
+};
+
+__host__ __device__ constexpr int affine_mode(int64_t S)
+{
+    return S == 1 ? AFF_ROW : (S & 3) == 0 ? AFF_CHAN : AFF_ANY;
+}
+
+// gamma/beta of elements e .. e+3 of a segment whose first channel is cbase.
+template <typename T, int MODE>
+__device__ __forceinline__ void seg_affine4(const T *gm, const T *bt, int64_t cbase, int64_t e, int64_t S,
+                                            bool narrow, uint64_t pol, float4 &g, float4 &b)
+{
+    if (MODE == AFF_ROW) {
+        g = gm ? Io<T>::ld4_ro(gm + cbase + e, pol) : make_float4(1.f, 1.f, 1.f, 1.f);
+        b = bt ? Io<T>::ld4_ro(bt + cbase + e, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (MODE == AFF_CHAN) {
+        const int64_t c = cbase + seg_div(e, S, narrow);
+        const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
+        g = make_float4(gv, gv, gv, gv);
+        b = make_float4(bv, bv, bv, bv);
+    } else {
+        float gv[4], bv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t c = cbase + seg_div(e + k, S, narrow);
+            gv[k] = gm ? Io<T>::ld1(gm + c) : 1.f;
+            bv[k] = bt ? Io<T>::ld1(bt + c) : 0.f;
+        }
+        g = make_float4(gv[0], gv[1], gv[2], gv[3]);
+        b = make_float4(bv[0], bv[1], bv[2], bv[3]);
+    }
+}
+
+__device__ __forceinline__ float4 gn_apply4(float4 v, const RowMean &rm, float4 g, float4 b, float slope)
+{
+    float4 t = ln_apply4(v, rm, g, b);
+    t.x = lrelu_x2(t.x, slope);
+    t.y = lrelu_x2(t.y, slope);
+    t.z = lrelu_x2(t.z, slope);
+    t.w = lrelu_x2(t.w, slope);
+    return t;
+}
+
+// ------------------------------------------------------------------ register path
+
+// grid: clusters of CL CTAs (CL = p.parts), each cluster walks segments
+// r = cluster id, + cluster count, ...; CTA `rank` of a cluster owns vectors
+// [rank*per, rank*per + per) of every segment it visits.
+template <typename T, int NT, int V, int MODE>
+__global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
+{
+    __shared__ float red[2][NT / 32];
+    __shared__ float xch[2];
+    const int tid = threadIdx.x;
+    const unsigned CL = static_cast<unsigned>(p.parts);
+    const bool clustered = CL > 1;
+    const unsigned rank = clustered ? cluster_rank() : 0u;
+    const int64_t cid = clustered ? cluster_id_x() : blockIdx.x;
+    const int64_t ncl = clustered ? cluster_count_x() : gridDim.x;
+    const int64_t L4 = p.seg_len >> 2;
+    const int64_t per = (L4 + CL - 1) / CL;
+    const int64_t lo = per * rank;
+    const int64_t n4 = lo < L4 ? (L4 - lo < per ? L4 - lo : per) : 0;
+    const float Lf = static_cast<float>(p.seg_len);
+    constexpr bool narrow = true; // segments here are at most 16 * NT * V * 4 elements
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.y);
+    const T *gm = static_cast<const T *>(p.gamma);
+    const T *bt = static_cast<const T *>(p.beta);
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    for (int64_t r = cid; r < p.rows; r += ncl) {
+        const T *xr = x + r * p.seg_len;
+        float4 v[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t i = tid + k * NT;
+            v[k] = i < n4 ? Io<T>::ld4_stream(xr + 4 * (lo + i), pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // Every CTA of the cluster reads the pivot before the first cluster
+        // barrier and stores only after the second, so y == x is safe.
+        const float K = Io<T>::ld1(xr);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            if (tid + k * NT < n4)
+                s += ((v[k].x - K) + (v[k].y - K)) + ((v[k].z - K) + (v[k].w - K));
+        }
+        s = block_sum<NT>(s, red[0]);
+        if (clustered)
+            s = cluster_sum(s, &xch[0], CL);
+        Moments tot;
+        tot.n = Lf;
+        tot.mean = s / Lf;
+        tot.m2 = 0.f;
+        RowMean rm = finish_row(K, tot, p.eps);
+        float q = 0.f;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            if (tid + k * NT < n4) {
+                const float a = (v[k].x - rm.hi) - rm.lo, b = (v[k].y - rm.hi) - rm.lo;
+                const float c = (v[k].z - rm.hi) - rm.lo, d = (v[k].w - rm.hi) - rm.lo;
+                q += (a * a + b * b) + (c * c + d * d);
+            }
+        }
+        q = block_sum<NT>(q, red[1]);
+        if (clustered)
+            q = cluster_sum(q, &xch[1], CL);
+        rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        const int64_t cbase = (r % p.G) * p.M;
+        T *yr = y + r * p.seg_len;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t i = tid + k * NT;
+            if (i < n4) {
+                const int64_t e = 4 * (lo + i);
+                float4 g, b;
+                seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, b);
+                Io<T>::st4_stream(yr + e, gn_apply4(v[k], rm, g, b, p.slope), pol_stream);
+            }
+        }
+    }
+    // no CTA may exit while a peer can still read its partials
+    if (clustered)
+        cluster_sync_all();
+}
+
+// ------------------------------------------------------------------ split path: apply
+
+constexpr int GS_T = 256;
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(GS_T) gns_split_apply_kernel(GnSegParams p)
+{
+    __shared__ RowMean row_mean;
+    const int P = p.parts;
+    const bool narrow = p.seg_len <= int64_t(0xffffffff);
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.y);
+    const T *gm = static_cast<const T *>(p.gamma);
+    const T *bt = static_cast<const T *>(p.beta);
+    for (int64_t r = blockIdx.y; r < p.rows; r += gridDim.y) {
+        const int pc = blockIdx.x;
+        const T *xr = x + r * p.seg_len;
+        T *yr = y + r * p.seg_len;
+        if (threadIdx.x < 32) {
+            const float K = ld_l2_f4(p.part + r * P).w;
+            const Moments tot = merge_partials_warp(p.part + r * P, P, K);
+            if (threadIdx.x == 0)
+                row_mean = finish_row(K, tot, p.eps);
+        }
+        __syncthreads();
+        const RowMean rm = row_mean;
+        const int64_t cbase = (r % p.G) * p.M;
+        const int64_t lo = static_cast<int64_t>(pc) * p.chunk;
+        const int64_t hi = (lo + p.chunk < p.seg_len) ? lo + p.chunk : p.seg_len;
+        if (VEC) {
+            const uint64_t pol = policy_evict_first();
+            const uint64_t pol_gb = policy_evict_last();
+            for (int64_t i = lo / 4 + threadIdx.x; i < hi / 4; i += GS_T) {
+                const float4 q = Io<T>::ld4_stream(xr + 4 * i, pol);
+                float4 g, b;
+                switch (affine_mode(p.S)) {
+                case AFF_ROW: seg_affine4<T, AFF_ROW>(gm, bt, cbase, 4 * i, p.S, narrow, pol_gb, g, b); break;
+                case AFF_CHAN: seg_affine4<T, AFF_CHAN>(gm, bt, cbase, 4 * i, p.S, narrow, pol_gb, g, b); break;
+                default: seg_affine4<T, AFF_ANY>(gm, bt, cbase, 4 * i, p.S, narrow, pol_gb, g, b); break;
+                }
+                Io<T>::st4_stream(yr + 4 * i, gn_apply4(q, rm, g, b, p.slope), pol);
+            }
+        } else {
+            for (int64_t i = lo + threadIdx.x; i < hi; i += GS_T) {
+                const int64_t c = cbase + seg_div(i, p.S, narrow);
+                const float g = gm ? Io<T>::ld1(gm + c) : 1.f;
+                const float b = bt ? Io<T>::ld1(bt + c) : 0.f;
+                const float t = fmaf(((Io<T>::ld1(xr + i) - rm.hi) - rm.lo) * rm.rstd, g, b);
+                Io<T>::st1(yr + i, lrelu_x2(t, p.slope));
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ warp path
+
+// One warp per segment: mean, then M2 about the mean (a second read that
+// hits L1/L2), then apply (a third).
+template <typename T>
+__global__ void __launch_bounds__(256) gns_warp_kernel(GnSegParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const bool narrow = p.seg_len <= int64_t(0xffffffff);
+    const float Lf = static_cast<float>(p.seg_len);
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.y);
+    const T *gm = static_cast<const T *>(p.gamma);
+    const T *bt = static_cast<const T *>(p.beta);
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < p.rows;
+         r += warps) {
+        const T *xr = x + r * p.seg_len;
+        T *yr = y + r * p.seg_len;
+        // the pivot keeps the sum small when |mean| >> std
+        const float K = Io<T>::ld1(xr);
+        float s = 0.f;
+        for (int64_t j = lane; j < p.seg_len; j += 32)
+            s += Io<T>::ld1(xr + j) - K;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+        Moments tot;
+        tot.n = Lf;
+        tot.mean = s / Lf;
+        tot.m2 = 0.f;
+        RowMean rm = finish_row(K, tot, p.eps);
+        float q = 0.f;
+        for (int64_t j = lane; j < p.seg_len; j += 32) {
+            const float d = (Io<T>::ld1(xr + j) - rm.hi) - rm.lo;
+            q = fmaf(d, d, q);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            q += __shfl_xor_sync(0xffffffffu, q, o);
+        rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        const int64_t cbase = (r % p.G) * p.M;
+        // every lane has read the whole segment (the shuffles above are
+        // warp-wide), so with y == x the stores below are safe
+        for (int64_t j = lane; j < p.seg_len; j += 32) {
+            const int64_t c = cbase + seg_div(j, p.S, narrow);
+            const float g = gm ? Io<T>::ld1(gm + c) : 1.f;
+            const float b = bt ? Io<T>::ld1(bt + c) : 0.f;
+            const float t = fmaf(((Io<T>::ld1(xr + j) - rm.hi) - rm.lo) * rm.rstd, g, b);
+            Io<T>::st1(yr + j, lrelu_x2(t, p.slope));
+        }
+    }
+}
+
+// ------------------------------------------------------------------ register-path dispatch
+
+constexpr int GNS_MAX_V = 8;
+constexpr int GNS_MAX_NT = 256;
+constexpr int GNS_MAX_CLUSTER = 16;
+
+using RegKernel = void (*)(GnSegParams);
+
+constexpr int GNS_VARIANTS = 18; // 6 CTA shapes x 3 affine modes
+
+// Threads and vectors per thread for a CTA slice of `per` vectors: the
+// smallest CTA that holds it with at most 4 (64 threads) or 8 vectors a
+// thread, vectors a power of two.  *idx numbers the variant.
+template <typename T, int MODE>
+RegKernel reg_kernel_for(int64_t per, int *nt, int *idx)
+{
+    *nt = 0;
+    *idx = -1;
+    if (per <= 0 || per > 2048)
+        return nullptr;
+    if (per <= 64) {
+        *nt = 64, *idx = 0;
+        return gns_reg_kernel<T, 64, 1, MODE>;
+    }
+    if (per <= 128) {
+        *nt = 64, *idx = 1;
+        return gns_reg_kernel<T, 64, 2, MODE>;
+    }
+    if (per <= 256) {
+        *nt = 64, *idx = 2;
+        return gns_reg_kernel<T, 64, 4, MODE>;
+    }
+    if (per <= 512) {
+        *nt = 128, *idx = 3;
+        return gns_reg_kernel<T, 128, 4, MODE>;
+    }
+    if (per <= 1024) {
+        *nt = 128, *idx = 4;
+        return gns_reg_kernel<T, 128, 8, MODE>;
+    }
+    *nt = 256, *idx = 5;
+    return gns_reg_kernel<T, 256, 8, MODE>;
+}
+
+template <typename T>
+RegKernel reg_kernel_t(int64_t per, int mode, int *nt, int *idx)
+{
+    switch (mode) {
+    case AFF_ROW: return reg_kernel_for<T, AFF_ROW>(per, nt, idx);
+    case AFF_CHAN: return reg_kernel_for<T, AFF_CHAN>(per, nt, idx);
+    default: return reg_kernel_for<T, AFF_ANY>(per, nt, idx);
+    }
+}
+
+// The kernel for a segment of seg_len elements with S positions per channel
+// over `cluster` CTAs; *idx numbers it among the variants of its dtype.
+RegKernel reg_kernel(int64_t seg_len, int64_t S, bool bf16, int cluster, int *nt, int *idx)
+{
+    const int64_t L4 = seg_len / 4;
+    const int64_t per = (L4 + cluster - 1) / cluster;
+    const int mode = affine_mode(S);
+    const RegKernel k = bf16 ? reg_kernel_t<__nv_bfloat16>(per, mode, nt, idx)
+                             : reg_kernel_t<float>(per, mode, nt, idx);
+    *idx += 6 * mode;
+    return k;
+}
+
+void cluster_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, int nt, int cluster, unsigned grid,
+                    cudaStream_t stream)
+{
+    std::memset(cfg, 0, sizeof(*cfg));
+    cfg->gridDim = dim3(grid);
+    cfg->blockDim = dim3(static_cast<unsigned>(nt));
+    cfg->dynamicSmemBytes = 0;
+    cfg->stream = stream;
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
+
+int log2_cluster(int cluster)
+{
+    int l = 0;
+    while ((1 << l) < cluster)
+        ++l;
+    return l;
+}
+
+// Co-resident clusters per (device, dtype, variant, cluster size), queried
+// once: -1 = not yet known.
+constexpr int GNS_DEVICES = 64;
+std::atomic<int> g_active[GNS_DEVICES][2][GNS_VARIANTS][5];
+std::once_flag g_active_init;
+
+cudaError_t query_active(RegKernel k, int nt, int cluster, int *clusters)
+{
+    *clusters = 0;
+    if (cluster == 1) {
+        int per_sm = 0, sms = 0, dev = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, nt, 0);
+        if (e == cudaSuccess)
+            e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        *clusters = per_sm * sms;
+        return e;
+    }
+    if (cluster > 8) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess)
+            return e;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr;
+    cluster_config(&cfg, &attr, nt, cluster, static_cast<unsigned>(cluster), 0);
+    return cudaOccupancyMaxActiveClusters(clusters, k, &cfg);
+}
+
+} // namespace
+
+int64_t gns_reg_capacity4(int cluster)
+{
+    return int64_t(GNS_MAX_NT) * GNS_MAX_V * cluster;
+}
+
+cudaError_t gns_reg_max_clusters(int64_t seg_len, int64_t S, bool bf16, int cluster, int *clusters)
+{
+    *clusters = 0;
+    if (cluster < 1 || cluster > GNS_MAX_CLUSTER || (cluster & (cluster - 1)) != 0)
+        return cudaErrorInvalidValue;
+    int nt = 0, idx = 0, dev = 0;
+    const RegKernel k = reg_kernel(seg_len, S, bf16, cluster, &nt, &idx);
+    if (!k)
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::call_once(g_active_init, [] {
+        for (auto &a : g_active)
+            for (auto &b : a)
+                for (auto &c : b)
+                    for (auto &v : c)
+                        v.store(-1);
+    });
+    std::atomic<int> *slot =
+        dev >= 0 && dev < GNS_DEVICES ? &g_active[dev][bf16 ? 1 : 0][idx][log2_cluster(cluster)] : nullptr;
+    if (slot) {
+        const int known = slot->load();
+        if (known >= 0) {
+            *clusters = known;
+            return cudaSuccess;
+        }
+    }
+    e = query_active(k, nt, cluster, clusters);
+    if (e == cudaSuccess && slot)
+        slot->store(*clusters);
+    return e;
+}
+
+cudaError_t gns_reg_launch(const GnSegParams &p, bool bf16, int cluster, cudaStream_t stream)
+{
+    int nt = 0, idx = 0;
+    const RegKernel k = reg_kernel(p.seg_len, p.S, bf16, cluster, &nt, &idx);
+    if (!k)
+        return cudaErrorInvalidValue;
+    int active = 0;
+    cudaError_t e = gns_reg_max_clusters(p.seg_len, p.S, bf16, cluster, &active);
+    if (e != cudaSuccess)
+        return e;
+    if (active < 1)
+        return cudaErrorInvalidConfiguration;
+    // every co-resident cluster walks segments; no more clusters than segments
+    int64_t clusters = active;
+    if (clusters > p.rows)
+        clusters = p.rows;
+    GnSegParams args = p;
+    args.parts = cluster;
+    const unsigned grid = static_cast<unsigned>(clusters * cluster);
+    if (cluster == 1) {
+        k<<<grid, nt, 0, stream>>>(args);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr;
+    cluster_config(&cfg, &attr, nt, cluster, grid, stream);
+    return cudaLaunchKernelEx(&cfg, k, args);
+}
+
+cudaError_t gns_split_apply_launch(const GnSegParams &p, bool bf16, bool vec4, cudaStream_t stream)
+{
+    dim3 grid(static_cast<unsigned>(p.parts), static_cast<unsigned>(p.rows < 65535 ? p.rows : 65535));
+    if (bf16) {
+        if (vec4)
+            gns_split_apply_kernel<__nv_bfloat16, true><<<grid, GS_T, 0, stream>>>(p);
+        else
+            gns_split_apply_kernel<__nv_bfloat16, false><<<grid, GS_T, 0, stream>>>(p);
+    } else {
+        if (vec4)
+            gns_split_apply_kernel<float, true><<<grid, GS_T, 0, stream>>>(p);
+        else
+            gns_split_apply_kernel<float, false><<<grid, GS_T, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t gns_warp_launch(const GnSegParams &p, bool bf16, int sm_count, cudaStream_t stream)
+{
+    int64_t blocks = (p.rows + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 16;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    if (bf16)
+        gns_warp_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    else
+        gns_warp_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+} // namespace normk

@@ -84,68 +84,6 @@ static_assert(LN_APPLY_WARP0 % 4 == 0 && LN_A % 128 == 0, "apply warps fill whol
 static_assert((LN_THREADS / 128 - 1) * LN_TM_COLS <= static_cast<int>(LN_TMEM_COLS),
               "gamma/beta of a quarter fit TMEM");
 
-struct RowMean {
-    float hi, lo, rstd;
-};
-
-// Fold `cnt` partials part[0..cnt) = (n, mean of x - K_i, M2, K_i) in a
-// fixed order with one warp; every mean is first re-expressed against K_ref.
-// All lanes return the same result.  Count-weighted, so empty partials are
-// harmless.
-__device__ __forceinline__ Moments merge_partials_warp(const float4 *part, int cnt, float K_ref)
-{
-    const int lane = threadIdx.x & 31;
-    Moments acc = {0.f, 0.f, 0.f};
-    for (int i = lane; i < cnt; i += 32) {
-        const float4 q = ld_l2_f4(part + i);
-        const Moments m = {q.x, (q.w - K_ref) + q.y, q.z};
-        chan_merge(acc, m);
-    }
-    return warp_merge(acc);
-}
-
-__device__ __forceinline__ RowMean finish_row(float K, const Moments &tot, float eps)
-{
-    // mean = K + tot.mean, kept as an exact two-term sum (Knuth TwoSum).
-    const float s = K + tot.mean;
-    const float bp = s - K;
-    const float err = (K - (s - bp)) + (tot.mean - bp);
-    const float var = fmaxf(tot.m2 / tot.n, 0.f);
-    RowMean rm;
-    rm.hi = s;
-    rm.lo = err;
-    rm.rstd = rsqrtf(var + eps);
-    return rm;
-}
-
-__device__ __forceinline__ float4 ln_apply4(float4 v, const RowMean &rm, float4 g, float4 b)
-{
-    float4 o;
-    o.x = fmaf(((v.x - rm.hi) - rm.lo) * rm.rstd, g.x, b.x);
-    o.y = fmaf(((v.y - rm.hi) - rm.lo) * rm.rstd, g.y, b.y);
-    o.z = fmaf(((v.z - rm.hi) - rm.lo) * rm.rstd, g.z, b.z);
-    o.w = fmaf(((v.w - rm.hi) - rm.lo) * rm.rstd, g.w, b.w);
-    return o;
-}
-
-// CTA-wide fold of per-thread triples; the result is valid in thread 0.
-template <int T>
-__device__ __forceinline__ Moments cta_merge(Moments m, Moments *scratch)
-{
-    m = warp_merge(m);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0)
-        scratch[warp] = m;
-    __syncthreads();
-    Moments r = {0.f, 0.f, 0.f};
-    if (warp == 0) {
-        if (lane < T / 32)
-            r = scratch[lane];
-        r = warp_merge(r);
-    }
-    return r;
-}
-
 // ---------------------------------------------------------------- persistent path
 
 __device__ __forceinline__ unsigned long long tagged(unsigned tag, float v)
@@ -631,25 +569,6 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 
 constexpr int LR_T = 256;
 
-// Sum of v over a CTA of NT threads, in a fixed order; every thread gets the
-// result.  `scratch` (NT / 32 floats) must not be in use by the previous call.
-template <int NT>
-__device__ __forceinline__ float block_sum(float v, float *scratch)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0)
-        scratch[warp] = v;
-    __syncthreads();
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < NT / 32; ++w)
-        t += scratch[w];
-    return t;
-}
-
 // NT threads a CTA, V 4-element vectors a thread.
 template <typename T, int NT, int V>
 __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
@@ -915,6 +834,23 @@ cudaError_t ln_split_launch_t(const LnParams &p, bool vec4, cudaStream_t stream)
 cudaError_t ln_split_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_t stream)
 {
     return bf16 ? ln_split_launch_t<__nv_bfloat16>(p, vec4, stream) : ln_split_launch_t<float>(p, vec4, stream);
+}
+
+cudaError_t ln_split_stats_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_t stream)
+{
+    dim3 grid(static_cast<unsigned>(p.parts), static_cast<unsigned>(p.rows < 65535 ? p.rows : 65535));
+    if (bf16) {
+        if (vec4)
+            ln_split_stats_kernel<__nv_bfloat16, true><<<grid, LS_T, 0, stream>>>(p);
+        else
+            ln_split_stats_kernel<__nv_bfloat16, false><<<grid, LS_T, 0, stream>>>(p);
+    } else {
+        if (vec4)
+            ln_split_stats_kernel<float, true><<<grid, LS_T, 0, stream>>>(p);
+        else
+            ln_split_stats_kernel<float, false><<<grid, LS_T, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
 }
 
 } // namespace normk

@@ -34,6 +34,8 @@ struct DeviceState {
     unsigned *err = nullptr;
     void *ws = nullptr;
     size_t ws_bytes = 0;
+    void *gn_ws = nullptr; // GroupNorm split-path partials (never shared with LayerNorm)
+    size_t gn_ws_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -43,6 +45,8 @@ std::atomic<int64_t> g_opt_ln_path{0};
 std::atomic<int64_t> g_opt_timeout_ns{200000000};
 std::atomic<int64_t> g_opt_extra_arrivals{0};
 std::atomic<int64_t> g_opt_ln_ctas{0};
+std::atomic<int64_t> g_opt_gn_path{0};
+std::atomic<int64_t> g_opt_gn_cluster{0};
 
 // Resolve (and on first use initialize) the state of the current device.
 norm_status_t device_state(DeviceState **out)
@@ -210,6 +214,51 @@ bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
     return true;
 }
 
+// ------------------------------------------------------------------ GN plan
+
+// Segment GroupNorm paths (NORM_OPT_GN_PATH values).
+constexpr int kGnReg = 1, kGnSplit = 2, kGnWarp = 3;
+// Longest non-vector segment the warp path takes on its own.
+constexpr int64_t kGnWarpMaxLen = 4096;
+
+struct GnPlan {
+    int path = 0;
+    bool vec4 = false;
+    int parts = 0;
+    int64_t chunk = 0;
+    size_t ws_bytes = 0;
+};
+
+// Smallest cluster whose CTAs each hold at most a full CTA slice.
+int gn_auto_cluster(int64_t L4)
+{
+    for (int cl = 1; cl <= 16; cl <<= 1)
+        if ((L4 + cl - 1) / cl <= normk::gns_reg_capacity4(1))
+            return cl;
+    return 0;
+}
+
+// Partials of the split path: R * P triples; P as the LayerNorm split path.
+void plan_gn_split(int64_t R, int64_t L, bool vec4, const DeviceState &d, GnPlan *pl)
+{
+    LnPlan lp;
+    plan_split(R, L, vec4, d, &lp);
+    pl->path = kGnSplit;
+    pl->vec4 = vec4;
+    pl->parts = lp.parts;
+    pl->chunk = lp.chunk;
+    pl->ws_bytes = static_cast<size_t>(R) * static_cast<size_t>(lp.parts) * 16u;
+}
+
+// Upper bound of plan_gn_split's workspace over both vector forms.
+size_t gn_split_ws_bound(int64_t R, int64_t L, const DeviceState &d)
+{
+    GnPlan a, b;
+    plan_gn_split(R, L, false, d, &a);
+    plan_gn_split(R, L, true, d, &b);
+    return a.ws_bytes > b.ws_bytes ? a.ws_bytes : b.ws_bytes;
+}
+
 } // namespace
 
 extern "C" {
@@ -251,6 +300,16 @@ norm_status_t norm_set_option(norm_option_t option, int64_t value)
     case NORM_OPT_LN_CTAS:
         g_opt_ln_ctas = value;
         return NORM_OK;
+    case NORM_OPT_GN_PATH:
+        if (value > 3)
+            return NORM_ERR_INVALID_ARG;
+        g_opt_gn_path = value;
+        return NORM_OK;
+    case NORM_OPT_GN_CLUSTER:
+        if (value > 16 || (value & (value - 1)) != 0)
+            return NORM_ERR_INVALID_ARG;
+        g_opt_gn_cluster = value;
+        return NORM_OK;
     }
     return NORM_ERR_INVALID_ARG;
 }
@@ -262,6 +321,8 @@ int64_t norm_get_option(norm_option_t option)
     case NORM_OPT_BARRIER_TIMEOUT_NS: return g_opt_timeout_ns.load();
     case NORM_OPT_BARRIER_EXTRA_ARRIVALS: return g_opt_extra_arrivals.load();
     case NORM_OPT_LN_CTAS: return g_opt_ln_ctas.load();
+    case NORM_OPT_GN_PATH: return g_opt_gn_path.load();
+    case NORM_OPT_GN_CLUSTER: return g_opt_gn_cluster.load();
     }
     return -1;
 }
@@ -447,13 +508,17 @@ norm_status_t rms_channel_fwd(const void *x, void *y, int64_t B, int64_t C, int6
     return NORM_OK;
 }
 
-// GroupNorm + LeakyReLU + x2 on tensors of esz-byte elements.
+// GroupNorm + LeakyReLU + x2 over x[N][C][S] of esz-byte elements.  The
+// (N, C) entry points pass S = 1 and nchw = false: they take the page's
+// vector kernel where it applies and never the split path (they have no
+// workspace).
 norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
-                                 int64_t num_groups, float eps, float negative_slope, cudaStream_t stream, int esz)
+                                 int64_t S, int64_t num_groups, float eps, float negative_slope, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream, int esz, bool nchw)
 {
-    int64_t n = 0;
-    if (N < 0 || C < 0 || num_groups <= 0 || !valid_eps(eps) || !std::isfinite(negative_slope) ||
-        !safe_mul(N, C, &n))
+    int64_t nc = 0, n = 0;
+    if (N < 0 || C < 0 || S < 0 || num_groups <= 0 || !valid_eps(eps) || !std::isfinite(negative_slope) ||
+        !safe_mul(N, C, &nc) || !safe_mul(nc, S, &n))
         return NORM_ERR_INVALID_ARG;
     if (C % num_groups != 0)
         return NORM_ERR_INVALID_ARG;
@@ -466,19 +531,121 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     const size_t nb = static_cast<size_t>(n) * esz, pb = static_cast<size_t>(C) * esz;
     if ((x != y && overlaps(x, nb, y, nb)) || overlaps(gamma, pb, y, nb) || overlaps(beta, pb, y, nb))
         return NORM_ERR_INVALID_ARG;
+    if (workspace && (!aligned(workspace, 16) || overlaps(workspace, workspace_bytes, y, nb) ||
+                      overlaps(workspace, workspace_bytes, x, nb)))
+        return NORM_ERR_WORKSPACE;
     DeviceState *d = nullptr;
     norm_status_t st = device_state(&d);
     if (st != NORM_OK)
         return st;
-    const int64_t M = C / num_groups;
-    const bool pow2 = M >= 4 && M <= 128 && (M & (M - 1)) == 0;
-    const uintptr_t va = 4u * esz;
-    const bool vec = pow2 && (C & 3) == 0 && C / 4 < (int64_t(1) << 30) && aligned(x, va) && aligned(y, va) &&
-                     aligned(gamma, va) && aligned(beta, va);
     const bool bf16 = esz == 2;
-    cudaError_t e = vec ? normk::gn_vec4_launch(x, gamma, beta, y, N, C, M, eps, negative_slope, bf16, d->sm_count, stream)
-                        : normk::gn_warp_launch(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, bf16,
-                                                d->sm_count, stream);
+    const int64_t M = C / num_groups, L = M * S, R = N * num_groups;
+    const uintptr_t va = 4u * esz;
+    const bool vec4 = (L & 3) == 0 && aligned(x, va) && aligned(y, va) && aligned(gamma, va) && aligned(beta, va);
+    const int64_t opt = g_opt_gn_path.load();
+    cudaError_t e;
+
+    // The page's design: M a power of two in 4..128, 4 channels a thread.
+    const bool pow2 = M >= 4 && M <= 128 && (M & (M - 1)) == 0;
+    if (opt == 0 && S == 1 && pow2 && vec4 && (C & 3) == 0 && C / 4 < (int64_t(1) << 30)) {
+        e = normk::gn_vec4_launch(x, gamma, beta, y, N, C, M, eps, negative_slope, bf16, d->sm_count, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return NORM_ERR_CUDA;
+        }
+        return NORM_OK;
+    }
+
+    // Register path: the smallest cluster that holds a segment (or the
+    // forced one), if such clusters can be resident.
+    int cluster = 0;
+    if (vec4) {
+        const int64_t forced = g_opt_gn_cluster.load();
+        const int64_t L4 = L / 4;
+        cluster = forced ? static_cast<int>(forced) : gn_auto_cluster(L4);
+        if (cluster && (L4 + cluster - 1) / cluster > normk::gns_reg_capacity4(1))
+            cluster = 0;
+        int active = 0;
+        if (cluster && (normk::gns_reg_max_clusters(L, S, bf16, cluster, &active) != cudaSuccess || active < 1)) {
+            cudaGetLastError();
+            cluster = 0;
+        }
+    }
+    GnPlan pl;
+    if (opt == kGnReg && !cluster)
+        return NORM_ERR_UNSUPPORTED;
+    if (opt == kGnSplit && !nchw)
+        return NORM_ERR_UNSUPPORTED;
+    if (opt)
+        pl.path = static_cast<int>(opt);
+    else if (cluster)
+        pl.path = kGnReg;
+    else if (!nchw || (!vec4 && L <= kGnWarpMaxLen))
+        pl.path = kGnWarp;
+    else
+        pl.path = kGnSplit;
+
+    normk::GnSegParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = x;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.y = y;
+    p.rows = R;
+    p.seg_len = L;
+    p.G = num_groups;
+    p.M = M;
+    p.S = S;
+    p.eps = eps;
+    p.slope = negative_slope;
+
+    if (pl.path == kGnReg) {
+        e = normk::gns_reg_launch(p, bf16, cluster, stream);
+    } else if (pl.path == kGnWarp) {
+        e = normk::gns_warp_launch(p, bf16, d->sm_count, stream);
+    } else {
+        plan_gn_split(R, L, vec4, *d, &pl);
+        void *ws = workspace;
+        if (!ws) {
+            std::lock_guard<std::mutex> lock(g_mu);
+            if (d->gn_ws_bytes < pl.ws_bytes) {
+                // Grow the library-owned workspace (callers serialize these calls).
+                if (cudaDeviceSynchronize() != cudaSuccess) {
+                    cudaGetLastError();
+                    return NORM_ERR_CUDA;
+                }
+                if (d->gn_ws)
+                    cudaFree(d->gn_ws);
+                d->gn_ws = nullptr;
+                d->gn_ws_bytes = 0;
+                void *q = nullptr;
+                if (cudaMalloc(&q, pl.ws_bytes) != cudaSuccess) {
+                    cudaGetLastError();
+                    return NORM_ERR_CUDA;
+                }
+                d->gn_ws = q;
+                d->gn_ws_bytes = pl.ws_bytes;
+            }
+            ws = d->gn_ws;
+        } else if (workspace_bytes < pl.ws_bytes) {
+            return NORM_ERR_WORKSPACE;
+        }
+        LnParams lp;
+        std::memset(&lp, 0, sizeof(lp));
+        lp.x = x;
+        lp.rows = R;
+        lp.row_len = L;
+        lp.eps = eps;
+        lp.part = static_cast<float4 *>(ws);
+        lp.chunk = pl.chunk;
+        lp.parts = pl.parts;
+        p.part = static_cast<const float4 *>(ws);
+        p.chunk = pl.chunk;
+        p.parts = pl.parts;
+        e = normk::ln_split_stats_launch(lp, bf16, pl.vec4, stream);
+        if (e == cudaSuccess)
+            e = normk::gns_split_apply_launch(p, bf16, pl.vec4, stream);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
@@ -520,14 +687,45 @@ norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const 
                                       int64_t C, int64_t num_groups, float eps, float negative_slope,
                                       cudaStream_t stream)
 {
-    return group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream, 4);
+    return group_lrelu_x2_fwd(x, gamma, beta, y, N, C, 1, num_groups, eps, negative_slope, nullptr, 0, stream, 4,
+                              false);
 }
 
 norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta,
                                            uint16_t *y, int64_t N, int64_t C, int64_t num_groups, float eps,
                                            float negative_slope, cudaStream_t stream)
 {
-    return group_lrelu_x2_fwd(x, gamma, beta, y, N, C, num_groups, eps, negative_slope, stream, 2);
+    return group_lrelu_x2_fwd(x, gamma, beta, y, N, C, 1, num_groups, eps, negative_slope, nullptr, 0, stream, 2,
+                              false);
+}
+
+size_t norm_group_lrelu_x2_nchw_workspace_bytes(int64_t N, int64_t C, int64_t S, int64_t num_groups)
+{
+    int64_t R = 0, L = 0;
+    if (N <= 0 || C <= 0 || S <= 0 || num_groups <= 0 || C % num_groups != 0 || !safe_mul(N, num_groups, &R) ||
+        !safe_mul(C / num_groups, S, &L))
+        return 0;
+    DeviceState *d = nullptr;
+    if (device_state(&d) != NORM_OK)
+        return 0;
+    return gn_split_ws_bound(R, L, *d);
+}
+
+norm_status_t norm_group_lrelu_x2_nchw_fwd(const float *x, const float *gamma, const float *beta, float *y, int64_t N,
+                                           int64_t C, int64_t S, int64_t num_groups, float eps, float negative_slope,
+                                           void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return group_lrelu_x2_fwd(x, gamma, beta, y, N, C, S, num_groups, eps, negative_slope, workspace,
+                              workspace_bytes, stream, 4, true);
+}
+
+norm_status_t norm_group_lrelu_x2_nchw_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta,
+                                                uint16_t *y, int64_t N, int64_t C, int64_t S, int64_t num_groups,
+                                                float eps, float negative_slope, void *workspace,
+                                                size_t workspace_bytes, cudaStream_t stream)
+{
+    return group_lrelu_x2_fwd(x, gamma, beta, y, N, C, S, num_groups, eps, negative_slope, workspace,
+                              workspace_bytes, stream, 2, true);
 }
 
 norm_status_t norm_last_error(cudaStream_t stream)

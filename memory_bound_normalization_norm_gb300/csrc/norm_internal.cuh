@@ -447,6 +447,88 @@ __device__ __forceinline__ Moments warp_merge(Moments a)
     return a;
 }
 
+// The row mean as an unevaluated fp32 pair (hi + lo) and 1/sqrt(var + eps).
+struct RowMean {
+    float hi, lo, rstd;
+};
+
+// Fold `cnt` partials part[0..cnt) = (n, mean of x - K_i, M2, K_i) in a
+// fixed order with one warp; every mean is first re-expressed against K_ref.
+// All lanes return the same result.  Count-weighted, so empty partials are
+// harmless.
+__device__ __forceinline__ Moments merge_partials_warp(const float4 *part, int cnt, float K_ref)
+{
+    const int lane = threadIdx.x & 31;
+    Moments acc = {0.f, 0.f, 0.f};
+    for (int i = lane; i < cnt; i += 32) {
+        const float4 q = ld_l2_f4(part + i);
+        const Moments m = {q.x, (q.w - K_ref) + q.y, q.z};
+        chan_merge(acc, m);
+    }
+    return warp_merge(acc);
+}
+
+__device__ __forceinline__ RowMean finish_row(float K, const Moments &tot, float eps)
+{
+    // mean = K + tot.mean, kept as an exact two-term sum (Knuth TwoSum).
+    const float s = K + tot.mean;
+    const float bp = s - K;
+    const float err = (K - (s - bp)) + (tot.mean - bp);
+    const float var = fmaxf(tot.m2 / tot.n, 0.f);
+    RowMean rm;
+    rm.hi = s;
+    rm.lo = err;
+    rm.rstd = rsqrtf(var + eps);
+    return rm;
+}
+
+__device__ __forceinline__ float4 ln_apply4(float4 v, const RowMean &rm, float4 g, float4 b)
+{
+    float4 o;
+    o.x = fmaf(((v.x - rm.hi) - rm.lo) * rm.rstd, g.x, b.x);
+    o.y = fmaf(((v.y - rm.hi) - rm.lo) * rm.rstd, g.y, b.y);
+    o.z = fmaf(((v.z - rm.hi) - rm.lo) * rm.rstd, g.z, b.z);
+    o.w = fmaf(((v.w - rm.hi) - rm.lo) * rm.rstd, g.w, b.w);
+    return o;
+}
+
+// CTA-wide fold of per-thread triples; the result is valid in thread 0.
+template <int T>
+__device__ __forceinline__ Moments cta_merge(Moments m, Moments *scratch)
+{
+    m = warp_merge(m);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0)
+        scratch[warp] = m;
+    __syncthreads();
+    Moments r = {0.f, 0.f, 0.f};
+    if (warp == 0) {
+        if (lane < T / 32)
+            r = scratch[lane];
+        r = warp_merge(r);
+    }
+    return r;
+}
+
+// Sum of v over a CTA of NT threads, in a fixed order; every thread gets the
+// result.  `scratch` (NT / 32 floats) must not be in use by the previous call.
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float *scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0)
+        scratch[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w)
+        t += scratch[w];
+    return t;
+}
+
 // ---------------------------------------------------------------- launchers
 
 // Workspace header of the LayerNorm kernels (256 bytes).  The caller zeroes
@@ -498,6 +580,9 @@ cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cuda
 // the tensors are bf16, else fp32.  vec4: rows are a multiple of 4 elements
 // and the pointers 4-element aligned.
 cudaError_t ln_split_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_t stream);
+// Its first kernel alone: part[r * P + pc] = (n, mean of x - K, M2, K) of
+// chunk pc of row r (K = x[r][0]).
+cudaError_t ln_split_stats_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_t stream);
 
 // One-launch LayerNorm for rows of at most ln_rows_max_row_len() elements
 // (a multiple of 4, 4-element aligned pointers); no workspace.
@@ -507,8 +592,35 @@ cudaError_t ln_rows_launch(const LnParams &p, bool bf16, int sm_count, cudaStrea
 // GroupNorm + LeakyReLU + x2 (bf16: the tensors are bf16, else fp32).
 cudaError_t gn_vec4_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
                            int64_t M, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream);
-cudaError_t gn_warp_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
-                           int64_t G, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream);
+
+// GroupNorm + LeakyReLU + x2 over segments: x[R][L] with R = N * G segments of
+// L = M * S elements; element e of segment r belongs to channel
+// (r % G) * M + e / S.  The 2-D (N, C) form is S = 1.
+struct GnSegParams {
+    const void *x;
+    const void *gamma; // [C] or null
+    const void *beta;  // [C] or null
+    void *y;
+    int64_t rows;    // R = N * G
+    int64_t seg_len; // L = M * S
+    int64_t G, M, S;
+    float eps, slope;
+    const float4 *part; // split path: partials [R][parts] from ln_split_stats_launch
+    int64_t chunk;      // split path: elements per CTA
+    int parts;          // split path: CTAs per segment; register path: cluster size
+};
+// Segment in registers: NT threads a CTA, a cluster of `cluster` CTAs per
+// segment (1, 2, 4, 8 or 16), V 4-element vectors a thread.  Needs L % 4 == 0,
+// 4-element aligned pointers and L / 4 <= gns_reg_capacity4(cluster).
+int64_t gns_reg_capacity4(int cluster);
+// Clusters that can be co-resident (0 if the cluster size cannot launch).
+cudaError_t gns_reg_max_clusters(int64_t seg_len, int64_t S, bool bf16, int cluster, int *clusters);
+cudaError_t gns_reg_launch(const GnSegParams &p, bool bf16, int cluster, cudaStream_t stream);
+// Apply kernel of the split path (after ln_split_stats_launch on the same
+// segments); vec4 as for the LayerNorm split path.
+cudaError_t gns_split_apply_launch(const GnSegParams &p, bool bf16, bool vec4, cudaStream_t stream);
+// One warp per segment, scalar loads; any shape (x is re-read from L1/L2).
+cudaError_t gns_warp_launch(const GnSegParams &p, bool bf16, int sm_count, cudaStream_t stream);
 
 // RMSNorm over dim 1 of [B][C][S] (bf16: the tensors are bf16, else fp32).
 cudaError_t rms_channel_launch(const void *x, void *y, int64_t B, int64_t C, int64_t S, float eps, bool bf16,

@@ -35,9 +35,9 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(norm_[a-z0-9_]+)\s*\(", text)))
 
 
-def test_header_declares_the_three_operations():
+def test_header_declares_the_operations():
     names = declared_functions()
-    for fn in ("norm_layer_fwd", "norm_rms_channel_fwd", "norm_group_lrelu_x2_fwd"):
+    for fn in ("norm_layer_fwd", "norm_rms_channel_fwd", "norm_group_lrelu_x2_fwd", "norm_group_lrelu_x2_nchw_fwd"):
         assert fn in names
 
 
@@ -76,6 +76,15 @@ def test_options_validate_and_round_trip(lib):
     assert raw.norm_set_option(lib.NORM_OPT_BARRIER_TIMEOUT_NS, 12345) == OK
     assert raw.norm_get_option(lib.NORM_OPT_BARRIER_TIMEOUT_NS) == 12345
     assert raw.norm_set_option(lib.NORM_OPT_BARRIER_TIMEOUT_NS, old) == OK
+    assert raw.norm_set_option(lib.NORM_OPT_GN_PATH, 4) == INVALID
+    for path in (3, 2, 1, 0):
+        assert raw.norm_set_option(lib.NORM_OPT_GN_PATH, path) == OK
+        assert raw.norm_get_option(lib.NORM_OPT_GN_PATH) == path
+    for bad in (3, 5, 12, 32, -1):
+        assert raw.norm_set_option(lib.NORM_OPT_GN_CLUSTER, bad) == INVALID
+    for cl in (16, 8, 4, 2, 1, 0):
+        assert raw.norm_set_option(lib.NORM_OPT_GN_CLUSTER, cl) == OK
+        assert raw.norm_get_option(lib.NORM_OPT_GN_CLUSTER) == cl
 
 
 # Fake, well-aligned device addresses: validation must reject before any use.
@@ -127,6 +136,28 @@ def test_group_norm_argument_errors(lib):
     assert f(X, G, B + 2, Y, 4, 16, 4, 1e-5, 0.01, None) == MISALIGNED
     assert f(X, G, B, B, 4, 16, 4, 1e-5, 0.01, None) == INVALID
     assert f(None, None, None, None, 0, 16, 4, 1e-5, 0.01, None) == OK
+
+
+def test_group_norm_nchw_argument_errors(lib):
+    f = lib.raw().norm_group_lrelu_x2_nchw_fwd
+    assert f(X, G, B, Y, 4, 16, 9, 3, 1e-5, 0.01, None, 0, None) == INVALID  # 16 % 3 != 0
+    assert f(X, G, B, Y, 4, 16, -9, 4, 1e-5, 0.01, None, 0, None) == INVALID
+    assert f(X, G, B, Y, 4, 16, 9, 4, float("nan"), 0.01, None, 0, None) == INVALID
+    assert f(X, G, B, Y, 4, 16, 9, 4, 1e-5, float("nan"), None, 0, None) == INVALID
+    assert f(X + 2, G, B, Y, 4, 16, 9, 4, 1e-5, 0.01, None, 0, None) == MISALIGNED
+    # y overlapping x (not exactly), y overlapping beta
+    assert f(X, G, B, X + 64, 4, 16, 9, 4, 1e-5, 0.01, None, 0, None) == INVALID
+    assert f(X, G, B, B - 8, 4, 16, 9, 4, 1e-5, 0.01, None, 0, None) == INVALID
+    # a workspace overlapping y, or not 16-byte aligned
+    assert f(X, G, B, Y, 4, 16, 9, 4, 1e-5, 0.01, Y + 64, 4096, None) == WORKSPACE
+    assert f(X, G, B, Y, 4, 16, 9, 4, 1e-5, 0.01, W + 8, 4096, None) == WORKSPACE
+    # N * C * S overflowing 2^60
+    assert f(X, G, B, Y, 1 << 30, 1 << 20, 1 << 20, 4, 1e-5, 0.01, None, 0, None) == INVALID
+    assert f(None, None, None, None, 4, 16, 0, 4, 1e-5, 0.01, None, 0, None) == OK
+    assert lib.raw().norm_group_lrelu_x2_nchw_fwd_bf16(X + 1, G, B, Y, 4, 16, 9, 4, 1e-5, 0.01, None, 0,
+                                                        None) == MISALIGNED
+    assert lib.norm_group_lrelu_x2_nchw_workspace_bytes(0, 16, 9, 4) == 0
+    assert lib.norm_group_lrelu_x2_nchw_workspace_bytes(4, 16, 9, 3) == 0
 
 
 def test_workspace_reset_rejects_bad_arguments(lib):

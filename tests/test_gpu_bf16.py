@@ -10,7 +10,8 @@ Covered: LayerNorm through the row kernel and the two-kernel path (vector and sc
 forms, long rows, misaligned pointers, in place, NULL affine, the full (16, 64, 256,
 256) shape), RMSNorm (several channel counts, in place, the (2, 64, 32, 32)
 workload), GroupNorm + LeakyReLU + x2 (vector and warp kernels, the (1024, 8192)
-workload), and guard zones around every output.
+workload), GroupNorm over NCHW tensors (register kernel, clusters, two-kernel and
+warp paths, the (8, 512, 64, 64) workload), and guard zones around every output.
 """
 import numpy as np
 import pytest
@@ -30,6 +31,8 @@ def ng():
     import memory_bound_normalization_norm_gb300 as m
     yield m
     m.norm_set_option(m.NORM_OPT_LN_PATH, 0)
+    m.norm_set_option(m.NORM_OPT_GN_PATH, 0)
+    m.norm_set_option(m.NORM_OPT_GN_CLUSTER, 0)
 
 
 class BGuarded:
@@ -162,3 +165,37 @@ def test_bf16_entry_points_check_dtype(ng):
     x = torch.zeros(64, device="cuda")
     with pytest.raises(TypeError):
         ng.norm_rms_channel_fwd_bf16(x, x, 1, 4, 16, 1e-5)
+
+
+# ------------------------------------------------------------------ GroupNorm over NCHW
+
+@pytest.mark.parametrize("N,C,S,G,path,cluster", [
+    (2, 32, 64, 8, 0, 0),         # register kernel, one CTA per group
+    (2, 8, 6, 4, 0, 0),           # channels change inside a vector
+    (2, 64, 1024, 4, 0, 0),       # automatic cluster of 2
+    (1, 3, 2732, 1, 1, 16),       # forced cluster of 16, ragged slices
+    (8, 512, 4096, 32, 0, 0),     # the (8, 512, 64, 64) 32-group workload: clusters of 8
+    (1, 128, 65536, 32, 0, 0),    # two-kernel path, vector form
+    (3, 9, 5, 3, 2, 0),           # two-kernel path, scalar form
+    (3, 9, 5, 3, 0, 0),           # warp path
+])
+def test_group_norm_nchw_bf16(ng, N, C, S, G, path, cluster):
+    n = N * C * S
+    x = bf16_inputs(n, seed=N + C + S)
+    g = bf16_inputs(C, 1.0, 0.1, seed=N + C + S, tensor_id=1)
+    b = bf16_inputs(C, 0.0, 0.1, seed=N + C + S, tensor_id=2)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    xb, gb, bb, yb = BGuarded(n, x), BGuarded(C, g), BGuarded(C, b), BGuarded(n)
+    ng.norm_set_option(ng.NORM_OPT_GN_PATH, path)
+    ng.norm_set_option(ng.NORM_OPT_GN_CLUSTER, cluster)
+    try:
+        ng.norm_group_lrelu_x2_nchw_fwd_bf16(xb.t, gb.t, bb.t, yb.t, N, C, S, G, 1e-5, 0.01)
+        assert ng.norm_last_error() == 0
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_GN_PATH, 0)
+        ng.norm_set_option(ng.NORM_OPT_GN_CLUSTER, 0)
+    assert_bf16_parity(yb.values(), want, f"GN NCHW bf16 ({N},{C},{S})/{G}")
+    assert yb.guards_intact()
+    # in place
+    ng.norm_group_lrelu_x2_nchw_fwd_bf16(xb.t, gb.t, bb.t, xb.t, N, C, S, G, 1e-5, 0.01)
+    assert_bf16_parity(xb.values(), want, f"GN NCHW bf16 in place ({N},{C},{S})/{G}")

@@ -1,0 +1,228 @@
+"""GroupNorm + LeakyReLU + x2 over NCHW tensors on the GPU against the float64 oracle,
+element by element.
+
+A group is its M = C/G channels at all S = H*W positions, M*S contiguous values.
+Covered: the register kernel with one CTA per group (channel-per-vector, per-element
+and S = 1 channel maps), thread-block clusters of 2..16 CTAs (automatic and forced,
+ragged slices), the two-kernel path (vector and scalar, caller and library
+workspace, more than 65,535 groups), the warp path, NULL affine, in place,
+misaligned pointers, cancellation-heavy inputs, and the (8, 512, 64, 64) 32-group
+workload.
+"""
+import numpy as np
+import pytest
+
+import normgen
+import oracle
+from gpu_util import Guarded, assert_parity
+
+pytestmark = pytest.mark.gpu
+
+REG, SPLIT, WARP = 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def ng():
+    import memory_bound_normalization_norm_gb300 as m
+    yield m
+    m.norm_set_option(m.NORM_OPT_GN_PATH, 0)
+    m.norm_set_option(m.NORM_OPT_GN_CLUSTER, 0)
+
+
+def inputs(N, C, S, seed, mean=0.0, std=1.0, affine=True):
+    x = normgen.normal(N * C * S, mean, std, seed=seed, tensor_id=0)
+    if not affine:
+        return x, None, None
+    return x, normgen.normal(C, 1.0, 0.1, seed=seed, tensor_id=1), normgen.normal(C, 0.0, 0.1, seed=seed, tensor_id=2)
+
+
+def run(ng, x, g, b, N, C, S, G, path=0, cluster=0, slope=0.01, offset=0, inplace=False, workspace=None,
+        ws_bytes=0):
+    ng.norm_set_option(ng.NORM_OPT_GN_PATH, path)
+    ng.norm_set_option(ng.NORM_OPT_GN_CLUSTER, cluster)
+    try:
+        n = N * C * S
+        xb = Guarded(n, x, offset=offset)
+        gd = None if g is None else Guarded(C, g, offset=offset).t
+        bd = None if b is None else Guarded(C, b, offset=offset).t
+        yb = xb if inplace else Guarded(n, offset=offset)
+        ng.norm_group_lrelu_x2_nchw_fwd(xb.t, gd, bd, yb.t, N, C, S, G, 1e-5, slope, workspace, ws_bytes)
+        assert ng.norm_last_error() == 0
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_GN_PATH, 0)
+        ng.norm_set_option(ng.NORM_OPT_GN_CLUSTER, 0)
+    out = yb.numpy()
+    assert yb.guards_intact(), "GroupNorm NCHW wrote outside its output"
+    return out
+
+
+def check(ng, N, C, S, G, seed=0, **kw):
+    x, g, b = inputs(N, C, S, seed)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, slope=kw.get("slope", 0.01), f64=True)
+    assert_parity(run(ng, x, g, b, N, C, S, G, **kw), want, f"GN NCHW ({N},{C},{S})/{G} {kw}")
+
+
+# ------------------------------------------------------------------ register kernel, one CTA per group
+
+@pytest.mark.parametrize("N,C,S,G", [
+    (2, 32, 64, 8),     # M = 4, L = 256: one channel per 4-element vector
+    (3, 64, 1024, 32),  # L = 2048
+    (2, 96, 36, 12),    # L = 288: ragged last vectors of the CTA
+    (2, 8, 6, 4),       # S = 6: channels change inside a vector
+    (3, 12, 7, 3),      # S = 7, L = 28
+    (4, 48, 1, 6),      # S = 1: consecutive channels
+    (5, 256, 1, 2),     # S = 1, M = 128
+    (1, 16, 512, 2),    # L = 4096: 128 threads x 8 vectors
+    (2, 4, 2048, 1),    # L = 8192: a full 256-thread CTA
+])
+def test_register_kernel(ng, N, C, S, G):
+    check(ng, N, C, S, G, seed=N * C + S, path=REG)
+    check(ng, N, C, S, G, seed=N * C + S)
+
+
+# ------------------------------------------------------------------ clusters
+
+@pytest.mark.parametrize("cluster", [0, 2, 4, 8, 16])
+@pytest.mark.parametrize("N,C,S,G", [
+    (2, 64, 1024, 4),   # L = 16384: automatic cluster of 2
+    (1, 3, 2732, 1),    # L = 8196: slices of 1025 and 1024 vectors, S % 4 != 0
+    (3, 32, 1000, 8),   # L = 4000
+])
+def test_clusters(ng, cluster, N, C, S, G):
+    check(ng, N, C, S, G, seed=cluster + S, path=REG, cluster=cluster)
+
+
+def test_cluster_of_sixteen_at_capacity(ng):
+    # L = 131072, the longest group the register kernel holds: 16 CTAs of 8192
+    check(ng, 2, 32, 16384, 4, seed=5)
+
+
+def test_cluster_ragged_empty_ranks(ng):
+    # L = 20 (5 vectors) over 8 CTAs: three ranks hold nothing and still take part
+    check(ng, 3, 20, 4, 4, seed=6, path=REG, cluster=8)
+
+
+def test_full_size(ng):
+    """(8, 512, 64, 64), 32 groups: groups of 16 channels x 4096 positions, L = 65536."""
+    check(ng, 8, 512, 4096, 32, seed=0)
+
+
+# ------------------------------------------------------------------ two-kernel path
+
+@pytest.mark.parametrize("N,C,S,G,path", [
+    (1, 128, 65536, 32, 0),  # L = 262144: longer than a 16-CTA cluster holds
+    (2, 8, 36000, 2, 0),     # L = 144000
+    (3, 12, 7, 3, SPLIT),    # vector form, short groups
+    (3, 9, 5, 3, SPLIT),     # scalar form (L = 15)
+    (2, 6, 2001, 3, 0),      # scalar form, L = 4002 ... taken by the warp path
+    (1, 5, 1001, 1, 0),      # scalar form, L = 5005 > 4096: two-kernel path
+])
+def test_split(ng, N, C, S, G, path):
+    check(ng, N, C, S, G, seed=C + S, path=path)
+
+
+def test_split_caller_workspace(ng):
+    import torch
+    N, C, S, G = 1, 64, 8192, 4
+    need = ng.norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, G)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    check(ng, N, C, S, G, seed=31, path=SPLIT, workspace=ws, ws_bytes=need)
+    x, g, b = inputs(N, C, S, 31)
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, N, C, S, G, path=SPLIT, workspace=ws, ws_bytes=16)
+    assert e.value.status == ng.NORM_ERR_WORKSPACE
+
+
+def test_split_many_groups_fold_grid(ng):
+    # more groups than one grid dimension holds (65535)
+    check(ng, 70000, 4, 2, 1, seed=32, path=SPLIT)
+
+
+# ------------------------------------------------------------------ warp path
+
+@pytest.mark.parametrize("N,C,S,G", [(3, 9, 5, 3), (4, 6, 1, 2), (2, 16, 64, 4), (5, 3, 301, 1)])
+def test_warp(ng, N, C, S, G):
+    check(ng, N, C, S, G, seed=C * S, path=WARP)
+
+
+# ------------------------------------------------------------------ affine, in place, alignment
+
+@pytest.mark.parametrize("N,C,S,G", [(4, 64, 64, 8), (2, 32, 4096, 4), (3, 9, 5, 3), (1, 8, 1001, 2)])
+def test_no_affine_in_place_and_misaligned(ng, N, C, S, G):
+    x, _, _ = inputs(N, C, S, seed=41, affine=False)
+    want = oracle.group_lrelu_x2_nchw(x, None, None, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, None, None, N, C, S, G), want, "GN NCHW no affine")
+    assert_parity(run(ng, x, None, None, N, C, S, G, inplace=True), want, "GN NCHW in place")
+    x, g, b = inputs(N, C, S, seed=42)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, g, b, N, C, S, G, offset=1), want, "GN NCHW misaligned")
+    assert_parity(run(ng, x, g, b, N, C, S, G, offset=1, inplace=True), want, "GN NCHW misaligned in place")
+
+
+@pytest.mark.parametrize("path,cluster", [(REG, 1), (REG, 4), (SPLIT, 0), (WARP, 0)])
+def test_in_place_every_path(ng, path, cluster):
+    N, C, S, G = 3, 32, 512, 4
+    x, g, b = inputs(N, C, S, seed=43)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, g, b, N, C, S, G, path=path, cluster=cluster, inplace=True), want,
+                  f"GN NCHW in place path={path}")
+
+
+@pytest.mark.parametrize("slope", [0.0, 0.2, 1.0, -0.5])
+def test_slopes(ng, slope):
+    check(ng, 2, 64, 256, 16, seed=44, slope=slope)
+
+
+@pytest.mark.parametrize("path,cluster", [(REG, 0), (REG, 16), (SPLIT, 0), (WARP, 0)])
+def test_cancellation(ng, path, cluster):
+    # x ~ N(1000, 0.01^2): the mean is 1e5 standard deviations from zero
+    N, C, S, G = 2, 16, 4096, 2
+    x, g, b = inputs(N, C, S, seed=45, mean=1000.0, std=0.01)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, g, b, N, C, S, G, path=path, cluster=cluster), want,
+                  f"GN NCHW N(1000, 0.01^2) path={path}")
+
+
+def test_s1_matches_the_2d_operation(ng):
+    N, C, G = 7, 384, 8
+    x, g, b = inputs(N, C, 1, seed=46)
+    want = oracle.group_lrelu_x2(x, g, b, N, C, G, f64=True)
+    assert_parity(run(ng, x, g, b, N, C, 1, G), want, "GN NCHW S = 1")
+
+
+def test_forced_paths_that_cannot_serve_refuse(ng):
+    N, C, S, G = 1, 128, 65536, 32  # L = 262144: no register kernel holds it
+    x, g, b = inputs(N, C, S, seed=47)
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, N, C, S, G, path=REG)
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    x, g, b = inputs(2, 16, 64, seed=47)
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, 2, 16, 64, 4, path=REG, cluster=2, offset=1)  # not 16-byte aligned
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    x, g, b = inputs(1, 8, 4096, seed=47)  # L = 32768: a cluster of 2 cannot hold it
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, 1, 8, 4096, 1, path=REG, cluster=2)
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+
+
+def test_2d_entry_refuses_the_split_path(ng):
+    import torch
+    x = torch.zeros(64, device="cuda")
+    ng.norm_set_option(ng.NORM_OPT_GN_PATH, SPLIT)
+    try:
+        with pytest.raises(ng.NormError) as e:
+            ng.norm_group_lrelu_x2_fwd(x, None, None, x, 4, 16, 4, 1e-5, 0.01)
+        assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_GN_PATH, 0)
+
+
+def test_tensor_convenience_4d(ng):
+    import torch
+    x, g, b = inputs(2, 32, 48, seed=48)
+    xt = torch.from_numpy(x).cuda().reshape(2, 32, 6, 8)
+    y = ng.group_norm_lrelu_x2(xt, 4, torch.from_numpy(g).cuda(), torch.from_numpy(b).cuda())
+    want = oracle.group_lrelu_x2_nchw(x, g, b, 2, 32, 48, 4, f64=True)
+    assert_parity(y.cpu().numpy().reshape(-1), want, "group_norm_lrelu_x2 on (2, 32, 6, 8)")
