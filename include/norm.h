@@ -222,7 +222,13 @@ norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *ga
  *   - L a multiple of 4 with 16-byte aligned pointers and L <= 131,072: one
  *     launch; each group is held in registers by one CTA or by a thread-
  *     block cluster of up to 16 CTAs that reduce the statistics through
- *     distributed shared memory; x is read from HBM once;
+ *     distributed shared memory; x is read from HBM once.  Where each CTA's
+ *     share of a group is 1,024 elements or more (and, for bf16, L is a
+ *     multiple of 8), a persistent grid of clusters streams the next group
+ *     into shared memory by bulk copy while the current one is reduced;
+ *     its waits are bounded by NORM_OPT_BARRIER_TIMEOUT_NS (a CTA that gives
+ *     up records NORM_ERR_TIMEOUT and leaves its part of the remaining
+ *     groups of y unwritten);
  *   - longer groups and unaligned vectors: a statistics kernel writes
  *     per-chunk partials to the workspace and an apply kernel re-reads x;
  *   - non-vector groups of at most 4,096 elements: one warp per group.
@@ -280,7 +286,8 @@ const char *norm_status_string(norm_status_t status);
  *   NORM_OPT_GN_PATH             GroupNorm: 0 = choose automatically, 1 =
  *                                force the register kernel, 2 = force the
  *                                two-kernel path (NCHW entry points only),
- *                                3 = force the warp-per-group kernel (error
+ *                                3 = force the warp-per-group kernel, 4 =
+ *                                force the streamed register kernel (error
  *                                NORM_ERR_UNSUPPORTED where the forced path
  *                                cannot serve the call).
  *   NORM_OPT_GN_CLUSTER          CTAs per group of the register kernel: 0 =

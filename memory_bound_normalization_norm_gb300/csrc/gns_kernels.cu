@@ -9,16 +9,28 @@
 // N*G segments of L = M*S elements, and element e of segment r belongs to
 // channel (r % G)*M + e/S.  The (N, C) form of the page is S = 1, L = M.
 //
-// Three kernels:
+// Four kernels:
 //  - register path: a segment is split over a thread-block cluster of CL
 //    CTAs (CL = 1 for segments that fit one CTA).  Each CTA holds its slice
 //    in registers, so x is read from HBM once and y written once.  The mean
 //    (about the pivot x[r][0]) and then the exact M2 about the mean are
 //    reduced over the CTA and then over the cluster through distributed
 //    shared memory: every CTA publishes its partial in its own shared memory,
-//    the cluster barrier (a hardware barrier, not a spin on memory) orders
-//    it, and every warp reads the CL partials with ld.shared::cluster and
-//    sums them in lane order, so all CTAs get the same value.
+//    the cluster barrier orders it, and every warp reads the CL partials with
+//    ld.shared::cluster and sums them in lane order, so all CTAs get the
+//    same value.
+//  - streamed register path (the same split, for slices of more than 256
+//    vectors with 16-byte aligned rows; the automatic choice there): a
+//    persistent grid of clusters walks segments, and each CTA's slice of the
+//    segment after next arrives by bulk copy (TMA engine, cp.async.bulk +
+//    mbarrier) into one of two shared-memory buffers while the current one
+//    is reduced and written.  Each CTA reduces its slice to an exact
+//    two-pass (mean, M2) and one all-to-all exchange per segment (st.async
+//    into every CTA's shared memory, counted on that CTA's mbarrier) gives
+//    every CTA the partials, merged with Chan's update in rank order.  A
+//    cluster barrier with release semantics would wait for the CTA's
+//    earlier y stores to drain (measured as the top stall, "membar"); the
+//    mbarrier exchange does not.  Every wait is bounded; see the kernel.
 //  - split path (segments longer than a 16-CTA cluster holds, or unaligned
 //    vectors): the LayerNorm split path's statistics kernel writes one
 //    (n, mean, M2, pivot) partial per (segment, chunk), and the apply kernel
@@ -93,6 +105,67 @@ __device__ __forceinline__ float cluster_sum(float v, float *slot, unsigned CL)
     for (int o = 16; o > 0; o >>= 1)
         t += __shfl_xor_sync(0xffffffffu, t, o);
     return t;
+}
+
+// Address of `local` (this CTA's shared memory) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void *local, unsigned rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    return ra;
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory whose arrival
+// is counted (as transaction bytes) on that CTA's mbarrier.  Unlike a
+// release at a cluster barrier it does not wait for this thread's earlier
+// global stores.
+__device__ __forceinline__ void st_async_f4(uint32_t remote, float4 v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
+// One all-to-all exchange of the cluster's partial statistics: every CTA
+// sends (mean, M2, flag, 0) of its slice into slot[rank] of every CTA
+// (itself included), waits on its own `bar` (phase `parity`) for the CL
+// slots, and merges them, rank j holding count_of(j) values, with Chan's
+// pairwise update in a fixed order (the same result in every CTA).
+// *flag_or gets the largest flag; *timed_out is set, for the whole CTA, if
+// the wait gave up.
+//
+// A slot set and its mbarrier are reused two segments later.  A CTA sends
+// into them only after it has received every CTA's exchange of the segment
+// in between, which each CTA sends after it has read the set, so a send
+// never overwrites unread values nor lands in the previous phase.
+template <typename CountOf>
+__device__ __forceinline__ Moments cluster_moments(float mean, float m2, float flag, float4 *slot, uint64_t *bar,
+                                                   unsigned CL, unsigned rank, uint32_t parity, uint64_t wait_ns,
+                                                   CountOf count_of, float *flag_or, bool *timed_out)
+{
+    if (threadIdx.x == 0)
+        mbar_arrive_expect_tx(bar, CL * 16u);
+    if (threadIdx.x < CL)
+        st_async_f4(peer_addr(&slot[rank], threadIdx.x), make_float4(mean, m2, flag, 0.f),
+                    peer_addr(bar, threadIdx.x));
+    const bool ok = mbar_wait_bounded(bar, parity, wait_ns);
+    *timed_out = __syncthreads_or(!ok) != 0;
+    const unsigned lane = threadIdx.x & 31;
+    Moments m = {0.f, 0.f, 0.f};
+    float f = 0.f;
+    if (lane < CL) {
+        const float4 w = slot[lane];
+        m.n = count_of(lane);
+        m.mean = w.x;
+        m.m2 = w.y;
+        f = w.z;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, o));
+    *flag_or = f;
+    return warp_merge(m);
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -238,6 +311,210 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
     // no CTA may exit while a peer can still read its partials
     if (clustered)
         cluster_sync_all();
+}
+
+// ------------------------------------------------------------------ streamed register path
+
+template <typename T>
+__device__ __forceinline__ float4 ld4_smem(const T *p);
+
+template <>
+__device__ __forceinline__ float4 ld4_smem<float>(const float *p)
+{
+    return *reinterpret_cast<const float4 *>(p);
+}
+
+template <>
+__device__ __forceinline__ float4 ld4_smem<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return Io<__nv_bfloat16>::unpack(u.x, u.y);
+}
+
+template <typename T>
+__device__ __forceinline__ float first_elem(const float4 &raw)
+{
+    if constexpr (sizeof(T) == 4)
+        return raw.x;
+    else
+        return Io<__nv_bfloat16>::unpack(__float_as_uint(raw.x), 0u).x;
+}
+
+// grid: a persistent set of clusters of CL = p.parts CTAs (CL = 1 allowed);
+// cluster c walks segments r_k = c + k * (cluster count).  CTA `rank` owns
+// vectors [rank * per, rank * per + per) of each segment (per = p.per4).
+// Dynamic shared memory: two slice buffers of per vectors; the slice of the
+// segment after next is in flight while the current one is reduced and
+// written.  Per segment each CTA computes the exact two-pass (mean, M2) of
+// its slice about the pivot, and one all-to-all exchange (st.async into
+// every CTA's shared memory, counted on its mbarrier) gives every CTA the
+// CL partials, merged in rank order.
+//
+// Failure handling: a CTA whose bulk-copy wait gives up flags its partials
+// from then on; every CTA sees a flag in the same exchange, so from that
+// segment on the whole cluster writes nothing, stops waiting for copies and
+// keeps exchanging (the exchanges still complete) until the end; each CTA
+// then drains its own copies.
+template <typename T, int NT, int V, int MODE>
+__global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(16) float4 piv[2]; // first 16 bytes of the segment, copied with the slice
+    __shared__ __align__(8) uint64_t full[2];
+    __shared__ __align__(8) uint64_t xbar[2];     // exchange, per segment parity
+    __shared__ __align__(16) float4 xslot[2][16]; // (mean, M2, flag, 0) per rank
+    __shared__ float red[2][NT / 32];
+    const int tid = threadIdx.x;
+    const unsigned CL = static_cast<unsigned>(p.parts);
+    const bool clustered = CL > 1;
+    const unsigned rank = clustered ? cluster_rank() : 0u;
+    const int64_t cid = clustered ? cluster_id_x() : blockIdx.x;
+    const int64_t ncl = clustered ? cluster_count_x() : gridDim.x;
+    const int64_t L4 = p.seg_len >> 2;
+    const int per = p.per4;
+    const int64_t lo = static_cast<int64_t>(per) * rank;
+    const int n4 = lo < L4 ? static_cast<int>(L4 - lo < per ? L4 - lo : per) : 0;
+    const float nloc = 4.f * static_cast<float>(n4);
+    // values held by rank j
+    const auto count_of = [L4, per](unsigned j) {
+        const int64_t l = static_cast<int64_t>(per) * j;
+        return l < L4 ? 4.f * static_cast<float>(L4 - l < per ? L4 - l : per) : 0.f;
+    };
+    const uint32_t slice_bytes = static_cast<uint32_t>(n4) * 4u * sizeof(T);
+    T *buf0 = reinterpret_cast<T *>(smem);
+    T *buf1 = buf0 + static_cast<size_t>(per) * 4;
+    constexpr bool narrow = true;
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.y);
+    const T *gm = static_cast<const T *>(p.gamma);
+    const T *bt = static_cast<const T *>(p.beta);
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    const int64_t nk = cid < p.rows ? (p.rows - cid + ncl - 1) / ncl : 0;
+    const uint64_t xwait_ns = p.timeout_ns > 100000000ull ? p.timeout_ns : 100000000ull;
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        fence_mbar_init();
+    }
+    // every CTA's barriers are initialized before any CTA sends to them
+    if (clustered)
+        cluster_sync_all();
+    else
+        __syncthreads();
+    // thread 0: copy this CTA's slice of segment k (and the segment's first
+    // 16 bytes, which hold the pivot) into buffer k & 1
+    auto issue = [&](int64_t k) {
+        const int b = static_cast<int>(k & 1);
+        const T *xr = x + (cid + k * ncl) * p.seg_len;
+        mbar_arrive_expect_tx(&full[b], slice_bytes + 16u);
+        bulk_g2s(&piv[b], xr, 16u, &full[b], pol_stream);
+        if (slice_bytes)
+            bulk_g2s(b ? buf1 : buf0, xr + 4 * lo, slice_bytes, &full[b], pol_stream);
+    };
+    int64_t issued = 0;
+    if (tid == 0) {
+        for (; issued < 2 && issued < nk; ++issued)
+            issue(issued);
+    }
+    bool stopped = false; // this cluster writes nothing more
+    bool gave_up = false; // this CTA's own wait gave up
+    int64_t consumed = 0; // segments whose copies this CTA has seen complete
+    for (int64_t k = 0; k < nk; ++k) {
+        const int b = static_cast<int>(k & 1);
+        const uint32_t par = static_cast<uint32_t>((k >> 1) & 1);
+        if (!stopped) {
+            const bool ok = mbar_wait_bounded(&full[b], par, p.timeout_ns);
+            // one decision for the whole CTA
+            if (__syncthreads_or(!ok)) {
+                gave_up = true;
+                stopped = true;
+            } else {
+                consumed = k + 1;
+            }
+        }
+        const T *sb = b ? buf1 : buf0;
+        float4 v[V];
+        float K = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!stopped) {
+            K = first_elem<T>(piv[b]);
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const int i = tid + j * NT;
+                if (i < n4)
+                    v[j] = ld4_smem<T>(sb + 4 * i);
+            }
+        }
+        // exact two-pass statistics of this CTA's slice about the pivot
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            if (tid + j * NT < n4)
+                s += ((v[j].x - K) + (v[j].y - K)) + ((v[j].z - K) + (v[j].w - K));
+        }
+        s = block_sum<NT>(s, red[0]);
+        // every thread has its values in registers: refill this buffer with
+        // the segment after next
+        if (tid == 0 && !stopped && issued < nk && issued == k + 2) {
+            fence_proxy_async_smem();
+            issue(issued);
+            ++issued;
+        }
+        const float mloc = n4 ? s / nloc : 0.f;
+        float q = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            if (tid + j * NT < n4) {
+                const float a = (v[j].x - K) - mloc, c = (v[j].y - K) - mloc;
+                const float d = (v[j].z - K) - mloc, e = (v[j].w - K) - mloc;
+                q += (a * a + c * c) + (d * d + e * e);
+            }
+        }
+        q = block_sum<NT>(q, red[1]);
+        Moments tot;
+        tot.n = nloc;
+        tot.mean = mloc;
+        tot.m2 = q;
+        if (clustered) {
+            // a stopped CTA's partial is flagged, so no CTA uses it
+            float f = 0.f;
+            bool to = false;
+            tot = cluster_moments(mloc, q, stopped ? 1.f : 0.f, xslot[b], &xbar[b], CL, rank, par, xwait_ns,
+                                  count_of, &f, &to);
+            if (f != 0.f || to)
+                stopped = true;
+        }
+        if (stopped)
+            continue; // keep exchanging, write nothing
+        const RowMean rm = finish_row(K, tot, p.eps);
+        const int64_t r = cid + k * ncl;
+        const int64_t cbase = (r % p.G) * p.M;
+        T *yr = y + r * p.seg_len;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int i = tid + j * NT;
+            if (i < n4) {
+                const int64_t e = 4 * (lo + i);
+                float4 g, bb;
+                seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb);
+                Io<T>::st4_stream(yr + e, gn_apply4(v[j], rm, g, bb, p.slope), pol_stream);
+            }
+        }
+    }
+    if (stopped && tid == 0) {
+        if (gave_up)
+            record_error(p.err, NORM_ERR_TIMEOUT);
+        // the copies this CTA issued and never saw complete still write its
+        // shared memory: wait for them before the CTA exits
+        for (int64_t j = consumed; j < issued; ++j)
+            mbar_wait_bounded(&full[j & 1], static_cast<uint32_t>((j >> 1) & 1), xwait_ns);
+    }
 }
 
 // ------------------------------------------------------------------ split path: apply
@@ -537,6 +814,148 @@ cudaError_t gns_reg_launch(const GnSegParams &p, bool bf16, int cluster, cudaStr
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr;
     cluster_config(&cfg, &attr, nt, cluster, grid, stream);
+    return cudaLaunchKernelEx(&cfg, k, args);
+}
+
+namespace {
+
+// Streamed variants: 256 threads, 4 or 8 vectors a thread.
+constexpr int GNS_STREAM_NT = 256;
+
+template <typename T, int MODE>
+RegKernel stream_kernel_for(int per, int *idx)
+{
+    if (per <= 1024) {
+        *idx = 0;
+        return gns_stream_kernel<T, GNS_STREAM_NT, 4, MODE>;
+    }
+    if (per <= 2048) {
+        *idx = 1;
+        return gns_stream_kernel<T, GNS_STREAM_NT, 8, MODE>;
+    }
+    *idx = -1;
+    return nullptr;
+}
+
+template <typename T>
+RegKernel stream_kernel_t(int per, int mode, int *idx)
+{
+    switch (mode) {
+    case AFF_ROW: return stream_kernel_for<T, AFF_ROW>(per, idx);
+    case AFF_CHAN: return stream_kernel_for<T, AFF_CHAN>(per, idx);
+    default: return stream_kernel_for<T, AFF_ANY>(per, idx);
+    }
+}
+
+constexpr int GNS_STREAM_VARIANTS = 6; // 2 CTA shapes x 3 affine modes
+std::atomic<int> g_stream_active[GNS_DEVICES][2][GNS_STREAM_VARIANTS][5];
+std::once_flag g_stream_init;
+
+// Vectors per CTA slice of the streamed kernel: ceil(L4 / cluster), even so
+// that bf16 slices start on 16-byte boundaries.
+int64_t stream_per(int64_t seg_len, int cluster)
+{
+    const int64_t L4 = seg_len / 4;
+    const int64_t per = (L4 + cluster - 1) / cluster;
+    return (per + 1) & ~int64_t(1);
+}
+
+size_t stream_smem(int64_t per, bool bf16)
+{
+    return 2u * static_cast<size_t>(per) * 4u * (bf16 ? 2u : 4u);
+}
+
+} // namespace
+
+cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, int cluster, int *clusters)
+{
+    *clusters = 0;
+    if (cluster < 1 || cluster > GNS_MAX_CLUSTER || (cluster & (cluster - 1)) != 0)
+        return cudaErrorInvalidValue;
+    const int64_t per = stream_per(seg_len, cluster);
+    int idx = 0, dev = 0;
+    const int mode = affine_mode(S);
+    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, &idx)
+                             : stream_kernel_t<float>(static_cast<int>(per), mode, &idx);
+    if (!k || per > 2048)
+        return cudaErrorInvalidValue;
+    idx += 2 * mode;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::call_once(g_stream_init, [] {
+        for (auto &a : g_stream_active)
+            for (auto &b : a)
+                for (auto &c : b)
+                    for (auto &v : c)
+                        v.store(-1);
+    });
+    // occupancy depends on the dynamic shared memory, i.e. on per: cache only
+    // the full-slice case (per of 1024 or 2048), query the others
+    const size_t smem = stream_smem(per, bf16);
+    const bool cacheable = per == 1024 || per == 2048;
+    std::atomic<int> *slot = cacheable && dev >= 0 && dev < GNS_DEVICES
+                                 ? &g_stream_active[dev][bf16 ? 1 : 0][idx][log2_cluster(cluster)]
+                                 : nullptr;
+    if (slot) {
+        const int known = slot->load();
+        if (known >= 0) {
+            *clusters = known;
+            return cudaSuccess;
+        }
+    }
+    // the attribute covers the variant's largest slice, so any launch of it fits
+    const size_t smem_max = stream_smem(idx % 2 == 0 ? 1024 : 2048, bf16);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
+    if (e == cudaSuccess && cluster > 8)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess)
+        return e;
+    const int nt = GNS_STREAM_NT;
+    if (cluster == 1) {
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, nt, smem);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        *clusters = per_sm * sms;
+    } else {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr;
+        cluster_config(&cfg, &attr, nt, cluster, static_cast<unsigned>(cluster), 0);
+        cfg.dynamicSmemBytes = smem;
+        e = cudaOccupancyMaxActiveClusters(clusters, k, &cfg);
+    }
+    if (e == cudaSuccess && slot)
+        slot->store(*clusters);
+    return e;
+}
+
+cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, int cluster, cudaStream_t stream)
+{
+    int active = 0;
+    cudaError_t e = gns_stream_max_clusters(p.seg_len, p.S, bf16, cluster, &active);
+    if (e != cudaSuccess)
+        return e;
+    if (active < 1)
+        return cudaErrorInvalidConfiguration;
+    const int64_t per = stream_per(p.seg_len, cluster);
+    int idx = 0;
+    const int mode = affine_mode(p.S);
+    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, &idx)
+                             : stream_kernel_t<float>(static_cast<int>(per), mode, &idx);
+    int64_t clusters = active;
+    if (clusters > p.rows)
+        clusters = p.rows;
+    GnSegParams args = p;
+    args.parts = cluster;
+    args.per4 = static_cast<int>(per);
+    const size_t smem = stream_smem(per, bf16);
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr;
+    cluster_config(&cfg, &attr, GNS_STREAM_NT, cluster, static_cast<unsigned>(clusters * cluster), stream);
+    cfg.dynamicSmemBytes = smem;
+    if (cluster == 1)
+        cfg.numAttrs = 0;
     return cudaLaunchKernelEx(&cfg, k, args);
 }
 

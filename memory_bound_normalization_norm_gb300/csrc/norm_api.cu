@@ -217,7 +217,9 @@ bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
 // ------------------------------------------------------------------ GN plan
 
 // Segment GroupNorm paths (NORM_OPT_GN_PATH values).
-constexpr int kGnReg = 1, kGnSplit = 2, kGnWarp = 3;
+constexpr int kGnReg = 1, kGnSplit = 2, kGnWarp = 3, kGnStream = 4;
+// Shortest CTA slice (vectors) for which the automatic choice streams.
+constexpr int64_t kGnStreamMinPer = 256;
 // Longest non-vector segment the warp path takes on its own.
 constexpr int64_t kGnWarpMaxLen = 4096;
 
@@ -301,7 +303,7 @@ norm_status_t norm_set_option(norm_option_t option, int64_t value)
         g_opt_ln_ctas = value;
         return NORM_OK;
     case NORM_OPT_GN_PATH:
-        if (value > 3)
+        if (value > 4)
             return NORM_ERR_INVALID_ARG;
         g_opt_gn_path = value;
         return NORM_OK;
@@ -571,13 +573,29 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
             cluster = 0;
         }
     }
+    // Streamed form of the register path: 16-byte aligned x rows and slices.
+    bool stream_ok = false;
+    int64_t stream_slice = 0;
+    if (cluster && aligned(x, 16) && (bf16 ? (L & 7) == 0 : true)) {
+        stream_slice = (L / 4 + cluster - 1) / cluster;
+        stream_slice = (stream_slice + 1) & ~int64_t(1);
+        int active = 0;
+        stream_ok = stream_slice <= 2048 &&
+                    normk::gns_stream_max_clusters(L, S, bf16, cluster, &active) == cudaSuccess && active >= 1;
+        if (!stream_ok)
+            cudaGetLastError();
+    }
     GnPlan pl;
     if (opt == kGnReg && !cluster)
+        return NORM_ERR_UNSUPPORTED;
+    if (opt == kGnStream && !stream_ok)
         return NORM_ERR_UNSUPPORTED;
     if (opt == kGnSplit && !nchw)
         return NORM_ERR_UNSUPPORTED;
     if (opt)
         pl.path = static_cast<int>(opt);
+    else if (stream_ok && stream_slice > kGnStreamMinPer)
+        pl.path = kGnStream;
     else if (cluster)
         pl.path = kGnReg;
     else if (!nchw || (!vec4 && L <= kGnWarpMaxLen))
@@ -598,8 +616,12 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     p.S = S;
     p.eps = eps;
     p.slope = negative_slope;
+    p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
+    p.err = d->err;
 
-    if (pl.path == kGnReg) {
+    if (pl.path == kGnStream) {
+        e = normk::gns_stream_launch(p, bf16, cluster, stream);
+    } else if (pl.path == kGnReg) {
         e = normk::gns_reg_launch(p, bf16, cluster, stream);
     } else if (pl.path == kGnWarp) {
         e = normk::gns_warp_launch(p, bf16, d->sm_count, stream);

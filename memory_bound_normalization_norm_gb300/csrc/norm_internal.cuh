@@ -607,7 +607,10 @@ struct GnSegParams {
     float eps, slope;
     const float4 *part; // split path: partials [R][parts] from ln_split_stats_launch
     int64_t chunk;      // split path: elements per CTA
-    int parts;          // split path: CTAs per segment; register path: cluster size
+    int parts;          // split path: CTAs per segment; register paths: cluster size
+    int per4;           // streamed path: vectors per CTA slice
+    uint64_t timeout_ns; // streamed path: longest mbarrier wait
+    unsigned *err;       // streamed path: the device error word
 };
 // Segment in registers: NT threads a CTA, a cluster of `cluster` CTAs per
 // segment (1, 2, 4, 8 or 16), V 4-element vectors a thread.  Needs L % 4 == 0,
@@ -616,6 +619,12 @@ int64_t gns_reg_capacity4(int cluster);
 // Clusters that can be co-resident (0 if the cluster size cannot launch).
 cudaError_t gns_reg_max_clusters(int64_t seg_len, int64_t S, bool bf16, int cluster, int *clusters);
 cudaError_t gns_reg_launch(const GnSegParams &p, bool bf16, int cluster, cudaStream_t stream);
+// Streamed register path: persistent clusters, each CTA's next slices arrive
+// by bulk copy into two shared-memory buffers.  Needs L % 4 == 0 (L % 8 for
+// bf16), 16-byte aligned x, 4-element aligned y/gamma/beta, and a slice of
+// 2..2048 vectors.
+cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, int cluster, int *clusters);
+cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, int cluster, cudaStream_t stream);
 // Apply kernel of the split path (after ln_split_stats_launch on the same
 // segments); vec4 as for the LayerNorm split path.
 cudaError_t gns_split_apply_launch(const GnSegParams &p, bool bf16, bool vec4, cudaStream_t stream);

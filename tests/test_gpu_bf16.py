@@ -174,7 +174,11 @@ def test_bf16_entry_points_check_dtype(ng):
     (2, 8, 6, 4, 0, 0),           # channels change inside a vector
     (2, 64, 1024, 4, 0, 0),       # automatic cluster of 2
     (1, 3, 2732, 1, 1, 16),       # forced cluster of 16, ragged slices
-    (8, 512, 4096, 32, 0, 0),     # the (8, 512, 64, 64) 32-group workload: clusters of 8
+    (8, 512, 4096, 32, 0, 0),     # the (8, 512, 64, 64) 32-group workload: clusters of 8, streamed
+    (8, 512, 4096, 32, 1, 0),     # the same through the unstreamed register kernel
+    (64, 64, 1024, 16, 4, 1),     # streamed, one CTA per group, many groups per CTA
+    (2, 64, 1024, 4, 4, 16),      # streamed over clusters of 16
+    (2, 16, 2046, 4, 4, 2),       # streamed, channels change inside a vector (L = 8184)
     (1, 128, 65536, 32, 0, 0),    # two-kernel path, vector form
     (3, 9, 5, 3, 2, 0),           # two-kernel path, scalar form
     (3, 9, 5, 3, 0, 0),           # warp path

@@ -4,7 +4,8 @@ element by element.
 A group is its M = C/G channels at all S = H*W positions, M*S contiguous values.
 Covered: the register kernel with one CTA per group (channel-per-vector, per-element
 and S = 1 channel maps), thread-block clusters of 2..16 CTAs (automatic and forced,
-ragged slices), the two-kernel path (vector and scalar, caller and library
+ragged slices), its streamed form (bulk copies into double-buffered shared memory,
+clusters walking many groups, bounded waits that give up cleanly), the two-kernel path (vector and scalar, caller and library
 workspace, more than 65,535 groups), the warp path, NULL affine, in place,
 misaligned pointers, cancellation-heavy inputs, and the (8, 512, 64, 64) 32-group
 workload.
@@ -18,7 +19,7 @@ from gpu_util import Guarded, assert_parity
 
 pytestmark = pytest.mark.gpu
 
-REG, SPLIT, WARP = 1, 2, 3
+REG, SPLIT, WARP, STREAM = 1, 2, 3, 4
 
 
 @pytest.fixture(scope="module")
@@ -107,6 +108,61 @@ def test_full_size(ng):
     check(ng, 8, 512, 4096, 32, seed=0)
 
 
+# ------------------------------------------------------------------ streamed register kernel
+
+@pytest.mark.parametrize("N,C,S,G,cluster", [
+    (3, 64, 1024, 32, 1),    # L = 2048: 512-vector slices, 4 vectors a thread
+    (2, 4, 2048, 1, 1),      # L = 8192: 2048-vector slices, 8 vectors a thread
+    (64, 64, 1024, 16, 1),   # 1024 groups: every CTA walks many groups through both buffers
+    (2, 64, 1024, 4, 2),     # L = 16384 over clusters of 2 .. 16
+    (2, 64, 1024, 4, 4),
+    (2, 64, 1024, 4, 8),
+    (2, 64, 1024, 4, 16),
+    (1, 3, 2732, 1, 2),      # L = 8196: slices of 1026 and 1023 vectors
+    (5, 8192, 1, 2, 1),      # S = 1: consecutive channels
+    (2, 8, 2046, 4, 2),      # S = 2046: channels change inside a vector
+    (40, 256, 1024, 8, 4),   # 320 groups over clusters of 4
+])
+def test_streamed(ng, N, C, S, G, cluster):
+    check(ng, N, C, S, G, seed=N + C + S + cluster, path=STREAM, cluster=cluster)
+
+
+def test_streamed_is_the_automatic_choice_at_full_size(ng):
+    # the (8, 512, 64, 64) workload: clusters of 8 CTAs with 2048-vector slices
+    N, C, S, G = 8, 512, 4096, 32
+    x, g, b = inputs(N, C, S, seed=51)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, g, b, N, C, S, G, path=STREAM), want, "GN NCHW streamed full size")
+    assert_parity(run(ng, x, g, b, N, C, S, G, path=STREAM, inplace=True), want, "GN NCHW streamed in place")
+
+
+def test_streamed_tiny_wait_limit_gives_up_cleanly(ng):
+    """With a 1 ns limit the CTAs stop waiting for their bulk copies: the call records
+    NORM_ERR_TIMEOUT (or finishes, if every copy had landed at its first check), every
+    element of y keeps its previous value or holds its correct result, and the next
+    call with the default limit is correct."""
+    N, C, S, G = 16, 64, 1024, 8
+    x, g, b = inputs(N, C, S, seed=52)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    old = ng.norm_get_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS)
+    xb, gb, bb, yb = Guarded(N * C * S, x), Guarded(C, g), Guarded(C, b), Guarded(N * C * S)
+    ng.norm_set_option(ng.NORM_OPT_GN_PATH, STREAM)
+    ng.norm_set_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS, 1)
+    try:
+        ng.norm_group_lrelu_x2_nchw_fwd(xb.t, gb.t, bb.t, yb.t, N, C, S, G, 1e-5, 0.01)
+        status = ng.norm_last_error()
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS, old)
+        ng.norm_set_option(ng.NORM_OPT_GN_PATH, 0)
+    assert status in (ng.NORM_OK, ng.NORM_ERR_TIMEOUT)
+    got = yb.numpy().astype(np.float64)
+    untouched = np.isnan(got)  # the guard sentinel is a NaN no kernel writes
+    ok = np.abs(got - want) <= 1e-4 * (1.0 + np.abs(want))
+    assert np.all(untouched | ok), "an element of y is neither untouched nor correct"
+    assert yb.guards_intact()
+    assert_parity(run(ng, x, g, b, N, C, S, G, path=STREAM), want, "GN NCHW streamed after a timeout")
+
+
 # ------------------------------------------------------------------ two-kernel path
 
 @pytest.mark.parametrize("N,C,S,G,path", [
@@ -160,7 +216,7 @@ def test_no_affine_in_place_and_misaligned(ng, N, C, S, G):
     assert_parity(run(ng, x, g, b, N, C, S, G, offset=1, inplace=True), want, "GN NCHW misaligned in place")
 
 
-@pytest.mark.parametrize("path,cluster", [(REG, 1), (REG, 4), (SPLIT, 0), (WARP, 0)])
+@pytest.mark.parametrize("path,cluster", [(REG, 1), (REG, 4), (STREAM, 1), (STREAM, 4), (SPLIT, 0), (WARP, 0)])
 def test_in_place_every_path(ng, path, cluster):
     N, C, S, G = 3, 32, 512, 4
     x, g, b = inputs(N, C, S, seed=43)
@@ -174,7 +230,7 @@ def test_slopes(ng, slope):
     check(ng, 2, 64, 256, 16, seed=44, slope=slope)
 
 
-@pytest.mark.parametrize("path,cluster", [(REG, 0), (REG, 16), (SPLIT, 0), (WARP, 0)])
+@pytest.mark.parametrize("path,cluster", [(REG, 0), (REG, 16), (STREAM, 0), (STREAM, 8), (SPLIT, 0), (WARP, 0)])
 def test_cancellation(ng, path, cluster):
     # x ~ N(1000, 0.01^2): the mean is 1e5 standard deviations from zero
     N, C, S, G = 2, 16, 4096, 2
@@ -200,6 +256,9 @@ def test_forced_paths_that_cannot_serve_refuse(ng):
     x, g, b = inputs(2, 16, 64, seed=47)
     with pytest.raises(ng.NormError) as e:
         run(ng, x, g, b, 2, 16, 64, 4, path=REG, cluster=2, offset=1)  # not 16-byte aligned
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, 2, 16, 64, 4, path=STREAM, offset=1)
     assert e.value.status == ng.NORM_ERR_UNSUPPORTED
     x, g, b = inputs(1, 8, 4096, seed=47)  # L = 32768: a cluster of 2 cannot hold it
     with pytest.raises(ng.NormError) as e:
