@@ -549,16 +549,30 @@ __global__ void __launch_bounds__(GS_T) gns_split_apply_kernel(GnSegParams p)
         if (VEC) {
             const uint64_t pol = policy_evict_first();
             const uint64_t pol_gb = policy_evict_last();
-            for (int64_t i = lo / 4 + threadIdx.x; i < hi / 4; i += GS_T) {
-                const float4 q = Io<T>::ld4_stream(xr + 4 * i, pol);
+            const int mode = affine_mode(p.S);
+            auto one = [&](int64_t i, const float4 &q) {
                 float4 g, b;
-                switch (affine_mode(p.S)) {
+                switch (mode) {
                 case AFF_ROW: seg_affine4<T, AFF_ROW>(gm, bt, cbase, 4 * i, p.S, narrow, pol_gb, g, b); break;
                 case AFF_CHAN: seg_affine4<T, AFF_CHAN>(gm, bt, cbase, 4 * i, p.S, narrow, pol_gb, g, b); break;
                 default: seg_affine4<T, AFF_ANY>(gm, bt, cbase, 4 * i, p.S, narrow, pol_gb, g, b); break;
                 }
                 Io<T>::st4_stream(yr + 4 * i, gn_apply4(q, rm, g, b, p.slope), pol);
+            };
+            int64_t i = lo / 4 + threadIdx.x;
+            const int64_t e4 = hi / 4;
+            // four loads of x in flight per thread
+            for (; i + 3 * GS_T < e4; i += 4 * GS_T) {
+                float4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    q[u] = Io<T>::ld4_stream(xr + 4 * (i + u * GS_T), pol);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    one(i + u * GS_T, q[u]);
             }
+            for (; i < e4; i += GS_T)
+                one(i, Io<T>::ld4_stream(xr + 4 * i, pol));
         } else {
             for (int64_t i = lo + threadIdx.x; i < hi; i += GS_T) {
                 const int64_t c = cbase + seg_div(i, p.S, narrow);

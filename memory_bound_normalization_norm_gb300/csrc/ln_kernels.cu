@@ -652,9 +652,11 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
 
 constexpr int LS_T = 256;
 
-// One triple per (chunk p, row r) CTA.  Vector form folds each 4-element
-// vector as a two-pass group of 4 into the thread's triple; scalar form is
-// Welford.
+// One triple per (chunk p, row r) CTA.  Vector form: each thread keeps four
+// 4-element loads in flight and accumulates the shifted sums sum d and
+// sum d^2 of d = x - K, which the pivot (an element of the row) keeps well
+// conditioned, then turns them into its (n, mean, M2); scalar form is
+// Welford.  The threads' triples are merged with Chan's update.
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(LS_T) ln_split_stats_kernel(LnParams p)
 {
@@ -670,15 +672,30 @@ __global__ void __launch_bounds__(LS_T) ln_split_stats_kernel(LnParams p)
         Moments m = {0.f, 0.f, 0.f};
         if (VEC) {
             const uint64_t pol = policy_evict_first();
-            for (int64_t i = lo / 4 + threadIdx.x; i < hi / 4; i += LS_T) {
-                const float4 q = Io<T>::ld4_stream(xr + 4 * i, pol);
+            float s1 = 0.f, s2 = 0.f, cnt = 0.f;
+            auto add = [&](const float4 &q) {
                 const float a = q.x - K, b = q.y - K, c = q.z - K, d = q.w - K;
-                Moments g;
-                g.n = 4.f;
-                g.mean = ((a + b) + (c + d)) * 0.25f;
-                const float da = a - g.mean, db = b - g.mean, dc = c - g.mean, dd = d - g.mean;
-                g.m2 = (da * da + db * db) + (dc * dc + dd * dd);
-                chan_merge(m, g);
+                s1 += (a + b) + (c + d);
+                s2 += (a * a + b * b) + (c * c + d * d);
+                cnt += 4.f;
+            };
+            int64_t i = lo / 4 + threadIdx.x;
+            const int64_t e4 = hi / 4;
+            for (; i + 3 * LS_T < e4; i += 4 * LS_T) {
+                float4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    q[u] = Io<T>::ld4_stream(xr + 4 * (i + u * LS_T), pol);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    add(q[u]);
+            }
+            for (; i < e4; i += LS_T)
+                add(Io<T>::ld4_stream(xr + 4 * i, pol));
+            if (cnt > 0.f) {
+                m.n = cnt;
+                m.mean = s1 / cnt;
+                m.m2 = fmaxf(s2 - s1 * m.mean, 0.f);
             }
         } else {
             for (int64_t i = lo + threadIdx.x; i < hi; i += LS_T) {
@@ -724,12 +741,25 @@ __global__ void __launch_bounds__(LS_T) ln_split_apply_kernel(LnParams p)
         if (VEC) {
             const uint64_t pol = policy_evict_first();
             const uint64_t pol_gb = policy_evict_last();
-            for (int64_t i = lo / 4 + threadIdx.x; i < hi / 4; i += LS_T) {
-                const float4 q = Io<T>::ld4_stream(xr + 4 * i, pol);
+            auto one = [&](int64_t i, const float4 &q) {
                 const float4 g = gm ? Io<T>::ld4_ro(gm + 4 * i, pol_gb) : make_float4(1.f, 1.f, 1.f, 1.f);
                 const float4 bb = bt ? Io<T>::ld4_ro(bt + 4 * i, pol_gb) : make_float4(0.f, 0.f, 0.f, 0.f);
                 Io<T>::st4_stream(yr + 4 * i, ln_apply4(q, rm, g, bb), pol);
+            };
+            int64_t i = lo / 4 + threadIdx.x;
+            const int64_t e4 = hi / 4;
+            // four loads of x in flight per thread
+            for (; i + 3 * LS_T < e4; i += 4 * LS_T) {
+                float4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    q[u] = Io<T>::ld4_stream(xr + 4 * (i + u * LS_T), pol);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    one(i + u * LS_T, q[u]);
             }
+            for (; i < e4; i += LS_T)
+                one(i, Io<T>::ld4_stream(xr + 4 * i, pol));
         } else {
             for (int64_t i = lo + threadIdx.x; i < hi; i += LS_T) {
                 const float g = gm ? Io<T>::ld1(gm + i) : 1.f;

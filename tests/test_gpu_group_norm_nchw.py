@@ -177,6 +177,16 @@ def test_split(ng, N, C, S, G, path):
     check(ng, N, C, S, G, seed=C + S, path=path)
 
 
+@pytest.mark.parametrize("N,C,S,G", [(3, 64, 65536, 8), (3, 40, 131072, 5)])
+def test_split_large(ng, N, C, S, G):
+    # 50 and 60 MB of x through the two-kernel path, groups of 524,288 and
+    # 1,048,576 values
+    check(ng, N, C, S, G, seed=S + G)
+    x, g, b = inputs(N, C, S, S + G)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, g, b, N, C, S, G, inplace=True), want, "GN NCHW large split in place")
+
+
 def test_split_caller_workspace(ng):
     import torch
     N, C, S, G = 1, 64, 8192, 4

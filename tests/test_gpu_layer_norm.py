@@ -209,3 +209,14 @@ def test_layer_norm_row_kernel_refuses_what_it_cannot_take(ng, L, offset):
         ng.norm_set_option(ng.NORM_OPT_LN_PATH, AUTO)
     assert_parity(run_ln(ng, x, g, b, rows, L, offset=offset), oracle.layer_norm(x, g, b, rows, L),
                   f"LN auto {rows}x{L}")
+
+
+@pytest.mark.parametrize("rows,L,offset", [(24, 1 << 19, 0), (11, (1 << 20) + 1, 1)])
+def test_split_path_large(ng, rows, L, offset):
+    # 50 MB of x through the two-kernel path: vector form, and scalar form with a
+    # ragged length and misaligned pointers
+    x, g, b = inputs(rows, L, seed=rows + L)
+    want = oracle.layer_norm(x, g, b, rows, L)
+    assert_parity(run_ln(ng, x, g, b, rows, L, path=SPLIT, offset=offset), want, f"LN large split {rows}x{L}")
+    assert_parity(run_ln(ng, x, g, b, rows, L, path=SPLIT, offset=offset, inplace=True), want,
+                  f"LN large split in place {rows}x{L}")
