@@ -531,8 +531,11 @@ __global__ void __launch_bounds__(GS_T) gns_split_apply_kernel(GnSegParams p)
     T *y = static_cast<T *>(p.y);
     const T *gm = static_cast<const T *>(p.gamma);
     const T *bt = static_cast<const T *>(p.beta);
-    for (int64_t r = blockIdx.y; r < p.rows; r += gridDim.y) {
-        const int pc = blockIdx.x;
+    // Segments and chunks in the reverse of the statistics kernel's order:
+    // the most recently read part of x is the likeliest still in L2.
+    for (int64_t rr = blockIdx.y; rr < p.rows; rr += gridDim.y) {
+        const int64_t r = p.rows - 1 - rr;
+        const int pc = P - 1 - static_cast<int>(blockIdx.x);
         const T *xr = x + r * p.seg_len;
         T *yr = y + r * p.seg_len;
         if (threadIdx.x < 32) {

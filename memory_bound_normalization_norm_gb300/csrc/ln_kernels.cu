@@ -671,7 +671,8 @@ __global__ void __launch_bounds__(LS_T) ln_split_stats_kernel(LnParams p)
         const int64_t hi = (lo + p.chunk < p.row_len) ? lo + p.chunk : p.row_len;
         Moments m = {0.f, 0.f, 0.f};
         if (VEC) {
-            const uint64_t pol = policy_evict_first();
+            // x stays in L2 for the apply kernel's re-read where it fits
+            const uint64_t pol = policy_evict_last();
             float s1 = 0.f, s2 = 0.f, cnt = 0.f;
             auto add = [&](const float4 &q) {
                 const float a = q.x - K, b = q.y - K, c = q.z - K, d = q.w - K;
@@ -724,8 +725,11 @@ __global__ void __launch_bounds__(LS_T) ln_split_apply_kernel(LnParams p)
     T *y = static_cast<T *>(p.y);
     const T *gm = static_cast<const T *>(p.gamma);
     const T *bt = static_cast<const T *>(p.beta);
-    for (int64_t r = blockIdx.y; r < p.rows; r += gridDim.y) {
-        const int pc = blockIdx.x;
+    // Rows and chunks in the reverse of the statistics kernel's order: the
+    // most recently read part of x is the likeliest still in L2.
+    for (int64_t rr = blockIdx.y; rr < p.rows; rr += gridDim.y) {
+        const int64_t r = p.rows - 1 - rr;
+        const int pc = P - 1 - static_cast<int>(blockIdx.x);
         const T *xr = x + r * p.row_len;
         T *yr = y + r * p.row_len;
         if (threadIdx.x < 32) {
