@@ -149,7 +149,9 @@ __device__ __forceinline__ Moments cluster_moments(float mean, float m2, float f
     if (threadIdx.x < CL)
         st_async_f4(peer_addr(&slot[rank], threadIdx.x), make_float4(mean, m2, flag, 0.f),
                     peer_addr(bar, threadIdx.x));
-    const bool ok = mbar_wait_bounded(bar, parity, wait_ns);
+    // one thread polls; the others wait at the CTA barrier without taking
+    // issue slots, and see the slots through it
+    const bool ok = threadIdx.x != 0 || mbar_wait_bounded(bar, parity, wait_ns);
     *timed_out = __syncthreads_or(!ok) != 0;
     const unsigned lane = threadIdx.x & 31;
     Moments m = {0.f, 0.f, 0.f};
@@ -392,6 +394,14 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
     const uint64_t pol_keep = policy_evict_last();
     const int64_t nk = cid < p.rows ? (p.rows - cid + ncl - 1) / ncl : 0;
     const uint64_t xwait_ns = p.timeout_ns > 100000000ull ? p.timeout_ns : 100000000ull;
+    // with one channel per vector, the channel of this thread's vector j
+    // within a segment is the same for every segment
+    int coff[MODE == AFF_CHAN ? V : 1];
+    if constexpr (MODE == AFF_CHAN) {
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            coff[j] = static_cast<int>(static_cast<uint32_t>(4 * (lo + tid + j * NT)) / static_cast<uint32_t>(p.S));
+    }
 
     if (tid == 0) {
         mbar_init(&full[0], 1);
@@ -427,8 +437,9 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
         const int b = static_cast<int>(k & 1);
         const uint32_t par = static_cast<uint32_t>((k >> 1) & 1);
         if (!stopped) {
-            const bool ok = mbar_wait_bounded(&full[b], par, p.timeout_ns);
-            // one decision for the whole CTA
+            // one thread polls, the others wait at the CTA barrier; the
+            // decision is the whole CTA's
+            const bool ok = tid != 0 || mbar_wait_bounded(&full[b], par, p.timeout_ns);
             if (__syncthreads_or(!ok)) {
                 gave_up = true;
                 stopped = true;
@@ -444,20 +455,21 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
             v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (!stopped) {
             K = first_elem<T>(piv[b]);
+            // from here on v holds d = x - K
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int i = tid + j * NT;
-                if (i < n4)
-                    v[j] = ld4_smem<T>(sb + 4 * i);
+                if (i < n4) {
+                    const float4 xv = ld4_smem<T>(sb + 4 * i);
+                    v[j] = make_float4(xv.x - K, xv.y - K, xv.z - K, xv.w - K);
+                }
             }
         }
         // exact two-pass statistics of this CTA's slice about the pivot
         float s = 0.f;
 #pragma unroll
-        for (int j = 0; j < V; ++j) {
-            if (tid + j * NT < n4)
-                s += ((v[j].x - K) + (v[j].y - K)) + ((v[j].z - K) + (v[j].w - K));
-        }
+        for (int j = 0; j < V; ++j)
+            s += (v[j].x + v[j].y) + (v[j].z + v[j].w); // zero outside the slice
         s = block_sum<NT>(s, red[0]);
         // every thread has its values in registers: refill this buffer with
         // the segment after next
@@ -471,8 +483,7 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             if (tid + j * NT < n4) {
-                const float a = (v[j].x - K) - mloc, c = (v[j].y - K) - mloc;
-                const float d = (v[j].z - K) - mloc, e = (v[j].w - K) - mloc;
+                const float a = v[j].x - mloc, c = v[j].y - mloc, d = v[j].z - mloc, e = v[j].w - mloc;
                 q += (a * a + c * c) + (d * d + e * e);
             }
         }
@@ -492,18 +503,40 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
         }
         if (stopped)
             continue; // keep exchanging, write nothing
-        const RowMean rm = finish_row(K, tot, p.eps);
+        // y = 2 * LReLU((x - mean) * rstd * gamma + beta), with x - mean =
+        // d - tot.mean; LReLU is positively homogeneous, so the factor 2 goes
+        // into the affine map: 2t = d * a + c, a = 2 * rstd * gamma,
+        // c = 2 * beta - tot.mean * a.
+        const float rstd = rsqrtf(fmaxf(tot.m2 / tot.n, 0.f) + p.eps);
+        const float mean_d = tot.mean;
+        const float slope = p.slope;
         const int64_t r = cid + k * ncl;
         const int64_t cbase = (r % p.G) * p.M;
         T *yr = y + r * p.seg_len;
+        auto lrelu = [slope](float t) { return t > 0.f ? t : slope * t; };
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int i = tid + j * NT;
             if (i < n4) {
                 const int64_t e = 4 * (lo + i);
-                float4 g, bb;
-                seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb);
-                Io<T>::st4_stream(yr + e, gn_apply4(v[j], rm, g, bb, p.slope), pol_stream);
+                float4 o;
+                if constexpr (MODE == AFF_CHAN) {
+                    const int64_t c = cbase + coff[j];
+                    const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
+                    const float a = 2.f * rstd * gv, cc = fmaf(-mean_d, a, 2.f * bv);
+                    o = make_float4(lrelu(fmaf(v[j].x, a, cc)), lrelu(fmaf(v[j].y, a, cc)),
+                                    lrelu(fmaf(v[j].z, a, cc)), lrelu(fmaf(v[j].w, a, cc)));
+                } else {
+                    float4 g, bb;
+                    seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb);
+                    const float ax = 2.f * rstd * g.x, ay = 2.f * rstd * g.y;
+                    const float az = 2.f * rstd * g.z, aw = 2.f * rstd * g.w;
+                    o = make_float4(lrelu(fmaf(v[j].x, ax, fmaf(-mean_d, ax, 2.f * bb.x))),
+                                    lrelu(fmaf(v[j].y, ay, fmaf(-mean_d, ay, 2.f * bb.y))),
+                                    lrelu(fmaf(v[j].z, az, fmaf(-mean_d, az, 2.f * bb.z))),
+                                    lrelu(fmaf(v[j].w, aw, fmaf(-mean_d, aw, 2.f * bb.w))));
+                }
+                Io<T>::st4_stream(yr + e, o, pol_stream);
             }
         }
     }
