@@ -183,16 +183,21 @@ def device_tensor(a, cfg, dev):
 
 def main_kernel_name(cfg) -> str:
     if cfg["op"] == "ln":
-        return "ln_rows_kernel" if cfg["L"] <= 16384 else "ln_persistent_kernel"
+        L, bf16 = cfg["L"], bool(cfg.get("bf16"))
+        if L <= 8192:
+            return "ln_rows_kernel"
+        if L <= 131072 and not bf16:
+            return "gns_stream_kernel"
+        return "ln_persistent_kernel" if L >= (1 << 20) and not bf16 else "ln_split_apply_kernel"
     if cfg["op"] == "gn":
         return "gn_vec4_kernel"
     if cfg["op"] == "gn_nchw":
-        return "gns_reg_kernel" if gn_nchw_one_launch(cfg) else "gns_split_apply_kernel"
+        return "gns_stream_kernel" if gn_nchw_one_launch(cfg) else "gns_split_apply_kernel"
     return "rms_reg_kernel"
 
 
 def gn_nchw_one_launch(cfg) -> bool:
-    """Groups of at most 131,072 values (a multiple of 4) take the one-launch register kernel."""
+    """Groups of at most 131,072 values (a multiple of 4) take the one-launch cluster kernel."""
     L = cfg["C"] // cfg["G"] * cfg["S"]
     return L % 4 == 0 and L <= 131072
 
@@ -203,7 +208,7 @@ def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
     bf16 = bool(cfg.get("bf16"))
     if op == "ln":
         rows, L = cfg["rows"], cfg["L"]
-        one_launch = L % 4 == 0 and (L <= 16384 or
+        one_launch = L % 4 == 0 and (L <= 8192 or (not bf16 and L <= 131072) or
                                      (not bf16 and (1 << 20) <= L <= ng.norm_layer_max_resident_row_len()))
         fn = ng.norm_layer_fwd_bf16 if bf16 else ng.norm_layer_fwd
         return (lambda: fn(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if one_launch else 2)
@@ -306,7 +311,7 @@ def hbm_peak():
 
 
 # the kernel source files each workload's counters depend on
-KERNEL_SOURCES = {"ln": ("ln_kernels.cu", "norm_internal.cuh"), "gn": ("gn_kernels.cu", "norm_internal.cuh"),
+KERNEL_SOURCES = {"ln": ("ln_kernels.cu", "gns_kernels.cu", "norm_internal.cuh"), "gn": ("gn_kernels.cu", "norm_internal.cuh"),
                   "gn_nchw": ("gns_kernels.cu", "ln_kernels.cu", "norm_internal.cuh"),
                   "rms": ("rms_kernels.cu", "norm_internal.cuh")}
 

@@ -84,9 +84,15 @@ typedef enum {
  *
  * Paths, all with a row length that is a multiple of 4 and 16-byte aligned
  * x/y/gamma/beta unless stated:
- *   - rows of at most 16,384 elements: one launch, one CTA per row at a
+ *   - rows of at most 8,192 elements: one launch, one CTA per row at a
  *     time with the row in registers; x is read from HBM once and the
  *     workspace is not used;
+ *   - rows of 8,193 to 131,072 elements: one launch of the thread-block
+ *     cluster kernel that GroupNorm over NCHW tensors uses (one group per
+ *     row): each row is split over one CTA or a cluster of up to 16 CTAs,
+ *     each CTA's next slices arrive by bulk copy into shared memory, and
+ *     the CTAs of a row exchange their partial statistics through
+ *     distributed shared memory; x is read from HBM once; no workspace;
  *   - rows of 2^20 or more elements (up to norm_layer_max_resident_row_len()):
  *     a persistent cooperative kernel (one CTA per SM) gives every CTA the
  *     same column slice of each row, holds the slice on chip (shared memory,
@@ -109,9 +115,13 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
  * bf16 form of the same operation; the pages work in fp32.  Same arguments,
  * workspace and errors as norm_layer_fwd, with 2-byte elements: pointers must
  * be 2-byte aligned, and the one-read paths want 8-byte aligned pointers and a
- * length that is a multiple of 4.  Rows of at most 16,384 elements take the
- * row kernel; longer rows the two-kernel path (the persistent kernel is fp32
- * only, so NORM_OPT_LN_PATH = 1 returns NORM_ERR_UNSUPPORTED here). */
+ * length that is a multiple of 4.  The automatic choice gives rows of at
+ * most 8,192 elements the row kernel and longer rows the two-kernel path,
+ * which measured faster for bf16 than the row kernel (up to 16,384) and the
+ * cluster kernel (up to 131,072, 16-byte aligned x, a length that is a
+ * multiple of 8); NORM_OPT_LN_PATH = 3 and 4 force those.  The persistent
+ * kernel is fp32 only, so NORM_OPT_LN_PATH = 1 returns NORM_ERR_UNSUPPORTED
+ * here. */
 norm_status_t norm_layer_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta, uint16_t *y,
                                   int64_t rows, int64_t row_len, float eps,
                                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
@@ -266,9 +276,10 @@ const char *norm_status_string(norm_status_t status);
  * while other threads are launching.
  *   NORM_OPT_LN_PATH             0 = choose automatically, 1 = force the
  *                                persistent single-read kernel, 2 = force the
- *                                two-kernel path, 3 = force the row kernel
- *                                (1 and 3: error NORM_ERR_UNSUPPORTED if the
- *                                shape does not fit).
+ *                                two-kernel path, 3 = force the row kernel,
+ *                                4 = force the thread-block cluster kernel
+ *                                (1, 3 and 4: error NORM_ERR_UNSUPPORTED if
+ *                                the shape does not fit).
  *   NORM_OPT_BARRIER_TIMEOUT_NS  how long a CTA waits at the LayerNorm grid
  *                                barrier (or for its own bulk copies) before
  *                                it records NORM_ERR_TIMEOUT and stops.  CTAs

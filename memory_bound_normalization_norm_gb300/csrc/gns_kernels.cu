@@ -357,7 +357,7 @@ __device__ __forceinline__ float first_elem(const float4 &raw)
 // segment on the whole cluster writes nothing, stops waiting for copies and
 // keeps exchanging (the exchanges still complete) until the end; each CTA
 // then drains its own copies.
-template <typename T, int NT, int V, int MODE>
+template <typename T, int NT, int V, int MODE, bool ACT>
 __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -503,17 +503,19 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
         }
         if (stopped)
             continue; // keep exchanging, write nothing
-        // y = 2 * LReLU((x - mean) * rstd * gamma + beta), with x - mean =
-        // d - tot.mean; LReLU is positively homogeneous, so the factor 2 goes
-        // into the affine map: 2t = d * a + c, a = 2 * rstd * gamma,
-        // c = 2 * beta - tot.mean * a.
+        // ACT: y = 2 * LReLU((x - mean) * rstd * gamma + beta), with x - mean
+        // = d - tot.mean; LReLU is positively homogeneous, so the factor 2
+        // goes into the affine map: 2t = d * a + c, a = 2 * rstd * gamma,
+        // c = 2 * beta - tot.mean * a.  Without ACT (LayerNorm): y = d * a + c
+        // with a = rstd * gamma, c = beta - tot.mean * a.
         const float rstd = rsqrtf(fmaxf(tot.m2 / tot.n, 0.f) + p.eps);
         const float mean_d = tot.mean;
         const float slope = p.slope;
+        constexpr float sc = ACT ? 2.f : 1.f;
         const int64_t r = cid + k * ncl;
         const int64_t cbase = (r % p.G) * p.M;
         T *yr = y + r * p.seg_len;
-        auto lrelu = [slope](float t) { return t > 0.f ? t : slope * t; };
+        auto lrelu = [slope](float t) { return ACT ? (t > 0.f ? t : slope * t) : t; };
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int i = tid + j * NT;
@@ -523,18 +525,18 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
                 if constexpr (MODE == AFF_CHAN) {
                     const int64_t c = cbase + coff[j];
                     const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
-                    const float a = 2.f * rstd * gv, cc = fmaf(-mean_d, a, 2.f * bv);
+                    const float a = sc * rstd * gv, cc = fmaf(-mean_d, a, sc * bv);
                     o = make_float4(lrelu(fmaf(v[j].x, a, cc)), lrelu(fmaf(v[j].y, a, cc)),
                                     lrelu(fmaf(v[j].z, a, cc)), lrelu(fmaf(v[j].w, a, cc)));
                 } else {
                     float4 g, bb;
                     seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb);
-                    const float ax = 2.f * rstd * g.x, ay = 2.f * rstd * g.y;
-                    const float az = 2.f * rstd * g.z, aw = 2.f * rstd * g.w;
-                    o = make_float4(lrelu(fmaf(v[j].x, ax, fmaf(-mean_d, ax, 2.f * bb.x))),
-                                    lrelu(fmaf(v[j].y, ay, fmaf(-mean_d, ay, 2.f * bb.y))),
-                                    lrelu(fmaf(v[j].z, az, fmaf(-mean_d, az, 2.f * bb.z))),
-                                    lrelu(fmaf(v[j].w, aw, fmaf(-mean_d, aw, 2.f * bb.w))));
+                    const float ax = sc * rstd * g.x, ay = sc * rstd * g.y;
+                    const float az = sc * rstd * g.z, aw = sc * rstd * g.w;
+                    o = make_float4(lrelu(fmaf(v[j].x, ax, fmaf(-mean_d, ax, sc * bb.x))),
+                                    lrelu(fmaf(v[j].y, ay, fmaf(-mean_d, ay, sc * bb.y))),
+                                    lrelu(fmaf(v[j].z, az, fmaf(-mean_d, az, sc * bb.z))),
+                                    lrelu(fmaf(v[j].w, aw, fmaf(-mean_d, aw, sc * bb.w))));
                 }
                 Io<T>::st4_stream(yr + e, o, pol_stream);
             }
@@ -872,32 +874,36 @@ namespace {
 // Streamed variants: 256 threads, 4 or 8 vectors a thread.
 constexpr int GNS_STREAM_NT = 256;
 
-template <typename T, int MODE>
+template <typename T, int MODE, bool ACT>
 RegKernel stream_kernel_for(int per, int *idx)
 {
     if (per <= 1024) {
         *idx = 0;
-        return gns_stream_kernel<T, GNS_STREAM_NT, 4, MODE>;
+        return gns_stream_kernel<T, GNS_STREAM_NT, 4, MODE, ACT>;
     }
     if (per <= 2048) {
         *idx = 1;
-        return gns_stream_kernel<T, GNS_STREAM_NT, 8, MODE>;
+        return gns_stream_kernel<T, GNS_STREAM_NT, 8, MODE, ACT>;
     }
     *idx = -1;
     return nullptr;
 }
 
+// GroupNorm (act: LeakyReLU x2) in all three channel maps; LayerNorm (no
+// act) is one group of the whole row with per-element gamma/beta (S = 1).
 template <typename T>
-RegKernel stream_kernel_t(int per, int mode, int *idx)
+RegKernel stream_kernel_t(int per, int mode, bool act, int *idx)
 {
+    if (!act)
+        return mode == AFF_ROW ? stream_kernel_for<T, AFF_ROW, false>(per, idx) : nullptr;
     switch (mode) {
-    case AFF_ROW: return stream_kernel_for<T, AFF_ROW>(per, idx);
-    case AFF_CHAN: return stream_kernel_for<T, AFF_CHAN>(per, idx);
-    default: return stream_kernel_for<T, AFF_ANY>(per, idx);
+    case AFF_ROW: return stream_kernel_for<T, AFF_ROW, true>(per, idx);
+    case AFF_CHAN: return stream_kernel_for<T, AFF_CHAN, true>(per, idx);
+    default: return stream_kernel_for<T, AFF_ANY, true>(per, idx);
     }
 }
 
-constexpr int GNS_STREAM_VARIANTS = 6; // 2 CTA shapes x 3 affine modes
+constexpr int GNS_STREAM_VARIANTS = 8; // 2 CTA shapes x (3 GroupNorm channel maps + LayerNorm)
 std::atomic<int> g_stream_active[GNS_DEVICES][2][GNS_STREAM_VARIANTS][5];
 std::once_flag g_stream_init;
 
@@ -917,19 +923,21 @@ size_t stream_smem(int64_t per, bool bf16)
 
 } // namespace
 
-cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, int cluster, int *clusters)
+cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool act, int cluster, int *clusters)
 {
     *clusters = 0;
     if (cluster < 1 || cluster > GNS_MAX_CLUSTER || (cluster & (cluster - 1)) != 0)
         return cudaErrorInvalidValue;
     const int64_t per = stream_per(seg_len, cluster);
+    if (per > 2048)
+        return cudaErrorInvalidValue;
     int idx = 0, dev = 0;
     const int mode = affine_mode(S);
-    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, &idx)
-                             : stream_kernel_t<float>(static_cast<int>(per), mode, &idx);
-    if (!k || per > 2048)
+    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, act, &idx)
+                             : stream_kernel_t<float>(static_cast<int>(per), mode, act, &idx);
+    if (!k)
         return cudaErrorInvalidValue;
-    idx += 2 * mode;
+    idx += 2 * (act ? mode : 3);
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
@@ -980,10 +988,10 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, int c
     return e;
 }
 
-cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, int cluster, cudaStream_t stream)
+cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int cluster, cudaStream_t stream)
 {
     int active = 0;
-    cudaError_t e = gns_stream_max_clusters(p.seg_len, p.S, bf16, cluster, &active);
+    cudaError_t e = gns_stream_max_clusters(p.seg_len, p.S, bf16, act, cluster, &active);
     if (e != cudaSuccess)
         return e;
     if (active < 1)
@@ -991,8 +999,8 @@ cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, int cluster, cuda
     const int64_t per = stream_per(p.seg_len, cluster);
     int idx = 0;
     const int mode = affine_mode(p.S);
-    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, &idx)
-                             : stream_kernel_t<float>(static_cast<int>(per), mode, &idx);
+    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, act, &idx)
+                             : stream_kernel_t<float>(static_cast<int>(per), mode, act, &idx);
     int64_t clusters = active;
     if (clusters > p.rows)
         clusters = p.rows;

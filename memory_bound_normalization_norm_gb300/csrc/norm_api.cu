@@ -22,6 +22,15 @@ constexpr size_t kWsHeader = sizeof(normk::LnSync);
 // row must stream for longer than a grid barrier takes for the barrier to hide
 // behind the prefetch of the next rows.
 constexpr int64_t kPersistentMinRowLen = int64_t(1) << 20;
+// NORM_OPT_LN_PATH value of the streamed cluster kernel, and the longest
+// row the automatic choice gives the row kernel.  Measured on GB300 (GB/s
+// fractions of the copy peak): fp32 rows of 4,096 run best on the row kernel
+// (0.85 vs 0.81 streamed), rows of 16,384 to 131,072 on the streamed kernel
+// (0.71 to 0.58 vs 0.65 on the row kernel and 0.52 on the two-kernel path);
+// bf16 rows above 8,192 run best on the two-kernel path (0.44 vs 0.42
+// streamed and 0.38 on the row kernel).
+constexpr int64_t kLnStream = 4;
+constexpr int64_t kLnRowsMaxAuto = 8192;
 
 struct DeviceState {
     bool init = false;
@@ -285,7 +294,7 @@ norm_status_t norm_set_option(norm_option_t option, int64_t value)
         return NORM_ERR_INVALID_ARG;
     switch (option) {
     case NORM_OPT_LN_PATH:
-        if (value > 3)
+        if (value > 4)
             return NORM_ERR_INVALID_ARG;
         g_opt_ln_path = value;
         return NORM_OK;
@@ -399,18 +408,38 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     const int64_t path_opt = g_opt_ln_path.load();
     LnPlan pl;
     bool persistent = false;
+    // Streamed cluster kernel (shared with GroupNorm: one group per row, no
+    // activation): rows of up to 131,072 elements, read once.
+    int ln_cluster = 0;
+    if (vec4 && aligned(x, 16) && (bf16 ? (row_len & 7) == 0 : true)) {
+        const int cl = gn_auto_cluster(row_len / 4);
+        int64_t per = cl ? (row_len / 4 + cl - 1) / cl : 0;
+        per = (per + 1) & ~int64_t(1);
+        int active = 0;
+        if (cl && per <= 2048 && normk::gns_stream_max_clusters(row_len, 1, bf16, false, cl, &active) == cudaSuccess &&
+            active >= 1)
+            ln_cluster = cl;
+        else
+            cudaGetLastError();
+    }
+    if (path_opt == kLnStream && !ln_cluster)
+        return NORM_ERR_UNSUPPORTED;
+    const bool ln_stream =
+        ln_cluster && (path_opt == kLnStream || (path_opt == 0 && !bf16 && row_len > kLnRowsMaxAuto &&
+                                                 row_len < kPersistentMinRowLen));
     const bool row_kernel_fits = vec4 && row_len <= normk::ln_rows_max_row_len();
-    const bool row_kernel = row_kernel_fits && (path_opt == 3 || (path_opt == 0 && row_len < kPersistentMinRowLen));
+    const bool row_kernel = !ln_stream && row_kernel_fits &&
+                            (path_opt == 3 || (path_opt == 0 && row_len <= (bf16 ? kLnRowsMaxAuto : 16384)));
     if (path_opt == 3 && !row_kernel)
         return NORM_ERR_UNSUPPORTED;
-    if (row_kernel) {
-        pl.path = 3;
+    if (row_kernel || ln_stream) {
+        pl.path = ln_stream ? kLnStream : 3;
         pl.ws_bytes = 0;
     }
     // the persistent kernel is fp32 only
     if (path_opt == 1 && bf16)
         return NORM_ERR_UNSUPPORTED;
-    if (!row_kernel && path_opt != 2 && vec4 && !bf16) {
+    if (!row_kernel && !ln_stream && path_opt != 2 && vec4 && !bf16) {
         LnPlan pp;
         if (plan_persistent(rows, row_len, *d, &pp) && (path_opt == 1 || row_len >= kPersistentMinRowLen)) {
             pl = pp;
@@ -419,7 +448,7 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     }
     if (path_opt == 1 && !persistent)
         return NORM_ERR_UNSUPPORTED;
-    if (!persistent && !row_kernel)
+    if (!persistent && !row_kernel && !ln_stream)
         plan_split(rows, row_len, vec4, *d, &pl);
 
     void *ws = workspace;
@@ -467,7 +496,23 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     p.chunk = pl.chunk;
     p.parts = pl.parts;
     cudaError_t e;
-    if (row_kernel) {
+    if (ln_stream) {
+        normk::GnSegParams q;
+        std::memset(&q, 0, sizeof(q));
+        q.x = x;
+        q.gamma = gamma;
+        q.beta = beta;
+        q.y = y;
+        q.rows = rows;
+        q.seg_len = row_len;
+        q.G = 1;
+        q.M = row_len;
+        q.S = 1;
+        q.eps = eps;
+        q.timeout_ns = p.timeout_ns;
+        q.err = d->err;
+        e = normk::gns_stream_launch(q, bf16, false, ln_cluster, stream);
+    } else if (row_kernel) {
         e = normk::ln_rows_launch(p, bf16, d->sm_count, stream);
     } else if (persistent) {
         p.tag_skew = static_cast<unsigned>(g_opt_extra_arrivals.load());
@@ -581,7 +626,7 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         stream_slice = (stream_slice + 1) & ~int64_t(1);
         int active = 0;
         stream_ok = stream_slice <= 2048 &&
-                    normk::gns_stream_max_clusters(L, S, bf16, cluster, &active) == cudaSuccess && active >= 1;
+                    normk::gns_stream_max_clusters(L, S, bf16, true, cluster, &active) == cudaSuccess && active >= 1;
         if (!stream_ok)
             cudaGetLastError();
     }
@@ -620,7 +665,7 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     p.err = d->err;
 
     if (pl.path == kGnStream) {
-        e = normk::gns_stream_launch(p, bf16, cluster, stream);
+        e = normk::gns_stream_launch(p, bf16, true, cluster, stream);
     } else if (pl.path == kGnReg) {
         e = normk::gns_reg_launch(p, bf16, cluster, stream);
     } else if (pl.path == kGnWarp) {

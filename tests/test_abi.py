@@ -65,8 +65,8 @@ def test_status_strings(lib):
 def test_options_validate_and_round_trip(lib):
     raw = lib.raw()
     assert raw.norm_set_option(99, 1) == INVALID
-    assert raw.norm_set_option(lib.NORM_OPT_LN_PATH, 4) == INVALID
-    for path in (3, 2, 1, 0):
+    assert raw.norm_set_option(lib.NORM_OPT_LN_PATH, 5) == INVALID
+    for path in (4, 3, 2, 1, 0):
         assert raw.norm_set_option(lib.NORM_OPT_LN_PATH, path) == OK
         assert raw.norm_get_option(lib.NORM_OPT_LN_PATH) == path
     assert raw.norm_set_option(lib.NORM_OPT_LN_PATH, -1) == INVALID

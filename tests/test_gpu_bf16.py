@@ -87,6 +87,7 @@ def run_ln(ng, x, g, b, rows, L, path=0, offset=0, inplace=False):
 
 @pytest.mark.parametrize("rows,L,path", [
     (3, 12, 3), (64, 4096, 3), (9, 16384, 3), (5, 1000, 3),   # row kernel
+    (64, 4096, 4), (5, 20000, 4), (2, 131072, 4), (3, 65544, 4),  # streamed cluster kernel
     (2, 16388, 2), (3, 4096, 2), (2, 1 << 20, 0),             # two-kernel path, vector form
     (3, 1001, 0),                                             # two-kernel path, scalar form
 ])

@@ -1,9 +1,10 @@
 """LayerNorm on the GPU against the float64 oracle, element by element.
 
-All three paths are covered: the persistent single-read kernel (forced, and chosen
+All four paths are covered: the persistent single-read kernel (forced, and chosen
 automatically for long rows), the one-launch row kernel (forced, and chosen
-automatically for rows of at most 16,384 elements) and the two-kernel split path
-(forced, and taken for ragged or misaligned rows).  Shapes span several CTAs per row with ragged slices,
+automatically for rows of at most 8,192 elements), the thread-block cluster kernel
+shared with GroupNorm (forced, and chosen for fp32 rows of 8,193 to 131,072) and the
+two-kernel split path (forced, and taken for ragged or misaligned rows).  Shapes span several CTAs per row with ragged slices,
 rows shorter than one float4 per CTA, the largest row the persistent kernel
 holds on chip, and the two full-size workloads: (16, 64, 256, 256) with N(0,1)
 inputs and the cancellation stress x ~ N(1000, 0.01^2).
@@ -179,8 +180,11 @@ def test_layer_norm_row_kernel(ng, rows, L):
     want = oracle.layer_norm(x, g, b, rows, L)
     forced = run_ln(ng, x, g, b, rows, L, path=ROWS)
     assert_parity(forced, want, f"LN row kernel {rows}x{L}")
-    # chosen automatically for these shapes: the same bits
-    assert np.array_equal(run_ln(ng, x, g, b, rows, L), forced)
+    if L <= 8192:
+        # chosen automatically for these shapes: the same bits
+        assert np.array_equal(run_ln(ng, x, g, b, rows, L), forced)
+    else:
+        assert_parity(run_ln(ng, x, g, b, rows, L), want, f"LN auto {rows}x{L}")
 
 
 def test_layer_norm_row_kernel_stress_in_place_and_no_affine(ng):
@@ -220,3 +224,38 @@ def test_split_path_large(ng, rows, L, offset):
     assert_parity(run_ln(ng, x, g, b, rows, L, path=SPLIT, offset=offset), want, f"LN large split {rows}x{L}")
     assert_parity(run_ln(ng, x, g, b, rows, L, path=SPLIT, offset=offset, inplace=True), want,
                   f"LN large split in place {rows}x{L}")
+
+
+STREAM = 4
+
+
+@pytest.mark.parametrize("rows,L", [(3, 4096), (5, 20000), (2, 131072), (7, 65544), (300, 2048), (33, 16388)])
+def test_streamed_cluster_kernel(ng, rows, L):
+    # the cluster kernel shared with GroupNorm: one CTA (L <= 8192) or a cluster
+    # of up to 16 per row, slices by bulk copy, one exchange of partials per row
+    x, g, b = inputs(rows, L, seed=rows + 3 * L)
+    want = oracle.layer_norm(x, g, b, rows, L)
+    assert_parity(run_ln(ng, x, g, b, rows, L, path=STREAM), want, f"LN streamed {rows}x{L}")
+    assert_parity(run_ln(ng, x, g, b, rows, L, path=STREAM, inplace=True), want, f"LN streamed in place {rows}x{L}")
+    xn, _, _ = inputs(rows, L, seed=rows + 3 * L, affine=False)
+    assert_parity(run_ln(ng, xn, None, None, rows, L, path=STREAM), oracle.layer_norm(xn, None, None, rows, L),
+                  f"LN streamed no affine {rows}x{L}")
+
+
+def test_streamed_cluster_kernel_cancellation(ng):
+    rows, L = 6, 65536
+    x, _, _ = inputs(rows, L, seed=77, mean=1000.0, std=0.01, affine=False)
+    assert_parity(run_ln(ng, x, None, None, rows, L, path=STREAM), oracle.layer_norm(x, None, None, rows, L),
+                  "LN streamed N(1000, 0.01^2)")
+
+
+def test_streamed_cluster_kernel_refusals(ng):
+    x, g, b = inputs(2, 4096, seed=78)
+    with pytest.raises(ng.NormError) as e:
+        run_ln(ng, x, g, b, 2, 4096, path=STREAM, offset=1)  # not 16-byte aligned
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    x, g, b = inputs(1, 262144, seed=79)
+    with pytest.raises(ng.NormError) as e:
+        run_ln(ng, x, g, b, 1, 262144, path=STREAM)  # longer than 16 CTAs hold
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, AUTO)
