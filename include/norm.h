@@ -115,13 +115,11 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
  * bf16 form of the same operation; the pages work in fp32.  Same arguments,
  * workspace and errors as norm_layer_fwd, with 2-byte elements: pointers must
  * be 2-byte aligned, and the one-read paths want 8-byte aligned pointers and a
- * length that is a multiple of 4.  The automatic choice gives rows of at
- * most 8,192 elements the row kernel and longer rows the two-kernel path,
- * which measured faster for bf16 than the row kernel (up to 16,384) and the
- * cluster kernel (up to 131,072, 16-byte aligned x, a length that is a
- * multiple of 8); NORM_OPT_LN_PATH = 3 and 4 force those.  The persistent
- * kernel is fp32 only, so NORM_OPT_LN_PATH = 1 returns NORM_ERR_UNSUPPORTED
- * here. */
+ * length that is a multiple of 4.  Paths as for fp32, except that the
+ * cluster kernel wants 16-byte aligned x and a length that is a multiple of 8,
+ * and that the persistent kernel is fp32 only (NORM_OPT_LN_PATH = 1 returns
+ * NORM_ERR_UNSUPPORTED here): rows above 131,072 elements take the
+ * two-kernel path. */
 norm_status_t norm_layer_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta, uint16_t *y,
                                   int64_t rows, int64_t row_len, float eps,
                                   void *workspace, size_t workspace_bytes, cudaStream_t stream);

@@ -22,9 +22,9 @@
 //  - streamed register path (the same split, for slices of more than 256
 //    vectors with 16-byte aligned rows; the automatic choice there): a
 //    persistent grid of clusters walks segments, and each CTA's slice of the
-//    segment after next arrives by bulk copy (TMA engine, cp.async.bulk +
-//    mbarrier) into one of two shared-memory buffers while the current one
-//    is reduced and written.  Each CTA reduces its slice to an exact
+//    next segment arrives by bulk copy (TMA engine, cp.async.bulk +
+//    mbarrier) into a shared-memory buffer while the current one is reduced
+//    and written from registers.  Each CTA reduces its slice to an exact
 //    two-pass (mean, M2) and one all-to-all exchange per segment (st.async
 //    into every CTA's shared memory, counted on that CTA's mbarrier) gives
 //    every CTA the partials, merged with Chan's update in rank order.  A
@@ -317,6 +317,14 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
 
 // ------------------------------------------------------------------ streamed register path
 
+// One slice buffer per CTA and registers sized for 4 CTAs per SM (a few
+// spilled bytes at 8 vectors a thread) measured faster than two buffers at 3
+// CTAs per SM: more clusters are resident, so the last wave of segments is
+// shorter (GroupNorm (8,512,64,64): 29.6 vs 30.9 us; LayerNorm rows of
+// 131,072: 112 vs 136 us).
+constexpr int GNS_NBUF = 1;     // shared-memory slice buffers per CTA
+constexpr int GNS_MIN_CTAS = 4; // CTAs per SM the register budget is sized for
+
 template <typename T>
 __device__ __forceinline__ float4 ld4_smem(const T *p);
 
@@ -345,9 +353,10 @@ __device__ __forceinline__ float first_elem(const float4 &raw)
 // grid: a persistent set of clusters of CL = p.parts CTAs (CL = 1 allowed);
 // cluster c walks segments r_k = c + k * (cluster count).  CTA `rank` owns
 // vectors [rank * per, rank * per + per) of each segment (per = p.per4).
-// Dynamic shared memory: two slice buffers of per vectors; the slice of the
-// segment after next is in flight while the current one is reduced and
-// written.  Per segment each CTA computes the exact two-pass (mean, M2) of
+// Dynamic shared memory: GNS_NBUF slice buffers of per vectors; a slice
+// moves to registers as soon as it lands and the buffer is refilled at once,
+// so the next segment's slice is in flight while the current one is reduced
+// and written.  Per segment each CTA computes the exact two-pass (mean, M2) of
 // its slice about the pivot, and one all-to-all exchange (st.async into
 // every CTA's shared memory, counted on its mbarrier) gives every CTA the
 // CL partials, merged in rank order.
@@ -358,7 +367,7 @@ __device__ __forceinline__ float first_elem(const float4 &raw)
 // keeps exchanging (the exchanges still complete) until the end; each CTA
 // then drains its own copies.
 template <typename T, int NT, int V, int MODE, bool ACT>
-__global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
+__global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float4 piv[2]; // first 16 bytes of the segment, copied with the slice
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
     };
     const uint32_t slice_bytes = static_cast<uint32_t>(n4) * 4u * sizeof(T);
     T *buf0 = reinterpret_cast<T *>(smem);
-    T *buf1 = buf0 + static_cast<size_t>(per) * 4;
+    T *buf1 = GNS_NBUF > 1 ? buf0 + static_cast<size_t>(per) * 4 : buf0;
     constexpr bool narrow = true;
     const T *x = static_cast<const T *>(p.x);
     T *y = static_cast<T *>(p.y);
@@ -418,7 +427,7 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
     // thread 0: copy this CTA's slice of segment k (and the segment's first
     // 16 bytes, which hold the pivot) into buffer k & 1
     auto issue = [&](int64_t k) {
-        const int b = static_cast<int>(k & 1);
+        const int b = static_cast<int>(k % GNS_NBUF);
         const T *xr = x + (cid + k * ncl) * p.seg_len;
         mbar_arrive_expect_tx(&full[b], slice_bytes + 16u);
         bulk_g2s(&piv[b], xr, 16u, &full[b], pol_stream);
@@ -427,19 +436,21 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
     };
     int64_t issued = 0;
     if (tid == 0) {
-        for (; issued < 2 && issued < nk; ++issued)
+        for (; issued < GNS_NBUF && issued < nk; ++issued)
             issue(issued);
     }
     bool stopped = false; // this cluster writes nothing more
     bool gave_up = false; // this CTA's own wait gave up
     int64_t consumed = 0; // segments whose copies this CTA has seen complete
     for (int64_t k = 0; k < nk; ++k) {
-        const int b = static_cast<int>(k & 1);
+        const int b = static_cast<int>(k & 1); // exchange slots: segment parity
         const uint32_t par = static_cast<uint32_t>((k >> 1) & 1);
+        const int db = static_cast<int>(k % GNS_NBUF); // data buffer
+        const uint32_t dpar = static_cast<uint32_t>((k / GNS_NBUF) & 1);
         if (!stopped) {
             // one thread polls, the others wait at the CTA barrier; the
             // decision is the whole CTA's
-            const bool ok = tid != 0 || mbar_wait_bounded(&full[b], par, p.timeout_ns);
+            const bool ok = tid != 0 || mbar_wait_bounded(&full[db], dpar, p.timeout_ns);
             if (__syncthreads_or(!ok)) {
                 gave_up = true;
                 stopped = true;
@@ -447,14 +458,14 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
                 consumed = k + 1;
             }
         }
-        const T *sb = b ? buf1 : buf0;
+        const T *sb = db ? buf1 : buf0;
         float4 v[V];
         float K = 0.f;
 #pragma unroll
         for (int j = 0; j < V; ++j)
             v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (!stopped) {
-            K = first_elem<T>(piv[b]);
+            K = first_elem<T>(piv[db]);
             // from here on v holds d = x - K
 #pragma unroll
             for (int j = 0; j < V; ++j) {
@@ -472,8 +483,8 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
             s += (v[j].x + v[j].y) + (v[j].z + v[j].w); // zero outside the slice
         s = block_sum<NT>(s, red[0]);
         // every thread has its values in registers: refill this buffer with
-        // the segment after next
-        if (tid == 0 && !stopped && issued < nk && issued == k + 2) {
+        // the segment GNS_NBUF ahead
+        if (tid == 0 && !stopped && issued < nk && issued == k + GNS_NBUF) {
             fence_proxy_async_smem();
             issue(issued);
             ++issued;
@@ -548,7 +559,7 @@ __global__ void __launch_bounds__(NT) gns_stream_kernel(GnSegParams p)
         // the copies this CTA issued and never saw complete still write its
         // shared memory: wait for them before the CTA exits
         for (int64_t j = consumed; j < issued; ++j)
-            mbar_wait_bounded(&full[j & 1], static_cast<uint32_t>((j >> 1) & 1), xwait_ns);
+            mbar_wait_bounded(&full[j % GNS_NBUF], static_cast<uint32_t>((j / GNS_NBUF) & 1), xwait_ns);
     }
 }
 
@@ -918,7 +929,7 @@ int64_t stream_per(int64_t seg_len, int cluster)
 
 size_t stream_smem(int64_t per, bool bf16)
 {
-    return 2u * static_cast<size_t>(per) * 4u * (bf16 ? 2u : 4u);
+    return static_cast<size_t>(GNS_NBUF) * static_cast<size_t>(per) * 4u * (bf16 ? 2u : 4u);
 }
 
 } // namespace

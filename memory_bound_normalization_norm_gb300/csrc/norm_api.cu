@@ -24,11 +24,11 @@ constexpr size_t kWsHeader = sizeof(normk::LnSync);
 constexpr int64_t kPersistentMinRowLen = int64_t(1) << 20;
 // NORM_OPT_LN_PATH value of the streamed cluster kernel, and the longest
 // row the automatic choice gives the row kernel.  Measured on GB300 (GB/s
-// fractions of the copy peak): fp32 rows of 4,096 run best on the row kernel
-// (0.85 vs 0.81 streamed), rows of 16,384 to 131,072 on the streamed kernel
-// (0.71 to 0.58 vs 0.65 on the row kernel and 0.52 on the two-kernel path);
-// bf16 rows above 8,192 run best on the two-kernel path (0.44 vs 0.42
-// streamed and 0.38 on the row kernel).
+// fractions of the copy peak): rows of 4,096 run best on the row kernel
+// (fp32 0.84 vs 0.82 streamed, bf16 0.61 vs 0.49), rows of 16,384 to
+// 131,072 on the streamed kernel (fp32 0.74 to 0.70 vs 0.64 on the row
+// kernel and 0.52 on the two-kernel path; bf16 0.47 to 0.38 vs 0.43 to 0.37
+// on the two-kernel path).
 constexpr int64_t kLnStream = 4;
 constexpr int64_t kLnRowsMaxAuto = 8192;
 
@@ -425,11 +425,11 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     if (path_opt == kLnStream && !ln_cluster)
         return NORM_ERR_UNSUPPORTED;
     const bool ln_stream =
-        ln_cluster && (path_opt == kLnStream || (path_opt == 0 && !bf16 && row_len > kLnRowsMaxAuto &&
-                                                 row_len < kPersistentMinRowLen));
+        ln_cluster && (path_opt == kLnStream ||
+                       (path_opt == 0 && row_len > kLnRowsMaxAuto && row_len < kPersistentMinRowLen));
     const bool row_kernel_fits = vec4 && row_len <= normk::ln_rows_max_row_len();
     const bool row_kernel = !ln_stream && row_kernel_fits &&
-                            (path_opt == 3 || (path_opt == 0 && row_len <= (bf16 ? kLnRowsMaxAuto : 16384)));
+                            (path_opt == 3 || (path_opt == 0 && row_len < kPersistentMinRowLen));
     if (path_opt == 3 && !row_kernel)
         return NORM_ERR_UNSUPPORTED;
     if (row_kernel || ln_stream) {
