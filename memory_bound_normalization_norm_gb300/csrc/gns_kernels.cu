@@ -350,6 +350,36 @@ __device__ __forceinline__ float first_elem(const float4 &raw)
         return Io<__nv_bfloat16>::unpack(__float_as_uint(raw.x), 0u).x;
 }
 
+// A thread's copy of one 4-element vector of its slice.  fp32: d = x - K
+// in a float4.  bf16: the packed values as loaded (two registers, so a CTA
+// holds twice as many vectors), widened and shifted each time they are used.
+template <typename T>
+struct Held;
+
+template <>
+struct Held<float> {
+    float4 d;
+    __device__ __forceinline__ void clear() { d = make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ __forceinline__ void load(const float *p, float K)
+    {
+        const float4 x = ld4_smem<float>(p);
+        d = make_float4(x.x - K, x.y - K, x.z - K, x.w - K);
+    }
+    __device__ __forceinline__ float4 get(float) const { return d; }
+};
+
+template <>
+struct Held<__nv_bfloat16> {
+    uint2 raw;
+    __device__ __forceinline__ void clear() { raw = make_uint2(0u, 0u); }
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p, float) { raw = *reinterpret_cast<const uint2 *>(p); }
+    __device__ __forceinline__ float4 get(float K) const
+    {
+        const float4 x = Io<__nv_bfloat16>::unpack(raw.x, raw.y);
+        return make_float4(x.x - K, x.y - K, x.z - K, x.w - K);
+    }
+};
+
 // grid: a persistent set of clusters of CL = p.parts CTAs (CL = 1 allowed);
 // cluster c walks segments r_k = c + k * (cluster count).  CTA `rank` owns
 // vectors [rank * per, rank * per + per) of each segment (per = p.per4).
@@ -403,14 +433,13 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
     const uint64_t pol_keep = policy_evict_last();
     const int64_t nk = cid < p.rows ? (p.rows - cid + ncl - 1) / ncl : 0;
     const uint64_t xwait_ns = p.timeout_ns > 100000000ull ? p.timeout_ns : 100000000ull;
-    // with one channel per vector, the channel of this thread's vector j
-    // within a segment is the same for every segment
-    int coff[MODE == AFF_CHAN ? V : 1];
-    if constexpr (MODE == AFF_CHAN) {
-#pragma unroll
-        for (int j = 0; j < V; ++j)
-            coff[j] = static_cast<int>(static_cast<uint32_t>(4 * (lo + tid + j * NT)) / static_cast<uint32_t>(p.S));
-    }
+    // With one channel per vector, the channel of this thread's vector j
+    // within a segment is the same for every segment: c0 and r0 are those of
+    // vector 0 (quotient and remainder of its first element by S); vector
+    // j + 1 starts 4 * NT elements further on.
+    const uint32_t S32 = static_cast<uint32_t>(p.S);
+    const uint32_t e0 = static_cast<uint32_t>(4 * (lo + tid));
+    const uint32_t c0 = MODE == AFF_CHAN ? e0 / S32 : 0u, r0 = MODE == AFF_CHAN ? e0 % S32 : 0u;
 
     if (tid == 0) {
         mbar_init(&full[0], 1);
@@ -442,7 +471,15 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
     bool stopped = false; // this cluster writes nothing more
     bool gave_up = false; // this CTA's own wait gave up
     int64_t consumed = 0; // segments whose copies this CTA has seen complete
+    // group index (segment mod G) of the current segment, stepped without a
+    // division per segment
+    int64_t rg_next = cid % p.G;
+    const int64_t rg_step = ncl % p.G;
     for (int64_t k = 0; k < nk; ++k) {
+        const int64_t rg = rg_next;
+        rg_next += rg_step;
+        if (rg_next >= p.G)
+            rg_next -= p.G;
         const int b = static_cast<int>(k & 1); // exchange slots: segment parity
         const uint32_t par = static_cast<uint32_t>((k >> 1) & 1);
         const int db = static_cast<int>(k % GNS_NBUF); // data buffer
@@ -459,28 +496,29 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
             }
         }
         const T *sb = db ? buf1 : buf0;
-        float4 v[V];
+        Held<T> v[V];
         float K = 0.f;
 #pragma unroll
         for (int j = 0; j < V; ++j)
-            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j].clear();
         if (!stopped) {
             K = first_elem<T>(piv[db]);
-            // from here on v holds d = x - K
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int i = tid + j * NT;
-                if (i < n4) {
-                    const float4 xv = ld4_smem<T>(sb + 4 * i);
-                    v[j] = make_float4(xv.x - K, xv.y - K, xv.z - K, xv.w - K);
-                }
+                if (i < n4)
+                    v[j].load(sb + 4 * i, K);
             }
         }
         // exact two-pass statistics of this CTA's slice about the pivot
         float s = 0.f;
 #pragma unroll
-        for (int j = 0; j < V; ++j)
-            s += (v[j].x + v[j].y) + (v[j].z + v[j].w); // zero outside the slice
+        for (int j = 0; j < V; ++j) {
+            if (tid + j * NT < n4) {
+                const float4 d = v[j].get(K);
+                s += (d.x + d.y) + (d.z + d.w);
+            }
+        }
         s = block_sum<NT>(s, red[0]);
         // every thread has its values in registers: refill this buffer with
         // the segment GNS_NBUF ahead
@@ -494,7 +532,8 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             if (tid + j * NT < n4) {
-                const float a = v[j].x - mloc, c = v[j].y - mloc, d = v[j].z - mloc, e = v[j].w - mloc;
+                const float4 dv = v[j].get(K);
+                const float a = dv.x - mloc, c = dv.y - mloc, d = dv.z - mloc, e = dv.w - mloc;
                 q += (a * a + c * c) + (d * d + e * e);
             }
         }
@@ -527,29 +566,45 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
         const int64_t cbase = (r % p.G) * p.M;
         T *yr = y + r * p.seg_len;
         auto lrelu = [slope](float t) { return ACT ? (t > 0.f ? t : slope * t) : t; };
+        uint32_t cj = c0, rj = r0; // channel of vector j within the segment, and the remainder
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int i = tid + j * NT;
             if (i < n4) {
                 const int64_t e = 4 * (lo + i);
+                const float4 dv = v[j].get(K);
                 float4 o;
                 if constexpr (MODE == AFF_CHAN) {
-                    const int64_t c = cbase + coff[j];
+                    const int64_t c = cbase + cj;
                     const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
                     const float a = sc * rstd * gv, cc = fmaf(-mean_d, a, sc * bv);
-                    o = make_float4(lrelu(fmaf(v[j].x, a, cc)), lrelu(fmaf(v[j].y, a, cc)),
-                                    lrelu(fmaf(v[j].z, a, cc)), lrelu(fmaf(v[j].w, a, cc)));
+                    o = make_float4(lrelu(fmaf(dv.x, a, cc)), lrelu(fmaf(dv.y, a, cc)), lrelu(fmaf(dv.z, a, cc)),
+                                    lrelu(fmaf(dv.w, a, cc)));
                 } else {
                     float4 g, bb;
                     seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb);
                     const float ax = sc * rstd * g.x, ay = sc * rstd * g.y;
                     const float az = sc * rstd * g.z, aw = sc * rstd * g.w;
-                    o = make_float4(lrelu(fmaf(v[j].x, ax, fmaf(-mean_d, ax, sc * bb.x))),
-                                    lrelu(fmaf(v[j].y, ay, fmaf(-mean_d, ay, sc * bb.y))),
-                                    lrelu(fmaf(v[j].z, az, fmaf(-mean_d, az, sc * bb.z))),
-                                    lrelu(fmaf(v[j].w, aw, fmaf(-mean_d, aw, sc * bb.w))));
+                    o = make_float4(lrelu(fmaf(dv.x, ax, fmaf(-mean_d, ax, sc * bb.x))),
+                                    lrelu(fmaf(dv.y, ay, fmaf(-mean_d, ay, sc * bb.y))),
+                                    lrelu(fmaf(dv.z, az, fmaf(-mean_d, az, sc * bb.z))),
+                                    lrelu(fmaf(dv.w, aw, fmaf(-mean_d, aw, sc * bb.w))));
                 }
                 Io<T>::st4_stream(yr + e, o, pol_stream);
+            }
+            if constexpr (MODE == AFF_CHAN) {
+                // S % 4 == 0: a step of 4 * NT elements crosses at most one
+                // channel boundary when S >= 4 * NT; otherwise divide
+                if (S32 >= 4u * NT) {
+                    rj += 4u * NT;
+                    if (rj >= S32) {
+                        rj -= S32;
+                        ++cj;
+                    }
+                } else {
+                    const uint32_t ej = e0 + 4u * NT * static_cast<uint32_t>(j + 1);
+                    cj = ej / S32;
+                }
             }
         }
     }
@@ -885,6 +940,13 @@ namespace {
 // Streamed variants: 256 threads, 4 or 8 vectors a thread.
 constexpr int GNS_STREAM_NT = 256;
 
+// Vectors a CTA slice of the streamed kernel holds: bf16 keeps its values
+// packed, so twice as many.
+constexpr int stream_cap(bool bf16)
+{
+    return bf16 ? 4096 : 2048;
+}
+
 template <typename T, int MODE, bool ACT>
 RegKernel stream_kernel_for(int per, int *idx)
 {
@@ -895,6 +957,12 @@ RegKernel stream_kernel_for(int per, int *idx)
     if (per <= 2048) {
         *idx = 1;
         return gns_stream_kernel<T, GNS_STREAM_NT, 8, MODE, ACT>;
+    }
+    if constexpr (sizeof(T) == 2) {
+        if (per <= 4096) {
+            *idx = 2;
+            return gns_stream_kernel<T, GNS_STREAM_NT, 16, MODE, ACT>;
+        }
     }
     *idx = -1;
     return nullptr;
@@ -914,7 +982,7 @@ RegKernel stream_kernel_t(int per, int mode, bool act, int *idx)
     }
 }
 
-constexpr int GNS_STREAM_VARIANTS = 8; // 2 CTA shapes x (3 GroupNorm channel maps + LayerNorm)
+constexpr int GNS_STREAM_VARIANTS = 12; // 3 CTA shapes x (3 GroupNorm channel maps + LayerNorm)
 std::atomic<int> g_stream_active[GNS_DEVICES][2][GNS_STREAM_VARIANTS][5];
 std::once_flag g_stream_init;
 
@@ -940,7 +1008,7 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool 
     if (cluster < 1 || cluster > GNS_MAX_CLUSTER || (cluster & (cluster - 1)) != 0)
         return cudaErrorInvalidValue;
     const int64_t per = stream_per(seg_len, cluster);
-    if (per > 2048)
+    if (per > stream_cap(bf16))
         return cudaErrorInvalidValue;
     int idx = 0, dev = 0;
     const int mode = affine_mode(S);
@@ -948,7 +1016,8 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool 
                              : stream_kernel_t<float>(static_cast<int>(per), mode, act, &idx);
     if (!k)
         return cudaErrorInvalidValue;
-    idx += 2 * (act ? mode : 3);
+    const int shape = idx;
+    idx += 3 * (act ? mode : 3);
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
@@ -960,9 +1029,10 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool 
                         v.store(-1);
     });
     // occupancy depends on the dynamic shared memory, i.e. on per: cache only
-    // the full-slice case (per of 1024 or 2048), query the others
+    // the full-slice case (per of 1024, 2048 or 4096), query the others
     const size_t smem = stream_smem(per, bf16);
-    const bool cacheable = per == 1024 || per == 2048;
+    const int shape_per = 1024 << shape;
+    const bool cacheable = per == shape_per;
     std::atomic<int> *slot = cacheable && dev >= 0 && dev < GNS_DEVICES
                                  ? &g_stream_active[dev][bf16 ? 1 : 0][idx][log2_cluster(cluster)]
                                  : nullptr;
@@ -974,7 +1044,7 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool 
         }
     }
     // the attribute covers the variant's largest slice, so any launch of it fits
-    const size_t smem_max = stream_smem(idx % 2 == 0 ? 1024 : 2048, bf16);
+    const size_t smem_max = stream_smem(shape_per, bf16);
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
     if (e == cudaSuccess && cluster > 8)
         e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -997,6 +1067,11 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool 
     if (e == cudaSuccess && slot)
         slot->store(*clusters);
     return e;
+}
+
+int64_t gns_stream_capacity4(bool bf16)
+{
+    return stream_cap(bf16);
 }
 
 cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int cluster, cudaStream_t stream)

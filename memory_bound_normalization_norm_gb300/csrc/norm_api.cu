@@ -27,10 +27,13 @@ constexpr int64_t kPersistentMinRowLen = int64_t(1) << 20;
 // fractions of the copy peak): rows of 4,096 run best on the row kernel
 // (fp32 0.84 vs 0.82 streamed, bf16 0.61 vs 0.49), rows of 16,384 to
 // 131,072 on the streamed kernel (fp32 0.74 to 0.70 vs 0.64 on the row
-// kernel and 0.52 on the two-kernel path; bf16 0.47 to 0.38 vs 0.43 to 0.37
+// kernel and 0.52 on the two-kernel path; bf16 0.57 to 0.48 vs 0.44 to 0.38
 // on the two-kernel path).
 constexpr int64_t kLnStream = 4;
 constexpr int64_t kLnRowsMaxAuto = 8192;
+// Longest row the automatic choice gives the cluster kernel: bf16 rows of
+// 262,144 (which it can hold) measured faster on the two-kernel path.
+constexpr int64_t kLnStreamMaxAuto = 131072;
 
 struct DeviceState {
     bool init = false;
@@ -249,6 +252,19 @@ int gn_auto_cluster(int64_t L4)
     return 0;
 }
 
+// Smallest cluster whose streamed-kernel slices (an even number of vectors)
+// hold at most cap vectors each; 0 if none of 1..16 does.
+int stream_auto_cluster(int64_t L4, int64_t cap)
+{
+    for (int cl = 1; cl <= 16; cl <<= 1) {
+        int64_t per = (L4 + cl - 1) / cl;
+        per = (per + 1) & ~int64_t(1);
+        if (per <= cap)
+            return cl;
+    }
+    return 0;
+}
+
 // Partials of the split path: R * P triples; P as the LayerNorm split path.
 void plan_gn_split(int64_t R, int64_t L, bool vec4, const DeviceState &d, GnPlan *pl)
 {
@@ -412,12 +428,9 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     // activation): rows of up to 131,072 elements, read once.
     int ln_cluster = 0;
     if (vec4 && aligned(x, 16) && (bf16 ? (row_len & 7) == 0 : true)) {
-        const int cl = gn_auto_cluster(row_len / 4);
-        int64_t per = cl ? (row_len / 4 + cl - 1) / cl : 0;
-        per = (per + 1) & ~int64_t(1);
+        const int cl = stream_auto_cluster(row_len / 4, normk::gns_stream_capacity4(bf16));
         int active = 0;
-        if (cl && per <= 2048 && normk::gns_stream_max_clusters(row_len, 1, bf16, false, cl, &active) == cudaSuccess &&
-            active >= 1)
+        if (cl && normk::gns_stream_max_clusters(row_len, 1, bf16, false, cl, &active) == cudaSuccess && active >= 1)
             ln_cluster = cl;
         else
             cudaGetLastError();
@@ -426,7 +439,7 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
         return NORM_ERR_UNSUPPORTED;
     const bool ln_stream =
         ln_cluster && (path_opt == kLnStream ||
-                       (path_opt == 0 && row_len > kLnRowsMaxAuto && row_len < kPersistentMinRowLen));
+                       (path_opt == 0 && row_len > kLnRowsMaxAuto && row_len <= kLnStreamMaxAuto));
     const bool row_kernel_fits = vec4 && row_len <= normk::ln_rows_max_row_len();
     const bool row_kernel = !ln_stream && row_kernel_fits &&
                             (path_opt == 3 || (path_opt == 0 && row_len < kPersistentMinRowLen));
@@ -618,15 +631,23 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
             cluster = 0;
         }
     }
-    // Streamed form of the register path: 16-byte aligned x rows and slices.
+    // Streamed form of the register path: 16-byte aligned x rows and slices,
+    // its own cluster size (bf16 slices hold twice as many vectors).
     bool stream_ok = false;
     int64_t stream_slice = 0;
-    if (cluster && aligned(x, 16) && (bf16 ? (L & 7) == 0 : true)) {
-        stream_slice = (L / 4 + cluster - 1) / cluster;
-        stream_slice = (stream_slice + 1) & ~int64_t(1);
-        int active = 0;
-        stream_ok = stream_slice <= 2048 &&
-                    normk::gns_stream_max_clusters(L, S, bf16, true, cluster, &active) == cudaSuccess && active >= 1;
+    int stream_cl = 0;
+    if (vec4 && aligned(x, 16) && (bf16 ? (L & 7) == 0 : true)) {
+        const int64_t forced = g_opt_gn_cluster.load();
+        const int64_t cap = normk::gns_stream_capacity4(bf16);
+        stream_cl = forced ? static_cast<int>(forced) : stream_auto_cluster(L / 4, cap);
+        if (stream_cl) {
+            stream_slice = (L / 4 + stream_cl - 1) / stream_cl;
+            stream_slice = (stream_slice + 1) & ~int64_t(1);
+            int active = 0;
+            stream_ok = stream_slice <= cap &&
+                        normk::gns_stream_max_clusters(L, S, bf16, true, stream_cl, &active) == cudaSuccess &&
+                        active >= 1;
+        }
         if (!stream_ok)
             cudaGetLastError();
     }
@@ -665,7 +686,7 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     p.err = d->err;
 
     if (pl.path == kGnStream) {
-        e = normk::gns_stream_launch(p, bf16, true, cluster, stream);
+        e = normk::gns_stream_launch(p, bf16, true, stream_cl, stream);
     } else if (pl.path == kGnReg) {
         e = normk::gns_reg_launch(p, bf16, cluster, stream);
     } else if (pl.path == kGnWarp) {

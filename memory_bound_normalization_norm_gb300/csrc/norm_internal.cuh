@@ -619,14 +619,16 @@ int64_t gns_reg_capacity4(int cluster);
 // Clusters that can be co-resident (0 if the cluster size cannot launch).
 cudaError_t gns_reg_max_clusters(int64_t seg_len, int64_t S, bool bf16, int cluster, int *clusters);
 cudaError_t gns_reg_launch(const GnSegParams &p, bool bf16, int cluster, cudaStream_t stream);
-// Streamed register path: persistent clusters, each CTA's next slices arrive
-// by bulk copy into two shared-memory buffers.  Needs L % 4 == 0 (L % 8 for
-// bf16), 16-byte aligned x, 4-element aligned y/gamma/beta, and a slice of
-// 2..2048 vectors.
+// Streamed register path: persistent clusters, each CTA's next slice arrives
+// by bulk copy into shared memory.  Needs L % 4 == 0 (L % 8 for bf16),
+// 16-byte aligned x, 4-element aligned y/gamma/beta, and a slice of at most
+// gns_stream_capacity4() vectors.
 // act: GroupNorm's LeakyReLU x2 epilogue; without it the kernel is
 // LayerNorm over rows of seg_len with per-element gamma/beta (G = 1, M = L,
 // S = 1).
 cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool act, int cluster, int *clusters);
+// Largest CTA slice (4-element vectors) of the streamed kernel.
+int64_t gns_stream_capacity4(bool bf16);
 cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int cluster, cudaStream_t stream);
 // Apply kernel of the split path (after ln_split_stats_launch on the same
 // segments); vec4 as for the LayerNorm split path.

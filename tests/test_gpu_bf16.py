@@ -88,6 +88,7 @@ def run_ln(ng, x, g, b, rows, L, path=0, offset=0, inplace=False):
 @pytest.mark.parametrize("rows,L,path", [
     (3, 12, 3), (64, 4096, 3), (9, 16384, 3), (5, 1000, 3),   # row kernel
     (64, 4096, 4), (5, 20000, 4), (2, 131072, 4), (3, 65544, 4),  # streamed cluster kernel
+    (2, 262144, 4), (3, 32768, 0),                                # bf16 slices of 4,096 packed vectors
     (2, 16388, 2), (3, 4096, 2), (2, 1 << 20, 0),             # two-kernel path, vector form
     (3, 1001, 0),                                             # two-kernel path, scalar form
 ])
@@ -180,6 +181,8 @@ def test_bf16_entry_points_check_dtype(ng):
     (64, 64, 1024, 16, 4, 1),     # streamed, one CTA per group, many groups per CTA
     (2, 64, 1024, 4, 4, 16),      # streamed over clusters of 16
     (2, 16, 2046, 4, 4, 2),       # streamed, channels change inside a vector (L = 8184)
+    (2, 64, 1024, 4, 4, 1),       # streamed, one CTA holding 4,096 packed vectors
+    (1, 32, 16384, 2, 0, 0),      # L = 262,144: 16 CTAs of 4,096 packed vectors
     (1, 128, 65536, 32, 0, 0),    # two-kernel path, vector form
     (3, 9, 5, 3, 2, 0),           # two-kernel path, scalar form
     (3, 9, 5, 3, 0, 0),           # warp path
