@@ -39,6 +39,14 @@ def test_channels(ng, C, B, S):
     assert_parity(run_rms(ng, x, B, C, S), oracle.rms_channel(x, B, C, S), f"RMS B={B} C={C} S={S}")
 
 
+@pytest.mark.parametrize("B,C,S", [(2, 33, 40000), (3, 64, 30000), (1, 17, 70001)])
+def test_more_positions_than_one_wave(ng, B, C, S):
+    # 30,000 to 80,000 positions: several position blocks per batch entry, with
+    # exact and predicated channel counts
+    x = normgen.normal(B * C * S, seed=B + C + S, tensor_id=0)
+    assert_parity(run_rms(ng, x, B, C, S), oracle.rms_channel(x, B, C, S), f"RMS B={B} C={C} S={S}")
+
+
 def test_in_place_and_misaligned(ng):
     B, C, S = 3, 64, 1023
     x = normgen.normal(B * C * S, seed=5)
