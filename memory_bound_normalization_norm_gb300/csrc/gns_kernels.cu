@@ -196,13 +196,20 @@ __host__ __device__ constexpr int affine_mode(int64_t S)
 }
 
 // gamma/beta of elements e .. e+3 of a segment whose first channel is cbase.
+// cache: consecutive channels are read through L1 (worth it where every SM's
+// CTAs read few distinct parts of gamma/beta), else with an L2 policy only.
 template <typename T, int MODE>
 __device__ __forceinline__ void seg_affine4(const T *gm, const T *bt, int64_t cbase, int64_t e, int64_t S,
-                                            bool narrow, uint64_t pol, float4 &g, float4 &b)
+                                            bool narrow, uint64_t pol, float4 &g, float4 &b, bool cache = false)
 {
     if (MODE == AFF_ROW) {
-        g = gm ? Io<T>::ld4_ro(gm + cbase + e, pol) : make_float4(1.f, 1.f, 1.f, 1.f);
-        b = bt ? Io<T>::ld4_ro(bt + cbase + e, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (cache) {
+            g = gm ? Io<T>::ld4_param(gm + cbase + e) : make_float4(1.f, 1.f, 1.f, 1.f);
+            b = bt ? Io<T>::ld4_param(bt + cbase + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            g = gm ? Io<T>::ld4_ro(gm + cbase + e, pol) : make_float4(1.f, 1.f, 1.f, 1.f);
+            b = bt ? Io<T>::ld4_ro(bt + cbase + e, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     } else if (MODE == AFF_CHAN) {
         const int64_t c = cbase + seg_div(e, S, narrow);
         const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
@@ -582,7 +589,7 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
                                     lrelu(fmaf(dv.w, a, cc)));
                 } else {
                     float4 g, bb;
-                    seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb);
+                    seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb, p.cache_gb != 0);
                     const float ax = sc * rstd * g.x, ay = sc * rstd * g.y;
                     const float az = sc * rstd * g.z, aw = sc * rstd * g.w;
                     o = make_float4(lrelu(fmaf(dv.x, ax, fmaf(-mean_d, ax, sc * bb.x))),

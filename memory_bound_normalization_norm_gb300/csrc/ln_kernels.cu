@@ -639,8 +639,8 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
                     g = gk[k];
                     b = bk[k];
                 } else {
-                    g = gm ? Io<T>::ld4_ro(gm + 4 * i, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
-                    b = bt ? Io<T>::ld4_ro(bt + 4 * i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    g = gm ? Io<T>::ld4_param(gm + 4 * i) : make_float4(1.f, 1.f, 1.f, 1.f);
+                    b = bt ? Io<T>::ld4_param(bt + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
                 Io<T>::st4_stream(yr + 4 * i, ln_apply4(v[k], rm, g, b), pol_stream);
             }

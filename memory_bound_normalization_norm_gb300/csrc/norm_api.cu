@@ -34,6 +34,12 @@ constexpr int64_t kLnRowsMaxAuto = 8192;
 // Longest row the automatic choice gives the cluster kernel: bf16 rows of
 // 262,144 (which it can hold) measured faster on the two-kernel path.
 constexpr int64_t kLnStreamMaxAuto = 131072;
+// Largest gamma (and beta) in bytes for which the cluster kernel reads them
+// through L1: the CTAs on one SM belong to different clusters and may each
+// hold a different part of gamma/beta.  Measured: L1 reads help up to rows of
+// 32,768 fp32 / 65,536 bf16 (fp32 rows of 16,384: 0.74 -> 0.80 of peak) and
+// cost a little beyond (fp32 rows of 131,072: 0.70 -> 0.67).
+constexpr size_t kGbL1Bytes = size_t(128) << 10;
 
 struct DeviceState {
     bool init = false;
@@ -524,6 +530,7 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
         q.eps = eps;
         q.timeout_ns = p.timeout_ns;
         q.err = d->err;
+        q.cache_gb = static_cast<size_t>(row_len) * esz <= kGbL1Bytes;
         e = normk::gns_stream_launch(q, bf16, false, ln_cluster, stream);
     } else if (row_kernel) {
         e = normk::ln_rows_launch(p, bf16, d->sm_count, stream);
@@ -684,6 +691,7 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     p.slope = negative_slope;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
     p.err = d->err;
+    p.cache_gb = S == 1 && static_cast<size_t>(L) * esz <= kGbL1Bytes;
 
     if (pl.path == kGnStream) {
         e = normk::gns_stream_launch(p, bf16, true, stream_cl, stream);

@@ -62,6 +62,15 @@ __device__ __forceinline__ float ld_stream_f1(const float *p, uint64_t pol)
 
 // Read-only (non-coherent path) 128-bit load with an L2 policy: for gamma/beta,
 // which the kernels never write.
+// A parameter vector (gamma/beta) that every row reads again: read-only and
+// L1-allocating, so the rows a CTA walks find it in L1.
+__device__ __forceinline__ float4 ld_param_f4(const float4 *p)
+{
+    float4 v;
+    asm("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_ro_f4(const float4 *p, uint64_t pol)
 {
     float4 v;
@@ -257,6 +266,10 @@ struct Io<float> {
     {
         return ld_ro_f4(reinterpret_cast<const float4 *>(p), pol);
     }
+    static __device__ __forceinline__ float4 ld4_param(const float *p)
+    {
+        return ld_param_f4(reinterpret_cast<const float4 *>(p));
+    }
     static __device__ __forceinline__ void st4_stream(float *p, float4 v, uint64_t pol)
     {
         st_stream_f4(reinterpret_cast<float4 *>(p), v, pol);
@@ -296,6 +309,12 @@ struct Io<__nv_bfloat16> {
         asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
             : "=r"(a), "=r"(b)
             : "l"(p), "l"(pol));
+        return unpack(a, b);
+    }
+    static __device__ __forceinline__ float4 ld4_param(const __nv_bfloat16 *p)
+    {
+        uint32_t a, b;
+        asm("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "l"(p));
         return unpack(a, b);
     }
     static __device__ __forceinline__ void st4_stream(__nv_bfloat16 *p, float4 v, uint64_t pol)
@@ -609,6 +628,7 @@ struct GnSegParams {
     int64_t chunk;      // split path: elements per CTA
     int parts;          // split path: CTAs per segment; register paths: cluster size
     int per4;           // streamed path: vectors per CTA slice
+    int cache_gb;       // streamed path, one channel per element: read gamma/beta through L1
     uint64_t timeout_ns; // streamed path: longest mbarrier wait
     unsigned *err;       // streamed path: the device error word
 };
