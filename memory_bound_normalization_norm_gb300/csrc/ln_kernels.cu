@@ -844,8 +844,14 @@ cudaError_t ln_rows_launch_t(const LnParams &p, int sm_count, cudaStream_t strea
 // many rows (of half the bytes) are in flight per SM.
 cudaError_t ln_rows_launch(const LnParams &p, bool bf16, int sm_count, cudaStream_t stream)
 {
-    if (!bf16)
+    if (!bf16) {
+        // fp32 rows of 2,049 to 8,192 elements: 128-thread CTAs, gamma/beta
+        // through L1, so 8 rows are in flight per SM instead of 3 (rows of
+        // 4,096: 0.83 -> 0.93 of the measured peak)
+        if (p.row_len > int64_t(LR_T / 2) * 4 * 4 && p.row_len <= int64_t(LR_T / 2) * 16 * 4)
+            return ln_rows_launch_t<float, LR_T / 2>(p, sm_count, stream);
         return ln_rows_launch_t<float, LR_T>(p, sm_count, stream);
+    }
     if (p.row_len <= int64_t(LR_T / 2) * 16 * 4)
         return ln_rows_launch_t<__nv_bfloat16, LR_T / 2>(p, sm_count, stream);
     return ln_rows_launch_t<__nv_bfloat16, LR_T>(p, sm_count, stream);
