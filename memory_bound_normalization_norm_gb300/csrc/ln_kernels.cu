@@ -839,22 +839,27 @@ cudaError_t ln_rows_launch_t(const LnParams &p, int sm_count, cudaStream_t strea
     return cudaGetLastError();
 }
 
-// bf16 rows up to 8,192 elements use 128-thread CTAs: a row then holds as
-// many registers per thread as an fp32 row in 256 threads, and twice as
-// many rows (of half the bytes) are in flight per SM.
+// CTA size for a row of L4 vectors: the smallest of 32..256 threads that
+// holds it with 8 vectors a thread (16 at 256 threads), gamma/beta through
+// L1.  Small CTAs keep many rows in flight per SM: the row lives in
+// registers, so rows in flight are what hides the loads' latency.
+template <typename T>
+cudaError_t ln_rows_launch_sized(const LnParams &p, int sm_count, cudaStream_t stream)
+{
+    const int64_t L4 = p.row_len / 4;
+    if (L4 <= 32 * 8)
+        return ln_rows_launch_t<T, 32>(p, sm_count, stream);
+    if (L4 <= 64 * 8)
+        return ln_rows_launch_t<T, 64>(p, sm_count, stream);
+    if (L4 <= 128 * 8)
+        return ln_rows_launch_t<T, 128>(p, sm_count, stream);
+    return ln_rows_launch_t<T, LR_T>(p, sm_count, stream);
+}
+
 cudaError_t ln_rows_launch(const LnParams &p, bool bf16, int sm_count, cudaStream_t stream)
 {
-    if (!bf16) {
-        // fp32 rows of 2,049 to 8,192 elements: 128-thread CTAs, gamma/beta
-        // through L1, so 8 rows are in flight per SM instead of 3 (rows of
-        // 4,096: 0.83 -> 0.93 of the measured peak)
-        if (p.row_len > int64_t(LR_T / 2) * 4 * 4 && p.row_len <= int64_t(LR_T / 2) * 16 * 4)
-            return ln_rows_launch_t<float, LR_T / 2>(p, sm_count, stream);
-        return ln_rows_launch_t<float, LR_T>(p, sm_count, stream);
-    }
-    if (p.row_len <= int64_t(LR_T / 2) * 16 * 4)
-        return ln_rows_launch_t<__nv_bfloat16, LR_T / 2>(p, sm_count, stream);
-    return ln_rows_launch_t<__nv_bfloat16, LR_T>(p, sm_count, stream);
+    return bf16 ? ln_rows_launch_sized<__nv_bfloat16>(p, sm_count, stream)
+                : ln_rows_launch_sized<float>(p, sm_count, stream);
 }
 
 template <typename T>
