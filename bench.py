@@ -184,7 +184,7 @@ def device_tensor(a, cfg, dev):
 def main_kernel_name(cfg) -> str:
     if cfg["op"] == "ln":
         L, bf16 = cfg["L"], bool(cfg.get("bf16"))
-        if L <= 8192:
+        if L <= (8192 if bf16 else 16384):
             return "ln_rows_kernel"
         if L <= 131072 and L % (8 if bf16 else 4) == 0:
             return "gns_stream_kernel"
@@ -208,7 +208,7 @@ def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
     bf16 = bool(cfg.get("bf16"))
     if op == "ln":
         rows, L = cfg["rows"], cfg["L"]
-        one_launch = L % 4 == 0 and (L <= 8192 or (L <= 131072 and L % (8 if bf16 else 4) == 0) or
+        one_launch = L % 4 == 0 and (L <= (8192 if bf16 else 16384) or (L <= 131072 and L % (8 if bf16 else 4) == 0) or
                                      (not bf16 and (1 << 20) <= L <= ng.norm_layer_max_resident_row_len()))
         fn = ng.norm_layer_fwd_bf16 if bf16 else ng.norm_layer_fwd
         return (lambda: fn(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if one_launch else 2)

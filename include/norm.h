@@ -84,10 +84,10 @@ typedef enum {
  *
  * Paths, all with a row length that is a multiple of 4 and 16-byte aligned
  * x/y/gamma/beta unless stated:
- *   - rows of at most 8,192 elements: one launch, one CTA per row at a
- *     time with the row in registers; x is read from HBM once and the
- *     workspace is not used;
- *   - rows of 8,193 to 131,072 elements: one launch of the thread-block
+ *   - rows of at most 8,192 elements (16,384 for fp32): one launch, one
+ *     CTA per row at a time, sized to the row, with the row in registers;
+ *     x is read from HBM once and the workspace is not used;
+ *   - longer rows of up to 131,072 elements: one launch of the thread-block
  *     cluster kernel that GroupNorm over NCHW tensors uses (one group per
  *     row): each row is split over one CTA or a cluster of up to 16 CTAs,
  *     each CTA's next slices arrive by bulk copy into shared memory, and

@@ -812,7 +812,7 @@ cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cuda
 
 int64_t ln_rows_max_row_len()
 {
-    return int64_t(LR_T) * 16 * 4;
+    return int64_t(512) * 8 * 4;
 }
 
 template <typename T, int NT>
@@ -839,9 +839,8 @@ cudaError_t ln_rows_launch_t(const LnParams &p, int sm_count, cudaStream_t strea
     return cudaGetLastError();
 }
 
-// CTA size for a row of L4 vectors: the smallest of 32..256 threads that
-// holds it with 8 vectors a thread (16 at 256 threads), gamma/beta through
-// L1.  Small CTAs keep many rows in flight per SM: the row lives in
+// CTA size for a row of L4 vectors: the smallest of 32..512 threads that
+// holds it with 8 vectors a thread, gamma/beta through L1.  Small CTAs keep many rows in flight per SM: the row lives in
 // registers, so rows in flight are what hides the loads' latency.
 template <typename T>
 cudaError_t ln_rows_launch_sized(const LnParams &p, int sm_count, cudaStream_t stream)
@@ -853,7 +852,9 @@ cudaError_t ln_rows_launch_sized(const LnParams &p, int sm_count, cudaStream_t s
         return ln_rows_launch_t<T, 64>(p, sm_count, stream);
     if (L4 <= 128 * 8)
         return ln_rows_launch_t<T, 128>(p, sm_count, stream);
-    return ln_rows_launch_t<T, LR_T>(p, sm_count, stream);
+    if (L4 <= 256 * 8)
+        return ln_rows_launch_t<T, 256>(p, sm_count, stream);
+    return ln_rows_launch_t<T, 512>(p, sm_count, stream);
 }
 
 cudaError_t ln_rows_launch(const LnParams &p, bool bf16, int sm_count, cudaStream_t stream)

@@ -24,13 +24,17 @@ constexpr size_t kWsHeader = sizeof(normk::LnSync);
 constexpr int64_t kPersistentMinRowLen = int64_t(1) << 20;
 // NORM_OPT_LN_PATH value of the streamed cluster kernel, and the longest
 // row the automatic choice gives the row kernel.  Measured on GB300 (GB/s
-// fractions of the copy peak): rows of 4,096 run best on the row kernel
-// (fp32 0.84 vs 0.82 streamed, bf16 0.61 vs 0.49), rows of 16,384 to
-// 131,072 on the streamed kernel (fp32 0.74 to 0.70 vs 0.64 on the row
-// kernel and 0.52 on the two-kernel path; bf16 0.57 to 0.48 vs 0.44 to 0.38
-// on the two-kernel path).
+// fractions of the copy peak): the row kernel, its CTA sized to the row,
+// runs rows of 256 to 8,192 at 0.88-0.93 (fp32) and 0.55-0.69 (bf16), ahead
+// of the cluster kernel (0.78 fp32, 0.55 bf16 at 8,192); rows of 16,384 to
+// 131,072 run best on the cluster kernel (fp32 0.79 to 0.70, bf16 0.58 to
+// 0.48, vs 0.52 and 0.43 to 0.37 on the two-kernel path), except fp32 rows
+// of 16,384 (below).
 constexpr int64_t kLnStream = 4;
 constexpr int64_t kLnRowsMaxAuto = 8192;
+// fp32 rows of 16,384 run a little faster on the row kernel's 512-thread form
+// (0.81 vs 0.79 on the cluster kernel); bf16 ones on the cluster kernel.
+constexpr int64_t kLnRowsMaxAutoF32 = 16384;
 // Longest row the automatic choice gives the cluster kernel: bf16 rows of
 // 262,144 (which it can hold) measured faster on the two-kernel path.
 constexpr int64_t kLnStreamMaxAuto = 131072;
@@ -443,9 +447,10 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     }
     if (path_opt == kLnStream && !ln_cluster)
         return NORM_ERR_UNSUPPORTED;
+    const int64_t rows_max_auto = bf16 ? kLnRowsMaxAuto : kLnRowsMaxAutoF32;
     const bool ln_stream =
         ln_cluster && (path_opt == kLnStream ||
-                       (path_opt == 0 && row_len > kLnRowsMaxAuto && row_len <= kLnStreamMaxAuto));
+                       (path_opt == 0 && row_len > rows_max_auto && row_len <= kLnStreamMaxAuto));
     const bool row_kernel_fits = vec4 && row_len <= normk::ln_rows_max_row_len();
     const bool row_kernel = !ln_stream && row_kernel_fits &&
                             (path_opt == 3 || (path_opt == 0 && row_len < kPersistentMinRowLen));
