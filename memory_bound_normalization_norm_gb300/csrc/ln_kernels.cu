@@ -606,29 +606,28 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
         // every thread reads the pivot before any thread of the CTA stores
         // (the block sums below are barriers), so y == x is safe
         const float K = Io<T>::ld1(xr);
+        // from here on v holds d = x - K (zero outside the row)
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
-            if (tid + k * NT < L4)
-                s += ((v[k].x - K) + (v[k].y - K)) + ((v[k].z - K) + (v[k].w - K));
+            if (tid + k * NT < L4) {
+                v[k] = make_float4(v[k].x - K, v[k].y - K, v[k].z - K, v[k].w - K);
+                s += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+            }
         }
         s = block_sum<NT>(s, red[0]);
-        Moments tot;
-        tot.n = Lf;
-        tot.mean = s / Lf;
-        tot.m2 = 0.f;
-        RowMean rm = finish_row(K, tot, p.eps);
+        const float mean_d = s / Lf;
         float q = 0.f;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             if (tid + k * NT < L4) {
-                const float a = (v[k].x - rm.hi) - rm.lo, b = (v[k].y - rm.hi) - rm.lo;
-                const float c = (v[k].z - rm.hi) - rm.lo, d = (v[k].w - rm.hi) - rm.lo;
+                const float a = v[k].x - mean_d, b = v[k].y - mean_d;
+                const float c = v[k].z - mean_d, d = v[k].w - mean_d;
                 q += (a * a + b * b) + (c * c + d * d);
             }
         }
         q = block_sum<NT>(q, red[1]);
-        rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        const float rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
         T *yr = y + r * p.row_len;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
@@ -642,7 +641,13 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
                     g = gm ? Io<T>::ld4_param(gm + 4 * i) : make_float4(1.f, 1.f, 1.f, 1.f);
                     b = bt ? Io<T>::ld4_param(bt + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                Io<T>::st4_stream(yr + 4 * i, ln_apply4(v[k], rm, g, b), pol_stream);
+                // y = (d - mean_d) * rstd * g + b = d * a + c
+                const float4 a = make_float4(rstd * g.x, rstd * g.y, rstd * g.z, rstd * g.w);
+                const float4 o = make_float4(fmaf(v[k].x, a.x, fmaf(-mean_d, a.x, b.x)),
+                                             fmaf(v[k].y, a.y, fmaf(-mean_d, a.y, b.y)),
+                                             fmaf(v[k].z, a.z, fmaf(-mean_d, a.z, b.z)),
+                                             fmaf(v[k].w, a.w, fmaf(-mean_d, a.w, b.w)));
+                Io<T>::st4_stream(yr + 4 * i, o, pol_stream);
             }
         }
     }
