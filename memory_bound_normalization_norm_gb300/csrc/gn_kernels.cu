@@ -11,7 +11,8 @@
 // shuffles (the group's values never leave registers), the epilogue is
 // applied in fp32 registers and the vector is stored once.  A CTA keeps its
 // columns' gamma/beta in registers and walks rows with two rows of x loads in
-// flight.  Every byte of x is read once and every byte of y written once.
+// flight, held as loaded (bf16 packed, two registers a vector) until their
+// turn.  Every byte of x is read once and every byte of y written once.
 #include "norm_internal.cuh"
 
 namespace normk {
@@ -29,6 +30,34 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
+// A prefetched 4-element vector as loaded: fp32 as a float4, bf16 packed
+// (two registers), widened when its row's turn comes.
+template <typename T>
+struct Raw4;
+
+template <>
+struct Raw4<float> {
+    using type = float4;
+    static __device__ __forceinline__ type load(const float *p, uint64_t pol) { return Io<float>::ld4_stream(p, pol); }
+    static __device__ __forceinline__ type zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    static __device__ __forceinline__ float4 get(const type &r) { return r; }
+};
+
+template <>
+struct Raw4<__nv_bfloat16> {
+    using type = uint2;
+    static __device__ __forceinline__ type load(const __nv_bfloat16 *p, uint64_t pol)
+    {
+        uint2 r;
+        asm("ld.global.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+            : "=r"(r.x), "=r"(r.y)
+            : "l"(p), "l"(pol));
+        return r;
+    }
+    static __device__ __forceinline__ type zero() { return make_uint2(0u, 0u); }
+    static __device__ __forceinline__ float4 get(const type &r) { return Io<__nv_bfloat16>::unpack(r.x, r.y); }
+};
+
 // grid: x = column blocks of GN_THREADS*U vectors, y = row walkers.
 // x, y: [N][C] of T; "vector" = 4 consecutive channels; C4 = C / 4.
 // A CTA owns a fixed block of GN_THREADS * U vectors of columns and walks
@@ -44,7 +73,9 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     const int col0 = blockIdx.x * (GN_THREADS * U) + threadIdx.x;
-    float4 g[U], b[U], cur[U], nxt[U], nx2[U];
+    using R = Raw4<T>;
+    float4 g[U], b[U];
+    typename R::type cur[U], nxt[U], nx2[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int c = col0 + u * GN_THREADS;
@@ -52,12 +83,12 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
         g[u] = (in && gamma) ? Io<T>::ld4_ro(gamma + 4 * c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
         b[u] = (in && beta) ? Io<T>::ld4_ro(beta + 4 * c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    auto load_row = [&](int64_t n, float4 *dst) {
+    auto load_row = [&](int64_t n, typename R::type *dst) {
         const T *xr = x + n * C4 * 4;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int c = col0 + u * GN_THREADS;
-            dst[u] = c < C4 ? Io<T>::ld4_stream(xr + 4 * c, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+            dst[u] = c < C4 ? R::load(xr + 4 * c, pol_stream) : R::zero();
         }
     };
     if (blockIdx.y < N)
@@ -80,8 +111,9 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
             const int c = col0 + u * GN_THREADS;
             // C4 is a multiple of TPG, so whole groups are in or out of range
             // together and every lane takes part in the shuffles.
-            const float mean = group_sum<TPG>((cur[u].x + cur[u].y) + (cur[u].z + cur[u].w)) * invM;
-            const float dx = cur[u].x - mean, dy = cur[u].y - mean, dz = cur[u].z - mean, dw = cur[u].w - mean;
+            const float4 cv = R::get(cur[u]);
+            const float mean = group_sum<TPG>((cv.x + cv.y) + (cv.z + cv.w)) * invM;
+            const float dx = cv.x - mean, dy = cv.y - mean, dz = cv.z - mean, dw = cv.w - mean;
             const float m2 = group_sum<TPG>((dx * dx + dy * dy) + (dz * dz + dw * dw));
             const float rstd = rsqrtf(fmaf(m2, invM, eps));
             if (c < C4) {
