@@ -134,7 +134,8 @@ def test_layer_norm_bf16_full_size(ng):
 
 # ------------------------------------------------------------------ RMSNorm
 
-@pytest.mark.parametrize("B,C,S", [(2, 64, 1024), (3, 1, 37), (2, 3, 129), (2, 128, 300), (2, 200, 65), (1, 48, 513)])
+@pytest.mark.parametrize("B,C,S", [(2, 64, 1024), (3, 1, 37), (2, 3, 129), (2, 128, 300), (2, 200, 65), (1, 48, 513),
+                                   (2, 32, 1000), (3, 16, 2), (2, 64, 40002)])
 def test_rms_bf16(ng, B, C, S):
     x = bf16_inputs(B * C * S, seed=B * C + S)
     want = oracle.rms_channel(x, B, C, S, f64=True)
@@ -160,6 +161,18 @@ def test_group_norm_bf16(ng, N, C, G):
     ng.norm_group_lrelu_x2_fwd_bf16(xb.t, gb.t, bb.t, yb.t, N, C, G, 1e-5, 0.01)
     assert ng.norm_last_error() == 0
     assert_bf16_parity(yb.values(), want, f"GN bf16 ({N},{C})/{G}")
+    assert yb.guards_intact()
+
+
+def test_rms_bf16_misaligned(ng):
+    # x and y 2-byte but not 4-byte aligned
+    B, C, S = 2, 64, 1024
+    x = bf16_inputs(B * C * S, seed=77)
+    want = oracle.rms_channel(x, B, C, S, f64=True)
+    xb, yb = BGuarded(B * C * S, x, offset=1), BGuarded(B * C * S, offset=1)
+    ng.norm_rms_channel_fwd_bf16(xb.t, yb.t, B, C, S, 1e-5)
+    assert ng.norm_last_error() == 0
+    assert_bf16_parity(yb.values(), want, "RMS bf16 misaligned")
     assert yb.guards_intact()
 
 
