@@ -37,6 +37,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -316,12 +317,21 @@ KERNEL_SOURCES = {"ln": ("ln_kernels.cu", "gns_kernels.cu", "norm_internal.cuh")
                   "rms": ("rms_kernels.cu", "norm_internal.cuh")}
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source with comments and blank-space runs removed: what the compiler sees of it
+    (string literals here hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(op: str) -> str:
+    """Hash of the code (not the comments) of the sources a workload's kernels are built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "memory_bound_normalization_norm_gb300", "csrc")
     for name in KERNEL_SOURCES[op]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -30,7 +30,11 @@
 //    every CTA the partials, merged with Chan's update in rank order.  A
 //    cluster barrier with release semantics would wait for the CTA's
 //    earlier y stores to drain (measured as the top stall, "membar"); the
-//    mbarrier exchange does not.  Every wait is bounded; see the kernel.
+//    mbarrier exchange does not.  bf16 slices stay packed in registers, so a
+//    CTA holds twice as many vectors.  Every wait is bounded; see the
+//    kernel.  Without the LeakyReLU x2 epilogue the same kernel is the
+//    LayerNorm of rows of up to 131,072 elements (one group per row,
+//    per-element gamma/beta).
 //  - split path (segments longer than a 16-CTA cluster holds, or unaligned
 //    vectors): the LayerNorm split path's statistics kernel writes one
 //    (n, mean, M2, pivot) partial per (segment, chunk), and the apply kernel
@@ -944,7 +948,7 @@ cudaError_t gns_reg_launch(const GnSegParams &p, bool bf16, int cluster, cudaStr
 
 namespace {
 
-// Streamed variants: 256 threads, 4 or 8 vectors a thread.
+// Streamed variants: 256 threads, 4 or 8 vectors a thread (16 for bf16).
 constexpr int GNS_STREAM_NT = 256;
 
 // Vectors a CTA slice of the streamed kernel holds: bf16 keeps its values

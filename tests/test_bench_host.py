@@ -99,3 +99,13 @@ def test_buffer_sets_keep_every_step_out_of_l2():
         assert n > 1 and n * 8 * bench.elements(cfg) >= 3 * l2
         assert (n - 1) * 8 * bench.elements(cfg) < 3 * l2
     assert "rotate through" in bench.l2_note(bench.CONFIGS["gn"], l2)
+
+
+def test_kernel_source_hash_ignores_comments():
+    import bench
+    a = "int f(int x) { return x + 1; } // add one\n/* block\n comment */ int g;"
+    b = "// header\nint   f(int x)\n{\n    return x + 1; /* inline */\n}\nint g;"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only("int f(int x) { return x + 2; }") != bench.code_only(a)
+    for op in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_source_hash(op)) == 16
