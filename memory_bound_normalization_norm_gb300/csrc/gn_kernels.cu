@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
 {
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
+    pdl_begin();
     const int col0 = blockIdx.x * (GN_THREADS * U) + threadIdx.x;
     using R = Raw4<T>;
     float4 g[U], b[U];
@@ -155,10 +156,9 @@ cudaError_t launch_vec(const void *x, const void *gamma, const void *beta, void 
     if (gy < 1)
         gy = 1;
     dim3 grid(gx, static_cast<unsigned>(gy));
-    gn_vec4_kernel<T, TPG, U><<<grid, GN_THREADS, 0, stream>>>(
-        static_cast<const T *>(x), static_cast<const T *>(gamma), static_cast<const T *>(beta), static_cast<T *>(y),
-        N, C4, 1.0f / static_cast<float>(M), eps, slope);
-    return cudaGetLastError();
+    return launch_pdl(gn_vec4_kernel<T, TPG, U>, grid, dim3(GN_THREADS), 0, stream, static_cast<const T *>(x),
+                      static_cast<const T *>(gamma), static_cast<const T *>(beta), static_cast<T *>(y), N, C4,
+                      1.0f / static_cast<float>(M), eps, slope);
 }
 
 } // namespace

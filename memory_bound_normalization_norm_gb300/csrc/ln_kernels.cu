@@ -573,6 +573,7 @@ constexpr int LR_T = 256;
 template <typename T, int NT, int V>
 __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
 {
+    pdl_begin();
     __shared__ float red[2][NT / 32];
     const int tid = threadIdx.x;
     const int64_t L4 = p.row_len >> 2; // 4-element vectors per row
@@ -665,6 +666,7 @@ constexpr int LS_T = 256;
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(LS_T) ln_split_stats_kernel(LnParams p)
 {
+    pdl_begin();
     __shared__ Moments red[LS_T / 32];
     const int P = p.parts;
     const T *x = static_cast<const T *>(p.x);
@@ -724,6 +726,7 @@ __global__ void __launch_bounds__(LS_T) ln_split_stats_kernel(LnParams p)
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(LS_T) ln_split_apply_kernel(LnParams p)
 {
+    pdl_begin();
     __shared__ RowMean row_mean;
     const int P = p.parts;
     const T *x = static_cast<const T *>(p.x);
@@ -830,18 +833,16 @@ cudaError_t ln_rows_launch_t(const LnParams &p, int sm_count, cudaStream_t strea
         grid = cap;
     const dim3 g(static_cast<unsigned>(grid));
     if (L4 <= NT)
-        ln_rows_kernel<T, NT, 1><<<g, NT, 0, stream>>>(p);
-    else if (L4 <= 2 * NT)
-        ln_rows_kernel<T, NT, 2><<<g, NT, 0, stream>>>(p);
-    else if (L4 <= 4 * NT)
-        ln_rows_kernel<T, NT, 4><<<g, NT, 0, stream>>>(p);
-    else if (L4 <= 8 * NT)
-        ln_rows_kernel<T, NT, 8><<<g, NT, 0, stream>>>(p);
-    else if (L4 <= 16 * NT)
-        ln_rows_kernel<T, NT, 16><<<g, NT, 0, stream>>>(p);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_pdl(ln_rows_kernel<T, NT, 1>, g, dim3(NT), 0, stream, p);
+    if (L4 <= 2 * NT)
+        return launch_pdl(ln_rows_kernel<T, NT, 2>, g, dim3(NT), 0, stream, p);
+    if (L4 <= 4 * NT)
+        return launch_pdl(ln_rows_kernel<T, NT, 4>, g, dim3(NT), 0, stream, p);
+    if (L4 <= 8 * NT)
+        return launch_pdl(ln_rows_kernel<T, NT, 8>, g, dim3(NT), 0, stream, p);
+    if (L4 <= 16 * NT)
+        return launch_pdl(ln_rows_kernel<T, NT, 16>, g, dim3(NT), 0, stream, p);
+    return cudaErrorInvalidValue;
 }
 
 // CTA size for a row of L4 vectors: the smallest of 32..512 threads that
@@ -872,14 +873,17 @@ template <typename T>
 cudaError_t ln_split_launch_t(const LnParams &p, bool vec4, cudaStream_t stream)
 {
     dim3 grid(static_cast<unsigned>(p.parts), static_cast<unsigned>(p.rows < 65535 ? p.rows : 65535));
+    cudaError_t e;
     if (vec4) {
-        ln_split_stats_kernel<T, true><<<grid, LS_T, 0, stream>>>(p);
-        ln_split_apply_kernel<T, true><<<grid, LS_T, 0, stream>>>(p);
+        e = launch_pdl(ln_split_stats_kernel<T, true>, grid, dim3(LS_T), 0, stream, p);
+        if (e == cudaSuccess)
+            e = launch_pdl(ln_split_apply_kernel<T, true>, grid, dim3(LS_T), 0, stream, p);
     } else {
-        ln_split_stats_kernel<T, false><<<grid, LS_T, 0, stream>>>(p);
-        ln_split_apply_kernel<T, false><<<grid, LS_T, 0, stream>>>(p);
+        e = launch_pdl(ln_split_stats_kernel<T, false>, grid, dim3(LS_T), 0, stream, p);
+        if (e == cudaSuccess)
+            e = launch_pdl(ln_split_apply_kernel<T, false>, grid, dim3(LS_T), 0, stream, p);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t ln_split_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_t stream)
@@ -890,18 +894,11 @@ cudaError_t ln_split_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_
 cudaError_t ln_split_stats_launch(const LnParams &p, bool bf16, bool vec4, cudaStream_t stream)
 {
     dim3 grid(static_cast<unsigned>(p.parts), static_cast<unsigned>(p.rows < 65535 ? p.rows : 65535));
-    if (bf16) {
-        if (vec4)
-            ln_split_stats_kernel<__nv_bfloat16, true><<<grid, LS_T, 0, stream>>>(p);
-        else
-            ln_split_stats_kernel<__nv_bfloat16, false><<<grid, LS_T, 0, stream>>>(p);
-    } else {
-        if (vec4)
-            ln_split_stats_kernel<float, true><<<grid, LS_T, 0, stream>>>(p);
-        else
-            ln_split_stats_kernel<float, false><<<grid, LS_T, 0, stream>>>(p);
-    }
-    return cudaGetLastError();
+    if (bf16)
+        return vec4 ? launch_pdl(ln_split_stats_kernel<__nv_bfloat16, true>, grid, dim3(LS_T), 0, stream, p)
+                    : launch_pdl(ln_split_stats_kernel<__nv_bfloat16, false>, grid, dim3(LS_T), 0, stream, p);
+    return vec4 ? launch_pdl(ln_split_stats_kernel<float, true>, grid, dim3(LS_T), 0, stream, p)
+                : launch_pdl(ln_split_stats_kernel<float, false>, grid, dim3(LS_T), 0, stream, p);
 }
 
 } // namespace normk

@@ -26,6 +26,7 @@ template <typename T, int CMAX, bool EXACT>
 __global__ void __launch_bounds__(RMS_THREADS, (EXACT && CMAX <= 64) ? 4 : 2) rms_reg_kernel(const T *x, T *y, int64_t B, int C,
                                                                  int64_t S, float invC, float eps)
 {
+    pdl_begin();
     const uint64_t pol = policy_evict_first();
     const int64_t s = static_cast<int64_t>(blockIdx.x) * RMS_THREADS + threadIdx.x;
     if (s >= S)
@@ -90,13 +91,11 @@ cudaError_t launch_reg(const T *x, T *y, int64_t B, int64_t C, int64_t S, float 
     if (bx > 0x7fffffff)
         return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(B < 65535 ? B : 65535));
+    const int Ci = static_cast<int>(C);
+    const float invC = 1.0f / static_cast<float>(C);
     if (C == CMAX)
-        rms_reg_kernel<T, CMAX, true><<<grid, RMS_THREADS, 0, stream>>>(x, y, B, static_cast<int>(C), S,
-                                                                     1.0f / static_cast<float>(C), eps);
-    else
-        rms_reg_kernel<T, CMAX, false><<<grid, RMS_THREADS, 0, stream>>>(x, y, B, static_cast<int>(C), S,
-                                                                      1.0f / static_cast<float>(C), eps);
-    return cudaGetLastError();
+        return launch_pdl(rms_reg_kernel<T, CMAX, true>, grid, dim3(RMS_THREADS), 0, stream, x, y, B, Ci, S, invC, eps);
+    return launch_pdl(rms_reg_kernel<T, CMAX, false>, grid, dim3(RMS_THREADS), 0, stream, x, y, B, Ci, S, invC, eps);
 }
 
 } // namespace
