@@ -223,11 +223,6 @@ __device__ __forceinline__ void bulk_wait_all()
 
 // ---- gpu-scope synchronization primitives
 
-__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long *p, unsigned long long v)
-{
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 // 64-bit load from L2 (bypassing L1) that the compiler may not merge or drop,
 // and that the hardware may overlap with other loads (unlike ld.relaxed.gpu,
 // whose loads were measured to complete one after another).  A naturally
