@@ -296,9 +296,12 @@ const char *norm_status_string(norm_status_t status);
  *                                force the register kernel, 2 = force the
  *                                two-kernel path (NCHW entry points only),
  *                                3 = force the warp-per-group kernel, 4 =
- *                                force the streamed register kernel (error
- *                                NORM_ERR_UNSUPPORTED where the forced path
- *                                cannot serve the call).
+ *                                force the streamed register kernel, 5 =
+ *                                force the team-per-group kernel (groups of
+ *                                at most 256 four-element vectors, or 256
+ *                                elements when the vector form is off)
+ *                                (error NORM_ERR_UNSUPPORTED where the forced
+ *                                path cannot serve the call).
  *   NORM_OPT_GN_CLUSTER          CTAs per group of the register kernel: 0 =
  *                                the fewest that hold a group, or 1, 2, 4, 8
  *                                or 16.

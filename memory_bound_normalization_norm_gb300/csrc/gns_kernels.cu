@@ -345,13 +345,6 @@ __device__ __forceinline__ float4 ld4_smem<float>(const float *p)
     return *reinterpret_cast<const float4 *>(p);
 }
 
-template <>
-__device__ __forceinline__ float4 ld4_smem<__nv_bfloat16>(const __nv_bfloat16 *p)
-{
-    const uint2 u = *reinterpret_cast<const uint2 *>(p);
-    return Io<__nv_bfloat16>::unpack(u.x, u.y);
-}
-
 template <typename T>
 __device__ __forceinline__ float first_elem(const float4 &raw)
 {
@@ -482,15 +475,7 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
     bool stopped = false; // this cluster writes nothing more
     bool gave_up = false; // this CTA's own wait gave up
     int64_t consumed = 0; // segments whose copies this CTA has seen complete
-    // group index (segment mod G) of the current segment, stepped without a
-    // division per segment
-    int64_t rg_next = cid % p.G;
-    const int64_t rg_step = ncl % p.G;
     for (int64_t k = 0; k < nk; ++k) {
-        const int64_t rg = rg_next;
-        rg_next += rg_step;
-        if (rg_next >= p.G)
-            rg_next -= p.G;
         const int b = static_cast<int>(k & 1); // exchange slots: segment parity
         const uint32_t par = static_cast<uint32_t>((k >> 1) & 1);
         const int db = static_cast<int>(k % GNS_NBUF); // data buffer
@@ -699,6 +684,151 @@ __global__ void __launch_bounds__(GS_T) gns_split_apply_kernel(GnSegParams p)
             }
         }
         __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ team path
+
+// Short segments (at most 256 items, an item being E = 4, 2 or 1 consecutive
+// elements): a team of T = 2^tlog lanes owns one segment, lane j of the team
+// holding items j, j + T, ..., j + (W - 1) T (W <= WMAX, guarded at the
+// segment's end).  T is the narrowest team that gives each lane at most
+// TEAM_TARGET_W items (up to a full warp): wider teams spend more shuffles
+// per element, narrower ones more registers (a group of 48 channels is 4
+// lanes x 3 vectors).  32 / T segments per warp, 8 warps a CTA, grid-stride
+// over segments.  The mean about the pivot (the segment's first element) and
+// then M2 about the mean are reduced with xor shuffles within the team: no
+// CTA barrier.  Teams of a warp may leave the loop at different times;
+// shuffles name only the team's lanes.
+constexpr int TEAM_W = 8;
+constexpr int TEAM_TARGET_W = 4;
+
+template <int E>
+__device__ __forceinline__ float comp(const float4 &v, int k)
+{
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+
+template <typename T, int E>
+__device__ __forceinline__ float4 team_load(const T *p, uint64_t pol)
+{
+    if constexpr (E == 4)
+        return Io<T>::ld4_stream(p, pol);
+    if constexpr (E == 2) {
+        const float2 t = Io<T>::ld2_stream(p, pol);
+        return make_float4(t.x, t.y, 0.f, 0.f);
+    }
+    return make_float4(Io<T>::ld1_stream(p, pol), 0.f, 0.f, 0.f);
+}
+
+template <typename T, int E>
+__device__ __forceinline__ void team_store(T *p, const float4 &o, uint64_t pol)
+{
+    if constexpr (E == 4)
+        Io<T>::st4_stream(p, o, pol);
+    else if constexpr (E == 2)
+        Io<T>::st2_stream(p, make_float2(o.x, o.y), pol);
+    else
+        Io<T>::st1_stream(p, o.x, pol);
+}
+
+template <typename T, int E, int MODE, int WMAX>
+__global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, int W)
+{
+    pdl_begin();
+    const int Tn = 1 << tlog;
+    const int lane = threadIdx.x & 31;
+    const int j = lane & (Tn - 1);
+    const int first = lane & ~(Tn - 1);
+    const unsigned tmask = Tn == 32 ? 0xffffffffu : (((1u << Tn) - 1u) << first);
+    const int64_t teams_per_cta = blockDim.x >> tlog;
+    const int64_t nteams = static_cast<int64_t>(gridDim.x) * teams_per_cta;
+    const int items = static_cast<int>(p.seg_len / E);
+    const float Lf = static_cast<float>(p.seg_len);
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.y);
+    const T *gm = static_cast<const T *>(p.gamma);
+    const T *bt = static_cast<const T *>(p.beta);
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    const float slope = p.slope;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * teams_per_cta + (threadIdx.x >> tlog); r < p.rows;
+         r += nteams) {
+        const T *xr = x + r * p.seg_len;
+        float4 v[WMAX];
+#pragma unroll
+        for (int w = 0; w < WMAX; ++w) {
+            const int i = j + w * Tn;
+            v[w] = w < W && i < items ? team_load<T, E>(xr + E * i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // the segment's first element, from the team's first lane; every
+        // lane reads it before any lane of the team stores (the shuffles
+        // below order them), so y == x is safe
+        const float K = __shfl_sync(tmask, v[0].x, first);
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < WMAX; ++w) {
+            const int i = j + w * Tn;
+            if (w < W && i < items) {
+                if constexpr (E == 4)
+                    s += ((v[w].x - K) + (v[w].y - K)) + ((v[w].z - K) + (v[w].w - K));
+                else if constexpr (E == 2)
+                    s += (v[w].x - K) + (v[w].y - K);
+                else
+                    s += v[w].x - K;
+            }
+        }
+        for (int o = Tn >> 1; o > 0; o >>= 1)
+            s += __shfl_xor_sync(tmask, s, o);
+        const float mean_d = s / Lf;
+        float q = 0.f;
+#pragma unroll
+        for (int w = 0; w < WMAX; ++w) {
+            const int i = j + w * Tn;
+            if (w < W && i < items) {
+                float qw = 0.f;
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    const float a = (comp<E>(v[w], k) - K) - mean_d;
+                    qw = fmaf(a, a, qw);
+                }
+                q += qw;
+            }
+        }
+        for (int o = Tn >> 1; o > 0; o >>= 1)
+            q += __shfl_xor_sync(tmask, q, o);
+        const float rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        const int64_t cbase = (r % p.G) * p.M;
+        T *yr = y + r * p.seg_len;
+#pragma unroll
+        for (int w = 0; w < WMAX; ++w) {
+            const int i = j + w * Tn;
+            if (!(w < W && i < items))
+                continue;
+            float g[4], b[4];
+            if constexpr (E == 4) {
+                float4 g4, b4;
+                seg_affine4<T, MODE>(gm, bt, cbase, int64_t(4) * i, p.S, true, pol_keep, g4, b4, p.cache_gb != 0);
+                g[0] = g4.x, g[1] = g4.y, g[2] = g4.z, g[3] = g4.w;
+                b[0] = b4.x, b[1] = b4.y, b[2] = b4.z, b[3] = b4.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    const int e = E * i + k;
+                    const int64_t c = cbase + (MODE == AFF_ROW ? int64_t(e) : seg_div(e, p.S, true));
+                    g[k] = gm ? Io<T>::ld1(gm + c) : 1.f;
+                    b[k] = bt ? Io<T>::ld1(bt + c) : 0.f;
+                }
+            }
+            float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < E; ++k) {
+                float t = fmaf(((comp<E>(v[w], k) - K) - mean_d) * rstd, g[k], b[k]);
+                t = t > 0.f ? t : slope * t;
+                o[k] = t + t;
+            }
+            team_store<T, E>(yr + E * i, make_float4(o[0], o[1], o[2], o[3]), pol_stream);
+        }
     }
 }
 
@@ -1127,6 +1257,65 @@ cudaError_t gns_split_apply_launch(const GnSegParams &p, bool bf16, bool vec4, c
                     : launch_pdl(gns_split_apply_kernel<__nv_bfloat16, false>, grid, dim3(GS_T), 0, stream, p);
     return vec4 ? launch_pdl(gns_split_apply_kernel<float, true>, grid, dim3(GS_T), 0, stream, p)
                 : launch_pdl(gns_split_apply_kernel<float, false>, grid, dim3(GS_T), 0, stream, p);
+}
+
+int64_t gns_team_max_items()
+{
+    return int64_t(32) * TEAM_W;
+}
+
+template <typename T, int WMAX>
+cudaError_t team_launch_w(const GnSegParams &p, int elems, dim3 grid, dim3 block, int tlog, int W,
+                          cudaStream_t stream)
+{
+    const int mode = affine_mode(p.S);
+    if (elems == 4) {
+        switch (mode) {
+        case AFF_ROW: return launch_pdl(gns_team_kernel<T, 4, AFF_ROW, WMAX>, grid, block, 0, stream, p, tlog, W);
+        case AFF_CHAN:
+            return launch_pdl(gns_team_kernel<T, 4, AFF_CHAN, WMAX>, grid, block, 0, stream, p, tlog, W);
+        default: return launch_pdl(gns_team_kernel<T, 4, AFF_ANY, WMAX>, grid, block, 0, stream, p, tlog, W);
+        }
+    }
+    if (elems == 2)
+        return mode == AFF_ROW ? launch_pdl(gns_team_kernel<T, 2, AFF_ROW, WMAX>, grid, block, 0, stream, p, tlog, W)
+                               : launch_pdl(gns_team_kernel<T, 2, AFF_ANY, WMAX>, grid, block, 0, stream, p, tlog, W);
+    return mode == AFF_ROW ? launch_pdl(gns_team_kernel<T, 1, AFF_ROW, WMAX>, grid, block, 0, stream, p, tlog, W)
+                           : launch_pdl(gns_team_kernel<T, 1, AFF_ANY, WMAX>, grid, block, 0, stream, p, tlog, W);
+}
+
+template <typename T>
+cudaError_t team_launch_t(const GnSegParams &p, int elems, int sm_count, cudaStream_t stream)
+{
+    if ((elems != 1 && elems != 2 && elems != 4) || p.seg_len % elems != 0)
+        return cudaErrorInvalidValue;
+    const int64_t items = p.seg_len / elems;
+    if (items < 1 || items > gns_team_max_items())
+        return cudaErrorInvalidValue;
+    // the narrowest team that gives each lane at most TEAM_TARGET_W items,
+    // up to a warp (at most TEAM_W items a lane)
+    int tlog = 0;
+    while (tlog < 5 && (int64_t(1) << tlog) * TEAM_TARGET_W < items)
+        ++tlog;
+    const int Tn = 1 << tlog;
+    const int W = static_cast<int>((items + Tn - 1) / Tn);
+    const int64_t teams_per_cta = 256 / Tn;
+    int64_t blocks = (p.rows + teams_per_cta - 1) / teams_per_cta;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap)
+        blocks = cap;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(256);
+    if (W <= 2)
+        return team_launch_w<T, 2>(p, elems, grid, block, tlog, W, stream);
+    if (W <= 4)
+        return team_launch_w<T, 4>(p, elems, grid, block, tlog, W, stream);
+    return team_launch_w<T, TEAM_W>(p, elems, grid, block, tlog, W, stream);
+}
+
+cudaError_t gns_team_launch(const GnSegParams &p, bool bf16, int elems, int sm_count, cudaStream_t stream)
+{
+    return bf16 ? team_launch_t<__nv_bfloat16>(p, elems, sm_count, stream)
+                : team_launch_t<float>(p, elems, sm_count, stream);
 }
 
 cudaError_t gns_warp_launch(const GnSegParams &p, bool bf16, int sm_count, cudaStream_t stream)

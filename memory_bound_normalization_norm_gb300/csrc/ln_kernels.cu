@@ -558,16 +558,14 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 
 // ---------------------------------------------------------------- row path
 //
-// Rows of at most LR_T * 16 4-element vectors (16,384 elements), length a multiple of
-// 4, 16-byte aligned: one CTA per row at a time (grid-stride over rows),
+// Rows of at most 512 threads x 8 4-element vectors (16,384 elements), length a
+// multiple of 4, 16-byte aligned: one CTA per row at a time (grid-stride over rows),
 // the row in registers, so x is read from HBM once and there is no
 // workspace and a single launch.  Mean and M2 are the exact two-pass
 // definition over the registers, about the pivot K = x[r][0]:
 //   delta = sum(x - K) / L, mean = K + delta (an fp32 pair), M2 = sum((x -
 //   mean)^2).
 // Several CTAs per SM keep several rows in flight.
-
-constexpr int LR_T = 256;
 
 // NT threads a CTA, V 4-element vectors a thread.
 template <typename T, int NT, int V>

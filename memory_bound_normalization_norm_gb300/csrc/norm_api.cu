@@ -239,7 +239,7 @@ bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
 // ------------------------------------------------------------------ GN plan
 
 // Segment GroupNorm paths (NORM_OPT_GN_PATH values).
-constexpr int kGnReg = 1, kGnSplit = 2, kGnWarp = 3, kGnStream = 4;
+constexpr int kGnReg = 1, kGnSplit = 2, kGnWarp = 3, kGnStream = 4, kGnTeam = 5;
 // Shortest CTA slice (vectors) for which the automatic choice streams.
 constexpr int64_t kGnStreamMinPer = 256;
 // Longest non-vector segment the warp path takes on its own.
@@ -338,7 +338,7 @@ norm_status_t norm_set_option(norm_option_t option, int64_t value)
         g_opt_ln_ctas = value;
         return NORM_OK;
     case NORM_OPT_GN_PATH:
-        if (value > 4)
+        if (value > 5)
             return NORM_ERR_INVALID_ARG;
         g_opt_gn_path = value;
         return NORM_OK;
@@ -663,7 +663,17 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         if (!stream_ok)
             cudaGetLastError();
     }
+    // Team path: segments of at most 256 items of 4, 2 or 1 elements.  The
+    // automatic choice leaves its longest groups (over 128 items) to the
+    // register kernel for bf16, where that kernel was measured faster.
+    const bool pair = (L & 1) == 0 && aligned(x, 2u * esz) && aligned(y, 2u * esz);
+    const int team_elems = vec4 ? 4 : pair ? 2 : 1;
+    const int64_t team_items = L / team_elems;
+    const bool team_ok = team_items <= normk::gns_team_max_items();
+    const bool team_auto = team_ok && (team_items <= normk::gns_team_max_items() / 2 || !bf16 || !cluster);
     GnPlan pl;
+    if (opt == kGnTeam && !team_ok)
+        return NORM_ERR_UNSUPPORTED;
     if (opt == kGnReg && !cluster)
         return NORM_ERR_UNSUPPORTED;
     if (opt == kGnStream && !stream_ok)
@@ -672,6 +682,8 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         return NORM_ERR_UNSUPPORTED;
     if (opt)
         pl.path = static_cast<int>(opt);
+    else if (team_auto)
+        pl.path = kGnTeam;
     else if (stream_ok && stream_slice > kGnStreamMinPer)
         pl.path = kGnStream;
     else if (cluster)
@@ -704,6 +716,8 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         e = normk::gns_reg_launch(p, bf16, cluster, stream);
     } else if (pl.path == kGnWarp) {
         e = normk::gns_warp_launch(p, bf16, d->sm_count, stream);
+    } else if (pl.path == kGnTeam) {
+        e = normk::gns_team_launch(p, bf16, team_elems, d->sm_count, stream);
     } else {
         plan_gn_split(R, L, vec4, *d, &pl);
         void *ws = workspace;

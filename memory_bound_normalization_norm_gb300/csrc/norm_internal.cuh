@@ -88,6 +88,23 @@ __device__ __forceinline__ void st_stream_f4(float4 *p, float4 v, uint64_t pol)
                  : "memory");
 }
 
+__device__ __forceinline__ float2 ld_stream_f2(const float2 *p, uint64_t pol)
+{
+    float2 v;
+    asm("ld.global.L1::no_allocate.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;"
+        : "=f"(v.x), "=f"(v.y)
+        : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream_f2(float2 *p, float2 v, uint64_t pol)
+{
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;"
+                 :
+                 : "l"(p), "f"(v.x), "f"(v.y), "l"(pol)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_stream_f1(float *p, float v, uint64_t pol)
 {
     asm volatile("st.global.L1::no_allocate.L2::cache_hint.f32 [%0], %1, %2;"
@@ -263,7 +280,8 @@ __device__ __forceinline__ void bar_sync_named(int id, int count)
 // ---------------------------------------------------------------- element types
 // Io<T> moves elements of type T (float, or __nv_bfloat16 with fp32
 // arithmetic) between memory and fp32 registers.  The 4-element forms need
-// p aligned to 4 elements (16 bytes for fp32, 8 for bf16).  bf16 -> fp32 is
+// p aligned to 4 elements (16 bytes for fp32, 8 for bf16), the 2-element
+// forms to 2 elements.  bf16 -> fp32 is
 // exact; fp32 -> bf16 rounds to nearest even (CUDA's __float2bfloat16_rn).
 template <typename T>
 struct Io;
@@ -285,6 +303,14 @@ struct Io<float> {
     static __device__ __forceinline__ void st4_stream(float *p, float4 v, uint64_t pol)
     {
         st_stream_f4(reinterpret_cast<float4 *>(p), v, pol);
+    }
+    static __device__ __forceinline__ float2 ld2_stream(const float *p, uint64_t pol)
+    {
+        return ld_stream_f2(reinterpret_cast<const float2 *>(p), pol);
+    }
+    static __device__ __forceinline__ void st2_stream(float *p, float2 v, uint64_t pol)
+    {
+        st_stream_f2(reinterpret_cast<float2 *>(p), v, pol);
     }
     static __device__ __forceinline__ float ld1(const float *p) { return ld_plain_f1(p); }
     static __device__ __forceinline__ float ld1_stream(const float *p, uint64_t pol) { return ld_stream_f1(p, pol); }
@@ -333,6 +359,18 @@ struct Io<__nv_bfloat16> {
     {
         asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p),
                      "r"(pack_bf16x2(v.x, v.y)), "r"(pack_bf16x2(v.z, v.w)), "l"(pol)
+                     : "memory");
+    }
+    static __device__ __forceinline__ float2 ld2_stream(const __nv_bfloat16 *p, uint64_t pol)
+    {
+        uint32_t a;
+        asm("ld.global.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(a) : "l"(p), "l"(pol));
+        return make_float2(bf16_bits_to_f32(a & 0xffffu), bf16_bits_to_f32(a >> 16));
+    }
+    static __device__ __forceinline__ void st2_stream(__nv_bfloat16 *p, float2 v, uint64_t pol)
+    {
+        asm volatile("st.global.L1::no_allocate.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(pack_bf16x2(v.x, v.y)),
+                     "l"(pol)
                      : "memory");
     }
     static __device__ __forceinline__ float ld1(const __nv_bfloat16 *p)
@@ -682,6 +720,11 @@ cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int clu
 // Apply kernel of the split path (after ln_split_stats_launch on the same
 // segments); vec4 as for the LayerNorm split path.
 cudaError_t gns_split_apply_launch(const GnSegParams &p, bool bf16, bool vec4, cudaStream_t stream);
+// Short segments: a team of lanes per segment, up to 8 items a lane, an item
+// being `elems` (4, 2 or 1) consecutive elements, so x, y and seg_len
+// aligned to that many; at most gns_team_max_items() items a segment.
+int64_t gns_team_max_items();
+cudaError_t gns_team_launch(const GnSegParams &p, bool bf16, int elems, int sm_count, cudaStream_t stream);
 // One warp per segment, scalar loads; any shape (x is re-read from L1/L2).
 cudaError_t gns_warp_launch(const GnSegParams &p, bool bf16, int sm_count, cudaStream_t stream);
 

@@ -185,8 +185,13 @@ def test_bf16_entry_points_check_dtype(ng):
 # ------------------------------------------------------------------ GroupNorm over NCHW
 
 @pytest.mark.parametrize("N,C,S,G,path,cluster", [
-    (2, 32, 64, 8, 0, 0),         # register kernel, one CTA per group
-    (2, 8, 6, 4, 0, 0),           # channels change inside a vector
+    (2, 32, 64, 8, 1, 0),         # register kernel, one CTA per group
+    (2, 32, 64, 8, 0, 0),         # team kernel (L = 256), the automatic choice
+    (2, 8, 6, 4, 0, 0),           # team kernel, channels change inside a vector
+    (2, 256, 4, 1, 5, 0),         # team kernel, 256 vectors a group
+    (4, 240, 1, 6, 5, 0),         # team kernel, S = 1, M = 40
+    (3, 30, 1, 1, 5, 0),          # team kernel, pairs of elements (M = 30)
+    (3, 9, 5, 3, 5, 0),           # team kernel, single elements (L = 15)
     (2, 64, 1024, 4, 0, 0),       # automatic cluster of 2
     (1, 3, 2732, 1, 1, 16),       # forced cluster of 16, ragged slices
     (8, 512, 4096, 32, 0, 0),     # the (8, 512, 64, 64) 32-group workload: clusters of 8, streamed
@@ -198,7 +203,7 @@ def test_bf16_entry_points_check_dtype(ng):
     (1, 32, 16384, 2, 0, 0),      # L = 262,144: 16 CTAs of 4,096 packed vectors
     (1, 128, 65536, 32, 0, 0),    # two-kernel path, vector form
     (3, 9, 5, 3, 2, 0),           # two-kernel path, scalar form
-    (3, 9, 5, 3, 0, 0),           # warp path
+    (3, 9, 5, 3, 3, 0),           # warp path
 ])
 def test_group_norm_nchw_bf16(ng, N, C, S, G, path, cluster):
     n = N * C * S

@@ -1,8 +1,9 @@
 """GroupNorm + LeakyReLU + x2 on the GPU against the float64 oracle, element by element.
 
 Covers the vector kernel (M = 4..128, powers of two) at ragged and wide shapes, the
-warp-per-group kernel (M = 1, 2, 3, 48, 256, misaligned pointers), NULL affine,
-in-place, slopes, and the full-size (1024, 8192), 512-group workload.
+team-per-group kernel (M = 1, 2, 3, 48, 256 and other sizes up to 1,024, misaligned
+pointers), NULL affine, in-place, slopes, and the full-size (1024, 8192), 512-group
+workload.
 """
 import numpy as np
 import pytest
@@ -110,3 +111,19 @@ def test_wide_rows(ng):
     N, C, G = 9, 16384, 512
     x, g, b = inputs(N, C, seed=21)
     assert_parity(run_gn(ng, x, g, b, N, C, G), oracle.group_lrelu_x2(x, g, b, N, C, G), "GN C=16384")
+
+
+@pytest.mark.parametrize("N,C,G", [
+    (2000, 1536, 32),   # M = 48
+    (1000, 1200, 40),   # M = 30: the scalar form
+    (500, 3072, 32),    # M = 96
+    (300, 6144, 32),    # M = 192
+    (100, 1000, 1),     # M = 1000: 250 vectors a group
+    (50, 2048, 2),      # M = 1024: the longest team group
+    (40, 2052, 2),      # M = 1026: past the team kernel, to the register kernel
+])
+def test_group_sizes_not_powers_of_two(ng, N, C, G):
+    x, g, b = inputs(N, C, seed=N + C + G)
+    want = oracle.group_lrelu_x2(x, g, b, N, C, G)
+    assert_parity(run_gn(ng, x, g, b, N, C, G), want, f"GN N={N} C={C} G={G}")
+    assert_parity(run_gn(ng, x, g, b, N, C, G, offset=1), want, f"GN misaligned N={N} C={C} G={G}")

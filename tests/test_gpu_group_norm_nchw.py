@@ -19,7 +19,7 @@ from gpu_util import Guarded, assert_parity
 
 pytestmark = pytest.mark.gpu
 
-REG, SPLIT, WARP, STREAM = 1, 2, 3, 4
+REG, SPLIT, WARP, STREAM, TEAM = 1, 2, 3, 4, 5
 
 
 @pytest.fixture(scope="module")
@@ -79,6 +79,67 @@ def check(ng, N, C, S, G, seed=0, **kw):
 def test_register_kernel(ng, N, C, S, G):
     check(ng, N, C, S, G, seed=N * C + S, path=REG)
     check(ng, N, C, S, G, seed=N * C + S)
+
+
+# ------------------------------------------------------------------ team kernel (short groups)
+
+@pytest.mark.parametrize("N,C,S,G", [
+    (2, 32, 64, 8),      # L = 256: 64 vectors, teams of 16 lanes x 4
+    (2, 256, 4, 1),      # L = 1024: 256 vectors, a warp x 8, the longest team group
+    (4, 48, 1, 1),       # S = 1, M = 48: 12 vectors, teams of 4 lanes x 3
+    (5, 240, 1, 6),      # S = 1, M = 40: 10 vectors, ragged last lane
+    (3, 96, 1, 1),       # S = 1, M = 96: 24 vectors, teams of 8 x 3
+    (2, 8, 6, 4),        # S = 6: channels change inside a vector (L = 12)
+    (3, 12, 7, 3),       # S = 7, L = 28
+    (9, 4, 1, 1),        # L = 4: one vector, a team of one lane
+    (700, 64, 3, 16),    # 11,200 groups of 12: grid-stride over many teams per CTA
+])
+def test_team_kernel(ng, N, C, S, G):
+    check(ng, N, C, S, G, seed=N * C + S + 7, path=TEAM)
+    x, g, b = inputs(N, C, S, seed=N + S)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, g, b, N, C, S, G, path=TEAM, inplace=True), want, "GN team in place")
+
+
+@pytest.mark.parametrize("N,C,S,G", [
+    (3, 30, 1, 1),       # M = 30: pairs of elements (L even, not a multiple of 4)
+    (5, 18, 3, 3),       # L = 18, S = 3: pairs whose channels differ
+    (2, 510, 1, 1),      # L = 510: 255 pairs, a warp x 8
+    (2, 9, 5, 3),        # L = 15: one element an item
+    (1, 1, 1, 1),        # a group of one value: y = 2 LeakyReLU(beta)
+    (2, 256, 1, 1),      # L = 256: vectors here, single elements (256, the most) misaligned
+    (4, 32, 2, 4),       # L = 16, misaligned below
+])
+def test_team_kernel_pair_and_scalar_forms(ng, N, C, S, G):
+    # offset 0: 4-element or 2-element items by L; offset 1 (4 bytes): single elements,
+    # at most 256 of them
+    check(ng, N, C, S, G, seed=N + C + S, path=TEAM)
+    if C // G * S <= 256:
+        check(ng, N, C, S, G, seed=N + C + S + 1, path=TEAM, offset=1)
+    else:
+        x, g, b = inputs(N, C, S, seed=1)
+        with pytest.raises(ng.NormError) as e:
+            run(ng, x, g, b, N, C, S, G, path=TEAM, offset=1)
+        assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+        check(ng, N, C, S, G, seed=N + C + S + 1, offset=1)  # the automatic choice serves it
+
+
+def test_team_kernel_no_affine(ng):
+    N, C, S, G = 6, 96, 2, 4
+    x, _, _ = inputs(N, C, S, seed=61, affine=False)
+    want = oracle.group_lrelu_x2_nchw(x, None, None, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, None, None, N, C, S, G, path=TEAM), want, "GN team no affine")
+
+
+def test_team_kernel_refuses_long_groups(ng):
+    x, g, b = inputs(1, 4, 260, seed=62)  # L = 1040: 260 vectors
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, 1, 4, 260, 1, path=TEAM)
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    x, g, b = inputs(1, 4, 65, seed=62)  # L = 260 elements, misaligned: the scalar form holds 256
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, 1, 4, 65, 1, path=TEAM, offset=1)
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
 
 
 # ------------------------------------------------------------------ clusters
