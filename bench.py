@@ -89,13 +89,17 @@ CONFIGS = {
                          beta=(0.0, 0.1), bf16=True,
                          workload="GroupNorm+LeakyReLU(0.01)+x2 bf16 NCHW (8,512,64,64), 32 groups, fp32 "
                                   "arithmetic"),
+    "gn_m48": dict(op="gn", N=8192, C=1536, G=32, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
+                   workload="GroupNorm+LeakyReLU(0.01)+x2 fp32 (8192,1536), 32 groups of 48 contiguous channels "
+                            "(not a power of two: the team-per-group kernel), x~N(0,1), gamma~N(1,0.1), "
+                            "beta~N(0,0.1), eps 1e-5"),
     "gn_nchw_long": dict(op="gn_nchw", N=1, C=128, S=512 * 512, G=32, x=(0.0, 1.0), gamma=(1.0, 0.1),
                          beta=(0.0, 0.1),
                          workload="GroupNorm+LeakyReLU(0.01)+x2 fp32 NCHW (1,128,512,512), 32 groups of 4 "
                                   "channels x 262144 positions (1,048,576 values: the two-kernel path)"),
 }
 EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_rows", "ln_rows_bf16", "gn_bf16", "rms_bf16",
-               "gn_nchw", "gn_nchw_bf16", "gn_nchw_long"]
+               "gn_nchw", "gn_nchw_bf16", "gn_nchw_long", "gn_m48"]
 
 
 # ---------------------------------------------------------------------------- sizes
@@ -191,7 +195,11 @@ def main_kernel_name(cfg) -> str:
             return "gns_stream_kernel"
         return "ln_persistent_kernel" if L >= (1 << 20) and not bf16 else "ln_split_apply_kernel"
     if cfg["op"] == "gn":
-        return "gn_vec4_kernel"
+        M, bf16 = cfg["C"] // cfg["G"], bool(cfg.get("bf16"))
+        if 4 <= M <= 128 and M & (M - 1) == 0:
+            return "gn_vec4_kernel"
+        items = M // 4 if M % 4 == 0 else M // 2 if M % 2 == 0 else M
+        return "gns_team_kernel" if items <= (128 if bf16 else 256) else "gns_reg_kernel"
     if cfg["op"] == "gn_nchw":
         return "gns_stream_kernel" if gn_nchw_one_launch(cfg) else "gns_split_apply_kernel"
     return "rms_reg_kernel"
@@ -312,7 +320,7 @@ def hbm_peak():
 
 
 # the kernel source files each workload's counters depend on
-KERNEL_SOURCES = {"ln": ("ln_kernels.cu", "gns_kernels.cu", "norm_internal.cuh"), "gn": ("gn_kernels.cu", "norm_internal.cuh"),
+KERNEL_SOURCES = {"ln": ("ln_kernels.cu", "gns_kernels.cu", "norm_internal.cuh"), "gn": ("gn_kernels.cu", "gns_kernels.cu", "norm_internal.cuh"),
                   "gn_nchw": ("gns_kernels.cu", "ln_kernels.cu", "norm_internal.cuh"),
                   "rms": ("rms_kernels.cu", "norm_internal.cuh")}
 

@@ -194,11 +194,16 @@ norm_status_t norm_rms_channel_fwd_bf16(const uint16_t *x, uint16_t *y, int64_t 
  * gamma, beta   [C] per-channel weight and bias, or NULL (1 and 0).
  * num_groups    must divide C.
  * M a power of two in 4..128 with C % 4 == 0 and 16-byte aligned pointers
- * takes the vectorized kernel (4 channels per thread).  Any other M that is a
- * multiple of 4 (up to 131,072, 16-byte aligned pointers) takes the register
- * kernel of norm_group_lrelu_x2_nchw_fwd (one CTA, or a cluster of up to 16
- * CTAs, per group); the rest a warp-per-group kernel that re-reads the group
- * from cache.  Nothing is allocated.
+ * takes the vectorized kernel (4 channels per thread).  Any other M of at
+ * most 256 items (an item being 4 channels with 16-byte aligned pointers and
+ * M % 4 == 0, else 2 channels with M even and 2-element aligned pointers,
+ * else 1) takes a team-per-group kernel: 2^k adjacent lanes hold the group in
+ * registers and reduce it with shuffles (bf16 groups over 128 items go to the
+ * register kernel below).  Longer groups that are a multiple of 4 (up to
+ * 131,072, 16-byte aligned pointers) take the register kernel of
+ * norm_group_lrelu_x2_nchw_fwd (one CTA, or a cluster of up to 16 CTAs, per
+ * group); the rest a warp-per-group kernel that re-reads the group from
+ * cache.  Nothing is allocated.
  */
 norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const float *beta,
                                       float *y, int64_t N, int64_t C, int64_t num_groups,
@@ -227,6 +232,9 @@ norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *ga
  *               (such calls must be serialized by the caller).  It must not
  *               be a LayerNorm workspace that is still in use.
  * Paths (L = M*S):
+ *   - groups of at most 256 items (4, 2 or 1 elements an item, as for
+ *     norm_group_lrelu_x2_fwd): one launch, a team of adjacent lanes per
+ *     group, statistics by shuffles, x read once;
  *   - L a multiple of 4 with 16-byte aligned pointers and L <= 131,072: one
  *     launch; each group is held in registers by one CTA or by a thread-
  *     block cluster of up to 16 CTAs that reduce the statistics through
@@ -239,7 +247,7 @@ norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *ga
  *     groups of y unwritten);
  *   - longer groups and unaligned vectors: a statistics kernel writes
  *     per-chunk partials to the workspace and an apply kernel re-reads x;
- *   - non-vector groups of at most 4,096 elements: one warp per group.
+ *   - non-vector groups of 257 to 4,096 elements: one warp per group.
  */
 size_t norm_group_lrelu_x2_nchw_workspace_bytes(int64_t N, int64_t C, int64_t S, int64_t num_groups);
 

@@ -745,6 +745,11 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
     const int64_t nteams = static_cast<int64_t>(gridDim.x) * teams_per_cta;
     const int items = static_cast<int>(p.seg_len / E);
     const float Lf = static_cast<float>(p.seg_len);
+    // which of this lane's item slots hold an item: the same in every segment
+    bool in[WMAX];
+#pragma unroll
+    for (int w = 0; w < WMAX; ++w)
+        in[w] = w < W && j + w * Tn < items;
     const T *x = static_cast<const T *>(p.x);
     T *y = static_cast<T *>(p.y);
     const T *gm = static_cast<const T *>(p.gamma);
@@ -752,30 +757,38 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     const float slope = p.slope;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * teams_per_cta + (threadIdx.x >> tlog); r < p.rows;
-         r += nteams) {
+    int64_t r = static_cast<int64_t>(blockIdx.x) * teams_per_cta + (threadIdx.x >> tlog);
+    // group index (r mod G) of the current segment, stepped without a
+    // division per segment
+    int64_t rg = r % p.G;
+    const int64_t rg_step = nteams % p.G;
+    for (; r < p.rows; r += nteams) {
         const T *xr = x + r * p.seg_len;
         float4 v[WMAX];
 #pragma unroll
-        for (int w = 0; w < WMAX; ++w) {
-            const int i = j + w * Tn;
-            v[w] = w < W && i < items ? team_load<T, E>(xr + E * i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int w = 0; w < WMAX; ++w)
+            v[w] = in[w] ? team_load<T, E>(xr + E * (j + w * Tn), pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
         // the segment's first element, from the team's first lane; every
         // lane reads it before any lane of the team stores (the shuffles
-        // below order them), so y == x is safe
+        // below order them), so y == x is safe.  From here on v holds
+        // d = x - K.
         const float K = __shfl_sync(tmask, v[0].x, first);
         float s = 0.f;
 #pragma unroll
         for (int w = 0; w < WMAX; ++w) {
-            const int i = j + w * Tn;
-            if (w < W && i < items) {
-                if constexpr (E == 4)
-                    s += ((v[w].x - K) + (v[w].y - K)) + ((v[w].z - K) + (v[w].w - K));
-                else if constexpr (E == 2)
-                    s += (v[w].x - K) + (v[w].y - K);
-                else
-                    s += v[w].x - K;
+            if (in[w]) {
+                v[w].x -= K;
+                if constexpr (E >= 2)
+                    v[w].y -= K;
+                if constexpr (E == 4) {
+                    v[w].z -= K;
+                    v[w].w -= K;
+                    s += (v[w].x + v[w].y) + (v[w].z + v[w].w);
+                } else if constexpr (E == 2) {
+                    s += v[w].x + v[w].y;
+                } else {
+                    s += v[w].x;
+                }
             }
         }
         for (int o = Tn >> 1; o > 0; o >>= 1)
@@ -784,27 +797,26 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
         float q = 0.f;
 #pragma unroll
         for (int w = 0; w < WMAX; ++w) {
-            const int i = j + w * Tn;
-            if (w < W && i < items) {
-                float qw = 0.f;
+            if (in[w]) {
 #pragma unroll
                 for (int k = 0; k < E; ++k) {
-                    const float a = (comp<E>(v[w], k) - K) - mean_d;
-                    qw = fmaf(a, a, qw);
+                    const float a = comp<E>(v[w], k) - mean_d;
+                    q = fmaf(a, a, q);
                 }
-                q += qw;
             }
         }
         for (int o = Tn >> 1; o > 0; o >>= 1)
             q += __shfl_xor_sync(tmask, q, o);
-        const float rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
-        const int64_t cbase = (r % p.G) * p.M;
+        // 2 LeakyReLU(t) = LeakyReLU(2 t), and 2 t = d * sc + c with
+        // sc = 2 rstd gamma, c = 2 beta - mean_d * sc: one FMA an element
+        const float rstd2 = 2.f * rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        const int64_t cbase = rg * p.M;
         T *yr = y + r * p.seg_len;
 #pragma unroll
         for (int w = 0; w < WMAX; ++w) {
-            const int i = j + w * Tn;
-            if (!(w < W && i < items))
+            if (!in[w])
                 continue;
+            const int i = j + w * Tn;
             float g[4], b[4];
             if constexpr (E == 4) {
                 float4 g4, b4;
@@ -823,12 +835,15 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
             float o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < E; ++k) {
-                float t = fmaf(((comp<E>(v[w], k) - K) - mean_d) * rstd, g[k], b[k]);
-                t = t > 0.f ? t : slope * t;
-                o[k] = t + t;
+                const float sc = rstd2 * g[k];
+                const float t = fmaf(comp<E>(v[w], k), sc, fmaf(-mean_d, sc, b[k] + b[k]));
+                o[k] = t > 0.f ? t : slope * t;
             }
             team_store<T, E>(yr + E * i, make_float4(o[0], o[1], o[2], o[3]), pol_stream);
         }
+        rg += rg_step;
+        if (rg >= p.G)
+            rg -= p.G;
     }
 }
 

@@ -109,3 +109,11 @@ def test_kernel_source_hash_ignores_comments():
     assert bench.code_only("int f(int x) { return x + 2; }") != bench.code_only(a)
     for op in bench.KERNEL_SOURCES:
         assert len(bench.kernel_source_hash(op)) == 16
+
+
+def test_main_kernel_of_group_norm_workloads():
+    assert bench.main_kernel_name(bench.CONFIGS["gn"]) == "gn_vec4_kernel"
+    assert bench.main_kernel_name(bench.CONFIGS["gn_m48"]) == "gns_team_kernel"
+    assert bench.main_kernel_name(dict(op="gn", C=4096, G=4)) == "gns_team_kernel"  # 256 vectors a group
+    assert bench.main_kernel_name(dict(op="gn", C=4096, G=4, bf16=True)) == "gns_reg_kernel"
+    assert bench.main_kernel_name(dict(op="gn", C=960, G=32)) == "gns_team_kernel"  # pairs of elements
