@@ -55,6 +55,9 @@ FALLBACK_HBM_GBS = 6800.0
 DATA = ("synthetic: seeded counter-based SplitMix64 + Box-Muller normals (seed 0; tensor ids x=0, "
         "gamma=1, beta=2), identical bytes for the GPU path and the CPU oracle")
 
+# GB300's nominal HBM3e bandwidth (GB/s), reported beside the measured copy peak.
+NOMINAL_HBM_GBS = 7900.0
+
 CONFIGS = {
     "rms_small": dict(op="rms", B=2, C=64, S=32 * 32, x=(0.0, 1.0),
                       workload="RMSNorm over dim 1 of fp32 NCHW (2,64,32,32), x~N(0,1), eps 1e-5"),
@@ -776,6 +779,7 @@ def main(argv=None):
                 "note": "median single launch after an L2 flush (2x L2 written), CUDA events around each launch"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                          "peak_source": peak_note, "traffic_note": traffic_note,
                          "kernel": main_kernel_name(cfg)},
             "cpu_baseline": cpu,
