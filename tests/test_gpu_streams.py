@@ -4,8 +4,8 @@ The library's calls are stream-ordered and allocate nothing when given a workspa
 they may run at the same time on different streams (each with its own workspace) and be
 captured into CUDA graphs.  Covered: two persistent LayerNorm launches (cooperative, every
 SM) on two streams at once beside the cluster kernels of GroupNorm and LayerNorm, the
-row kernel, the (N, C) GroupNorm and RMSNorm; and a graph replaying every
-non-cooperative path several times.
+row kernel, the (N, C) GroupNorm (vector and team-per-group kernels) and RMSNorm; and a
+graph replaying every non-cooperative path several times.
 """
 import numpy as np
 import pytest
@@ -75,6 +75,14 @@ def test_concurrent_streams(ng):
     yd2 = torch.empty_like(xd2)
     jobs.append((lambda s=None: ng.norm_group_lrelu_x2_fwd(xd2, gd2, bd2, yd2, 512, 8192, 512, 1e-5, 0.01, stream=s),
                  yd2, oracle.group_lrelu_x2(x2, g2, b2, 512, 8192, 512), "GN (N, C)"))
+    # GroupNorm with groups of 48 channels: the team-per-group kernel
+    x5 = normgen.normal(1000 * 1536, seed=8, tensor_id=0)
+    g5 = normgen.normal(1536, 1.0, 0.1, seed=8, tensor_id=1)
+    b5 = normgen.normal(1536, 0.0, 0.1, seed=8, tensor_id=2)
+    xd5, gd5, bd5 = dev(x5), dev(g5), dev(b5)
+    yd5 = torch.empty_like(xd5)
+    jobs.append((lambda s=None: ng.norm_group_lrelu_x2_fwd(xd5, gd5, bd5, yd5, 1000, 1536, 32, 1e-5, 0.01, stream=s),
+                 yd5, oracle.group_lrelu_x2(x5, g5, b5, 1000, 1536, 32), "GN groups of 48"))
     # RMSNorm
     x3 = normgen.normal(4 * 64 * 65536, seed=7, tensor_id=0)
     xd3 = dev(x3)
@@ -104,11 +112,16 @@ def test_graph_capture_and_replay(ng):
     x3, g3, b3, w3 = gn_case(2, 128, 4096, 8, 13)
     x4 = normgen.normal(2 * 64 * 1024, seed=14, tensor_id=0)
     w4 = oracle.rms_channel(x4, 2, 64, 1024)
+    x5 = normgen.normal(300 * 960, seed=15, tensor_id=0)
+    g5 = normgen.normal(960, 1.0, 0.1, seed=15, tensor_id=1)
+    b5 = normgen.normal(960, 0.0, 0.1, seed=15, tensor_id=2)
+    w5 = oracle.group_lrelu_x2(x5, g5, b5, 300, 960, 32)
     d1 = [dev(a) for a in (x1, g1, b1)]
     d2 = [dev(a) for a in (x2, g2, b2)]
     d3 = [dev(a) for a in (x3, g3, b3)]
     d4 = dev(x4)
-    y1, y2, y3, y4 = (torch.empty_like(t) for t in (d1[0], d2[0], d3[0], d4))
+    d5 = [dev(a) for a in (x5, g5, b5)]
+    y1, y2, y3, y4, y5 = (torch.empty_like(t) for t in (d1[0], d2[0], d3[0], d4, d5[0]))
     s = torch.cuda.Stream()
 
     def step():
@@ -116,6 +129,8 @@ def test_graph_capture_and_replay(ng):
         ng.norm_layer_fwd(d2[0], d2[1], d2[2], y2, rows2, L2, 1e-5, stream=s.cuda_stream)
         ng.norm_group_lrelu_x2_nchw_fwd(d3[0], d3[1], d3[2], y3, 2, 128, 4096, 8, 1e-5, 0.01, stream=s.cuda_stream)
         ng.norm_rms_channel_fwd(d4, y4, 2, 64, 1024, 1e-5, stream=s.cuda_stream)
+        # groups of 30 channels: the team kernel's 2-element form
+        ng.norm_group_lrelu_x2_fwd(d5[0], d5[1], d5[2], y5, 300, 960, 32, 1e-5, 0.01, stream=s.cuda_stream)
 
     with torch.cuda.stream(s):
         step()  # first calls outside the capture: per-device setup happens here
@@ -123,7 +138,7 @@ def test_graph_capture_and_replay(ng):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
         step()
-    for y in (y1, y2, y3, y4):
+    for y in (y1, y2, y3, y4, y5):
         y.fill_(float("nan"))
     torch.cuda.synchronize()
     for _ in range(5):
@@ -131,5 +146,5 @@ def test_graph_capture_and_replay(ng):
     torch.cuda.synchronize()
     assert ng.norm_last_error() == 0
     for y, want, what in ((y1, w1, "LN cluster kernel"), (y2, w2, "LN row kernel"), (y3, w3, "GN NCHW"),
-                          (y4, w4, "RMS")):
+                          (y4, w4, "RMS"), (y5, w5, "GN team kernel")):
         assert_parity(y.cpu().numpy(), want, f"{what} replayed from a graph")
