@@ -643,6 +643,14 @@ def reference_arm(args, world, rank):
     cfg = CONFIGS[args.config]
     import oracle
     x, g, b = host_inputs(cfg)
+    # the GPU arm's config names the L2 it rotated buffers against: the same text here
+    l2 = None
+    try:
+        import torch
+        if torch.cuda.is_available():
+            l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    except Exception:  # pragma: no cover - CPU-only host
+        l2 = None
     # size each step so that the whole run stays within a few minutes
     budget_s = 150.0
     gbs, el, reps, used, sample = time_oracle(cfg, 0.0, max_reps=1, x=x, g=g, b=b)
@@ -666,7 +674,7 @@ def reference_arm(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
-        "config": shape_config(args.config, cfg),
+        "config": shape_config(args.config, cfg, l2),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
                          "sample": sample + " (float64 two-pass C oracle, OpenMP over independent units)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -22,8 +22,8 @@
  *   - Every call is asynchronous on `stream` (0 = the legacy default stream).
  *     Argument errors are returned synchronously, before anything is
  *     launched.  A launch failure returns NORM_ERR_CUDA.  Faults detected on
- *     the device (a grid barrier that gave up waiting) are recorded in a
- *     per-device error word that norm_last_error() reads.
+ *     the device (a grid barrier that gave up waiting) are recorded in an
+ *     error word of the stream that norm_last_error(stream) reads.
  *   - y == x (exact aliasing, in place) is allowed.  Any other overlap of y
  *     with an input is rejected with NORM_ERR_INVALID_ARG.
  *   - eps must be finite and >= 0.  Sizes must be >= 0; a size of 0 in any
@@ -78,9 +78,13 @@ typedef enum {
  *          it must be zero-filled again.  A workspace must not be shared by calls that
  *          can run at the same time (different streams).
  *          workspace == NULL: the library uses its own per-device workspace,
- *          allocated with cudaMalloc on the first such call on a device and
- *          kept until exit; such calls must then be serialized by the caller
- *          (one stream at a time).
+ *          allocated stream-ordered (cudaMallocAsync, then cudaMemsetAsync,
+ *          on `stream`) the first time a call needs one or a larger one, and
+ *          kept until exit; no call synchronizes the device.  Such calls must
+ *          be serialized by the caller (one stream at a time, or streams
+ *          ordered by events).  A call that would grow it while `stream` is
+ *          being captured into a CUDA graph returns NORM_ERR_WORKSPACE: make
+ *          a first call of the largest shape before capturing.
  *
  * Paths, all with a row length that is a multiple of 4 and 16-byte aligned
  * x/y/gamma/beta unless stated:
@@ -130,18 +134,21 @@ norm_status_t norm_layer_fwd_bf16(const uint16_t *x, const uint16_t *gamma, cons
  * in a plugin that is handed only its inputs and outputs), so they can pass
  * neither a workspace nor workspace == NULL (which allocates once).
  *
- * Same operation, arguments and results as norm_layer_fwd without the
- * workspace: the scratch lives in a static device array of
+ * Same operation, arguments, path choice and results as norm_layer_fwd
+ * without the workspace: the scratch lives in a static device array of
  * NORM_NOALLOC_SCRATCH_BYTES (1 MiB) inside the library, held by every device
  * that loads the library until the process exits.
- *   - Returns NORM_ERR_WORKSPACE, without launching, when the shape needs
- *     more scratch than that (norm_layer_workspace_bytes(rows, row_len) >
- *     NORM_NOALLOC_SCRATCH_BYTES, e.g. more than ~65,000 rows of short
- *     length).
+ *   - The row kernel and the cluster kernel use no scratch, so every shape
+ *     they take is served, however many rows.  The persistent kernel uses
+ *     about 20 KB.  The two-kernel path (ragged lengths, misaligned pointers,
+ *     rows between 131,072 and 2^20 elements) uses 256 bytes plus 16 bytes
+ *     per (row, chunk).
+ *   - Returns NORM_ERR_WORKSPACE, without launching, when the path chosen
+ *     for the shape needs more scratch than the array holds (e.g. more than
+ *     ~65,000 rows of a ragged length on the two-kernel path).
  *   - The first call on a device looks up the array's device address on the
  *     current device; make that first call before any stream capture.
- *   - Every call zeroes the part of the array that the shape uses
- *     (norm_layer_workspace_bytes(rows, row_len) bytes) with a
+ *   - A call whose path uses scratch zeroes the bytes that path uses with a
  *     stream-ordered memset, then runs the LayerNorm kernels on `stream`.
  *   - All calls on a device share the one array: calls that can overlap on
  *     the GPU (different streams, or different host threads without
@@ -228,8 +235,10 @@ norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *ga
  * workspace     used only by the two-kernel path below: at least
  *               norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, num_groups)
  *               bytes, 16-byte aligned, no initial contents needed.  NULL:
- *               the library allocates its own on first need and keeps it
- *               (such calls must be serialized by the caller).  It must not
+ *               the library allocates its own, stream-ordered
+ *               (cudaMallocAsync on `stream`), on first need and keeps it
+ *               (such calls must be serialized by the caller; growth
+ *               during a stream capture returns NORM_ERR_WORKSPACE).  It must not
  *               be a LayerNorm workspace that is still in use.
  * Paths (L = M*S):
  *   - groups of at most 256 items (4, 2 or 1 elements an item, as for
@@ -265,12 +274,17 @@ norm_status_t norm_group_lrelu_x2_nchw_fwd_bf16(const uint16_t *x, const uint16_
                                                 size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ status
- * Synchronize `stream`, then read and clear the current device's error word.
- * Returns NORM_OK if no device-side wait gave up since the last call, else
- * the recorded status (NORM_ERR_TIMEOUT).  After a timeout the library-owned
- * LayerNorm workspace of this device is reset here; caller-owned workspaces
- * must be reset by the caller.  Returns NORM_ERR_CUDA if the synchronize
- * itself fails.
+ * Every stream has its own error word on each device (the first 255 streams
+ * a device sees; further streams share one word).  A launch records its
+ * first device-side failure in the word of the stream it was launched on
+ * (for a CUDA graph: the stream it was captured on).
+ * norm_last_error(stream) synchronizes `stream` only, then reads and clears
+ * that stream's word.  Returns NORM_OK if no device-side wait of a call on
+ * this stream gave up since the last call, else the recorded status
+ * (NORM_ERR_TIMEOUT).  After a timeout the library-owned LayerNorm workspace
+ * of this device is reset here (stream-ordered on `stream`);
+ * caller-owned workspaces must be reset by the caller.  Returns
+ * NORM_ERR_CUDA if the synchronize itself fails.
  */
 norm_status_t norm_last_error(cudaStream_t stream);
 

@@ -33,12 +33,26 @@
 // elements travel with each row's bulk copy.
 //
 // Grid barrier without atomics.  Each CTA publishes its (mean, M2) as two
-// 64-bit words, each carrying a 32-bit tag in its high half, written with
-// st.relaxed.gpu (single-copy atomic).  Warp 0 polls the G records of the
-// row with plain L2 loads (ld.global.cg, which overlap) until every tag
-// matches, so the barrier and its data arrive in the same round trip.  It
-// polls after the CTA's y stores have been issued: its loads would
-// otherwise queue behind them.  Records sit in 4 rotating slots.  Tags count
+// 64-bit words, each carrying a 32-bit tag in its high half, in one 16-byte
+// record written by a bulk store (cp.async.bulk shared -> global, issued by
+// one statistics thread; a generic store would wait behind the CTA's queued
+// y stores).  Warp 0 polls the G records of the row with weak L2 loads
+// (ld.global.cg, 8 bytes each, which overlap) until every tag matches, so the
+// barrier and its data arrive in the same round trip.  It polls after the
+// CTA's y stores have been issued: its loads would otherwise queue behind
+// them.
+// What this relies on: an aligned 8-byte word of the 16-byte record is never
+// observed half old and half new by an 8-byte load from L2.  That is a
+// property of the hardware (the record is one aligned 16-byte write into one
+// L2 sector), not a promise of the PTX memory model, under which these weak
+// loads race with the async-proxy store.  Nothing else is needed: each word
+// carries its own tag, a word is used only when its tag is the one awaited,
+// and a stale word (an older tag) is simply polled again, so no ordering
+// between the two words or with other memory is required.  A slot is
+// rewritten (4 rows later) only after every CTA has merged the row it held:
+// a CTA publishes row q + 4 at its iteration q + 2, which it reaches only
+// after merging row q + 2, whose records every CTA publishes only after it
+// has merged row q.  Records sit in 4 rotating slots.  Tags count
 // rows: row r of a launch is tagged row_base + r + 1, where row_base
 // (workspace header) is the number of rows the persistent kernel has already
 // processed on this workspace.  A slot therefore only ever holds tags

@@ -1,7 +1,8 @@
 // ln_noalloc.cu - LayerNorm for callers that cannot allocate device memory.
 //
-// norm_layer_fwd needs a scratch workspace (the grid-barrier counters and the
-// per-CTA partial statistics).  Some callers cannot provide one: code that
+// norm_layer_fwd needs a scratch workspace on two of its paths (the
+// persistent kernel's grid-barrier header and tagged records, the two-kernel
+// path's per-chunk partials).  Some callers cannot provide one: code that
 // runs where cudaMalloc is not allowed (inside a custom allocator's own
 // callbacks, in a process whose memory pool is fixed up front, or in a
 // plugin that receives only input and output pointers from its host).  For
@@ -50,23 +51,22 @@ norm_status_t scratch_address(void **out)
 extern "C" norm_status_t norm_layer_fwd_noalloc(const float *x, const float *gamma, const float *beta, float *y,
                                                 int64_t rows, int64_t row_len, float eps, cudaStream_t stream)
 {
-    if (rows < 0 || row_len < 0)
-        return NORM_ERR_INVALID_ARG;
-    if (rows == 0 || row_len == 0)
-        return norm_layer_fwd(x, gamma, beta, y, rows, row_len, eps, nullptr, 0, stream);
-    const size_t need = norm_layer_workspace_bytes(rows, row_len);
-    if (need == 0)
-        return NORM_ERR_UNSUPPORTED;
+    // The path norm_layer_fwd takes for this call, and the scratch it needs
+    // (none on the row and cluster kernels).
+    size_t need = 0;
+    norm_status_t st = normapi::layer_fwd_workspace_need(x, gamma, beta, y, rows, row_len, eps, 4, &need);
+    if (st != NORM_OK)
+        return st;
     if (need > NORM_NOALLOC_SCRATCH_BYTES)
         return NORM_ERR_WORKSPACE;
     void *scratch = nullptr;
-    norm_status_t st = scratch_address(&scratch);
+    st = scratch_address(&scratch);
     if (st != NORM_OK)
         return st;
-    // The array keeps whatever the previous call left in it (including the
-    // state of a call that gave up waiting): start from zeros, as from a
-    // fresh workspace, over every byte this shape uses.
-    if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) {
+    // The array keeps whatever the previous call left in it (another shape's
+    // partials, or the state of a call that gave up waiting): start from
+    // zeros, as from a fresh workspace, over every byte this path uses.
+    if (need > 0 && cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
     }

@@ -5,12 +5,16 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "norm_internal.cuh"
 
-// Per-device error word: kernels record the first device-side failure here
-// (NORM_ERR_TIMEOUT); norm_last_error() reads and clears it.
-__device__ unsigned g_norm_error_word;
+// Per-device error words, one per stream slot: a launch on a stream records
+// its first device-side failure (NORM_ERR_TIMEOUT) in that stream's word, and
+// norm_last_error(stream) reads and clears only that word.  Slot 0 is shared
+// by the streams beyond the first kErrSlots - 1 a device sees.
+constexpr int kErrSlots = 256;
+__device__ unsigned g_norm_error_words[kErrSlots];
 
 namespace {
 
@@ -53,7 +57,9 @@ struct DeviceState {
     int coop = 0;
     int ln_max_dyn_smem = 0; // dynamic smem the persistent kernel may use
     int ln_ctas_per_sm = 0;  // at the full dynamic smem budget
-    unsigned *err = nullptr;
+    unsigned *err = nullptr; // kErrSlots words
+    std::unordered_map<cudaStream_t, int> err_slot; // stream -> its error word
+    int err_next = 1;
     void *ws = nullptr;
     size_t ws_bytes = 0;
     void *gn_ws = nullptr; // GroupNorm split-path partials (never shared with LayerNorm)
@@ -90,7 +96,7 @@ norm_status_t device_state(DeviceState **out)
             return NORM_ERR_CUDA;
         }
         void *err = nullptr;
-        if (cudaGetSymbolAddress(&err, g_norm_error_word) != cudaSuccess) {
+        if (cudaGetSymbolAddress(&err, g_norm_error_words) != cudaSuccess) {
             cudaGetLastError();
             return NORM_ERR_CUDA;
         }
@@ -112,6 +118,60 @@ norm_status_t device_state(DeviceState **out)
     if (!s.ok)
         return NORM_ERR_CUDA;
     *out = &s;
+    return NORM_OK;
+}
+
+// The error word of launches on `stream` (a slot assigned on first use).
+unsigned *stream_err(DeviceState &d, cudaStream_t stream)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = d.err_slot.find(stream);
+    if (it != d.err_slot.end())
+        return d.err + it->second;
+    int slot = 0;
+    if (d.err_next < kErrSlots)
+        slot = d.err_next++;
+    d.err_slot.emplace(stream, slot);
+    return d.err + slot;
+}
+
+// The library-owned workspace of `bytes` or more at *ws (of *ws_bytes bytes),
+// grown stream-ordered on `stream`: the old buffer is freed and a new one
+// allocated and zero-filled with cudaFreeAsync / cudaMallocAsync /
+// cudaMemsetAsync, so no call synchronizes the device.  Callers serialize the
+// calls that use it.  Growth is refused (NORM_ERR_WORKSPACE) while `stream`
+// is being captured into a CUDA graph: an allocation made inside a capture
+// belongs to the graph.
+norm_status_t grow_library_workspace(void **ws, size_t *ws_bytes, size_t bytes, bool zero, cudaStream_t stream)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (*ws_bytes >= bytes)
+        return NORM_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone)
+        return NORM_ERR_WORKSPACE;
+    if (*ws && cudaFreeAsync(*ws, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    *ws = nullptr;
+    *ws_bytes = 0;
+    void *p = nullptr;
+    if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    if (zero && cudaMemsetAsync(p, 0, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeAsync(p, stream);
+        return NORM_ERR_CUDA;
+    }
+    *ws = p;
+    *ws_bytes = bytes;
     return NORM_OK;
 }
 
@@ -402,16 +462,29 @@ norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStre
 
 namespace {
 
-// LayerNorm on tensors of esz-byte elements: 4 = fp32, 2 = bf16.
-norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void *y, int64_t rows, int64_t row_len,
-                        float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream, int esz)
+// The path a LayerNorm call takes and what it needs.
+struct LnChoice {
+    bool persistent = false, row_kernel = false, ln_stream = false;
+    int ln_cluster = 0; // CTAs per row of the cluster kernel
+    LnPlan pl;          // ws_bytes: the workspace the path uses (0 for none)
+};
+
+// Validate a LayerNorm call on tensors of esz-byte elements (4 = fp32, 2 =
+// bf16) and choose its path for the current device and options, launching
+// nothing.  *empty is set when the call has no elements (a no-op).
+norm_status_t layer_plan(const void *x, const void *gamma, const void *beta, const void *y, int64_t rows,
+                         int64_t row_len, float eps, const void *workspace, size_t workspace_bytes, int esz,
+                         DeviceState **dev, LnChoice *ch, bool *empty)
 {
     const bool bf16 = esz == 2;
     int64_t n = 0;
+    *empty = false;
     if (rows < 0 || row_len < 0 || !valid_eps(eps) || !safe_mul(rows, row_len, &n))
         return NORM_ERR_INVALID_ARG;
-    if (n == 0)
+    if (n == 0) {
+        *empty = true;
         return NORM_OK;
+    }
     if (!x || !y)
         return NORM_ERR_INVALID_ARG;
     if (!aligned(x, esz) || !aligned(y, esz) || !aligned(gamma, esz) || !aligned(beta, esz))
@@ -427,77 +500,75 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     norm_status_t st = device_state(&d);
     if (st != NORM_OK)
         return st;
+    *dev = d;
 
     const uintptr_t va = 4u * esz; // alignment of a 4-element vector
     const bool vec4 = (row_len & 3) == 0 && aligned(x, va) && aligned(y, va) && aligned(gamma, va) &&
                       aligned(beta, va);
     const int64_t path_opt = g_opt_ln_path.load();
-    LnPlan pl;
-    bool persistent = false;
+    LnChoice c;
     // Streamed cluster kernel (shared with GroupNorm: one group per row, no
     // activation): rows of up to 131,072 elements, read once.
-    int ln_cluster = 0;
     if (vec4 && aligned(x, 16) && (bf16 ? (row_len & 7) == 0 : true)) {
         const int cl = stream_auto_cluster(row_len / 4, normk::gns_stream_capacity4(bf16));
         int active = 0;
         if (cl && normk::gns_stream_max_clusters(row_len, 1, bf16, false, cl, &active) == cudaSuccess && active >= 1)
-            ln_cluster = cl;
+            c.ln_cluster = cl;
         else
             cudaGetLastError();
     }
-    if (path_opt == kLnStream && !ln_cluster)
+    if (path_opt == kLnStream && !c.ln_cluster)
         return NORM_ERR_UNSUPPORTED;
     const int64_t rows_max_auto = bf16 ? kLnRowsMaxAuto : kLnRowsMaxAutoF32;
-    const bool ln_stream =
-        ln_cluster && (path_opt == kLnStream ||
-                       (path_opt == 0 && row_len > rows_max_auto && row_len <= kLnStreamMaxAuto));
+    c.ln_stream = c.ln_cluster && (path_opt == kLnStream ||
+                                   (path_opt == 0 && row_len > rows_max_auto && row_len <= kLnStreamMaxAuto));
     const bool row_kernel_fits = vec4 && row_len <= normk::ln_rows_max_row_len();
-    const bool row_kernel = !ln_stream && row_kernel_fits &&
-                            (path_opt == 3 || (path_opt == 0 && row_len < kPersistentMinRowLen));
-    if (path_opt == 3 && !row_kernel)
+    c.row_kernel = !c.ln_stream && row_kernel_fits &&
+                   (path_opt == 3 || (path_opt == 0 && row_len < kPersistentMinRowLen));
+    if (path_opt == 3 && !c.row_kernel)
         return NORM_ERR_UNSUPPORTED;
-    if (row_kernel || ln_stream) {
-        pl.path = ln_stream ? kLnStream : 3;
-        pl.ws_bytes = 0;
+    if (c.row_kernel || c.ln_stream) {
+        c.pl.path = c.ln_stream ? kLnStream : 3;
+        c.pl.ws_bytes = 0;
     }
     // the persistent kernel is fp32 only
     if (path_opt == 1 && bf16)
         return NORM_ERR_UNSUPPORTED;
-    if (!row_kernel && !ln_stream && path_opt != 2 && vec4 && !bf16) {
+    if (!c.row_kernel && !c.ln_stream && path_opt != 2 && vec4 && !bf16) {
         LnPlan pp;
         if (plan_persistent(rows, row_len, *d, &pp) && (path_opt == 1 || row_len >= kPersistentMinRowLen)) {
-            pl = pp;
-            persistent = true;
+            c.pl = pp;
+            c.persistent = true;
         }
     }
-    if (path_opt == 1 && !persistent)
+    if (path_opt == 1 && !c.persistent)
         return NORM_ERR_UNSUPPORTED;
-    if (!persistent && !row_kernel && !ln_stream)
-        plan_split(rows, row_len, vec4, *d, &pl);
+    if (!c.persistent && !c.row_kernel && !c.ln_stream)
+        plan_split(rows, row_len, vec4, *d, &c.pl);
+    *ch = c;
+    return NORM_OK;
+}
+
+// LayerNorm on tensors of esz-byte elements: 4 = fp32, 2 = bf16.
+norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void *y, int64_t rows, int64_t row_len,
+                        float eps, void *workspace, size_t workspace_bytes, cudaStream_t stream, int esz)
+{
+    const bool bf16 = esz == 2;
+    DeviceState *d = nullptr;
+    LnChoice ch;
+    bool empty = false;
+    norm_status_t st = layer_plan(x, gamma, beta, y, rows, row_len, eps, workspace, workspace_bytes, esz, &d, &ch,
+                                  &empty);
+    if (st != NORM_OK || empty)
+        return st;
+    const LnPlan &pl = ch.pl;
 
     void *ws = workspace;
     if (!ws) {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (d->ws_bytes < pl.ws_bytes) {
-            // Grow the library-owned workspace (callers serialize these calls).
-            if (cudaDeviceSynchronize() != cudaSuccess) {
-                cudaGetLastError();
-                return NORM_ERR_CUDA;
-            }
-            if (d->ws)
-                cudaFree(d->ws);
-            d->ws = nullptr;
-            d->ws_bytes = 0;
-            void *p = nullptr;
-            if (cudaMalloc(&p, pl.ws_bytes) != cudaSuccess || cudaMemset(p, 0, pl.ws_bytes) != cudaSuccess ||
-                cudaDeviceSynchronize() != cudaSuccess) {
-                cudaGetLastError();
-                if (p)
-                    cudaFree(p);
-                return NORM_ERR_CUDA;
-            }
-            d->ws = p;
-            d->ws_bytes = pl.ws_bytes;
+        if (pl.ws_bytes > 0) {
+            st = grow_library_workspace(&d->ws, &d->ws_bytes, pl.ws_bytes, true, stream);
+            if (st != NORM_OK)
+                return st;
         }
         ws = d->ws;
     } else if (workspace_bytes < pl.ws_bytes) {
@@ -514,13 +585,13 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     p.row_len = row_len;
     p.eps = eps;
     p.sync = static_cast<normk::LnSync *>(ws);
-    p.part = reinterpret_cast<float4 *>(static_cast<char *>(ws) + kWsHeader);
-    p.err = d->err;
+    p.part = ws ? reinterpret_cast<float4 *>(static_cast<char *>(ws) + kWsHeader) : nullptr;
+    p.err = stream_err(*d, stream);
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
     p.chunk = pl.chunk;
     p.parts = pl.parts;
     cudaError_t e;
-    if (ln_stream) {
+    if (ch.ln_stream) {
         normk::GnSegParams q;
         std::memset(&q, 0, sizeof(q));
         q.x = x;
@@ -534,12 +605,12 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
         q.S = 1;
         q.eps = eps;
         q.timeout_ns = p.timeout_ns;
-        q.err = d->err;
+        q.err = p.err;
         q.cache_gb = static_cast<size_t>(row_len) * esz <= kGbL1Bytes;
-        e = normk::gns_stream_launch(q, bf16, false, ln_cluster, stream);
-    } else if (row_kernel) {
+        e = normk::gns_stream_launch(q, bf16, false, ch.ln_cluster, stream);
+    } else if (ch.row_kernel) {
         e = normk::ln_rows_launch(p, bf16, d->sm_count, stream);
-    } else if (persistent) {
+    } else if (ch.persistent) {
         p.tag_skew = static_cast<unsigned>(g_opt_extra_arrivals.load());
         p.max_n4 = pl.max_n4;
         e = normk::ln_persistent_launch(p, pl.grid, pl.dyn_smem, stream);
@@ -707,7 +778,7 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     p.eps = eps;
     p.slope = negative_slope;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
-    p.err = d->err;
+    p.err = stream_err(*d, stream);
     p.cache_gb = S == 1 && static_cast<size_t>(L) * esz <= kGbL1Bytes;
 
     if (pl.path == kGnStream) {
@@ -722,25 +793,10 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         plan_gn_split(R, L, vec4, *d, &pl);
         void *ws = workspace;
         if (!ws) {
-            std::lock_guard<std::mutex> lock(g_mu);
-            if (d->gn_ws_bytes < pl.ws_bytes) {
-                // Grow the library-owned workspace (callers serialize these calls).
-                if (cudaDeviceSynchronize() != cudaSuccess) {
-                    cudaGetLastError();
-                    return NORM_ERR_CUDA;
-                }
-                if (d->gn_ws)
-                    cudaFree(d->gn_ws);
-                d->gn_ws = nullptr;
-                d->gn_ws_bytes = 0;
-                void *q = nullptr;
-                if (cudaMalloc(&q, pl.ws_bytes) != cudaSuccess) {
-                    cudaGetLastError();
-                    return NORM_ERR_CUDA;
-                }
-                d->gn_ws = q;
-                d->gn_ws_bytes = pl.ws_bytes;
-            }
+            // the partials need no initial contents
+            st = grow_library_workspace(&d->gn_ws, &d->gn_ws_bytes, pl.ws_bytes, false, stream);
+            if (st != NORM_OK)
+                return st;
             ws = d->gn_ws;
         } else if (workspace_bytes < pl.ws_bytes) {
             return NORM_ERR_WORKSPACE;
@@ -769,6 +825,23 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
 }
 
 } // namespace
+
+namespace normapi {
+
+norm_status_t layer_fwd_workspace_need(const void *x, const void *gamma, const void *beta, const void *y,
+                                       int64_t rows, int64_t row_len, float eps, int esz, size_t *ws_bytes)
+{
+    DeviceState *d = nullptr;
+    LnChoice ch;
+    bool empty = false;
+    *ws_bytes = 0;
+    const norm_status_t st = layer_plan(x, gamma, beta, y, rows, row_len, eps, nullptr, 0, esz, &d, &ch, &empty);
+    if (st == NORM_OK && !empty)
+        *ws_bytes = ch.pl.ws_bytes;
+    return st;
+}
+
+} // namespace normapi
 
 extern "C" {
 
@@ -849,29 +922,28 @@ norm_status_t norm_last_error(cudaStream_t stream)
     norm_status_t st = device_state(&d);
     if (st != NORM_OK)
         return st;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) {
-        cudaGetLastError();
-        return NORM_ERR_CUDA;
-    }
+    unsigned *w = stream_err(*d, stream);
     unsigned word = 0;
-    if (cudaMemcpy(&word, d->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    // stream-ordered: waits for this stream's work only
+    if (cudaMemcpyAsync(&word, w, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
     }
     if (word == 0)
         return NORM_OK;
-    if (cudaMemset(d->err, 0, sizeof(unsigned)) != cudaSuccess) {
+    if (cudaMemsetAsync(w, 0, sizeof(unsigned), stream) != cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
     }
     if (word == NORM_ERR_TIMEOUT) {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (d->ws && cudaMemset(d->ws, 0, d->ws_bytes) != cudaSuccess) {
+        if (d->ws && cudaMemsetAsync(d->ws, 0, d->ws_bytes, stream) != cudaSuccess) {
             cudaGetLastError();
             return NORM_ERR_CUDA;
         }
     }
-    if (cudaDeviceSynchronize() != cudaSuccess) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
         cudaGetLastError();
         return NORM_ERR_CUDA;
     }

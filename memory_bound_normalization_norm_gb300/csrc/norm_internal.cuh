@@ -733,3 +733,15 @@ cudaError_t rms_channel_launch(const void *x, void *y, int64_t B, int64_t C, int
                                cudaStream_t stream);
 
 } // namespace normk
+
+namespace normapi {
+// Validate a LayerNorm call on esz-byte elements (4 = fp32, 2 = bf16) and
+// choose its path exactly as norm_layer_fwd would (current device, current
+// options), launching nothing.  *ws_bytes = the workspace bytes that path
+// uses: 0 for the row kernel and the cluster kernel, the header and tagged
+// records for the persistent kernel, the header and per-chunk partials for
+// the two-kernel path.  Returns the status norm_layer_fwd would return for
+// the same arguments before its launch.
+norm_status_t layer_fwd_workspace_need(const void *x, const void *gamma, const void *beta, const void *y,
+                                       int64_t rows, int64_t row_len, float eps, int esz, size_t *ws_bytes);
+} // namespace normapi

@@ -57,3 +57,31 @@ def assert_parity(got, want, what: str, tol: float = TOL):
     err = scaled_error(got, want)
     assert err <= tol, f"{what}: max scaled error {err:.3e} > {tol:.1e}"
     return err
+
+
+# ------------------------------------------------------------------ bfloat16
+
+def bf16_device(a: np.ndarray) -> torch.Tensor:
+    """float32 values on the device as bfloat16 (rounded to nearest even on the host)."""
+    import normgen
+    return torch.from_numpy(normgen.bf16_bits(a).view(np.int16)).to(dev()).view(torch.bfloat16)
+
+
+def bf16_values(t: torch.Tensor) -> np.ndarray:
+    """float32 values of a bfloat16 device tensor (exact)."""
+    import normgen
+    return normgen.bf16_to_f32(t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def assert_bf16_parity(got, want, what):
+    """|y - y_ref| <= 2^-8 |y_ref| + 1e-4 (1 + |y_ref|) elementwise: the bfloat16 rounding of the
+    result plus the fp32 tolerance."""
+    got = np.asarray(got, dtype=np.float64).reshape(-1)
+    want = np.asarray(want, dtype=np.float64).reshape(-1)
+    bound = 2.0**-8 * np.abs(want) + TOL * (1.0 + np.abs(want))
+    err = np.abs(got - want)
+    bad = ~(err <= bound)
+    if bad.any():
+        k = int(np.argmax(np.where(bad, err - bound, -np.inf)))
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of bound, worst at {k}: "
+                             f"got {got[k]}, want {want[k]}")

@@ -19,6 +19,7 @@ import torch
 
 import normgen
 import oracle
+from gpu_util import assert_bf16_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -52,16 +53,6 @@ class BGuarded:
     def guards_intact(self) -> bool:
         bits = self.buf.view(torch.int16).cpu().numpy().view(np.uint16)
         return bool((bits[:self.lo] == SENTINEL).all() and (bits[self.lo + self.n:] == SENTINEL).all())
-
-
-def assert_bf16_parity(got, want, what):
-    got = np.asarray(got, dtype=np.float64).reshape(-1)
-    want = np.asarray(want, dtype=np.float64).reshape(-1)
-    bound = 2.0**-8 * np.abs(want) + 1e-4 * (1.0 + np.abs(want))
-    err = np.abs(got - want)
-    bad = ~(err <= bound)
-    assert not bad.any(), (f"{what}: {int(bad.sum())} elements out of bound, worst at {int(np.argmax(err - bound))}: "
-                           f"got {got[np.argmax(err - bound)]}, want {want[np.argmax(err - bound)]}")
 
 
 def bf16_inputs(n, mean=0.0, std=1.0, seed=0, tensor_id=0):

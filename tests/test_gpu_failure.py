@@ -8,6 +8,8 @@
 2. A 1 ns limit makes the other waits give up too (a row's bulk copy, the
    gamma/beta copies): the CTA still records the error and drains its copies;
    every element of y is then either untouched or correct.
+3. Error words are per stream: a timeout on one stream is reported by
+   norm_last_error on that stream only.
 """
 import pytest
 import torch
@@ -87,3 +89,22 @@ def test_tiny_wait_limit_aborts_cleanly(ng):
     ng.norm_layer_fwd(xb.t, gb.t, bb.t, yb.t, rows, L, 1e-5)
     assert ng.norm_last_error() == 0
     assert_parity(yb.numpy(), want.reshape(-1), "LN after the aborted calls")
+
+
+def test_error_word_is_per_stream(ng):
+    rows, L = 3, 152 * 4 * 64
+    xb, yb = Guarded(rows * L, normgen.normal(rows * L, seed=9)), Guarded(rows * L)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    assert ng.norm_last_error(sa) == 0 and ng.norm_last_error(sb) == 0
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, 1)
+    ng.norm_set_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS, 2_000_000)
+    ng.norm_set_option(ng.NORM_OPT_BARRIER_EXTRA_ARRIVALS, 1)
+    torch.cuda.synchronize()
+    ng.norm_layer_fwd(xb.t, None, None, yb.t, rows, L, 1e-5, stream=sa)
+    ng.norm_set_option(ng.NORM_OPT_BARRIER_EXTRA_ARRIVALS, 0)
+    ng.norm_set_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS, 200_000_000)
+    sa.synchronize()
+    assert ng.norm_last_error(sb) == 0, "a timeout on another stream must not be reported here"
+    assert ng.norm_last_error() == 0, "nor on the current stream"
+    assert ng.norm_last_error(sa) == ng.NORM_ERR_TIMEOUT
+    assert ng.norm_last_error(sa) == 0

@@ -139,6 +139,41 @@ def test_layer_norm_deterministic(ng):
     assert a.tobytes() == c.tobytes()
 
 
+def test_persistent_exchange_200_launches_back_to_back(ng):
+    """The grid exchange across 200 persistent launches queued back to back on one
+    stream and one caller workspace, with no synchronization between them.  The
+    inputs cycle through 8 seeded tensors of different means and spreads, so a
+    record read from the wrong row, the wrong slot or the previous launch (a stale
+    or torn word accepted by its tag) would give visibly wrong statistics.  Each
+    launch writes its own output; every element of every output is compared with
+    the oracle.  6 rows a launch cycle the 4 record slots 300 times and the tags
+    through 1,200 rows."""
+    rows, L, launches, distinct = 6, 1 << 20, 200, 8
+    sets, wants = [], []
+    for k in range(distinct):
+        x, g, b = inputs(rows, L, seed=500 + k, mean=3.0 * k - 10.0, std=0.5 + k)
+        sets.append((device(x), device(g), device(b)))
+        wants.append(oracle.layer_norm(x, g, b, rows, L))
+    nbytes = ng.norm_layer_workspace_bytes(rows, L)
+    ws = torch.zeros((nbytes + 255) // 4 + 64, dtype=torch.float32, device="cuda")
+    ys = torch.full((launches, rows * L), float("nan"), dtype=torch.float32, device="cuda")
+    ng.norm_set_option(ng.NORM_OPT_LN_PATH, PERSISTENT)
+    try:
+        for i in range(launches):
+            xd, gd, bd = sets[i % distinct]
+            ng.norm_layer_fwd(xd, gd, bd, ys[i], rows, L, 1e-5, ws, nbytes)
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_LN_PATH, AUTO)
+    assert ng.norm_last_error() == 0
+    for k in range(distinct):
+        want = torch.from_numpy(wants[k].astype(np.float64)).cuda()
+        got = ys[k::distinct].double()
+        err = ((got - want).abs() / (1.0 + want.abs())).amax(dim=1)
+        assert bool(torch.isfinite(got).all()), f"input {k}: a launch left NaN in its output"
+        worst = float(err.max())
+        assert worst <= TOL, f"input {k}: worst launch {int(err.argmax()) * distinct + k} scaled error {worst:.3e}"
+
+
 def test_layer_norm_empty_is_noop(ng):
     yb = Guarded(16)
     ng.norm_layer_fwd(None, None, None, yb.t, 0, 16, 1e-5)

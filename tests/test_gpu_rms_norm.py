@@ -2,9 +2,9 @@
 
 Covers every register-resident channel bucket (exact and ragged C up to 128),
 the two-read kernel (C > 128), odd spatial sizes, in place, misaligned pointers,
-the small (2, 64, 32, 32) workload in full, and the (112, 64, 512, 512) workload
-(7.5 GB in) on sampled outputs: whole batch entries at both ends and the middle
-plus random positions, each recomputed by the oracle from regenerated inputs.
+and the small (2, 64, 32, 32) workload in full.  The (112, 64, 512, 512) workload
+(7.5 GB in) is compared element by element, one batch entry at a time, in
+test_gpu_bench_shapes.py.
 """
 import numpy as np
 import pytest
@@ -78,31 +78,3 @@ def test_many_batches_fold_grid(ng):
     B, C, S = 70000, 4, 3
     x = normgen.normal(B * C * S, seed=7)
     assert_parity(run_rms(ng, x, B, C, S), oracle.rms_channel(x, B, C, S), "RMS 70000 batches")
-
-
-@pytest.mark.slow
-def test_full_size_sampled(ng):
-    """(112, 64, 512, 512), x ~ N(0,1) seed 0: 1.88e9 elements, int64 indexing throughout."""
-    B, C, S = 112, 64, 512 * 512
-    n = B * C * S
-    x = normgen.normal(n, seed=0, tensor_id=0)
-    xd = torch.from_numpy(x).to("cuda")
-    yd = torch.empty_like(xd)
-    ng.norm_rms_channel_fwd(xd, yd, B, C, S, 1e-5)
-    torch.cuda.synchronize()
-    del xd
-    # whole batch entries: first, middle, last
-    for b in (0, 57, B - 1):
-        sl = slice(b * C * S, (b + 1) * C * S)
-        want = oracle.rms_channel(x[sl], 1, C, S)
-        assert_parity(yd[sl].cpu().numpy(), want, f"RMS full size batch {b}")
-    # random positions anywhere, inputs regenerated from the stream one channel at a time
-    rng = np.random.default_rng(0)
-    bs = rng.integers(0, B, 512)
-    ss = rng.integers(0, S, 512)
-    idx = (bs[:, None] * C * S + np.arange(C)[None, :] * S + ss[:, None]).astype(np.int64)
-    cols = np.stack([np.concatenate([normgen.normal(1, seed=0, tensor_id=0, start=int(i)) for i in row])
-                     for row in idx])
-    want = np.stack([oracle.rms_channel(cols[k], 1, C, 1) for k in range(len(bs))])
-    got = yd[torch.from_numpy(idx.ravel()).to("cuda")].cpu().numpy().reshape(want.shape)
-    assert_parity(got, want, "RMS full size sampled positions")
