@@ -6,7 +6,8 @@ depends only on ``(seed, tensor_id, i)``, so any sub-range can be produced on it
 own and the bytes do not depend on the thread count.  Nothing in this module
 computes any part of a normalization.
 
-Tensor ids used throughout the repository: 0 = x, 1 = gamma, 2 = beta.
+Tensor ids used throughout the repository: 0 = x, 1 = gamma, 2 = beta, and for the
+Linear that feeds GroupNorm 3 = its weight W, 4 = its bias.
 """
 from __future__ import annotations
 
@@ -26,6 +27,8 @@ _LIB = os.path.join(_LIB_DIR, "libnormgen.so")
 TENSOR_X = 0
 TENSOR_GAMMA = 1
 TENSOR_BETA = 2
+TENSOR_W = 3
+TENSOR_LIN_BIAS = 4
 
 _lock = threading.Lock()
 _lib = None

@@ -89,6 +89,8 @@ class Oracle:
         lib.oracle_group_lrelu_x2.argtypes = [vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp, ci]
         lib.oracle_group_lrelu_x2_nchw.restype = ci
         lib.oracle_group_lrelu_x2_nchw.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, vp, vp, ci]
+        lib.oracle_linear_group_lrelu_x2.restype = ci
+        lib.oracle_linear_group_lrelu_x2.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, dbl, dbl, vp, vp, ci]
         self._lib = lib
 
     @staticmethod
@@ -153,6 +155,23 @@ class Oracle:
         return y64 if f64 else y32
 
 
+    def linear_group_lrelu_x2(self, x, w, bias, gamma, beta, Mr, K, N, G, eps=1e-5, slope=0.01, *, f64=False,
+                              threads=None):
+        """2 * LeakyReLU(GroupNorm(x W^T + bias)): x [Mr][K], W [N][K] (nn.Linear's layout), bias
+        gamma, beta [N] (or None); G groups of N/G contiguous channels."""
+        x = _f32(x, "x")
+        w = _f32(w, "w")
+        if x.size != Mr * K or w.size != N * K:
+            raise ValueError("x or w has the wrong size")
+        bb, g, b = _opt_f32(bias), _opt_f32(gamma), _opt_f32(beta)
+        y64, y32 = self._outputs((Mr * N,), f64)
+        rc = self._lib.oracle_linear_group_lrelu_x2(_ptr(x), _ptr(w), _ptr(bb), _ptr(g), _ptr(b), Mr, K, N, G, eps,
+                                                    slope, _ptr(y64), _ptr(y32), threads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_linear_group_lrelu_x2 rejected its arguments ({rc})")
+        return y64 if f64 else y32
+
+
 def get() -> Oracle:
     """The oracle built from ``norm_oracle.c`` as committed."""
     global _default
@@ -187,3 +206,7 @@ def group_lrelu_x2(*a, **k):
 
 def group_lrelu_x2_nchw(*a, **k):
     return get().group_lrelu_x2_nchw(*a, **k)
+
+
+def linear_group_lrelu_x2(*a, **k):
+    return get().linear_group_lrelu_x2(*a, **k)

@@ -6,7 +6,8 @@
  * shares no code, header, table or helper with it, and neither includes
  * the other.
  *
- * Every function takes the fp32 input bytes the GPU sees, promotes them to
+ * Every function takes the fp32 input bytes the GPU sees (for the Linear:
+ * the bfloat16 values of x and W, widened exactly to float), promotes them to
  * double, evaluates the operation's textbook definition in double with an
  * explicit two-pass variance, and writes the result in double (y64) and/or
  * rounded once to float (y32).  Either output pointer may be NULL.
@@ -29,6 +30,12 @@
  *  - RMSNorm: transcript "Kimi-K2.6 l1_p36", reference model quoted in the
  *    analysis turn: rms = sqrt(mean(x^2, dim=1) + eps), y = x / rms, over
  *    dim 1 of an NCHW tensor whose trailing dims flatten to S = H*W.
+ *  - Linear, then GroupNorm + LeakyReLU + x+x: transcript "Kimi-K2.6
+ *    l2_p62", the module and its forward as the page writes them:
+ *    h = F.linear(x, W, b) = x W^T + b with W [out][in] as nn.Linear stores
+ *    it, then the GroupNorm + LeakyReLU + x+x above on each row of h (the
+ *    page's first design turn weighs computing the group statistics in the
+ *    GEMM's epilogue).
  *
  * Pins (tests/test_oracle_pins.py): exact rational brute force on tiny
  * inputs, closed forms (constant rows, affine invariance, two-valued rows,
@@ -40,6 +47,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <stdlib.h>
 
 #define ORACLE_OK 0
 #define ORACLE_BAD_ARG -1
@@ -201,4 +209,66 @@ int oracle_group_lrelu_x2_nchw(const float *x, const float *gamma, const float *
         }
     }
     return ORACLE_OK;
+}
+
+/* Linear, then GroupNorm + LeakyReLU + x+x.  x[Mr][K] (rows), w[N][K] (the
+ * Linear's weight, one row per output channel), bias [N] or NULL (0):
+ *     h[m][n] = sum_k x[m][k] * w[n][k] + bias[n]
+ * in double, summed in order of k; then each row h[m][0..N-1] goes through
+ * the GroupNorm + LeakyReLU + x+x of oracle_group_lrelu_x2 (G groups of N/G
+ * contiguous channels, gamma/beta [N] or NULL), with h kept in double. */
+int oracle_linear_group_lrelu_x2(const float *x, const float *w, const float *bias,
+                                 const float *gamma, const float *beta,
+                                 int64_t Mr, int64_t K, int64_t N, int64_t G, double eps, double slope,
+                                 double *y64, float *y32, int threads)
+{
+    if (!x || !w || Mr < 0 || K <= 0 || N <= 0 || G <= 0 || N % G != 0 || !(eps >= 0.0) ||
+        (!y64 && !y32))
+        return ORACLE_BAD_ARG;
+    if (threads < 1)
+        threads = 1;
+    const int64_t M = N / G;
+    int bad = 0;
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 1)
+    for (int64_t m = 0; m < Mr; ++m) {
+        double *h = (double *)malloc((size_t)N * sizeof(double));
+        if (!h) {
+#pragma omp atomic write
+            bad = 1;
+            continue;
+        }
+        const float *xm = x + m * K;
+        /* the Linear: one dot product of length K per output channel */
+        for (int64_t n = 0; n < N; ++n) {
+            const float *wn = w + n * K;
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)xm[k] * (double)wn[k];
+            h[n] = acc + (bias ? (double)bias[n] : 0.0);
+        }
+        /* GroupNorm over groups of M contiguous channels, then LeakyReLU, then x+x */
+        for (int64_t g = 0; g < G; ++g) {
+            const int64_t c0 = g * M;
+            double sum = 0.0;
+            for (int64_t j = 0; j < M; ++j)
+                sum += h[c0 + j];
+            const double mean = sum / (double)M;
+            double sq = 0.0;
+            for (int64_t j = 0; j < M; ++j) {
+                const double d = h[c0 + j] - mean;
+                sq += d * d;
+            }
+            const double denom = sqrt(sq / (double)M + eps);
+            for (int64_t j = 0; j < M; ++j) {
+                const int64_t c = c0 + j;
+                const double gw = gamma ? (double)gamma[c] : 1.0;
+                const double bw = beta ? (double)beta[c] : 0.0;
+                const double t = (h[c] - mean) / denom * gw + bw;
+                const double l = fmax(0.0, t) + slope * fmin(0.0, t);
+                oracle_store(l + l, m * N + c, y64, y32);
+            }
+        }
+        free(h);
+    }
+    return bad ? ORACLE_BAD_ARG : ORACLE_OK;
 }

@@ -130,6 +130,33 @@ def exact_group_lrelu_x2_nchw(x, gamma, beta, N, C, S, G, eps, slope):
     return out
 
 
+def exact_linear_group_lrelu_x2(x, w, bias, gamma, beta, Mr, K, N, G, eps, slope):
+    """h = x W^T + bias exactly (Fractions), then the GroupNorm + LeakyReLU + x+x of each row of h."""
+    x = np.asarray(x, dtype=np.float32).reshape(Mr, K)
+    w = np.asarray(w, dtype=np.float32).reshape(N, K)
+    M = N // G
+    out = np.empty((Mr, N), dtype=np.float64)
+    fe, fs = Fraction(eps), Fraction(slope)
+    for m in range(Mr):
+        h = []
+        for n in range(N):
+            acc = sum(Fraction(float(x[m, k])) * Fraction(float(w[n, k])) for k in range(K))
+            h.append(acc + (Fraction(float(bias[n])) if bias is not None else Fraction(0)))
+        for g in range(G):
+            hs = h[g * M:(g + 1) * M]
+            mean = sum(hs) / M
+            var = sum((v - mean) ** 2 for v in hs) / M
+            den = _dsqrt(var + fe)
+            for j, v in enumerate(hs):
+                c = g * M + j
+                gw = Fraction(float(gamma[c])) if gamma is not None else Fraction(1)
+                bw = Fraction(float(beta[c])) if beta is not None else Fraction(0)
+                t = _dec(v - mean) / den * _dec(gw) + _dec(bw)
+                l = t if t > 0 else _dec(fs) * t
+                out[m, c] = float(l + l)
+    return out
+
+
 # ----------------------------------------------------------------------------- LayerNorm
 
 def layer_norm_pins(o) -> None:
@@ -386,9 +413,82 @@ def group_lrelu_x2_nchw_pins(o) -> None:
     _close(o.group_lrelu_x2_nchw(x, g, b, 2, 8, 5, 2, EPS, 0.01, f64=True), want, 0.0, "GN NCHW constant group")
 
 
+# ----------------------------------------------------------------------------- Linear + GroupNorm
+
+def linear_group_lrelu_x2_pins(o) -> None:
+    rng = np.random.default_rng(20241203)
+
+    # 1. exact brute force: h = x W^T + bias in Fractions, then the group statistics
+    for (Mr, K, N, G) in ((2, 3, 4, 2), (3, 5, 8, 4), (1, 8, 6, 3), (2, 4, 4, 1), (3, 2, 6, 6)):
+        x = _dyadic(rng, Mr * K)
+        w = _dyadic(rng, N * K, k=32, den=8)
+        bias = _dyadic(rng, N, k=32, den=8)
+        g = _dyadic(rng, N, k=32, den=8)
+        b = _dyadic(rng, N, k=32, den=8)
+        for slope in (0.01, 0.25):
+            want = exact_linear_group_lrelu_x2(x, w, bias, g, b, Mr, K, N, G, EPS, slope).reshape(-1)
+            got = o.linear_group_lrelu_x2(x, w, bias, g, b, Mr, K, N, G, EPS, slope, f64=True)
+            _close(got, want, 1e-11, f"Linear+GN brute force {(Mr, K, N, G)} slope={slope}")
+        assert np.array_equal(o.linear_group_lrelu_x2(x, w, bias, g, b, Mr, K, N, G, EPS, 0.01),
+                              o.linear_group_lrelu_x2(x, w, bias, g, b, Mr, K, N, G, EPS, 0.01,
+                                                      f64=True).astype(np.float32)), "Linear+GN fp32 rounding"
+
+    # 2. reductions to the (pinned) GroupNorm oracle, bit for bit:
+    #    a permutation weight (not symmetric) selects channels: h[m][n] = x[m][perm[n]]
+    Mr, K, G = 5, 48, 6
+    x = normgen.normal(Mr * K, seed=11)
+    g = normgen.normal(K, 1.0, 0.1, seed=11, tensor_id=1)
+    b = normgen.normal(K, 0.0, 0.1, seed=11, tensor_id=2)
+    perm = rng.permutation(K)
+    assert np.any(perm[perm] != np.arange(K)), "the permutation must not be its own inverse"
+    w = np.zeros((K, K), dtype=np.float32)
+    w[np.arange(K), perm] = 1.0
+    want = o.group_lrelu_x2(x.reshape(Mr, K)[:, perm].copy(), g, b, Mr, K, G, EPS, 0.01, f64=True).reshape(-1)
+    assert np.array_equal(o.linear_group_lrelu_x2(x, w, None, g, b, Mr, K, K, G, EPS, 0.01, f64=True), want), \
+        "Linear+GN with a permutation weight"
+    #    a zero weight leaves the bias: every row is the GroupNorm of the bias
+    N = 24
+    bias = normgen.normal(N, 0.0, 2.0, seed=12, tensor_id=4)
+    g2 = normgen.normal(N, 1.0, 0.1, seed=12, tensor_id=1)
+    b2 = normgen.normal(N, 0.0, 0.1, seed=12, tensor_id=2)
+    want = o.group_lrelu_x2(np.tile(bias, 3), g2, b2, 3, N, 4, EPS, 0.01, f64=True)
+    got = o.linear_group_lrelu_x2(normgen.normal(3 * 7, seed=13), np.zeros((N, 7), np.float32), bias, g2, b2,
+                                  3, 7, N, 4, EPS, 0.01, f64=True)
+    assert np.array_equal(got, want), "Linear+GN with a zero weight"
+
+    # 3. third voice: float64 torch F.linear -> group_norm -> leaky_relu -> x + x
+    import torch
+    Mr, K, N, G = 6, 40, 32, 4
+    x = normgen.normal(Mr * K, seed=14)
+    w = normgen.uniform(N * K, -K ** -0.5, K ** -0.5, seed=14, tensor_id=3)
+    bias = normgen.uniform(N, -K ** -0.5, K ** -0.5, seed=14, tensor_id=4)
+    g = normgen.normal(N, 1.0, 0.1, seed=14, tensor_id=1)
+    b = normgen.normal(N, 0.0, 0.1, seed=14, tensor_id=2)
+    d = lambda a: torch.from_numpy(a.astype(np.float64))  # noqa: E731
+    h = torch.nn.functional.linear(d(x).reshape(Mr, K), d(w).reshape(N, K), d(bias))
+    t = torch.nn.functional.group_norm(h, G, d(g), d(b), EPS)
+    for slope in (0.01, 1.0):
+        l = torch.nn.functional.leaky_relu(t, slope)
+        _close(o.linear_group_lrelu_x2(x, w, bias, g, b, Mr, K, N, G, EPS, slope, f64=True),
+               (l + l).numpy().reshape(-1), 1e-12, f"Linear+GN vs torch slope={slope}")
+
+    # 4. invariant: gamma=1, beta=0, slope=1: y/2 per group has mean 0 and population
+    #    variance var/(var+eps), var taken from h = x W^T + bias (float64 matmul)
+    Mr, K, N, G = 4, 24, 32, 8
+    x = normgen.normal(Mr * K, 1.0, 2.0, seed=15)
+    w = normgen.normal(N * K, seed=15, tensor_id=3)
+    bias = normgen.normal(N, seed=15, tensor_id=4)
+    y = o.linear_group_lrelu_x2(x, w, bias, None, None, Mr, K, N, G, EPS, 1.0, f64=True).reshape(Mr, G, -1) / 2.0
+    hd = (x.astype(np.float64).reshape(Mr, K) @ w.astype(np.float64).reshape(N, K).T + bias).reshape(Mr, G, -1)
+    var = np.mean((hd - hd.mean(axis=2, keepdims=True)) ** 2, axis=2)
+    assert np.max(np.abs(y.mean(axis=2))) < 1e-13, "Linear+GN group mean"
+    assert np.max(np.abs(np.mean(y * y, axis=2) - var / (var + EPS))) < 1e-12, "Linear+GN group variance"
+
+
 ALL_PINS = {
     "layer_norm": layer_norm_pins,
     "rms_channel": rms_channel_pins,
     "group_lrelu_x2": group_lrelu_x2_pins,
     "group_lrelu_x2_nchw": group_lrelu_x2_nchw_pins,
+    "linear_group_lrelu_x2": linear_group_lrelu_x2_pins,
 }

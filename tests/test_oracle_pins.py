@@ -53,7 +53,9 @@ MUTANTS = [
     ("group_lrelu_x2", "unbiased variance", "const double var = sq / (double)M;", "const double var = sq / (double)(M + 1);"),
     ("group_lrelu_x2", "eps outside sqrt", "const double denom = sqrt(var + eps);\n            for (int64_t j",
      "const double denom = sqrt(var) + eps;\n            for (int64_t j"),
-    ("group_lrelu_x2", "slope on positive side", "fmax(0.0, t) + slope * fmin(0.0, t)", "slope * fmax(0.0, t) + fmin(0.0, t)"),
+    ("group_lrelu_x2", "slope on positive side",
+     "const double l = fmax(0.0, t) + slope * fmin(0.0, t);\n                oracle_store(l + l, n * C + c",
+     "const double l = slope * fmax(0.0, t) + fmin(0.0, t);\n                oracle_store(l + l, n * C + c"),
     ("group_lrelu_x2", "x+x dropped", "oracle_store(l + l, n * C + c, y64, y32);", "oracle_store(l, n * C + c, y64, y32);"),
     ("group_lrelu_x2", "gamma per group", "const double w = gamma ? (double)gamma[c] : 1.0;", "const double w = gamma ? (double)gamma[g] : 1.0;"),
     ("group_lrelu_x2", "beta dropped", "const double t = ((double)xg[j] - mean) / denom * w + b;",
@@ -65,13 +67,30 @@ MUTANTS = [
      "sum += (double)x[(n * S + s) * C + c];"),
     ("group_lrelu_x2_nchw", "eps outside sqrt", "const double denom = sqrt(sq / cnt + eps);",
      "const double denom = sqrt(sq / cnt) + eps;"),
-    ("group_lrelu_x2_nchw", "gamma per group", "const double gw = gamma ? (double)gamma[c] : 1.0;",
-     "const double gw = gamma ? (double)gamma[c0] : 1.0;"),
+    ("group_lrelu_x2_nchw", "gamma per group",
+     "const double gw = gamma ? (double)gamma[c] : 1.0;\n                const double bw = beta ? (double)beta[c] : 0.0;\n                for (int64_t s",
+     "const double gw = gamma ? (double)gamma[c0] : 1.0;\n                const double bw = beta ? (double)beta[c] : 0.0;\n                for (int64_t s"),
     ("group_lrelu_x2_nchw", "beta per position", "const double v = ((double)x[i] - mean) / denom * gw + bw;",
      "const double v = ((double)x[i] - mean) / denom * gw + (beta ? (double)beta[(c0 + s) % C] : 0.0);"),
     ("group_lrelu_x2_nchw", "slope on positive side", "fmax(0.0, v) + slope * fmin(0.0, v)",
      "slope * fmax(0.0, v) + fmin(0.0, v)"),
     ("group_lrelu_x2_nchw", "x+x dropped", "oracle_store(l + l, i, y64, y32);", "oracle_store(l, i, y64, y32);"),
+    ("linear_group_lrelu_x2", "weight transposed", "acc += (double)xm[k] * (double)wn[k];",
+     "acc += (double)xm[k] * (double)w[(k * N + n) % (N * K)];"),
+    ("linear_group_lrelu_x2", "last k skipped", "for (int64_t k = 0; k < K; ++k)\n                acc +=",
+     "for (int64_t k = 0; k < K - 1; ++k)\n                acc +="),
+    ("linear_group_lrelu_x2", "bias dropped", "h[n] = acc + (bias ? (double)bias[n] : 0.0);", "h[n] = acc;"),
+    ("linear_group_lrelu_x2", "bias by row", "h[n] = acc + (bias ? (double)bias[n] : 0.0);",
+     "h[n] = acc + (bias ? (double)bias[m % N] : 0.0);"),
+    ("linear_group_lrelu_x2", "x row 0 for every row", "const float *xm = x + m * K;", "const float *xm = x + 0 * K;"),
+    ("linear_group_lrelu_x2", "strided groups", "sum += h[c0 + j];", "sum += h[(g + j * G) % N];"),
+    ("linear_group_lrelu_x2", "unbiased variance", "sqrt(sq / (double)M + eps)", "sqrt(sq / (double)(M + 1) + eps)"),
+    ("linear_group_lrelu_x2", "gamma per group", "const double gw = gamma ? (double)gamma[c] : 1.0;\n                const double bw = beta ? (double)beta[c] : 0.0;\n                const double t = (h[c]",
+     "const double gw = gamma ? (double)gamma[g] : 1.0;\n                const double bw = beta ? (double)beta[c] : 0.0;\n                const double t = (h[c]"),
+    ("linear_group_lrelu_x2", "slope on positive side",
+     "const double l = fmax(0.0, t) + slope * fmin(0.0, t);\n                oracle_store(l + l, m * N + c",
+     "const double l = slope * fmax(0.0, t) + fmin(0.0, t);\n                oracle_store(l + l, m * N + c"),
+    ("linear_group_lrelu_x2", "x+x dropped", "oracle_store(l + l, m * N + c, y64, y32);", "oracle_store(l, m * N + c, y64, y32);"),
     ("group_lrelu_x2_nchw", "variance about zero", "const double d = (double)x[(n * C + c) * S + s] - mean;",
      "const double d = (double)x[(n * C + c) * S + s];"),
 ]
