@@ -2,14 +2,17 @@
  * norm.h - C ABI of libnormgb300.so: fp32 reduce-then-apply normalization on
  * NVIDIA GB300 (sm_103a).
  *
- * Four operations, each one stream-ordered launch sequence of the library's
+ * Five operations, each one stream-ordered launch sequence of the library's
  * own CUDA kernels:
  *
- *   norm_layer_fwd                LayerNorm over very long contiguous rows
- *   norm_rms_channel_fwd          RMSNorm over dim 1 of an NCHW tensor
- *   norm_group_lrelu_x2_fwd       per-row GroupNorm, then LeakyReLU, then x + x
- *   norm_group_lrelu_x2_nchw_fwd  the same over an NCHW tensor (groups span
- *                                 channels and positions)
+ *   norm_layer_fwd                  LayerNorm over very long contiguous rows
+ *   norm_rms_channel_fwd            RMSNorm over dim 1 of an NCHW tensor
+ *   norm_group_lrelu_x2_fwd         per-row GroupNorm, then LeakyReLU, then x + x
+ *   norm_group_lrelu_x2_nchw_fwd    the same over an NCHW tensor (groups span
+ *                                   channels and positions)
+ *   norm_linear_group_lrelu_x2_fwd  a Linear (tensor-core GEMM) with the
+ *                                   GroupNorm + LeakyReLU + x + x in its
+ *                                   epilogue
  *
  * Conventions shared by every entry point:
  *   - Pointers named x, y, gamma, beta, workspace are DEVICE pointers on the
@@ -272,6 +275,39 @@ norm_status_t norm_group_lrelu_x2_nchw_fwd_bf16(const uint16_t *x, const uint16_
                                                 uint16_t *y, int64_t N, int64_t C, int64_t S, int64_t num_groups,
                                                 float eps, float negative_slope, void *workspace,
                                                 size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------- Linear + GroupNorm + LeakyReLU + x + x
+ * The GroupNorm page's whole module (POPCORNBENCH transcript "Kimi-K2.6
+ * l2_p62": forward = F.linear(x, W, bias), then GroupNorm + LeakyReLU + x + x
+ * as in norm_group_lrelu_x2_fwd; the page's first design turn weighs
+ * computing the group statistics in the GEMM's epilogue), in one kernel:
+ *     h[m][n] = sum_k x[m][k] * W[n][k] + bias[n]
+ *     y[m][.] = norm_group_lrelu_x2 of the row h[m][.] (groups of N/num_groups
+ *               contiguous channels, gamma/beta per channel)
+ * h is never written to memory: the group statistics are taken in the
+ * epilogue of the tensor-core GEMM, from its fp32 accumulators.
+ *
+ * x        [M][K] bfloat16 (uint16_t bit patterns), contiguous.
+ * W        [N][K] bfloat16, contiguous: one row per output channel, the layout
+ *          nn.Linear stores its weight in.
+ * bias, gamma, beta  [N] fp32, or NULL (0, 1 and 0).
+ * y        [M][N] fp32, contiguous; must not overlap any input.
+ * Products are exact in fp32 and accumulated in fp32 by the tensor cores (in
+ * an order of their own); the epilogue is fp32 (two-pass group statistics).
+ * This is a bfloat16-input form: the pages' fp32 Linear is not reproduced
+ * bit for bit, and results match a float64 evaluation on the same bfloat16
+ * values within 1e-4 (1 + |y|).
+ * Requirements (NORM_ERR_UNSUPPORTED otherwise): x, W and y 16-byte aligned,
+ * K a multiple of 8, N / num_groups one of 16, 32 or 64, and M, N, K below
+ * 2^31.  Any M and N (multiples of the group size) are served; rows and
+ * channels past a 128 x 256 tile edge are masked.  Nothing is allocated.
+ * Waits inside the kernel are bounded by NORM_OPT_BARRIER_TIMEOUT_NS (a
+ * timeout is reported by norm_last_error on the stream).
+ */
+norm_status_t norm_linear_group_lrelu_x2_fwd(const uint16_t *x, const uint16_t *w, const float *bias,
+                                             const float *gamma, const float *beta, float *y, int64_t M, int64_t K,
+                                             int64_t N, int64_t num_groups, float eps, float negative_slope,
+                                             cudaStream_t stream);
 
 /* ------------------------------------------------------------------ status
  * Every stream has its own error word on each device (the first 255 streams

@@ -16,6 +16,9 @@ Entry points (same names and argument order as the C functions):
   workspace=None, workspace_bytes=0, stream=None)``
 * ``norm_layer_fwd_bf16``, ``norm_rms_channel_fwd_bf16``, ``norm_group_lrelu_x2_fwd_bf16``,
   ``norm_group_lrelu_x2_nchw_fwd_bf16``: the same arguments with bfloat16 tensors
+* ``norm_linear_group_lrelu_x2_fwd(x, w, bias, gamma, beta, y, M, K, N, num_groups, eps,
+  negative_slope, stream=None)``: a Linear with GroupNorm + LeakyReLU + x2 in its epilogue
+  (bfloat16 x and w, float32 bias/gamma/beta and y)
 * ``norm_last_error(stream=None)``, ``norm_layer_workspace_bytes(rows, row_len)``,
   ``norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, num_groups)``,
   ``norm_layer_workspace_reset(ws, nbytes, stream=None)``, ``norm_set_option``,
@@ -65,6 +68,7 @@ EXPORTED = (
     "norm_group_lrelu_x2_nchw_workspace_bytes",
     "norm_group_lrelu_x2_nchw_fwd",
     "norm_group_lrelu_x2_nchw_fwd_bf16",
+    "norm_linear_group_lrelu_x2_fwd",
     "norm_last_error",
     "norm_status_string",
     "norm_set_option",
@@ -114,6 +118,8 @@ _lib.norm_group_lrelu_x2_nchw_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64
 for _name in ("norm_group_lrelu_x2_nchw_fwd", "norm_group_lrelu_x2_nchw_fwd_bf16"):
     getattr(_lib, _name).restype = _int
     getattr(_lib, _name).argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _vp, _sz, _vp]
+_lib.norm_linear_group_lrelu_x2_fwd.restype = _int
+_lib.norm_linear_group_lrelu_x2_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _vp]
 _lib.norm_last_error.restype = _int
 _lib.norm_last_error.argtypes = [_vp]
 _lib.norm_status_string.restype = ctypes.c_char_p
@@ -232,6 +238,15 @@ def norm_group_lrelu_x2_nchw_fwd_bf16(x, gamma, beta, y, N, C, S, num_groups, ep
                                                   _ptr(y, True), N, C, S, num_groups, eps, negative_slope,
                                                   _ptr(workspace), workspace_bytes, _stream(stream)),
            "norm_group_lrelu_x2_nchw_fwd_bf16")
+
+
+def norm_linear_group_lrelu_x2_fwd(x, w, bias, gamma, beta, y, M, K, N, num_groups, eps, negative_slope,
+                                   stream=None):
+    """2 * LeakyReLU(GroupNorm(x W^T + bias)) in one kernel: x [M][K] and w [N][K] bfloat16,
+    bias/gamma/beta [N] and y [M][N] float32."""
+    _check(_lib.norm_linear_group_lrelu_x2_fwd(_ptr(x, True), _ptr(w, True), _ptr(bias), _ptr(gamma), _ptr(beta),
+                                               _ptr(y), M, K, N, num_groups, eps, negative_slope, _stream(stream)),
+           "norm_linear_group_lrelu_x2_fwd")
 
 
 def norm_last_error(stream=None) -> int:

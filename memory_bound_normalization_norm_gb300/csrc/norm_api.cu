@@ -916,6 +916,62 @@ norm_status_t norm_group_lrelu_x2_nchw_fwd_bf16(const uint16_t *x, const uint16_
                               workspace_bytes, stream, 2, true);
 }
 
+norm_status_t norm_linear_group_lrelu_x2_fwd(const uint16_t *x, const uint16_t *w, const float *bias,
+                                             const float *gamma, const float *beta, float *y, int64_t M, int64_t K,
+                                             int64_t N, int64_t num_groups, float eps, float negative_slope,
+                                             cudaStream_t stream)
+{
+    int64_t mk = 0, nk = 0, mn = 0;
+    if (M < 0 || K < 0 || N < 0 || num_groups <= 0 || !valid_eps(eps) || !std::isfinite(negative_slope) ||
+        !safe_mul(M, K, &mk) || !safe_mul(N, K, &nk) || !safe_mul(M, N, &mn))
+        return NORM_ERR_INVALID_ARG;
+    if (N % num_groups != 0)
+        return NORM_ERR_INVALID_ARG;
+    if (mn == 0)
+        return NORM_OK;
+    if (K == 0 || !x || !w || !y)
+        return NORM_ERR_INVALID_ARG;
+    if (!aligned(x, 2) || !aligned(w, 2) || !aligned(y, 4) || !aligned(bias, 4) || !aligned(gamma, 4) ||
+        !aligned(beta, 4))
+        return NORM_ERR_MISALIGNED;
+    const size_t yb = static_cast<size_t>(mn) * 4, pb = static_cast<size_t>(N) * 4;
+    if (overlaps(x, static_cast<size_t>(mk) * 2, y, yb) || overlaps(w, static_cast<size_t>(nk) * 2, y, yb) ||
+        overlaps(bias, pb, y, yb) || overlaps(gamma, pb, y, yb) || overlaps(beta, pb, y, yb))
+        return NORM_ERR_INVALID_ARG;
+    // the tensor-core path: 16-byte aligned operands and rows (K % 8 == 0),
+    // groups of 16, 32 or 64 channels, extents that fit its 32-bit tile
+    // coordinates
+    const int64_t group = N / num_groups;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || K % 8 != 0 ||
+        !normk::linear_gn_group_size_ok(group) || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+        K >= (int64_t(1) << 31))
+        return NORM_ERR_UNSUPPORTED;
+    DeviceState *d = nullptr;
+    norm_status_t st = device_state(&d);
+    if (st != NORM_OK)
+        return st;
+    normk::LinGnParams p;
+    p.x = x;
+    p.w = w;
+    p.bias = bias;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.y = y;
+    p.Mr = M;
+    p.K = K;
+    p.N = N;
+    p.group = group;
+    p.eps = eps;
+    p.slope = negative_slope;
+    p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
+    p.err = stream_err(*d, stream);
+    if (normk::linear_gn_launch(p, d->sm_count, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return NORM_ERR_CUDA;
+    }
+    return NORM_OK;
+}
+
 norm_status_t norm_last_error(cudaStream_t stream)
 {
     DeviceState *d = nullptr;

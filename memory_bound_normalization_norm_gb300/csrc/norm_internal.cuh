@@ -728,6 +728,22 @@ cudaError_t gns_team_launch(const GnSegParams &p, bool bf16, int elems, int sm_c
 // One warp per segment, scalar loads; any shape (x is re-read from L1/L2).
 cudaError_t gns_warp_launch(const GnSegParams &p, bool bf16, int sm_count, cudaStream_t stream);
 
+// Linear then GroupNorm + LeakyReLU + x2: y = 2 LReLU(GN(x W^T + bias)), x
+// [Mr][K] and W [N][K] bfloat16 (K-major), bias/gamma/beta [N] fp32 or null,
+// y [Mr][N] fp32; groups of `group` contiguous channels.  Needs K % 8 == 0,
+// 16-byte aligned x, W and y, and linear_gn_group_size_ok(group).
+struct LinGnParams {
+    const void *x, *w;
+    const float *bias, *gamma, *beta;
+    float *y;
+    int64_t Mr, K, N, group;
+    float eps, slope;
+    uint64_t timeout_ns;
+    unsigned *err;
+};
+bool linear_gn_group_size_ok(int64_t group);
+cudaError_t linear_gn_launch(const LinGnParams &p, int sm_count, cudaStream_t stream);
+
 // RMSNorm over dim 1 of [B][C][S] (bf16: the tensors are bf16, else fp32).
 cudaError_t rms_channel_launch(const void *x, void *y, int64_t B, int64_t C, int64_t S, float eps, bool bf16,
                                cudaStream_t stream);
