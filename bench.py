@@ -100,14 +100,24 @@ CONFIGS = {
                          beta=(0.0, 0.1),
                          workload="GroupNorm+LeakyReLU(0.01)+x2 fp32 NCHW (1,128,512,512), 32 groups of 4 "
                                   "channels x 262144 positions (1,048,576 values: the two-kernel path)"),
+    # the GroupNorm page's whole module: Linear(8192, 8192) on (1024, 8192), then the
+    # normalization, one kernel (tensor-core GEMM, group statistics in its epilogue)
+    "linear_gn": dict(op="linear_gn", M=1024, K=8192, N=8192, G=512, x=(0.0, 1.0), gamma=(1.0, 0.1),
+                      beta=(0.0, 0.1),
+                      workload="Linear(8192, 8192) + GroupNorm(512 groups of 16) + LeakyReLU(0.01) + x2 on x "
+                               "(1024, 8192); x ~ N(0,1) and W ~ U(-1/sqrt(8192), 1/sqrt(8192)) in bf16, bias ~ "
+                               "U(-1/sqrt(8192), 1/sqrt(8192)), gamma ~ N(1,0.1), beta ~ N(0,0.1) fp32; y fp32"),
 }
 EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_rows", "ln_rows_bf16", "gn_bf16", "rms_bf16",
-               "gn_nchw", "gn_nchw_bf16", "gn_nchw_long", "gn_m48"]
+               "gn_nchw", "gn_nchw_bf16", "gn_nchw_long", "gn_m48", "linear_gn"]
 
 
 # ---------------------------------------------------------------------------- sizes
 
 def elements(cfg) -> int:
+    """Output elements of a step."""
+    if cfg["op"] == "linear_gn":
+        return cfg["M"] * cfg["N"]
     if cfg["op"] == "ln":
         return cfg["rows"] * cfg["L"]
     if cfg["op"] == "gn":
@@ -130,11 +140,22 @@ def elem_bytes(cfg) -> int:
 
 
 def algorithmic_bytes(cfg) -> int:
-    """x read once + y written once + gamma/beta read once."""
+    """x read once + y written once + gamma/beta read once (for the Linear: bf16 x and W read
+    once, fp32 bias/gamma/beta read once, fp32 y written once)."""
+    if cfg["op"] == "linear_gn":
+        return 2 * (cfg["M"] * cfg["K"] + cfg["N"] * cfg["K"]) + 4 * (3 * cfg["N"] + cfg["M"] * cfg["N"])
     return elem_bytes(cfg) * (2 * elements(cfg) + param_elems(cfg))
 
 
+def algorithmic_flops(cfg) -> int:
+    """The Linear's multiply-adds (2 M N K); the epilogue's few operations per output are not counted."""
+    return 2 * cfg["M"] * cfg["N"] * cfg["K"] if cfg["op"] == "linear_gn" else 0
+
+
 def l2_note(cfg, l2_bytes=None) -> str:
+    if cfg["op"] == "linear_gn":
+        return ("inputs larger than L2: x (16 MiB) and W (128 MiB) of one step exceed the L2; K back-to-back "
+                "steps between one pair of CUDA events")
     if l2_bytes is None:
         return "inputs larger than L2 (back-to-back steps rotate through enough buffer sets)"
     n = buffer_sets(cfg, l2_bytes)
@@ -149,7 +170,7 @@ def l2_note(cfg, l2_bytes=None) -> str:
 def shape_config(name, cfg, l2_bytes=None):
     out = {"workload": cfg["workload"], "name": name, "elements": elements(cfg),
            "algorithmic_bytes_per_step": algorithmic_bytes(cfg), "l2": l2_note(cfg, l2_bytes)}
-    for k in ("rows", "L", "N", "C", "G", "B", "S"):
+    for k in ("rows", "L", "M", "K", "N", "C", "G", "B", "S"):
         if k in cfg:
             out[{"L": "row_len"}.get(k, k)] = cfg[k]
     return out
@@ -160,6 +181,17 @@ def shape_config(name, cfg, l2_bytes=None):
 def host_inputs(cfg, seed=0):
     import numpy as np
     import normgen
+    if cfg["op"] == "linear_gn":
+        # x and W as the GPU reads them (bf16), bias/gamma/beta fp32: returned as (x, (W, bias), (gamma, beta))
+        M, K, N = cfg["M"], cfg["K"], cfg["N"]
+        bound = K ** -0.5
+        x = normgen.round_bf16(normgen.normal(M * K, cfg["x"][0], cfg["x"][1], seed=seed,
+                                              tensor_id=normgen.TENSOR_X))
+        w = normgen.round_bf16(normgen.uniform(N * K, -bound, bound, seed=seed, tensor_id=normgen.TENSOR_W))
+        bias = normgen.uniform(N, -bound, bound, seed=seed, tensor_id=normgen.TENSOR_LIN_BIAS)
+        g = normgen.normal(N, cfg["gamma"][0], cfg["gamma"][1], seed=seed, tensor_id=normgen.TENSOR_GAMMA)
+        b = normgen.normal(N, cfg["beta"][0], cfg["beta"][1], seed=seed, tensor_id=normgen.TENSOR_BETA)
+        return x, (w, bias), (g, b)
     n = elements(cfg)
     x = normgen.normal(n, cfg["x"][0], cfg["x"][1], seed=seed, tensor_id=normgen.TENSOR_X)
     g = b = None
@@ -190,6 +222,8 @@ def device_tensor(a, cfg, dev):
 
 
 def main_kernel_name(cfg) -> str:
+    if cfg["op"] == "linear_gn":
+        return "linear_gn_kernel"
     if cfg["op"] == "ln":
         L, bf16 = cfg["L"], bool(cfg.get("bf16"))
         if L <= (8192 if bf16 else 16384):
@@ -218,6 +252,10 @@ def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
     """The C-ABI call of one step (device pointers) and the number of our kernel launches it makes."""
     op = cfg["op"]
     bf16 = bool(cfg.get("bf16"))
+    if op == "linear_gn":  # g = (W, bias), b = (gamma, beta) on the device
+        (w, bias), (gm, bt) = g, b
+        return (lambda: ng.norm_linear_group_lrelu_x2_fwd(x, w, bias, gm, bt, y, cfg["M"], cfg["K"], cfg["N"],
+                                                          cfg["G"], 1e-5, 0.01, stream)), 1
     if op == "ln":
         rows, L = cfg["rows"], cfg["L"]
         one_launch = L % 4 == 0 and (L <= (8192 if bf16 else 16384) or (L <= 131072 and L % (8 if bf16 else 4) == 0) or
@@ -322,10 +360,22 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
 
 
+def bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the burst figure, for a kernel timed alone in a short loop."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured (MEASURED_PEAKS.json bf16_tflops: cuBLAS bf16 8192^3, burst)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback 1.9 PFLOP/s bf16 burst (no measured peak file)"
+
+
 # the kernel source files each workload's counters depend on
 KERNEL_SOURCES = {"ln": ("ln_kernels.cu", "gns_kernels.cu", "norm_internal.cuh"), "gn": ("gn_kernels.cu", "gns_kernels.cu", "norm_internal.cuh"),
                   "gn_nchw": ("gns_kernels.cu", "ln_kernels.cu", "norm_internal.cuh"),
-                  "rms": ("rms_kernels.cu", "norm_internal.cuh")}
+                  "rms": ("rms_kernels.cu", "norm_internal.cuh"),
+                  "linear_gn": ("linear_gn_kernels.cu", "norm_internal.cuh")}
 
 
 def code_only(text: str) -> str:
@@ -484,6 +534,10 @@ def time_same_size_copy(xs, ys, steps, stream):
 def buffer_sets(cfg, l2_bytes: int) -> int:
     """Input/output sets to rotate through so that no step finds its data in L2: one set
     when a step's x + y exceed twice the L2, else enough sets to cover three L2s."""
+    if cfg["op"] == "linear_gn":
+        return 1  # its inputs (x 16 MiB + W 128 MiB) exceed the L2; the GEMM is bound by the tensor cores
+    if "sets" in cfg:
+        return cfg["sets"]
     set_bytes = 2 * elem_bytes(cfg) * elements(cfg)
     if set_bytes > 2 * l2_bytes:
         return 1
@@ -496,15 +550,31 @@ def check_status(ng):
         raise RuntimeError(f"device status {ng.norm_status_string(st)}")
 
 
+def linear_gn_device(cfg, x, wb, gb, dev):
+    """Device tensors of the Linear + GroupNorm workload: x, (W, bias), (gamma, beta) and y."""
+    import torch
+    import normgen
+    import numpy as np
+    bf = lambda a: torch.from_numpy(normgen.bf16_bits(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa: E731
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)  # noqa: E731
+    y = torch.empty(cfg["M"] * cfg["N"], dtype=torch.float32, device=dev)
+    return bf(x), (bf(wb[0]), f32(wb[1])), (f32(gb[0]), f32(gb[1])), y
+
+
 def run_config(ng, name, cfg, steps, warmup, stream, flush, l2_bytes, sampler=None, world=1, want_e2e=False,
                cold_steps=100, want_graph=False, want_copy=False):
     import torch
     x, g, b = host_inputs(cfg)
     dev = torch.device("cuda")
-    xd, gd, bd = (None if a is None else device_tensor(a, cfg, dev) for a in (x, g, b))
     nset = buffer_sets(cfg, l2_bytes)
-    xs = [xd] + [xd.clone() for _ in range(nset - 1)]
-    ys = [torch.empty_like(xd) for _ in range(nset)]
+    if cfg["op"] == "linear_gn":
+        xd, gd, bd, yd = linear_gn_device(cfg, x, g, b, dev)
+        xs, ys = [xd], [yd]
+        want_copy = False
+    else:
+        xd, gd, bd = (None if a is None else device_tensor(a, cfg, dev) for a in (x, g, b))
+        xs = [xd] + [xd.clone() for _ in range(nset - 1)]
+        ys = [torch.empty_like(xd) for _ in range(nset)]
     ws = None
     ws_bytes = 0
     if cfg["op"] == "ln":
@@ -729,6 +799,7 @@ def main(argv=None):
     value = weak_scaling_value(nbytes, world, sec)
     e2e_sec = dist_max(main_res["e2e"]["seconds_per_step"], world, device="cuda")
     peak, peak_note = hbm_peak()
+    tflops_peak, tflops_note = bf16_peak()
     achieved = nbytes / main_res["seconds_per_step"] / 1e9
     traffic, traffic_note = ncu_traffic(args.config, cfg["op"])
 
@@ -753,6 +824,23 @@ def main(argv=None):
                 cs = r["copy_seconds_per_step"]
                 more["same_size_copy_us"] = round(cs * 1e6, 3)
                 more["same_size_copy_frac_of_measured_peak"] = round(2 * elem_bytes(c) * elements(c) / cs / 1e9 / peak, 4)
+            if name == "rms_small":
+                # the per-call floor: the same entry point on a (1, 64, 32) tensor (16 KiB moved)
+                tiny = dict(c, B=1, S=32, sets=64, workload="RMSNorm over dim 1 of fp32 (1,64,32)")
+                rt = run_config(ng, "rms_floor", tiny, k, 5, stream, flush, l2, cold_steps=0, want_graph=True)
+                more["launch_floor"] = {
+                    "us_per_step": round(rt["seconds_per_step"] * 1e6, 3),
+                    "graph_us_per_step": (round(rt["graph_seconds_per_step"] * 1e6, 3)
+                                          if rt["graph_seconds_per_step"] else None),
+                    "note": "the same call on a (1, 64, 32) tensor (16 KiB moved), timed the same way: what any "
+                            "call costs before its bytes"}
+            fl = algorithmic_flops(c)
+            if fl:
+                tf = fl / r["seconds_per_step"] / 1e12
+                more["achieved_tflops"] = round(tf, 2)
+                more["tensor_roofline"] = {"bound": "tensor", "achieved": round(tf, 2), "peak": tflops_peak,
+                                           "unit": "TFLOP/s", "frac": round(tf / tflops_peak, 4),
+                                           "peak_source": tflops_note}
             extras.append({"config": name, "workload": c["workload"], "steps": k,
                            "us_per_step": round(r["seconds_per_step"] * 1e6, 3),
                            "algorithmic_bytes": algorithmic_bytes(c), "achieved_gbs": round(a, 2),

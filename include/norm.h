@@ -343,7 +343,10 @@ const char *norm_status_string(norm_status_t status);
  *                                element of y either keeps its previous value
  *                                or holds its correct result.  Default 200 ms;
  *                                waits that drain a CTA's own copies before it
- *                                exits use at least 100 ms.
+ *                                exits use at least 100 ms.  A limit below 1 us
+ *                                makes every wait for a CTA's own bulk copy
+ *                                that is not over at its first (non-blocking)
+ *                                look give up at once.
  *   NORM_OPT_BARRIER_EXTRA_ARRIVALS  test hook: when > 0, the grid barrier
  *                                waits for partial statistics that no CTA
  *                                publishes, so it can only end by timing

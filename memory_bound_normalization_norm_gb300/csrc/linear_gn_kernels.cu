@@ -9,28 +9,31 @@
 // bfloat16 (K-major, as nn.Linear stores W), products are accumulated in fp32
 // in tensor memory, and the epilogue is fp32.
 //
-// One CTA per SM walks output tiles of 128 rows x 256 channels (persistent,
-// tile t -> rows (t % tiles_m) * 128, channels (t / tiles_m) * 256, so the CTAs
-// running at once share W's rows through L2).  Warp roles:
-//   warp 0, one lane     TMA producer: 64-wide K slices of x (128 x 64) and W
+// One CTA per SM walks output tiles of 256 rows x 256 channels (persistent,
+// tile t -> rows (t % tiles_m) * 256, channels (t / tiles_m) * 256, so the CTAs
+// running at once share W's rows through L2).  A 256-row tile is two MMA row
+// halves of 128 that share every slice of W: per MMA cycle a CTA pulls 64
+// bytes of operands from L2 instead of the 96 of a 128 x 256 tile, which is
+// what the operand fetch of the whole GPU can sustain.  Warp roles:
+//   warp 0, one lane     TMA producer: 64-wide K slices of x (256 x 64) and W
 //                        (256 x 64) by cp.async.bulk.tensor, 128-byte
 //                        swizzled, into a ring of LG_STAGES shared-memory
 //                        stages, each tracked by a "full" mbarrier;
-//   warp 1, one lane     MMA issuer: four tcgen05.mma (M 128, N 256, K 16) per
-//                        stage into one of two TMEM accumulators (256 fp32
+//   warp 1, one lane     MMA issuer: per stage, four K steps of two
+//                        tcgen05.mma (M 128, N 256, K 16), one per row half,
+//                        into the two halves of the TMEM accumulator (256 fp32
 //                        columns each); tcgen05.commit releases the stage
 //                        ("empty" mbarrier) and, after the tile's last stage,
 //                        hands the accumulator to the epilogue;
-//   warps 2..5           epilogue: thread t of the 128 owns row t of the tile
-//                        (TMEM lane t).  A group of CG contiguous channels is
-//                        CG consecutive TMEM columns of one lane, so each
-//                        thread holds whole groups in registers: it adds the
-//                        bias, takes the group's mean and then the exact M2
-//                        about it, applies gamma/beta, LeakyReLU and x + x, and
-//                        stores the group's CG floats.  Then it releases the
-//                        accumulator, which the MMA warp refills two tiles on,
-//                        so the epilogue of one tile overlaps the MMAs of the
-//                        next.
+//   warps 2..5           epilogue: thread t of the 128 owns rows t and 128 + t
+//                        of the tile (TMEM lane t of each half).  A group of CG
+//                        contiguous channels is CG consecutive TMEM columns
+//                        of one lane, so each thread holds whole groups in
+//                        registers: it adds the bias, takes the group's mean
+//                        and then the exact M2 about it, applies gamma/beta,
+//                        LeakyReLU and x + x, and stores the group's CG
+//                        floats.  Then it releases the accumulator for the
+//                        CTA's next tile.
 // Every wait is bounded (%globaltimer): a role that gives up records
 // NORM_ERR_TIMEOUT, tells the others through shared memory, and the CTA drains
 // its own bulk copies and MMAs before it frees TMEM and exits.
@@ -45,23 +48,24 @@ namespace normk {
 
 namespace {
 
-constexpr int LG_BM = 128;  // rows of x per tile (MMA M)
+constexpr int LG_BM = 256;  // rows of x per tile: two MMA row halves
+constexpr int LG_MH = 128;  // rows per MMA (M)
 constexpr int LG_BN = 256;  // output channels per tile (MMA N)
 constexpr int LG_BK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int LG_UK = 16;   // K per tcgen05.mma of kind f16
-constexpr int LG_STAGES = 4;
+constexpr int LG_STAGES = 3;
 constexpr uint32_t LG_A_BYTES = LG_BM * LG_BK * 2;
 constexpr uint32_t LG_B_BYTES = LG_BN * LG_BK * 2;
 constexpr uint32_t LG_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES;
 constexpr int LG_THREADS = 192;
-constexpr uint32_t LG_TMEM_COLS = 2 * LG_BN; // two accumulators
+constexpr uint32_t LG_TMEM_COLS = 2 * LG_BN; // the accumulator: two row halves
 constexpr size_t LG_SMEM = LG_STAGES * LG_STAGE_BYTES + 1024; // + room to align to 1024
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
 // and B bfloat16 (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 constexpr uint32_t LG_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(LG_BN >> 3) << 17) |
-                              (static_cast<uint32_t>(LG_BM >> 4) << 24);
+                              (static_cast<uint32_t>(LG_MH >> 4) << 24);
 
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (the
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(LG_THREADS, 1)
 {
     extern __shared__ uint8_t lg_smem_raw[];
     __shared__ __align__(8) uint64_t full[LG_STAGES], empty[LG_STAGES];
-    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain;
+    __shared__ __align__(8) uint64_t acc_full, acc_empty, drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
 
@@ -179,10 +183,8 @@ __global__ void __launch_bounds__(LG_THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 4); // one arrival per epilogue warp
-        }
+        mbar_init(&acc_full, 1);
+        mbar_init(&acc_empty, 4); // one arrival per epilogue warp
         mbar_init(&drain, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -238,15 +240,12 @@ __global__ void __launch_bounds__(LG_THREADS, 1)
             int local = 0; // tiles of this CTA so far
             bool issued = false;
             for (int t = blockIdx.x; t < a.tiles && !failed; t += gridDim.x, ++local) {
-                const int acc = local & 1;
-                const uint32_t use = static_cast<uint32_t>(local >> 1);
-                // the epilogue has read this accumulator's previous tile
-                if (!lg_wait(&acc_empty[acc], (use & 1u) ^ 1u, a.timeout_ns, abort)) {
+                // the epilogue has read the accumulator's previous tile
+                if (!lg_wait(&acc_empty, (static_cast<uint32_t>(local) & 1u) ^ 1u, a.timeout_ns, abort)) {
                     failed = true;
                     break;
                 }
                 tmem_fence_after_sync();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * LG_BN);
                 for (int kb = 0; kb < nk; ++kb, ++fills) {
                     const int s = static_cast<int>(fills % LG_STAGES);
                     if (!lg_wait(&full[s], static_cast<uint32_t>((fills / LG_STAGES) & 1), a.timeout_ns, abort)) {
@@ -258,15 +257,19 @@ __global__ void __launch_bounds__(LG_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < LG_BK / LG_UK; ++k) {
                         const uint32_t koff = static_cast<uint32_t>(k * LG_UK * 2);
-                        mma_bf16(d, sw128_desc(sa + koff), sw128_desc(sa + LG_A_BYTES + koff),
-                                 (kb > 0 || k > 0) ? 1u : 0u);
+                        const uint64_t bdesc = sw128_desc(sa + LG_A_BYTES + koff);
+                        const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+#pragma unroll
+                        for (int h = 0; h < LG_BM / LG_MH; ++h)
+                            mma_bf16(tmem_base + static_cast<uint32_t>(h * LG_BN),
+                                     sw128_desc(sa + static_cast<uint32_t>(h * LG_MH * LG_BK * 2) + koff), bdesc, acc);
                     }
                     issued = true;
                     mma_commit(&empty[s]); // the stage is free once these MMAs have read it
                 }
                 if (failed)
                     break;
-                mma_commit(&acc_full[acc]); // the tile's sums are complete
+                mma_commit(&acc_full); // the tile's sums are complete
             }
             if (failed) {
                 *abort = 1;
@@ -283,65 +286,66 @@ __global__ void __launch_bounds__(LG_THREADS, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;              // TMEM lane quarter of this warp
-        const int row_in_tile = 32 * q + lane; // = TMEM lane
+        const int q = warp & 3; // TMEM lane quarter of this warp
         int local = 0;
         for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++local) {
-            const int acc = local & 1;
-            const uint32_t use = static_cast<uint32_t>(local >> 1);
-            if (!lg_wait(&acc_full[acc], use & 1u, a.timeout_ns, abort)) {
+            if (!lg_wait(&acc_full, static_cast<uint32_t>(local) & 1u, a.timeout_ns, abort)) {
                 *abort = 1;
                 record_error(a.err, NORM_ERR_TIMEOUT);
                 break;
             }
             tmem_fence_after_sync();
             const int m0 = (t % a.tiles_m) * LG_BM, n0 = (t / a.tiles_m) * LG_BN;
-            const int row = m0 + row_in_tile;
-            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * LG_BN);
-            float *yr = a.y + static_cast<int64_t>(row) * a.N;
 #pragma unroll 1
-            for (int g0 = 0; g0 < LG_BN; g0 += CG) {
-                const int c0 = n0 + g0;
-                float v[CG];
+            for (int h = 0; h < LG_BM / LG_MH; ++h) {
+                const int row = m0 + h * LG_MH + 32 * q + lane; // TMEM lane 32 q + lane of half h
+                const uint32_t tacc =
+                    tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * LG_BN);
+                float *yr = a.y + static_cast<int64_t>(row) * a.N;
+#pragma unroll 1
+                for (int g0 = 0; g0 < LG_BN; g0 += CG) {
+                    const int c0 = n0 + g0;
+                    float v[CG];
 #pragma unroll
-                for (int j = 0; j < CG; j += 16) {
-                    float w[16];
-                    tmem_ld16(tacc + static_cast<uint32_t>(g0 + j), w);
+                    for (int j = 0; j < CG; j += 16) {
+                        float w[16];
+                        tmem_ld16(tacc + static_cast<uint32_t>(g0 + j), w);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        v[j + i] = w[i];
-                }
-                tmem_wait_ld();
-                if (c0 >= a.N) // a whole group past the last channel (N % CG == 0)
-                    continue;
-                // h = x W^T + bias, then the group's mean and exact M2 about it
-                float s = 0.f;
+                        for (int i = 0; i < 16; ++i)
+                            v[j + i] = w[i];
+                    }
+                    tmem_wait_ld();
+                    if (c0 >= a.N) // a whole group past the last channel (N % CG == 0)
+                        continue;
+                    // h = x W^T + bias, then the group's mean and exact M2 about it
+                    float s = 0.f;
 #pragma unroll
-                for (int j = 0; j < CG; ++j) {
-                    v[j] += a.bias ? __ldg(a.bias + c0 + j) : 0.f;
-                    s += v[j];
-                }
-                const float mean = s * (1.0f / CG);
-                float m2 = 0.f;
+                    for (int j = 0; j < CG; ++j) {
+                        v[j] += a.bias ? __ldg(a.bias + c0 + j) : 0.f;
+                        s += v[j];
+                    }
+                    const float mean = s * (1.0f / CG);
+                    float m2 = 0.f;
 #pragma unroll
-                for (int j = 0; j < CG; ++j) {
-                    const float d = v[j] - mean;
-                    m2 = fmaf(d, d, m2);
-                }
-                const float rstd = rsqrtf(m2 * (1.0f / CG) + a.eps);
-                if (row < a.Mr) {
+                    for (int j = 0; j < CG; ++j) {
+                        const float d = v[j] - mean;
+                        m2 = fmaf(d, d, m2);
+                    }
+                    const float rstd = rsqrtf(m2 * (1.0f / CG) + a.eps);
+                    if (row < a.Mr) {
 #pragma unroll
-                    for (int j = 0; j < CG; j += 4) {
-                        float o[4];
+                        for (int j = 0; j < CG; j += 4) {
+                            float o[4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float gw = a.gamma ? __ldg(a.gamma + c0 + j + i) : 1.f;
-                            const float bw = a.beta ? __ldg(a.beta + c0 + j + i) : 0.f;
-                            float u = fmaf((v[j + i] - mean) * rstd, gw, bw);
-                            u = u > 0.f ? u : a.slope * u;
-                            o[i] = u + u;
+                            for (int i = 0; i < 4; ++i) {
+                                const float gw = a.gamma ? __ldg(a.gamma + c0 + j + i) : 1.f;
+                                const float bw = a.beta ? __ldg(a.beta + c0 + j + i) : 0.f;
+                                float u = fmaf((v[j + i] - mean) * rstd, gw, bw);
+                                u = u > 0.f ? u : a.slope * u;
+                                o[i] = u + u;
+                            }
+                            *reinterpret_cast<float4 *>(yr + c0 + j) = make_float4(o[0], o[1], o[2], o[3]);
                         }
-                        *reinterpret_cast<float4 *>(yr + c0 + j) = make_float4(o[0], o[1], o[2], o[3]);
                     }
                 }
             }
@@ -349,7 +353,7 @@ __global__ void __launch_bounds__(LG_THREADS, 1)
             tmem_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&acc_empty[acc]);
+                mbar_arrive(&acc_empty);
         }
     }
     tmem_fence_before_sync();

@@ -23,14 +23,18 @@
 // slices arrive by bulk copy (TMA engine, 32 KB pieces) into two
 // shared-memory buffers; the slice of the row being written lives in
 // registers, and gamma/beta of the slice live in tensor memory (TMEM),
-// loaded once per launch.  x is read from HBM once and stays on chip until y
-// is written; gamma and beta are read from HBM once.  Three warp roles run
-// concurrently: warps 1..3 reduce a row's statistics as soon as it lands and
-// publish the CTA's triple, warp 0 merges the triples of all CTAs, warps
-// 4..15 write y.  A row's triples go out about two rows before its y is
-// written, which hides the grid-wide exchange (several microseconds under
-// full HBM load) behind other rows' work.  The pivot's three candidate
-// elements travel with each row's bulk copy.
+// loaded once per launch by the apply warps' own 16-byte loads.  x is read
+// from HBM once and stays on chip until y is written; gamma and beta are
+// read from HBM once.  Three warp roles run concurrently: warps 1..3 reduce
+// a row's statistics as soon as it lands and publish the CTA's triple, warp
+// 0 merges the triples of all CTAs, warps 4..15 write y.  A row's triples go
+// out about two rows before its y is written, which hides the grid-wide
+// exchange (several microseconds under full HBM load) behind other rows'
+// work.  Before the first y store the apply warps have nothing to write, so
+// they reduce rows 0 and 1 together with warps 1..3 (480 threads instead of
+// 96), and row 0 is copied alone first so that it lands, is reduced and
+// crosses the grid while row 1 and gamma/beta are still arriving.  The
+// pivot's three candidate elements travel with each row's bulk copy.
 //
 // Grid barrier without atomics.  Each CTA publishes its (mean, M2) as two
 // 64-bit words, each carrying a 32-bit tag in its high half, in one 16-byte
@@ -90,7 +94,9 @@ constexpr int LN_MAX_GRID = 160;          // CTAs whose records one warp loads a
 constexpr uint32_t LN_BULK_CHUNK = 32768;
 constexpr int LN_BAR_APPLIED = 1;         // named barrier of warp 0 and the apply warps
 constexpr int LN_BAR_STATS = 2;           // named barrier of the statistics warps
-constexpr int LN_BAR_FILL = 3;            // named barrier of the apply warps (TMEM fill)
+constexpr int LN_BAR_PRO = 3;             // statistics and apply warps (rows 0 and 1)
+constexpr int LN_BAR_FILL = 4;            // apply warps (buffers read, gamma/beta to TMEM)
+constexpr int LN_PRO_WARPS = LN_THREADS / 32 - 1; // warps that reduce rows 0 and 1
 static_assert(LN_V % LN_GB == 0, "whole gamma/beta batches");
 static_assert(LN_APPLY_WARP0 % 4 == 0 && LN_A % 128 == 0, "apply warps fill whole TMEM quarters");
 // apply warp w sits in TMEM quarter w % 4 and takes column range
@@ -228,12 +234,46 @@ __device__ __forceinline__ float row_pivot(const float4 *piece, int64_t row_len)
     return fmaxf(fminf(a, b), fminf(fmaxf(a, b), c));
 }
 
+// Shifted sums of d = x - K over float4 i = pi, pi + np, ... < n4 of a row
+// slice in shared memory, with four independent accumulator pairs, as this
+// thread's (count, mean, M2).
+__device__ __forceinline__ Moments slice_moments(const float4 *buf, int n4, int pi, int np, float K)
+{
+    float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+    int i = pi;
+    for (; i + 3 * np < n4; i += 4 * np) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float4 v = buf[i + u * np];
+            const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
+            s1[u] += (a + b) + (c + d);
+            s2[u] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[u]))));
+        }
+    }
+    for (; i < n4; i += np) {
+        const float4 v = buf[i];
+        const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
+        s1[0] += (a + b) + (c + d);
+        s2[0] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[0]))));
+    }
+    Moments m = {0.f, 0.f, 0.f};
+    const int nv = n4 > pi ? (n4 - pi + np - 1) / np : 0; // float4 of this thread
+    if (nv > 0) {
+        const float S1 = (s1[0] + s1[1]) + (s1[2] + s1[3]);
+        const float S2 = (s2[0] + s2[1]) + (s2[2] + s2[3]);
+        m.n = 4.f * static_cast<float>(nv);
+        m.mean = S1 / m.n;
+        m.m2 = fmaxf(fmaf(-S1, m.mean, S2), 0.f);
+    }
+    return m;
+}
+
 __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p)
 {
     extern __shared__ __align__(128) float4 ln_smem[];
     __shared__ __align__(8) uint64_t bar_x[2];
-    __shared__ __align__(8) uint64_t bar_gb; // gamma, then beta, into buffer 1
-    __shared__ Moments red[2][LN_STATS_WARPS];          // per-warp triples, by row parity
+    __shared__ __align__(8) uint64_t bar_g, bar_b; // gamma into buffer 1, beta into buffer 0
+    __shared__ Moments red[2][LN_PRO_WARPS];            // per-warp triples, by row parity
     __shared__ __align__(16) unsigned long long rec_out[2][2]; // this CTA's record, by row parity
     __shared__ float4 piv_in[2][3];                     // a row's pivot candidates, by row parity
     __shared__ float piv_k[2];                          // a row's pivot, by row parity
@@ -271,7 +311,8 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     if (tid == 0) {
         mbar_init(&bar_x[0], 1);
         mbar_init(&bar_x[1], 1);
-        mbar_init(&bar_gb, 1);
+        mbar_init(&bar_g, 1);
+        mbar_init(&bar_b, 1);
         fence_mbar_init();
         fence_proxy_async_smem();
         row_base_s = ld_relaxed_gpu_u32(&p.sync->row_base);
@@ -314,6 +355,13 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     // A row's triples are published about two iterations before its y is
     // written, so the grid-wide exchange has that long to complete, and the
     // reduction of a row overlaps the writing of an earlier one.
+    // Prologue (r = -2, -1): no y is written yet, so the apply warps reduce
+    // rows 0 and 1 together with the statistics warps (15 warps instead of
+    // 3; LN_BAR_PRO).  Row 0 (buffer 0) and gamma (buffer 1) are copied at the
+    // start.  As soon as row 0 is reduced the apply warps move it into their
+    // registers, which frees buffer 0 for beta; gamma goes from buffer 1 to
+    // TMEM, which frees buffer 1 for row 1; then beta goes to TMEM.  So row 0
+    // crosses the grid while gamma, beta and row 1 are still arriving.
     if (warp == 0) {
         // ------------------------------------------------ coordinator
         bool fail = false; // the merge of the previous row gave up
@@ -353,49 +401,27 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             const int64_t q = r + 2; // the row reduced and published now
             if (q >= R)
                 continue;
+            // rows 0 and 1 are reduced by the apply warps too
+            const bool pro = q < 2;
+            const int np = pro ? 32 * LN_PRO_WARPS : LN_S;
             fail = !mbar_wait_bounded(&bar_x[q & 1], x_parity(q), p.timeout_ns);
-            Moments m = {0.f, 0.f, 0.f};
             const float K = fail ? 0.f : row_pivot(piv_in[q & 1], p.row_len);
-            if (!fail) {
-                // shifted sums of d = x - K over this thread's float4, four
-                // independent accumulator pairs
-                const float4 *buf = ln_smem + (q & 1) * buf_f4;
-                float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
-                int i = st;
-                for (; i + 3 * LN_S < n4; i += 4 * LN_S) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float4 v = buf[i + u * LN_S];
-                        const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
-                        s1[u] += (a + b) + (c + d);
-                        s2[u] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[u]))));
-                    }
-                }
-                for (; i < n4; i += LN_S) {
-                    const float4 v = buf[i];
-                    const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
-                    s1[0] += (a + b) + (c + d);
-                    s2[0] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[0]))));
-                }
-                const int nv = n4 > st ? (n4 - st + LN_S - 1) / LN_S : 0; // float4 of this thread
-                if (nv > 0) {
-                    const float S1 = (s1[0] + s1[1]) + (s1[2] + s1[3]);
-                    const float S2 = (s2[0] + s2[1]) + (s2[2] + s2[3]);
-                    m.n = 4.f * static_cast<float>(nv);
-                    m.mean = S1 / m.n;
-                    m.m2 = fmaxf(fmaf(-S1, m.mean, S2), 0.f);
-                }
-            }
+            Moments m = {0.f, 0.f, 0.f};
+            if (!fail)
+                m = slice_moments(ln_smem + (q & 1) * buf_f4, n4, st, np, K);
             m = warp_merge(m);
             if (lane == 0)
                 red[q & 1][warp - 1] = m;
-            bar_sync_named(LN_BAR_STATS, LN_S);
+            if (pro)
+                bar_sync_named(LN_BAR_PRO, 32 * LN_PRO_WARPS);
+            else
+                bar_sync_named(LN_BAR_STATS, LN_S);
             if (warp == 1) {
                 // The CTA's triple of row q goes out now as a 16-byte bulk
                 // store: a plain store would stall this warp until the
                 // CTA's y stores ahead of it drain.
                 Moments c = {0.f, 0.f, 0.f};
-                if (lane < LN_STATS_WARPS)
+                if (lane < (pro ? LN_PRO_WARPS : LN_STATS_WARPS))
                     c = red[q & 1][lane];
                 c = warp_merge(c);
                 if (lane == 0 && !fail) {
@@ -417,81 +443,109 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     } else {
         // ------------------------------------------------ apply warps 4..15
         const int at = tid - 32 * LN_APPLY_WARP0;
-        // Thread 32 * LN_APPLY_WARP0 issues the bulk copies of x.  It tracks
-        // those it issued (rows < issued) and those whose completion it
-        // observed (rows < waited), so that an early exit can drain them.
+        const int pt = tid - 32; // index among the warps that reduce rows 0 and 1
+        // Thread 32 * LN_APPLY_WARP0 issues the bulk copies.  It tracks the
+        // rows it issued (rows < issued) and those whose completion it
+        // observed (rows < waited), and the same for gamma and beta, so that
+        // an early exit can drain them.
         const bool issuer = at == 0;
         int64_t issued = 0, waited = 0;
-        // The slice of gamma (h = 0) or beta (h = 1) into buffer 1, for the
-        // TMEM fill before row 1 takes that buffer.
-        auto issue_gb = [&](int h) {
-            const float4 *src = h == 0 ? g4 : b4;
+        bool g_out = false, b_out = false; // gamma / beta copy issued and not seen complete
+        bool fail = false; // a copy the prologue waits for did not land in time
+        // gamma or beta of the slice (h = 0, 1) into buffer 1 or 0, on bar
+        auto issue_param = [&](const float4 *src, int buf, uint64_t *bar) {
             const uint32_t bytes = src ? static_cast<uint32_t>(n4) * 16u : 0u;
-            mbar_arrive_expect_tx(&bar_gb, bytes);
-            float4 *dst = ln_smem + buf_f4;
+            mbar_arrive_expect_tx(bar, bytes);
+            float4 *dst = ln_smem + buf * buf_f4;
             for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
                 bulk_g2s(dst + off / 16, src + f0 + off / 16,
-                         (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, &bar_gb, pol_stream);
+                         (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, bar, pol_stream);
         };
         if (issuer) {
             issue_x(0);
             issued = 1;
-            issue_gb(0);
+            issue_param(g4, 1, &bar_g);
+            g_out = true;
         }
         // This thread's TMEM cells: lane 32*(warp % 4) + lane of its warp's
         // quarter, LN_TM_COLS columns from (warp / 4 - 1) * LN_TM_COLS:
         // gamma of its k-th float4 at column 4k, beta at LN_TM_BETA + 4k.
         const uint32_t tm = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
                             static_cast<uint32_t>((warp / 4 - 1) * LN_TM_COLS);
+        // Help reduce prologue row q (0 or 1) from its buffer: this thread's
+        // share of the 15-warp partition, merged over the warp, to red[].
+        auto help_reduce = [&](int64_t q) {
+            const bool ok = mbar_wait_bounded(&bar_x[q & 1], x_parity(q), p.timeout_ns);
+            fail = fail || !ok;
+            if (ok && issuer)
+                waited = q + 1;
+            Moments m = {0.f, 0.f, 0.f};
+            if (ok)
+                m = slice_moments(ln_smem + (q & 1) * buf_f4, n4, pt, 32 * LN_PRO_WARPS,
+                                  row_pivot(piv_in[q & 1], p.row_len));
+            m = warp_merge(m);
+            if (lane == 0)
+                red[q & 1][warp - 1] = m;
+            bar_sync_named(LN_BAR_PRO, 32 * LN_PRO_WARPS);
+        };
+        // gamma or beta (wait on bar, then buffer buf -> this thread's TMEM
+        // columns from col0; 1 / 0 where the parameter is absent)
+        auto fill_tmem = [&](const float4 *src, int buf, uint64_t *bar, uint32_t col0, float dflt) {
+            const bool ok = mbar_wait_bounded(bar, 0, p.timeout_ns);
+            fail = fail || !ok;
+            const float4 *b = ln_smem + buf * buf_f4;
+            const float4 d = make_float4(dflt, dflt, dflt, dflt);
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < LN_V; k += 2) {
+                float4 a0, a1;
+                const int i0 = at + k * LN_A, i1 = at + (k + 1) * LN_A;
+                a0 = (src && ok && i0 < n4) ? b[i0] : d;
+                a1 = (src && ok && i1 < n4) ? b[i1] : d;
+                tmem_st4(tm + col0 + static_cast<uint32_t>(4 * k), a0);
+                tmem_st4(tm + col0 + static_cast<uint32_t>(4 * (k + 1)), a1);
+            }
+            tmem_wait_st();
+            return ok;
+        };
         float4 v[LN_V]; // this thread's part of the slice of row r
         for (int64_t r = -2; r < R; ++r) {
-            if (__syncthreads_or(0)) {
+            if (__syncthreads_or(fail ? 1 : 0)) {
                 aborted = true;
                 break;
             }
             if (r == -2) {
-                // Before the first row: gamma, then beta, of the slice
-                // arrive by bulk copy in buffer 1 and go to TMEM once; then
-                // buffer 1 receives row 1.  (Bulk copies keep this traffic
-                // off the load path that the statistics warps' shared-memory
-                // reads share.)  If a copy does not land in time, row 1 is
-                // never issued, so the statistics warps give up on it and
-                // the CTA aborts at a later vote.
-                const float4 *buf = ln_smem + buf_f4;
-                bool ok = true;
+                // row 0: reduce it with the statistics warps, then hold it in
+                // registers, so its buffer can take beta
+                help_reduce(0);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const bool landed = mbar_wait_bounded(&bar_gb, static_cast<uint32_t>(h), p.timeout_ns);
-                    if (issuer && !landed && ok) {
-                        // drain it before anything else uses buffer 1
-                        if (!mbar_wait_bounded(&bar_gb, static_cast<uint32_t>(h), drain_ns))
-                            record_error(p.err, NORM_ERR_TIMEOUT);
-                    }
-                    ok = ok && landed;
-                    const float4 *src = h == 0 ? g4 : b4;
-                    const float4 dflt = h == 0 ? make_float4(1.f, 1.f, 1.f, 1.f) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int k = 0; k < LN_V; ++k) {
-                        const int i = at + k * LN_A;
-                        v[k] = (src && ok && i < n4) ? buf[i] : dflt;
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < LN_V; ++k)
-                        tmem_st4(tm + static_cast<uint32_t>(h * LN_TM_BETA + 4 * k), v[k]);
-                    tmem_wait_st();
-                    // every apply thread has read buffer 1: refill it
-                    bar_sync_named(LN_BAR_FILL, LN_A);
-                    if (issuer && ok) {
-                        fence_proxy_async_smem();
-                        if (h == 0) {
-                            issue_gb(1);
-                        } else if (R > 1) {
-                            issue_x(1);
-                            issued = 2;
-                        }
-                    }
+                for (int k = 0; k < LN_V; ++k) {
+                    const int i = at + k * LN_A;
+                    v[k] = (i < n4) ? ln_smem[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+                // every apply thread has read buffer 0 (the statistics warps
+                // finished with it at LN_BAR_PRO)
+                bar_sync_named(LN_BAR_FILL, LN_A);
+                if (issuer && !fail) {
+                    fence_proxy_async_smem();
+                    issue_param(b4, 0, &bar_b);
+                    b_out = true;
+                }
+                // gamma: buffer 1 -> TMEM, then row 1 into buffer 1
+                const bool g_ok = fill_tmem(g4, 1, &bar_g, 0u, 1.f);
+                if (issuer && g_ok)
+                    g_out = false;
+                bar_sync_named(LN_BAR_FILL, LN_A);
+                if (issuer && !fail && R > 1) {
+                    fence_proxy_async_smem();
+                    issue_x(1);
+                    issued = 2;
+                }
+                // beta: buffer 0 -> TMEM (buffer 0 takes row 2 at r = -1)
+                const bool b_ok = fill_tmem(b4, 0, &bar_b, LN_TM_BETA, 0.f);
+                if (issuer && b_ok)
+                    b_out = false;
+                bar_sync_named(LN_BAR_FILL, LN_A);
             }
             if (r >= 0) {
                 // y of row r from registers, gamma/beta from TMEM in batches
@@ -525,11 +579,10 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                     }
                 }
             }
-            const int64_t q = r + 1; // the row moved into registers now
-            if (q >= 0 && q < R) {
-                // row q landed before the statistics warps reduced it (an
-                // iteration ago); the issuer's wait returns at once and
-                // lets it account for the copy
+            const int64_t q = r + 1; // the row moved into registers now (row 0 was at r = -2)
+            if (q >= 1 && q < R) {
+                // row q landed before it was reduced (an iteration ago); the
+                // issuer's wait returns at once and lets it account for the copy
                 if (issuer && mbar_wait_bounded(&bar_x[q & 1], x_parity(q), drain_ns))
                     waited = q + 1;
                 const float4 *buf = ln_smem + (q & 1) * buf_f4;
@@ -541,13 +594,17 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             }
             __syncwarp();
             bar_sync_named(LN_BAR_APPLIED, LN_A + 32);
-            // buffer q & 1 and its pivot pieces are free (the statistics
-            // warps reduced row q an iteration ago): refill them with row q + 2
-            if (issuer && q + 2 >= 2 && q + 2 < R) {
+            // buffer q & 1 and its pivot pieces are free (row q was reduced
+            // an iteration ago, and beta left buffer 0 at r = -2): refill them
+            // with row q + 2
+            if (issuer && q >= 0 && q + 2 < R) {
                 fence_proxy_async_smem();
                 issue_x(q + 2);
                 issued = q + 3;
             }
+            // r = -1: help reduce row 1 while warp 0 merges row 0
+            if (r == -1 && R > 1)
+                help_reduce(1);
         }
         // Drain: never leave a bulk copy in flight into shared memory.
         if (issuer) {
@@ -555,6 +612,10 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 if (!mbar_wait_bounded(&bar_x[qq & 1], x_parity(qq), drain_ns))
                     record_error(p.err, NORM_ERR_TIMEOUT);
             }
+            if (g_out && !mbar_wait_bounded(&bar_g, 0, drain_ns))
+                record_error(p.err, NORM_ERR_TIMEOUT);
+            if (b_out && !mbar_wait_bounded(&bar_b, 0, drain_ns))
+                record_error(p.err, NORM_ERR_TIMEOUT);
         }
     }
     // Whichever role's wait gave up, the vote ended every role's loop: one

@@ -186,11 +186,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of whether phase `parity` of `bar` has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete, giving up after timeout_ns.
+// The first look does not suspend the thread (mbarrier.try_wait may, for a
+// hardware-defined time), and a limit below one microsecond, finer than
+// %globaltimer is guaranteed to resolve, gives up at that first look if the
+// phase is not complete: tiny limits make every wait that is not already
+// over give up, deterministically.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t timeout_ns)
 {
-    if (mbar_try_wait(bar, parity))
+    if (mbar_test_wait(bar, parity))
         return true;
+    if (timeout_ns < 1000)
+        return false;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer_ns() - t0 > timeout_ns)

@@ -47,6 +47,9 @@ def _workspace(ng, cfg):
 def _oracle(cfg, x, g, b):
     f64 = bool(cfg.get("bf16"))
     op = cfg["op"]
+    if op == "linear_gn":  # g = (W, bias), b = (gamma, beta)
+        return oracle.linear_group_lrelu_x2(x, g[0], g[1], b[0], b[1], cfg["M"], cfg["K"], cfg["N"], cfg["G"],
+                                            1e-5, 0.01)
     if op == "ln":
         return oracle.layer_norm(x, g, b, cfg["rows"], cfg["L"], 1e-5, f64=f64)
     if op == "gn":
@@ -68,8 +71,11 @@ def test_bench_workload(ng, name):
     cfg = bench.CONFIGS[name]
     dev = torch.device("cuda")
     x, g, b = bench.host_inputs(cfg)
-    xd, gd, bd = (None if a is None else bench.device_tensor(a, cfg, dev) for a in (x, g, b))
-    yd = torch.empty_like(xd)
+    if cfg["op"] == "linear_gn":
+        xd, gd, bd, yd = bench.linear_gn_device(cfg, x, g, b, dev)
+    else:
+        xd, gd, bd = (None if a is None else bench.device_tensor(a, cfg, dev) for a in (x, g, b))
+        yd = torch.empty_like(xd)
     ws, ws_bytes = _workspace(ng, cfg)
     stream = torch.cuda.current_stream().cuda_stream
     call, _ = bench.make_call(ng, cfg, xd, gd, bd, yd, ws, ws_bytes, stream)

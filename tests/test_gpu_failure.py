@@ -5,9 +5,10 @@
    drain its own bulk copies and return without writing y; norm_last_error()
    reports the status and resets the library-owned workspace, after which a
    normal call works again.
-2. A 1 ns limit makes the other waits give up too (a row's bulk copy, the
-   gamma/beta copies): the CTA still records the error and drains its copies;
-   every element of y is then either untouched or correct.
+2. A 1 ns limit makes the other waits give up too (a row's bulk copy that has
+   not landed at the first, non-blocking look, as row 0 has not at the start):
+   the CTA still records the error and drains its copies; every element of y
+   is then either untouched or correct.
 3. Error words are per stream: a timeout on one stream is reported by
    norm_last_error on that stream only.
 """
@@ -55,11 +56,11 @@ def test_barrier_timeout_is_reported_and_recoverable(ng):
 
 def test_tiny_wait_limit_aborts_cleanly(ng):
     """A 1 ns limit makes any wait that is not over at its first look give up: the
-    statistics warps' wait for a row's bulk copy, the apply warps' wait for gamma/beta,
-    or warp 0's poll.  Whichever gives up, the CTA must record NORM_ERR_TIMEOUT and
-    drain its copies (drains wait at least 100 ms whatever the limit).  CTAs stop
-    independently, so y may be partly written: every element is untouched or correct.
-    Then a normal call works."""
+    statistics and apply warps' waits for a row's bulk copy (row 0 has not landed
+    when they first look), or warp 0's poll.  Whichever gives up, the CTA must record
+    NORM_ERR_TIMEOUT and drain its copies (drains wait at least 100 ms whatever the
+    limit).  CTAs stop independently, so y may be partly written: every element is
+    untouched or correct.  Then a normal call works."""
     rows, L = 3, 152 * 4 * 64
     x, g, b = (normgen.normal(rows * L, seed=5), normgen.normal(L, 1.0, 0.1, seed=5, tensor_id=1),
                normgen.normal(L, 0.0, 0.1, seed=5, tensor_id=2))
