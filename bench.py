@@ -81,6 +81,9 @@ CONFIGS = {
                     workload="GroupNorm+LeakyReLU(0.01)+x2 bf16 (1024,8192), 512 groups of 16, fp32 arithmetic"),
     "rms_bf16": dict(op="rms", B=112, C=64, S=512 * 512, x=(0.0, 1.0), bf16=True,
                      workload="RMSNorm over dim 1 of bf16 NCHW (112,64,512,512), fp32 arithmetic, eps 1e-5"),
+    "ln_mid": dict(op="ln", rows=256, L=262144, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
+                   workload="LayerNorm fp32 (256, 262144) over the last dim, x~N(0,1), gamma~N(1,0.1), "
+                            "beta~N(0,0.1), eps 1e-5 (rows of mid length: the persistent kernel in 8 row groups)"),
     "ln_rows": dict(op="ln", rows=16384, L=4096, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
                     workload="LayerNorm fp32 (16384, 4096) over the last dim, x~N(0,1), gamma~N(1,0.1), "
                              "beta~N(0,0.1), eps 1e-5 (many short rows)"),
@@ -108,7 +111,7 @@ CONFIGS = {
                                "(1024, 8192); x ~ N(0,1) and W ~ U(-1/sqrt(8192), 1/sqrt(8192)) in bf16, bias ~ "
                                "U(-1/sqrt(8192), 1/sqrt(8192)), gamma ~ N(1,0.1), beta ~ N(0,0.1) fp32; y fp32"),
 }
-EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_rows", "ln_rows_bf16", "gn_bf16", "rms_bf16",
+EXTRA_ORDER = ["rms_small", "gn", "rms", "ln_stress", "ln_mid", "ln_rows", "ln_rows_bf16", "gn_bf16", "rms_bf16",
                "gn_nchw", "gn_nchw_bf16", "gn_nchw_long", "gn_m48", "linear_gn"]
 
 
@@ -230,7 +233,7 @@ def main_kernel_name(cfg) -> str:
             return "ln_rows_kernel"
         if L <= 131072 and L % (8 if bf16 else 4) == 0:
             return "gns_stream_kernel"
-        return "ln_persistent_kernel" if L >= (1 << 20) and not bf16 else "ln_split_apply_kernel"
+        return "ln_persistent_kernel" if L % 4 == 0 and not bf16 else "ln_split_apply_kernel"
     if cfg["op"] == "gn":
         M, bf16 = cfg["C"] // cfg["G"], bool(cfg.get("bf16"))
         if 4 <= M <= 128 and M & (M - 1) == 0:
@@ -259,7 +262,7 @@ def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
     if op == "ln":
         rows, L = cfg["rows"], cfg["L"]
         one_launch = L % 4 == 0 and (L <= (8192 if bf16 else 16384) or (L <= 131072 and L % (8 if bf16 else 4) == 0) or
-                                     (not bf16 and (1 << 20) <= L <= ng.norm_layer_max_resident_row_len()))
+                                     (not bf16 and L <= ng.norm_layer_max_resident_row_len()))
         fn = ng.norm_layer_fwd_bf16 if bf16 else ng.norm_layer_fwd
         return (lambda: fn(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if one_launch else 2)
     if op == "gn":
@@ -604,7 +607,7 @@ def run_config(ng, name, cfg, steps, warmup, stream, flush, l2_bytes, sampler=No
     res = {"name": name, "seconds_per_step": sec, "launches_per_step": launches, "clocks": clocks,
            "t_region_s": t1 - t0, "buffer_sets": nset, "cold_seconds_per_launch": cold,
            "graph_seconds_per_step": graph, "copy_seconds_per_step": copy}
-    if want_e2e:
+    if want_e2e and cfg["op"] != "linear_gn":
         res["e2e"] = run_e2e(ng, cfg, x, g, b, xd, gd, bd, ys[0], ws, ws_bytes, stream, min(steps, 20), world)
     del xs, ys, xd, gd, bd, ws
     torch.cuda.empty_cache()
@@ -670,7 +673,17 @@ def time_oracle(cfg, min_seconds, max_reps=1000, rows_per_step=None, x=None, g=N
     if x is None:
         x, g, b = host_inputs(cfg)
     op = cfg["op"]
-    if op == "ln":
+    if op == "linear_gn":
+        # a bounded sample: the first rows of x through the whole module (float64 matmul + groups)
+        rows = max(1, min(cfg["M"], rows_per_step or 16))
+        (w, bias), (gm, bt) = g, b
+        xs = x[: rows * cfg["K"]]
+        fn = lambda: o.linear_group_lrelu_x2(xs, w, bias, gm, bt, rows, cfg["K"], cfg["N"], cfg["G"], 1e-5, 0.01,  # noqa
+                                             threads=threads)
+        nbytes = algorithmic_bytes(dict(cfg, M=rows))
+        sample = f"{rows} of {cfg['M']} rows of the workload per repetition"
+        used = min(threads, rows)
+    elif op == "ln":
         rows = cfg["rows"] if rows_per_step is None else max(1, min(cfg["rows"], rows_per_step))
         xs = x[: rows * cfg["L"]]
         fn = lambda: o.layer_norm(xs, g, b, rows, cfg["L"], 1e-5, threads=threads)  # noqa: E731
@@ -797,7 +810,7 @@ def main(argv=None):
     sec = dist_max(main_res["seconds_per_step"], world, device="cuda")
     nbytes = algorithmic_bytes(cfg)
     value = weak_scaling_value(nbytes, world, sec)
-    e2e_sec = dist_max(main_res["e2e"]["seconds_per_step"], world, device="cuda")
+    e2e_sec = dist_max(main_res["e2e"]["seconds_per_step"], world, device="cuda") if "e2e" in main_res else None
     peak, peak_note = hbm_peak()
     tflops_peak, tflops_note = bf16_peak()
     achieved = nbytes / main_res["seconds_per_step"] / 1e9
@@ -861,7 +874,8 @@ def main(argv=None):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": DATA,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if cfg.get("bf16") or cfg["op"] == "linear_gn" else "f32", "data": DATA,
             "config": shape_config(args.config, cfg, l2),
             "elements_per_s": round(elements(cfg) * world / sec, 1),
             "same_size_copy": None if not main_res["copy_seconds_per_step"] else {
@@ -873,16 +887,21 @@ def main(argv=None):
                 "us": round(main_res["cold_seconds_per_launch"] * 1e6, 3),
                 "frac_of_measured_peak": round(nbytes / main_res["cold_seconds_per_launch"] / 1e9 / peak, 4),
                 "note": "median single launch after an L2 flush (2x L2 written), CUDA events around each launch"},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-                         "peak_source": peak_note, "traffic_note": traffic_note,
-                         "kernel": main_kernel_name(cfg)},
+            "roofline": ({"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                          "frac": round(achieved / peak, 4), "traffic": traffic,
+                          "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                          "peak_source": peak_note, "traffic_note": traffic_note,
+                          "kernel": main_kernel_name(cfg)} if not algorithmic_flops(cfg) else
+                         {"bound": "tensor", "achieved": round(algorithmic_flops(cfg) / sec / 1e12, 2),
+                          "peak": tflops_peak, "unit": "TFLOP/s",
+                          "frac": round(algorithmic_flops(cfg) / sec / 1e12 / tflops_peak, 4), "traffic": traffic,
+                          "peak_source": tflops_note, "traffic_note": traffic_note, "kernel": main_kernel_name(cfg)}),
             "cpu_baseline": cpu,
-            "e2e": {"value": round(weak_scaling_value(nbytes, world, e2e_sec), 3), "unit": "GB/s",
-                    "h2d_bytes_per_step": main_res["e2e"]["h2d_bytes_per_step"],
-                    "d2h_bytes_per_step": main_res["e2e"]["d2h_bytes_per_step"],
-                    "ms_per_step": round(e2e_sec * 1e3, 4), "note": main_res["e2e"]["note"]},
+            "e2e": None if e2e_sec is None else {
+                "value": round(weak_scaling_value(nbytes, world, e2e_sec), 3), "unit": "GB/s",
+                "h2d_bytes_per_step": main_res["e2e"]["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": main_res["e2e"]["d2h_bytes_per_step"],
+                "ms_per_step": round(e2e_sec * 1e3, 4), "note": main_res["e2e"]["note"]},
             "gpu_launches": main_res["launches_per_step"] * args.steps,
             "clocks": main_res["clocks"],
             "per_config": extras,

@@ -100,14 +100,16 @@ typedef enum {
  *     each CTA's next slices arrive by bulk copy into shared memory, and
  *     the CTAs of a row exchange their partial statistics through
  *     distributed shared memory; x is read from HBM once; no workspace;
- *   - rows of 2^20 or more elements (up to norm_layer_max_resident_row_len()):
- *     a persistent cooperative kernel (one CTA per SM) gives every CTA the
+ *   - longer rows (fp32, up to norm_layer_max_resident_row_len()): a
+ *     persistent cooperative kernel (one CTA per SM) gives every CTA the
  *     same column slice of each row, holds the slice on chip (shared memory,
  *     then registers) from the moment it arrives until y is written, and
- *     merges the row's statistics across the GPU with one bounded grid
- *     barrier per row; x is read from HBM once;
- *   - any other shape (including ragged lengths and misaligned pointers): a
- *     two-kernel path that reads x twice.
+ *     merges the row's statistics across its CTAs with one bounded exchange
+ *     per row; x is read from HBM once.  Rows shorter than about 3 Mi
+ *     elements are spread over groups of CTAs, each group taking every k-th
+ *     row, so that each row's exchange hides behind the group's next rows;
+ *   - any other shape (ragged lengths, misaligned pointers, bf16 rows above
+ *     131,072 elements): a two-kernel path that reads x twice.
  * All produce the same statistics definition.
  */
 size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len);

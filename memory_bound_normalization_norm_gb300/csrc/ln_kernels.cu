@@ -61,8 +61,16 @@
 // (workspace header) is the number of rows the persistent kernel has already
 // processed on this workspace.  A slot therefore only ever holds tags
 // smaller than the one awaited, and a zeroed workspace holds tag 0, which is
-// never awaited.  row_base is read at kernel start and advanced by CTA 0
-// after its last merge, which proves every CTA has read it.  Every wait is
+// never awaited.  row_base is read at kernel start; at its end every CTA
+// counts itself in the header, and the last one (which knows that every CTA
+// has read row_base) resets the count and advances row_base.
+//
+// Row groups.  For rows too short for one grid-wide exchange per row to hide
+// behind the next rows' traffic, the grid is split into `groups` groups of
+// G/groups CTAs: group j takes rows j, j + groups, j + 2 groups, ..., each
+// row split over the group's CTAs, and exchanges records only within the
+// group.  Slots and buffers follow a group's own row sequence; tags use the
+// global row index.  With one group this is the whole grid on every row.  Every wait is
 // bounded by %globaltimer: on timeout a CTA records NORM_ERR_TIMEOUT, drains
 // its own bulk copies, frees its TMEM and returns without writing its slice
 // of the remaining rows (other CTAs may have written theirs).
@@ -283,13 +291,20 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, cta = blockIdx.x;
-    const int64_t R = p.rows;
+    const int NG = p.groups;         // row groups
+    const int Gk = G / NG;           // CTAs per group
+    const int grp = cta / Gk;        // this CTA's group
+    const int crank = cta - grp * Gk; // its rank in the group
+    // The group's rows: local row t is row grp + t * NG of the launch.
+    const int64_t R = p.rows > grp ? (p.rows - grp + NG - 1) / NG : 0;
+    auto grow = [&](int64_t t) { return grp + t * NG; };
     const int64_t L4 = p.row_len >> 2;
-    // CTA c owns n4 = q4 (+1 for the first rem CTAs) float4 of every row,
-    // starting at f0; the merge recomputes every CTA's count the same way.
-    const unsigned q4 = static_cast<unsigned>(L4 / G), rem = static_cast<unsigned>(L4 % G);
-    const int64_t f0 = static_cast<int64_t>(cta) * q4 + min(static_cast<unsigned>(cta), rem);
-    const int n4 = static_cast<int>(q4 + (static_cast<unsigned>(cta) < rem ? 1u : 0u));
+    // CTA rank c owns n4 = q4 (+1 for the first rem ranks) float4 of every row
+    // of its group, starting at f0; the merge recomputes every rank's count
+    // the same way.
+    const unsigned q4 = static_cast<unsigned>(L4 / Gk), rem = static_cast<unsigned>(L4 % Gk);
+    const int64_t f0 = static_cast<int64_t>(crank) * q4 + min(static_cast<unsigned>(crank), rem);
+    const int n4 = static_cast<int>(q4 + (static_cast<unsigned>(crank) < rem ? 1u : 0u));
     const float4 *x4 = reinterpret_cast<const float4 *>(p.x);
     float4 *y4 = reinterpret_cast<float4 *>(p.y);
     const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma);
@@ -330,7 +345,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
         uint64_t *bar = &bar_x[q & 1];
         const uint32_t bytes = static_cast<uint32_t>(n4) * 16u;
         mbar_arrive_expect_tx(bar, bytes + 48u);
-        const float4 *row = x4 + q * L4;
+        const float4 *row = x4 + grow(q) * L4;
         bulk_g2s(&piv_in[q & 1][0], row, 16u, bar, pol_stream);
         bulk_g2s(&piv_in[q & 1][1], row + ((p.row_len >> 1) >> 2), 16u, bar, pol_stream);
         bulk_g2s(&piv_in[q & 1][2], row + (L4 - 1), 16u, bar, pol_stream);
@@ -362,7 +377,10 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     // registers, which frees buffer 0 for beta; gamma goes from buffer 1 to
     // TMEM, which frees buffer 1 for row 1; then beta goes to TMEM.  So row 0
     // crosses the grid while gamma, beta and row 1 are still arriving.
-    if (warp == 0) {
+    // (every group has a row: the host never makes more groups than rows)
+    if (R == 0) {
+        // nothing to do
+    } else if (warp == 0) {
         // ------------------------------------------------ coordinator
         bool fail = false; // the merge of the previous row gave up
         for (int64_t r = -2; r < R; ++r) {
@@ -375,17 +393,15 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             // issued while those stores queue would wait behind them.
             bar_sync_named(LN_BAR_APPLIED, LN_A + 32);
             if (q >= 0 && q < R) {
-                const GridMerge gm = poll_and_merge(records + static_cast<int64_t>(q % LN_SLOTS) * G * 2, G, q4,
-                                                    rem, row_tag(row_base, q) + p.tag_skew, p.timeout_ns);
+                const GridMerge gm =
+                    poll_and_merge(records + (static_cast<int64_t>(q % LN_SLOTS) * G + grp * Gk) * 2, Gk, q4, rem,
+                                   row_tag(row_base, grow(q)) + p.tag_skew, p.timeout_ns);
                 if (!gm.ok) {
                     fail = true;
                     if (lane == 0)
                         record_error(p.err, NORM_ERR_TIMEOUT);
                 } else if (lane == 0) {
                     row_mean[q & 1] = finish_row(piv_k[q & 1], gm.tot, p.eps);
-                    // every CTA has read row_base once CTA 0 has merged the last row
-                    if (q + 1 == R && cta == 0)
-                        st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(R));
                 }
             }
         }
@@ -426,7 +442,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 c = warp_merge(c);
                 if (lane == 0 && !fail) {
                     piv_k[q & 1] = K;
-                    const unsigned tag = row_tag(row_base, q);
+                    const unsigned tag = row_tag(row_base, grow(q));
                     // the store of row q - 2 has read its source
                     bulk_wait_read_all();
                     rec_out[q & 1][0] = tagged(tag, c.mean);
@@ -551,7 +567,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 // y of row r from registers, gamma/beta from TMEM in batches
                 // of LN_GB float4
                 const RowMean rm = row_mean[r & 1];
-                float4 *yr = y4 + r * L4 + f0;
+                float4 *yr = y4 + grow(r) * L4 + f0;
 #pragma unroll
                 for (int bt = 0; bt < LN_NB; ++bt) {
                     float4 g[LN_GB], bb[LN_GB];
@@ -625,6 +641,15 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     // Every TMEM access of every thread is complete before warp 0 frees it.
     tmem_fence_before_sync();
     __syncthreads();
+    // This CTA is done with row_base; the last CTA of the launch advances it
+    // by the launch's rows (and resets the count for the next launch).
+    if (tid == 0) {
+        const unsigned seen = atomicAdd(&p.sync->done, 1u);
+        if (seen == static_cast<unsigned>(G) - 1u) {
+            st_relaxed_gpu_u32(&p.sync->done, 0u);
+            st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(p.rows));
+        }
+    }
     if (warp == 0) {
         tmem_fence_after_sync();
         tmem_dealloc(tmem_base, LN_TMEM_COLS);

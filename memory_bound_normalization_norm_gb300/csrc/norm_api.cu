@@ -22,10 +22,11 @@ using normk::LnParams;
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kWsHeader = sizeof(normk::LnSync);
-// Shortest row for which the automatic choice takes the persistent kernel: a
-// row must stream for longer than a grid barrier takes for the barrier to hide
-// behind the prefetch of the next rows.
-constexpr int64_t kPersistentMinRowLen = int64_t(1) << 20;
+// Shortest row for which the automatic choice takes the persistent kernel
+// (fp32): rows past the cluster kernel's.  Rows shorter than about 1.6 Mi
+// elements are split over row groups (persistent_groups) so that each
+// group's row streams long enough to hide its grid exchange.
+constexpr int64_t kPersistentMinRowLen = 131073;
 // NORM_OPT_LN_PATH value of the streamed cluster kernel, and the longest
 // row the automatic choice gives the row kernel.  Measured on GB300 (GB/s
 // fractions of the copy peak): the row kernel, its CTA sized to the row,
@@ -210,6 +211,7 @@ bool safe_mul(int64_t a, int64_t b, int64_t *out)
 struct LnPlan {
     int path = 0; // 1 persistent, 2 split
     int grid = 0;
+    int groups = 1; // persistent: row groups
     int max_n4 = 0;
     int dyn_smem = 0;
     int parts = 0;
@@ -275,21 +277,60 @@ int64_t persistent_max_row_len(const DeviceState &d)
     return m & ~int64_t(3);
 }
 
+// Row groups of the persistent kernel for `rows` rows of L elements on a grid
+// of at most gmax CTAs, or 0 if no split of the grid holds a row slice.  A
+// group's CTAs must hold its slices (at most max_slice float4 each), and a
+// group's row must stream for about 4 us or more at the HBM rate (4 us *
+// 6.5 TB/s / 8 bytes an element = 3,250,000 / L groups at least) so that the
+// grid exchange, two rows ahead, hides behind it.  Measured on GB300 (fraction
+// of the copy peak): 2.6 us a group row gave 0.73-0.76, 3.9-5.2 us 0.87-0.92.  Among the admissible
+// counts (at most one group per row), the one that leaves the fewest idle
+// row slots (ceil(rows / k) * k) wins; ties go to more groups.
+int persistent_groups(int64_t rows, int64_t L, int gmax, int64_t max_slice)
+{
+    const int64_t L4 = L / 4;
+    const int64_t gk_min = (L4 + max_slice - 1) / max_slice;
+    if (gk_min < 1 || gk_min > gmax)
+        return 0;
+    int64_t kmax = gmax / gk_min;
+    if (kmax > rows)
+        kmax = rows;
+    int64_t kmin = (int64_t(3250000) + L - 1) / L;
+    if (kmin < 1)
+        kmin = 1;
+    if (kmin > kmax)
+        kmin = kmax;
+    int64_t best = kmin, best_slots = (rows + kmin - 1) / kmin * kmin;
+    for (int64_t k = kmin + 1; k <= kmax; ++k) {
+        const int64_t slots = (rows + k - 1) / k * k;
+        if (slots <= best_slots) {
+            best = k;
+            best_slots = slots;
+        }
+    }
+    return static_cast<int>(best);
+}
+
 // Fills the persistent plan if the shape qualifies; returns false if not.
 bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
 {
-    (void)rows;
-    if ((L & 3) != 0 || L > persistent_max_row_len(d))
+    if ((L & 3) != 0 || L > persistent_max_row_len(d) || rows < 1)
         return false;
     const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
-    const int grid = persistent_grid(d);
+    const int gmax = persistent_grid(d);
+    const int groups = persistent_groups(rows, L, gmax, persistent_max_slice(d));
+    if (groups < 1)
+        return false;
+    const int gk = gmax / groups;
+    const int grid = gk * groups;
     const int64_t L4 = L / 4;
-    int64_t max_n4 = (L4 + grid - 1) / grid;
+    int64_t max_n4 = (L4 + gk - 1) / gk;
     if (max_n4 < 1)
         max_n4 = 1;
     pl->path = 1;
     pl->vec4 = true;
     pl->grid = grid;
+    pl->groups = groups;
     pl->max_n4 = static_cast<int>(max_n4);
     pl->dyn_smem = static_cast<int>(2 * ((max_n4 + 7) / 8 * 8) * 16);
     pl->ws_bytes = kWsHeader + static_cast<size_t>(cfg.record_bytes_per_cta) * static_cast<size_t>(grid);
@@ -613,6 +654,7 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
     } else if (ch.persistent) {
         p.tag_skew = static_cast<unsigned>(g_opt_extra_arrivals.load());
         p.max_n4 = pl.max_n4;
+        p.groups = pl.groups;
         e = normk::ln_persistent_launch(p, pl.grid, pl.dyn_smem, stream);
     } else {
         e = normk::ln_split_launch(p, bf16, pl.vec4, stream);

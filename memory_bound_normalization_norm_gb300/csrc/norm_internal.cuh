@@ -643,7 +643,8 @@ cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, 
 // the persistent kernel keeps it consistent from call to call.
 struct LnSync {
     unsigned row_base; // rows the persistent kernel has processed on this workspace (mod 2^32)
-    unsigned pad[63];
+    unsigned done;     // CTAs of the current launch that are done with row_base
+    unsigned pad[62];
 };
 static_assert(sizeof(LnSync) == 256, "LnSync must be 256 bytes");
 
@@ -663,6 +664,7 @@ struct LnParams {
     uint64_t timeout_ns;
     unsigned tag_skew; // test hook: 0, or an offset that makes the grid barrier unreachable
     int max_n4;        // float4 capacity of each shared-memory row buffer
+    int groups;        // persistent: row groups (the grid is groups x CTAs per group)
     int64_t chunk;     // split: elements per CTA (multiple of 4 on the vector path)
     int parts;         // split: CTAs per row (P)
 };

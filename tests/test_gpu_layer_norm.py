@@ -1,7 +1,7 @@
 """LayerNorm on the GPU against the float64 oracle, element by element.
 
 All four paths are covered: the persistent single-read kernel (forced, and chosen
-automatically for long rows), the one-launch row kernel (forced, and chosen
+automatically for long rows, over the whole grid or split into row groups), the one-launch row kernel (forced, and chosen
 automatically for rows of at most 8,192 elements), the thread-block cluster kernel
 shared with GroupNorm (forced, and chosen for fp32 rows of 8,193 to 131,072) and the
 two-kernel split path (forced, and taken for ragged or misaligned rows).  Shapes span several CTAs per row with ragged slices,
@@ -172,6 +172,26 @@ def test_persistent_exchange_200_launches_back_to_back(ng):
         assert bool(torch.isfinite(got).all()), f"input {k}: a launch left NaN in its output"
         worst = float(err.max())
         assert worst <= TOL, f"input {k}: worst launch {int(err.argmax()) * distinct + k} scaled error {worst:.3e}"
+
+
+@pytest.mark.parametrize("rows,L,path", [
+    (256, 262144, AUTO),        # 8 row groups of 19 CTAs (the automatic choice)
+    (64, 1 << 20, AUTO),        # 4 groups of 38
+    (11, (1 << 20) + 4, AUTO),  # 4 groups, 3, 3, 3 and 2 rows
+    (3, 1 << 20, AUTO),         # one row per group
+    (40, 131076, PERSISTENT),   # 25 groups of 6 CTAs, forced
+    (7, 200004, AUTO),          # a length that is not a multiple of the group size
+])
+def test_persistent_row_groups(ng, rows, L, path):
+    """Rows of 131,073 to about 1.6 Mi elements: the persistent kernel splits its grid into
+    row groups, each taking every k-th row with its own grid exchange."""
+    x, g, b = inputs(rows, L, seed=rows + L)
+    want = oracle.layer_norm(x, g, b, rows, L)
+    assert_parity(run_ln(ng, x, g, b, rows, L, path=path), want, f"LN row groups {rows}x{L}")
+    # the cancellation stress through the same groups
+    xs = normgen.normal(rows * L, 1000.0, 1e-2, seed=rows, tensor_id=0)
+    ws = oracle.layer_norm(xs, None, None, rows, L)
+    assert_parity(run_ln(ng, xs, None, None, rows, L, path=path), ws, f"LN row groups stress {rows}x{L}")
 
 
 def test_layer_norm_empty_is_noop(ng):
