@@ -102,7 +102,7 @@ CONFIGS = {
     "gn_nchw_long": dict(op="gn_nchw", N=1, C=128, S=512 * 512, G=32, x=(0.0, 1.0), gamma=(1.0, 0.1),
                          beta=(0.0, 0.1),
                          workload="GroupNorm+LeakyReLU(0.01)+x2 fp32 NCHW (1,128,512,512), 32 groups of 4 "
-                                  "channels x 262144 positions (1,048,576 values: the two-kernel path)"),
+                                  "channels x 262144 positions (1,048,576 values: the persistent kernel)"),
     # the GroupNorm page's whole module: Linear(8192, 8192) on (1024, 8192), then the
     # normalization, one kernel (tensor-core GEMM, group statistics in its epilogue)
     "linear_gn": dict(op="linear_gn", M=1024, K=8192, N=8192, G=512, x=(0.0, 1.0), gamma=(1.0, 0.1),
@@ -241,14 +241,26 @@ def main_kernel_name(cfg) -> str:
         items = M // 4 if M % 4 == 0 else M // 2 if M % 2 == 0 else M
         return "gns_team_kernel" if items <= (128 if bf16 else 256) else "gns_reg_kernel"
     if cfg["op"] == "gn_nchw":
-        return "gns_stream_kernel" if gn_nchw_one_launch(cfg) else "gns_split_apply_kernel"
+        L = cfg["C"] // cfg["G"] * cfg["S"]
+        if L % 4 == 0 and L <= 131072:
+            return "gns_stream_kernel"
+        return "ln_persistent_kernel" if gn_nchw_persistent(cfg) else "gns_split_apply_kernel"
     return "rms_reg_kernel"
 
 
-def gn_nchw_one_launch(cfg) -> bool:
-    """Groups of at most 131,072 values (a multiple of 4) take the one-launch cluster kernel."""
+def gn_nchw_persistent(cfg) -> bool:
+    """fp32 groups longer than 131,072 values with S a multiple of 4, and x of 48 MiB or more, take
+    the persistent kernel."""
     L = cfg["C"] // cfg["G"] * cfg["S"]
-    return L % 4 == 0 and L <= 131072
+    n = cfg["N"] * cfg["C"] * cfg["S"]
+    return not cfg.get("bf16") and cfg["S"] % 4 == 0 and L > 131072 and 4 * n >= 48 << 20
+
+
+def gn_nchw_one_launch(cfg) -> bool:
+    """Groups of at most 131,072 values (a multiple of 4) take the one-launch cluster kernel, longer
+    fp32 ones the persistent kernel; the rest two launches."""
+    L = cfg["C"] // cfg["G"] * cfg["S"]
+    return (L % 4 == 0 and L <= 131072) or gn_nchw_persistent(cfg)
 
 
 def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):

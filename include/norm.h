@@ -237,14 +237,22 @@ norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *ga
  * contiguous.  Their population mean and variance normalize every one of
  * them; gamma/beta [C] are per channel (or NULL: 1 and 0); then LeakyReLU
  * and x + x.  S = 1 is norm_group_lrelu_x2_fwd.
- * workspace     used only by the two-kernel path below: at least
- *               norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, num_groups)
- *               bytes, 16-byte aligned, no initial contents needed.  NULL:
- *               the library allocates its own, stream-ordered
- *               (cudaMallocAsync on `stream`), on first need and keeps it
- *               (such calls must be serialized by the caller; growth
- *               during a stream capture returns NORM_ERR_WORKSPACE).  It must not
- *               be a LayerNorm workspace that is still in use.
+ * workspace     used only by the two-kernel and persistent paths below: at
+ *               least norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S,
+ *               num_groups) bytes, 16-byte aligned, zero-filled once before
+ *               its first use (cudaMemset or norm_layer_workspace_reset).
+ *               The persistent path keeps a header and tagged records at its
+ *               start, consistent from call to call; the two-kernel path
+ *               writes its partials after them (from byte 10,496), so any
+ *               mix of calls may share it as long as they are serialized
+ *               (one stream).  After a NORM_ERR_TIMEOUT it must be
+ *               zero-filled again.  NULL: the library allocates its own,
+ *               stream-ordered (cudaMallocAsync on `stream`), on first need
+ *               and keeps it (such calls must be serialized by the caller;
+ *               growth during a stream capture returns NORM_ERR_WORKSPACE);
+ *               the persistent path then shares the library's LayerNorm
+ *               workspace.  It must not be a LayerNorm workspace that is
+ *               still in use.
  * Paths (L = M*S):
  *   - groups of at most 256 items (4, 2 or 1 elements an item, as for
  *     norm_group_lrelu_x2_fwd): one launch, a team of adjacent lanes per
@@ -259,7 +267,16 @@ norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *ga
  *     its waits are bounded by NORM_OPT_BARRIER_TIMEOUT_NS (a CTA that gives
  *     up records NORM_ERR_TIMEOUT and leaves its part of the remaining
  *     groups of y unwritten);
- *   - longer groups and unaligned vectors: a statistics kernel writes
+ *   - fp32 groups of more than 131,072 values with S a multiple of 4 and
+ *     16-byte aligned x and y, up to norm_layer_max_resident_row_len()
+ *     values, x of 48 MiB or more (smaller x is re-read mostly from L2 by
+ *     the two-kernel path, which is then faster): the persistent LayerNorm
+ *     kernel in its GroupNorm form (one
+ *     launch, x read from HBM once; each segment is split over the CTAs of
+ *     a row group, which exchange partial statistics through the workspace;
+ *     gamma/beta are read per channel; waits bounded as for
+ *     norm_layer_fwd, a timeout leaves y partly unwritten);
+ *   - other long groups and unaligned vectors: a statistics kernel writes
  *     per-chunk partials to the workspace and an apply kernel re-reads x;
  *   - non-vector groups of 257 to 4,096 elements: one warp per group.
  */
@@ -362,7 +379,9 @@ const char *norm_status_string(norm_status_t status);
  *                                force the streamed register kernel, 5 =
  *                                force the team-per-group kernel (groups of
  *                                at most 256 four-element vectors, or 256
- *                                elements when the vector form is off)
+ *                                elements when the vector form is off), 6 =
+ *                                force the persistent single-read kernel (fp32
+ *                                NCHW with S % 4 == 0)
  *                                (error NORM_ERR_UNSUPPORTED where the forced
  *                                path cannot serve the call).
  *   NORM_OPT_GN_CLUSTER          CTAs per group of the register kernel: 0 =

@@ -276,7 +276,13 @@ __device__ __forceinline__ Moments slice_moments(const float4 *buf, int n4, int 
     return m;
 }
 
-__global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p)
+// GN: GroupNorm + LeakyReLU + x2 over NCHW segments instead of LayerNorm
+// rows: row r is segment r (sample r / G, group r % G) of L = M * S values;
+// gamma/beta are per channel (channel g * M + e / S for element e), read
+// from L1 per 4-element vector (S % 4 == 0) instead of held in TMEM, and the
+// output is 2 LReLU((x - mean) * rstd * gamma + beta).
+template <bool GN>
+__global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p, GnPersist gp_)
 {
     extern __shared__ __align__(128) float4 ln_smem[];
     __shared__ __align__(8) uint64_t bar_x[2];
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 
     // The CTA holds all 512 TMEM columns (it is alone on its SM: its 512
     // threads at 128 registers take the whole register file).
-    if (warp == 0)
+    if (!GN && warp == 0)
         tmem_alloc(&tmem_base_s, LN_TMEM_COLS);
     if (tid == 0) {
         mbar_init(&bar_x[0], 1);
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     __syncthreads();
     tmem_fence_after_sync();
     const unsigned row_base = row_base_s;
-    const uint32_t tmem_base = tmem_base_s;
+    const uint32_t tmem_base = GN ? 0u : tmem_base_s;
     bool aborted = false;
 
     // Row q's slice, plus the three 16-byte pieces of the row that hold its
@@ -480,8 +486,16 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
         if (issuer) {
             issue_x(0);
             issued = 1;
-            issue_param(g4, 1, &bar_g);
-            g_out = true;
+            if (GN) {
+                // no gamma/beta to stage: row 1 goes to buffer 1 at once
+                if (R > 1) {
+                    issue_x(1);
+                    issued = 2;
+                }
+            } else {
+                issue_param(g4, 1, &bar_g);
+                g_out = true;
+            }
         }
         // This thread's TMEM cells: lane 32*(warp % 4) + lane of its warp's
         // quarter, LN_TM_COLS columns from (warp / 4 - 1) * LN_TM_COLS:
@@ -530,7 +544,17 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 aborted = true;
                 break;
             }
-            if (r == -2) {
+            if (GN && r == -2) {
+                // row 0: reduce it with the statistics warps, then hold it in
+                // registers (buffer 0 takes row 2 at r = -1)
+                help_reduce(0);
+#pragma unroll
+                for (int k = 0; k < LN_V; ++k) {
+                    const int i = at + k * LN_A;
+                    v[k] = (i < n4) ? ln_smem[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                __syncwarp();
+            } else if (r == -2) {
                 // row 0: reduce it with the statistics warps, then hold it in
                 // registers, so its buffer can take beta
                 help_reduce(0);
@@ -563,7 +587,51 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                     b_out = false;
                 bar_sync_named(LN_BAR_FILL, LN_A);
             }
-            if (r >= 0) {
+            if (GN && r >= 0) {
+                // y of segment r from registers: 2 LReLU(d * rstd * gamma_c +
+                // beta_c), gamma/beta doubled (LReLU is positively homogeneous
+                // and doubling is exact).  Vector k of this thread starts at
+                // element e_k = e_0 + 4 LN_A k of the segment; its channel is
+                // e_k / S within the group, tracked incrementally.
+                const RowMean rm = row_mean[r & 1];
+                const int64_t gr = grow(r);
+                const int64_t cbase = (gr % gp_.G) * gp_.M;
+                float4 *yr = y4 + gr * L4 + f0;
+                const uint32_t S = gp_.S, e0 = 4u * static_cast<uint32_t>(f0 + at);
+                uint32_t cq = e0 / S, rq = e0 - cq * S;
+                const float *gp = p.gamma ? static_cast<const float *>(p.gamma) + cbase : nullptr;
+                const float *bp = p.beta ? static_cast<const float *>(p.beta) + cbase : nullptr;
+#pragma unroll
+                for (int k = 0; k < LN_V; ++k) {
+                    const int i = at + k * LN_A;
+                    if (i < n4) {
+                        const float gv = gp ? __ldg(gp + cq) : 1.f, bv = bp ? __ldg(bp + cq) : 0.f;
+                        const float g2 = gv + gv, b2 = bv + bv;
+                        float4 o;
+                        o.x = fmaf(((v[k].x - rm.hi) - rm.lo) * rm.rstd, g2, b2);
+                        o.y = fmaf(((v[k].y - rm.hi) - rm.lo) * rm.rstd, g2, b2);
+                        o.z = fmaf(((v[k].z - rm.hi) - rm.lo) * rm.rstd, g2, b2);
+                        o.w = fmaf(((v[k].w - rm.hi) - rm.lo) * rm.rstd, g2, b2);
+                        o.x = o.x > 0.f ? o.x : gp_.slope * o.x;
+                        o.y = o.y > 0.f ? o.y : gp_.slope * o.y;
+                        o.z = o.z > 0.f ? o.z : gp_.slope * o.z;
+                        o.w = o.w > 0.f ? o.w : gp_.slope * o.w;
+                        st_stream_f4(yr + i, o, pol_stream);
+                    }
+                    // next vector: 4 LN_A elements on
+                    rq += 4u * LN_A;
+                    if (S >= 4u * LN_A) {
+                        if (rq >= S) {
+                            rq -= S;
+                            ++cq;
+                        }
+                    } else {
+                        const uint32_t e = e0 + 4u * LN_A * static_cast<uint32_t>(k + 1);
+                        cq = e / S;
+                        rq = e - cq * S;
+                    }
+                }
+            } else if (r >= 0) {
                 // y of row r from registers, gamma/beta from TMEM in batches
                 // of LN_GB float4
                 const RowMean rm = row_mean[r & 1];
@@ -650,7 +718,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             st_relaxed_gpu_u32(&p.sync->row_base, row_base + static_cast<unsigned>(p.rows));
         }
     }
-    if (warp == 0) {
+    if (!GN && warp == 0) {
         tmem_fence_after_sync();
         tmem_dealloc(tmem_base, LN_TMEM_COLS);
     }
@@ -891,7 +959,7 @@ LnPersistentConfig ln_persistent_config()
 cudaError_t ln_persistent_static_smem(int *bytes)
 {
     cudaFuncAttributes a;
-    const cudaError_t e = cudaFuncGetAttributes(&a, ln_persistent_kernel);
+    const cudaError_t e = cudaFuncGetAttributes(&a, ln_persistent_kernel<false>);
     if (e == cudaSuccess)
         *bytes = static_cast<int>(a.sharedSizeBytes);
     return e;
@@ -899,21 +967,28 @@ cudaError_t ln_persistent_static_smem(int *bytes)
 
 cudaError_t ln_persistent_setup(int max_dynamic_smem)
 {
-    return cudaFuncSetAttribute(ln_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(ln_persistent_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+    if (e != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(ln_persistent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 max_dynamic_smem);
 }
 
 cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, ln_persistent_kernel, LN_THREADS, dyn_smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, ln_persistent_kernel<false>, LN_THREADS,
+                                                         dyn_smem);
 }
 
-cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream)
+cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream, const GnPersist *gn)
 {
     LnParams args = p;
-    void *kargs[] = {&args};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ln_persistent_kernel), dim3(grid),
-                                       dim3(LN_THREADS), kargs, static_cast<size_t>(dyn_smem), stream);
+    GnPersist gargs = gn ? *gn : GnPersist{1, 1, 4, 0.f};
+    void *kargs[] = {&args, &gargs};
+    const void *k = gn ? reinterpret_cast<const void *>(ln_persistent_kernel<true>)
+                       : reinterpret_cast<const void *>(ln_persistent_kernel<false>);
+    return cudaLaunchCooperativeKernel(k, dim3(grid), dim3(LN_THREADS), kargs, static_cast<size_t>(dyn_smem), stream);
 }
 
 int64_t ln_rows_max_row_len()

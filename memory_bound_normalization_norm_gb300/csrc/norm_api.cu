@@ -340,11 +340,17 @@ bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
 // ------------------------------------------------------------------ GN plan
 
 // Segment GroupNorm paths (NORM_OPT_GN_PATH values).
-constexpr int kGnReg = 1, kGnSplit = 2, kGnWarp = 3, kGnStream = 4, kGnTeam = 5;
+constexpr int kGnReg = 1, kGnSplit = 2, kGnWarp = 3, kGnStream = 4, kGnTeam = 5, kGnPersistent = 6;
 // Shortest CTA slice (vectors) for which the automatic choice streams.
 constexpr int64_t kGnStreamMinPer = 256;
 // Longest non-vector segment the warp path takes on its own.
 constexpr int64_t kGnWarpMaxLen = 4096;
+// Smallest x (bytes) for which the automatic choice takes the persistent path
+// over the two-kernel one: below it the second read of x mostly hits L2.
+// Measured on GB300 with segments of 262,144 and 1,048,576 values: 33.5 MB
+// of x took 20.8-21.5 us by two kernels and 22.2-24.9 us persistent; 67 MB
+// took 39.3 and 35.6 us; 134 MB 66.2 and 56.6 us.
+constexpr size_t kGnPersistentMinBytes = size_t(48) << 20;
 
 struct GnPlan {
     int path = 0;
@@ -376,7 +382,18 @@ int stream_auto_cluster(int64_t L4, int64_t cap)
     return 0;
 }
 
-// Partials of the split path: R * P triples; P as the LayerNorm split path.
+// Offset of the split path's partials in a GroupNorm workspace: past the
+// header and records of the persistent path at its largest grid, so that
+// neither path overwrites what the other keeps there.
+size_t gn_split_offset()
+{
+    const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
+    const size_t b = kWsHeader + static_cast<size_t>(cfg.record_bytes_per_cta) * static_cast<size_t>(cfg.max_grid);
+    return (b + 255) & ~size_t(255);
+}
+
+// Partials of the split path: R * P triples after gn_split_offset(); P as the
+// LayerNorm split path.
 void plan_gn_split(int64_t R, int64_t L, bool vec4, const DeviceState &d, GnPlan *pl)
 {
     LnPlan lp;
@@ -385,7 +402,7 @@ void plan_gn_split(int64_t R, int64_t L, bool vec4, const DeviceState &d, GnPlan
     pl->vec4 = vec4;
     pl->parts = lp.parts;
     pl->chunk = lp.chunk;
-    pl->ws_bytes = static_cast<size_t>(R) * static_cast<size_t>(lp.parts) * 16u;
+    pl->ws_bytes = gn_split_offset() + static_cast<size_t>(R) * static_cast<size_t>(lp.parts) * 16u;
 }
 
 // Upper bound of plan_gn_split's workspace over both vector forms.
@@ -439,7 +456,7 @@ norm_status_t norm_set_option(norm_option_t option, int64_t value)
         g_opt_ln_ctas = value;
         return NORM_OK;
     case NORM_OPT_GN_PATH:
-        if (value > 5)
+        if (value > 6)
             return NORM_ERR_INVALID_ARG;
         g_opt_gn_path = value;
         return NORM_OK;
@@ -784,7 +801,14 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     const int64_t team_items = L / team_elems;
     const bool team_ok = team_items <= normk::gns_team_max_items();
     const bool team_auto = team_ok && (team_items <= normk::gns_team_max_items() / 2 || !bf16 || !cluster);
+    // Persistent path (the LayerNorm persistent kernel in its GroupNorm form):
+    // fp32, each 4-element vector inside one channel (S % 4 == 0), x read
+    // from HBM once for segments too long for a cluster to hold.
+    LnPlan pp;
+    const bool pers_ok = !bf16 && vec4 && (S & 3) == 0 && plan_persistent(R, L, *d, &pp);
     GnPlan pl;
+    if (opt == kGnPersistent && !pers_ok)
+        return NORM_ERR_UNSUPPORTED;
     if (opt == kGnTeam && !team_ok)
         return NORM_ERR_UNSUPPORTED;
     if (opt == kGnReg && !cluster)
@@ -801,6 +825,8 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         pl.path = kGnStream;
     else if (cluster)
         pl.path = kGnReg;
+    else if (pers_ok && L >= kPersistentMinRowLen && nb >= kGnPersistentMinBytes)
+        pl.path = kGnPersistent;
     else if (!nchw || (!vec4 && L <= kGnWarpMaxLen))
         pl.path = kGnWarp;
     else
@@ -831,6 +857,42 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         e = normk::gns_warp_launch(p, bf16, d->sm_count, stream);
     } else if (pl.path == kGnTeam) {
         e = normk::gns_team_launch(p, bf16, team_elems, d->sm_count, stream);
+    } else if (pl.path == kGnPersistent) {
+        // Header and tagged records at the start of the workspace: the
+        // library's LayerNorm workspace, or the caller's (zero-filled once;
+        // the launches advance its row base and the split path never writes
+        // there).
+        void *ws = workspace;
+        if (!ws) {
+            st = grow_library_workspace(&d->ws, &d->ws_bytes, pp.ws_bytes, true, stream);
+            if (st != NORM_OK)
+                return st;
+            ws = d->ws;
+        } else if (workspace_bytes < pp.ws_bytes) {
+            return NORM_ERR_WORKSPACE;
+        }
+        LnParams lp;
+        std::memset(&lp, 0, sizeof(lp));
+        lp.x = x;
+        lp.gamma = gamma;
+        lp.beta = beta;
+        lp.y = y;
+        lp.rows = R;
+        lp.row_len = L;
+        lp.eps = eps;
+        lp.sync = static_cast<normk::LnSync *>(ws);
+        lp.part = reinterpret_cast<float4 *>(static_cast<char *>(ws) + kWsHeader);
+        lp.err = p.err;
+        lp.timeout_ns = p.timeout_ns;
+        lp.tag_skew = static_cast<unsigned>(g_opt_extra_arrivals.load());
+        lp.max_n4 = pp.max_n4;
+        lp.groups = pp.groups;
+        normk::GnPersist gp;
+        gp.G = num_groups;
+        gp.M = static_cast<uint32_t>(M);
+        gp.S = static_cast<uint32_t>(S);
+        gp.slope = negative_slope;
+        e = normk::ln_persistent_launch(lp, pp.grid, pp.dyn_smem, stream, &gp);
     } else {
         plan_gn_split(R, L, vec4, *d, &pl);
         void *ws = workspace;
@@ -843,16 +905,17 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         } else if (workspace_bytes < pl.ws_bytes) {
             return NORM_ERR_WORKSPACE;
         }
+        float4 *part = reinterpret_cast<float4 *>(static_cast<char *>(ws) + gn_split_offset());
         LnParams lp;
         std::memset(&lp, 0, sizeof(lp));
         lp.x = x;
         lp.rows = R;
         lp.row_len = L;
         lp.eps = eps;
-        lp.part = static_cast<float4 *>(ws);
+        lp.part = part;
         lp.chunk = pl.chunk;
         lp.parts = pl.parts;
-        p.part = static_cast<const float4 *>(ws);
+        p.part = part;
         p.chunk = pl.chunk;
         p.parts = pl.parts;
         e = normk::ln_split_stats_launch(lp, bf16, pl.vec4, stream);
@@ -938,7 +1001,11 @@ size_t norm_group_lrelu_x2_nchw_workspace_bytes(int64_t N, int64_t C, int64_t S,
     DeviceState *d = nullptr;
     if (device_state(&d) != NORM_OK)
         return 0;
-    return gn_split_ws_bound(R, L, *d);
+    size_t bytes = gn_split_ws_bound(R, L, *d);
+    LnPlan pp;
+    if ((S & 3) == 0 && plan_persistent(R, L, *d, &pp) && pp.ws_bytes > bytes)
+        bytes = pp.ws_bytes;
+    return bytes;
 }
 
 norm_status_t norm_group_lrelu_x2_nchw_fwd(const float *x, const float *gamma, const float *beta, float *y, int64_t N,

@@ -518,21 +518,28 @@ __device__ __forceinline__ Moments shfl_xor_moments(const Moments &a, int lane_m
 }
 
 // Butterfly merge over the 32 lanes of a warp; every lane ends with the
-// result.  The order of merges is fixed, so the result is deterministic.
+// result.  Each step is Chan's update with the lower lane's partial (lo)
+// first and the upper lane's (up) second, on both partners: n and
+// lo.m2 + up.m2 are symmetric, and delta = up.mean - lo.mean is the
+// partners' difference negated exactly on the upper lane, so both compute
+// the same bits and the result is deterministic.
 __device__ __forceinline__ Moments warp_merge(Moments a)
 {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        Moments b = shfl_xor_moments(a, o);
-        // Merge in lane order so both partners compute the same value.
-        const int lane = threadIdx.x & 31;
-        if (lane & o) {
-            Moments lo = b;
-            chan_merge(lo, a);
-            a = lo;
-        } else {
-            chan_merge(a, b);
-        }
+        const Moments b = shfl_xor_moments(a, o);
+        const bool upper = (lane & o) != 0;
+        const float n = a.n + b.n;
+        const float d = b.mean - a.mean;
+        const float delta = upper ? -d : d;
+        const float up_n = upper ? a.n : b.n;
+        const float lo_n = upper ? b.n : a.n;
+        const float lo_mean = upper ? b.mean : a.mean;
+        const float f = n > 0.f ? up_n / n : 0.f;
+        a.mean = fmaf(delta, f, lo_mean);
+        a.m2 = (a.m2 + b.m2) + delta * delta * lo_n * f;
+        a.n = n;
     }
     return a;
 }
@@ -683,7 +690,17 @@ cudaError_t ln_persistent_static_smem(int *bytes);
 cudaError_t ln_persistent_setup(int max_dynamic_smem);
 // Number of co-resident CTAs per SM for `dyn_smem` bytes.
 cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm);
-cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream);
+// The persistent kernel's GroupNorm form: row r is segment (r / G, r % G) of
+// M channels x S positions (S % 4 == 0); gamma/beta of LnParams are per
+// channel [G * M]; the output is 2 LReLU((x - mean) * rstd * gamma + beta).
+struct GnPersist {
+    int64_t G;
+    uint32_t M, S;
+    float slope;
+};
+// gn: null for LayerNorm, else the GroupNorm form over NCHW segments.
+cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream,
+                                 const GnPersist *gn = nullptr);
 
 // Two-kernel LayerNorm (partials, then merge + apply); any shape.  bf16:
 // the tensors are bf16, else fp32.  vec4: rows are a multiple of 4 elements

@@ -76,8 +76,8 @@ def test_options_validate_and_round_trip(lib):
     assert raw.norm_set_option(lib.NORM_OPT_BARRIER_TIMEOUT_NS, 12345) == OK
     assert raw.norm_get_option(lib.NORM_OPT_BARRIER_TIMEOUT_NS) == 12345
     assert raw.norm_set_option(lib.NORM_OPT_BARRIER_TIMEOUT_NS, old) == OK
-    assert raw.norm_set_option(lib.NORM_OPT_GN_PATH, 6) == INVALID
-    for path in (5, 4, 3, 2, 1, 0):
+    assert raw.norm_set_option(lib.NORM_OPT_GN_PATH, 7) == INVALID
+    for path in (6, 5, 4, 3, 2, 1, 0):
         assert raw.norm_set_option(lib.NORM_OPT_GN_PATH, path) == OK
         assert raw.norm_get_option(lib.NORM_OPT_GN_PATH) == path
     for bad in (3, 5, 12, 32, -1):

@@ -216,3 +216,16 @@ def test_group_norm_nchw_bf16(ng, N, C, S, G, path, cluster):
     # in place
     ng.norm_group_lrelu_x2_nchw_fwd_bf16(xb.t, gb.t, bb.t, xb.t, N, C, S, G, 1e-5, 0.01)
     assert_bf16_parity(xb.values(), want, f"GN NCHW bf16 in place ({N},{C},{S})/{G}")
+
+
+def test_group_norm_nchw_bf16_refuses_the_persistent_path(ng):
+    # the persistent kernel is fp32 only; the automatic choice takes the two-kernel path
+    N, C, S, G = 1, 128, 65536, 32
+    xb, yb = BGuarded(N * C * S, bf16_inputs(N * C * S, seed=3)), BGuarded(N * C * S)
+    ng.norm_set_option(ng.NORM_OPT_GN_PATH, 6)
+    try:
+        with pytest.raises(ng.NormError) as e:
+            ng.norm_group_lrelu_x2_nchw_fwd_bf16(xb.t, None, None, yb.t, N, C, S, G, 1e-5, 0.01)
+        assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_GN_PATH, 0)

@@ -5,10 +5,12 @@ A group is its M = C/G channels at all S = H*W positions, M*S contiguous values.
 Covered: the register kernel with one CTA per group (channel-per-vector, per-element
 and S = 1 channel maps), thread-block clusters of 2..16 CTAs (automatic and forced,
 ragged slices), its streamed form (bulk copies into double-buffered shared memory,
-clusters walking many groups, bounded waits that give up cleanly), the two-kernel path (vector and scalar, caller and library
-workspace, more than 65,535 groups), the warp path, NULL affine, in place,
-misaligned pointers, cancellation-heavy inputs, and the (8, 512, 64, 64) 32-group
-workload.
+clusters walking many groups, bounded waits that give up cleanly), the persistent
+single-read kernel in its GroupNorm form (row groups, channel maps with S below and above
+a CTA's vector stride, a caller workspace shared with the two-kernel path, bounded
+waits), the two-kernel path (vector and scalar, caller and library workspace, more
+than 65,535 groups), the warp path, NULL affine, in place, misaligned pointers,
+cancellation-heavy inputs, and the (8, 512, 64, 64) 32-group workload.
 """
 import numpy as np
 import pytest
@@ -19,7 +21,7 @@ from gpu_util import Guarded, assert_parity
 
 pytestmark = pytest.mark.gpu
 
-REG, SPLIT, WARP, STREAM, TEAM = 1, 2, 3, 4, 5
+REG, SPLIT, WARP, STREAM, TEAM, PERS = 1, 2, 3, 4, 5, 6
 
 
 @pytest.fixture(scope="module")
@@ -227,8 +229,8 @@ def test_streamed_tiny_wait_limit_gives_up_cleanly(ng):
 # ------------------------------------------------------------------ two-kernel path
 
 @pytest.mark.parametrize("N,C,S,G,path", [
-    (1, 128, 65536, 32, 0),  # L = 262144: longer than a 16-CTA cluster holds
-    (2, 8, 36000, 2, 0),     # L = 144000
+    (1, 128, 65536, 32, SPLIT),  # L = 262144: longer than a 16-CTA cluster holds
+    (2, 8, 36000, 2, SPLIT),     # L = 144000
     (3, 12, 7, 3, SPLIT),    # vector form, short groups
     (3, 9, 5, 3, SPLIT),     # scalar form (L = 15)
     (2, 6, 2001, 3, 0),      # scalar form, L = 4002 ... taken by the warp path
@@ -242,10 +244,10 @@ def test_split(ng, N, C, S, G, path):
 def test_split_large(ng, N, C, S, G):
     # 50 and 60 MB of x through the two-kernel path, groups of 524,288 and
     # 1,048,576 values
-    check(ng, N, C, S, G, seed=S + G)
+    check(ng, N, C, S, G, seed=S + G, path=SPLIT)
     x, g, b = inputs(N, C, S, S + G)
     want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
-    assert_parity(run(ng, x, g, b, N, C, S, G, inplace=True), want, "GN NCHW large split in place")
+    assert_parity(run(ng, x, g, b, N, C, S, G, path=SPLIT, inplace=True), want, "GN NCHW large split in place")
 
 
 def test_split_caller_workspace(ng):
@@ -253,7 +255,7 @@ def test_split_caller_workspace(ng):
     N, C, S, G = 1, 64, 8192, 4
     need = ng.norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, G)
     assert need > 0
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     check(ng, N, C, S, G, seed=31, path=SPLIT, workspace=ws, ws_bytes=need)
     x, g, b = inputs(N, C, S, 31)
     with pytest.raises(ng.NormError) as e:
@@ -264,6 +266,108 @@ def test_split_caller_workspace(ng):
 def test_split_many_groups_fold_grid(ng):
     # more groups than one grid dimension holds (65535)
     check(ng, 70000, 4, 2, 1, seed=32, path=SPLIT)
+
+
+# ------------------------------------------------------------------ persistent kernel, GroupNorm form
+
+@pytest.mark.parametrize("N,C,S,G,path", [
+    (1, 128, 65536, 32, PERS), # L = 262144: 32 segments over row groups
+    (2, 8, 36000, 2, PERS),    # L = 144000, 4 segments: a row group each
+    (1, 4, 262144, 1, PERS),   # L = 1,048,576: one segment over the whole grid
+    (2, 6, 65540, 3, PERS),    # L = 131080: S not a multiple of a CTA's vector stride
+    (2, 2048, 4, 16, PERS),    # S = 4: a new channel at every vector
+    (3, 96, 12, 8, PERS),      # S = 12: a new channel every three vectors
+    (64, 64, 4096, 8, PERS),   # 512 segments of 32,768: many segments per row group
+    (5, 10, 8, 5, PERS),       # L = 16: fewer vectors than a row group has CTAs
+])
+def test_persistent(ng, N, C, S, G, path):
+    check(ng, N, C, S, G, seed=N + C + S + G, path=path)
+
+
+@pytest.mark.parametrize("N,C,S,G", [(3, 64, 65536, 8), (3, 40, 131072, 5)])
+def test_persistent_large(ng, N, C, S, G):
+    # the two-kernel path's large cases (x of 48 and 60 MiB): the automatic choice
+    # is the persistent kernel, one read of x
+    check(ng, N, C, S, G, seed=S + G + 1)
+    x, g, b = inputs(N, C, S, S + G + 1)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    assert_parity(run(ng, x, g, b, N, C, S, G, inplace=True), want, "GN NCHW persistent in place")
+
+
+def test_persistent_long_workload(ng):
+    """(1, 128, 512, 512), 32 groups: 32 segments of 1,048,576 values."""
+    check(ng, 1, 128, 512 * 512, 32, seed=0)
+
+
+@pytest.mark.parametrize("slope", [0.0, 0.2, 1.0, -0.5])
+def test_persistent_slopes_and_no_affine(ng, slope):
+    N, C, S, G = 2, 8, 36000, 2
+    check(ng, N, C, S, G, seed=72, slope=slope, path=PERS)
+    x, _, _ = inputs(N, C, S, seed=73, affine=False)
+    want = oracle.group_lrelu_x2_nchw(x, None, None, N, C, S, G, slope=slope, f64=True)
+    assert_parity(run(ng, x, None, None, N, C, S, G, slope=slope, path=PERS), want,
+                  f"GN persistent no affine {slope}")
+
+
+def test_persistent_and_split_share_a_caller_workspace(ng):
+    """The persistent path keeps its header and records at the start of the workspace and
+    the two-kernel path writes its partials after them: calls of both, in any order, on one
+    zero-filled workspace stay correct."""
+    import torch
+    N, C, S, G = 2, 8, 36000, 2
+    need = ng.norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, G)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    x, g, b = inputs(N, C, S, seed=74)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    for path in (PERS, SPLIT, PERS, 0, SPLIT, SPLIT, PERS):
+        assert_parity(run(ng, x, g, b, N, C, S, G, path=path, workspace=ws, ws_bytes=need), want,
+                      f"shared workspace path={path}")
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, N, C, S, G, path=PERS, workspace=ws, ws_bytes=64)
+    assert e.value.status == ng.NORM_ERR_WORKSPACE
+
+
+def test_persistent_refusals(ng):
+    x, g, b = inputs(2, 6, 2001, seed=75)  # S % 4 != 0: a vector would straddle two channels
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, 2, 6, 2001, 3, path=PERS)
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+    x, g, b = inputs(2, 16, 64, seed=75)
+    with pytest.raises(ng.NormError) as e:
+        run(ng, x, g, b, 2, 16, 64, 4, path=PERS, offset=1)  # not 16-byte aligned
+    assert e.value.status == ng.NORM_ERR_UNSUPPORTED
+
+
+def test_persistent_tiny_wait_limit_gives_up_cleanly(ng):
+    """With a 1 ns limit the waits that are not over at their first look give up: the call
+    records NORM_ERR_TIMEOUT (or finishes), every element of y keeps its previous value or
+    holds its correct result, and the next call with the default limit is correct (the
+    library's workspace is reset when the timeout is read)."""
+    N, C, S, G = 3, 64, 16384, 8  # L = 131072, 24 segments, forced
+    x, g, b = inputs(N, C, S, seed=76)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    old = ng.norm_get_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS)
+    xb, gb, bb = Guarded(N * C * S, x), Guarded(C, g), Guarded(C, b)
+    timeouts = 0
+    for _ in range(3):
+        yb = Guarded(N * C * S)
+        ng.norm_set_option(ng.NORM_OPT_GN_PATH, PERS)
+        ng.norm_set_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS, 1)
+        try:
+            ng.norm_group_lrelu_x2_nchw_fwd(xb.t, gb.t, bb.t, yb.t, N, C, S, G, 1e-5, 0.01)
+            status = ng.norm_last_error()
+        finally:
+            ng.norm_set_option(ng.NORM_OPT_BARRIER_TIMEOUT_NS, old)
+            ng.norm_set_option(ng.NORM_OPT_GN_PATH, 0)
+        assert status in (ng.NORM_OK, ng.NORM_ERR_TIMEOUT)
+        timeouts += status == ng.NORM_ERR_TIMEOUT
+        got = yb.numpy().astype(np.float64)
+        untouched = np.isnan(got)  # the guard sentinel is a NaN no kernel writes
+        ok = np.abs(got - want) <= 1e-4 * (1.0 + np.abs(want))
+        assert np.all(untouched | ok), "an element of y is neither untouched nor correct"
+        assert yb.guards_intact()
+    assert timeouts > 0, "a 1 ns limit must make some wait give up"
+    assert_parity(run(ng, x, g, b, N, C, S, G, path=PERS), want, "GN NCHW persistent after a timeout")
 
 
 # ------------------------------------------------------------------ warp path
@@ -287,7 +391,8 @@ def test_no_affine_in_place_and_misaligned(ng, N, C, S, G):
     assert_parity(run(ng, x, g, b, N, C, S, G, offset=1, inplace=True), want, "GN NCHW misaligned in place")
 
 
-@pytest.mark.parametrize("path,cluster", [(REG, 1), (REG, 4), (STREAM, 1), (STREAM, 4), (SPLIT, 0), (WARP, 0)])
+@pytest.mark.parametrize("path,cluster", [(REG, 1), (REG, 4), (STREAM, 1), (STREAM, 4), (SPLIT, 0), (WARP, 0),
+                                          (PERS, 0)])
 def test_in_place_every_path(ng, path, cluster):
     N, C, S, G = 3, 32, 512, 4
     x, g, b = inputs(N, C, S, seed=43)
@@ -301,7 +406,8 @@ def test_slopes(ng, slope):
     check(ng, 2, 64, 256, 16, seed=44, slope=slope)
 
 
-@pytest.mark.parametrize("path,cluster", [(REG, 0), (REG, 16), (STREAM, 0), (STREAM, 8), (SPLIT, 0), (WARP, 0)])
+@pytest.mark.parametrize("path,cluster", [(REG, 0), (REG, 16), (STREAM, 0), (STREAM, 8), (SPLIT, 0), (WARP, 0),
+                                          (PERS, 0)])
 def test_cancellation(ng, path, cluster):
     # x ~ N(1000, 0.01^2): the mean is 1e5 standard deviations from zero
     N, C, S, G = 2, 16, 4096, 2
