@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
     pdl_begin();
     const int col0 = blockIdx.x * (GN_THREADS * U) + threadIdx.x;
     using R = Raw4<T>;
-    float4 g[U], b[U];
+    float2 g[U][2], b[U][2]; // gamma/beta of the vector's two pairs
     typename R::type cur[U], nxt[U], nx2[U];
     // gamma and beta are held doubled: 2 LReLU(t) = LReLU(2 t) and doubling is
     // exact, so the x + x costs nothing per element and the result is the same
@@ -83,11 +83,16 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
     for (int u = 0; u < U; ++u) {
         const int c = col0 + u * GN_THREADS;
         const bool in = c < C4;
-        g[u] = (in && gamma) ? Io<T>::ld4_ro(gamma + 4 * c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
-        b[u] = (in && beta) ? Io<T>::ld4_ro(beta + 4 * c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
-        g[u] = make_float4(g[u].x + g[u].x, g[u].y + g[u].y, g[u].z + g[u].z, g[u].w + g[u].w);
-        b[u] = make_float4(b[u].x + b[u].x, b[u].y + b[u].y, b[u].z + b[u].z, b[u].w + b[u].w);
+        const float4 gv = (in && gamma) ? Io<T>::ld4_ro(gamma + 4 * c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float4 bv = (in && beta) ? Io<T>::ld4_ro(beta + 4 * c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g[u][0] = make_float2(gv.x + gv.x, gv.y + gv.y);
+        g[u][1] = make_float2(gv.z + gv.z, gv.w + gv.w);
+        b[u][0] = make_float2(bv.x + bv.x, bv.y + bv.y);
+        b[u][1] = make_float2(bv.z + bv.z, bv.w + bv.w);
     }
+    const float2 slope2 = make_float2(slope, slope);
+    // LReLU(t) = max(t, slope t) for slope <= 1, min(t, slope t) above
+    const bool steep = slope > 1.f;
     auto load_row = [&](int64_t n, typename R::type *dst) {
         const T *xr = x + n * C4 * 4;
 #pragma unroll
@@ -115,23 +120,27 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
         for (int u = 0; u < U; ++u) {
             const int c = col0 + u * GN_THREADS;
             // C4 is a multiple of TPG, so whole groups are in or out of range
-            // together and every lane takes part in the shuffles.
+            // together and every lane takes part in the shuffles.  The
+            // arithmetic is in f32x2 pairs.
             const float4 cv = R::get(cur[u]);
-            const float mean = group_sum<TPG>((cv.x + cv.y) + (cv.z + cv.w)) * invM;
-            const float dx = cv.x - mean, dy = cv.y - mean, dz = cv.z - mean, dw = cv.w - mean;
-            const float m2 = group_sum<TPG>((dx * dx + dy * dy) + (dz * dz + dw * dw));
+            const float2 xl = make_float2(cv.x, cv.y), xh = make_float2(cv.z, cv.w);
+            const float2 s2 = __fadd2_rn(xl, xh);
+            const float mean = group_sum<TPG>(s2.x + s2.y) * invM;
+            const float2 nm = make_float2(-mean, -mean);
+            const float2 dl = __fadd2_rn(xl, nm), dh = __fadd2_rn(xh, nm);
+            const float2 q2 = __ffma2_rn(dh, dh, __fmul2_rn(dl, dl));
+            const float m2 = group_sum<TPG>(q2.x + q2.y);
             const float rstd = rsqrtf(fmaf(m2, invM, eps));
             if (c < C4) {
-                float4 t;
-                t.x = fmaf(dx * rstd, g[u].x, b[u].x);
-                t.y = fmaf(dy * rstd, g[u].y, b[u].y);
-                t.z = fmaf(dz * rstd, g[u].z, b[u].z);
-                t.w = fmaf(dw * rstd, g[u].w, b[u].w);
-                t.x = t.x > 0.f ? t.x : slope * t.x;
-                t.y = t.y > 0.f ? t.y : slope * t.y;
-                t.z = t.z > 0.f ? t.z : slope * t.z;
-                t.w = t.w > 0.f ? t.w : slope * t.w;
-                Io<T>::st4_stream(yr + 4 * c, t, pol_stream);
+                const float2 r2 = make_float2(rstd, rstd);
+                float2 tl = __ffma2_rn(__fmul2_rn(dl, r2), g[u][0], b[u][0]);
+                float2 th = __ffma2_rn(__fmul2_rn(dh, r2), g[u][1], b[u][1]);
+                const float2 ul = __fmul2_rn(tl, slope2), uh = __fmul2_rn(th, slope2);
+                tl = steep ? make_float2(fminf(tl.x, ul.x), fminf(tl.y, ul.y))
+                           : make_float2(fmaxf(tl.x, ul.x), fmaxf(tl.y, ul.y));
+                th = steep ? make_float2(fminf(th.x, uh.x), fminf(th.y, uh.y))
+                           : make_float2(fmaxf(th.x, uh.x), fmaxf(th.y, uh.y));
+                Io<T>::st4_stream(yr + 4 * c, make_float4(tl.x, tl.y, th.x, th.y), pol_stream);
             }
         }
     }

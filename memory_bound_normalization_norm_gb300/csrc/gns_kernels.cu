@@ -354,22 +354,31 @@ __device__ __forceinline__ float first_elem(const float4 &raw)
         return Io<__nv_bfloat16>::unpack(__float_as_uint(raw.x), 0u).x;
 }
 
-// A thread's copy of one 4-element vector of its slice.  fp32: d = x - K
-// in a float4.  bf16: the packed values as loaded (two registers, so a CTA
-// holds twice as many vectors), widened and shifted each time they are used.
+// A thread's copy of one 4-element vector of its slice, read as two float2
+// pairs for the packed (f32x2) arithmetic.  fp32: d = x - K.  bf16: the
+// packed values as loaded (two registers, so a CTA holds twice as many
+// vectors), widened (a shift or a mask a pair) and shifted by `off` where
+// used; for fp32 `off` is added to d.
 template <typename T>
 struct Held;
 
 template <>
 struct Held<float> {
-    float4 d;
-    __device__ __forceinline__ void clear() { d = make_float4(0.f, 0.f, 0.f, 0.f); }
+    float2 lo, hi;
+    __device__ __forceinline__ void clear() { lo = hi = make_float2(0.f, 0.f); }
     __device__ __forceinline__ void load(const float *p, float K)
     {
         const float4 x = ld4_smem<float>(p);
-        d = make_float4(x.x - K, x.y - K, x.z - K, x.w - K);
+        const float2 nk = make_float2(-K, -K);
+        lo = __fadd2_rn(make_float2(x.x, x.y), nk);
+        hi = __fadd2_rn(make_float2(x.z, x.w), nk);
     }
-    __device__ __forceinline__ float4 get(float) const { return d; }
+    // d (+ off for a nonzero off)
+    __device__ __forceinline__ void pair(float2 off, bool add, float2 &l, float2 &h) const
+    {
+        l = add ? __fadd2_rn(lo, off) : lo;
+        h = add ? __fadd2_rn(hi, off) : hi;
+    }
 };
 
 template <>
@@ -377,12 +386,21 @@ struct Held<__nv_bfloat16> {
     uint2 raw;
     __device__ __forceinline__ void clear() { raw = make_uint2(0u, 0u); }
     __device__ __forceinline__ void load(const __nv_bfloat16 *p, float) { raw = *reinterpret_cast<const uint2 *>(p); }
-    __device__ __forceinline__ float4 get(float K) const
+    // x + off (off = -K for d)
+    __device__ __forceinline__ void pair(float2 off, bool, float2 &l, float2 &h) const
     {
-        const float4 x = Io<__nv_bfloat16>::unpack(raw.x, raw.y);
-        return make_float4(x.x - K, x.y - K, x.z - K, x.w - K);
+        l = __fadd2_rn(make_float2(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u)), off);
+        h = __fadd2_rn(make_float2(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)), off);
     }
 };
+
+// LeakyReLU of a pair: max(t, slope t) for slope <= 1 (negative slopes too)
+// and min(t, slope t) for slope > 1 are t > 0 ? t : slope t.
+__device__ __forceinline__ float2 lrelu2(float2 t, float2 slope2, bool steep)
+{
+    const float2 u = __fmul2_rn(t, slope2);
+    return steep ? make_float2(fminf(t.x, u.x), fminf(t.y, u.y)) : make_float2(fmaxf(t.x, u.x), fmaxf(t.y, u.y));
+}
 
 // grid: a persistent set of clusters of CL = p.parts CTAs (CL = 1 allowed);
 // cluster c walks segments r_k = c + k * (cluster count).  CTA `rank` owns
@@ -506,15 +524,21 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
                     v[j].load(sb + 4 * i, K);
             }
         }
-        // exact two-pass statistics of this CTA's slice about the pivot
-        float s = 0.f;
+        // exact two-pass statistics of this CTA's slice about the pivot, in
+        // f32x2 pairs
+        constexpr bool bf = sizeof(T) == 2;
+        const float2 negk = make_float2(-K, -K); // bf16: d = x - K as it is widened
+        float2 sl = make_float2(0.f, 0.f), sh = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             if (tid + j * NT < n4) {
-                const float4 d = v[j].get(K);
-                s += (d.x + d.y) + (d.z + d.w);
+                float2 l, h;
+                v[j].pair(negk, false, l, h);
+                sl = __fadd2_rn(sl, l);
+                sh = __fadd2_rn(sh, h);
             }
         }
+        float s = (sl.x + sl.y) + (sh.x + sh.y);
         s = block_sum<NT>(s, red[0]);
         // every thread has its values in registers: refill this buffer with
         // the segment GNS_NBUF ahead
@@ -524,15 +548,21 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
             ++issued;
         }
         const float mloc = n4 ? s / nloc : 0.f;
-        float q = 0.f;
+        // deviations from the slice mean: d - mloc (fp32), or x - (K + mloc)
+        // with the centre rounded once (bf16; its offset from the exact
+        // centre adds at most n * ulp(K)^2 / 4 to M2)
+        const float2 nc = bf ? make_float2(-(K + mloc), -(K + mloc)) : make_float2(-mloc, -mloc);
+        float2 ql = make_float2(0.f, 0.f), qh = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             if (tid + j * NT < n4) {
-                const float4 dv = v[j].get(K);
-                const float a = dv.x - mloc, c = dv.y - mloc, d = dv.z - mloc, e = dv.w - mloc;
-                q += (a * a + c * c) + (d * d + e * e);
+                float2 l, h;
+                v[j].pair(nc, true, l, h);
+                ql = __ffma2_rn(l, l, ql);
+                qh = __ffma2_rn(h, h, qh);
             }
         }
+        float q = (ql.x + ql.y) + (qh.x + qh.y);
         q = block_sum<NT>(q, red[1]);
         Moments tot;
         tot.n = nloc;
@@ -553,40 +583,59 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
         // = d - tot.mean; LReLU is positively homogeneous, so the factor 2
         // goes into the affine map: 2t = d * a + c, a = 2 * rstd * gamma,
         // c = 2 * beta - tot.mean * a.  Without ACT (LayerNorm): y = d * a + c
-        // with a = rstd * gamma, c = beta - tot.mean * a.
+        // with a = rstd * gamma, c = beta - tot.mean * a.  Pairs in f32x2.
         const float rstd = rsqrtf(fmaxf(tot.m2 / tot.n, 0.f) + p.eps);
         const float mean_d = tot.mean;
-        const float slope = p.slope;
+        const float2 slope2 = make_float2(p.slope, p.slope);
+        const bool steep = p.slope > 1.f;
         constexpr float sc = ACT ? 2.f : 1.f;
+        const float sr = sc * rstd;
         const int64_t r = cid + k * ncl;
         const int64_t cbase = (r % p.G) * p.M;
         T *yr = y + r * p.seg_len;
-        auto lrelu = [slope](float t) { return ACT ? (t > 0.f ? t : slope * t) : t; };
-        uint32_t cj = c0, rj = r0; // channel of vector j within the segment, and the remainder
+        uint32_t cj = c0, rj = r0;  // channel of vector j within the segment, and the remainder
+        uint32_t cur = 0xffffffffu; // the channel a2 / c2 belong to
+        float2 a2 = make_float2(0.f, 0.f), c2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int i = tid + j * NT;
             if (i < n4) {
                 const int64_t e = 4 * (lo + i);
-                const float4 dv = v[j].get(K);
-                float4 o;
+                float2 l, h;
+                v[j].pair(negk, false, l, h);
                 if constexpr (MODE == AFF_CHAN) {
-                    const int64_t c = cbase + cj;
-                    const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
-                    const float a = sc * rstd * gv, cc = fmaf(-mean_d, a, sc * bv);
-                    o = make_float4(lrelu(fmaf(dv.x, a, cc)), lrelu(fmaf(dv.y, a, cc)), lrelu(fmaf(dv.z, a, cc)),
-                                    lrelu(fmaf(dv.w, a, cc)));
+                    if (cj != cur) {
+                        // a new channel: its gamma/beta (each run of a
+                        // thread's vectors in one channel loads them once)
+                        cur = cj;
+                        const int64_t c = cbase + cj;
+                        const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
+                        const float a = sr * gv;
+                        a2 = make_float2(a, a);
+                        const float cc = fmaf(-mean_d, a, sc * bv);
+                        c2 = make_float2(cc, cc);
+                    }
+                    l = __ffma2_rn(l, a2, c2);
+                    h = __ffma2_rn(h, a2, c2);
                 } else {
                     float4 g, bb;
                     seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb, p.cache_gb != 0);
-                    const float ax = sc * rstd * g.x, ay = sc * rstd * g.y;
-                    const float az = sc * rstd * g.z, aw = sc * rstd * g.w;
-                    o = make_float4(lrelu(fmaf(dv.x, ax, fmaf(-mean_d, ax, sc * bb.x))),
-                                    lrelu(fmaf(dv.y, ay, fmaf(-mean_d, ay, sc * bb.y))),
-                                    lrelu(fmaf(dv.z, az, fmaf(-mean_d, az, sc * bb.z))),
-                                    lrelu(fmaf(dv.w, aw, fmaf(-mean_d, aw, sc * bb.w))));
+                    const float2 sr2 = make_float2(sr, sr), nm = make_float2(-mean_d, -mean_d);
+                    const float2 al = __fmul2_rn(make_float2(g.x, g.y), sr2);
+                    const float2 ah = __fmul2_rn(make_float2(g.z, g.w), sr2);
+                    float2 bl = make_float2(bb.x, bb.y), bh = make_float2(bb.z, bb.w);
+                    if constexpr (ACT) {
+                        bl = __fadd2_rn(bl, bl);
+                        bh = __fadd2_rn(bh, bh);
+                    }
+                    l = __ffma2_rn(l, al, __ffma2_rn(nm, al, bl));
+                    h = __ffma2_rn(h, ah, __ffma2_rn(nm, ah, bh));
                 }
-                Io<T>::st4_stream(yr + e, o, pol_stream);
+                if constexpr (ACT) {
+                    l = lrelu2(l, slope2, steep);
+                    h = lrelu2(h, slope2, steep);
+                }
+                Io<T>::st4_stream(yr + e, make_float4(l.x, l.y, h.x, h.y), pol_stream);
             }
             if constexpr (MODE == AFF_CHAN) {
                 // S % 4 == 0: a step of 4 * NT elements crosses at most one

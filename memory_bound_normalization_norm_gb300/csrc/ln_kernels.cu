@@ -764,37 +764,46 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
     }
     for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
         const T *xr = x + r * p.row_len;
-        float4 v[V];
+        float2 vl[V], vh[V]; // the vectors' pairs, as f32x2 operands
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t i = tid + k * NT;
-            v[k] = i < L4 ? Io<T>::ld4_stream(xr + 4 * i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 t = i < L4 ? Io<T>::ld4_stream(xr + 4 * i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+            vl[k] = make_float2(t.x, t.y);
+            vh[k] = make_float2(t.z, t.w);
         }
         // every thread reads the pivot before any thread of the CTA stores
         // (the block sums below are barriers), so y == x is safe
         const float K = Io<T>::ld1(xr);
-        // from here on v holds d = x - K (zero outside the row)
-        float s = 0.f;
+        const float2 negk = make_float2(-K, -K);
+        // from here on vl/vh hold d = x - K (zero outside the row)
+        float2 sl = make_float2(0.f, 0.f), sh = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             if (tid + k * NT < L4) {
-                v[k] = make_float4(v[k].x - K, v[k].y - K, v[k].z - K, v[k].w - K);
-                s += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+                vl[k] = __fadd2_rn(vl[k], negk);
+                vh[k] = __fadd2_rn(vh[k], negk);
+                sl = __fadd2_rn(sl, vl[k]);
+                sh = __fadd2_rn(sh, vh[k]);
             }
         }
+        float s = (sl.x + sl.y) + (sh.x + sh.y);
         s = block_sum<NT>(s, red[0]);
         const float mean_d = s / Lf;
-        float q = 0.f;
+        const float2 nm = make_float2(-mean_d, -mean_d);
+        float2 ql = make_float2(0.f, 0.f), qh = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             if (tid + k * NT < L4) {
-                const float a = v[k].x - mean_d, b = v[k].y - mean_d;
-                const float c = v[k].z - mean_d, d = v[k].w - mean_d;
-                q += (a * a + b * b) + (c * c + d * d);
+                const float2 el = __fadd2_rn(vl[k], nm), eh = __fadd2_rn(vh[k], nm);
+                ql = __ffma2_rn(el, el, ql);
+                qh = __ffma2_rn(eh, eh, qh);
             }
         }
+        float q = (ql.x + ql.y) + (qh.x + qh.y);
         q = block_sum<NT>(q, red[1]);
         const float rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        const float2 r2 = make_float2(rstd, rstd);
         T *yr = y + r * p.row_len;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
@@ -808,13 +817,12 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
                     g = gm ? Io<T>::ld4_param(gm + 4 * i) : make_float4(1.f, 1.f, 1.f, 1.f);
                     b = bt ? Io<T>::ld4_param(bt + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                // y = (d - mean_d) * rstd * g + b = d * a + c
-                const float4 a = make_float4(rstd * g.x, rstd * g.y, rstd * g.z, rstd * g.w);
-                const float4 o = make_float4(fmaf(v[k].x, a.x, fmaf(-mean_d, a.x, b.x)),
-                                             fmaf(v[k].y, a.y, fmaf(-mean_d, a.y, b.y)),
-                                             fmaf(v[k].z, a.z, fmaf(-mean_d, a.z, b.z)),
-                                             fmaf(v[k].w, a.w, fmaf(-mean_d, a.w, b.w)));
-                Io<T>::st4_stream(yr + 4 * i, o, pol_stream);
+                // y = (d - mean_d) * rstd * g + b = d * a + c, a = rstd * g,
+                // c = b - mean_d * a
+                const float2 al = __fmul2_rn(make_float2(g.x, g.y), r2), ah = __fmul2_rn(make_float2(g.z, g.w), r2);
+                const float2 ol = __ffma2_rn(vl[k], al, __ffma2_rn(nm, al, make_float2(b.x, b.y)));
+                const float2 oh = __ffma2_rn(vh[k], ah, __ffma2_rn(nm, ah, make_float2(b.z, b.w)));
+                Io<T>::st4_stream(yr + 4 * i, make_float4(ol.x, ol.y, oh.x, oh.y), pol_stream);
             }
         }
     }
