@@ -175,7 +175,7 @@ def test_persistent_exchange_200_launches_back_to_back(ng):
 
 
 @pytest.mark.parametrize("rows,L,path", [
-    (256, 262144, AUTO),        # 8 row groups of 19 CTAs (the automatic choice)
+    (256, 262144, AUTO),        # 13 row groups of 11 CTAs (the automatic choice)
     (64, 1 << 20, AUTO),        # 4 groups of 38
     (11, (1 << 20) + 4, AUTO),  # 4 groups, 3, 3, 3 and 2 rows
     (3, 1 << 20, AUTO),         # one row per group
