@@ -811,32 +811,64 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
     // division per segment
     int64_t rg = r % p.G;
     const int64_t rg_step = nteams % p.G;
-    for (; r < p.rows; r += nteams) {
-        const T *xr = x + r * p.seg_len;
-        float4 v[WMAX];
+    const float2 slope2 = make_float2(slope, slope);
+    const bool steep = slope > 1.f;
+    // fp32: x of this team's next segment is loaded while the current one is
+    // reduced and written (another segment, so y == x is safe), doubling the
+    // bytes in flight.  bf16 loads widen as they arrive, which would stall
+    // right behind the prefetch: measured slower, so bf16 loads in turn.
+    constexpr bool PF = sizeof(T) == 4;
+    float4 nx[PF ? WMAX : 1];
+    auto load_seg = [&](int64_t rr, float4 *dst) {
+        const T *xr = x + rr * p.seg_len;
 #pragma unroll
         for (int w = 0; w < WMAX; ++w)
-            v[w] = in[w] ? team_load<T, E>(xr + E * (j + w * Tn), pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+            dst[w] = (in[w] && rr < p.rows) ? team_load<T, E>(xr + E * (j + w * Tn), pol_stream)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    if constexpr (PF)
+        load_seg(r, nx);
+    for (; r < p.rows; r += nteams) {
+        float4 v[WMAX];
+        if constexpr (PF) {
+#pragma unroll
+            for (int w = 0; w < WMAX; ++w)
+                v[w] = nx[w];
+            load_seg(r + nteams, nx);
+        } else {
+            load_seg(r, v);
+        }
         // the segment's first element, from the team's first lane; every
         // lane reads it before any lane of the team stores (the shuffles
         // below order them), so y == x is safe.  From here on v holds
         // d = x - K.
         const float K = __shfl_sync(tmask, v[0].x, first);
         float s = 0.f;
+        if constexpr (E == 4) {
+            // four-element items: the arithmetic in f32x2 pairs
+            const float2 negk = make_float2(-K, -K);
+            float2 sp = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < WMAX; ++w) {
-            if (in[w]) {
-                v[w].x -= K;
-                if constexpr (E >= 2)
-                    v[w].y -= K;
-                if constexpr (E == 4) {
-                    v[w].z -= K;
-                    v[w].w -= K;
-                    s += (v[w].x + v[w].y) + (v[w].z + v[w].w);
-                } else if constexpr (E == 2) {
-                    s += v[w].x + v[w].y;
-                } else {
-                    s += v[w].x;
+            for (int w = 0; w < WMAX; ++w) {
+                if (in[w]) {
+                    const float2 l = __fadd2_rn(make_float2(v[w].x, v[w].y), negk);
+                    const float2 h = __fadd2_rn(make_float2(v[w].z, v[w].w), negk);
+                    v[w] = make_float4(l.x, l.y, h.x, h.y);
+                    sp = __fadd2_rn(sp, __fadd2_rn(l, h));
+                }
+            }
+            s = sp.x + sp.y;
+        } else {
+#pragma unroll
+            for (int w = 0; w < WMAX; ++w) {
+                if (in[w]) {
+                    v[w].x -= K;
+                    if constexpr (E == 2) {
+                        v[w].y -= K;
+                        s += v[w].x + v[w].y;
+                    } else {
+                        s += v[w].x;
+                    }
                 }
             }
         }
@@ -844,13 +876,27 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
             s += __shfl_xor_sync(tmask, s, o);
         const float mean_d = s / Lf;
         float q = 0.f;
+        if constexpr (E == 4) {
+            const float2 nm = make_float2(-mean_d, -mean_d);
+            float2 qp = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < WMAX; ++w) {
-            if (in[w]) {
+            for (int w = 0; w < WMAX; ++w) {
+                if (in[w]) {
+                    const float2 l = __fadd2_rn(make_float2(v[w].x, v[w].y), nm);
+                    const float2 h = __fadd2_rn(make_float2(v[w].z, v[w].w), nm);
+                    qp = __ffma2_rn(h, h, __ffma2_rn(l, l, qp));
+                }
+            }
+            q = qp.x + qp.y;
+        } else {
 #pragma unroll
-                for (int k = 0; k < E; ++k) {
-                    const float a = comp<E>(v[w], k) - mean_d;
-                    q = fmaf(a, a, q);
+            for (int w = 0; w < WMAX; ++w) {
+                if (in[w]) {
+#pragma unroll
+                    for (int k = 0; k < E; ++k) {
+                        const float a = comp<E>(v[w], k) - mean_d;
+                        q = fmaf(a, a, q);
+                    }
                 }
             }
         }
@@ -866,13 +912,19 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
             if (!in[w])
                 continue;
             const int i = j + w * Tn;
-            float g[4], b[4];
             if constexpr (E == 4) {
                 float4 g4, b4;
                 seg_affine4<T, MODE>(gm, bt, cbase, int64_t(4) * i, p.S, true, pol_keep, g4, b4, p.cache_gb != 0);
-                g[0] = g4.x, g[1] = g4.y, g[2] = g4.z, g[3] = g4.w;
-                b[0] = b4.x, b[1] = b4.y, b[2] = b4.z, b[3] = b4.w;
+                const float2 r2 = make_float2(rstd2, rstd2), nm = make_float2(-mean_d, -mean_d);
+                const float2 al = __fmul2_rn(make_float2(g4.x, g4.y), r2), ah = __fmul2_rn(make_float2(g4.z, g4.w), r2);
+                const float2 bl = make_float2(b4.x, b4.y), bh = make_float2(b4.z, b4.w);
+                float2 tl = __ffma2_rn(make_float2(v[w].x, v[w].y), al, __ffma2_rn(nm, al, __fadd2_rn(bl, bl)));
+                float2 th = __ffma2_rn(make_float2(v[w].z, v[w].w), ah, __ffma2_rn(nm, ah, __fadd2_rn(bh, bh)));
+                tl = lrelu2(tl, slope2, steep);
+                th = lrelu2(th, slope2, steep);
+                team_store<T, E>(yr + E * i, make_float4(tl.x, tl.y, th.x, th.y), pol_stream);
             } else {
+                float g[4], b[4];
 #pragma unroll
                 for (int k = 0; k < E; ++k) {
                     const int e = E * i + k;
@@ -880,15 +932,15 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
                     g[k] = gm ? Io<T>::ld1(gm + c) : 1.f;
                     b[k] = bt ? Io<T>::ld1(bt + c) : 0.f;
                 }
-            }
-            float o[4] = {0.f, 0.f, 0.f, 0.f};
+                float o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < E; ++k) {
-                const float sc = rstd2 * g[k];
-                const float t = fmaf(comp<E>(v[w], k), sc, fmaf(-mean_d, sc, b[k] + b[k]));
-                o[k] = t > 0.f ? t : slope * t;
+                for (int k = 0; k < E; ++k) {
+                    const float sc = rstd2 * g[k];
+                    const float t = fmaf(comp<E>(v[w], k), sc, fmaf(-mean_d, sc, b[k] + b[k]));
+                    o[k] = t > 0.f ? t : slope * t;
+                }
+                team_store<T, E>(yr + E * i, make_float4(o[0], o[1], o[2], o[3]), pol_stream);
             }
-            team_store<T, E>(yr + E * i, make_float4(o[0], o[1], o[2], o[3]), pol_stream);
         }
         rg += rg_step;
         if (rg >= p.G)
