@@ -233,7 +233,7 @@ def main_kernel_name(cfg) -> str:
             return "ln_rows_kernel"
         if L <= 131072 and L % (8 if bf16 else 4) == 0:
             return "gns_stream_kernel"
-        return "ln_persistent_kernel" if L % 4 == 0 and not bf16 else "ln_split_apply_kernel"
+        return "ln_persistent_kernel" if L % (8 if bf16 else 4) == 0 else "ln_split_apply_kernel"
     if cfg["op"] == "gn":
         M, bf16 = cfg["C"] // cfg["G"], bool(cfg.get("bf16"))
         if 4 <= M <= 128 and M & (M - 1) == 0:
@@ -249,11 +249,12 @@ def main_kernel_name(cfg) -> str:
 
 
 def gn_nchw_persistent(cfg) -> bool:
-    """fp32 groups longer than 131,072 values with S a multiple of 4, and x of 48 MiB or more, take
-    the persistent kernel."""
+    """Groups longer than 131,072 values with S a multiple of the 16-byte unit (4 fp32 or 8 bf16
+    values), and x of 48 MiB or more, take the persistent kernel."""
+    bf16 = bool(cfg.get("bf16"))
     L = cfg["C"] // cfg["G"] * cfg["S"]
     n = cfg["N"] * cfg["C"] * cfg["S"]
-    return not cfg.get("bf16") and cfg["S"] % 4 == 0 and L > 131072 and 4 * n >= 48 << 20
+    return cfg["S"] % (8 if bf16 else 4) == 0 and L > 131072 and (2 if bf16 else 4) * n >= 48 << 20
 
 
 def gn_nchw_one_launch(cfg) -> bool:
@@ -273,8 +274,10 @@ def make_call(ng, cfg, x, g, b, y, ws=None, ws_bytes=0, stream=None):
                                                           cfg["G"], 1e-5, 0.01, stream)), 1
     if op == "ln":
         rows, L = cfg["rows"], cfg["L"]
+        # the persistent kernel's longest bf16 row is twice its fp32 one (8 values a 16-byte unit)
         one_launch = L % 4 == 0 and (L <= (8192 if bf16 else 16384) or (L <= 131072 and L % (8 if bf16 else 4) == 0) or
-                                     (not bf16 and L <= ng.norm_layer_max_resident_row_len()))
+                                     (L % (8 if bf16 else 4) == 0
+                                      and L <= (2 if bf16 else 1) * ng.norm_layer_max_resident_row_len()))
         fn = ng.norm_layer_fwd_bf16 if bf16 else ng.norm_layer_fwd
         return (lambda: fn(x, g, b, y, rows, L, 1e-5, ws, ws_bytes, stream)), (1 if one_launch else 2)
     if op == "gn":

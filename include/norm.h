@@ -100,7 +100,9 @@ typedef enum {
  *     each CTA's next slices arrive by bulk copy into shared memory, and
  *     the CTAs of a row exchange their partial statistics through
  *     distributed shared memory; x is read from HBM once; no workspace;
- *   - longer rows (fp32, up to norm_layer_max_resident_row_len()): a
+ *   - longer rows (up to norm_layer_max_resident_row_len() fp32 elements,
+ *     or twice as many bf16; a length that is a multiple of 4 fp32 or 8
+ *     bf16 values and 16-byte aligned x, y, gamma and beta): a
  *     persistent cooperative kernel (one CTA per SM) gives every CTA the
  *     same column slice of each row, holds the slice on chip (shared memory,
  *     then registers) from the moment it arrives until y is written, and
@@ -108,8 +110,8 @@ typedef enum {
  *     per row; x is read from HBM once.  Rows shorter than about 3 Mi
  *     elements are spread over groups of CTAs, each group taking every k-th
  *     row, so that each row's exchange hides behind the group's next rows;
- *   - any other shape (ragged lengths, misaligned pointers, bf16 rows above
- *     131,072 elements): a two-kernel path that reads x twice.
+ *   - any other shape (ragged lengths, misaligned pointers): a two-kernel
+ *     path that reads x twice.
  * All produce the same statistics definition.
  */
 size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len);
@@ -125,10 +127,9 @@ norm_status_t norm_layer_fwd(const float *x, const float *gamma, const float *be
  * workspace and errors as norm_layer_fwd, with 2-byte elements: pointers must
  * be 2-byte aligned, and the one-read paths want 8-byte aligned pointers and a
  * length that is a multiple of 4.  Paths as for fp32, except that the
- * cluster kernel wants 16-byte aligned x and a length that is a multiple of 8,
- * and that the persistent kernel is fp32 only (NORM_OPT_LN_PATH = 1 returns
- * NORM_ERR_UNSUPPORTED here): rows above 131,072 elements take the
- * two-kernel path. */
+ * cluster kernel and the persistent kernel want 16-byte aligned tensors and a
+ * length that is a multiple of 8 (the persistent kernel keeps gamma/beta
+ * packed in tensor memory and serves rows twice as long as in fp32). */
 norm_status_t norm_layer_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta, uint16_t *y,
                                   int64_t rows, int64_t row_len, float eps,
                                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
@@ -145,9 +146,8 @@ norm_status_t norm_layer_fwd_bf16(const uint16_t *x, const uint16_t *gamma, cons
  * that loads the library until the process exits.
  *   - The row kernel and the cluster kernel use no scratch, so every shape
  *     they take is served, however many rows.  The persistent kernel uses
- *     about 20 KB.  The two-kernel path (ragged lengths, misaligned pointers,
- *     rows between 131,072 and 2^20 elements) uses 256 bytes plus 16 bytes
- *     per (row, chunk).
+ *     about 20 KB.  The two-kernel path (ragged lengths, misaligned pointers)
+ *     uses 256 bytes plus 16 bytes per (row, chunk).
  *   - Returns NORM_ERR_WORKSPACE, without launching, when the path chosen
  *     for the shape needs more scratch than the array holds (e.g. more than
  *     ~65,000 rows of a ragged length on the two-kernel path).
@@ -166,10 +166,11 @@ norm_status_t norm_layer_fwd_noalloc(const float *x, const float *gamma, const f
 /* Zero `bytes` of a LayerNorm workspace on `stream` (stream-ordered). */
 norm_status_t norm_layer_workspace_reset(void *workspace, size_t bytes, cudaStream_t stream);
 
-/* Longest row (in elements) that the single-read persistent LayerNorm kernel
- * serves on the current device: each CTA's slice of a row must fit its two
- * shared-memory row buffers and its threads' registers (6,912 float4 per CTA,
- * 4,202,496 elements on a 152-SM GB300).  0 if the device cannot run the
+/* Longest fp32 row (in elements) that the single-read persistent LayerNorm
+ * kernel serves on the current device: each CTA's slice of a row must fit its
+ * two shared-memory row buffers and its threads' registers (6,912 16-byte
+ * units per CTA, 4,202,496 fp32 elements on a 152-SM GB300).  bf16 rows may
+ * be twice as long (8 values a unit).  0 if the device cannot run the
  * kernel. */
 int64_t norm_layer_max_resident_row_len(void);
 
@@ -267,9 +268,10 @@ norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *ga
  *     its waits are bounded by NORM_OPT_BARRIER_TIMEOUT_NS (a CTA that gives
  *     up records NORM_ERR_TIMEOUT and leaves its part of the remaining
  *     groups of y unwritten);
- *   - fp32 groups of more than 131,072 values with S a multiple of 4 and
- *     16-byte aligned x and y, up to norm_layer_max_resident_row_len()
- *     values, x of 48 MiB or more (smaller x is re-read mostly from L2 by
+ *   - groups of more than 131,072 values with S a multiple of 4 (fp32) or 8
+ *     (bf16) and 16-byte aligned x and y, up to
+ *     norm_layer_max_resident_row_len() values (twice that in bf16), x of
+ *     48 MiB or more (smaller x is re-read mostly from L2 by
  *     the two-kernel path, which is then faster): the persistent LayerNorm
  *     kernel in its GroupNorm form (one
  *     launch, x read from HBM once; each segment is split over the CTAs of
@@ -380,8 +382,8 @@ const char *norm_status_string(norm_status_t status);
  *                                force the team-per-group kernel (groups of
  *                                at most 256 four-element vectors, or 256
  *                                elements when the vector form is off), 6 =
- *                                force the persistent single-read kernel (fp32
- *                                NCHW with S % 4 == 0)
+ *                                force the persistent single-read kernel (NCHW
+ *                                with S a multiple of 4 fp32 or 8 bf16 values)
  *                                (error NORM_ERR_UNSUPPORTED where the forced
  *                                path cannot serve the call).
  *   NORM_OPT_GN_CLUSTER          CTAs per group of the register kernel: 0 =

@@ -19,22 +19,24 @@
 // ((x - hi) - lo) * rstd * gamma + beta.
 //
 // Persistent path (one CTA per SM, cooperative launch so all CTAs are
-// co-resident).  CTA c owns the same float4 column slice of every row.  Row
+// co-resident).  A row is counted in 16-byte units (4 fp32 or 8 bf16
+// values); CTA c owns the same column slice of units of every row.  Row
 // slices arrive by bulk copy (TMA engine, 32 KB pieces) into two
 // shared-memory buffers; the slice of the row being written lives in
-// registers, and gamma/beta of the slice live in tensor memory (TMEM),
-// loaded once per launch by the apply warps' own 16-byte loads.  x is read
-// from HBM once and stays on chip until y is written; gamma and beta are
-// read from HBM once.  Three warp roles run concurrently: warps 1..3 reduce
-// a row's statistics as soon as it lands and publish the CTA's triple, warp
-// 0 merges the triples of all CTAs, warps 4..15 write y.  A row's triples go
+// registers (4 registers a unit, bf16 kept packed), and gamma/beta of the
+// slice live in tensor memory (TMEM, 4 cells a unit, bf16 kept packed),
+// bulk-copied through the row buffers once per launch.  x is read from HBM
+// once and stays on chip until y is written; gamma and beta are read from
+// HBM once.  Three warp roles run concurrently: warps 1..3 reduce a row's
+// statistics as soon as it lands and publish the CTA's triple, warp 0
+// merges the triples of all CTAs, warps 4..15 write y.  A row's triples go
 // out about two rows before its y is written, which hides the grid-wide
 // exchange (several microseconds under full HBM load) behind other rows'
 // work.  Before the first y store the apply warps have nothing to write, so
 // they reduce rows 0 and 1 together with warps 1..3 (480 threads instead of
-// 96), and row 0 is copied alone first so that it lands, is reduced and
-// crosses the grid while row 1 and gamma/beta are still arriving.  The
-// pivot's three candidate elements travel with each row's bulk copy.
+// 96); row 0 and gamma are copied first, and beta and row 1 follow into the
+// buffers that row 0 and gamma leave.  The pivot's three candidate elements
+// travel with each row's bulk copy.
 //
 // Grid barrier without atomics.  Each CTA publishes its (mean, M2) as two
 // 64-bit words, each carrying a 32-bit tag in its high half, in one 16-byte
@@ -145,21 +147,23 @@ struct GridMerge {
 // row's one pivot K), held by warp 0 as w[j][0..1] for CTA lane + 32 j, with
 // the two-pass formula over partials:
 //   delta = sum_c n_c m_c / N,   M2 = sum_c M2_c + sum_c n_c (m_c - delta)^2,
-// with each count n_c known from the partition (q4 or q4 + 1 float4).  The
-// sums are warp reductions in a fixed order, so every CTA computes the same
-// bits; all lanes return the result.
+// with each count n_c known from the partition (qu or qu + 1 units of UE
+// elements).  The sums are warp reductions in a fixed order, so every CTA
+// computes the same bits; all lanes return the result.
+template <int UE>
 __device__ __forceinline__ Moments merge_records(const unsigned long long (&w)[LN_MAX_GRID / 32][2], int G,
-                                                 unsigned q4, unsigned rem)
+                                                 unsigned qu, unsigned rem)
 {
     constexpr int J = LN_MAX_GRID / 32;
+    constexpr float ue = static_cast<float>(UE);
     const int lane = threadIdx.x & 31;
-    const float N = 4.f * (static_cast<float>(q4) * static_cast<float>(G) + static_cast<float>(rem));
+    const float N = ue * (static_cast<float>(qu) * static_cast<float>(G) + static_cast<float>(rem));
     float sm = 0.f; // sum of n_c * m_c
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int i = lane + 32 * j;
         if (i < G) {
-            const float n = 4.f * static_cast<float>(q4 + (static_cast<unsigned>(i) < rem ? 1u : 0u));
+            const float n = ue * static_cast<float>(qu + (static_cast<unsigned>(i) < rem ? 1u : 0u));
             sm = fmaf(n, record_value(w[j][0]), sm);
         }
     }
@@ -172,7 +176,7 @@ __device__ __forceinline__ Moments merge_records(const unsigned long long (&w)[L
     for (int j = 0; j < J; ++j) {
         const int i = lane + 32 * j;
         if (i < G) {
-            const float n = 4.f * static_cast<float>(q4 + (static_cast<unsigned>(i) < rem ? 1u : 0u));
+            const float n = ue * static_cast<float>(qu + (static_cast<unsigned>(i) < rem ? 1u : 0u));
             const float dm = record_value(w[j][0]) - delta;
             sq += fmaf(n * dm, dm, record_value(w[j][1]));
         }
@@ -190,7 +194,8 @@ __device__ __forceinline__ Moments merge_records(const unsigned long long (&w)[L
 // Warp 0: read the G records of a row with plain L2 loads (ld.global.cg,
 // which overlap) until every tag equals `tag` (bounded by timeout_ns), then
 // merge them.
-__device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *rec, int G, unsigned q4, unsigned rem,
+template <int UE>
+__device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *rec, int G, unsigned qu, unsigned rem,
                                                     unsigned tag, uint64_t timeout_ns)
 {
     constexpr int J = LN_MAX_GRID / 32;
@@ -213,7 +218,7 @@ __device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *re
             }
         }
         if (__all_sync(0xffffffffu, bad == 0)) {
-            g.tot = merge_records(w, G, q4, rem);
+            g.tot = merge_records<UE>(w, G, qu, rem);
             return g;
         }
         if (attempt == 0)
@@ -226,64 +231,182 @@ __device__ __forceinline__ GridMerge poll_and_merge(const unsigned long long *re
     }
 }
 
+// Element k of a 16-byte unit of T held in a float4's bits: fp32 component
+// k, or bf16 k (the low half of 32-bit word k / 2 for even k), widened.
+template <typename T>
+__device__ __forceinline__ float unit_elem(const float4 &u, int k)
+{
+    if constexpr (sizeof(T) == 4) {
+        return k == 0 ? u.x : k == 1 ? u.y : k == 2 ? u.z : u.w;
+    } else {
+        const float wf = (k >> 1) == 0 ? u.x : (k >> 1) == 1 ? u.y : (k >> 1) == 2 ? u.z : u.w;
+        const uint32_t wd = __float_as_uint(wf);
+        return __uint_as_float((k & 1) ? (wd & 0xffff0000u) : (wd << 16));
+    }
+}
+
+// The two bf16 of 32-bit word `wf` (held as a float's bits) as an f32x2 pair.
+__device__ __forceinline__ float2 bf16_pair(float wf)
+{
+    const uint32_t wd = __float_as_uint(wf);
+    return make_float2(__uint_as_float(wd << 16), __uint_as_float(wd & 0xffff0000u));
+}
+
 // Pivot of a row: the median of its first, middle and last elements.  A
 // pivot inside the bulk of the row keeps the shifted sums small, and one
 // outlier cannot become the pivot.  The three elements arrive by bulk copy
-// with the row, each in the 16-byte piece that contains it (row_len is a
-// multiple of 4, so element i sits at float i % 4 of piece i / 4).
+// with the row, each in the 16-byte unit that contains it (row_len is a
+// multiple of UE = 16 / sizeof(T), so element i is element i % UE of unit
+// i / UE).
+template <typename T>
 __device__ __forceinline__ float row_pivot(const float4 *piece, int64_t row_len)
 {
+    constexpr int UE = 16 / static_cast<int>(sizeof(T));
     const int64_t mid = row_len >> 1;
-    const float a = piece[0].x;
-    const float4 pm = piece[1], pl = piece[2];
-    const int jm = static_cast<int>(mid & 3);
-    const float b = jm == 0 ? pm.x : jm == 1 ? pm.y : jm == 2 ? pm.z : pm.w;
-    const float c = pl.w; // row_len - 1 is float 3 of its piece
+    const float a = unit_elem<T>(piece[0], 0);
+    const float b = unit_elem<T>(piece[1], static_cast<int>(mid % UE));
+    const float c = unit_elem<T>(piece[2], UE - 1);
     return fmaxf(fminf(a, b), fminf(fmaxf(a, b), c));
 }
 
-// Shifted sums of d = x - K over float4 i = pi, pi + np, ... < n4 of a row
+// Shifted sums of d = x - K over units i = pi, pi + np, ... < nu of a row
 // slice in shared memory, with four independent accumulator pairs, as this
-// thread's (count, mean, M2).
-__device__ __forceinline__ Moments slice_moments(const float4 *buf, int n4, int pi, int np, float K)
+// thread's (count, mean, M2).  bf16 units (8 values) are widened a 32-bit
+// word at a time and summed in f32x2 pairs.
+template <typename T>
+__device__ __forceinline__ Moments slice_moments(const float4 *buf, int nu, int pi, int np, float K)
 {
+    constexpr int UE = 16 / static_cast<int>(sizeof(T));
     float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
     int i = pi;
-    for (; i + 3 * np < n4; i += 4 * np) {
+    if constexpr (sizeof(T) == 4) {
+        for (; i + 3 * np < nu; i += 4 * np) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float4 v = buf[i + u * np];
-            const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
-            s1[u] += (a + b) + (c + d);
-            s2[u] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[u]))));
+            for (int u = 0; u < 4; ++u) {
+                const float4 v = buf[i + u * np];
+                const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
+                s1[u] += (a + b) + (c + d);
+                s2[u] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[u]))));
+            }
         }
-    }
-    for (; i < n4; i += np) {
-        const float4 v = buf[i];
-        const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
-        s1[0] += (a + b) + (c + d);
-        s2[0] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[0]))));
+        for (; i < nu; i += np) {
+            const float4 v = buf[i];
+            const float a = v.x - K, b = v.y - K, c = v.z - K, d = v.w - K;
+            s1[0] += (a + b) + (c + d);
+            s2[0] = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, s2[0]))));
+        }
+    } else {
+        const float2 negk = make_float2(-K, -K);
+        float2 p1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float2 p2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        auto add_unit = [&](const float4 &v, int a) {
+            const float2 d0 = __fadd2_rn(bf16_pair(v.x), negk), d1 = __fadd2_rn(bf16_pair(v.y), negk);
+            const float2 d2 = __fadd2_rn(bf16_pair(v.z), negk), d3 = __fadd2_rn(bf16_pair(v.w), negk);
+            p1[a] = __fadd2_rn(p1[a], __fadd2_rn(__fadd2_rn(d0, d1), __fadd2_rn(d2, d3)));
+            p2[a] = __ffma2_rn(d3, d3, __ffma2_rn(d2, d2, __ffma2_rn(d1, d1, __ffma2_rn(d0, d0, p2[a]))));
+        };
+        for (; i + np < nu; i += 2 * np) {
+            add_unit(buf[i], 0);
+            add_unit(buf[i + np], 1);
+        }
+        for (; i < nu; i += np)
+            add_unit(buf[i], 0);
+        s1[0] = p1[0].x + p1[0].y;
+        s1[1] = p1[1].x + p1[1].y;
+        s2[0] = p2[0].x + p2[0].y;
+        s2[1] = p2[1].x + p2[1].y;
     }
     Moments m = {0.f, 0.f, 0.f};
-    const int nv = n4 > pi ? (n4 - pi + np - 1) / np : 0; // float4 of this thread
+    const int nv = nu > pi ? (nu - pi + np - 1) / np : 0; // units of this thread
     if (nv > 0) {
         const float S1 = (s1[0] + s1[1]) + (s1[2] + s1[3]);
         const float S2 = (s2[0] + s2[1]) + (s2[2] + s2[3]);
-        m.n = 4.f * static_cast<float>(nv);
+        m.n = static_cast<float>(UE) * static_cast<float>(nv);
         m.mean = S1 / m.n;
         m.m2 = fmaxf(fmaf(-S1, m.mean, S2), 0.f);
     }
     return m;
 }
 
+// y of one unit of a LayerNorm row: ((x - hi) - lo) * rstd * gamma + beta.
+// fp32: the unit's 4 values, gamma/beta from 4 TMEM cells.  bf16: 8 values,
+// gamma/beta 8 packed bf16 in the 4 cells, arithmetic in f32x2 pairs, the
+// result packed to bf16 once.  Returns the 16 bytes to store.
+template <typename T>
+__device__ __forceinline__ float4 ln_unit(const float4 &v, const RowMean &rm, const float4 &g, const float4 &b)
+{
+    if constexpr (sizeof(T) == 4) {
+        return ln_apply4(v, rm, g, b);
+    } else {
+        const float2 nh = make_float2(-rm.hi, -rm.hi), nl = make_float2(-rm.lo, -rm.lo);
+        const float2 r2 = make_float2(rm.rstd, rm.rstd);
+        auto word = [&](float xv, float gv, float bv) {
+            const float2 t = __fmul2_rn(__fadd2_rn(__fadd2_rn(bf16_pair(xv), nh), nl), r2);
+            const float2 o = __ffma2_rn(t, bf16_pair(gv), bf16_pair(bv));
+            return __uint_as_float(pack_bf16x2(o.x, o.y));
+        };
+        return make_float4(word(v.x, g.x, b.x), word(v.y, g.y, b.y), word(v.z, g.z, b.z), word(v.w, g.w, b.w));
+    }
+}
+
+// One gamma/beta value of the GroupNorm form (read through the read-only
+// path; a channel's value is shared by many units).
+__device__ __forceinline__ float ldg_param(const float *p)
+{
+    return __ldg(p);
+}
+
+__device__ __forceinline__ float ldg_param(const __nv_bfloat16 *p)
+{
+    return __bfloat162float(__ldg(p));
+}
+
+// y of one unit of the GroupNorm form, all of it in one channel:
+// LReLU(((x - hi) - lo) * rstd * g2 + b2) with gamma/beta already doubled.
+template <typename T>
+__device__ __forceinline__ float4 gn_unit(const float4 &v, const RowMean &rm, float g2, float b2, float slope)
+{
+    if constexpr (sizeof(T) == 4) {
+        float4 o;
+        o.x = fmaf(((v.x - rm.hi) - rm.lo) * rm.rstd, g2, b2);
+        o.y = fmaf(((v.y - rm.hi) - rm.lo) * rm.rstd, g2, b2);
+        o.z = fmaf(((v.z - rm.hi) - rm.lo) * rm.rstd, g2, b2);
+        o.w = fmaf(((v.w - rm.hi) - rm.lo) * rm.rstd, g2, b2);
+        o.x = o.x > 0.f ? o.x : slope * o.x;
+        o.y = o.y > 0.f ? o.y : slope * o.y;
+        o.z = o.z > 0.f ? o.z : slope * o.z;
+        o.w = o.w > 0.f ? o.w : slope * o.w;
+        return o;
+    } else {
+        const float2 nh = make_float2(-rm.hi, -rm.hi), nl = make_float2(-rm.lo, -rm.lo);
+        const float2 r2 = make_float2(rm.rstd, rm.rstd), gg = make_float2(g2, g2), bb = make_float2(b2, b2);
+        const float2 s2 = make_float2(slope, slope);
+        const bool steep = slope > 1.f;
+        auto word = [&](float xv) {
+            const float2 t = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(bf16_pair(xv), nh), nl), r2), gg, bb);
+            // LReLU: max(t, slope t) for slope <= 1, min(t, slope t) above
+            const float2 u = __fmul2_rn(t, s2);
+            const float lo = steep ? fminf(t.x, u.x) : fmaxf(t.x, u.x);
+            const float hi = steep ? fminf(t.y, u.y) : fmaxf(t.y, u.y);
+            return __uint_as_float(pack_bf16x2(lo, hi));
+        };
+        return make_float4(word(v.x), word(v.y), word(v.z), word(v.w));
+    }
+}
+
 // GN: GroupNorm + LeakyReLU + x2 over NCHW segments instead of LayerNorm
 // rows: row r is segment r (sample r / G, group r % G) of L = M * S values;
 // gamma/beta are per channel (channel g * M + e / S for element e), read
-// from L1 per 4-element vector (S % 4 == 0) instead of held in TMEM, and the
-// output is 2 LReLU((x - mean) * rstd * gamma + beta).
-template <bool GN>
+// through L1 per unit (S a multiple of the unit's UE values) instead of held
+// in TMEM, and the output is 2 LReLU((x - mean) * rstd * gamma + beta).
+// T: float or __nv_bfloat16 (x, y, gamma, beta), fp32 arithmetic.
+template <typename T, bool GN>
 __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p, GnPersist gp_)
 {
+    // A unit is 16 bytes of a row: UE = 4 fp32 or 8 bf16 values.  Slices,
+    // buffers, registers (4 a unit) and TMEM cells (4 a unit: gamma/beta of
+    // bf16 rows stay packed) are all counted in units.
+    constexpr int UE = 16 / static_cast<int>(sizeof(T));
     extern __shared__ __align__(128) float4 ln_smem[];
     __shared__ __align__(8) uint64_t bar_x[2];
     __shared__ __align__(8) uint64_t bar_g, bar_b; // gamma into buffer 1, beta into buffer 0
@@ -304,19 +427,19 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     // The group's rows: local row t is row grp + t * NG of the launch.
     const int64_t R = p.rows > grp ? (p.rows - grp + NG - 1) / NG : 0;
     auto grow = [&](int64_t t) { return grp + t * NG; };
-    const int64_t L4 = p.row_len >> 2;
-    // CTA rank c owns n4 = q4 (+1 for the first rem ranks) float4 of every row
+    const int64_t Lu = p.row_len / UE;
+    // CTA rank c owns nu = qu (+1 for the first rem ranks) units of every row
     // of its group, starting at f0; the merge recomputes every rank's count
     // the same way.
-    const unsigned q4 = static_cast<unsigned>(L4 / Gk), rem = static_cast<unsigned>(L4 % Gk);
-    const int64_t f0 = static_cast<int64_t>(crank) * q4 + min(static_cast<unsigned>(crank), rem);
-    const int n4 = static_cast<int>(q4 + (static_cast<unsigned>(crank) < rem ? 1u : 0u));
+    const unsigned qu = static_cast<unsigned>(Lu / Gk), rem = static_cast<unsigned>(Lu % Gk);
+    const int64_t f0 = static_cast<int64_t>(crank) * qu + min(static_cast<unsigned>(crank), rem);
+    const int nu = static_cast<int>(qu + (static_cast<unsigned>(crank) < rem ? 1u : 0u));
     const float4 *x4 = reinterpret_cast<const float4 *>(p.x);
     float4 *y4 = reinterpret_cast<float4 *>(p.y);
     const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma);
     const float4 *b4 = reinterpret_cast<const float4 *>(p.beta);
     unsigned long long *records = reinterpret_cast<unsigned long long *>(p.part);
-    const int buf_f4 = (p.max_n4 + 7) & ~7;
+    const int buf_u = (p.max_n4 + 7) & ~7;
 
     const uint64_t pol_stream = policy_evict_first();
     // Waits for this CTA's own bulk copies after a failure (drains) use at
@@ -349,14 +472,14 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     // pivot candidates, all on bar_x[q & 1] (row q lives in buffer q & 1).
     auto issue_x = [&](int64_t q) {
         uint64_t *bar = &bar_x[q & 1];
-        const uint32_t bytes = static_cast<uint32_t>(n4) * 16u;
+        const uint32_t bytes = static_cast<uint32_t>(nu) * 16u;
         mbar_arrive_expect_tx(bar, bytes + 48u);
-        const float4 *row = x4 + grow(q) * L4;
+        const float4 *row = x4 + grow(q) * Lu;
         bulk_g2s(&piv_in[q & 1][0], row, 16u, bar, pol_stream);
-        bulk_g2s(&piv_in[q & 1][1], row + ((p.row_len >> 1) >> 2), 16u, bar, pol_stream);
-        bulk_g2s(&piv_in[q & 1][2], row + (L4 - 1), 16u, bar, pol_stream);
+        bulk_g2s(&piv_in[q & 1][1], row + ((p.row_len >> 1) / UE), 16u, bar, pol_stream);
+        bulk_g2s(&piv_in[q & 1][2], row + (Lu - 1), 16u, bar, pol_stream);
         const float4 *src = row + f0;
-        float4 *dst = ln_smem + (q & 1) * buf_f4;
+        float4 *dst = ln_smem + (q & 1) * buf_u;
         for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
             bulk_g2s(dst + off / 16, src + off / 16, (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK,
                      bar, pol_stream);
@@ -400,7 +523,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             bar_sync_named(LN_BAR_APPLIED, LN_A + 32);
             if (q >= 0 && q < R) {
                 const GridMerge gm =
-                    poll_and_merge(records + (static_cast<int64_t>(q % LN_SLOTS) * G + grp * Gk) * 2, Gk, q4, rem,
+                    poll_and_merge<UE>(records + (static_cast<int64_t>(q % LN_SLOTS) * G + grp * Gk) * 2, Gk, qu, rem,
                                    row_tag(row_base, grow(q)) + p.tag_skew, p.timeout_ns);
                 if (!gm.ok) {
                     fail = true;
@@ -427,10 +550,10 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             const bool pro = q < 2;
             const int np = pro ? 32 * LN_PRO_WARPS : LN_S;
             fail = !mbar_wait_bounded(&bar_x[q & 1], x_parity(q), p.timeout_ns);
-            const float K = fail ? 0.f : row_pivot(piv_in[q & 1], p.row_len);
+            const float K = fail ? 0.f : row_pivot<T>(piv_in[q & 1], p.row_len);
             Moments m = {0.f, 0.f, 0.f};
             if (!fail)
-                m = slice_moments(ln_smem + (q & 1) * buf_f4, n4, st, np, K);
+                m = slice_moments<T>(ln_smem + (q & 1) * buf_u, nu, st, np, K);
             m = warp_merge(m);
             if (lane == 0)
                 red[q & 1][warp - 1] = m;
@@ -476,9 +599,9 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
         bool fail = false; // a copy the prologue waits for did not land in time
         // gamma or beta of the slice (h = 0, 1) into buffer 1 or 0, on bar
         auto issue_param = [&](const float4 *src, int buf, uint64_t *bar) {
-            const uint32_t bytes = src ? static_cast<uint32_t>(n4) * 16u : 0u;
+            const uint32_t bytes = src ? static_cast<uint32_t>(nu) * 16u : 0u;
             mbar_arrive_expect_tx(bar, bytes);
-            float4 *dst = ln_smem + buf * buf_f4;
+            float4 *dst = ln_smem + buf * buf_u;
             for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
                 bulk_g2s(dst + off / 16, src + f0 + off / 16,
                          (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, bar, pol_stream);
@@ -511,27 +634,26 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 waited = q + 1;
             Moments m = {0.f, 0.f, 0.f};
             if (ok)
-                m = slice_moments(ln_smem + (q & 1) * buf_f4, n4, pt, 32 * LN_PRO_WARPS,
-                                  row_pivot(piv_in[q & 1], p.row_len));
+                m = slice_moments<T>(ln_smem + (q & 1) * buf_u, nu, pt, 32 * LN_PRO_WARPS,
+                                     row_pivot<T>(piv_in[q & 1], p.row_len));
             m = warp_merge(m);
             if (lane == 0)
                 red[q & 1][warp - 1] = m;
             bar_sync_named(LN_BAR_PRO, 32 * LN_PRO_WARPS);
         };
         // gamma or beta (wait on bar, then buffer buf -> this thread's TMEM
-        // columns from col0; 1 / 0 where the parameter is absent)
-        auto fill_tmem = [&](const float4 *src, int buf, uint64_t *bar, uint32_t col0, float dflt) {
+        // columns from col0; the unit d where the parameter is absent)
+        auto fill_tmem = [&](const float4 *src, int buf, uint64_t *bar, uint32_t col0, float4 d) {
             const bool ok = mbar_wait_bounded(bar, 0, p.timeout_ns);
             fail = fail || !ok;
-            const float4 *b = ln_smem + buf * buf_f4;
-            const float4 d = make_float4(dflt, dflt, dflt, dflt);
+            const float4 *b = ln_smem + buf * buf_u;
             __syncwarp();
 #pragma unroll
             for (int k = 0; k < LN_V; k += 2) {
                 float4 a0, a1;
                 const int i0 = at + k * LN_A, i1 = at + (k + 1) * LN_A;
-                a0 = (src && ok && i0 < n4) ? b[i0] : d;
-                a1 = (src && ok && i1 < n4) ? b[i1] : d;
+                a0 = (src && ok && i0 < nu) ? b[i0] : d;
+                a1 = (src && ok && i1 < nu) ? b[i1] : d;
                 tmem_st4(tm + col0 + static_cast<uint32_t>(4 * k), a0);
                 tmem_st4(tm + col0 + static_cast<uint32_t>(4 * (k + 1)), a1);
             }
@@ -551,7 +673,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 #pragma unroll
                 for (int k = 0; k < LN_V; ++k) {
                     const int i = at + k * LN_A;
-                    v[k] = (i < n4) ? ln_smem[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[k] = (i < nu) ? ln_smem[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
                 __syncwarp();
             } else if (r == -2) {
@@ -561,7 +683,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 #pragma unroll
                 for (int k = 0; k < LN_V; ++k) {
                     const int i = at + k * LN_A;
-                    v[k] = (i < n4) ? ln_smem[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[k] = (i < nu) ? ln_smem[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
                 // every apply thread has read buffer 0 (the statistics warps
                 // finished with it at LN_BAR_PRO)
@@ -572,7 +694,9 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                     b_out = true;
                 }
                 // gamma: buffer 1 -> TMEM, then row 1 into buffer 1
-                const bool g_ok = fill_tmem(g4, 1, &bar_g, 0u, 1.f);
+                // an absent gamma is 1: four fp32 ones, or eight bf16 ones
+                const float one = sizeof(T) == 4 ? 1.f : __uint_as_float(0x3f803f80u);
+                const bool g_ok = fill_tmem(g4, 1, &bar_g, 0u, make_float4(one, one, one, one));
                 if (issuer && g_ok)
                     g_out = false;
                 bar_sync_named(LN_BAR_FILL, LN_A);
@@ -582,7 +706,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                     issued = 2;
                 }
                 // beta: buffer 0 -> TMEM (buffer 0 takes row 2 at r = -1)
-                const bool b_ok = fill_tmem(b4, 0, &bar_b, LN_TM_BETA, 0.f);
+                const bool b_ok = fill_tmem(b4, 0, &bar_b, LN_TM_BETA, make_float4(0.f, 0.f, 0.f, 0.f));
                 if (issuer && b_ok)
                     b_out = false;
                 bar_sync_named(LN_BAR_FILL, LN_A);
@@ -590,43 +714,34 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             if (GN && r >= 0) {
                 // y of segment r from registers: 2 LReLU(d * rstd * gamma_c +
                 // beta_c), gamma/beta doubled (LReLU is positively homogeneous
-                // and doubling is exact).  Vector k of this thread starts at
-                // element e_k = e_0 + 4 LN_A k of the segment; its channel is
+                // and doubling is exact).  Unit k of this thread starts at
+                // element e_k = e_0 + UE LN_A k of the segment; its channel is
                 // e_k / S within the group, tracked incrementally.
                 const RowMean rm = row_mean[r & 1];
                 const int64_t gr = grow(r);
                 const int64_t cbase = (gr % gp_.G) * gp_.M;
-                float4 *yr = y4 + gr * L4 + f0;
-                const uint32_t S = gp_.S, e0 = 4u * static_cast<uint32_t>(f0 + at);
+                float4 *yr = y4 + gr * Lu + f0;
+                constexpr uint32_t step = static_cast<uint32_t>(UE) * LN_A;
+                const uint32_t S = gp_.S, e0 = static_cast<uint32_t>(UE) * static_cast<uint32_t>(f0 + at);
                 uint32_t cq = e0 / S, rq = e0 - cq * S;
-                const float *gp = p.gamma ? static_cast<const float *>(p.gamma) + cbase : nullptr;
-                const float *bp = p.beta ? static_cast<const float *>(p.beta) + cbase : nullptr;
+                const T *gp = p.gamma ? static_cast<const T *>(p.gamma) + cbase : nullptr;
+                const T *bp = p.beta ? static_cast<const T *>(p.beta) + cbase : nullptr;
 #pragma unroll
                 for (int k = 0; k < LN_V; ++k) {
                     const int i = at + k * LN_A;
-                    if (i < n4) {
-                        const float gv = gp ? __ldg(gp + cq) : 1.f, bv = bp ? __ldg(bp + cq) : 0.f;
-                        const float g2 = gv + gv, b2 = bv + bv;
-                        float4 o;
-                        o.x = fmaf(((v[k].x - rm.hi) - rm.lo) * rm.rstd, g2, b2);
-                        o.y = fmaf(((v[k].y - rm.hi) - rm.lo) * rm.rstd, g2, b2);
-                        o.z = fmaf(((v[k].z - rm.hi) - rm.lo) * rm.rstd, g2, b2);
-                        o.w = fmaf(((v[k].w - rm.hi) - rm.lo) * rm.rstd, g2, b2);
-                        o.x = o.x > 0.f ? o.x : gp_.slope * o.x;
-                        o.y = o.y > 0.f ? o.y : gp_.slope * o.y;
-                        o.z = o.z > 0.f ? o.z : gp_.slope * o.z;
-                        o.w = o.w > 0.f ? o.w : gp_.slope * o.w;
-                        st_stream_f4(yr + i, o, pol_stream);
+                    if (i < nu) {
+                        const float gv = gp ? ldg_param(gp + cq) : 1.f, bv = bp ? ldg_param(bp + cq) : 0.f;
+                        st_stream_f4(yr + i, gn_unit<T>(v[k], rm, gv + gv, bv + bv, gp_.slope), pol_stream);
                     }
-                    // next vector: 4 LN_A elements on
-                    rq += 4u * LN_A;
-                    if (S >= 4u * LN_A) {
+                    // next unit: UE LN_A elements on
+                    rq += step;
+                    if (S >= step) {
                         if (rq >= S) {
                             rq -= S;
                             ++cq;
                         }
                     } else {
-                        const uint32_t e = e0 + 4u * LN_A * static_cast<uint32_t>(k + 1);
+                        const uint32_t e = e0 + step * static_cast<uint32_t>(k + 1);
                         cq = e / S;
                         rq = e - cq * S;
                     }
@@ -635,7 +750,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 // y of row r from registers, gamma/beta from TMEM in batches
                 // of LN_GB float4
                 const RowMean rm = row_mean[r & 1];
-                float4 *yr = y4 + grow(r) * L4 + f0;
+                float4 *yr = y4 + grow(r) * Lu + f0;
 #pragma unroll
                 for (int bt = 0; bt < LN_NB; ++bt) {
                     float4 g[LN_GB], bb[LN_GB];
@@ -658,8 +773,8 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                     for (int j = 0; j < LN_GB; ++j) {
                         const int k = bt * LN_GB + j;
                         const int i = at + k * LN_A;
-                        if (i < n4)
-                            st_stream_f4(yr + i, ln_apply4(v[k], rm, g[j], bb[j]), pol_stream);
+                        if (i < nu)
+                            st_stream_f4(yr + i, ln_unit<T>(v[k], rm, g[j], bb[j]), pol_stream);
                     }
                 }
             }
@@ -669,11 +784,11 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 // issuer's wait returns at once and lets it account for the copy
                 if (issuer && mbar_wait_bounded(&bar_x[q & 1], x_parity(q), drain_ns))
                     waited = q + 1;
-                const float4 *buf = ln_smem + (q & 1) * buf_f4;
+                const float4 *buf = ln_smem + (q & 1) * buf_u;
 #pragma unroll
                 for (int k = 0; k < LN_V; ++k) {
                     const int i = at + k * LN_A;
-                    v[k] = (i < n4) ? buf[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[k] = (i < nu) ? buf[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
             __syncwarp();
@@ -967,36 +1082,70 @@ LnPersistentConfig ln_persistent_config()
 cudaError_t ln_persistent_static_smem(int *bytes)
 {
     cudaFuncAttributes a;
-    const cudaError_t e = cudaFuncGetAttributes(&a, ln_persistent_kernel<false>);
-    if (e == cudaSuccess)
-        *bytes = static_cast<int>(a.sharedSizeBytes);
-    return e;
+    // the four forms declare the same static shared memory; report the largest
+    int most = 0;
+    const void *forms[] = {reinterpret_cast<const void *>(ln_persistent_kernel<float, false>),
+                           reinterpret_cast<const void *>(ln_persistent_kernel<float, true>),
+                           reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, false>),
+                           reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, true>)};
+    for (const void *k : forms) {
+        const cudaError_t e = cudaFuncGetAttributes(&a, k);
+        if (e != cudaSuccess)
+            return e;
+        most = static_cast<int>(a.sharedSizeBytes) > most ? static_cast<int>(a.sharedSizeBytes) : most;
+    }
+    *bytes = most;
+    return cudaSuccess;
 }
+
+namespace {
+
+const void *persistent_form(bool bf16, bool gn)
+{
+    if (bf16)
+        return gn ? reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, true>)
+                  : reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, false>);
+    return gn ? reinterpret_cast<const void *>(ln_persistent_kernel<float, true>)
+              : reinterpret_cast<const void *>(ln_persistent_kernel<float, false>);
+}
+
+} // namespace
 
 cudaError_t ln_persistent_setup(int max_dynamic_smem)
 {
-    const cudaError_t e = cudaFuncSetAttribute(ln_persistent_kernel<false>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
-    if (e != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(ln_persistent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_dynamic_smem);
+    for (int f = 0; f < 4; ++f) {
+        const cudaError_t e = cudaFuncSetAttribute(persistent_form(f >= 2, f & 1),
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, ln_persistent_kernel<false>, LN_THREADS,
-                                                         dyn_smem);
+    // the smallest over the four forms (each is one CTA a SM by design)
+    int least = 1 << 30;
+    for (int f = 0; f < 4; ++f) {
+        int n = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, persistent_form(f >= 2, f & 1),
+                                                                            LN_THREADS, dyn_smem);
+        if (e != cudaSuccess)
+            return e;
+        least = n < least ? n : least;
+    }
+    *ctas_per_sm = least;
+    return cudaSuccess;
 }
 
-cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream, const GnPersist *gn)
+cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream, bool bf16,
+                                 const GnPersist *gn)
 {
     LnParams args = p;
-    GnPersist gargs = gn ? *gn : GnPersist{1, 1, 4, 0.f};
+    GnPersist gargs = gn ? *gn : GnPersist{1, 1, 8, 0.f};
     void *kargs[] = {&args, &gargs};
-    const void *k = gn ? reinterpret_cast<const void *>(ln_persistent_kernel<true>)
-                       : reinterpret_cast<const void *>(ln_persistent_kernel<false>);
-    return cudaLaunchCooperativeKernel(k, dim3(grid), dim3(LN_THREADS), kargs, static_cast<size_t>(dyn_smem), stream);
+    return cudaLaunchCooperativeKernel(persistent_form(bf16, gn != nullptr), dim3(grid), dim3(LN_THREADS), kargs,
+                                       static_cast<size_t>(dyn_smem), stream);
 }
 
 int64_t ln_rows_max_row_len()

@@ -263,39 +263,45 @@ int64_t persistent_max_slice(const DeviceState &d)
     return m < by_smem ? m : by_smem;
 }
 
-// Longest row the persistent kernel serves with one HBM read of x: every
-// CTA's slice fits its shared-memory buffers, and the kernel partitions rows
-// with 32-bit arithmetic (row_len/4 * (grid + 1) < 2^32).
-int64_t persistent_max_row_len(const DeviceState &d)
+// Longest row of esz-byte elements the persistent kernel serves with one HBM
+// read of x: every CTA's slice of 16-byte units fits its shared-memory
+// buffers, and the kernel partitions rows with 32-bit arithmetic (units per
+// row * (grid + 1) < 2^32, elements of a row < 2^32).
+int64_t persistent_max_row_len(const DeviceState &d, int esz = 4)
 {
     if (!d.coop || d.ln_ctas_per_sm < 1)
         return 0;
+    const int64_t ue = 16 / esz; // elements per unit
     const int grid = persistent_grid(d);
-    const int64_t by_slice = persistent_max_slice(d) * grid * 4;
-    const int64_t by_index = ((int64_t(1) << 32) - 1) / (grid + 1) * 4;
-    const int64_t m = by_slice < by_index ? by_slice : by_index;
-    return m & ~int64_t(3);
+    const int64_t by_slice = persistent_max_slice(d) * grid * ue;
+    const int64_t by_index = ((int64_t(1) << 32) - 1) / (grid + 1) * ue;
+    int64_t m = by_slice < by_index ? by_slice : by_index;
+    if (m > (int64_t(1) << 31))
+        m = int64_t(1) << 31;
+    return m / ue * ue;
 }
 
-// Row groups of the persistent kernel for `rows` rows of L elements on a grid
-// of at most gmax CTAs, or 0 if no split of the grid holds a row slice.  A
-// group's CTAs must hold its slices (at most max_slice float4 each), and a
-// group's row must stream for about 4 us or more at the HBM rate (4 us *
-// 6.5 TB/s / 8 bytes an element = 3,250,000 / L groups at least) so that the
-// grid exchange, two rows ahead, hides behind it.  Measured on GB300 (fraction
+// Row groups of the persistent kernel for `rows` rows of L elements of esz
+// bytes on a grid of at most gmax CTAs, or 0 if no split of the grid holds a
+// row slice.  A group's CTAs must hold its slices (at most max_slice 16-byte
+// units each), and a group's row must stream for about 4 us or more at the
+// HBM rate (4 us * 6.5 TB/s / (2 esz bytes an element) = 13,000,000 /
+// (esz L) groups at least; 3,250,000 / L for fp32) so that the grid
+// exchange, two rows ahead, hides behind it.  Measured on GB300 (fraction
 // of the copy peak): 2.6 us a group row gave 0.73-0.76, 3.9-5.2 us 0.87-0.92.  Among the admissible
 // counts (at most one group per row), the one that leaves the fewest idle
 // row slots (ceil(rows / k) * k) wins; ties go to more groups.
-int persistent_groups(int64_t rows, int64_t L, int gmax, int64_t max_slice)
+int persistent_groups(int64_t rows, int64_t L, int gmax, int64_t max_slice, int esz)
 {
-    const int64_t L4 = L / 4;
-    const int64_t gk_min = (L4 + max_slice - 1) / max_slice;
+    const int64_t Lu = L * esz / 16;
+    const int64_t gk_min = (Lu + max_slice - 1) / max_slice;
     if (gk_min < 1 || gk_min > gmax)
         return 0;
     int64_t kmax = gmax / gk_min;
     if (kmax > rows)
         kmax = rows;
-    int64_t kmin = (int64_t(3250000) + L - 1) / L;
+    const int64_t per_group_bytes = int64_t(13000000) / esz; // elements x esz
+    int64_t kmin = (per_group_bytes + L - 1) / L;
     if (kmin < 1)
         kmin = 1;
     if (kmin > kmax)
@@ -311,20 +317,22 @@ int persistent_groups(int64_t rows, int64_t L, int gmax, int64_t max_slice)
     return static_cast<int>(best);
 }
 
-// Fills the persistent plan if the shape qualifies; returns false if not.
-bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl)
+// Fills the persistent plan for rows of L elements of esz bytes (4 fp32, 2
+// bf16) if the shape qualifies (whole 16-byte units); returns false if not.
+bool plan_persistent(int64_t rows, int64_t L, const DeviceState &d, LnPlan *pl, int esz = 4)
 {
-    if ((L & 3) != 0 || L > persistent_max_row_len(d) || rows < 1)
+    const int64_t ue = 16 / esz;
+    if (L % ue != 0 || L > persistent_max_row_len(d, esz) || rows < 1)
         return false;
     const normk::LnPersistentConfig cfg = normk::ln_persistent_config();
     const int gmax = persistent_grid(d);
-    const int groups = persistent_groups(rows, L, gmax, persistent_max_slice(d));
+    const int groups = persistent_groups(rows, L, gmax, persistent_max_slice(d), esz);
     if (groups < 1)
         return false;
     const int gk = gmax / groups;
     const int grid = gk * groups;
-    const int64_t L4 = L / 4;
-    int64_t max_n4 = (L4 + gk - 1) / gk;
+    const int64_t Lu = L / ue;
+    int64_t max_n4 = (Lu + gk - 1) / gk;
     if (max_n4 < 1)
         max_n4 = 1;
     pl->path = 1;
@@ -492,8 +500,11 @@ size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len)
     LnPlan ps, pp;
     plan_split(rows, row_len, (row_len & 3) == 0, *d, &ps);
     size_t bytes = ps.ws_bytes;
-    if (plan_persistent(rows, row_len, *d, &pp) && pp.ws_bytes > bytes)
-        bytes = pp.ws_bytes;
+    // the persistent plan of either element type (the call does not say which)
+    for (int esz = 4; esz >= 2; esz -= 2) {
+        if (plan_persistent(rows, row_len, *d, &pp, esz) && pp.ws_bytes > bytes)
+            bytes = pp.ws_bytes;
+    }
     return bytes;
 }
 
@@ -589,12 +600,13 @@ norm_status_t layer_plan(const void *x, const void *gamma, const void *beta, con
         c.pl.path = c.ln_stream ? kLnStream : 3;
         c.pl.ws_bytes = 0;
     }
-    // the persistent kernel is fp32 only
-    if (path_opt == 1 && bf16)
-        return NORM_ERR_UNSUPPORTED;
-    if (!c.row_kernel && !c.ln_stream && path_opt != 2 && vec4 && !bf16) {
+    // the persistent kernel moves whole 16-byte units (4 fp32 or 8 bf16
+    // values) of 16-byte aligned tensors
+    const bool unit_ok = row_len % (16 / esz) == 0 && aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
+                         aligned(beta, 16);
+    if (!c.row_kernel && !c.ln_stream && path_opt != 2 && unit_ok) {
         LnPlan pp;
-        if (plan_persistent(rows, row_len, *d, &pp) && (path_opt == 1 || row_len >= kPersistentMinRowLen)) {
+        if (plan_persistent(rows, row_len, *d, &pp, esz) && (path_opt == 1 || row_len >= kPersistentMinRowLen)) {
             c.pl = pp;
             c.persistent = true;
         }
@@ -672,7 +684,7 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
         p.tag_skew = static_cast<unsigned>(g_opt_extra_arrivals.load());
         p.max_n4 = pl.max_n4;
         p.groups = pl.groups;
-        e = normk::ln_persistent_launch(p, pl.grid, pl.dyn_smem, stream);
+        e = normk::ln_persistent_launch(p, pl.grid, pl.dyn_smem, stream, bf16);
     } else {
         e = normk::ln_split_launch(p, bf16, pl.vec4, stream);
     }
@@ -802,10 +814,12 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     const bool team_ok = team_items <= normk::gns_team_max_items();
     const bool team_auto = team_ok && (team_items <= normk::gns_team_max_items() / 2 || !bf16 || !cluster);
     // Persistent path (the LayerNorm persistent kernel in its GroupNorm form):
-    // fp32, each 4-element vector inside one channel (S % 4 == 0), x read
-    // from HBM once for segments too long for a cluster to hold.
+    // each 16-byte unit (4 fp32 or 8 bf16 values) inside one channel (S a
+    // multiple of it), 16-byte aligned x and y, x read from HBM once for
+    // segments too long for a cluster to hold.
     LnPlan pp;
-    const bool pers_ok = !bf16 && vec4 && (S & 3) == 0 && plan_persistent(R, L, *d, &pp);
+    const bool pers_ok = S % (16 / esz) == 0 && aligned(x, 16) && aligned(y, 16) &&
+                         plan_persistent(R, L, *d, &pp, esz);
     GnPlan pl;
     if (opt == kGnPersistent && !pers_ok)
         return NORM_ERR_UNSUPPORTED;
@@ -892,7 +906,7 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         gp.M = static_cast<uint32_t>(M);
         gp.S = static_cast<uint32_t>(S);
         gp.slope = negative_slope;
-        e = normk::ln_persistent_launch(lp, pp.grid, pp.dyn_smem, stream, &gp);
+        e = normk::ln_persistent_launch(lp, pp.grid, pp.dyn_smem, stream, bf16, &gp);
     } else {
         plan_gn_split(R, L, vec4, *d, &pl);
         void *ws = workspace;
@@ -1003,8 +1017,10 @@ size_t norm_group_lrelu_x2_nchw_workspace_bytes(int64_t N, int64_t C, int64_t S,
         return 0;
     size_t bytes = gn_split_ws_bound(R, L, *d);
     LnPlan pp;
-    if ((S & 3) == 0 && plan_persistent(R, L, *d, &pp) && pp.ws_bytes > bytes)
-        bytes = pp.ws_bytes;
+    for (int esz = 4; esz >= 2; esz -= 2) {
+        if (S % (16 / esz) == 0 && plan_persistent(R, L, *d, &pp, esz) && pp.ws_bytes > bytes)
+            bytes = pp.ws_bytes;
+    }
     return bytes;
 }
 

@@ -691,15 +691,18 @@ cudaError_t ln_persistent_setup(int max_dynamic_smem);
 // Number of co-resident CTAs per SM for `dyn_smem` bytes.
 cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm);
 // The persistent kernel's GroupNorm form: row r is segment (r / G, r % G) of
-// M channels x S positions (S % 4 == 0); gamma/beta of LnParams are per
-// channel [G * M]; the output is 2 LReLU((x - mean) * rstd * gamma + beta).
+// M channels x S positions (S a multiple of the 16-byte unit's 4 fp32 or 8
+// bf16 values); gamma/beta of LnParams are per channel [G * M]; the output is
+// 2 LReLU((x - mean) * rstd * gamma + beta).
 struct GnPersist {
     int64_t G;
     uint32_t M, S;
     float slope;
 };
-// gn: null for LayerNorm, else the GroupNorm form over NCHW segments.
-cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream,
+// bf16: x, y, gamma, beta of bfloat16 (row_len a multiple of 8, max_n4 and
+// the slices counted in 16-byte units), else fp32.  gn: null for LayerNorm,
+// else the GroupNorm form over NCHW segments.
+cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cudaStream_t stream, bool bf16,
                                  const GnPersist *gn = nullptr);
 
 // Two-kernel LayerNorm (partials, then merge + apply); any shape.  bf16:

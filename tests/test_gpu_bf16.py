@@ -80,7 +80,7 @@ def run_ln(ng, x, g, b, rows, L, path=0, offset=0, inplace=False):
     (3, 12, 3), (64, 4096, 3), (9, 16384, 3), (5, 1000, 3),   # row kernel
     (64, 4096, 4), (5, 20000, 4), (2, 131072, 4), (3, 65544, 4),  # streamed cluster kernel
     (2, 262144, 4), (3, 32768, 0),                                # bf16 slices of 4,096 packed vectors
-    (2, 16388, 2), (3, 4096, 2), (2, 1 << 20, 0),             # two-kernel path, vector form
+    (2, 16388, 2), (3, 4096, 2), (2, 1 << 20, 2),             # two-kernel path, vector form
     (3, 1001, 0),                                             # two-kernel path, scalar form
 ])
 def test_layer_norm_bf16(ng, rows, L, path):
@@ -101,17 +101,49 @@ def test_layer_norm_bf16_in_place_no_affine_misaligned(ng, offset):
                        f"LN bf16 in place offset={offset}")
 
 
-def test_layer_norm_bf16_refuses_the_persistent_kernel(ng):
-    rows, L = 1, 1 << 20
-    x = BGuarded(rows * L, bf16_inputs(rows * L))
-    y = BGuarded(rows * L)
+@pytest.mark.parametrize("rows,L,path", [
+    (2, 1 << 20, 0),       # the automatic choice above 131,072: one row group per row
+    (3, 131080, 0),        # just above the cluster kernel's longest row
+    (16, 262144, 0),       # 16 row groups (a bf16 group row must stream as long as an fp32 one)
+    (40, 131088, 1),       # forced: many row groups of few CTAs
+    (5, 64, 1),            # forced: 8 units a row, most CTAs hold nothing
+    (3, 8, 1),             # forced: one unit a row
+    (1, (1 << 23) + 8, 0), # 8,388,616 values: 55,184 a CTA, close to the longest row
+])
+def test_layer_norm_bf16_persistent(ng, rows, L, path):
+    """bf16 rows on the persistent kernel: 16-byte units of 8 values, gamma/beta packed in TMEM."""
+    x = bf16_inputs(rows * L, seed=rows + L + 1)
+    g = bf16_inputs(L, 1.0, 0.1, seed=rows + L + 1, tensor_id=1)
+    b = bf16_inputs(L, 0.0, 0.1, seed=rows + L + 1, tensor_id=2)
+    want = oracle.layer_norm(x, g, b, rows, L, f64=True)
+    assert_bf16_parity(run_ln(ng, x, g, b, rows, L, path=path), want, f"LN bf16 persistent {rows}x{L} path={path}")
+
+
+def test_layer_norm_bf16_persistent_no_affine_in_place_offset_mean(ng):
+    rows, L = 3, 1 << 18
+    x = bf16_inputs(rows * L, 50.0, 1.0, seed=12)  # bf16 spacing at 50 is 0.25: values well away from the mean's zero
+    want = oracle.layer_norm(x, None, None, rows, L, f64=True)
+    assert_bf16_parity(run_ln(ng, x, None, None, rows, L, path=1), want, "LN bf16 persistent no affine")
+    assert_bf16_parity(run_ln(ng, x, None, None, rows, L, path=1, inplace=True), want,
+                       "LN bf16 persistent in place")
+
+
+@pytest.mark.parametrize("L,offset", [(131076, 0), (1 << 18, 4)])
+def test_layer_norm_bf16_persistent_refusals(ng, L, offset):
+    """Forced, the persistent kernel refuses rows that are not whole 16-byte units (L % 8 != 0) and
+    tensors that are not 16-byte aligned (an offset of 4 elements); the automatic choice serves both."""
+    rows = 2
+    x = bf16_inputs(rows * L, seed=13)
     ng.norm_set_option(ng.NORM_OPT_LN_PATH, 1)
     try:
+        xb, yb = BGuarded(rows * L, x, offset), BGuarded(rows * L, offset=offset)
         with pytest.raises(ng.NormError) as e:
-            ng.norm_layer_fwd_bf16(x.t, None, None, y.t, rows, L, 1e-5)
+            ng.norm_layer_fwd_bf16(xb.t, None, None, yb.t, rows, L, 1e-5)
         assert e.value.status == ng.NORM_ERR_UNSUPPORTED
     finally:
         ng.norm_set_option(ng.NORM_OPT_LN_PATH, 0)
+    want = oracle.layer_norm(x, None, None, rows, L, f64=True)
+    assert_bf16_parity(run_ln(ng, x, None, None, rows, L, offset=offset), want, f"LN bf16 {L} offset={offset}")
 
 
 def test_layer_norm_bf16_full_size(ng):
@@ -218,9 +250,32 @@ def test_group_norm_nchw_bf16(ng, N, C, S, G, path, cluster):
     assert_bf16_parity(xb.values(), want, f"GN NCHW bf16 in place ({N},{C},{S})/{G}")
 
 
-def test_group_norm_nchw_bf16_refuses_the_persistent_path(ng):
-    # the persistent kernel is fp32 only; the automatic choice takes the two-kernel path
-    N, C, S, G = 1, 128, 65536, 32
+@pytest.mark.parametrize("N,C,S,G,path", [
+    (1, 128, 512 * 512, 32, 0),  # (1, 128, 512, 512): 67 MB of x, the automatic choice
+    (1, 128, 65536, 32, 6),      # forced: 32 segments of 262,144
+    (2, 8, 36000, 2, 6),         # forced: S = 36000, a channel boundary inside a thread's stride
+    (2, 2048, 8, 16, 6),         # forced: S = 8, a new channel at every unit
+])
+def test_group_norm_nchw_bf16_persistent(ng, N, C, S, G, path):
+    n = N * C * S
+    x = bf16_inputs(n, seed=N + C + S + 5)
+    g = bf16_inputs(C, 1.0, 0.1, seed=N + C + S + 5, tensor_id=1)
+    b = bf16_inputs(C, 0.0, 0.1, seed=N + C + S + 5, tensor_id=2)
+    want = oracle.group_lrelu_x2_nchw(x, g, b, N, C, S, G, f64=True)
+    xb, gb, bb, yb = BGuarded(n, x), BGuarded(C, g), BGuarded(C, b), BGuarded(n)
+    ng.norm_set_option(ng.NORM_OPT_GN_PATH, path)
+    try:
+        ng.norm_group_lrelu_x2_nchw_fwd_bf16(xb.t, gb.t, bb.t, yb.t, N, C, S, G, 1e-5, 0.01)
+        assert ng.norm_last_error() == 0
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_GN_PATH, 0)
+    assert_bf16_parity(yb.values(), want, f"GN NCHW bf16 persistent ({N},{C},{S})/{G}")
+    assert yb.guards_intact()
+
+
+def test_group_norm_nchw_bf16_persistent_refuses_split_units(ng):
+    # S = 4: an 8-value unit would hold two channels
+    N, C, S, G = 2, 64, 4, 4
     xb, yb = BGuarded(N * C * S, bf16_inputs(N * C * S, seed=3)), BGuarded(N * C * S)
     ng.norm_set_option(ng.NORM_OPT_GN_PATH, 6)
     try:
