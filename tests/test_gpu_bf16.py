@@ -158,8 +158,10 @@ def test_layer_norm_bf16_full_size(ng):
 # ------------------------------------------------------------------ RMSNorm
 
 @pytest.mark.parametrize("B,C,S", [(2, 64, 1024), (3, 1, 37), (2, 3, 129), (2, 128, 300), (2, 200, 65), (1, 48, 513),
-                                   (2, 32, 1000), (3, 16, 2), (2, 64, 40002)])
+                                   (2, 32, 1000), (3, 16, 2), (2, 64, 40002), (4, 8, 6), (2, 4, 258)])
 def test_rms_bf16(ng, B, C, S):
+    """Even S with C in {4, 8, 16, 32, 64} takes two positions a thread (4-byte loads and stores of
+    bf16 pairs); odd S, other C and misaligned pointers take one position a thread."""
     x = bf16_inputs(B * C * S, seed=B * C + S)
     want = oracle.rms_channel(x, B, C, S, f64=True)
     xb, yb = BGuarded(B * C * S, x), BGuarded(B * C * S)
