@@ -877,40 +877,79 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
             bk[k] = (bt && i < L4) ? Io<T>::ld4_ro(bt + 4 * i, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    // fp32 rows, and bf16 rows of at most 8 vectors a thread, are held as
+    // d = x - K in f32x2 pairs.  bf16 rows of 16 vectors a thread are held
+    // packed as loaded (two registers a vector, so a thread keeps twice the
+    // bytes in flight that widened values would allow) and widened in each
+    // pass; measured faster for rows of 4,096 and 8,192 values, slower for
+    // shorter rows, where it adds the widening without adding bytes in flight.
+    constexpr bool RAW = sizeof(T) == 2 && V >= 16;
     for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
         const T *xr = x + r * p.row_len;
-        float2 vl[V], vh[V]; // the vectors' pairs, as f32x2 operands
+        float2 vl[RAW ? 1 : V], vh[RAW ? 1 : V];
+        uint2 raw[RAW ? V : 1];
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t i = tid + k * NT;
-            const float4 t = i < L4 ? Io<T>::ld4_stream(xr + 4 * i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
-            vl[k] = make_float2(t.x, t.y);
-            vh[k] = make_float2(t.z, t.w);
+            if constexpr (RAW) {
+                raw[k] = make_uint2(0u, 0u);
+                if (i < L4)
+                    asm("ld.global.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+                        : "=r"(raw[k].x), "=r"(raw[k].y)
+                        : "l"(xr + 4 * i), "l"(pol_stream));
+            } else {
+                const float4 t =
+                    i < L4 ? Io<T>::ld4_stream(xr + 4 * i, pol_stream) : make_float4(0.f, 0.f, 0.f, 0.f);
+                vl[k] = make_float2(t.x, t.y);
+                vh[k] = make_float2(t.z, t.w);
+            }
         }
+        // the vector's pairs widened and shifted by off (bf16), or the held
+        // pairs plus off (fp32, already d = x - K)
+        auto pair = [&](int k, float2 off, float2 &l, float2 &h) {
+            if constexpr (RAW) {
+                l = __fadd2_rn(make_float2(__uint_as_float(raw[k].x << 16), __uint_as_float(raw[k].x & 0xffff0000u)),
+                               off);
+                h = __fadd2_rn(make_float2(__uint_as_float(raw[k].y << 16), __uint_as_float(raw[k].y & 0xffff0000u)),
+                               off);
+            } else {
+                l = __fadd2_rn(vl[k], off);
+                h = __fadd2_rn(vh[k], off);
+            }
+        };
         // every thread reads the pivot before any thread of the CTA stores
         // (the block sums below are barriers), so y == x is safe
         const float K = Io<T>::ld1(xr);
-        const float2 negk = make_float2(-K, -K);
-        // from here on vl/vh hold d = x - K (zero outside the row)
-        float2 sl = make_float2(0.f, 0.f), sh = make_float2(0.f, 0.f);
+        const float2 negk = make_float2(-K, -K), zero2 = make_float2(0.f, 0.f);
+        // from here on the fp32 pairs hold d = x - K (zero outside the row)
+        float2 sl = zero2, sh = zero2;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             if (tid + k * NT < L4) {
-                vl[k] = __fadd2_rn(vl[k], negk);
-                vh[k] = __fadd2_rn(vh[k], negk);
-                sl = __fadd2_rn(sl, vl[k]);
-                sh = __fadd2_rn(sh, vh[k]);
+                float2 l, h;
+                pair(k, negk, l, h);
+                if constexpr (!RAW) {
+                    vl[k] = l;
+                    vh[k] = h;
+                }
+                sl = __fadd2_rn(sl, l);
+                sh = __fadd2_rn(sh, h);
             }
         }
         float s = (sl.x + sl.y) + (sh.x + sh.y);
         s = block_sum<NT>(s, red[0]);
         const float mean_d = s / Lf;
         const float2 nm = make_float2(-mean_d, -mean_d);
-        float2 ql = make_float2(0.f, 0.f), qh = make_float2(0.f, 0.f);
+        // deviations from the mean: d - mean_d (fp32), or x - (K + mean_d)
+        // with the centre rounded once (bf16; its offset from the exact
+        // centre adds at most L * ulp(K)^2 / 4 to M2)
+        const float2 nc = RAW ? make_float2(-(K + mean_d), -(K + mean_d)) : nm;
+        float2 ql = zero2, qh = zero2;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             if (tid + k * NT < L4) {
-                const float2 el = __fadd2_rn(vl[k], nm), eh = __fadd2_rn(vh[k], nm);
+                float2 el, eh;
+                pair(k, nc, el, eh);
                 ql = __ffma2_rn(el, el, ql);
                 qh = __ffma2_rn(eh, eh, qh);
             }
@@ -934,9 +973,11 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
                 }
                 // y = (d - mean_d) * rstd * g + b = d * a + c, a = rstd * g,
                 // c = b - mean_d * a
+                float2 dl, dh;
+                pair(k, RAW ? negk : zero2, dl, dh);
                 const float2 al = __fmul2_rn(make_float2(g.x, g.y), r2), ah = __fmul2_rn(make_float2(g.z, g.w), r2);
-                const float2 ol = __ffma2_rn(vl[k], al, __ffma2_rn(nm, al, make_float2(b.x, b.y)));
-                const float2 oh = __ffma2_rn(vh[k], ah, __ffma2_rn(nm, ah, make_float2(b.z, b.w)));
+                const float2 ol = __ffma2_rn(dl, al, __ffma2_rn(nm, al, make_float2(b.x, b.y)));
+                const float2 oh = __ffma2_rn(dh, ah, __ffma2_rn(nm, ah, make_float2(b.z, b.w)));
                 Io<T>::st4_stream(yr + 4 * i, make_float4(ol.x, ol.y, oh.x, oh.y), pol_stream);
             }
         }
@@ -1181,14 +1222,17 @@ cudaError_t ln_rows_launch_t(const LnParams &p, int sm_count, cudaStream_t strea
 template <typename T>
 cudaError_t ln_rows_launch_sized(const LnParams &p, int sm_count, cudaStream_t stream)
 {
+    // vectors a thread: 8, or 16 for bf16 rows of more than 2,048 values
+    // (held packed, so the same registers; 64 threads or more a row)
     const int64_t L4 = p.row_len / 4;
-    if (L4 <= 32 * 8)
+    const int64_t VT = sizeof(T) == 2 && L4 > 64 * 8 ? 16 : 8;
+    if (L4 <= 32 * VT)
         return ln_rows_launch_t<T, 32>(p, sm_count, stream);
-    if (L4 <= 64 * 8)
+    if (L4 <= 64 * VT)
         return ln_rows_launch_t<T, 64>(p, sm_count, stream);
-    if (L4 <= 128 * 8)
+    if (L4 <= 128 * VT)
         return ln_rows_launch_t<T, 128>(p, sm_count, stream);
-    if (L4 <= 256 * 8)
+    if (L4 <= 256 * VT)
         return ln_rows_launch_t<T, 256>(p, sm_count, stream);
     return ln_rows_launch_t<T, 512>(p, sm_count, stream);
 }
