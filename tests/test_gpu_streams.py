@@ -4,8 +4,9 @@ The library's calls are stream-ordered and allocate nothing when given a workspa
 they may run at the same time on different streams (each with its own workspace) and be
 captured into CUDA graphs.  Covered: two persistent LayerNorm launches (cooperative, every
 SM) on two streams at once beside the cluster kernels of GroupNorm and LayerNorm, the
-row kernel, the (N, C) GroupNorm (vector and team-per-group kernels) and RMSNorm; and a
-graph replaying every non-cooperative path several times.
+row kernel, the (N, C) GroupNorm (vector and team-per-group kernels) and RMSNorm; a graph
+replaying every non-cooperative path several times; and a graph replaying the cooperative
+persistent kernel (LayerNorm fp32 and bf16, the NCHW GroupNorm form) on caller workspaces.
 """
 import numpy as np
 import pytest
@@ -148,3 +149,62 @@ def test_graph_capture_and_replay(ng):
     for y, want, what in ((y1, w1, "LN cluster kernel"), (y2, w2, "LN row kernel"), (y3, w3, "GN NCHW"),
                           (y4, w4, "RMS"), (y5, w5, "GN team kernel")):
         assert_parity(y.cpu().numpy(), want, f"{what} replayed from a graph")
+
+
+def test_graph_capture_of_persistent_kernels(ng):
+    """The cooperative persistent kernel captured into a graph and replayed: LayerNorm fp32 and
+    bf16 and the NCHW GroupNorm form, each on a caller workspace (the kernel advances the
+    workspace's row base itself, so replays need no host step), plus bf16 RMSNorm pairs."""
+    rows, L = 3, 1 << 20
+    x1, g1, b1, w1 = ln_case(rows, L, 21)
+    nb1 = ng.norm_layer_workspace_bytes(rows, L)
+    ws1 = torch.zeros(nb1 // 4 + 64, device="cuda")
+    N, C, S, G = 2, 8, 36000, 2
+    x2, g2, b2, w2 = gn_case(N, C, S, G, 22)
+    nb2 = ng.norm_group_lrelu_x2_nchw_workspace_bytes(N, C, S, G)
+    ws2 = torch.zeros(nb2 // 4 + 64, device="cuda")
+    rows3, L3 = 2, 262144
+    x3 = normgen.round_bf16(normgen.normal(rows3 * L3, seed=23, tensor_id=0))
+    g3 = normgen.round_bf16(normgen.normal(L3, 1.0, 0.1, seed=23, tensor_id=1))
+    b3 = normgen.round_bf16(normgen.normal(L3, 0.0, 0.1, seed=23, tensor_id=2))
+    w3 = oracle.layer_norm(x3, g3, b3, rows3, L3, f64=True)
+    nb3 = ng.norm_layer_workspace_bytes(rows3, L3)
+    ws3 = torch.zeros(nb3 // 4 + 64, device="cuda")
+    x4 = normgen.round_bf16(normgen.normal(2 * 64 * 1024, seed=24, tensor_id=0))
+    w4 = oracle.rms_channel(x4, 2, 64, 1024, f64=True)
+    d1 = [dev(a) for a in (x1, g1, b1)]
+    d2 = [dev(a) for a in (x2, g2, b2)]
+    d3 = [dev(a).to(torch.bfloat16) for a in (x3, g3, b3)]
+    d4 = dev(x4).to(torch.bfloat16)
+    y1, y2, y3, y4 = (torch.empty_like(t) for t in (d1[0], d2[0], d3[0], d4))
+    s = torch.cuda.Stream()
+    ng.norm_set_option(ng.NORM_OPT_GN_PATH, 6)
+    try:
+        def step():
+            ng.norm_layer_fwd(d1[0], d1[1], d1[2], y1, rows, L, 1e-5, ws1, nb1, stream=s.cuda_stream)
+            ng.norm_group_lrelu_x2_nchw_fwd(d2[0], d2[1], d2[2], y2, N, C, S, G, 1e-5, 0.01, ws2, nb2,
+                                            stream=s.cuda_stream)
+            ng.norm_layer_fwd_bf16(d3[0], d3[1], d3[2], y3, rows3, L3, 1e-5, ws3, nb3, stream=s.cuda_stream)
+            ng.norm_rms_channel_fwd_bf16(d4, y4, 2, 64, 1024, 1e-5, stream=s.cuda_stream)
+
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            step()  # first calls outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    finally:
+        ng.norm_set_option(ng.NORM_OPT_GN_PATH, 0)
+    for y in (y1, y2, y3, y4):
+        y.fill_(float("nan"))
+    torch.cuda.synchronize()
+    for _ in range(5):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert ng.norm_last_error() == 0
+    from gpu_util import assert_bf16_parity
+    assert_parity(y1.cpu().numpy(), w1, "persistent LN replayed from a graph")
+    assert_parity(y2.cpu().numpy(), w2, "persistent GN NCHW replayed from a graph")
+    assert_bf16_parity(y3.float().cpu().numpy(), w3, "persistent LN bf16 replayed from a graph")
+    assert_bf16_parity(y4.float().cpu().numpy(), w4, "RMS bf16 pairs replayed from a graph")
