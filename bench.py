@@ -245,6 +245,9 @@ def main_kernel_name(cfg) -> str:
         if L % 4 == 0 and L <= 131072:
             return "gns_stream_kernel"
         return "ln_persistent_kernel" if gn_nchw_persistent(cfg) else "gns_split_apply_kernel"
+    # bf16 with even S and an exact channel count of at most 64 takes two positions a thread
+    if cfg.get("bf16") and cfg["S"] % 2 == 0 and cfg["C"] in (4, 8, 16, 32, 64):
+        return "rms_bf16x2_kernel"
     return "rms_reg_kernel"
 
 
