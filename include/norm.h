@@ -94,7 +94,8 @@ typedef enum {
  *   - rows of at most 8,192 elements (16,384 for fp32): one launch, one
  *     CTA per row at a time, sized to the row, with the row in registers;
  *     x is read from HBM once and the workspace is not used;
- *   - longer rows of up to 131,072 elements: one launch of the thread-block
+ *   - longer rows of up to 131,072 elements (over less than 96 MiB of x for
+ *     rows of 32,768 or more): one launch of the thread-block
  *     cluster kernel that GroupNorm over NCHW tensors uses (one group per
  *     row): each row is split over one CTA or a cluster of up to 16 CTAs,
  *     each CTA's next slices arrive by bulk copy into shared memory, and
@@ -102,7 +103,8 @@ typedef enum {
  *     distributed shared memory; x is read from HBM once; no workspace;
  *   - longer rows (up to norm_layer_max_resident_row_len() fp32 elements,
  *     or twice as many bf16; a length that is a multiple of 4 fp32 or 8
- *     bf16 values and 16-byte aligned x, y, gamma and beta): a
+ *     bf16 values and 16-byte aligned x, y, gamma and beta), and rows of
+ *     32,768 elements or more when x holds 96 MiB or more: a
  *     persistent cooperative kernel (one CTA per SM) gives every CTA the
  *     same column slice of each row, holds the slice on chip (shared memory,
  *     then registers) from the moment it arrives until y is written, and

@@ -27,6 +27,16 @@ constexpr size_t kWsHeader = sizeof(normk::LnSync);
 // elements are split over row groups (persistent_groups) so that each
 // group's row streams long enough to hide its grid exchange.
 constexpr int64_t kPersistentMinRowLen = 131073;
+// Rows of 32,768 to 131,072 elements take the persistent kernel (in row
+// groups) rather than the cluster kernel once x holds 96 MiB or more.
+// Measured on GB300 over 256 MiB of fp32 x (fraction of the copy peak):
+// rows of 32,768 0.81 vs 0.73, 65,536 0.85 vs 0.74, 131,072 0.86 vs 0.73;
+// bf16 over 128 MiB: 0.58 vs 0.57, 0.58 vs 0.45, 0.62 vs 0.52.  Below about
+// 60-100 MiB the persistent kernel's prologue (about 5 us more than the
+// cluster kernel's launch) outweighs its faster streaming.  Rows of 16,384
+// stay on the row and cluster kernels (fp32 0.84 vs 0.81 persistent).
+constexpr int64_t kPersistentMidRowLen = 32768;
+constexpr size_t kPersistentMidMinBytes = size_t(96) << 20;
 // NORM_OPT_LN_PATH value of the streamed cluster kernel, and the longest
 // row the automatic choice gives the row kernel.  Measured on GB300 (GB/s
 // fractions of the copy peak): the row kernel, its CTA sized to the row,
@@ -588,11 +598,26 @@ norm_status_t layer_plan(const void *x, const void *gamma, const void *beta, con
     }
     if (path_opt == kLnStream && !c.ln_cluster)
         return NORM_ERR_UNSUPPORTED;
+    // the persistent kernel moves whole 16-byte units (4 fp32 or 8 bf16
+    // values) of 16-byte aligned tensors
+    const bool unit_ok = row_len % (16 / esz) == 0 && aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
+                         aligned(beta, 16);
+    const bool pers_wanted = path_opt == 1 || (path_opt == 0 && (row_len >= kPersistentMinRowLen ||
+                                                                 (row_len >= kPersistentMidRowLen &&
+                                                                  nb >= kPersistentMidMinBytes)));
+    LnPlan pp;
+    if (pers_wanted && unit_ok && plan_persistent(rows, row_len, *d, &pp, esz)) {
+        c.pl = pp;
+        c.persistent = true;
+    }
+    if (path_opt == 1 && !c.persistent)
+        return NORM_ERR_UNSUPPORTED;
     const int64_t rows_max_auto = bf16 ? kLnRowsMaxAuto : kLnRowsMaxAutoF32;
-    c.ln_stream = c.ln_cluster && (path_opt == kLnStream ||
-                                   (path_opt == 0 && row_len > rows_max_auto && row_len <= kLnStreamMaxAuto));
+    c.ln_stream = !c.persistent && c.ln_cluster &&
+                  (path_opt == kLnStream ||
+                   (path_opt == 0 && row_len > rows_max_auto && row_len <= kLnStreamMaxAuto));
     const bool row_kernel_fits = vec4 && row_len <= normk::ln_rows_max_row_len();
-    c.row_kernel = !c.ln_stream && row_kernel_fits &&
+    c.row_kernel = !c.persistent && !c.ln_stream && row_kernel_fits &&
                    (path_opt == 3 || (path_opt == 0 && row_len < kPersistentMinRowLen));
     if (path_opt == 3 && !c.row_kernel)
         return NORM_ERR_UNSUPPORTED;
@@ -600,19 +625,6 @@ norm_status_t layer_plan(const void *x, const void *gamma, const void *beta, con
         c.pl.path = c.ln_stream ? kLnStream : 3;
         c.pl.ws_bytes = 0;
     }
-    // the persistent kernel moves whole 16-byte units (4 fp32 or 8 bf16
-    // values) of 16-byte aligned tensors
-    const bool unit_ok = row_len % (16 / esz) == 0 && aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
-                         aligned(beta, 16);
-    if (!c.row_kernel && !c.ln_stream && path_opt != 2 && unit_ok) {
-        LnPlan pp;
-        if (plan_persistent(rows, row_len, *d, &pp, esz) && (path_opt == 1 || row_len >= kPersistentMinRowLen)) {
-            c.pl = pp;
-            c.persistent = true;
-        }
-    }
-    if (path_opt == 1 && !c.persistent)
-        return NORM_ERR_UNSUPPORTED;
     if (!c.persistent && !c.row_kernel && !c.ln_stream)
         plan_split(rows, row_len, vec4, *d, &c.pl);
     *ch = c;

@@ -3,7 +3,8 @@
 All four paths are covered: the persistent single-read kernel (forced, and chosen
 automatically for long rows, over the whole grid or split into row groups), the one-launch row kernel (forced, and chosen
 automatically for rows of at most 8,192 elements), the thread-block cluster kernel
-shared with GroupNorm (forced, and chosen for fp32 rows of 8,193 to 131,072) and the
+shared with GroupNorm (forced, and chosen for fp32 rows of 16,385 to 131,072 over less
+than 96 MiB, and for rows of 16,385 to 32,767 over any size) and the
 two-kernel split path (forced, and taken for ragged or misaligned rows).  Shapes span several CTAs per row with ragged slices,
 rows shorter than one float4 per CTA, the largest row the persistent kernel
 holds on chip, and the two full-size workloads: (16, 64, 256, 256) with N(0,1)
@@ -181,10 +182,13 @@ def test_persistent_exchange_200_launches_back_to_back(ng):
     (3, 1 << 20, AUTO),         # one row per group
     (40, 131076, PERSISTENT),   # 25 groups of 6 CTAs, forced
     (7, 200004, AUTO),          # a length that is not a multiple of the group size
+    (1024, 32768, AUTO),        # 128 MiB of rows of 32,768: 76 groups of 2 CTAs (automatic)
+    (384, 65536, AUTO),         # 96 MiB of rows of 65,536: 50 groups of 3 CTAs (automatic)
 ])
 def test_persistent_row_groups(ng, rows, L, path):
-    """Rows of 131,073 to about 1.6 Mi elements: the persistent kernel splits its grid into
-    row groups, each taking every k-th row with its own grid exchange."""
+    """Rows of 131,073 to about 1.6 Mi elements, and rows of 32,768 or more over 96 MiB:
+    the persistent kernel splits its grid into row groups, each taking every k-th row
+    with its own grid exchange."""
     x, g, b = inputs(rows, L, seed=rows + L)
     want = oracle.layer_norm(x, g, b, rows, L)
     assert_parity(run_ln(ng, x, g, b, rows, L, path=path), want, f"LN row groups {rows}x{L}")
