@@ -231,13 +231,15 @@ def main_kernel_name(cfg) -> str:
         L, bf16 = cfg["L"], bool(cfg.get("bf16"))
         if L <= (8192 if bf16 else 16384):
             return "ln_rows_kernel"
-        if L <= 131072 and L % (8 if bf16 else 4) == 0:
+        big = cfg["rows"] * L * (2 if bf16 else 4) >= (96 << 20)
+        if L <= 131072 and L % (8 if bf16 else 4) == 0 and not (L >= 32768 and big):
             return "gns_stream_kernel"
         return "ln_persistent_kernel" if L % (8 if bf16 else 4) == 0 else "ln_split_apply_kernel"
     if cfg["op"] == "gn":
         M, bf16 = cfg["C"] // cfg["G"], bool(cfg.get("bf16"))
         if 4 <= M <= 128 and M & (M - 1) == 0:
-            return "gn_vec4_kernel"
+            # bench tensors are 16-byte aligned: bf16 groups of 8 or more take 8 channels a thread
+            return "gn_vec8_bf16_kernel" if bf16 and M >= 8 else "gn_vec4_kernel"
         items = M // 4 if M % 4 == 0 else M // 2 if M % 2 == 0 else M
         return "gns_team_kernel" if items <= (128 if bf16 else 256) else "gns_reg_kernel"
     if cfg["op"] == "gn_nchw":

@@ -226,8 +226,9 @@ norm_status_t norm_group_lrelu_x2_fwd(const float *x, const float *gamma, const 
 
 /* GroupNorm + LeakyReLU + x2 on bfloat16 x, gamma, beta and y (uint16_t bit
  * patterns), fp32 arithmetic, y rounded to nearest even once; pointers 2-byte
- * aligned (8-byte aligned with C % 4 == 0 for the vectorized kernel).
- * Otherwise as norm_group_lrelu_x2_fwd. */
+ * aligned (8-byte aligned with C % 4 == 0 for the vectorized kernel; with
+ * 16-byte aligned pointers and M of 8 to 128 it takes 8 channels per thread,
+ * one 16-byte access).  Otherwise as norm_group_lrelu_x2_fwd. */
 norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta,
                                            uint16_t *y, int64_t N, int64_t C, int64_t num_groups,
                                            float eps, float negative_slope, cudaStream_t stream);

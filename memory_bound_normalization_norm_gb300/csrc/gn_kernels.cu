@@ -13,6 +13,11 @@
 // columns' gamma/beta in registers and walks rows with two rows of x loads in
 // flight, held as loaded (bf16 packed, two registers a vector) until their
 // turn.  Every byte of x is read once and every byte of y written once.
+//
+// bf16 groups of 8 or more channels with 16-byte aligned tensors take a
+// wider form: a thread owns 8 channels (one 16-byte load, four registers
+// held packed) and keeps four rows of loads in flight, so an SM has as many
+// bytes of x in flight as in fp32 at half the bytes per element.
 #include "norm_internal.cuh"
 
 namespace normk {
@@ -147,6 +152,146 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
 }
 
 
+// bf16 vector path with 8 channels (one 16-byte access) a thread: a group of
+// M channels is TPG = M/8 adjacent lanes, and a warp covers 256 contiguous
+// elements (512 bytes).  Each row's x is held as loaded (four registers) from
+// its load, GN8_AHEAD rows ahead of the row being reduced, until its turn.
+constexpr int GN8_AHEAD = 4;
+// One resident wave: about 53 registers a thread leave room for 4 CTAs of
+// 256 threads an SM.  Measured at (1024, 8192) bf16, back to back: 7.95 us
+// against 8.97 us for the 4-channel form with two rows ahead; 3, 5, 6 and 8
+// rows ahead, two vectors a thread and 6 or 8 CTAs an SM measured 8.15-9.8 us.
+constexpr int GN8_CTAS_PER_SM = 4;
+
+__device__ __forceinline__ float2 bf16_pair(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint4 ld16_stream(const void *p, uint64_t pol)
+{
+    uint4 r;
+    asm("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld16_ro(const void *p, uint64_t pol)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+
+__device__ __forceinline__ void st16_stream(void *p, uint4 v, uint64_t pol)
+{
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+// grid: x = column blocks of GN_THREADS vectors of 8, y = row walkers.
+// x, y: [N][C] of bf16; C8 = C / 8.  Same walk as gn_vec4_kernel.
+template <int TPG>
+__global__ void __launch_bounds__(GN_THREADS) gn_vec8_bf16_kernel(const __nv_bfloat16 *x,
+                                                                  const __nv_bfloat16 *__restrict__ gamma,
+                                                                  const __nv_bfloat16 *__restrict__ beta,
+                                                                  __nv_bfloat16 *y, int64_t N, int C8, float invM,
+                                                                  float eps, float slope)
+{
+    constexpr int D = GN8_AHEAD;
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    pdl_begin();
+    const int c = blockIdx.x * GN_THREADS + threadIdx.x;
+    const bool in = c < C8;
+    // doubled gamma/beta of the vector's four pairs (see gn_vec4_kernel)
+    float2 g[4], b[4];
+    {
+        constexpr uint32_t one2 = 0x3f803f80u; // two bf16 1.0
+        const uint4 gv = (in && gamma) ? ld16_ro(gamma + 8 * c, pol_keep) : make_uint4(one2, one2, one2, one2);
+        const uint4 bv = (in && beta) ? ld16_ro(beta + 8 * c, pol_keep) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 gp = bf16_pair(gw[j]), bp = bf16_pair(bw[j]);
+            g[j] = make_float2(gp.x + gp.x, gp.y + gp.y);
+            b[j] = make_float2(bp.x + bp.x, bp.y + bp.y);
+        }
+    }
+    const float2 slope2 = make_float2(slope, slope);
+    const bool steep = slope > 1.f;
+    uint4 buf[D + 1]; // buf[0]: the row being reduced; buf[k]: k rows ahead
+    auto load_row = [&](int64_t n) {
+        return in ? ld16_stream(x + (n * C8 + c) * 8, pol_stream) : make_uint4(0u, 0u, 0u, 0u);
+    };
+#pragma unroll
+    for (int k = 0; k < D; ++k)
+        if (blockIdx.y + int64_t(k) * gridDim.y < N)
+            buf[k + 1] = load_row(blockIdx.y + int64_t(k) * gridDim.y);
+    for (int64_t n = blockIdx.y; n < N; n += gridDim.y) {
+#pragma unroll
+        for (int k = 0; k < D; ++k)
+            buf[k] = buf[k + 1];
+        // with y == x the rows ahead are other rows: loading them now cannot
+        // race with this row's stores
+        if (n + int64_t(D) * gridDim.y < N)
+            buf[D] = load_row(n + int64_t(D) * gridDim.y);
+        // C8 is a multiple of TPG, so whole groups are in or out of range
+        // together and every lane takes part in the shuffles
+        float2 p[4] = {bf16_pair(buf[0].x), bf16_pair(buf[0].y), bf16_pair(buf[0].z), bf16_pair(buf[0].w)};
+        const float2 s2 = __fadd2_rn(__fadd2_rn(p[0], p[1]), __fadd2_rn(p[2], p[3]));
+        const float mean = group_sum<TPG>(s2.x + s2.y) * invM;
+        const float2 nm = make_float2(-mean, -mean);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            p[j] = __fadd2_rn(p[j], nm);
+        float2 q2 = __fmul2_rn(p[0], p[0]);
+#pragma unroll
+        for (int j = 1; j < 4; ++j)
+            q2 = __ffma2_rn(p[j], p[j], q2);
+        const float m2 = group_sum<TPG>(q2.x + q2.y);
+        const float rstd = rsqrtf(fmaf(m2, invM, eps));
+        if (in) {
+            const float2 r2 = make_float2(rstd, rstd);
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float2 t = __ffma2_rn(__fmul2_rn(p[j], r2), g[j], b[j]);
+                const float2 w = __fmul2_rn(t, slope2);
+                t = steep ? make_float2(fminf(t.x, w.x), fminf(t.y, w.y))
+                          : make_float2(fmaxf(t.x, w.x), fmaxf(t.y, w.y));
+                o[j] = pack_bf16x2(t.x, t.y);
+            }
+            st16_stream(y + (n * C8 + c) * 8, make_uint4(o[0], o[1], o[2], o[3]), pol_stream);
+        }
+    }
+}
+
+template <int TPG>
+cudaError_t launch_vec8(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
+                        int64_t M, float eps, float slope, int sm_count, cudaStream_t stream)
+{
+    const int C8 = static_cast<int>(C / 8);
+    const int gx = (C8 + GN_THREADS - 1) / GN_THREADS;
+    int64_t gy = (static_cast<int64_t>(sm_count) * GN8_CTAS_PER_SM + gx - 1) / gx;
+    if (gy > N)
+        gy = N;
+    if (gy > 65535)
+        gy = 65535;
+    if (gy < 1)
+        gy = 1;
+    dim3 grid(gx, static_cast<unsigned>(gy));
+    return launch_pdl(gn_vec8_bf16_kernel<TPG>, grid, dim3(GN_THREADS), 0, stream,
+                      static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(gamma),
+                      static_cast<const __nv_bfloat16 *>(beta), static_cast<__nv_bfloat16 *>(y), N, C8,
+                      1.0f / static_cast<float>(M), eps, slope);
+}
+
+
 template <typename T, int TPG, int U>
 cudaError_t launch_vec(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
                        int64_t M, float eps, float slope, int sm_count, cudaStream_t stream)
@@ -195,6 +340,18 @@ cudaError_t gn_vec4_launch_t(const void *x, const void *gamma, const void *beta,
 cudaError_t gn_vec4_launch(const void *x, const void *gamma, const void *beta, void *y, int64_t N, int64_t C,
                            int64_t M, float eps, float slope, bool bf16, int sm_count, cudaStream_t stream)
 {
+    const bool a16 = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
+                       reinterpret_cast<uintptr_t>(gamma) | reinterpret_cast<uintptr_t>(beta)) & 15) == 0;
+    if (bf16 && a16) {
+        switch (M) {
+        case 8: return launch_vec8<1>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+        case 16: return launch_vec8<2>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+        case 32: return launch_vec8<4>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+        case 64: return launch_vec8<8>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+        case 128: return launch_vec8<16>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
+        default: break; // groups of 4 channels: the 4-channel form
+        }
+    }
     return bf16 ? gn_vec4_launch_t<__nv_bfloat16>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream)
                 : gn_vec4_launch_t<float>(x, gamma, beta, y, N, C, M, eps, slope, sm_count, stream);
 }

@@ -190,6 +190,47 @@ def test_group_norm_bf16(ng, N, C, G):
     assert yb.guards_intact()
 
 
+@pytest.mark.parametrize("M,G,N", [(8, 325, 13), (16, 163, 13), (32, 81, 13), (64, 41, 13), (128, 21, 13),
+                                   (16, 64, 4099)])
+@pytest.mark.parametrize("offset", [0, 4])
+def test_group_norm_bf16_vector_forms(ng, M, G, N, offset):
+    """Power-of-two groups of 8-128 channels: 16-byte aligned tensors take the 8-channel form
+    (one 16-byte access a thread, four rows ahead), 8-byte aligned ones (offset 4) the
+    4-channel form.  The widths leave a ragged last column block; (4099, 1024) walks about
+    seven rows a CTA, past the rows in flight."""
+    C = M * G
+    x = bf16_inputs(N * C, seed=M + G + offset)
+    g = bf16_inputs(C, 1.0, 0.1, seed=M + G + offset, tensor_id=1)
+    b = bf16_inputs(C, 0.0, 0.1, seed=M + G + offset, tensor_id=2)
+    want = oracle.group_lrelu_x2(x, g, b, N, C, G, f64=True)
+    xb, gb, bb = BGuarded(N * C, x, offset), BGuarded(C, g, offset), BGuarded(C, b, offset)
+    yb = BGuarded(N * C, offset=offset)
+    ng.norm_group_lrelu_x2_fwd_bf16(xb.t, gb.t, bb.t, yb.t, N, C, G, 1e-5, 0.01)
+    assert ng.norm_last_error() == 0
+    assert_bf16_parity(yb.values(), want, f"GN bf16 ({N},{C})/{G} offset={offset}")
+    assert yb.guards_intact()
+
+
+@pytest.mark.parametrize("slope", [-0.5, 0.0, 1.0, 1.5])
+def test_group_norm_bf16_vector_slopes_no_affine_in_place(ng, slope):
+    N, C, G = 21, 16 * 96, 96
+    x = bf16_inputs(N * C, 3.0, 2.0, seed=31)
+    g = bf16_inputs(C, 1.0, 0.1, seed=31, tensor_id=1)
+    b = bf16_inputs(C, 0.0, 0.1, seed=31, tensor_id=2)
+    want = oracle.group_lrelu_x2(x, g, b, N, C, G, slope=slope, f64=True)
+    xb, gb, bb, yb = BGuarded(N * C, x), BGuarded(C, g), BGuarded(C, b), BGuarded(N * C)
+    ng.norm_group_lrelu_x2_fwd_bf16(xb.t, gb.t, bb.t, yb.t, N, C, G, 1e-5, slope)
+    assert ng.norm_last_error() == 0
+    assert_bf16_parity(yb.values(), want, f"GN bf16 slope={slope}")
+    # no affine, in place
+    want = oracle.group_lrelu_x2(x, None, None, N, C, G, slope=slope, f64=True)
+    xb = BGuarded(N * C, x)
+    ng.norm_group_lrelu_x2_fwd_bf16(xb.t, None, None, xb.t, N, C, G, 1e-5, slope)
+    assert ng.norm_last_error() == 0
+    assert_bf16_parity(xb.values(), want, f"GN bf16 no affine in place slope={slope}")
+    assert xb.guards_intact()
+
+
 def test_rms_bf16_misaligned(ng):
     # x and y 2-byte but not 4-byte aligned
     B, C, S = 2, 64, 1024
