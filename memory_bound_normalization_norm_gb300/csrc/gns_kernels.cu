@@ -46,6 +46,7 @@
 #include <mutex>
 
 #include "norm_internal.cuh"
+#include <type_traits>
 
 namespace normk {
 
@@ -386,11 +387,20 @@ struct Held<__nv_bfloat16> {
     uint2 raw;
     __device__ __forceinline__ void clear() { raw = make_uint2(0u, 0u); }
     __device__ __forceinline__ void load(const __nv_bfloat16 *p, float) { raw = *reinterpret_cast<const uint2 *>(p); }
+    // the two values of a packed word, widened; volatile so that each pass
+    // widens again from the packed registers rather than keeping the
+    // widened values of a whole slice live between passes
+    static __device__ __forceinline__ float2 widen(uint32_t w)
+    {
+        uint32_t lo, hi;
+        asm volatile("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;" : "=r"(lo), "=r"(hi) : "r"(w));
+        return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+    }
     // x + off (off = -K for d)
     __device__ __forceinline__ void pair(float2 off, bool, float2 &l, float2 &h) const
     {
-        l = __fadd2_rn(make_float2(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u)), off);
-        h = __fadd2_rn(make_float2(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)), off);
+        l = __fadd2_rn(widen(raw.x), off);
+        h = __fadd2_rn(widen(raw.y), off);
     }
 };
 
@@ -510,148 +520,159 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
             }
         }
         const T *sb = db ? buf1 : buf0;
-        Held<T> v[V];
-        float K = 0.f;
+        // FAST: this CTA's slice fills every thread's V vectors, and (for
+        // one channel a vector) a step of 4 * NT elements crosses at most one
+        // channel boundary; then no vector needs a range check
+        auto seg = [&](auto fast_c) {
+            constexpr bool FAST = decltype(fast_c)::value;
+            Held<T> v[V];
+            float K = 0.f;
 #pragma unroll
-        for (int j = 0; j < V; ++j)
-            v[j].clear();
-        if (!stopped) {
-            K = first_elem<T>(piv[db]);
+            for (int j = 0; j < V; ++j)
+                v[j].clear();
+            if (!stopped) {
+                K = first_elem<T>(piv[db]);
+                const T *st = sb + 4 * tid;
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    if (FAST || tid + j * NT < n4)
+                        v[j].load(st + 4 * NT * j, K);
+                }
+            }
+            // exact two-pass statistics of this CTA's slice about the pivot, in
+            // f32x2 pairs
+            constexpr bool bf = sizeof(T) == 2;
+            const float2 negk = make_float2(-K, -K); // bf16: d = x - K as it is widened
+            float2 sl = make_float2(0.f, 0.f), sh = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                if (FAST || tid + j * NT < n4) {
+                    float2 l, h;
+                    v[j].pair(negk, false, l, h);
+                    sl = __fadd2_rn(sl, l);
+                    sh = __fadd2_rn(sh, h);
+                }
+            }
+            float s = (sl.x + sl.y) + (sh.x + sh.y);
+            s = block_sum<NT>(s, red[0]);
+            // every thread has its values in registers: refill this buffer with
+            // the segment GNS_NBUF ahead
+            if (tid == 0 && !stopped && issued < nk && issued == k + GNS_NBUF) {
+                fence_proxy_async_smem();
+                issue(issued);
+                ++issued;
+            }
+            const float mloc = n4 ? s / nloc : 0.f;
+            // deviations from the slice mean: d - mloc (fp32), or x - (K + mloc)
+            // with the centre rounded once (bf16; its offset from the exact
+            // centre adds at most n * ulp(K)^2 / 4 to M2)
+            const float2 nc = bf ? make_float2(-(K + mloc), -(K + mloc)) : make_float2(-mloc, -mloc);
+            float2 ql = make_float2(0.f, 0.f), qh = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                if (FAST || tid + j * NT < n4) {
+                    float2 l, h;
+                    v[j].pair(nc, true, l, h);
+                    ql = __ffma2_rn(l, l, ql);
+                    qh = __ffma2_rn(h, h, qh);
+                }
+            }
+            float q = (ql.x + ql.y) + (qh.x + qh.y);
+            q = block_sum<NT>(q, red[1]);
+            Moments tot;
+            tot.n = nloc;
+            tot.mean = mloc;
+            tot.m2 = q;
+            if (clustered) {
+                // a stopped CTA's partial is flagged, so no CTA uses it
+                float f = 0.f;
+                bool to = false;
+                tot = cluster_moments(mloc, q, stopped ? 1.f : 0.f, xslot[b], &xbar[b], CL, rank, par, xwait_ns,
+                                      count_of, &f, &to);
+                if (f != 0.f || to)
+                    stopped = true;
+            }
+            if (stopped)
+                return; // keep exchanging, write nothing
+            // ACT: y = 2 * LReLU((x - mean) * rstd * gamma + beta), with x - mean
+            // = d - tot.mean; LReLU is positively homogeneous, so the factor 2
+            // goes into the affine map: 2t = d * a + c, a = 2 * rstd * gamma,
+            // c = 2 * beta - tot.mean * a.  Without ACT (LayerNorm): y = d * a + c
+            // with a = rstd * gamma, c = beta - tot.mean * a.  Pairs in f32x2.
+            const float rstd = rsqrtf(fmaxf(tot.m2 / tot.n, 0.f) + p.eps);
+            const float mean_d = tot.mean;
+            const float2 slope2 = make_float2(p.slope, p.slope);
+            const bool steep = p.slope > 1.f;
+            constexpr float sc = ACT ? 2.f : 1.f;
+            const float sr = sc * rstd;
+            const int64_t r = cid + k * ncl;
+            const int64_t cbase = (r % p.G) * p.M;
+            T *yr = y + r * p.seg_len;
+            T *yt = yr + 4 * (lo + tid); // this thread's vector 0
+            uint32_t cj = c0, rj = r0;  // channel of vector j within the segment, and the remainder
+            uint32_t cur = 0xffffffffu; // the channel a2 / c2 belong to
+            float2 a2 = make_float2(0.f, 0.f), c2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int i = tid + j * NT;
-                if (i < n4)
-                    v[j].load(sb + 4 * i, K);
-            }
-        }
-        // exact two-pass statistics of this CTA's slice about the pivot, in
-        // f32x2 pairs
-        constexpr bool bf = sizeof(T) == 2;
-        const float2 negk = make_float2(-K, -K); // bf16: d = x - K as it is widened
-        float2 sl = make_float2(0.f, 0.f), sh = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-            if (tid + j * NT < n4) {
-                float2 l, h;
-                v[j].pair(negk, false, l, h);
-                sl = __fadd2_rn(sl, l);
-                sh = __fadd2_rn(sh, h);
-            }
-        }
-        float s = (sl.x + sl.y) + (sh.x + sh.y);
-        s = block_sum<NT>(s, red[0]);
-        // every thread has its values in registers: refill this buffer with
-        // the segment GNS_NBUF ahead
-        if (tid == 0 && !stopped && issued < nk && issued == k + GNS_NBUF) {
-            fence_proxy_async_smem();
-            issue(issued);
-            ++issued;
-        }
-        const float mloc = n4 ? s / nloc : 0.f;
-        // deviations from the slice mean: d - mloc (fp32), or x - (K + mloc)
-        // with the centre rounded once (bf16; its offset from the exact
-        // centre adds at most n * ulp(K)^2 / 4 to M2)
-        const float2 nc = bf ? make_float2(-(K + mloc), -(K + mloc)) : make_float2(-mloc, -mloc);
-        float2 ql = make_float2(0.f, 0.f), qh = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-            if (tid + j * NT < n4) {
-                float2 l, h;
-                v[j].pair(nc, true, l, h);
-                ql = __ffma2_rn(l, l, ql);
-                qh = __ffma2_rn(h, h, qh);
-            }
-        }
-        float q = (ql.x + ql.y) + (qh.x + qh.y);
-        q = block_sum<NT>(q, red[1]);
-        Moments tot;
-        tot.n = nloc;
-        tot.mean = mloc;
-        tot.m2 = q;
-        if (clustered) {
-            // a stopped CTA's partial is flagged, so no CTA uses it
-            float f = 0.f;
-            bool to = false;
-            tot = cluster_moments(mloc, q, stopped ? 1.f : 0.f, xslot[b], &xbar[b], CL, rank, par, xwait_ns,
-                                  count_of, &f, &to);
-            if (f != 0.f || to)
-                stopped = true;
-        }
-        if (stopped)
-            continue; // keep exchanging, write nothing
-        // ACT: y = 2 * LReLU((x - mean) * rstd * gamma + beta), with x - mean
-        // = d - tot.mean; LReLU is positively homogeneous, so the factor 2
-        // goes into the affine map: 2t = d * a + c, a = 2 * rstd * gamma,
-        // c = 2 * beta - tot.mean * a.  Without ACT (LayerNorm): y = d * a + c
-        // with a = rstd * gamma, c = beta - tot.mean * a.  Pairs in f32x2.
-        const float rstd = rsqrtf(fmaxf(tot.m2 / tot.n, 0.f) + p.eps);
-        const float mean_d = tot.mean;
-        const float2 slope2 = make_float2(p.slope, p.slope);
-        const bool steep = p.slope > 1.f;
-        constexpr float sc = ACT ? 2.f : 1.f;
-        const float sr = sc * rstd;
-        const int64_t r = cid + k * ncl;
-        const int64_t cbase = (r % p.G) * p.M;
-        T *yr = y + r * p.seg_len;
-        uint32_t cj = c0, rj = r0;  // channel of vector j within the segment, and the remainder
-        uint32_t cur = 0xffffffffu; // the channel a2 / c2 belong to
-        float2 a2 = make_float2(0.f, 0.f), c2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-            const int i = tid + j * NT;
-            if (i < n4) {
-                const int64_t e = 4 * (lo + i);
-                float2 l, h;
-                v[j].pair(negk, false, l, h);
-                if constexpr (MODE == AFF_CHAN) {
-                    if (cj != cur) {
-                        // a new channel: its gamma/beta (each run of a
-                        // thread's vectors in one channel loads them once)
-                        cur = cj;
-                        const int64_t c = cbase + cj;
-                        const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
-                        const float a = sr * gv;
-                        a2 = make_float2(a, a);
-                        const float cc = fmaf(-mean_d, a, sc * bv);
-                        c2 = make_float2(cc, cc);
+                if (FAST || i < n4) {
+                    const int64_t e = 4 * (lo + i);
+                    float2 l, h;
+                    v[j].pair(negk, false, l, h);
+                    if constexpr (MODE == AFF_CHAN) {
+                        if (cj != cur) {
+                            // a new channel: its gamma/beta (each run of a
+                            // thread's vectors in one channel loads them once)
+                            cur = cj;
+                            const int64_t c = cbase + cj;
+                            const float gv = gm ? Io<T>::ld1(gm + c) : 1.f, bv = bt ? Io<T>::ld1(bt + c) : 0.f;
+                            const float a = sr * gv;
+                            a2 = make_float2(a, a);
+                            const float cc = fmaf(-mean_d, a, sc * bv);
+                            c2 = make_float2(cc, cc);
+                        }
+                        l = __ffma2_rn(l, a2, c2);
+                        h = __ffma2_rn(h, a2, c2);
+                    } else {
+                        float4 g, bb;
+                        seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb, p.cache_gb != 0);
+                        const float2 sr2 = make_float2(sr, sr), nm = make_float2(-mean_d, -mean_d);
+                        const float2 al = __fmul2_rn(make_float2(g.x, g.y), sr2);
+                        const float2 ah = __fmul2_rn(make_float2(g.z, g.w), sr2);
+                        float2 bl = make_float2(bb.x, bb.y), bh = make_float2(bb.z, bb.w);
+                        if constexpr (ACT) {
+                            bl = __fadd2_rn(bl, bl);
+                            bh = __fadd2_rn(bh, bh);
+                        }
+                        l = __ffma2_rn(l, al, __ffma2_rn(nm, al, bl));
+                        h = __ffma2_rn(h, ah, __ffma2_rn(nm, ah, bh));
                     }
-                    l = __ffma2_rn(l, a2, c2);
-                    h = __ffma2_rn(h, a2, c2);
-                } else {
-                    float4 g, bb;
-                    seg_affine4<T, MODE>(gm, bt, cbase, e, p.S, narrow, pol_keep, g, bb, p.cache_gb != 0);
-                    const float2 sr2 = make_float2(sr, sr), nm = make_float2(-mean_d, -mean_d);
-                    const float2 al = __fmul2_rn(make_float2(g.x, g.y), sr2);
-                    const float2 ah = __fmul2_rn(make_float2(g.z, g.w), sr2);
-                    float2 bl = make_float2(bb.x, bb.y), bh = make_float2(bb.z, bb.w);
                     if constexpr (ACT) {
-                        bl = __fadd2_rn(bl, bl);
-                        bh = __fadd2_rn(bh, bh);
+                        l = lrelu2(l, slope2, steep);
+                        h = lrelu2(h, slope2, steep);
                     }
-                    l = __ffma2_rn(l, al, __ffma2_rn(nm, al, bl));
-                    h = __ffma2_rn(h, ah, __ffma2_rn(nm, ah, bh));
+                    Io<T>::st4_stream(yt + 4 * NT * j, make_float4(l.x, l.y, h.x, h.y), pol_stream);
                 }
-                if constexpr (ACT) {
-                    l = lrelu2(l, slope2, steep);
-                    h = lrelu2(h, slope2, steep);
-                }
-                Io<T>::st4_stream(yr + e, make_float4(l.x, l.y, h.x, h.y), pol_stream);
-            }
-            if constexpr (MODE == AFF_CHAN) {
-                // S % 4 == 0: a step of 4 * NT elements crosses at most one
-                // channel boundary when S >= 4 * NT; otherwise divide
-                if (S32 >= 4u * NT) {
-                    rj += 4u * NT;
-                    if (rj >= S32) {
-                        rj -= S32;
-                        ++cj;
+                if constexpr (MODE == AFF_CHAN) {
+                    // S % 4 == 0: a step of 4 * NT elements crosses at most one
+                    // channel boundary when S >= 4 * NT; otherwise divide
+                    if (FAST || S32 >= 4u * NT) {
+                        rj += 4u * NT;
+                        if (rj >= S32) {
+                            rj -= S32;
+                            ++cj;
+                        }
+                    } else {
+                        const uint32_t ej = e0 + 4u * NT * static_cast<uint32_t>(j + 1);
+                        cj = ej / S32;
                     }
-                } else {
-                    const uint32_t ej = e0 + 4u * NT * static_cast<uint32_t>(j + 1);
-                    cj = ej / S32;
                 }
             }
-        }
+        };
+        if (n4 == NT * V && (MODE != AFF_CHAN || S32 >= 4u * NT))
+            seg(std::true_type{});
+        else
+            seg(std::false_type{});
     }
     if (stopped && tid == 0) {
         if (gave_up)
