@@ -358,8 +358,8 @@ __device__ __forceinline__ float first_elem(const float4 &raw)
 // A thread's copy of one 4-element vector of its slice, read as two float2
 // pairs for the packed (f32x2) arithmetic.  fp32: d = x - K.  bf16: the
 // packed values as loaded (two registers, so a CTA holds twice as many
-// vectors), widened (a shift or a mask a pair) and shifted by `off` where
-// used; for fp32 `off` is added to d.
+// vectors), widened and shifted by `off` in one mixed-precision add a value
+// where used; for fp32 `off` is added to d.
 template <typename T>
 struct Held;
 
@@ -387,20 +387,11 @@ struct Held<__nv_bfloat16> {
     uint2 raw;
     __device__ __forceinline__ void clear() { raw = make_uint2(0u, 0u); }
     __device__ __forceinline__ void load(const __nv_bfloat16 *p, float) { raw = *reinterpret_cast<const uint2 *>(p); }
-    // the two values of a packed word, widened; volatile so that each pass
-    // widens again from the packed registers rather than keeping the
-    // widened values of a whole slice live between passes
-    static __device__ __forceinline__ float2 widen(uint32_t w)
-    {
-        uint32_t lo, hi;
-        asm volatile("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;" : "=r"(lo), "=r"(hi) : "r"(w));
-        return make_float2(__uint_as_float(lo), __uint_as_float(hi));
-    }
-    // x + off (off = -K for d)
+    // x + off (off = -K for d), widened again in each pass
     __device__ __forceinline__ void pair(float2 off, bool, float2 &l, float2 &h) const
     {
-        l = __fadd2_rn(widen(raw.x), off);
-        h = __fadd2_rn(widen(raw.y), off);
+        l = bf16x2_add(raw.x, off);
+        h = bf16x2_add(raw.y, off);
     }
 };
 

@@ -271,8 +271,8 @@ __device__ __forceinline__ float row_pivot(const float4 *piece, int64_t row_len)
 
 // Shifted sums of d = x - K over units i = pi, pi + np, ... < nu of a row
 // slice in shared memory, with four independent accumulator pairs, as this
-// thread's (count, mean, M2).  bf16 units (8 values) are widened a 32-bit
-// word at a time and summed in f32x2 pairs.
+// thread's (count, mean, M2).  bf16 units (8 values) are shifted by -K a
+// 32-bit word at a time (mixed-precision adds) and summed in f32x2 pairs.
 template <typename T>
 __device__ __forceinline__ Moments slice_moments(const float4 *buf, int nu, int pi, int np, float K)
 {
@@ -300,8 +300,8 @@ __device__ __forceinline__ Moments slice_moments(const float4 *buf, int nu, int 
         float2 p1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         float2 p2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         auto add_unit = [&](const float4 &v, int a) {
-            const float2 d0 = __fadd2_rn(bf16_pair(v.x), negk), d1 = __fadd2_rn(bf16_pair(v.y), negk);
-            const float2 d2 = __fadd2_rn(bf16_pair(v.z), negk), d3 = __fadd2_rn(bf16_pair(v.w), negk);
+            const float2 d0 = bf16x2_add(__float_as_uint(v.x), negk), d1 = bf16x2_add(__float_as_uint(v.y), negk);
+            const float2 d2 = bf16x2_add(__float_as_uint(v.z), negk), d3 = bf16x2_add(__float_as_uint(v.w), negk);
             p1[a] = __fadd2_rn(p1[a], __fadd2_rn(__fadd2_rn(d0, d1), __fadd2_rn(d2, d3)));
             p2[a] = __ffma2_rn(d3, d3, __ffma2_rn(d2, d2, __ffma2_rn(d1, d1, __ffma2_rn(d0, d0, p2[a]))));
         };
@@ -341,7 +341,7 @@ __device__ __forceinline__ float4 ln_unit(const float4 &v, const RowMean &rm, co
         const float2 nh = make_float2(-rm.hi, -rm.hi), nl = make_float2(-rm.lo, -rm.lo);
         const float2 r2 = make_float2(rm.rstd, rm.rstd);
         auto word = [&](float xv, float gv, float bv) {
-            const float2 t = __fmul2_rn(__fadd2_rn(__fadd2_rn(bf16_pair(xv), nh), nl), r2);
+            const float2 t = __fmul2_rn(__fadd2_rn(bf16x2_add(__float_as_uint(xv), nh), nl), r2);
             const float2 o = __ffma2_rn(t, bf16_pair(gv), bf16_pair(bv));
             return __uint_as_float(pack_bf16x2(o.x, o.y));
         };
@@ -383,7 +383,7 @@ __device__ __forceinline__ float4 gn_unit(const float4 &v, const RowMean &rm, fl
         const float2 s2 = make_float2(slope, slope);
         const bool steep = slope > 1.f;
         auto word = [&](float xv) {
-            const float2 t = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(bf16_pair(xv), nh), nl), r2), gg, bb);
+            const float2 t = __ffma2_rn(__fmul2_rn(__fadd2_rn(bf16x2_add(__float_as_uint(xv), nh), nl), r2), gg, bb);
             // LReLU: max(t, slope t) for slope <= 1, min(t, slope t) above
             const float2 u = __fmul2_rn(t, s2);
             const float lo = steep ? fminf(t.x, u.x) : fmaxf(t.x, u.x);
@@ -912,6 +912,9 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
         // pairs plus off (fp32, already d = x - K)
         auto pair = [&](int k, float2 off, float2 &l, float2 &h) {
             if constexpr (RAW) {
+                // a shift and a mask a pair: measured faster here than the
+                // mixed-precision adds of the other kernels (47.5 against
+                // 50.2 us at (16384, 4096))
                 l = __fadd2_rn(make_float2(__uint_as_float(raw[k].x << 16), __uint_as_float(raw[k].x & 0xffff0000u)),
                                off);
                 h = __fadd2_rn(make_float2(__uint_as_float(raw[k].y << 16), __uint_as_float(raw[k].y & 0xffff0000u)),

@@ -341,6 +341,22 @@ struct Io<float> {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
+// x + o for the two bf16 values x of a packed 32-bit word (low half first):
+// mixed-precision adds (sm_100 and later), which widen the bf16 operand
+// exactly and round the sum once, so the result is that of widening and
+// then adding in fp32, in one instruction a value.  volatile: each use
+// widens again from the packed word, so a pass over a slice does not keep the
+// widened values live for a later pass.
+__device__ __forceinline__ float2 bf16x2_add(uint32_t w, float2 o)
+{
+    float a, b;
+    asm volatile("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2;\n\t"
+                 "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4; }"
+                 : "=f"(a), "=f"(b)
+                 : "r"(w), "f"(o.x), "f"(o.y));
+    return make_float2(a, b);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
