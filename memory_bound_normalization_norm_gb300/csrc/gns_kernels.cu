@@ -454,15 +454,26 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
     const T *bt = static_cast<const T *>(p.beta);
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
-    const int64_t nk = cid < p.rows ? (p.rows - cid + ncl - 1) / ncl : 0;
+    // segments of this cluster (32-bit division when the counts fit)
+    int64_t nk = 0;
+    if (cid < p.rows) {
+        const int64_t num = p.rows - cid + ncl - 1;
+        nk = num <= 0xffffffffll ? static_cast<int64_t>(static_cast<uint32_t>(num) / static_cast<uint32_t>(ncl))
+                                 : num / ncl;
+    }
+    // group of segment cid + k * ncl, stepped by ncl mod G per segment
+    int64_t gcur = cid % p.G;
+    const int64_t gstep = ncl % p.G;
     const uint64_t xwait_ns = p.timeout_ns > 100000000ull ? p.timeout_ns : 100000000ull;
     // With one channel per vector, the channel of this thread's vector j
     // within a segment is the same for every segment: c0 and r0 are those of
     // vector 0 (quotient and remainder of its first element by S); vector
-    // j + 1 starts 4 * NT elements further on.
+    // j + 1 starts 4 * NT elements further on, qstep channels and rstep
+    // elements on.
     const uint32_t S32 = static_cast<uint32_t>(p.S);
     const uint32_t e0 = static_cast<uint32_t>(4 * (lo + tid));
     const uint32_t c0 = MODE == AFF_CHAN ? e0 / S32 : 0u, r0 = MODE == AFF_CHAN ? e0 % S32 : 0u;
+    const uint32_t qstep = MODE == AFF_CHAN ? (4u * NT) / S32 : 0u, rstep = MODE == AFF_CHAN ? (4u * NT) % S32 : 0u;
 
     if (tid == 0) {
         mbar_init(&full[0], 1);
@@ -597,7 +608,7 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
             constexpr float sc = ACT ? 2.f : 1.f;
             const float sr = sc * rstd;
             const int64_t r = cid + k * ncl;
-            const int64_t cbase = (r % p.G) * p.M;
+            const int64_t cbase = gcur * p.M;
             T *yr = y + r * p.seg_len;
             T *yt = yr + 4 * (lo + tid); // this thread's vector 0
             uint32_t cj = c0, rj = r0;  // channel of vector j within the segment, and the remainder
@@ -645,17 +656,18 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
                     Io<T>::st4_stream(yt + 4 * NT * j, make_float4(l.x, l.y, h.x, h.y), pol_stream);
                 }
                 if constexpr (MODE == AFF_CHAN) {
-                    // S % 4 == 0: a step of 4 * NT elements crosses at most one
-                    // channel boundary when S >= 4 * NT; otherwise divide
-                    if (FAST || S32 >= 4u * NT) {
+                    // S % 4 == 0: a step of 4 * NT elements is qstep whole
+                    // channels (none when S >= 4 * NT) and rstep elements,
+                    // which cross at most one more channel boundary
+                    if (FAST) {
                         rj += 4u * NT;
-                        if (rj >= S32) {
-                            rj -= S32;
-                            ++cj;
-                        }
                     } else {
-                        const uint32_t ej = e0 + 4u * NT * static_cast<uint32_t>(j + 1);
-                        cj = ej / S32;
+                        rj += rstep;
+                        cj += qstep;
+                    }
+                    if (rj >= S32) {
+                        rj -= S32;
+                        ++cj;
                     }
                 }
             }
@@ -664,6 +676,9 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
             seg(std::true_type{});
         else
             seg(std::false_type{});
+        gcur += gstep;
+        if (gcur >= p.G)
+            gcur -= p.G;
     }
     if (stopped && tid == 0) {
         if (gave_up)
