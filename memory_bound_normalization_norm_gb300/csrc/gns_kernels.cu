@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
     const int64_t cid = clustered ? cluster_id_x() : blockIdx.x;
     const int64_t ncl = clustered ? cluster_count_x() : gridDim.x;
     const int64_t L4 = p.seg_len >> 2;
-    const int64_t per = (L4 + CL - 1) / CL;
+    const int64_t per = small_ceil_div(L4, CL);
     const int64_t lo = per * rank;
     const int64_t n4 = lo < L4 ? (L4 - lo < per ? L4 - lo : per) : 0;
     const float Lf = static_cast<float>(p.seg_len);
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
         if (clustered)
             q = cluster_sum(q, &xch[1], CL);
         rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
-        const int64_t cbase = (r % p.G) * p.M;
+        const int64_t cbase = small_mod(r, p.G) * p.M;
         T *yr = y + r * p.seg_len;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
@@ -462,8 +462,8 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
                                  : num / ncl;
     }
     // group of segment cid + k * ncl, stepped by ncl mod G per segment
-    int64_t gcur = cid % p.G;
-    const int64_t gstep = ncl % p.G;
+    int64_t gcur = small_mod(cid, p.G);
+    const int64_t gstep = small_mod(ncl, p.G);
     const uint64_t xwait_ns = p.timeout_ns > 100000000ull ? p.timeout_ns : 100000000ull;
     // With one channel per vector, the channel of this thread's vector j
     // within a segment is the same for every segment: c0 and r0 are those of
@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(GS_T) gns_split_apply_kernel(GnSegParams p)
         }
         __syncthreads();
         const RowMean rm = row_mean;
-        const int64_t cbase = (r % p.G) * p.M;
+        const int64_t cbase = small_mod(r, p.G) * p.M;
         const int64_t lo = static_cast<int64_t>(pc) * p.chunk;
         const int64_t hi = (lo + p.chunk < p.seg_len) ? lo + p.chunk : p.seg_len;
         if (VEC) {
@@ -1016,7 +1016,7 @@ __global__ void __launch_bounds__(256) gns_warp_kernel(GnSegParams p)
         for (int o = 16; o > 0; o >>= 1)
             q += __shfl_xor_sync(0xffffffffu, q, o);
         rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
-        const int64_t cbase = (r % p.G) * p.M;
+        const int64_t cbase = small_mod(r, p.G) * p.M;
         // every lane has read the whole segment (the shuffles above are
         // warp-wide), so with y == x the stores below are safe
         for (int64_t j = lane; j < p.seg_len; j += 32) {

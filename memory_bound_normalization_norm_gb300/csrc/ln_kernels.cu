@@ -723,7 +723,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
                 // e_k / S within the group, tracked incrementally.
                 const RowMean rm = row_mean[r & 1];
                 const int64_t gr = grow(r);
-                const int64_t cbase = (gr % gp_.G) * gp_.M;
+                const int64_t cbase = small_mod(gr, gp_.G) * gp_.M;
                 float4 *yr = y4 + gr * Lu + f0;
                 constexpr uint32_t step = static_cast<uint32_t>(UE) * LN_A;
                 const uint32_t S = gp_.S, e0 = static_cast<uint32_t>(UE) * static_cast<uint32_t>(f0 + at);

@@ -339,6 +339,19 @@ struct Io<float> {
     static __device__ __forceinline__ void st1_stream(float *p, float v, uint64_t pol) { st_stream_f1(p, v, pol); }
 };
 
+// a % b and ceil(a / b) for non-negative a and positive b, in 32-bit
+// arithmetic when both fit (64-bit division is a long software routine)
+__device__ __forceinline__ int64_t small_mod(int64_t a, int64_t b)
+{
+    return (a | b) <= 0xffffffffll ? static_cast<int64_t>(static_cast<uint32_t>(a) % static_cast<uint32_t>(b)) : a % b;
+}
+
+__device__ __forceinline__ int64_t small_ceil_div(int64_t a, int64_t b)
+{
+    const int64_t n = a + b - 1;
+    return (n | b) <= 0xffffffffll ? static_cast<int64_t>(static_cast<uint32_t>(n) / static_cast<uint32_t>(b)) : n / b;
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
 // x + o for the two bf16 values x of a packed 32-bit word (low half first):
