@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
     const int64_t lo = per * rank;
     const int64_t n4 = lo < L4 ? (L4 - lo < per ? L4 - lo : per) : 0;
     const float Lf = static_cast<float>(p.seg_len);
+    const float invL = 1.f / Lf; // the means below are products, not divisions
     constexpr bool narrow = true; // segments here are at most 16 * NT * V * 4 elements
     const T *x = static_cast<const T *>(p.x);
     T *y = static_cast<T *>(p.y);
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
             s = cluster_sum(s, &xch[0], CL);
         Moments tot;
         tot.n = Lf;
-        tot.mean = s / Lf;
+        tot.mean = s * invL;
         tot.m2 = 0.f;
         RowMean rm = finish_row(K, tot, p.eps);
         float q = 0.f;
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
         q = block_sum<NT>(q, red[1]);
         if (clustered)
             q = cluster_sum(q, &xch[1], CL);
-        rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        rm.rstd = rsqrtf(fmaxf(q * invL, 0.f) + p.eps);
         const int64_t cbase = small_mod(r, p.G) * p.M;
         T *yr = y + r * p.seg_len;
 #pragma unroll
@@ -820,7 +821,8 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
     const int64_t teams_per_cta = blockDim.x >> tlog;
     const int64_t nteams = static_cast<int64_t>(gridDim.x) * teams_per_cta;
     const int items = static_cast<int>(p.seg_len / E);
-    const float Lf = static_cast<float>(p.seg_len);
+    // 1 / L once: the means below are products, not divisions
+    const float invL = 1.f / static_cast<float>(p.seg_len);
     // which of this lane's item slots hold an item: the same in every segment
     bool in[WMAX];
 #pragma unroll
@@ -846,24 +848,28 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
     // right behind the prefetch: measured slower, so bf16 loads in turn.
     constexpr bool PF = sizeof(T) == 4;
     float4 nx[PF ? WMAX : 1];
-    auto load_seg = [&](int64_t rr, float4 *dst) {
-        const T *xr = x + rr * p.seg_len;
+    // this lane's first item of segment r, in x and in y, stepped by
+    // nteams segments a loop
+    const int64_t seg_step = nteams * p.seg_len;
+    const T *xl = x + r * p.seg_len + E * j;
+    T *yl = y + r * p.seg_len + E * j;
+    auto load_seg = [&](int64_t rr, const T *src, float4 *dst) {
 #pragma unroll
         for (int w = 0; w < WMAX; ++w)
-            dst[w] = (in[w] && rr < p.rows) ? team_load<T, E>(xr + E * (j + w * Tn), pol_stream)
+            dst[w] = (in[w] && rr < p.rows) ? team_load<T, E>(src + E * w * Tn, pol_stream)
                                             : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     if constexpr (PF)
-        load_seg(r, nx);
-    for (; r < p.rows; r += nteams) {
+        load_seg(r, xl, nx);
+    for (; r < p.rows; r += nteams, xl += seg_step, yl += seg_step) {
         float4 v[WMAX];
         if constexpr (PF) {
 #pragma unroll
             for (int w = 0; w < WMAX; ++w)
                 v[w] = nx[w];
-            load_seg(r + nteams, nx);
+            load_seg(r + nteams, xl + seg_step, nx);
         } else {
-            load_seg(r, v);
+            load_seg(r, xl, v);
         }
         // the segment's first element, from the team's first lane; every
         // lane reads it before any lane of the team stores (the shuffles
@@ -901,7 +907,7 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
         }
         for (int o = Tn >> 1; o > 0; o >>= 1)
             s += __shfl_xor_sync(tmask, s, o);
-        const float mean_d = s / Lf;
+        const float mean_d = s * invL;
         float q = 0.f;
         if constexpr (E == 4) {
             const float2 nm = make_float2(-mean_d, -mean_d);
@@ -931,9 +937,8 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
             q += __shfl_xor_sync(tmask, q, o);
         // 2 LeakyReLU(t) = LeakyReLU(2 t), and 2 t = d * sc + c with
         // sc = 2 rstd gamma, c = 2 beta - mean_d * sc: one FMA an element
-        const float rstd2 = 2.f * rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        const float rstd2 = 2.f * rsqrtf(fmaxf(q * invL, 0.f) + p.eps);
         const int64_t cbase = rg * p.M;
-        T *yr = y + r * p.seg_len;
 #pragma unroll
         for (int w = 0; w < WMAX; ++w) {
             if (!in[w])
@@ -949,7 +954,7 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
                 float2 th = __ffma2_rn(make_float2(v[w].z, v[w].w), ah, __ffma2_rn(nm, ah, __fadd2_rn(bh, bh)));
                 tl = lrelu2(tl, slope2, steep);
                 th = lrelu2(th, slope2, steep);
-                team_store<T, E>(yr + E * i, make_float4(tl.x, tl.y, th.x, th.y), pol_stream);
+                team_store<T, E>(yl + E * w * Tn, make_float4(tl.x, tl.y, th.x, th.y), pol_stream);
             } else {
                 float g[4], b[4];
 #pragma unroll
@@ -966,7 +971,7 @@ __global__ void __launch_bounds__(256) gns_team_kernel(GnSegParams p, int tlog, 
                     const float t = fmaf(comp<E>(v[w], k), sc, fmaf(-mean_d, sc, b[k] + b[k]));
                     o[k] = t > 0.f ? t : slope * t;
                 }
-                team_store<T, E>(yr + E * i, make_float4(o[0], o[1], o[2], o[3]), pol_stream);
+                team_store<T, E>(yl + E * w * Tn, make_float4(o[0], o[1], o[2], o[3]), pol_stream);
             }
         }
         rg += rg_step;
@@ -986,6 +991,7 @@ __global__ void __launch_bounds__(256) gns_warp_kernel(GnSegParams p)
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const bool narrow = p.seg_len <= int64_t(0xffffffff);
     const float Lf = static_cast<float>(p.seg_len);
+    const float invL = 1.f / Lf; // the means below are products, not divisions
     const T *x = static_cast<const T *>(p.x);
     T *y = static_cast<T *>(p.y);
     const T *gm = static_cast<const T *>(p.gamma);
@@ -1004,7 +1010,7 @@ __global__ void __launch_bounds__(256) gns_warp_kernel(GnSegParams p)
             s += __shfl_xor_sync(0xffffffffu, s, o);
         Moments tot;
         tot.n = Lf;
-        tot.mean = s / Lf;
+        tot.mean = s * invL;
         tot.m2 = 0.f;
         RowMean rm = finish_row(K, tot, p.eps);
         float q = 0.f;
@@ -1015,7 +1021,7 @@ __global__ void __launch_bounds__(256) gns_warp_kernel(GnSegParams p)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             q += __shfl_xor_sync(0xffffffffu, q, o);
-        rm.rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        rm.rstd = rsqrtf(fmaxf(q * invL, 0.f) + p.eps);
         const int64_t cbase = small_mod(r, p.G) * p.M;
         // every lane has read the whole segment (the shuffles above are
         // warp-wide), so with y == x the stores below are safe

@@ -862,7 +862,7 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
     __shared__ float red[2][NT / 32];
     const int tid = threadIdx.x;
     const int64_t L4 = p.row_len >> 2; // 4-element vectors per row
-    const float Lf = static_cast<float>(p.row_len);
+    const float invL = 1.f / static_cast<float>(p.row_len); // the means below are products, not divisions
     const T *x = static_cast<const T *>(p.x);
     T *y = static_cast<T *>(p.y);
     const T *gm = static_cast<const T *>(p.gamma);
@@ -945,7 +945,7 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
         }
         float s = (sl.x + sl.y) + (sh.x + sh.y);
         s = block_sum<NT>(s, red[0]);
-        const float mean_d = s / Lf;
+        const float mean_d = s * invL;
         const float2 nm = make_float2(-mean_d, -mean_d);
         // deviations from the mean: d - mean_d (fp32), or x - (K + mean_d)
         // with the centre rounded once (bf16; its offset from the exact
@@ -963,7 +963,7 @@ __global__ void __launch_bounds__(NT) ln_rows_kernel(LnParams p)
         }
         float q = (ql.x + ql.y) + (qh.x + qh.y);
         q = block_sum<NT>(q, red[1]);
-        const float rstd = rsqrtf(fmaxf(q / Lf, 0.f) + p.eps);
+        const float rstd = rsqrtf(fmaxf(q * invL, 0.f) + p.eps);
         const float2 r2 = make_float2(rstd, rstd);
         T *yr = y + r * p.row_len;
 #pragma unroll
