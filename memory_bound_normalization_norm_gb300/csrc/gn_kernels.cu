@@ -16,8 +16,8 @@
 //
 // bf16 groups of 8 or more channels with 16-byte aligned tensors take a
 // wider form: a thread owns 8 channels (one 16-byte load, four registers
-// held packed) and keeps four rows of loads in flight, so an SM has as many
-// bytes of x in flight as in fp32 at half the bytes per element.
+// held packed) and keeps three rows of loads in flight, so an SM has about
+// as many bytes of x in flight as in fp32 at half the bytes per element.
 #include "norm_internal.cuh"
 
 namespace normk {
@@ -156,12 +156,15 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
 // M channels is TPG = M/8 adjacent lanes, and a warp covers 256 contiguous
 // elements (512 bytes).  Each row's x is held as loaded (four registers) from
 // its load, GN8_AHEAD rows ahead of the row being reduced, until its turn.
-constexpr int GN8_AHEAD = 4;
-// One resident wave: about 53 registers a thread leave room for 4 CTAs of
-// 256 threads an SM.  Measured at (1024, 8192) bf16, back to back: 7.95 us
-// against 8.97 us for the 4-channel form with two rows ahead; 3, 5, 6 and 8
-// rows ahead, two vectors a thread and 6 or 8 CTAs an SM measured 8.15-9.8 us.
-constexpr int GN8_CTAS_PER_SM = 4;
+constexpr int GN8_AHEAD = 3;
+// One resident wave of 5 CTAs of 256 threads an SM (the launch bound holds
+// the kernel to 48 registers), so a row walker takes at most 6 rows of 1,024.
+// Measured at (1024, 8192) bf16, back to back: 7.73 us, against 7.95 us with
+// 4 CTAs an SM and four rows ahead (53 registers, at most 7 rows a walker)
+// and 8.97 us for the 4-channel form; 5 CTAs with four rows ahead spilled
+// and took 8.13 us, 6 CTAs with three rows ahead 7.90 us; 2, 5, 6 and 8 rows
+// ahead, two vectors a thread and 6 or 8 CTAs at four rows ahead 8.15-9.8 us.
+constexpr int GN8_CTAS_PER_SM = 5;
 
 __device__ __forceinline__ float2 bf16_pair(uint32_t w)
 {
@@ -196,7 +199,7 @@ __device__ __forceinline__ void st16_stream(void *p, uint4 v, uint64_t pol)
 // grid: x = column blocks of GN_THREADS vectors of 8, y = row walkers.
 // x, y: [N][C] of bf16; C8 = C / 8.  Same walk as gn_vec4_kernel.
 template <int TPG>
-__global__ void __launch_bounds__(GN_THREADS) gn_vec8_bf16_kernel(const __nv_bfloat16 *x,
+__global__ void __launch_bounds__(GN_THREADS, GN8_CTAS_PER_SM) gn_vec8_bf16_kernel(const __nv_bfloat16 *x,
                                                                   const __nv_bfloat16 *__restrict__ gamma,
                                                                   const __nv_bfloat16 *__restrict__ beta,
                                                                   __nv_bfloat16 *y, int64_t N, int C8, float invM,
