@@ -267,6 +267,9 @@ def test_bf16_entry_points_check_dtype(ng):
     (2, 64, 1024, 4, 4, 16),      # streamed over clusters of 16
     (2, 16, 2046, 4, 4, 2),       # streamed, channels change inside a vector (L = 8184)
     (2, 64, 1024, 4, 4, 1),       # streamed, one CTA holding 4,096 packed vectors
+    (3, 64, 300, 2, 4, 2),        # streamed, S = 300 < 4 * NT: a step is 3 channels and 124 values
+    (2, 16, 1020, 1, 4, 0),       # streamed, S = 1020: a step is 1 channel and 4 values
+    (100, 32, 4096, 4, 4, 2),     # streamed, full slices, S >= 4 * NT (the check-free copy), 1-2 groups a cluster
     (1, 32, 16384, 2, 0, 0),      # L = 262,144: 16 CTAs of 4,096 packed vectors
     (1, 128, 65536, 32, 0, 0),    # two-kernel path, vector form
     (3, 9, 5, 3, 2, 0),           # two-kernel path, scalar form

@@ -185,6 +185,10 @@ def test_full_size(ng):
     (5, 8192, 1, 2, 1),      # S = 1: consecutive channels
     (2, 8, 2046, 4, 2),      # S = 2046: channels change inside a vector
     (40, 256, 1024, 8, 4),   # 320 groups over clusters of 4
+    (3, 64, 300, 2, 2),      # S = 300 < 4 * NT: a thread's step is 3 channels and 124 values
+    (2, 16, 1020, 1, 2),     # S = 1020: a step is 1 channel and 4 values
+    (4, 32, 516, 2, 0),      # S = 516, automatic cluster
+    (160, 32, 2048, 4, 2),   # S = 2048 >= 4 * NT, full slices (the check-free copy), 2-3 groups a cluster
 ])
 def test_streamed(ng, N, C, S, G, cluster):
     check(ng, N, C, S, G, seed=N + C + S + cluster, path=STREAM, cluster=cluster)
