@@ -854,15 +854,18 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
 //   mean)^2).
 // Several CTAs per SM keep several rows in flight.
 
-// NT threads a CTA, V 4-element vectors a thread.  The bf16 form with packed
-// rows (V >= 16) is held to 1,024 threads an SM's worth of registers (63 a
-// thread at NT = 64: 16 CTAs an SM instead of 14 at the 72 it takes
-// unbounded).  Measured back to back on GB300: bf16 (16384, 4096) 47.7 ->
-// 45.1 us, (8192, 8192) 48.0 -> 45.4 us, (16384, 8192) 89.3 -> 86.2 us; a
-// bound of 1,152 threads (56 registers) gave 46.7, 47.2 and 89.0 us, and
-// tighter bounds spilled.
+// NT threads a CTA, V 4-element vectors a thread.  The bf16 forms with
+// packed rows (V >= 16) and with 4 vectors a thread are held to 1,024
+// threads an SM's worth of registers (63-64 a thread: at NT = 64, 16 CTAs an
+// SM instead of 14 at the 72 the packed form takes unbounded).  Measured
+// back to back on GB300: bf16 (16384, 4096) 47.7 -> 45.1 us, (8192, 8192)
+// 48.0 -> 45.4 us, (16384, 8192) 89.3 -> 86.2 us, (131072, 512) 58.4 ->
+// 54.9 us; a bound of 1,152 threads (56 registers) gave 46.7, 47.2 and 89.0
+// us, tighter bounds spilled, and the same bound on 8 vectors a thread was
+// slower ((65536, 1024) 45.7 -> 47.5 us).
 template <typename T, int NT, int V>
-__global__ void __launch_bounds__(NT, (sizeof(T) == 2 && V >= 16) ? 1024 / NT : 1) ln_rows_kernel(LnParams p)
+__global__ void __launch_bounds__(NT, (sizeof(T) == 2 && (V >= 16 || V == 4)) ? 1024 / NT : 1)
+    ln_rows_kernel(LnParams p)
 {
     pdl_begin();
     __shared__ float red[2][NT / 32];
