@@ -80,6 +80,7 @@
 // Split path (any shape): kernel 1 writes one triple per (row, chunk) CTA;
 // kernel 2 merges the row's triples and applies, re-reading x.
 #include "norm_internal.cuh"
+#include <type_traits>
 
 namespace normk {
 
@@ -101,7 +102,15 @@ constexpr int LN_TM_COLS = 8 * LN_V;      // TMEM columns of one apply thread: g
 constexpr uint32_t LN_TM_BETA = 4 * LN_V; // column offset of beta within them
 constexpr int LN_SLOTS = 4;               // partial-record slots: reused 4 rows later
 constexpr int LN_MAX_GRID = 160;          // CTAs whose records one warp loads at once
+// Bytes a bulk copy of a slice moves at once.  With one row group (the whole
+// grid on every row) the slices go in 4 KB pieces: measured back to back on
+// GB300 at (16, 4194304), 92.9-93.1 us against 94.4 us with 32 KB pieces
+// (8 KB 93.7, 16 KB and 128 KB 94.5, 2 KB 99.5 us).  With several row groups
+// 32 KB pieces were faster ((256, 262144) in 13 groups: 94.0 us against
+// 96.4 us with 4 KB; (64, 1048576) in 4 groups: 91.7 against 92.2 us), and
+// small pieces only for the prologue's copies gained less (94.1 us).
 constexpr uint32_t LN_BULK_CHUNK = 32768;
+constexpr uint32_t LN_BULK_CHUNK_ONE_GROUP = 4096;
 constexpr int LN_BAR_APPLIED = 1;         // named barrier of warp 0 and the apply warps
 constexpr int LN_BAR_STATS = 2;           // named barrier of the statistics warps
 constexpr int LN_BAR_PRO = 3;             // statistics and apply warps (rows 0 and 1)
@@ -400,7 +409,9 @@ __device__ __forceinline__ float4 gn_unit(const float4 &v, const RowMean &rm, fl
 // through L1 per unit (S a multiple of the unit's UE values) instead of held
 // in TMEM, and the output is 2 LReLU((x - mean) * rstd * gamma + beta).
 // T: float or __nv_bfloat16 (x, y, gamma, beta), fp32 arithmetic.
-template <typename T, bool GN>
+// ONE: the grid is a single row group (fp32 LayerNorm form only); its slices
+// are copied in LN_BULK_CHUNK_ONE_GROUP pieces.
+template <typename T, bool GN, bool ONE>
 __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p, GnPersist gp_)
 {
     // A unit is 16 bytes of a row: UE = 4 fp32 or 8 bf16 values.  Slices,
@@ -446,6 +457,13 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
     const int buf_u = (p.max_n4 + 7) & ~7;
 
     const uint64_t pol_stream = policy_evict_first();
+    // bulk copy of `bytes` from src to dst on bar, in pieces (see
+    // LN_BULK_CHUNK)
+    auto copy_in = [&](float4 *dst, const float4 *src, uint32_t bytes, uint64_t *bar) {
+        constexpr uint32_t piece = ONE ? LN_BULK_CHUNK_ONE_GROUP : LN_BULK_CHUNK;
+        for (uint32_t off = 0; off < bytes; off += piece)
+            bulk_g2s(dst + off / 16, src + off / 16, (bytes - off < piece) ? (bytes - off) : piece, bar, pol_stream);
+    };
     // Waits for this CTA's own bulk copies after a failure (drains) use at
     // least 100 ms, whatever the configured limit: a copy always completes
     // in microseconds, and the CTA must not exit while one still writes its
@@ -484,9 +502,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
         bulk_g2s(&piv_in[q & 1][2], row + (Lu - 1), 16u, bar, pol_stream);
         const float4 *src = row + f0;
         float4 *dst = ln_smem + (q & 1) * buf_u;
-        for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
-            bulk_g2s(dst + off / 16, src + off / 16, (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK,
-                     bar, pol_stream);
+        copy_in(dst, src, bytes, bar);
     };
     auto x_parity = [](int64_t q) { return static_cast<uint32_t>((q >> 1) & 1); };
 
@@ -606,9 +622,7 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_persistent_kernel(LnParams p
             const uint32_t bytes = src ? static_cast<uint32_t>(nu) * 16u : 0u;
             mbar_arrive_expect_tx(bar, bytes);
             float4 *dst = ln_smem + buf * buf_u;
-            for (uint32_t off = 0; off < bytes; off += LN_BULK_CHUNK)
-                bulk_g2s(dst + off / 16, src + f0 + off / 16,
-                         (bytes - off < LN_BULK_CHUNK) ? (bytes - off) : LN_BULK_CHUNK, bar, pol_stream);
+            copy_in(dst, src + f0, bytes, bar);
         };
         if (issuer) {
             issue_x(0);
@@ -1136,16 +1150,31 @@ LnPersistentConfig ln_persistent_config()
     return LnPersistentConfig{LN_THREADS, LN_A, LN_V, LN_SLOTS * 16, LN_MAX_GRID};
 }
 
+namespace {
+
+// The persistent kernel's forms: fp32 and bf16 LayerNorm (fp32 also with a
+// single row group) and GroupNorm.
+const void *const kPersistentForms[] = {reinterpret_cast<const void *>(ln_persistent_kernel<float, false, false>),
+                                        reinterpret_cast<const void *>(ln_persistent_kernel<float, false, true>),
+                                        reinterpret_cast<const void *>(ln_persistent_kernel<float, true, false>),
+                                        reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, false, false>),
+                                        reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, true, false>)};
+
+const void *persistent_form(bool bf16, bool gn, bool one_group)
+{
+    if (bf16)
+        return gn ? kPersistentForms[4] : kPersistentForms[3];
+    return gn ? kPersistentForms[2] : one_group ? kPersistentForms[1] : kPersistentForms[0];
+}
+
+} // namespace
+
 cudaError_t ln_persistent_static_smem(int *bytes)
 {
     cudaFuncAttributes a;
-    // the four forms declare the same static shared memory; report the largest
+    // the forms declare the same static shared memory; report the largest
     int most = 0;
-    const void *forms[] = {reinterpret_cast<const void *>(ln_persistent_kernel<float, false>),
-                           reinterpret_cast<const void *>(ln_persistent_kernel<float, true>),
-                           reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, false>),
-                           reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, true>)};
-    for (const void *k : forms) {
+    for (const void *k : kPersistentForms) {
         const cudaError_t e = cudaFuncGetAttributes(&a, k);
         if (e != cudaSuccess)
             return e;
@@ -1155,24 +1184,10 @@ cudaError_t ln_persistent_static_smem(int *bytes)
     return cudaSuccess;
 }
 
-namespace {
-
-const void *persistent_form(bool bf16, bool gn)
-{
-    if (bf16)
-        return gn ? reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, true>)
-                  : reinterpret_cast<const void *>(ln_persistent_kernel<__nv_bfloat16, false>);
-    return gn ? reinterpret_cast<const void *>(ln_persistent_kernel<float, true>)
-              : reinterpret_cast<const void *>(ln_persistent_kernel<float, false>);
-}
-
-} // namespace
-
 cudaError_t ln_persistent_setup(int max_dynamic_smem)
 {
-    for (int f = 0; f < 4; ++f) {
-        const cudaError_t e = cudaFuncSetAttribute(persistent_form(f >= 2, f & 1),
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+    for (const void *k : kPersistentForms) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
         if (e != cudaSuccess)
             return e;
     }
@@ -1181,12 +1196,11 @@ cudaError_t ln_persistent_setup(int max_dynamic_smem)
 
 cudaError_t ln_persistent_occupancy(int dyn_smem, int *ctas_per_sm)
 {
-    // the smallest over the four forms (each is one CTA a SM by design)
+    // the smallest over the forms (each is one CTA a SM by design)
     int least = 1 << 30;
-    for (int f = 0; f < 4; ++f) {
+    for (const void *k : kPersistentForms) {
         int n = 0;
-        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, persistent_form(f >= 2, f & 1),
-                                                                            LN_THREADS, dyn_smem);
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, LN_THREADS, dyn_smem);
         if (e != cudaSuccess)
             return e;
         least = n < least ? n : least;
@@ -1201,8 +1215,8 @@ cudaError_t ln_persistent_launch(const LnParams &p, int grid, int dyn_smem, cuda
     LnParams args = p;
     GnPersist gargs = gn ? *gn : GnPersist{1, 1, 8, 0.f};
     void *kargs[] = {&args, &gargs};
-    return cudaLaunchCooperativeKernel(persistent_form(bf16, gn != nullptr), dim3(grid), dim3(LN_THREADS), kargs,
-                                       static_cast<size_t>(dyn_smem), stream);
+    return cudaLaunchCooperativeKernel(persistent_form(bf16, gn != nullptr, p.groups == 1), dim3(grid),
+                                       dim3(LN_THREADS), kargs, static_cast<size_t>(dyn_smem), stream);
 }
 
 int64_t ln_rows_max_row_len()
