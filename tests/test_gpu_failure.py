@@ -31,8 +31,9 @@ def ng():
     m.norm_set_option(m.NORM_OPT_LN_PATH, 0)
 
 
-def test_barrier_timeout_is_reported_and_recoverable(ng):
-    rows, L = 3, 152 * 4 * 64
+@pytest.mark.parametrize("rows", [3, 1])  # three row groups; one group (the one-group form)
+def test_barrier_timeout_is_reported_and_recoverable(ng, rows):
+    L = 152 * 4 * 64
     x = normgen.normal(rows * L, seed=1)
     xb = Guarded(rows * L, x)
     yb = Guarded(rows * L)
@@ -54,14 +55,15 @@ def test_barrier_timeout_is_reported_and_recoverable(ng):
     assert yb.guards_intact()
 
 
-def test_tiny_wait_limit_aborts_cleanly(ng):
+@pytest.mark.parametrize("rows", [3, 1])  # three row groups; one group (the one-group form)
+def test_tiny_wait_limit_aborts_cleanly(ng, rows):
     """A 1 ns limit makes any wait that is not over at its first look give up: the
     statistics and apply warps' waits for a row's bulk copy (row 0 has not landed
     when they first look), or warp 0's poll.  Whichever gives up, the CTA must record
     NORM_ERR_TIMEOUT and drain its copies (drains wait at least 100 ms whatever the
     limit).  CTAs stop independently, so y may be partly written: every element is
     untouched or correct.  Then a normal call works."""
-    rows, L = 3, 152 * 4 * 64
+    L = 152 * 4 * 64
     x, g, b = (normgen.normal(rows * L, seed=5), normgen.normal(L, 1.0, 0.1, seed=5, tensor_id=1),
                normgen.normal(L, 0.0, 0.1, seed=5, tensor_id=2))
     want = oracle.layer_norm(x, g, b, rows, L).reshape(rows, L)
