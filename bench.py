@@ -83,7 +83,7 @@ CONFIGS = {
                      workload="RMSNorm over dim 1 of bf16 NCHW (112,64,512,512), fp32 arithmetic, eps 1e-5"),
     "ln_mid": dict(op="ln", rows=256, L=262144, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
                    workload="LayerNorm fp32 (256, 262144) over the last dim, x~N(0,1), gamma~N(1,0.1), "
-                            "beta~N(0,0.1), eps 1e-5 (rows of mid length: the persistent kernel in 13 row groups)"),
+                            "beta~N(0,0.1), eps 1e-5 (rows of mid length: the persistent kernel in 15 row groups)"),
     "ln_rows": dict(op="ln", rows=16384, L=4096, x=(0.0, 1.0), gamma=(1.0, 0.1), beta=(0.0, 0.1),
                     workload="LayerNorm fp32 (16384, 4096) over the last dim, x~N(0,1), gamma~N(1,0.1), "
                              "beta~N(0,0.1), eps 1e-5 (many short rows)"),

@@ -112,8 +112,9 @@ typedef enum {
  *     per row; x is read from HBM once.  Rows shorter than about 3 Mi
  *     elements are spread over groups of CTAs, each group taking every k-th
  *     row, so that each row's exchange hides behind the group's next rows;
- *   - any other shape (ragged lengths, misaligned pointers): a two-kernel
- *     path that reads x twice.
+ *   - any other shape (ragged lengths, misaligned pointers), and rows of
+ *     131,073 to 1,048,575 elements over less than 24 MiB of x (where its
+ *     second read of x comes from L2): a two-kernel path that reads x twice.
  * All produce the same statistics definition.
  */
 size_t norm_layer_workspace_bytes(int64_t rows, int64_t row_len);

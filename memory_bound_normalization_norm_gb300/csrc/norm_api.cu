@@ -37,6 +37,15 @@ constexpr int64_t kPersistentMinRowLen = 131073;
 // stay on the row and cluster kernels (fp32 0.84 vs 0.81 persistent).
 constexpr int64_t kPersistentMidRowLen = 32768;
 constexpr size_t kPersistentMidMinBytes = size_t(96) << 20;
+// Rows of 131,073 to 1,048,575 elements over less than 24 MiB of x take the
+// two-kernel path, whose second read of x then comes from L2: measured on
+// GB300 (two-kernel vs persistent, us) fp32 (8, 262144) 10.8 vs 12.3,
+// (16, 262144) 15.3 vs 19.0, (32, 262144) 23.4 vs 24.3 (left to the
+// persistent kernel), (48, 262144) 31.7 vs 28.0; bf16 (16, 262144) 12.8 vs
+// 13.6, (32, 262144) 18.2 vs 19.9, (64, 262144) 28.7 vs 26.4.  Rows of 1 Mi
+// or more stay persistent at any size (fp32 (4, 1048576) 16.7 vs 16.4).
+constexpr size_t kPersistentSmallBytes = size_t(24) << 20;
+constexpr int64_t kPersistentAnySizeRowLen = int64_t(1) << 20;
 // NORM_OPT_LN_PATH value of the streamed cluster kernel, and the longest
 // row the automatic choice gives the row kernel.  Measured on GB300 (GB/s
 // fractions of the copy peak): the row kernel, its CTA sized to the row,
@@ -294,11 +303,13 @@ int64_t persistent_max_row_len(const DeviceState &d, int esz = 4)
 // Row groups of the persistent kernel for `rows` rows of L elements of esz
 // bytes on a grid of at most gmax CTAs, or 0 if no split of the grid holds a
 // row slice.  A group's CTAs must hold its slices (at most max_slice 16-byte
-// units each), and a group's row must stream for about 4 us or more at the
-// HBM rate (4 us * 6.5 TB/s / (2 esz bytes an element) = 13,000,000 /
-// (esz L) groups at least; 3,250,000 / L for fp32) so that the grid
+// units each), and a group's row must stream for about 5.5 us or more at
+// the HBM rate (5.5 us * 6.5 TB/s / (2 esz bytes an element) = 18,000,000 /
+// (esz L) groups at least; 4,500,000 / L for fp32) so that the grid
 // exchange, two rows ahead, hides behind it.  Measured on GB300 (fraction
-// of the copy peak): 2.6 us a group row gave 0.73-0.76, 3.9-5.2 us 0.87-0.92.  Among the admissible
+// of the copy peak): 2.6 us a group row gave 0.73-0.76, 3.9-5.2 us 0.87-0.92;
+// (256, 262144) took 92.7 us in 15 groups against 93.5 us in the 13 that a
+// 4 us floor gives, other shapes within 0.3 us.  Among the admissible
 // counts (at most one group per row), the one that leaves the fewest idle
 // row slots (ceil(rows / k) * k) wins; ties go to more groups.
 int persistent_groups(int64_t rows, int64_t L, int gmax, int64_t max_slice, int esz)
@@ -310,7 +321,7 @@ int persistent_groups(int64_t rows, int64_t L, int gmax, int64_t max_slice, int 
     int64_t kmax = gmax / gk_min;
     if (kmax > rows)
         kmax = rows;
-    const int64_t per_group_bytes = int64_t(13000000) / esz; // elements x esz
+    const int64_t per_group_bytes = int64_t(18000000) / esz; // elements x esz
     int64_t kmin = (per_group_bytes + L - 1) / L;
     if (kmin < 1)
         kmin = 1;
@@ -602,9 +613,11 @@ norm_status_t layer_plan(const void *x, const void *gamma, const void *beta, con
     // values) of 16-byte aligned tensors
     const bool unit_ok = row_len % (16 / esz) == 0 && aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
                          aligned(beta, 16);
-    const bool pers_wanted = path_opt == 1 || (path_opt == 0 && (row_len >= kPersistentMinRowLen ||
-                                                                 (row_len >= kPersistentMidRowLen &&
-                                                                  nb >= kPersistentMidMinBytes)));
+    const bool pers_wanted =
+        path_opt == 1 ||
+        (path_opt == 0 &&
+         ((row_len >= kPersistentMinRowLen && (nb >= kPersistentSmallBytes || row_len >= kPersistentAnySizeRowLen)) ||
+          (row_len >= kPersistentMidRowLen && nb >= kPersistentMidMinBytes)));
     LnPlan pp;
     if (pers_wanted && unit_ok && plan_persistent(rows, row_len, *d, &pp, esz)) {
         c.pl = pp;

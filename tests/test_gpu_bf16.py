@@ -103,8 +103,10 @@ def test_layer_norm_bf16_in_place_no_affine_misaligned(ng, offset):
 
 @pytest.mark.parametrize("rows,L,path", [
     (2, 1 << 20, 0),       # the automatic choice above 131,072: one row group per row
-    (3, 131080, 0),        # just above the cluster kernel's longest row
-    (16, 262144, 0),       # 16 row groups (a bf16 group row must stream as long as an fp32 one)
+    (3, 131080, 1),        # just above the cluster kernel's longest row (forced: the automatic choice
+                           # takes the two-kernel path below 24 MiB)
+    (16, 262144, 1),       # 16 row groups (a bf16 group row must stream as long as an fp32 one)
+    (64, 262144, 0),       # 32 MiB of rows of 262,144: the automatic choice
     (2048, 32768, 0),      # 128 MiB of rows of 32,768: the automatic choice, 152 groups of 1 CTA
     (40, 131088, 1),       # forced: many row groups of few CTAs
     (5, 64, 1),            # forced: 8 units a row, most CTAs hold nothing

@@ -176,12 +176,12 @@ def test_persistent_exchange_200_launches_back_to_back(ng):
 
 
 @pytest.mark.parametrize("rows,L,path", [
-    (256, 262144, AUTO),        # 13 row groups of 11 CTAs (the automatic choice)
+    (256, 262144, AUTO),        # 15 row groups of 10 CTAs (the automatic choice)
     (64, 1 << 20, AUTO),        # 4 groups of 38
     (11, (1 << 20) + 4, AUTO),  # 4 groups, 3, 3, 3 and 2 rows
     (3, 1 << 20, AUTO),         # one row per group
-    (40, 131076, PERSISTENT),   # 25 groups of 6 CTAs, forced
-    (7, 200004, AUTO),          # a length that is not a multiple of the group size
+    (40, 131076, PERSISTENT),   # 30 groups of 5 CTAs, forced
+    (7, 200004, PERSISTENT),    # a length that is not a multiple of the group size (5.6 MB: forced)
     (1024, 32768, AUTO),        # 128 MiB of rows of 32,768: 76 groups of 2 CTAs (automatic)
     (384, 65536, AUTO),         # 96 MiB of rows of 65,536: 50 groups of 3 CTAs (automatic)
 ])
