@@ -24,7 +24,11 @@ namespace normk {
 
 namespace {
 
-constexpr int GN_THREADS = 256;
+constexpr int GN_THREADS = 256;  // the 8-channel bf16 form
+// The 4-channel form: 128-thread CTAs.  Measured at (1024, 8192) fp32, back
+// to back: 11.84-11.90 us with grids of 16 to 32 CTAs of 128 an SM, against
+// 12.14-12.16 us with 256-thread CTAs (8 an SM) and 12.28 us with 512.
+constexpr int GN4_THREADS = 128;
 
 template <int TPG>
 __device__ __forceinline__ float group_sum(float v)
@@ -63,14 +67,14 @@ struct Raw4<__nv_bfloat16> {
     static __device__ __forceinline__ float4 get(const type &r) { return Io<__nv_bfloat16>::unpack(r.x, r.y); }
 };
 
-// grid: x = column blocks of GN_THREADS*U vectors, y = row walkers.
+// grid: x = column blocks of GN4_THREADS*U vectors, y = row walkers.
 // x, y: [N][C] of T; "vector" = 4 consecutive channels; C4 = C / 4.
-// A CTA owns a fixed block of GN_THREADS * U vectors of columns and walks
+// A CTA owns a fixed block of GN4_THREADS * U vectors of columns and walks
 // rows n = blockIdx.y, + gridDim.y, ...: gamma/beta of its columns are
 // loaded once, and the next two rows' x are loaded while the current row is
 // reduced and written, so every thread keeps two rows of loads in flight.
 template <typename T, int TPG, int U>
-__global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T *__restrict__ gamma,
+__global__ void __launch_bounds__(GN4_THREADS) gn_vec4_kernel(const T *x, const T *__restrict__ gamma,
                                                              const T *__restrict__ beta, T *y,
                                                              int64_t N, int C4, float invM, float eps,
                                                              float slope)
@@ -78,7 +82,7 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     pdl_begin();
-    const int col0 = blockIdx.x * (GN_THREADS * U) + threadIdx.x;
+    const int col0 = blockIdx.x * (GN4_THREADS * U) + threadIdx.x;
     using R = Raw4<T>;
     float2 g[U][2], b[U][2]; // gamma/beta of the vector's two pairs
     typename R::type cur[U], nxt[U], nx2[U];
@@ -86,7 +90,7 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
     // exact, so the x + x costs nothing per element and the result is the same
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int c = col0 + u * GN_THREADS;
+        const int c = col0 + u * GN4_THREADS;
         const bool in = c < C4;
         const float4 gv = (in && gamma) ? Io<T>::ld4_ro(gamma + 4 * c, pol_keep) : make_float4(1.f, 1.f, 1.f, 1.f);
         const float4 bv = (in && beta) ? Io<T>::ld4_ro(beta + 4 * c, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
         const T *xr = x + n * C4 * 4;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int c = col0 + u * GN_THREADS;
+            const int c = col0 + u * GN4_THREADS;
             dst[u] = c < C4 ? R::load(xr + 4 * c, pol_stream) : R::zero();
         }
     };
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(GN_THREADS) gn_vec4_kernel(const T *x, const T
         T *yr = y + n * C4 * 4;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int c = col0 + u * GN_THREADS;
+            const int c = col0 + u * GN4_THREADS;
             // C4 is a multiple of TPG, so whole groups are in or out of range
             // together and every lane takes part in the shuffles.  The
             // arithmetic is in f32x2 pairs.
@@ -300,14 +304,15 @@ cudaError_t launch_vec(const void *x, const void *gamma, const void *beta, void 
                        int64_t M, float eps, float slope, int sm_count, cudaStream_t stream)
 {
     const int C4 = static_cast<int>(C / 4);
-    const int per_block = GN_THREADS * U;
+    const int per_block = GN4_THREADS * U;
     const int gx = (C4 + per_block - 1) / per_block;
-    // Grid sized for 8 CTAs per SM; each walks N / gy rows.  Only 4 or 5
-    // are resident at once (about 55 registers a thread in fp32, 48 in
-    // bf16), so the launch runs as two waves of CTAs: measured faster at
-    // (1024, 8192) than a grid of one resident wave (fp32 12.2 vs 12.4 us,
-    // bf16 9.0 vs 10.0 us a call back to back).
-    constexpr int CTAS_PER_SM = 8;
+    // Grid sized for 20 CTAs of 128 threads per SM; each walks N / gy rows.
+    // About 9 are resident at once (54 registers a thread), so the launch
+    // runs as two waves: with 256-thread CTAs two waves also measured faster
+    // than one (fp32 12.2 vs 12.4 us, bf16 9.0 vs 10.0 us a call back to
+    // back); with 128 threads, 16 to 32 an SM measured the same (11.84-11.90
+    // us) and 12 slower (12.41 us).
+    constexpr int CTAS_PER_SM = 20;
     int64_t gy = (static_cast<int64_t>(sm_count) * CTAS_PER_SM + gx - 1) / gx;
     if (gy > N)
         gy = N;
@@ -316,7 +321,7 @@ cudaError_t launch_vec(const void *x, const void *gamma, const void *beta, void 
     if (gy < 1)
         gy = 1;
     dim3 grid(gx, static_cast<unsigned>(gy));
-    return launch_pdl(gn_vec4_kernel<T, TPG, U>, grid, dim3(GN_THREADS), 0, stream, static_cast<const T *>(x),
+    return launch_pdl(gn_vec4_kernel<T, TPG, U>, grid, dim3(GN4_THREADS), 0, stream, static_cast<const T *>(x),
                       static_cast<const T *>(gamma), static_cast<const T *>(beta), static_cast<T *>(y), N, C4,
                       1.0f / static_cast<float>(M), eps, slope);
 }
