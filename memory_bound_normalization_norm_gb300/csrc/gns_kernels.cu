@@ -1238,8 +1238,17 @@ cudaError_t gns_reg_launch(const GnSegParams &p, bool bf16, int cluster, cudaStr
 
 namespace {
 
-// Streamed variants: 256 threads, 4 or 8 vectors a thread (16 for bf16).
-constexpr int GNS_STREAM_NT = 256;
+// Streamed variants: GroupNorm (act) in 128-thread CTAs, LayerNorm rows in
+// 256-thread CTAs, with the same slices (1,024, 2,048 or, bf16, 4,096
+// vectors a CTA).  Measured on GB300, each build timed alone (us, 256 -> 128
+// threads): GN NCHW (8,512,64,64) fp32 27.0 -> 26.7, bf16 20.7 -> 20.5,
+// (16,64,128,128)/8 28.6 -> 26.8, (16,512,32,64) bf16 22.6 -> 20.6; LayerNorm
+// rows slower with 128 ((256, 65536) 30.8 -> 33.5, bf16 (512, 32768) 22.6 ->
+// 26.9).
+constexpr int stream_nt(bool act)
+{
+    return act ? 128 : 256;
+}
 
 // Vectors a CTA slice of the streamed kernel holds: bf16 keeps its values
 // packed, so twice as many.
@@ -1251,18 +1260,19 @@ constexpr int stream_cap(bool bf16)
 template <typename T, int MODE, bool ACT>
 RegKernel stream_kernel_for(int per, int *idx)
 {
+    constexpr int NT = stream_nt(ACT);
     if (per <= 1024) {
         *idx = 0;
-        return gns_stream_kernel<T, GNS_STREAM_NT, 4, MODE, ACT>;
+        return gns_stream_kernel<T, NT, 1024 / NT, MODE, ACT>;
     }
     if (per <= 2048) {
         *idx = 1;
-        return gns_stream_kernel<T, GNS_STREAM_NT, 8, MODE, ACT>;
+        return gns_stream_kernel<T, NT, 2048 / NT, MODE, ACT>;
     }
     if constexpr (sizeof(T) == 2) {
         if (per <= 4096) {
             *idx = 2;
-            return gns_stream_kernel<T, GNS_STREAM_NT, 16, MODE, ACT>;
+            return gns_stream_kernel<T, NT, 4096 / NT, MODE, ACT>;
         }
     }
     *idx = -1;
@@ -1351,7 +1361,7 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool 
         e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess)
         return e;
-    const int nt = GNS_STREAM_NT;
+    const int nt = stream_nt(act);
     if (cluster == 1) {
         int per_sm = 0, sms = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, nt, smem);
@@ -1401,7 +1411,7 @@ cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int clu
     // slower, 35.0 vs 29.0 us at (8,512,64,64)).
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr;
-    cluster_config(&cfg, &attr, GNS_STREAM_NT, cluster, static_cast<unsigned>(clusters * cluster), stream);
+    cluster_config(&cfg, &attr, stream_nt(act), cluster, static_cast<unsigned>(clusters * cluster), stream);
     cfg.dynamicSmemBytes = smem;
     if (cluster == 1)
         cfg.numAttrs = 0;
