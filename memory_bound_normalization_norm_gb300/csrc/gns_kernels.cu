@@ -488,6 +488,10 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
         cluster_sync_all();
     else
         __syncthreads();
+    // Launched with programmatic stream serialization (the GroupNorm form):
+    // wait for the previous kernel of the stream before the first global
+    // access.  Without that launch attribute this returns at once.
+    pdl_wait();
     // thread 0: copy this CTA's slice of segment k (and the segment's first
     // 16 bytes, which hold the pivot) into buffer k & 1
     auto issue = [&](int64_t k) {
@@ -595,6 +599,10 @@ __global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParam
                 if (f != 0.f || to)
                     stopped = true;
             }
+            // the last segment's statistics are merged: the next kernel of the
+            // stream may be scheduled onto SMs as this grid's CTAs finish
+            if (k == nk - 1)
+                pdl_trigger();
             if (stopped)
                 return; // keep exchanging, write nothing
             // ACT: y = 2 * LReLU((x - mean) * rstd * gamma + beta), with x - mean
@@ -1405,16 +1413,27 @@ cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int clu
     args.parts = cluster;
     args.per4 = static_cast<int>(per);
     const size_t smem = stream_smem(per, bf16);
-    // No programmatic dependent launch here: the grid is sized to the
-    // clusters that fit an idle GPU, and launched early onto SMs the previous
-    // kernel still holds, fewer of them were resident at once (measured
-    // slower, 35.0 vs 29.0 us at (8,512,64,64)).
+    // The GroupNorm form is launched with programmatic stream serialization:
+    // each CTA lets the next kernel be scheduled once its last segment's
+    // statistics are merged, so the next call's launch overlaps this one's
+    // last writes (back to back, µs per call: (8,512,64,64) bf16 20.4 ->
+    // 17.9, fp32 26.7 -> 26.3; (64,512,16,16) fp32 16.4 -> 13.8).  Letting it
+    // be scheduled at the start measured slower (fp32 (8,512,64,64) 29.5-29.8
+    // us: the next grid's clusters took SMs while this one still ran), and
+    // LayerNorm rows measured slower with either trigger ((256, 65536) fp32
+    // 30.8 -> 33.2 us, (512, 32768) bf16 22.6 -> 25.2 us), so they launch
+    // plainly and the kernel's wait and trigger do nothing.
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr;
-    cluster_config(&cfg, &attr, stream_nt(act), cluster, static_cast<unsigned>(clusters * cluster), stream);
+    cudaLaunchAttribute attr[2];
+    cluster_config(&cfg, &attr[0], stream_nt(act), cluster, static_cast<unsigned>(clusters * cluster), stream);
     cfg.dynamicSmemBytes = smem;
     if (cluster == 1)
         cfg.numAttrs = 0;
+    if (act) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
+    }
     return cudaLaunchKernelEx(&cfg, k, args);
 }
 

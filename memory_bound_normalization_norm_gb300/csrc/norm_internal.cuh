@@ -142,12 +142,24 @@ __device__ __forceinline__ float4 ld_l2_f4(const float4 *p)
 // its writes are visible: it must come before the kernel's first global
 // memory access.  Without a programmatic predecessor the wait returns at
 // once.  Used by the grid-stride kernels (row LayerNorm, (N, C) GroupNorm,
-// RMSNorm) and both kernels of the two-kernel paths; the persistent kernels,
-// whose grids are sized to what fits an idle GPU, launch normally.
-__device__ __forceinline__ void pdl_begin()
+// RMSNorm) and both kernels of the two-kernel paths.  The streamed cluster
+// kernel's GroupNorm form waits first and triggers late (pdl_wait, then
+// pdl_trigger once its last segment's statistics are merged); the
+// persistent LayerNorm kernel launches normally.
+__device__ __forceinline__ void pdl_trigger()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_begin()
+{
+    pdl_trigger();
+    pdl_wait();
 }
 
 // ---- mbarrier + bulk copy (TMA engine, non-tensor form)
