@@ -268,7 +268,10 @@ norm_status_t norm_group_lrelu_x2_fwd_bf16(const uint16_t *x, const uint16_t *ga
  *     distributed shared memory; x is read from HBM once.  Where each CTA's
  *     share of a group is 1,024 elements or more (and, for bf16, L is a
  *     multiple of 8), a persistent grid of clusters streams the next group
- *     into shared memory by bulk copy while the current one is reduced;
+ *     into shared memory by bulk copy while the current one is reduced (a
+ *     group already split over a cluster may be split over twice the CTAs,
+ *     up to 8, when the waves of groups over the resident clusters make
+ *     that faster);
  *     its waits are bounded by NORM_OPT_BARRIER_TIMEOUT_NS (a CTA that gives
  *     up records NORM_ERR_TIMEOUT and leaves its part of the remaining
  *     groups of y unwritten);

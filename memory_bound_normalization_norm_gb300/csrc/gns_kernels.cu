@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
 constexpr int GNS_NBUF = 1;     // shared-memory slice buffers per CTA
 constexpr int GNS_MIN_CTAS = 4; // CTAs per SM the register budget is sized for
 
+
 template <typename T>
 __device__ __forceinline__ float4 ld4_smem(const T *p);
 
@@ -420,8 +421,8 @@ __device__ __forceinline__ float2 lrelu2(float2 t, float2 slope2, bool steep)
 // segment on the whole cluster writes nothing, stops waiting for copies and
 // keeps exchanging (the exchanges still complete) until the end; each CTA
 // then drains its own copies.
-template <typename T, int NT, int V, int MODE, bool ACT>
-__global__ void __launch_bounds__(NT, GNS_MIN_CTAS) gns_stream_kernel(GnSegParams p)
+template <typename T, int NT, int V, int MODE, bool ACT, int MINB>
+__global__ void __launch_bounds__(NT, MINB) gns_stream_kernel(GnSegParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float4 piv[2]; // first 16 bytes of the segment, copied with the slice
@@ -1265,43 +1266,66 @@ constexpr int stream_cap(bool bf16)
     return bf16 ? 4096 : 2048;
 }
 
+// CTAs per SM a form's registers are sized for.  The 128-thread forms with
+// slices of 1,024 vectors (32 registers a thread of fp32, 16 of bf16) are
+// sized for 5 (at most 102 registers, none spilled).  bf16 slices of 2,048
+// vectors (32 registers) have two forms: 5 CTAs an SM where a group is split
+// over twice the CTAs that hold it ("wide": more clusters resident, more
+// groups streamed by each), 4 otherwise.  Measured back to back (µs, 4 ->
+// 5 CTAs an SM): (64,512,16,16) fp32 13.9 -> 13.1 and bf16 10.9 -> 10.6;
+// (8,512,64,64) bf16 split over 8 CTAs 19.6 -> 17.4; (32,512,16,32) bf16,
+// one CTA a group, 10.2 -> 11.8, which keeps the 4-CTA form.
 template <typename T, int MODE, bool ACT>
-RegKernel stream_kernel_for(int per, int *idx)
+RegKernel stream_kernel_for(int per, bool wide, int *idx)
 {
     constexpr int NT = stream_nt(ACT);
+    constexpr int SMALL = NT == 128 ? 5 : GNS_MIN_CTAS;
     if (per <= 1024) {
         *idx = 0;
-        return gns_stream_kernel<T, NT, 1024 / NT, MODE, ACT>;
+        return gns_stream_kernel<T, NT, 1024 / NT, MODE, ACT, SMALL>;
     }
     if (per <= 2048) {
+        if constexpr (sizeof(T) == 2 && NT == 128) {
+            if (wide) {
+                *idx = 3;
+                return gns_stream_kernel<T, NT, 2048 / NT, MODE, ACT, 5>;
+            }
+        }
         *idx = 1;
-        return gns_stream_kernel<T, NT, 2048 / NT, MODE, ACT>;
+        return gns_stream_kernel<T, NT, 2048 / NT, MODE, ACT, GNS_MIN_CTAS>;
     }
     if constexpr (sizeof(T) == 2) {
         if (per <= 4096) {
             *idx = 2;
-            return gns_stream_kernel<T, NT, 4096 / NT, MODE, ACT>;
+            return gns_stream_kernel<T, NT, 4096 / NT, MODE, ACT, GNS_MIN_CTAS>;
         }
     }
     *idx = -1;
     return nullptr;
 }
 
+// Largest slice (vectors) of the form with index idx.
+constexpr int stream_shape_per(int idx)
+{
+    return idx == 3 ? 2048 : 1024 << idx;
+}
+
 // GroupNorm (act: LeakyReLU x2) in all three channel maps; LayerNorm (no
 // act) is one group of the whole row with per-element gamma/beta (S = 1).
 template <typename T>
-RegKernel stream_kernel_t(int per, int mode, bool act, int *idx)
+RegKernel stream_kernel_t(int per, int mode, bool act, bool wide, int *idx)
 {
     if (!act)
-        return mode == AFF_ROW ? stream_kernel_for<T, AFF_ROW, false>(per, idx) : nullptr;
+        return mode == AFF_ROW ? stream_kernel_for<T, AFF_ROW, false>(per, false, idx) : nullptr;
     switch (mode) {
-    case AFF_ROW: return stream_kernel_for<T, AFF_ROW, true>(per, idx);
-    case AFF_CHAN: return stream_kernel_for<T, AFF_CHAN, true>(per, idx);
-    default: return stream_kernel_for<T, AFF_ANY, true>(per, idx);
+    case AFF_ROW: return stream_kernel_for<T, AFF_ROW, true>(per, wide, idx);
+    case AFF_CHAN: return stream_kernel_for<T, AFF_CHAN, true>(per, wide, idx);
+    default: return stream_kernel_for<T, AFF_ANY, true>(per, wide, idx);
     }
 }
 
-constexpr int GNS_STREAM_VARIANTS = 12; // 3 CTA shapes x (3 GroupNorm channel maps + LayerNorm)
+constexpr int GNS_STREAM_SHAPES = 4;                           // forms by slice (stream_kernel_for)
+constexpr int GNS_STREAM_VARIANTS = GNS_STREAM_SHAPES * 4;     // x (3 GroupNorm channel maps + LayerNorm)
 std::atomic<int> g_stream_active[GNS_DEVICES][2][GNS_STREAM_VARIANTS][5];
 std::once_flag g_stream_init;
 
@@ -1321,7 +1345,8 @@ size_t stream_smem(int64_t per, bool bf16)
 
 } // namespace
 
-cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool act, int cluster, int *clusters)
+cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool act, int cluster, bool wide,
+                                    int *clusters)
 {
     *clusters = 0;
     if (cluster < 1 || cluster > GNS_MAX_CLUSTER || (cluster & (cluster - 1)) != 0)
@@ -1331,12 +1356,12 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool 
         return cudaErrorInvalidValue;
     int idx = 0, dev = 0;
     const int mode = affine_mode(S);
-    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, act, &idx)
-                             : stream_kernel_t<float>(static_cast<int>(per), mode, act, &idx);
+    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, act, wide, &idx)
+                             : stream_kernel_t<float>(static_cast<int>(per), mode, act, wide, &idx);
     if (!k)
         return cudaErrorInvalidValue;
     const int shape = idx;
-    idx += 3 * (act ? mode : 3);
+    idx += GNS_STREAM_SHAPES * (act ? mode : 3);
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
@@ -1350,7 +1375,7 @@ cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool 
     // occupancy depends on the dynamic shared memory, i.e. on per: cache only
     // the full-slice case (per of 1024, 2048 or 4096), query the others
     const size_t smem = stream_smem(per, bf16);
-    const int shape_per = 1024 << shape;
+    const int shape_per = stream_shape_per(shape);
     const bool cacheable = per == shape_per;
     std::atomic<int> *slot = cacheable && dev >= 0 && dev < GNS_DEVICES
                                  ? &g_stream_active[dev][bf16 ? 1 : 0][idx][log2_cluster(cluster)]
@@ -1393,10 +1418,10 @@ int64_t gns_stream_capacity4(bool bf16)
     return stream_cap(bf16);
 }
 
-cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int cluster, cudaStream_t stream)
+cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int cluster, bool wide, cudaStream_t stream)
 {
     int active = 0;
-    cudaError_t e = gns_stream_max_clusters(p.seg_len, p.S, bf16, act, cluster, &active);
+    cudaError_t e = gns_stream_max_clusters(p.seg_len, p.S, bf16, act, cluster, wide, &active);
     if (e != cudaSuccess)
         return e;
     if (active < 1)
@@ -1404,8 +1429,8 @@ cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int clu
     const int64_t per = stream_per(p.seg_len, cluster);
     int idx = 0;
     const int mode = affine_mode(p.S);
-    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, act, &idx)
-                             : stream_kernel_t<float>(static_cast<int>(per), mode, act, &idx);
+    const RegKernel k = bf16 ? stream_kernel_t<__nv_bfloat16>(static_cast<int>(per), mode, act, wide, &idx)
+                             : stream_kernel_t<float>(static_cast<int>(per), mode, act, wide, &idx);
     int64_t clusters = active;
     if (clusters > p.rows)
         clusters = p.rows;

@@ -602,7 +602,7 @@ norm_status_t layer_plan(const void *x, const void *gamma, const void *beta, con
     if (vec4 && aligned(x, 16) && (bf16 ? (row_len & 7) == 0 : true)) {
         const int cl = stream_auto_cluster(row_len / 4, normk::gns_stream_capacity4(bf16));
         int active = 0;
-        if (cl && normk::gns_stream_max_clusters(row_len, 1, bf16, false, cl, &active) == cudaSuccess && active >= 1)
+        if (cl && normk::gns_stream_max_clusters(row_len, 1, bf16, false, cl, false, &active) == cudaSuccess && active >= 1)
             c.ln_cluster = cl;
         else
             cudaGetLastError();
@@ -702,7 +702,7 @@ norm_status_t layer_fwd(const void *x, const void *gamma, const void *beta, void
         q.timeout_ns = p.timeout_ns;
         q.err = p.err;
         q.cache_gb = static_cast<size_t>(row_len) * esz <= kGbL1Bytes;
-        e = normk::gns_stream_launch(q, bf16, false, ch.ln_cluster, stream);
+        e = normk::gns_stream_launch(q, bf16, false, ch.ln_cluster, false, stream);
     } else if (ch.row_kernel) {
         e = normk::ln_rows_launch(p, bf16, d->sm_count, stream);
     } else if (ch.persistent) {
@@ -815,20 +815,44 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     bool stream_ok = false;
     int64_t stream_slice = 0;
     int stream_cl = 0;
+    bool stream_wide = false;
     if (vec4 && aligned(x, 16) && (bf16 ? (L & 7) == 0 : true)) {
         const int64_t forced = g_opt_gn_cluster.load();
         const int64_t cap = normk::gns_stream_capacity4(bf16);
         stream_cl = forced ? static_cast<int>(forced) : stream_auto_cluster(L / 4, cap);
+        int active = 0;
         if (stream_cl) {
             stream_slice = (L / 4 + stream_cl - 1) / stream_cl;
             stream_slice = (stream_slice + 1) & ~int64_t(1);
-            int active = 0;
             stream_ok = stream_slice <= cap &&
-                        normk::gns_stream_max_clusters(L, S, bf16, true, stream_cl, &active) == cudaSuccess &&
+                        normk::gns_stream_max_clusters(L, S, bf16, true, stream_cl, false, &active) == cudaSuccess &&
                         active >= 1;
         }
         if (!stream_ok)
             cudaGetLastError();
+        // Groups already split over a cluster may be split over twice the
+        // CTAs (half the slice each, up to clusters of 8): those CTAs hold
+        // less, more of them are resident, and each cluster streams more
+        // groups.  Taken when the waves of groups over the resident clusters
+        // times the slice length, a model of the launch's time, is smaller.
+        if (stream_ok && !forced && stream_cl >= 2) {
+            const int alt = stream_auto_cluster(L / 4, cap / 2);
+            int alt_active = 0;
+            if (alt > stream_cl && alt <= 8 &&
+                normk::gns_stream_max_clusters(L, S, bf16, true, alt, true, &alt_active) == cudaSuccess &&
+                alt_active >= 1) {
+                int64_t alt_slice = (L / 4 + alt - 1) / alt;
+                alt_slice = (alt_slice + 1) & ~int64_t(1);
+                const int64_t waves = (R + active - 1) / active, alt_waves = (R + alt_active - 1) / alt_active;
+                if (alt_waves * alt_slice < waves * stream_slice) {
+                    stream_cl = alt;
+                    stream_slice = alt_slice;
+                    stream_wide = true;
+                }
+            } else {
+                cudaGetLastError();
+            }
+        }
     }
     // Team path: segments of at most 256 items of 4, 2 or 1 elements.  The
     // automatic choice leaves its longest groups (over 128 items) to the
@@ -889,7 +913,7 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
     p.cache_gb = S == 1 && static_cast<size_t>(L) * esz <= kGbL1Bytes;
 
     if (pl.path == kGnStream) {
-        e = normk::gns_stream_launch(p, bf16, true, stream_cl, stream);
+        e = normk::gns_stream_launch(p, bf16, true, stream_cl, stream_wide, stream);
     } else if (pl.path == kGnReg) {
         e = normk::gns_reg_launch(p, bf16, cluster, stream);
     } else if (pl.path == kGnWarp) {

@@ -796,11 +796,14 @@ cudaError_t gns_reg_launch(const GnSegParams &p, bool bf16, int cluster, cudaStr
 // gns_stream_capacity4() vectors.
 // act: GroupNorm's LeakyReLU x2 epilogue; without it the kernel is
 // LayerNorm over rows of seg_len with per-element gamma/beta (G = 1, M = L,
-// S = 1).
-cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool act, int cluster, int *clusters);
+// S = 1).  wide: the group is split over twice the CTAs of the smallest
+// cluster that holds it (bf16 slices of 2,048 vectors then take a form sized
+// for 5 CTAs per SM).
+cudaError_t gns_stream_max_clusters(int64_t seg_len, int64_t S, bool bf16, bool act, int cluster, bool wide,
+                                    int *clusters);
 // Largest CTA slice (4-element vectors) of the streamed kernel.
 int64_t gns_stream_capacity4(bool bf16);
-cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int cluster, cudaStream_t stream);
+cudaError_t gns_stream_launch(const GnSegParams &p, bool bf16, bool act, int cluster, bool wide, cudaStream_t stream);
 // Apply kernel of the split path (after ln_split_stats_launch on the same
 // segments); vec4 as for the LayerNorm split path.
 cudaError_t gns_split_apply_launch(const GnSegParams &p, bool bf16, bool vec4, cudaStream_t stream);

@@ -263,7 +263,10 @@ def test_bf16_entry_points_check_dtype(ng):
     (3, 9, 5, 3, 5, 0),           # team kernel, single elements (L = 15)
     (2, 64, 1024, 4, 0, 0),       # automatic cluster of 2
     (1, 3, 2732, 1, 1, 16),       # forced cluster of 16, ragged slices
-    (8, 512, 4096, 32, 0, 0),     # the (8, 512, 64, 64) 32-group workload: clusters of 8, streamed
+    (8, 512, 4096, 32, 0, 0),     # the (8, 512, 64, 64) 32-group workload: streamed, groups split over 8 CTAs
+    (16, 512, 2048, 32, 0, 0),    # 512 groups of 32,768: split over 4 CTAs instead of the 2 that hold one
+    (8, 512, 2048, 32, 0, 0),     # 256 groups of 32,768: the doubled split declined (one wave over clusters of 2)
+    (16, 512, 4096, 32, 0, 0),    # 512 groups of 65,536: split over 8 CTAs
     (8, 512, 4096, 32, 1, 0),     # the same through the unstreamed register kernel
     (64, 64, 1024, 16, 4, 1),     # streamed, one CTA per group, many groups per CTA
     (2, 64, 1024, 4, 4, 16),      # streamed over clusters of 16

@@ -194,6 +194,18 @@ def test_streamed(ng, N, C, S, G, cluster):
     check(ng, N, C, S, G, seed=N + C + S + cluster, path=STREAM, cluster=cluster)
 
 
+@pytest.mark.parametrize("N,C,S,G", [
+    (8, 512, 2048, 32),    # 256 groups of 32,768: split over 8 CTAs of 1,024 vectors, not 4 of 2,048
+    (16, 512, 2048, 32),   # 512 groups of 32,768: the same
+    (32, 512, 1024, 32),   # 1,024 groups of 16,384: split over 4 CTAs, not 2
+    (4, 512, 2048, 32),    # 128 groups: the doubled split declined (one wave over clusters of 4)
+])
+def test_streamed_split_over_twice_the_ctas(ng, N, C, S, G):
+    # the automatic choice may split a group over twice the CTAs of the smallest
+    # cluster that holds it, when the waves of groups make that faster
+    check(ng, N, C, S, G, seed=N + S + 5)
+
+
 def test_streamed_is_the_automatic_choice_at_full_size(ng):
     # the (8, 512, 64, 64) workload: clusters of 8 CTAs with 2048-vector slices
     N, C, S, G = 8, 512, 4096, 32
