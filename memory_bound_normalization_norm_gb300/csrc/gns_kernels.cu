@@ -338,7 +338,6 @@ __global__ void __launch_bounds__(NT) gns_reg_kernel(GnSegParams p)
 constexpr int GNS_NBUF = 1;     // shared-memory slice buffers per CTA
 constexpr int GNS_MIN_CTAS = 4; // CTAs per SM the register budget is sized for
 
-
 template <typename T>
 __device__ __forceinline__ float4 ld4_smem(const T *p);
 

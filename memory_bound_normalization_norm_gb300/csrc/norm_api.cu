@@ -838,9 +838,11 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
         if (stream_ok && !forced && stream_cl >= 2) {
             const int alt = stream_auto_cluster(L / 4, cap / 2);
             int alt_active = 0;
-            if (alt > stream_cl && alt <= 8 &&
-                normk::gns_stream_max_clusters(L, S, bf16, true, alt, true, &alt_active) == cudaSuccess &&
-                alt_active >= 1) {
+            if (alt > stream_cl && alt <= 8) {
+                if (normk::gns_stream_max_clusters(L, S, bf16, true, alt, true, &alt_active) != cudaSuccess)
+                    cudaGetLastError();
+            }
+            if (alt_active >= 1) {
                 int64_t alt_slice = (L / 4 + alt - 1) / alt;
                 alt_slice = (alt_slice + 1) & ~int64_t(1);
                 const int64_t waves = (R + active - 1) / active, alt_waves = (R + alt_active - 1) / alt_active;
@@ -849,8 +851,6 @@ norm_status_t group_lrelu_x2_fwd(const void *x, const void *gamma, const void *b
                     stream_slice = alt_slice;
                     stream_wide = true;
                 }
-            } else {
-                cudaGetLastError();
             }
         }
     }
